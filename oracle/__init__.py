@@ -1,0 +1,243 @@
+"""fp64 CPU oracle for Quest-style sparse decode attention (ctypes over ``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no
+code with the CUDA library; both sides only read the same seeded inputs.
+
+Every routine restates a passage of the pages (cited in ``oracle.c``):
+the Quest block bound and top-K selection with sink/recent blocks from the
+"Quest-style block-selector for long-context decode" page, and the absmax
+int8 cache and decode math from the "cpu-attn" card.  Arrays are numpy:
+f16 data travel as ``np.float16`` (bit patterns are passed through
+untouched), scales as ``np.float32``, results come back as ``np.float64``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+F16 = 0
+INT8 = 1
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        # ORACLE_LIB lets the mutation tests load a deliberately broken copy
+        path = os.environ.get("ORACLE_LIB") or _build.build()
+        L = C.CDLL(path)
+        p = C.c_void_p
+        i = C.c_int
+        d = C.c_double
+        L.orc_half_to_double.argtypes = [C.c_uint16]
+        L.orc_half_to_double.restype = d
+        L.orc_quantize_row.argtypes = [p, i, p, p]
+        L.orc_append.argtypes = [p, p, p, i]
+        L.orc_append.restype = i
+        L.orc_block_scores.argtypes = [i, i, i, p, p, p, p, p, p]
+        L.orc_forced_range.argtypes = [i, i, i, i, p, p]
+        L.orc_select.argtypes = [i, i, p, i, i, i, p, p]
+        L.orc_select.restype = i
+        L.orc_attend_f16.argtypes = [i, i, i, p, d, p, p, p, i, p]
+        L.orc_qk_int8.argtypes = [i, C.c_long, p, p, p]
+        L.orc_attend_int8.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, p]
+        L.orc_attend_dequant.argtypes = [i, i, i, p, p, C.c_float, d, p, p, p, p, p, i, p]
+        L.orc_decode.argtypes = [p, i, p, d, i, i, i, i, p, p, p, i]
+        L.orc_decode.restype = i
+        L.orc_num_threads_available.restype = i
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class _OrcCache(C.Structure):
+    _fields_ = [("dtype", C.c_int), ("B", C.c_int), ("Hkv", C.c_int), ("D", C.c_int),
+                ("max_seq", C.c_int), ("blk", C.c_int), ("len", C.c_int),
+                ("K", C.c_void_p), ("V", C.c_void_p), ("ks", C.c_void_p), ("vs", C.c_void_p),
+                ("kmin", C.c_void_p), ("kmax", C.c_void_p)]
+
+
+def half_to_double(h) -> float:
+    """binary16 bit pattern (int) -> exact float."""
+    return lib().orc_half_to_double(int(h) & 0xFFFF)
+
+
+def quantize_row(x):
+    """Absmax int8 codes and f32 scale of one f32 row (cpu-attn, Method)."""
+    x = _c(x, np.float32).ravel()
+    code = np.zeros(x.size, np.int8)
+    scale = np.zeros(1, np.float32)
+    lib().orc_quantize_row(_ptr(x), x.size, _ptr(code), _ptr(scale))
+    return code, np.float32(scale[0])
+
+
+class OracleCache:
+    """Head-major cache held in numpy arrays, filled by the oracle's own append.
+
+    K, V: [B, Hkv, max_seq, D] (float16 or int8); ks, vs: [B, Hkv, max_seq]
+    float32 (int8 only); kmin, kmax: [B, Hkv, max_seq // blk, D] float16.
+    """
+
+    def __init__(self, dtype: int, B: int, Hkv: int, D: int, max_seq: int, blk: int = 64):
+        assert max_seq % blk == 0
+        self.dtype, self.B, self.Hkv, self.D = dtype, B, Hkv, D
+        self.max_seq, self.blk, self.len = max_seq, blk, 0
+        kvt = np.float16 if dtype == F16 else np.int8
+        self.K = np.zeros((B, Hkv, max_seq, D), kvt)
+        self.V = np.zeros((B, Hkv, max_seq, D), kvt)
+        self.ks = np.zeros((B, Hkv, max_seq), np.float32) if dtype == INT8 else None
+        self.vs = np.zeros((B, Hkv, max_seq), np.float32) if dtype == INT8 else None
+        nb = max_seq // blk
+        self.kmin = np.zeros((B, Hkv, nb, D), np.float16)
+        self.kmax = np.zeros((B, Hkv, nb, D), np.float16)
+
+    def _struct(self):
+        s = _OrcCache(self.dtype, self.B, self.Hkv, self.D, self.max_seq, self.blk, self.len,
+                      _ptr(self.K), _ptr(self.V), _ptr(self.ks), _ptr(self.vs),
+                      _ptr(self.kmin), _ptr(self.kmax))
+        return s
+
+    def append(self, k_new, v_new):
+        """k_new, v_new: [B, n_new, Hkv, D] float16."""
+        k_new = _c(k_new, np.float16)
+        v_new = _c(v_new, np.float16)
+        n_new = k_new.shape[1]
+        assert k_new.shape == (self.B, n_new, self.Hkv, self.D) == v_new.shape
+        s = self._struct()
+        rc = lib().orc_append(C.byref(s), _ptr(k_new), _ptr(v_new), n_new)
+        if rc != 0:
+            raise ValueError("append passes max_seq")
+        self.len = s.len
+
+    def decode(self, q, scale: float, k_sel: int = 0, sink_tokens: int = 0,
+               recent_tokens: int = 0, dense: bool = False, n_threads: int = 1):
+        """One decode step: returns (out [B,H,D] f64, sel_idx, sel_cnt)."""
+        q = _c(q, np.float32)
+        B, H, D = q.shape
+        assert B == self.B and D == self.D
+        out = np.zeros((B, H, D), np.float64)
+        nbmax = self.max_seq // self.blk
+        sel_idx = np.full((B, self.Hkv, nbmax), -1, np.int32)
+        sel_cnt = np.zeros((B, self.Hkv), np.int32)
+        s = self._struct()
+        rc = lib().orc_decode(C.byref(s), H, _ptr(q), float(scale), int(k_sel),
+                              int(sink_tokens), int(recent_tokens), int(bool(dense)),
+                              _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), int(n_threads))
+        if rc != 0:
+            raise ValueError("bad decode arguments")
+        return out, sel_idx, sel_cnt
+
+
+def block_scores(q, kmin, kmax):
+    """Quest bounds of one KV head: (ub [NB], ub_heads [G, NB], mag [NB])."""
+    q = _c(q, np.float32)
+    if q.ndim == 1:
+        q = q[None]
+    G, D = q.shape
+    kmin = _c(kmin, np.float16)
+    kmax = _c(kmax, np.float16)
+    NB = kmin.shape[0]
+    ub = np.zeros(NB, np.float64)
+    ubh = np.zeros((G, NB), np.float64)
+    mag = np.zeros(NB, np.float64)
+    lib().orc_block_scores(G, D, NB, _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(ubh), _ptr(ub),
+                           _ptr(mag))
+    return ub, ubh, mag
+
+
+def forced_range(L, blk, sink_tokens, recent_tokens):
+    se = C.c_int()
+    rb = C.c_int()
+    lib().orc_forced_range(L, blk, sink_tokens, recent_tokens, C.byref(se), C.byref(rb))
+    return se.value, rb.value
+
+
+def select(L, blk, ub, k_sel, sink_tokens, recent_tokens):
+    """Selected block ids (ascending) and the bound of the K-th top-K pick."""
+    ub = _c(ub, np.float64)
+    NB = (L + blk - 1) // blk
+    assert ub.size >= NB
+    sel = np.zeros(max(NB, 1), np.int32)
+    kth = C.c_double()
+    n = lib().orc_select(L, blk, _ptr(ub), int(k_sel), int(sink_tokens), int(recent_tokens),
+                         _ptr(sel), C.byref(kth))
+    return sel[:n].copy(), kth.value
+
+
+def _sel_args(sel):
+    if sel is None:
+        return None, -1
+    sel = _c(sel, np.int32)
+    return sel, sel.size
+
+
+def attend_f16(q, K, V, L, blk, scale, sel=None):
+    q = _c(q, np.float32)
+    K = _c(K, np.float16)
+    V = _c(V, np.float16)
+    D = q.size
+    s, n = _sel_args(sel)
+    out = np.zeros(D, np.float64)
+    lib().orc_attend_f16(D, L, blk, _ptr(q), float(scale), _ptr(K), _ptr(V), _ptr(s), n,
+                         _ptr(out))
+    return out
+
+
+def qk_int8(q_code, K):
+    q_code = _c(q_code, np.int8)
+    K = _c(K, np.int8)
+    n, D = K.shape
+    dots = np.zeros(n, np.int64)
+    lib().orc_qk_int8(D, n, _ptr(q_code), _ptr(K), _ptr(dots))
+    return dots
+
+
+def attend_int8(q_code, q_scale, K, V, ks, vs, L, blk, scale, sel=None):
+    q_code = _c(q_code, np.int8)
+    K = _c(K, np.int8)
+    V = _c(V, np.int8)
+    ks = _c(ks, np.float32)
+    vs = _c(vs, np.float32)
+    D = q_code.size
+    s, n = _sel_args(sel)
+    out = np.zeros(D, np.float64)
+    lib().orc_attend_int8(D, L, blk, _ptr(q_code), float(q_scale), float(scale), _ptr(K),
+                          _ptr(V), _ptr(ks), _ptr(vs), _ptr(s), n, _ptr(out))
+    return out
+
+
+def attend_dequant(q, K, V, ks, vs, L, blk, scale, sel=None, q_code=None, q_scale=0.0):
+    q = _c(q, np.float32)
+    K = _c(K, np.int8)
+    V = _c(V, np.int8)
+    ks = _c(ks, np.float32)
+    vs = _c(vs, np.float32)
+    qc = None if q_code is None else _c(q_code, np.int8)
+    D = q.size
+    s, n = _sel_args(sel)
+    out = np.zeros(D, np.float64)
+    lib().orc_attend_dequant(D, L, blk, _ptr(q), _ptr(qc), float(q_scale), float(scale),
+                             _ptr(K), _ptr(V), _ptr(ks), _ptr(vs), _ptr(s), n, _ptr(out))
+    return out
+
+
+def threads_available() -> int:
+    return lib().orc_num_threads_available()
+
+
+__all__ = ["F16", "INT8", "OracleCache", "half_to_double", "quantize_row", "block_scores",
+           "forced_range", "select", "attend_f16", "qk_int8", "attend_int8", "attend_dequant",
+           "threads_available", "lib"]

@@ -1,0 +1,499 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for Quest-style sparse decode
+ * attention over an f16 or absmax-int8 KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or constant with the
+ * CUDA library; the two meet only at the seeded input tensors.
+ *
+ * Sources (the pages this restates, by title and section):
+ *  [QUEST]  "Sparse Attention -- Quest-style block-selector for long-context
+ *           decode (#551)", sections "Method: Quest-style min/max block
+ *           bounds", "S2/S3 engineering design" (fill op, selector op,
+ *           FA-VEC block-skip), "Gate ladder", and "All-KV-types composition
+ *           (bug-747)" (pre-quant envelope, merge-vs-overwrite fill).
+ *  [CPUATT] "cpu-attn" (Hugging Face kernels card), sections "Method",
+ *           "Usage", "Correctness", "Requirements and limits".
+ *  [SCSA]   "SCSA: Self-Calibrating Subquadratic Attention", section
+ *           "2. Mechanism" (sink / recent suffix always attended exactly).
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes with its reason):
+ *  R1  int8 code = round-half-to-even of the IEEE f32 quotient x/s, clamped
+ *      to [-127, 127]; s = fl32(absmax/127) stored as f32.
+ *  R2  a row whose f32 scale is 0 stores scale 0 and all-zero codes.
+ *  R3  the top-K budget counts non-forced blocks only; the sink and recent
+ *      blocks are added on top; ties in the bound go to the lower index.
+ *  R4  sink blocks are those meeting [0, sink_tokens); recent blocks are
+ *      those meeting [L - recent_tokens, L).
+ *  R5  the bound uses the raw f32 query (no softmax scale: a positive factor
+ *      does not change the ranking) on both cache types.
+ *  R6  attention over an empty token set returns the zero vector.
+ *
+ * Every floating-point step runs in IEEE binary64 unless a step of the
+ * method fixes f32 (the quantizer's scale and quotient, R1).  Build with
+ * -ffp-contract=off so no fused multiply-add changes a rounding.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_F16 0
+#define ORC_INT8 1
+
+/* ------------------------------------------------------------------ */
+/* binary16 -> binary64, exact.  Written from the IEEE 754 binary16     */
+/* layout: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.    */
+/* ------------------------------------------------------------------ */
+double orc_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)f, -24);             /* subnormal: f * 2^-24 */
+    else if (e == 31)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(f + 1024), e - 25); /* (1024+f) * 2^(e-15-10) */
+    return sign ? -mag : mag;
+}
+
+/* ------------------------------------------------------------------ */
+/* Absmax int8 quantization of one row  [CPUATT Method; R1, R2].        */
+/* The scale is the f32 value nearest absmax/127.  Each code is the     */
+/* f32 quotient x/s rounded half-to-even and clamped to +-127.          */
+/* A binary64 quotient of two f32 values rounded once to f32 equals the */
+/* correctly rounded f32 quotient (53 >= 2*24+2), so this reproduces    */
+/* IEEE f32 division exactly.                                            */
+/* ------------------------------------------------------------------ */
+void orc_quantize_row(const float *x, int n, int8_t *code, float *scale)
+{
+    double amax = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double a = fabs((double)x[i]);
+        if (a > amax) amax = a;
+    }
+    float s = (float)(amax / 127.0);
+    *scale = s;
+    for (int i = 0; i < n; ++i) {
+        if (s == 0.0f) { code[i] = 0; continue; }
+        float quot = (float)((double)x[i] / (double)s);
+        double r = nearbyint((double)quot);  /* default mode: ties to even */
+        if (r > 127.0) r = 127.0;
+        if (r < -127.0) r = -127.0;
+        code[i] = (int8_t)r;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Cache description (layouts of the head-major cache).                */
+/*   K, V     [B, Hkv, max_seq, D]   f16 bits or int8 codes            */
+/*   ks, vs   [B, Hkv, max_seq]      f32 (int8 cache only)             */
+/*   kmin/kmax[B, Hkv, max_seq/blk, D] f16 bits                        */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    int dtype, B, Hkv, D, max_seq, blk, len;
+    void *K, *V;
+    float *ks, *vs;
+    uint16_t *kmin, *kmax;
+} orc_cache;
+
+static size_t row_index(const orc_cache *c, int b, int h, long t)
+{
+    return ((size_t)b * c->Hkv + h) * (size_t)c->max_seq + (size_t)t;
+}
+
+static size_t bound_index(const orc_cache *c, int b, int h, int blk_id)
+{
+    size_t nbmax = (size_t)(c->max_seq / c->blk);
+    return (((size_t)b * c->Hkv + h) * nbmax + (size_t)blk_id) * (size_t)c->D;
+}
+
+/* ------------------------------------------------------------------ */
+/* Append n_new tokens  [QUEST S2/S3 "Fill op", All-KV-types            */
+/* composition; CPUATT Method "quantize per token per head at append"]. */
+/* k_new, v_new: [B, n_new, Hkv, D] f16 bits.                           */
+/* Cache rows: f16 stored verbatim, or int8 codes + f32 scale per row.  */
+/* Bounds: per (seq, KV head, block) channel-wise min and max of the     */
+/* f16 keys (the pre-quantization envelope).  A block that already       */
+/* holds tokens is merged (min with old min, max with old max); a block  */
+/* that starts inside the new range is overwritten.                      */
+/* Returns 0, or -1 if the append would pass max_seq.                    */
+/* ------------------------------------------------------------------ */
+int orc_append(orc_cache *c, const uint16_t *k_new, const uint16_t *v_new, int n_new)
+{
+    if (n_new < 0 || (long)c->len + n_new > c->max_seq) return -1;
+    const int D = c->D;
+    float *row = (float *)malloc(sizeof(float) * (size_t)D);
+    for (int b = 0; b < c->B; ++b)
+        for (int h = 0; h < c->Hkv; ++h) {
+            /* rows */
+            for (int i = 0; i < n_new; ++i) {
+                long t = (long)c->len + i;
+                const uint16_t *kin = k_new + (((size_t)b * n_new + i) * c->Hkv + h) * D;
+                const uint16_t *vin = v_new + (((size_t)b * n_new + i) * c->Hkv + h) * D;
+                size_t r = row_index(c, b, h, t);
+                if (c->dtype == ORC_F16) {
+                    memcpy((uint16_t *)c->K + r * D, kin, sizeof(uint16_t) * D);
+                    memcpy((uint16_t *)c->V + r * D, vin, sizeof(uint16_t) * D);
+                } else {
+                    for (int d = 0; d < D; ++d) row[d] = (float)orc_half_to_double(kin[d]);
+                    orc_quantize_row(row, D, (int8_t *)c->K + r * D, &c->ks[r]);
+                    for (int d = 0; d < D; ++d) row[d] = (float)orc_half_to_double(vin[d]);
+                    orc_quantize_row(row, D, (int8_t *)c->V + r * D, &c->vs[r]);
+                }
+            }
+            /* bounds of every block meeting [len, len+n_new) */
+            if (n_new == 0) continue;
+            int b0 = c->len / c->blk;
+            int b1 = (c->len + n_new - 1) / c->blk;
+            for (int q = b0; q <= b1; ++q) {
+                long lo = (long)q * c->blk, hi = lo + c->blk;
+                long nlo = lo > c->len ? lo : c->len;
+                long nhi = hi < (long)c->len + n_new ? hi : (long)c->len + n_new;
+                int merge = lo < c->len;         /* block held tokens already */
+                uint16_t *mn = c->kmin + bound_index(c, b, h, q);
+                uint16_t *mx = c->kmax + bound_index(c, b, h, q);
+                for (int d = 0; d < D; ++d) {
+                    uint16_t bmin = 0, bmax = 0;
+                    double vmin = INFINITY, vmax = -INFINITY;
+                    if (merge) {
+                        bmin = mn[d]; vmin = orc_half_to_double(bmin);
+                        bmax = mx[d]; vmax = orc_half_to_double(bmax);
+                    }
+                    for (long t = nlo; t < nhi; ++t) {
+                        int i = (int)(t - c->len);
+                        uint16_t kb = k_new[(((size_t)b * n_new + i) * c->Hkv + h) * D + d];
+                        double kv = orc_half_to_double(kb);
+                        if (kv < vmin) { vmin = kv; bmin = kb; }
+                        if (kv > vmax) { vmax = kv; bmax = kb; }
+                    }
+                    mn[d] = bmin;
+                    mx[d] = bmax;
+                }
+            }
+        }
+    free(row);
+    c->len += n_new;
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Block upper bounds  [QUEST Method "Per-query upper bound"; S2        */
+/* selector op "GQA -> max UB over the query group"].                    */
+/*   UB_h(j) = sum_d max(q_h[d]*kmin_j[d], q_h[d]*kmax_j[d])             */
+/*   UB(j)   = max over the G query heads h of the group of UB_h(j)      */
+/* q: [G, D] f32 (R5).  kmin, kmax: [NB, D] f16 bits of one KV head.     */
+/* ub_heads ([G, NB]) and mag ([NB]) may be NULL.  mag(j) is             */
+/* max_h sum_d |max(q_h[d]*kmin_j[d], q_h[d]*kmax_j[d])|, the size of    */
+/* the terms, which sets the scale of rounding in the sum.               */
+/* ------------------------------------------------------------------ */
+void orc_block_scores(int G, int D, int NB, const float *q,
+                      const uint16_t *kmin, const uint16_t *kmax,
+                      double *ub_heads, double *ub, double *mag)
+{
+    for (int j = 0; j < NB; ++j) {
+        double best = -INFINITY, best_mag = 0.0;
+        for (int h = 0; h < G; ++h) {
+            double s = 0.0, m = 0.0;
+            for (int d = 0; d < D; ++d) {
+                double qd = (double)q[(size_t)h * D + d];
+                double a = qd * orc_half_to_double(kmin[(size_t)j * D + d]);
+                double bb = qd * orc_half_to_double(kmax[(size_t)j * D + d]);
+                double t = a > bb ? a : bb;
+                s += t;
+                m += fabs(t);
+            }
+            if (ub_heads) ub_heads[(size_t)h * NB + j] = s;
+            if (s > best) best = s;
+            if (m > best_mag) best_mag = m;
+        }
+        ub[j] = best;
+        if (mag) mag[j] = best_mag;
+    }
+}
+
+/* Forced blocks  [QUEST Method "Top-K block selection ... PLUS the     */
+/* recent window + attention-sink block"; SCSA Mechanism; R4].          */
+/* Sink blocks: [0, sink_end).  Recent blocks: [recent_begin, NB).      */
+void orc_forced_range(int L, int blk, int sink_tokens, int recent_tokens,
+                      int *sink_end, int *recent_begin)
+{
+    int NB = (L + blk - 1) / blk;
+    int se = (sink_tokens + blk - 1) / blk;
+    if (se > NB) se = NB;
+    int rb = NB;
+    if (recent_tokens > 0) {
+        long start = (long)L - recent_tokens;
+        if (start < 0) start = 0;
+        rb = (int)(start / blk);
+    }
+    *sink_end = se;
+    *recent_begin = rb;
+}
+
+typedef struct { double ub; int idx; } orc_cand;
+
+static int cand_cmp(const void *pa, const void *pb)
+{
+    const orc_cand *a = (const orc_cand *)pa, *b = (const orc_cand *)pb;
+    if (a->ub > b->ub) return -1;           /* larger bound first */
+    if (a->ub < b->ub) return 1;
+    return (a->idx > b->idx) - (a->idx < b->idx); /* then lower index */
+}
+
+/* ------------------------------------------------------------------ */
+/* Block selection  [QUEST Method "Top-K block selection"; S2 selector  */
+/* op; R3, R4].  ub: [NB] group bounds.  Writes the selected block ids   */
+/* ascending into sel and returns their count.  If kth_ub is not NULL it */
+/* receives the bound of the last block taken by the top-K step (NAN if  */
+/* that step took none).                                                  */
+/* ------------------------------------------------------------------ */
+int orc_select(int L, int blk, const double *ub, int k_sel, int sink_tokens,
+               int recent_tokens, int *sel, double *kth_ub)
+{
+    int NB = (L + blk - 1) / blk;
+    int se, rb;
+    orc_forced_range(L, blk, sink_tokens, recent_tokens, &se, &rb);
+    char *take = (char *)calloc((size_t)(NB > 0 ? NB : 1), 1);
+    orc_cand *cand = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)(NB > 0 ? NB : 1));
+    int nc = 0;
+    for (int j = 0; j < NB; ++j) {
+        if (j < se || j >= rb) take[j] = 1;
+        else { cand[nc].ub = ub[j]; cand[nc].idx = j; ++nc; }
+    }
+    int keff = k_sel < nc ? k_sel : nc;
+    if (keff < 0) keff = 0;
+    qsort(cand, (size_t)nc, sizeof(orc_cand), cand_cmp);
+    for (int i = 0; i < keff; ++i) take[cand[i].idx] = 1;
+    if (kth_ub) *kth_ub = keff > 0 ? cand[keff - 1].ub : NAN;
+    int n = 0;
+    for (int j = 0; j < NB; ++j)
+        if (take[j]) sel[n++] = j;
+    free(cand);
+    free(take);
+    return n;
+}
+
+/* Softmax-weighted sum over n rows given their logits:                 */
+/*   out = sum_i exp(l_i - M) v_i / sum_i exp(l_i - M),  M = max_i l_i  */
+/* Values come from a callback-free row reader: vrow(i, d).             */
+/* The two attention routines below fill logits and read values.        */
+
+/* ------------------------------------------------------------------ */
+/* f16 attention of one query head over a token set  [QUEST S3 block    */
+/* skip: unselected blocks contribute nothing; CPUATT Method with       */
+/* f16 rows in place of int8].                                          */
+/*   logit_t = scale * sum_d q[d] * k_t[d];  p = softmax(logit);        */
+/*   out[d] = sum_t p_t v_t[d]                                          */
+/* K, V: [max_seq, D] rows of one (seq, KV head).  sel: ascending block */
+/* ids (n_sel >= 0), or n_sel < 0 for every token in [0, L).             */
+/* ------------------------------------------------------------------ */
+static long token_list(int L, int blk, const int *sel, int n_sel, long *tok)
+{
+    long n = 0;
+    if (n_sel < 0) {
+        for (long t = 0; t < L; ++t) tok[n++] = t;
+        return n;
+    }
+    for (int i = 0; i < n_sel; ++i)
+        for (long t = (long)sel[i] * blk; t < (long)(sel[i] + 1) * blk && t < L; ++t)
+            tok[n++] = t;
+    return n;
+}
+
+void orc_attend_f16(int D, int L, int blk, const float *q, double scale,
+                    const uint16_t *K, const uint16_t *V,
+                    const int *sel, int n_sel, double *out)
+{
+    long cap = (long)L + 1;
+    long *tok = (long *)malloc(sizeof(long) * (size_t)cap);
+    long n = token_list(L, blk, sel, n_sel, tok);
+    double *lg = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double M = -INFINITY;
+    for (long i = 0; i < n; ++i) {
+        const uint16_t *k = K + (size_t)tok[i] * D;
+        double s = 0.0;
+        for (int d = 0; d < D; ++d) s += (double)q[d] * orc_half_to_double(k[d]);
+        lg[i] = scale * s;
+        if (lg[i] > M) M = lg[i];
+    }
+    double Z = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        double w = exp(lg[i] - M);
+        Z += w;
+        const uint16_t *v = V + (size_t)tok[i] * D;
+        for (int d = 0; d < D; ++d) out[d] += w * orc_half_to_double(v[d]);
+    }
+    if (n > 0)
+        for (int d = 0; d < D; ++d) out[d] /= Z;   /* R6: empty set -> 0 */
+    free(lg);
+    free(tok);
+}
+
+/* ------------------------------------------------------------------ */
+/* Exact integer q.k dots  [CPUATT Method "Logit dots are exact int32"].*/
+/*   dot_t = sum_d q_code[d] * k_code_t[d]   (|dot| <= D*127*127)       */
+/* ------------------------------------------------------------------ */
+void orc_qk_int8(int D, long n, const int8_t *qc, const int8_t *K, int64_t *dots)
+{
+    for (long t = 0; t < n; ++t) {
+        int64_t s = 0;
+        for (int d = 0; d < D; ++d) s += (int64_t)qc[d] * (int64_t)K[(size_t)t * D + d];
+        dots[t] = s;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* int8 attention of one query head  [CPUATT Method]:                   */
+/*   logit_t = dot_t * q_scale * k_scale_t * softmax_scale              */
+/*   out[d]  = sum_t softmax(logit)_t * v_scale_t * v_code_t[d]         */
+/* qc/q_scale: the head's query quantized by orc_quantize_row.          */
+/* ------------------------------------------------------------------ */
+void orc_attend_int8(int D, int L, int blk, const int8_t *qc, float q_scale, double scale,
+                     const int8_t *K, const int8_t *V, const float *ks, const float *vs,
+                     const int *sel, int n_sel, double *out)
+{
+    long cap = (long)L + 1;
+    long *tok = (long *)malloc(sizeof(long) * (size_t)cap);
+    long n = token_list(L, blk, sel, n_sel, tok);
+    double *lg = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double M = -INFINITY;
+    for (long i = 0; i < n; ++i) {
+        int64_t dot = 0;
+        orc_qk_int8(D, 1, qc, K + (size_t)tok[i] * D, &dot);
+        lg[i] = (double)dot * (double)q_scale * (double)ks[tok[i]] * scale;
+        if (lg[i] > M) M = lg[i];
+    }
+    double Z = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        double w = exp(lg[i] - M);
+        Z += w;
+        double sv = (double)vs[tok[i]];
+        const int8_t *v = V + (size_t)tok[i] * D;
+        for (int d = 0; d < D; ++d) out[d] += w * sv * (double)v[d];
+    }
+    if (n > 0)
+        for (int d = 0; d < D; ++d) out[d] /= Z;
+    free(lg);
+    free(tok);
+}
+
+/* ------------------------------------------------------------------ */
+/* Attention over float rows (dequantized cache)  [CPUATT Correctness:  */
+/* "fp32 attention on the dequantized cache"].  q: [D] f32; K, V: the   */
+/* int8 rows times their scales, formed here in binary64.               */
+/* With q_code != NULL the query is the dequantized int8 query          */
+/* (q_scale * q_code) instead of q.                                      */
+/* ------------------------------------------------------------------ */
+void orc_attend_dequant(int D, int L, int blk, const float *q, const int8_t *q_code,
+                        float q_scale, double scale, const int8_t *K, const int8_t *V,
+                        const float *ks, const float *vs, const int *sel, int n_sel,
+                        double *out)
+{
+    long cap = (long)L + 1;
+    long *tok = (long *)malloc(sizeof(long) * (size_t)cap);
+    long n = token_list(L, blk, sel, n_sel, tok);
+    double *lg = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double M = -INFINITY;
+    for (long i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (int d = 0; d < D; ++d) {
+            double qd = q_code ? (double)q_scale * (double)q_code[d] : (double)q[d];
+            double kd = (double)ks[tok[i]] * (double)K[(size_t)tok[i] * D + d];
+            s += qd * kd;
+        }
+        lg[i] = scale * s;
+        if (lg[i] > M) M = lg[i];
+    }
+    double Z = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        double w = exp(lg[i] - M);
+        Z += w;
+        for (int d = 0; d < D; ++d)
+            out[d] += w * ((double)vs[tok[i]] * (double)V[(size_t)tok[i] * D + d]);
+    }
+    if (n > 0)
+        for (int d = 0; d < D; ++d) out[d] /= Z;
+    free(lg);
+    free(tok);
+}
+
+/* ------------------------------------------------------------------ */
+/* One decode step for every (seq, KV head) of a cache                   */
+/* [QUEST S2/S3: selector then block-skipping attention; CPUATT Usage:  */
+/* query head h reads KV head h / (H / Hkv)].                            */
+/* q: [B, H, D] f32.  out: [B, H, D].  With dense != 0 every token is    */
+/* attended and no selection is made.  sel_idx ([B, Hkv, NB]) and        */
+/* sel_cnt ([B, Hkv]) receive the selection when not NULL.  For the      */
+/* int8 cache each query head is quantized once (CPUATT Method).         */
+/* Problems (seq, KV head) are independent; n_threads > 1 spreads them   */
+/* over OpenMP threads.  Returns 0, or -1 on bad arguments.              */
+/* ------------------------------------------------------------------ */
+int orc_decode(const orc_cache *c, int H, const float *q, double scale, int k_sel,
+               int sink_tokens, int recent_tokens, int dense, int *sel_idx, int *sel_cnt,
+               double *out, int n_threads)
+{
+    if (H % c->Hkv != 0 || c->len <= 0) return -1;
+    const int G = H / c->Hkv, D = c->D, L = c->len;
+    const int NB = (L + c->blk - 1) / c->blk;
+    const int nbmax = c->max_seq / c->blk;
+    const int P = c->B * c->Hkv;
+#ifdef _OPENMP
+    if (n_threads < 1) n_threads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+#endif
+    for (int p = 0; p < P; ++p) {
+        int b = p / c->Hkv, g = p % c->Hkv;
+        const float *qg = q + ((size_t)b * H + (size_t)g * G) * D;
+        int *sel = (int *)malloc(sizeof(int) * (size_t)NB);
+        int n_sel = -1;
+        if (!dense) {
+            double *ub = (double *)malloc(sizeof(double) * (size_t)NB);
+            orc_block_scores(G, D, NB, qg, c->kmin + bound_index(c, b, g, 0),
+                             c->kmax + bound_index(c, b, g, 0), NULL, ub, NULL);
+            n_sel = orc_select(L, c->blk, ub, k_sel, sink_tokens, recent_tokens, sel, NULL);
+            free(ub);
+            if (sel_idx) memcpy(sel_idx + (size_t)p * nbmax, sel, sizeof(int) * (size_t)n_sel);
+            if (sel_cnt) sel_cnt[p] = n_sel;
+        }
+        size_t r0 = row_index(c, b, g, 0);
+        for (int hh = 0; hh < G; ++hh) {
+            const float *qh = qg + (size_t)hh * D;
+            double *o = out + ((size_t)b * H + (size_t)g * G + hh) * D;
+            if (c->dtype == ORC_F16) {
+                orc_attend_f16(D, L, c->blk, qh, scale, (const uint16_t *)c->K + r0 * D,
+                               (const uint16_t *)c->V + r0 * D, sel, n_sel, o);
+            } else {
+                int8_t *qc = (int8_t *)malloc((size_t)D);
+                float qs;
+                orc_quantize_row(qh, D, qc, &qs);
+                orc_attend_int8(D, L, c->blk, qc, qs, scale, (const int8_t *)c->K + r0 * D,
+                                (const int8_t *)c->V + r0 * D, c->ks + r0, c->vs + r0,
+                                sel, n_sel, o);
+                free(qc);
+            }
+        }
+        free(sel);
+    }
+    return 0;
+}
+
+int orc_num_threads_available(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

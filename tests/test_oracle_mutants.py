@@ -1,0 +1,84 @@
+"""The oracle's pins catch planted mistakes (no GPU).
+
+Each case copies oracle/oracle.c, plants one plausible mistake in the copy
+(a wrong sign, a dropped term, a transposed operand, an off-by-one, a wrong
+rounding rule), builds it, and runs the pin suite against that library.  The
+pin suite must fail for every mutant; a mutant that survives means some part
+of the oracle is not pinned.
+"""
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = {
+    "bound_min_not_max": ("double t = a > bb ? a : bb;", "double t = a < bb ? a : bb;"),
+    "bound_kmax_only": ("double a = qd * orc_half_to_double(kmin[(size_t)j * D + d]);",
+                        "double a = qd * orc_half_to_double(kmax[(size_t)j * D + d]);"),
+    "bound_group_min": ("if (s > best) best = s;", "if (s < best || h == 0) best = s;"),
+    "tie_to_higher_index": ("return (a->idx > b->idx) - (a->idx < b->idx);",
+                            "return (a->idx < b->idx) - (a->idx > b->idx);"),
+    "topk_smallest": ("if (a->ub > b->ub) return -1;", "if (a->ub > b->ub) return 1;"),
+    "recent_one_late": ("rb = (int)(start / blk);", "rb = (int)(start / blk) + 1;"),
+    "sink_floor": ("int se = (sink_tokens + blk - 1) / blk;", "int se = sink_tokens / blk;"),
+    "quant_half_away": ("double r = nearbyint((double)quot);", "double r = round((double)quot);"),
+    "quant_scale_128": ("float s = (float)(amax / 127.0);", "float s = (float)(amax / 128.0);"),
+    "quant_no_clamp_low": ("if (r < -127.0) r = -127.0;", "if (r < -128.0) r = -128.0;"),
+    "quant_double_quotient": ("double r = nearbyint((double)quot);",
+                              "double r = nearbyint((double)x[i] / (double)s);"),
+    "append_overwrite_not_merge": ("int merge = lo < c->len;", "int merge = 0;"),
+    "append_bounds_from_values": (
+        "uint16_t kb = k_new[(((size_t)b * n_new + i) * c->Hkv + h) * D + d];",
+        "uint16_t kb = v_new[(((size_t)b * n_new + i) * c->Hkv + h) * D + d];"),
+    "f16_no_scale": ("lg[i] = scale * s;\n        if (lg[i] > M) M = lg[i];\n    }\n    double Z = 0.0;\n    for (int d = 0; d < D; ++d) out[d] = 0.0;\n    for (long i = 0; i < n; ++i) {\n        double w = exp(lg[i] - M);\n        Z += w;\n        const uint16_t",
+                     "lg[i] = s;\n        if (lg[i] > M) M = lg[i];\n    }\n    double Z = 0.0;\n    for (int d = 0; d < D; ++d) out[d] = 0.0;\n    for (long i = 0; i < n; ++i) {\n        double w = exp(lg[i] - M);\n        Z += w;\n        const uint16_t"),
+    "f16_keys_as_values": ("const uint16_t *v = V + (size_t)tok[i] * D;",
+                           "const uint16_t *v = K + (size_t)tok[i] * D;"),
+    "int8_no_kscale": ("lg[i] = (double)dot * (double)q_scale * (double)ks[tok[i]] * scale;",
+                       "lg[i] = (double)dot * (double)q_scale * scale;"),
+    "int8_no_vscale": ("double sv = (double)vs[tok[i]];", "double sv = 1.0;"),
+    "int8_vscale_from_k": ("double sv = (double)vs[tok[i]];", "double sv = (double)ks[tok[i]];"),
+    "gqa_modulo_mapping": ("int b = p / c->Hkv, g = p % c->Hkv;\n        const float *qg = q + ((size_t)b * H + (size_t)g * G) * D;",
+                           "int b = p / c->Hkv, g = p % c->Hkv;\n        const float *qg = q + ((size_t)b * H + (size_t)g) * D;"),
+    "partial_block_overrun": ("t < (long)(sel[i] + 1) * blk && t < L; ++t)",
+                              "t < (long)(sel[i] + 1) * blk; ++t)"),
+    "half_subnormal_exp": ("mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);"),
+}
+
+
+def _run_mutant(name, old, new, tmp):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"{name}: snippet not found exactly once"
+    mdir = os.path.join(tmp, name)
+    os.makedirs(mdir)
+    cfile = os.path.join(mdir, "oracle.c")
+    with open(cfile, "w") as f:
+        f.write(src.replace(old, new))
+    lib = os.path.join(mdir, "liboracle.so")
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                    "-ffp-contract=off", "-o", lib, cfile, "-lm"], check=True)
+    env = dict(os.environ, ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return name, r.returncode
+
+
+def test_every_planted_mistake_is_caught():
+    tmp = tempfile.mkdtemp(prefix="orc_mut_")
+    try:
+        with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
+            res = list(ex.map(lambda kv: _run_mutant(kv[0], *kv[1], tmp), MUTANTS.items()))
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+    survivors = [n for n, rc in res if rc == 0]
+    assert not survivors, f"pins missed planted mistakes: {survivors}"
+    # a crash is not a catch: the suite must have run and failed
+    assert all(rc == 1 for _, rc in res), res
