@@ -1,0 +1,411 @@
+"""Benchmark: microseconds per decode step and effective KV GB/s of Quest-style
+sparse decode attention on one GB300, at long context.
+
+A step is one whole pass of the decode hot path for one new token per
+sequence, through the C ABI (kvd_decode_step): append the token's K/V
+(quantizing and updating the block envelope), score every block's bound,
+select top-K + sink + recent blocks, and attend over the selected blocks.
+Before each step the cache length is reset to the workload's L, so every
+step sees the same context (L is a multiple of 64, so the token opens a
+fresh block and its bounds are exact again).
+
+Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier
+and a device synchronize; each step is timed with CUDA events on the stream
+it runs on; L2 is flushed (a 256 MiB write, larger than the 129 MB L2)
+between steps, outside the events.  Under torchrun every rank runs the same
+per-GPU workload (independent sequences: weak scaling) and rank 0 prints the
+max over ranks.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                       [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import long_context_decode_kv_gb300 as kvd  # noqa: E402
+from long_context_decode_kv_gb300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = synth.CTX1M.name
+FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kv_bytes_per_token(dtype):
+    # K row + V row (+ one f32 scale each for int8)
+    return 2 * 128 + 2 * 4 if dtype == kvd.INT8 else 2 * 2 * 128
+
+
+def attended_tokens(sel_idx, sel_cnt, L):
+    idx = sel_idx.cpu().numpy()
+    cnt = sel_cnt.cpu().numpy()
+    tot = 0
+    for b in range(cnt.shape[0]):
+        for g in range(cnt.shape[1]):
+            blks = idx[b, g, :cnt[b, g]].astype(np.int64)
+            tot += int(np.minimum(64, L - blks * 64).sum())
+    return tot
+
+
+def decode_kernel_bytes(w, tokens, n_sel_total):
+    # selected rows (+ scales), the block lists, q in, out
+    return (tokens * kv_bytes_per_token(w.dtype) + n_sel_total * 4 + w.B * w.H * w.D * 4 * 2)
+
+
+def step_bytes(w, tokens, n_sel_total, L1):
+    """Algorithmic bytes of one whole step: the decode kernel's, plus the
+    bounds of every scored (non-forced) block, the selection keys written and
+    read once, and the one-token append (inputs read, row and bounds written)."""
+    nb = (L1 + 63) // 64
+    forced = kvd.selected_count(L1, 0, w.sink_tokens, w.recent_tokens)
+    n_cand = nb - forced
+    P = w.B * w.Hkv
+    scored = P * n_cand * 2 * 128 * 2
+    keys = P * n_cand * 4 * 2
+    row_out = 2 * 128 + 2 * 4 if w.dtype == kvd.INT8 else 2 * 2 * 128
+    append = P * (2 * 128 * 2 + row_out + 2 * 128 * 2)
+    return decode_kernel_bytes(w, tokens, n_sel_total) + scored + keys + append
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "long_context_decode_kv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload):
+    """dram bytes per decode-kernel launch from the committed ncu summary,
+    valid only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 3 and parts[0] == workload and parts[1] == digest:
+            return float(parts[2])
+    return None
+
+
+# --------------------------------------------------------------------------
+# CPU oracle leg (the only place bench.py runs the oracle)
+# --------------------------------------------------------------------------
+def oracle_leg(w, q, k, v, steps, problem=(0, 0)):
+    """Time the fp64 CPU oracle doing the same decode step on one (sequence,
+    KV head) problem; scale to the workload's B*Hkv independent problems."""
+    import oracle
+    b, g = problem
+    G = w.G
+    oc = oracle.OracleCache(w.dtype, 1, 1, w.D, w.L + 64, 64)
+    oc.append(k[b:b + 1, :, g:g + 1].contiguous().cpu().numpy(),
+              v[b:b + 1, :, g:g + 1].contiguous().cpu().numpy())
+    qg = q[b:b + 1, g * G:(g + 1) * G].cpu().numpy()
+    times = []
+    for s in range(steps):
+        kn, vn = synth.make_step_token(w, s, device="cpu")
+        t0 = time.perf_counter()
+        oc.len = w.L
+        oc.append(kn[b:b + 1, :, g:g + 1].numpy(), vn[b:b + 1, :, g:g + 1].numpy())
+        oc.decode(qg, w.scale, k_sel=w.k_sel, sink_tokens=w.sink_tokens,
+                  recent_tokens=w.recent_tokens, n_threads=1)
+        times.append(time.perf_counter() - t0)
+    per_problem_us = statistics.median(times) * 1e6
+    n_prob = w.B * w.Hkv
+    return per_problem_us * n_prob, {
+        "kind": "oracle", "cores": 1,
+        "sample": (f"1 of {n_prob} (sequence, KV head) problems of {w.name}, {steps} steps "
+                   f"(append + select + attend, fp64, 1 thread), median per-problem time "
+                   f"x {n_prob} problems")}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    q, k, v, _ = synth.make_workload(w, device="cuda")
+    steps = max(1, args.steps)
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_leg(w, q, k, v, 1)
+    value, base = oracle_leg(w, q, k, v, steps)
+    base["value"] = value
+    base["unit"] = "us/step"
+    line = {"impl": "reference", "metric": "us_per_decode_step", "value": value,
+            "unit": "us/step", "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "higher_is_better": False, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w), "cpu_baseline": base,
+            "e2e": {"value": value, "unit": "us/step", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "batch": w.B, "n_heads": w.H, "n_kv_heads": w.Hkv,
+            "head_dim": w.D, "context": w.L, "kv_dtype": "int8" if w.dtype == kvd.INT8 else "f16",
+            "block": 64, "k_sel": w.k_sel, "sink_tokens": w.sink_tokens,
+            "recent_tokens": w.recent_tokens, "keys": w.keys, "n_needles": w.n_needles,
+            "step": "append 1 token + select + sparse attend (kvd_decode_step)",
+            "l2": "flushed between timed steps (256 MiB write)", "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    warmup = max(3, args.warmup)
+
+    q, k, v, needles = synth.make_workload(w, device=dev)
+    cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev)
+    kvd.kv_append(cache, k, v)
+    ws = kvd.make_workspace(cache, w.H)
+    nbmax = cache.max_seq // 64
+    sel_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev)
+    sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev)
+    out = torch.empty(w.B, w.H, w.D, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    toks = [synth.make_step_token(w, s, device=dev) for s in range(8)]
+    L1 = w.L + 1
+    max_sel = kvd.selected_count(L1, w.k_sel, w.sink_tokens, w.recent_tokens)
+
+    def step(i, dense=False):
+        cache.len = w.L
+        kn, vn = toks[i % len(toks)]
+        kvd.decode_step(cache, q, kn, vn, w.scale, -1 if dense else w.k_sel, w.sink_tokens,
+                        w.recent_tokens, out, ws, sel_idx=sel_idx, sel_cnt=sel_cnt)
+
+    def timed(fn, n, warm):
+        for i in range(warm):
+            flush.fill_(i & 0xFF)
+            fn(i)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            fn(i)
+            ev[i][1].record(stream)
+        barrier(world)
+        wall = time.perf_counter() - t0
+        ms = [a.elapsed_time(b) for a, b in ev]
+        return ms, wall
+
+    # ---- the timed decode steps (value)
+    with Clocks(local) as clk:
+        step_ms, wall = timed(lambda i: step(i), args.steps, warmup)
+    clocks = clk.summary()
+    assert cache.device_status() == 0, "device-side fault reported"
+    us_step = statistics.mean(step_ms) * 1e3
+    us_step = max_over_ranks(us_step, world)
+
+    # ---- selection statistics of the timed configuration
+    tokens = attended_tokens(sel_idx, sel_cnt, L1)
+    n_sel_total = int(sel_cnt.sum().item())
+    needle_ok = all(int(p) // 64 in set(sel_idx[b, g, :sel_cnt[b, g]].tolist())
+                    for b in range(w.B) for g in range(w.Hkv) for p in needles[b, g].tolist())
+
+    # ---- the decode kernel alone (roofline of the dominant kernel)
+    cache.len = L1
+
+    def dec(i):
+        kvd.decode_attn(cache, q, w.scale, sel_idx, sel_cnt, max_sel, out, ws)
+    dec_ms, _ = timed(dec, args.steps, 3)
+    dec_us = statistics.mean(dec_ms) * 1e3
+
+    def sel(i):
+        kvd.select_blocks(cache, q, w.k_sel, w.sink_tokens, w.recent_tokens, sel_idx, sel_cnt,
+                          ws)
+    sel_ms, _ = timed(sel, args.steps, 3)
+
+    def app(i):
+        cache.len = w.L
+        kn, vn = toks[i % len(toks)]
+        kvd.kv_append(cache, kn, vn)
+    app_ms, _ = timed(app, args.steps, 3)
+
+    # ---- dense arm at the same context (append + dense attend)
+    dense_ms, _ = timed(lambda i: step(i, dense=True), max(5, args.steps // 5), 2)
+
+    # ---- e2e: host buffers through the C ABI, copies inside the timed region
+    qh = q.cpu().pin_memory()
+    kh = [(a.cpu().pin_memory(), b.cpu().pin_memory()) for a, b in toks]
+    oh = torch.empty(w.B, w.H, w.D).pin_memory()
+
+    def host_step(i):
+        cache.len = w.L
+        a, b = kh[i % len(kh)]
+        kvd.decode_step_host(cache, qh, a, b, w.scale, w.k_sel, w.sink_tokens, w.recent_tokens,
+                             oh, ws)
+    e2e_ms, _ = timed(host_step, args.steps, 3)
+    e2e_us = max_over_ranks(statistics.mean(e2e_ms) * 1e3, world)
+    h2d = qh.numel() * 4 + 2 * kh[0][0].numel() * 2
+    d2h = oh.numel() * 4
+
+    peak, peak_kind = peaks()
+    dbytes = decode_kernel_bytes(w, tokens, n_sel_total)
+    sbytes = step_bytes(w, tokens, n_sel_total, L1)
+    achieved = dbytes / (dec_us * 1e-6) / 1e9
+    eff_step = sbytes / (us_step * 1e-6) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            v_cpu, cpu = oracle_leg(w, q, k, v, 3)
+            cpu["value"] = v_cpu
+            cpu["unit"] = "us/step"
+        except Exception as e:  # the baseline must not hide the GPU number
+            cpu = {"kind": "oracle", "value": None, "error": str(e)[:200]}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "us_per_decode_step", "value": us_step, "unit": "us/step",
+        "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": us_step / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8" if w.dtype == kvd.INT8 else "f16", "data": "synthetic",
+        "config": config_of(w),
+        "effective_kv_gbs": eff_step,
+        "effective_kv_frac": eff_step / peak,
+        "step_bytes": sbytes,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "decode_kernel (kvd_decode_attn)", "bytes": dbytes,
+                     "us": dec_us, "traffic": measured_traffic(w.name)},
+        "breakdown_us": {"append": statistics.mean(app_ms) * 1e3,
+                         "select": statistics.mean(sel_ms) * 1e3, "decode": dec_us,
+                         "step": us_step, "dense_step": statistics.mean(dense_ms) * 1e3},
+        "sparse_over_dense": statistics.mean(dense_ms) * 1e3 / us_step,
+        "selected_blocks_per_problem": n_sel_total / (w.B * w.Hkv),
+        "coverage": n_sel_total / (w.B * w.Hkv) / ((L1 + 63) // 64),
+        "needles_selected": needle_ok,
+        "e2e": {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

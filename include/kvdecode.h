@@ -1,0 +1,254 @@
+/*
+ * kvdecode.h -- C ABI of libkvdecode.so: single-token decode attention over a
+ * long KV cache that reads only part of it (Quest-style block selection),
+ * for NVIDIA GB300 (sm_103a), one GPU.
+ *
+ * Sources, by page title and section:
+ *  [QUEST]  "Sparse Attention -- Quest-style block-selector for long-context
+ *           decode (#551)": "Method: Quest-style min/max block bounds",
+ *           "S2/S3 engineering design" (fill op, selector op, FA-VEC block
+ *           skip), "Knobs", "Gate ladder", "All-KV-types composition
+ *           (bug-747)".
+ *  [CPUATT] "cpu-attn" (Hugging Face kernels card): "Usage", "Method",
+ *           "Correctness", "Requirements and limits".
+ *
+ * Conventions for every entry point
+ *  - All device memory is allocated and owned by the caller.  The library
+ *    never allocates or frees device memory and never synchronizes: every
+ *    call enqueues its kernels on `stream` (a cudaStream_t passed as void*;
+ *    NULL means the legacy default stream) and returns.
+ *  - Arguments are checked on the host before anything is enqueued.  A call
+ *    that returns anything but KVD_OK has enqueued nothing (the one
+ *    exception, KVD_ERR_CUDA from a failed launch, is documented there).
+ *  - Device pointers must be 16-byte aligned.  Layouts are dense row-major
+ *    with the shapes given; no strides.
+ *  - Faults found on the device (a bounded wait that ran out) are written to
+ *    the cache's optional `dev_status` word (0 = fine); the kernels never
+ *    trap.  Read the word after the stream has finished.
+ *  - No call is thread-safe on the same cache or workspace; calls on one
+ *    stream are ordered by the stream.
+ */
+#ifndef KVDECODE_H
+#define KVDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVD_ABI_VERSION 1
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define KVD_API __attribute__((visibility("default")))
+#else
+#define KVD_API
+#endif
+
+typedef enum {
+    KVD_OK = 0,
+    KVD_ERR_INVALID = 1,      /* bad argument: NULL/misaligned pointer, bad size */
+    KVD_ERR_UNSUPPORTED = 2,  /* legal but not built: head_dim != 128, block != 64, ... */
+    KVD_ERR_CAPACITY = 3,     /* append would pass max_seq */
+    KVD_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    KVD_ERR_TIMEOUT = 5,      /* device only: a bounded wait ran out (dev_status) */
+    KVD_ERR_WORKSPACE = 6     /* workspace NULL, misaligned or too small */
+} kvd_status;
+
+typedef enum { KVD_F16 = 0, KVD_INT8 = 1 } kvd_kv_dtype;
+
+/*
+ * The cache: a plain descriptor of caller-owned device memory.
+ *
+ * Layout is head-major, so one block of `block` tokens of one (sequence,
+ * KV head) is one contiguous run of memory:
+ *   k, v        [batch, n_kv_heads, max_seq, head_dim]   f16 or int8 codes
+ *   k_scale,    [batch, n_kv_heads, max_seq]              f32, int8 only
+ *   v_scale                                               (NULL for f16)
+ *   kmin, kmax  [batch, n_kv_heads, max_seq / block, head_dim]  f16
+ * kmin/kmax is the per-(KV head, block) channel-wise key envelope [QUEST
+ * Method: "Store kmin[head_dim], kmax[head_dim] per block"], always taken
+ * from the f16 keys before quantization [QUEST All-KV-types composition].
+ * int8 rows hold per-token per-head absmax codes [CPUATT Method]: scale =
+ * absmax/127 (f32), code = round-half-even(x / scale) clamped to +-127, and
+ * a row whose scale is 0 holds zero codes.
+ *
+ * `len` (tokens cached; the same for every sequence) is host state, advanced
+ * by kvd_kv_append.  Rows at or beyond `len` are never read by a decode
+ * call's arithmetic (they may hold anything).
+ * `dev_status` may be NULL; if set it is one device int32 that kernels set
+ * to a kvd_status code when a bounded device wait runs out.
+ */
+typedef struct kvd_cache {
+    int32_t dtype;        /* kvd_kv_dtype */
+    int32_t batch;        /* independent sequences, >= 1 */
+    int32_t n_kv_heads;   /* Hkv >= 1 */
+    int32_t head_dim;     /* D; only 128 is built */
+    int32_t max_seq;      /* capacity in tokens, a multiple of `block` */
+    int32_t block;        /* B_SEL; only 64 is built [QUEST Knobs: default 64] */
+    int32_t len;          /* tokens currently cached, 0 <= len <= max_seq */
+    int32_t reserved;     /* must be 0 */
+    void *k;
+    void *v;
+    float *k_scale;
+    float *v_scale;
+    void *kmin;
+    void *kmax;
+    int32_t *dev_status;
+} kvd_cache;
+
+/* ---------------------------------------------------------------------- */
+/* Append n_new tokens to every sequence  [QUEST S2/S3 "Fill op" and       */
+/* All-KV-types composition; CPUATT Method "quantize at append time"].     */
+/*   k_new, v_new: device, [batch, n_new, n_kv_heads, head_dim] f16.        */
+/* Writes rows len .. len+n_new-1 (f16 verbatim, or int8 codes + scales)   */
+/* and the bounds of every block those rows touch: a block that already   */
+/* held tokens is min/max-merged, a block that starts in the new range is  */
+/* overwritten.  On KVD_OK, cache->len += n_new (host side; the kernels    */
+/* are only enqueued).  n_new == 0 is a no-op.                             */
+/* Errors: INVALID, UNSUPPORTED, CAPACITY (len + n_new > max_seq), CUDA.   */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_kv_append(kvd_cache *cache, const void *k_new, const void *v_new,
+                         int32_t n_new, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Quest block selection for one query token per sequence  [QUEST Method   */
+/* "Per-query upper bound", "Top-K block selection"; S2/S3 selector op:    */
+/* "GQA -> max UB over the query group per KV-head"].                      */
+/*   q: device [batch, n_heads, head_dim] f32; query head h belongs to KV   */
+/*      head h / (n_heads / n_kv_heads) [CPUATT Usage].                    */
+/*   For each (sequence, KV head) and block j < NB = ceil(len / block):    */
+/*     UB(j) = max over the group's heads h of                             */
+/*             sum_d max(q_h[d] * kmin_j[d], q_h[d] * kmax_j[d])            */
+/*   Forced blocks: those meeting [0, sink_tokens) (sink) and those        */
+/*   meeting [len - recent_tokens, len) (recent window).  Of the other     */
+/*   blocks the k_sel with the largest UB are taken (all of them if fewer),*/
+/*   equal bounds going to the lower block index.                          */
+/*   sel_idx: device [batch, n_kv_heads, max_seq / block] int32; row r     */
+/*            receives its selected block ids ascending in its first        */
+/*            sel_cnt[r] entries (the rest is left untouched).             */
+/*   sel_cnt: device [batch, n_kv_heads] int32; every row gets the same     */
+/*            count, kvd_selected_count(len, block, k_sel, sink, recent).  */
+/*   workspace: device scratch of kvd_workspace_bytes(...) bytes.          */
+/* Errors: INVALID (len == 0, k_sel/sink/recent < 0, n_heads not a         */
+/* multiple of n_kv_heads), UNSUPPORTED (group size not 1, 2, 4, 8 or 16;  */
+/* more than 49152 blocks), WORKSPACE, CUDA.                               */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_select_blocks(const kvd_cache *cache, const float *q, int32_t n_heads,
+                             int32_t k_sel, int32_t sink_tokens, int32_t recent_tokens,
+                             int32_t *sel_idx, int32_t *sel_cnt,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Split-KV decode attention over selected blocks only  [QUEST S3 FA-VEC   */
+/* block skip: unselected blocks are not read; CPUATT Method].             */
+/*   For query head h of KV head g, over the tokens t < len of the blocks  */
+/*   listed in sel_idx[b, g, :sel_cnt[b, g]] (ascending or not; each block */
+/*   once):                                                                 */
+/*     f16:  logit_t = softmax_scale * sum_d q[d] * k_t[d]                  */
+/*     int8: q is quantized once per head like a cache row; logit_t =      */
+/*           dot_int32(q_code, k_code_t) * q_scale * k_scale_t * softmax_scale */
+/*           and v_t = v_scale_t * v_code_t                                 */
+/*     out_h = sum_t softmax(logit)_t * v_t       (f32 accumulation)       */
+/*   An empty selection gives a zero output row.                           */
+/*   out: device [batch, n_heads, head_dim] f32.                            */
+/*   max_sel: an upper bound of every sel_cnt row (it only sizes the split  */
+/*   grid; sel_cnt values above max_sel are still attended in full), e.g.  */
+/*   kvd_selected_count(...).                                              */
+/*   workspace: as for kvd_select_blocks; holds split partials and the      */
+/*   per-problem arrival counters.  The workspace must be zero-filled      */
+/*   before its first use; every call that completes leaves the counters   */
+/*   at zero again.  After a call that reported a device fault, zero it.  */
+/* Errors: INVALID, UNSUPPORTED, WORKSPACE, CUDA.                          */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_decode_attn(const kvd_cache *cache, const float *q, int32_t n_heads,
+                           float softmax_scale, const int32_t *sel_idx,
+                           const int32_t *sel_cnt, int32_t max_sel, float *out,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Dense decode attention over all len tokens (no bounds, no selection):  */
+/* the no-skip reference arm  [QUEST Gate ladder "select-all ... sparse    */
+/* must equal dense"; CPUATT Method].  Same arithmetic and arguments as    */
+/* kvd_decode_attn with every block selected.                              */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_decode_attn_dense(const kvd_cache *cache, const float *q, int32_t n_heads,
+                                 float softmax_scale, float *out,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* One whole decode step on device buffers: append one token per sequence */
+/* (k_new, v_new: [batch, 1, n_kv_heads, head_dim] f16), then select and   */
+/* attend over the len+1 cached tokens.  Equivalent to kvd_kv_append,      */
+/* kvd_select_blocks and kvd_decode_attn in that order on `stream`; with   */
+/* k_sel < 0 the attention is dense.  sel_idx/sel_cnt may be NULL, and then */
+/* the selection lives in the workspace.  On KVD_OK cache->len has grown by */
+/* one (also when a later launch failed with KVD_ERR_CUDA after the append */
+/* was enqueued).                                                           */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
+                           const void *v_new, int32_t n_heads, float softmax_scale,
+                           int32_t k_sel, int32_t sink_tokens, int32_t recent_tokens,
+                           int32_t *sel_idx, int32_t *sel_cnt, float *out,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* kvd_decode_step with HOST inputs and output: q_host ([batch, n_heads,   */
+/* head_dim] f32), k_new_host/v_new_host ([batch, 1, n_kv_heads, head_dim] */
+/* f16) are copied into the workspace, the step runs, and the output is   */
+/* copied to out_host ([batch, n_heads, head_dim] f32), all enqueued on    */
+/* `stream`.  Host buffers should be page-locked for the copies to be      */
+/* asynchronous; out_host is valid once the stream has finished.          */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host,
+                                const void *k_new_host, const void *v_new_host,
+                                int32_t n_heads, float softmax_scale, int32_t k_sel,
+                                int32_t sink_tokens, int32_t recent_tokens,
+                                int32_t *sel_idx, int32_t *sel_cnt, float *out_host,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Workspace bytes that every call above needs for this cache geometry    */
+/* (batch, n_kv_heads, max_seq, dtype) and n_heads query heads, for any   */
+/* len <= max_seq and any selection.  One zero-filled workspace of this    */
+/* size serves all the calls (they use disjoint regions: split partials,   */
+/* per-problem arrival counters, selection keys, a selection for           */
+/* kvd_decode_step when the caller passes none, and the host-step staging  */
+/* buffers).  The split grid follows the current device's SM count, so    */
+/* query it with the device that will run the calls current.  0 on        */
+/* invalid arguments.                                                       */
+/* ---------------------------------------------------------------------- */
+KVD_API size_t kvd_workspace_bytes(const kvd_cache *cache, int32_t n_heads);
+
+/* Blocks selected per (sequence, KV head) for a cache of len tokens:      */
+/* forced sink and recent blocks plus min(k_sel, other blocks).  -1 on     */
+/* invalid arguments.  Host only.                                          */
+KVD_API int32_t kvd_selected_count(int32_t len, int32_t block, int32_t k_sel,
+                           int32_t sink_tokens, int32_t recent_tokens);
+
+/* Static description of a status code.  Host only. */
+KVD_API const char *kvd_status_string(kvd_status status);
+
+/* KVD_ABI_VERSION of the built library.  Host only. */
+KVD_API int32_t kvd_abi_version(void);
+
+/* ---------------------------------------------------------------------- */
+/* Test exports: the exact integer q.k dots and the block bounds, computed */
+/* by the same device routines the decode and select kernels use.         */
+/*   kvd_debug_qk_int8: dots [batch, n_heads, len] int32, q_codes [batch,   */
+/*   n_heads, head_dim] int8, q_scales [batch, n_heads] f32 (int8 cache     */
+/*   only)  [CPUATT Method "Logit dots are exact int32"].                   */
+/*   kvd_debug_scores: ub [batch, n_kv_heads, NB] f32, the group bound UB(j)*/
+/*   of every block j < NB = ceil(len / block)  [QUEST Method].             */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_debug_qk_int8(const kvd_cache *cache, const float *q, int32_t n_heads,
+                             int32_t *dots, int8_t *q_codes, float *q_scales, void *stream);
+KVD_API kvd_status kvd_debug_scores(const kvd_cache *cache, const float *q, int32_t n_heads,
+                            float *ub, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVDECODE_H */

@@ -1,0 +1,368 @@
+// api.cu -- the extern "C" entry points of libkvdecode.so: argument checks on
+// the host, workspace layout, and kernel dispatch on the caller's stream.
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvd {
+
+int max_select_blocks();
+
+int device_sm_count() {
+    static int cached_dev = -1, cached_sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 152;  // GB300
+    }
+    if (dev != cached_dev) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0) {
+            cudaGetLastError();
+            return 152;
+        }
+        cached_dev = dev;
+        cached_sms = sms;
+    }
+    return cached_sms;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kvd_status check_cache(const kvd_cache *c) {
+    if (!c) return KVD_ERR_INVALID;
+    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8) return KVD_ERR_INVALID;
+    if (c->batch < 1 || c->n_kv_heads < 1) return KVD_ERR_INVALID;
+    if (c->head_dim != kHeadDim) return KVD_ERR_UNSUPPORTED;
+    if (c->block != kBlock) return KVD_ERR_UNSUPPORTED;
+    if (c->max_seq < kBlock || c->max_seq % kBlock != 0) return KVD_ERR_INVALID;
+    if (c->len < 0 || c->len > c->max_seq) return KVD_ERR_INVALID;
+    if (c->reserved != 0) return KVD_ERR_INVALID;
+    const void *ptrs[4] = {c->k, c->v, c->kmin, c->kmax};
+    for (const void *p : ptrs)
+        if (!p || !aligned(p, 16)) return KVD_ERR_INVALID;
+    if (c->dtype == KVD_INT8) {
+        if (!c->k_scale || !c->v_scale || !aligned(c->k_scale, 16) || !aligned(c->v_scale, 16))
+            return KVD_ERR_INVALID;
+    }
+    if (c->dev_status && !aligned(c->dev_status, 4)) return KVD_ERR_INVALID;
+    if (static_cast<long long>(c->batch) * c->n_kv_heads * 16 > 65535) return KVD_ERR_UNSUPPORTED;
+    return KVD_OK;
+}
+
+kvd_status check_heads(const kvd_cache *c, int n_heads) {
+    if (n_heads < 1 || n_heads % c->n_kv_heads != 0) return KVD_ERR_INVALID;
+    const int G = n_heads / c->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return KVD_ERR_UNSUPPORTED;
+    return KVD_OK;
+}
+
+Geom make_geom(const kvd_cache *c, int n_heads, int len) {
+    Geom g;
+    g.dtype = c->dtype;
+    g.B = c->batch;
+    g.Hkv = c->n_kv_heads;
+    g.max_seq = c->max_seq;
+    g.len = len;
+    g.H = n_heads;
+    g.G = n_heads / c->n_kv_heads;
+    g.NB = (len + kBlock - 1) / kBlock;
+    g.nbmax = c->max_seq / kBlock;
+    return g;
+}
+
+// Workspace regions (byte offsets; every region 256-byte aligned).
+struct WsLayout {
+    size_t counters, partials, keys, sel_idx, sel_cnt, q, k_new, v_new, out, total;
+    DecodePlan plan;
+};
+
+WsLayout ws_layout(const kvd_cache *c, int n_heads) {
+    WsLayout w;
+    const Geom g = make_geom(c, n_heads, c->max_seq);
+    // splits never exceed the plan for a selection of every block
+    w.plan = plan_decode(g, g.nbmax, device_sm_count());
+    const size_t P = static_cast<size_t>(g.B) * g.Hkv;
+    size_t off = 0;
+    w.counters = off;
+    off += align_up(P * w.plan.subgroups * sizeof(uint32_t));
+    w.partials = off;
+    off += align_up(decode_partials_bytes(g, w.plan));
+    w.keys = off;
+    off += align_up(P * g.nbmax * sizeof(uint32_t));
+    w.sel_idx = off;
+    off += align_up(P * g.nbmax * sizeof(int32_t));
+    w.sel_cnt = off;
+    off += align_up(P * sizeof(int32_t));
+    w.q = off;
+    off += align_up(static_cast<size_t>(g.B) * g.H * kHeadDim * sizeof(float));
+    w.k_new = off;
+    off += align_up(P * kHeadDim * sizeof(__half));
+    w.v_new = off;
+    off += align_up(P * kHeadDim * sizeof(__half));
+    w.out = off;
+    off += align_up(static_cast<size_t>(g.B) * g.H * kHeadDim * sizeof(float));
+    w.total = off;
+    return w;
+}
+
+kvd_status check_ws(void *ws, size_t bytes, size_t need) {
+    if (!ws || !aligned(ws, kAlign) || bytes < need) return KVD_ERR_WORKSPACE;
+    return KVD_OK;
+}
+
+template <typename T>
+T *ws_at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+kvd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVD_OK : KVD_ERR_CUDA; }
+
+void forced_range(int len, int sink, int recent, int *se, int *rb) {
+    const int NB = (len + kBlock - 1) / kBlock;
+    int s = (sink + kBlock - 1) / kBlock;
+    if (s > NB) s = NB;
+    int r = NB;
+    if (recent > 0) {
+        long start = static_cast<long>(len) - recent;
+        if (start < 0) start = 0;
+        r = static_cast<int>(start / kBlock);
+    }
+    if (r < s) r = s;
+    *se = s;
+    *rb = r;
+}
+
+kvd_status select_impl(const kvd_cache *c, const float *q, int n_heads, int k_sel, int sink,
+                       int recent, int32_t *sel_idx, int32_t *sel_cnt, void *ws,
+                       const WsLayout &w, cudaStream_t st) {
+    const Geom g = make_geom(c, n_heads, c->len);
+    return cuda_status(launch_select(*c, g, q, k_sel, sink, recent, sel_idx, sel_cnt,
+                                     ws_at<uint32_t>(ws, w.keys), st, true));
+}
+
+kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float scale,
+                       const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel, float *out,
+                       void *ws, const WsLayout &w, cudaStream_t st) {
+    const Geom g = make_geom(c, n_heads, c->len);
+    const bool dense = sel_idx == nullptr;
+    int max_blocks = dense ? g.NB : max_sel;
+    if (max_blocks > g.NB) max_blocks = g.NB;
+    if (max_blocks < 1) max_blocks = 1;
+    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count());
+    return cuda_status(launch_decode(*c, g, p, q, scale, sel_idx, sel_cnt, out,
+                                     ws_at<float>(ws, w.partials),
+                                     ws_at<uint32_t>(ws, w.counters), st, true));
+}
+
+kvd_status check_select_args(const kvd_cache *c, int n_heads, int k_sel, int sink, int recent) {
+    kvd_status s = check_cache(c);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(c, n_heads)) != KVD_OK) return s;
+    if (c->len < 1 || k_sel < 0 || sink < 0 || recent < 0) return KVD_ERR_INVALID;
+    if ((c->len + kBlock - 1) / kBlock > max_select_blocks()) return KVD_ERR_UNSUPPORTED;
+    return KVD_OK;
+}
+
+}  // namespace
+}  // namespace kvd
+
+using namespace kvd;
+
+extern "C" {
+
+int32_t kvd_abi_version(void) { return KVD_ABI_VERSION; }
+
+const char *kvd_status_string(kvd_status s) {
+    switch (s) {
+        case KVD_OK: return "ok";
+        case KVD_ERR_INVALID: return "invalid argument";
+        case KVD_ERR_UNSUPPORTED: return "unsupported configuration";
+        case KVD_ERR_CAPACITY: return "append would pass max_seq";
+        case KVD_ERR_CUDA: return "CUDA runtime error";
+        case KVD_ERR_TIMEOUT: return "device wait timed out";
+        case KVD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        default: return "unknown status";
+    }
+}
+
+int32_t kvd_selected_count(int32_t len, int32_t block, int32_t k_sel, int32_t sink_tokens,
+                           int32_t recent_tokens) {
+    if (len < 1 || block != kBlock || k_sel < 0 || sink_tokens < 0 || recent_tokens < 0)
+        return -1;
+    int se, rb;
+    forced_range(len, sink_tokens, recent_tokens, &se, &rb);
+    const int NB = (len + kBlock - 1) / kBlock;
+    const int n_cand = rb - se;
+    return (NB - n_cand) + (k_sel < n_cand ? k_sel : n_cand);
+}
+
+size_t kvd_workspace_bytes(const kvd_cache *cache, int32_t n_heads) {
+    if (check_cache(cache) != KVD_OK || check_heads(cache, n_heads) != KVD_OK) return 0;
+    return ws_layout(cache, n_heads).total;
+}
+
+kvd_status kvd_kv_append(kvd_cache *cache, const void *k_new, const void *v_new, int32_t n_new,
+                         void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if (n_new < 0) return KVD_ERR_INVALID;
+    if (n_new == 0) return KVD_OK;
+    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVD_ERR_INVALID;
+    if (static_cast<long long>(cache->len) + n_new > cache->max_seq) return KVD_ERR_CAPACITY;
+    const cudaError_t e =
+        launch_append(*cache, k_new, v_new, n_new, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess) return KVD_ERR_CUDA;
+    cache->len += n_new;
+    return KVD_OK;
+}
+
+kvd_status kvd_select_blocks(const kvd_cache *cache, const float *q, int32_t n_heads,
+                             int32_t k_sel, int32_t sink_tokens, int32_t recent_tokens,
+                             int32_t *sel_idx, int32_t *sel_cnt, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    kvd_status s = check_select_args(cache, n_heads, k_sel, sink_tokens, recent_tokens);
+    if (s != KVD_OK) return s;
+    if (!q || !aligned(q, 16) || !sel_idx || !aligned(sel_idx, 4) || !sel_cnt ||
+        !aligned(sel_cnt, 4))
+        return KVD_ERR_INVALID;
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    return select_impl(cache, q, n_heads, k_sel, sink_tokens, recent_tokens, sel_idx, sel_cnt,
+                       workspace, w, static_cast<cudaStream_t>(stream));
+}
+
+kvd_status kvd_decode_attn(const kvd_cache *cache, const float *q, int32_t n_heads,
+                           float softmax_scale, const int32_t *sel_idx, const int32_t *sel_cnt,
+                           int32_t max_sel, float *out, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (cache->len < 1 || max_sel < 0) return KVD_ERR_INVALID;
+    if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
+    if (!sel_idx || !aligned(sel_idx, 4) || !sel_cnt || !aligned(sel_cnt, 4))
+        return KVD_ERR_INVALID;
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    return decode_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_cnt, max_sel, out,
+                       workspace, w, static_cast<cudaStream_t>(stream));
+}
+
+kvd_status kvd_decode_attn_dense(const kvd_cache *cache, const float *q, int32_t n_heads,
+                                 float softmax_scale, float *out, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (cache->len < 1) return KVD_ERR_INVALID;
+    if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    return decode_impl(cache, q, n_heads, softmax_scale, nullptr, nullptr, 0, out, workspace, w,
+                       static_cast<cudaStream_t>(stream));
+}
+
+kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
+                           const void *v_new, int32_t n_heads, float softmax_scale,
+                           int32_t k_sel, int32_t sink_tokens, int32_t recent_tokens,
+                           int32_t *sel_idx, int32_t *sel_cnt, float *out, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
+    if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVD_ERR_INVALID;
+    if (cache->len + 1 > cache->max_seq) return KVD_ERR_CAPACITY;
+    const bool dense = k_sel < 0;
+    if (!dense) {
+        if (sink_tokens < 0 || recent_tokens < 0) return KVD_ERR_INVALID;
+        if ((cache->len + 1 + kBlock - 1) / kBlock > max_select_blocks())
+            return KVD_ERR_UNSUPPORTED;
+        if ((sel_idx && !aligned(sel_idx, 4)) || (sel_cnt && !aligned(sel_cnt, 4)))
+            return KVD_ERR_INVALID;
+    }
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (launch_append(*cache, k_new, v_new, 1, st, true) != cudaSuccess) return KVD_ERR_CUDA;
+    cache->len += 1;
+    if (dense)
+        return decode_impl(cache, q, n_heads, softmax_scale, nullptr, nullptr, 0, out, workspace,
+                           w, st);
+    if (!sel_idx) sel_idx = ws_at<int32_t>(workspace, w.sel_idx);
+    if (!sel_cnt) sel_cnt = ws_at<int32_t>(workspace, w.sel_cnt);
+    s = select_impl(cache, q, n_heads, k_sel, sink_tokens, recent_tokens, sel_idx, sel_cnt,
+                    workspace, w, st);
+    if (s != KVD_OK) return s;
+    const int max_sel =
+        kvd_selected_count(cache->len, kBlock, k_sel, sink_tokens, recent_tokens);
+    return decode_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_cnt, max_sel, out,
+                       workspace, w, st);
+}
+
+kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host, const void *k_new_host,
+                                const void *v_new_host, int32_t n_heads, float softmax_scale,
+                                int32_t k_sel, int32_t sink_tokens, int32_t recent_tokens,
+                                int32_t *sel_idx, int32_t *sel_cnt, float *out_host,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (!q_host || !k_new_host || !v_new_host || !out_host) return KVD_ERR_INVALID;
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t qb = static_cast<size_t>(cache->batch) * n_heads * kHeadDim * sizeof(float);
+    const size_t kb = static_cast<size_t>(cache->batch) * cache->n_kv_heads * kHeadDim * 2;
+    float *q_dev = ws_at<float>(workspace, w.q);
+    void *k_dev = ws_at<void>(workspace, w.k_new);
+    void *v_dev = ws_at<void>(workspace, w.v_new);
+    float *o_dev = ws_at<float>(workspace, w.out);
+    if (cudaMemcpyAsync(q_dev, q_host, qb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(k_dev, k_new_host, kb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(v_dev, v_new_host, kb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return KVD_ERR_CUDA;
+    s = kvd_decode_step(cache, q_dev, k_dev, v_dev, n_heads, softmax_scale, k_sel, sink_tokens,
+                        recent_tokens, sel_idx, sel_cnt, o_dev, workspace, workspace_bytes,
+                        stream);
+    if (s != KVD_OK) return s;
+    if (cudaMemcpyAsync(out_host, o_dev, qb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KVD_ERR_CUDA;
+    return KVD_OK;
+}
+
+kvd_status kvd_debug_qk_int8(const kvd_cache *cache, const float *q, int32_t n_heads,
+                             int32_t *dots, int8_t *q_codes, float *q_scales, void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (cache->dtype != KVD_INT8 || cache->len < 1) return KVD_ERR_INVALID;
+    if (!q || !aligned(q, 16) || !dots || !aligned(dots, 4) || !q_codes ||
+        !aligned(q_codes, 4) || !q_scales || !aligned(q_scales, 4))
+        return KVD_ERR_INVALID;
+    const Geom g = make_geom(cache, n_heads, cache->len);
+    return cuda_status(launch_qk_debug(*cache, g, q, dots, q_codes, q_scales,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+kvd_status kvd_debug_scores(const kvd_cache *cache, const float *q, int32_t n_heads, float *ub,
+                            void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (cache->len < 1) return KVD_ERR_INVALID;
+    if (!q || !aligned(q, 16) || !ub || !aligned(ub, 4)) return KVD_ERR_INVALID;
+    const Geom g = make_geom(cache, n_heads, cache->len);
+    return cuda_status(launch_scores_debug(*cache, g, q, ub, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

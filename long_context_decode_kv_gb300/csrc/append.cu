@@ -1,0 +1,124 @@
+// append.cu -- KV append: copy (f16) or absmax-quantize (int8) the new rows
+// and fill the per-block key envelope in the same pass.
+//
+// "Sparse Attention -- Quest-style block-selector for long-context decode
+// (#551)", S2/S3 "Fill op" and "All-KV-types composition (bug-747)": for every
+// block the new tokens touch, reduce the channel-wise min and max of the new
+// f16 keys; merge (min/max) into a block that already held tokens, overwrite
+// a block that starts in the new range.  Bounds always come from the f16 keys
+// before quantization.  "cpu-attn", Method: K and V are quantized per token
+// per head (absmax int8) at append time.
+//
+// One warp per (sequence, KV head, touched block); lane l owns channels
+// 4l..4l+3, so every row is read as one coalesced 256-byte line.
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvd {
+namespace {
+
+constexpr int kAppendWarps = 4;
+
+__device__ __forceinline__ void load_half4(const __half *p, float (&x)[4]) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+__device__ __forceinline__ void store_half4(__half *p, const float (&x)[4]) {
+    __half2 a = __floats2half2_rn(x[0], x[1]);
+    __half2 b = __floats2half2_rn(x[2], x[3]);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t *>(&a);
+    w.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = w;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(32 * kAppendWarps)
+append_kernel(kvd_cache c, const __half *__restrict__ k_new, const __half *__restrict__ v_new,
+              int n_new, int len0, int first_blk, int n_aff) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int a = blockIdx.x * kAppendWarps + warp;
+    if (a >= n_aff) return;
+    const int p = blockIdx.y;
+    const int b = p / c.n_kv_heads, h = p % c.n_kv_heads;
+    const int blk = first_blk + a;
+    const long lo = static_cast<long>(blk) * kBlock;
+    const long nlo = lo > len0 ? lo : len0;
+    const long nhi = (lo + kBlock) < (static_cast<long>(len0) + n_new) ? (lo + kBlock)
+                                                                      : (static_cast<long>(len0) + n_new);
+    const bool merge = lo < len0;
+    const size_t row0 = (static_cast<size_t>(b) * c.n_kv_heads + h) * c.max_seq;
+
+    float mn[4], mx[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { mn[j] = __int_as_float(0x7f800000); mx[j] = -mn[j]; }
+
+    for (long t = nlo; t < nhi; ++t) {
+        const size_t src = ((static_cast<size_t>(b) * n_new + (t - len0)) * c.n_kv_heads + h) *
+                               kHeadDim + 4 * lane;
+        float kx[4], vx[4];
+        load_half4(k_new + src, kx);
+        load_half4(v_new + src, vx);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { mn[j] = fminf(mn[j], kx[j]); mx[j] = fmaxf(mx[j], kx[j]); }
+        const size_t dst = (row0 + t) * kHeadDim + 4 * lane;
+        if (DT == KVD_F16) {
+            // verbatim copy of the f16 bits
+            *reinterpret_cast<uint2 *>(static_cast<__half *>(c.k) + dst) =
+                *reinterpret_cast<const uint2 *>(k_new + src);
+            *reinterpret_cast<uint2 *>(static_cast<__half *>(c.v) + dst) =
+                *reinterpret_cast<const uint2 *>(v_new + src);
+        } else {
+            float ks, vs;
+            const uint32_t kc = quantize_row_warp(kx, &ks);
+            const uint32_t vc = quantize_row_warp(vx, &vs);
+            *reinterpret_cast<uint32_t *>(static_cast<int8_t *>(c.k) + dst) = kc;
+            *reinterpret_cast<uint32_t *>(static_cast<int8_t *>(c.v) + dst) = vc;
+            if (lane == 0) {
+                c.k_scale[row0 + t] = ks;
+                c.v_scale[row0 + t] = vs;
+            }
+        }
+    }
+    const size_t nbmax = static_cast<size_t>(c.max_seq / kBlock);
+    const size_t bidx = ((static_cast<size_t>(b) * c.n_kv_heads + h) * nbmax + blk) * kHeadDim +
+                        4 * lane;
+    __half *kmin = static_cast<__half *>(c.kmin) + bidx;
+    __half *kmax = static_cast<__half *>(c.kmax) + bidx;
+    if (merge) {
+        float om[4], oM[4];
+        load_half4(kmin, om);
+        load_half4(kmax, oM);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { mn[j] = fminf(mn[j], om[j]); mx[j] = fmaxf(mx[j], oM[j]); }
+    }
+    // every value is an f16 already, so the conversions back are exact
+    store_half4(kmin, mn);
+    store_half4(kmax, mx);
+}
+
+}  // namespace
+
+cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_new, int n_new,
+                          cudaStream_t st, bool pdl) {
+    const int len0 = c.len;
+    const int first = len0 / kBlock;
+    const int last = (len0 + n_new - 1) / kBlock;
+    const int n_aff = last - first + 1;
+    dim3 grid((n_aff + kAppendWarps - 1) / kAppendWarps, c.batch * c.n_kv_heads);
+    dim3 block(32 * kAppendWarps);
+    const __half *kn = static_cast<const __half *>(k_new);
+    const __half *vn = static_cast<const __half *>(v_new);
+    if (c.dtype == KVD_F16)
+        return launch_ex(append_kernel<KVD_F16>, grid, block, 0, st, pdl, c, kn, vn, n_new, len0,
+                         first, n_aff);
+    return launch_ex(append_kernel<KVD_INT8>, grid, block, 0, st, pdl, c, kn, vn, n_new, len0,
+                     first, n_aff);
+}
+
+}  // namespace kvd

@@ -1,0 +1,168 @@
+// common.cuh -- device helpers shared by the kvdecode kernels (sm_103a).
+//
+// Inline PTX for the Blackwell data-movement path: mbarrier phases, 1-D TMA
+// bulk copies global->shared (cp.async.bulk ... complete_tx), L2 cache
+// policies, and programmatic dependent launch (griddepcontrol).  Every wait
+// on an mbarrier is bounded in time; when the bound runs out the kernel
+// records KVD_ERR_TIMEOUT in the cache's status word and winds down instead
+// of trapping.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvdecode.h"
+
+namespace kvd {
+
+constexpr int kHeadDim = 128;     // D
+constexpr int kBlock = 64;        // B_SEL
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kNegBig = -1.0e30f;  // finite "minus infinity" for running maxima
+// Device waits give up after this many nanoseconds of wall time.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ---------------------------------------------------------------- PTX ---
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Both arrive forms return the barrier state token (unused by callers).
+__device__ __forceinline__ uint64_t mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    uint64_t state;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
+                 : "=l"(state)
+                 : "r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+    return state;
+}
+
+__device__ __forceinline__ uint64_t mbar_arrive(uint64_t *bar) {
+    uint64_t state;
+    asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];"
+                 : "=l"(state)
+                 : "r"(smem_addr(bar))
+                 : "memory");
+    return state;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits until the phase with the given parity has completed.  Returns false
+// when `abort_flag` (shared memory) becomes non-zero or the time limit passes.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// L2 policy for data read once per step (K/V blocks): evict first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D TMA bulk copy global -> shared; completes `bytes` transactions on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void tma_load_1d(void *dst, const void *src, uint32_t bytes,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Programmatic dependent launch: wait for the upstream grid's memory, and
+// allow the downstream grid to start its prologue.
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void report_status(int32_t *dev_status, int code) {
+    if (dev_status) atomicCAS(reinterpret_cast<int *>(dev_status), 0, code);
+}
+
+// ------------------------------------------------------------ numerics ---
+// Order-preserving map f32 -> u32 (larger float, larger key); -0 maps as +0.
+__device__ __forceinline__ uint32_t float_to_key(float f) {
+    if (f == 0.0f) f = 0.0f;
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Four signed bytes of `w` -> four exact floats.  Flipping the sign bit
+// turns int8 b into the unsigned byte b+128; placed as the low mantissa
+// byte of 2^23 it reads as the float 2^23 + b + 128, and subtracting
+// 2^23 + 128 leaves b exactly.
+__device__ __forceinline__ void s8x4_to_f32(uint32_t w, float (&f)[4]) {
+    const uint32_t u = w ^ 0x80808080u;
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.0f;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.0f;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
+}
+
+// Absmax int8 quantization of one 128-wide row held 4 values per lane by a
+// full warp (lane l holds x[4l..4l+3]).  scale = absmax/127 (IEEE f32
+// division), code = round-half-even(x/scale) clamped to +-127, and a zero
+// scale gives zero codes.  Returns the packed codes of the lane's 4 values
+// (value 4l in the low byte) and writes the scale to *scale (all lanes).
+__device__ __forceinline__ uint32_t quantize_row_warp(const float (&x)[4], float *scale) {
+    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float s = __fdiv_rn(a, 127.0f);
+    *scale = s;
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int c = 0;
+        if (s != 0.0f) {
+            c = __float2int_rn(__fdiv_rn(x[j], s));
+            c = max(-127, min(127, c));
+        }
+        packed |= (static_cast<uint32_t>(c) & 0xffu) << (8 * j);
+    }
+    return packed;
+}
+
+}  // namespace kvd

@@ -1,0 +1,767 @@
+// decode.cu -- split-KV single-token decode attention that reads only the
+// selected KV blocks (or all of them for the dense arm).
+//
+// "Sparse Attention -- Quest-style block-selector for long-context decode
+// (#551)", S3 "FA-VEC block-skip": unselected blocks are skipped before the
+// K read, the q.k product and the V accumulation; "the long-ctx decode hot
+// path is FA-VEC, not MMA" -- no tensor cores: the work is ~4 multiply-adds
+// per byte read, far under the ALU ridge, so HBM bandwidth bounds it.
+// "cpu-attn", Method: int8 rows with per-token scales, exact int32 q.k dots
+// on the query quantized once per head, f32 softmax and f32 accumulation.
+// "SCSA", Mechanism: an online-softmax (max, sum, accumulator) gauge over an
+// ascending sweep, merged across splits.
+//
+// CTA = (split s of the block list, sequence b, KV head g, head subgroup).
+// Warp 8 is the producer: one lane streams each listed 64-token block (K, V
+// and, for int8, both scale rows) into a ring of shared-memory stages with
+// 1-D TMA bulk copies completing on an mbarrier.  Warps 0..7 consume every
+// stage; warp w owns tokens 8w..8w+7 of each block and keeps its own online
+// softmax state for the CTA's query heads, so no CTA-wide barrier is needed
+// per block.  At the end the 8 warp states merge in shared memory and the
+// CTA writes a partial (m, l, acc[128]) per head; the last CTA of the
+// problem to arrive merges all splits into the output.
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvd {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+// Partial rows: m, l, two pad words, acc[128] (acc 16-byte aligned).
+constexpr int kPartStride = kHeadDim + 4;
+constexpr int kAccOff = 4;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int DT>
+struct Tile;
+template <>
+struct Tile<KVD_INT8> {
+    static constexpr int kRowBytes = kHeadDim;                      // int8 codes
+    static constexpr int kKBytes = kBlock * kRowBytes;              // 8192
+    static constexpr int kStageBytes = 2 * kKBytes + 2 * kBlock * 4;  // + both scale rows
+    static constexpr int kStages = 6;
+    static constexpr int kMinCtas = 2;
+};
+template <>
+struct Tile<KVD_F16> {
+    static constexpr int kRowBytes = 2 * kHeadDim;                  // f16
+    static constexpr int kKBytes = kBlock * kRowBytes;              // 16384
+    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kStages = 3;
+    static constexpr int kMinCtas = 2;
+};
+
+struct DecodeArgs {
+    const void *k, *v;
+    const float *k_scale, *v_scale;
+    const float *q;
+    float *out;
+    const int32_t *sel_idx, *sel_cnt;
+    float *partials;
+    uint32_t *counters;
+    int32_t *dev_status;
+    int Hkv, H, G, max_seq, nbmax, len, NB, splits, subgroups;
+    float scale_log2;  // softmax_scale * log2(e): logits live in base 2
+};
+
+template <int DT, int GC>
+struct SmemLayout {
+    static constexpr int kStageBytes = Tile<DT>::kStageBytes;
+    static constexpr int kStages = Tile<DT>::kStages;
+    static constexpr int kStagesOff = 0;
+    static constexpr int kMergeBytes = kConsumerWarps * GC * kPartStride * 4;
+    static constexpr int kRing = kStages * kStageBytes;
+    static constexpr int kBarOff = (kRing > kMergeBytes ? kRing : kMergeBytes);
+    static constexpr int kFullOff = kBarOff;
+    static constexpr int kEmptyOff = kFullOff + 8 * kStages;
+    static constexpr int kBlkOff = kEmptyOff + 8 * kStages;
+    static constexpr int kQOff = (kBlkOff + 4 * kStages + 15) / 16 * 16;
+    static constexpr int kQBytes = GC * kHeadDim * 4;                  // f32 q (f16) or codes
+    static constexpr int kCoefOff = kQOff + kQBytes;
+    static constexpr int kPwOff = kCoefOff + 16;
+    static constexpr int kPwBytes = kConsumerWarps * 8 * 4 * 4;        // [warp][8 tok][4] f32
+    static constexpr int kFlagOff = kPwOff + kPwBytes;
+    static constexpr int kTotal = kFlagOff + 16;
+};
+
+// ----------------------------------------------------------------------------
+// int32 reductions over the 4 quarter lanes (lane bits 0..1) returning to each
+// lane the total of head (c * GC) / 4.
+template <int GC>
+__device__ __forceinline__ int reduce4_scatter(int (&v)[GC], int c) {
+    if constexpr (GC == 4) {
+        const bool up = (c & 2) != 0;
+        int k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+        const int s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
+        k0 += __shfl_xor_sync(kFull, s0, 2);
+        k1 += __shfl_xor_sync(kFull, s1, 2);
+        const bool lo = (c & 1) != 0;
+        int k = lo ? k1 : k0;
+        k += __shfl_xor_sync(kFull, lo ? k0 : k1, 1);
+        return k;
+    } else if constexpr (GC == 2) {
+        const bool up = (c & 2) != 0;
+        int k = up ? v[1] : v[0];
+        k += __shfl_xor_sync(kFull, up ? v[0] : v[1], 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    } else {
+        int k = v[0];
+        k += __shfl_xor_sync(kFull, k, 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    }
+}
+
+// f32 version over the 8 eighth lanes (lane bits 0..2): head (e * GC) / 8.
+template <int GC>
+__device__ __forceinline__ float reduce8_scatter(float (&v)[GC], int e) {
+    if constexpr (GC == 4) {
+        const bool up = (e & 4) != 0;
+        float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+        const float s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
+        k0 += __shfl_xor_sync(kFull, s0, 4);
+        k1 += __shfl_xor_sync(kFull, s1, 4);
+        const bool mid = (e & 2) != 0;
+        float k = mid ? k1 : k0;
+        k += __shfl_xor_sync(kFull, mid ? k0 : k1, 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    } else if constexpr (GC == 2) {
+        const bool up = (e & 4) != 0;
+        float k = up ? v[1] : v[0];
+        k += __shfl_xor_sync(kFull, up ? v[0] : v[1], 4);
+        k += __shfl_xor_sync(kFull, k, 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    } else {
+        float k = v[0];
+        k += __shfl_xor_sync(kFull, k, 4);
+        k += __shfl_xor_sync(kFull, k, 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Query prologue, one warp per head hh < GC of the CTA.
+//  int8: the row is quantized like a cache row (absmax, per head, once); the
+//        packed codes go to q_s ([GC][32] words) and the logit coefficient
+//        q_scale * softmax_scale * log2(e) to coef[hh].
+//  f16:  q * softmax_scale * log2(e) in f32 goes to q_s ([GC][128] floats).
+template <int DT, int GC>
+__device__ __forceinline__ void load_query(const DecodeArgs &a, int b, int h0, int warp, int lane,
+                                           uint32_t *q_s, float *coef, int8_t *q_codes_out,
+                                           float *q_scales_out) {
+    if (warp >= GC) return;
+    const int hq = h0 + warp;
+    const float4 x4 = *reinterpret_cast<const float4 *>(
+        a.q + (static_cast<size_t>(b) * a.H + hq) * kHeadDim + 4 * lane);
+    const float x[4] = {x4.x, x4.y, x4.z, x4.w};
+    if constexpr (DT == KVD_INT8) {
+        float s;
+        const uint32_t packed = quantize_row_warp(x, &s);
+        q_s[warp * 32 + lane] = packed;
+        if (lane == 0) coef[warp] = s * a.scale_log2;
+        if (q_codes_out) {
+            *reinterpret_cast<uint32_t *>(q_codes_out +
+                                          (static_cast<size_t>(b) * a.H + hq) * kHeadDim +
+                                          4 * lane) = packed;
+            if (lane == 0) q_scales_out[static_cast<size_t>(b) * a.H + hq] = s;
+        }
+    } else {
+        float *qf = reinterpret_cast<float *>(q_s) + warp * kHeadDim + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qf[j] = x[j] * a.scale_log2;
+    }
+}
+
+// int8 QK mapping: lane = 4 t + c (t: token slot 0..7, c: quarter 0..3 of the
+// 128 channels).  The lane reads 16-byte chunks 2c and 2c+1 of its token row,
+// odd tokens in swapped order so that the 8 lanes of each quarter-warp hit
+// distinct banks.  qr holds the matching query words in that order.
+template <int GC>
+struct QRegsI8 {
+    uint32_t w[GC][8];
+};
+
+template <int GC>
+__device__ __forceinline__ void load_qregs_i8(const uint32_t *q_s, int t, int c, QRegsI8<GC> &r) {
+#pragma unroll
+    for (int h = 0; h < GC; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int chunk = 2 * c + (i ^ (t & 1));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r.w[h][4 * i + j] = q_s[h * 32 + 4 * chunk + j];
+        }
+}
+
+// Exact int32 dot of one token row with the query of head (c*GC)/4.
+template <int GC>
+__device__ __forceinline__ int qk_int8_row(const int8_t *row, const QRegsI8<GC> &r, int t, int c) {
+    const uint4 ka = *reinterpret_cast<const uint4 *>(row + 16 * (2 * c + (t & 1)));
+    const uint4 kb = *reinterpret_cast<const uint4 *>(row + 16 * (2 * c + 1 - (t & 1)));
+    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+    int d[GC];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        int s = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            s = __dp4a(static_cast<int>(kw[j]), static_cast<int>(r.w[h][j]), s);
+        d[h] = s;
+    }
+    return reduce4_scatter<GC>(d, c);
+}
+
+// f16 QK mapping: lane = 8 t4 + e (t4: token slot 0..3 per pass, e: eighth
+// 0..7 of the channels).  The lane reads chunks 2e and 2e+1 (8 halves each) of
+// its token row, lanes e >= 4 in swapped order (bank-conflict free).
+template <int GC>
+struct QRegsF16 {
+    float f[GC][16];
+};
+
+template <int GC>
+__device__ __forceinline__ void load_qregs_f16(const uint32_t *q_s, int e, QRegsF16<GC> &r) {
+    const float *qf = reinterpret_cast<const float *>(q_s);
+#pragma unroll
+    for (int h = 0; h < GC; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int chunk = 2 * e + (i ^ (e >> 2));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r.f[h][8 * i + j] = qf[h * kHeadDim + 8 * chunk + j];
+        }
+}
+
+template <int GC>
+__device__ __forceinline__ float qk_f16_row(const __half *row, const QRegsF16<GC> &r, int e) {
+    const uint4 ka = *reinterpret_cast<const uint4 *>(row + 8 * (2 * e + (e >> 2)));
+    const uint4 kb = *reinterpret_cast<const uint4 *>(row + 8 * (2 * e + 1 - (e >> 2)));
+    float kf[16];
+    const __half2 *ha = reinterpret_cast<const __half2 *>(&ka);
+    const __half2 *hb = reinterpret_cast<const __half2 *>(&kb);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 fa = __half22float2(ha[i]);
+        const float2 fb = __half22float2(hb[i]);
+        kf[2 * i] = fa.x;
+        kf[2 * i + 1] = fa.y;
+        kf[8 + 2 * i] = fb.x;
+        kf[8 + 2 * i + 1] = fb.y;
+    }
+    float d[GC];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) s = fmaf(r.f[h][j], kf[j], s);
+        d[h] = s;
+    }
+    return reduce8_scatter<GC>(d, e);
+}
+
+// Running softmax state of one consumer warp for the CTA's GC heads.
+template <int GC>
+struct WarpState {
+    float m;           // running max (base-2 logits) of this lane's QK head
+    float l;           // this lane's share of the running sum
+    float acc[GC][4];  // channels 4*lane .. 4*lane+3 of every head
+};
+
+template <int GC>
+__device__ __forceinline__ void rescale(WarpState<GC> &st, float alpha_own, int lane_of_head0,
+                                        int lanes_per_head) {
+    if (__any_sync(kFull, alpha_own != 1.0f)) {
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            const float al = __shfl_sync(kFull, alpha_own, lane_of_head0 + h * lanes_per_head);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) st.acc[h][j] *= al;
+        }
+    }
+}
+
+// One stage (64-token block) for one consumer warp, int8 cache.
+template <int GC>
+__device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, const float *coef,
+                                             const QRegsI8<GC> &qr, float *pw, int warp, int lane,
+                                             WarpState<GC> &st) {
+    const int8_t *Ks = reinterpret_cast<const int8_t *>(stage);
+    const int8_t *Vs = Ks + Tile<KVD_INT8>::kKBytes;
+    const float *ksc = reinterpret_cast<const float *>(stage + 2 * Tile<KVD_INT8>::kKBytes);
+    const float *vsc = ksc + kBlock;
+    const int t = lane >> 2, c = lane & 3;
+    const int tok = 8 * warp + t;
+    const int hq = (c * GC) >> 2;
+    const int dot = qk_int8_row<GC>(Ks + tok * kHeadDim, qr, t, c);
+    const float x = tok < n_valid ? static_cast<float>(dot) * coef[hq] * ksc[tok]
+                                  : -__int_as_float(0x7f800000);
+    float bm = x;
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+    const float m_new = fmaxf(st.m, bm);
+    const float alpha = exp2f(st.m - m_new);
+    const float p = exp2f(x - m_new);
+    st.l = st.l * alpha + p;
+    st.m = m_new;
+    constexpr int lph = 4 / GC;  // lanes per head among the quarters
+    if ((c % lph) == 0) pw[t * 4 + hq] = tok < n_valid ? p * vsc[tok] : 0.0f;
+    rescale<GC>(st, alpha, 0, lph);
+    __syncwarp();
+    const int nt = min(8, n_valid - 8 * warp);
+#pragma unroll 8
+    for (int t2 = 0; t2 < nt; ++t2) {
+        const uint32_t vw =
+            *reinterpret_cast<const uint32_t *>(Vs + (8 * warp + t2) * kHeadDim + 4 * lane);
+        const float4 pv = *reinterpret_cast<const float4 *>(pw + 4 * t2);
+        const float pp[4] = {pv.x, pv.y, pv.z, pv.w};
+        float f[4];
+        s8x4_to_f32(vw, f);
+#pragma unroll
+        for (int h = 0; h < GC; ++h)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) st.acc[h][j] = fmaf(pp[h], f[j], st.acc[h][j]);
+    }
+}
+
+// One stage for one consumer warp, f16 cache: two passes of 4 tokens.
+template <int GC>
+__device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
+                                            const QRegsF16<GC> &qr, float *pw, int warp,
+                                            int lane, WarpState<GC> &st) {
+    const __half *Ks = reinterpret_cast<const __half *>(stage);
+    const __half *Vs = Ks + kBlock * kHeadDim;
+    const int t4 = lane >> 3, e = lane & 7;
+    const int hq = (e * GC) >> 3;
+    const int tok0 = 8 * warp + t4, tok1 = tok0 + 4;
+    const float ninf = -__int_as_float(0x7f800000);
+    float x0 = qk_f16_row<GC>(Ks + tok0 * kHeadDim, qr, e);
+    float x1 = qk_f16_row<GC>(Ks + tok1 * kHeadDim, qr, e);
+    x0 = tok0 < n_valid ? x0 : ninf;
+    x1 = tok1 < n_valid ? x1 : ninf;
+    float bm = fmaxf(x0, x1);
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+    const float m_new = fmaxf(st.m, bm);
+    const float alpha = exp2f(st.m - m_new);
+    const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
+    st.l = st.l * alpha + (p0 + p1);
+    st.m = m_new;
+    constexpr int lph = 8 / GC;
+    if ((e % lph) == 0) {
+        pw[t4 * 4 + hq] = p0;
+        pw[(t4 + 4) * 4 + hq] = p1;
+    }
+    rescale<GC>(st, alpha, 0, lph);
+    __syncwarp();
+    const int nt = min(8, n_valid - 8 * warp);
+#pragma unroll 8
+    for (int t2 = 0; t2 < nt; ++t2) {
+        const uint2 vw =
+            *reinterpret_cast<const uint2 *>(Vs + (8 * warp + t2) * kHeadDim + 4 * lane);
+        const float2 va = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
+        const float2 vb = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
+        const float f[4] = {va.x, va.y, vb.x, vb.y};
+        const float4 pv = *reinterpret_cast<const float4 *>(pw + 4 * t2);
+        const float pp[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int h = 0; h < GC; ++h)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) st.acc[h][j] = fmaf(pp[h], f[j], st.acc[h][j]);
+    }
+}
+
+template <int DT, int GC, bool DENSE>
+__global__ void __launch_bounds__(kThreads, Tile<DT>::kMinCtas) decode_kernel(DecodeArgs a) {
+    using SL = SmemLayout<DT, GC>;
+    using TL = Tile<DT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SL::kFullOff);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + SL::kEmptyOff);
+    int *stage_blk = reinterpret_cast<int *>(smem + SL::kBlkOff);
+    uint32_t *q_s = reinterpret_cast<uint32_t *>(smem + SL::kQOff);
+    float *coef = reinterpret_cast<float *>(smem + SL::kCoefOff);
+    float *pw_all = reinterpret_cast<float *>(smem + SL::kPwOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SL::kFlagOff);
+    int *last_flag = reinterpret_cast<int *>(smem + SL::kFlagOff + 4);
+    int *issued_s = reinterpret_cast<int *>(smem + SL::kFlagOff + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x;
+    const int prob = blockIdx.y;  // ((b * Hkv) + g) * subgroups + sub
+    const int sub = prob % a.subgroups;
+    const int bg = prob / a.subgroups;  // b * Hkv + g
+    const int b = bg / a.Hkv, g = bg % a.Hkv;
+    const int h0 = g * a.G + sub * GC;
+
+    if (tid == 0) {
+        for (int i = 0; i < TL::kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        *issued_s = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_wait();  // upstream kernels (append, select) are complete past here
+
+    load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
+    int cnt = DENSE ? a.NB : a.sel_cnt[bg];
+    cnt = max(0, min(cnt, a.NB));
+    const int beg = static_cast<int>((static_cast<long long>(split) * cnt) / a.splits);
+    const int end = static_cast<int>((static_cast<long long>(split + 1) * cnt) / a.splits);
+    const int n = end - beg;
+    __syncthreads();
+    pdl_launch_dependents();
+
+    const size_t row0 = static_cast<size_t>(bg) * a.max_seq;  // first token row of (b, g)
+    WarpState<GC> st;
+    st.m = kNegBig;
+    st.l = 0.0f;
+#pragma unroll
+    for (int h = 0; h < GC; ++h)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st.acc[h][j] = 0.0f;
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        const uint64_t pol = l2_policy_evict_first();
+        const int32_t *list = a.sel_idx + static_cast<size_t>(bg) * a.nbmax + beg;
+        int issued = 0;
+        bool ok = true;
+        for (int i0 = 0; i0 < n && ok; i0 += 32) {
+            int mine = 0;
+            if (i0 + lane < n) mine = DENSE ? beg + i0 + lane : list[i0 + lane];
+            const int m = min(32, n - i0);
+            for (int j = 0; j < m; ++j) {
+                const int blk = __shfl_sync(kFull, mine, j);
+                const int i = i0 + j;
+                const int s = i % TL::kStages;
+                if (lane == 0) {
+                    if (i >= TL::kStages)
+                        ok = mbar_wait(&empty[s], ((i / TL::kStages) - 1) & 1, abort_flag);
+                    if (ok) {
+                        if (blk >= 0 && blk < a.NB) {
+                            stage_blk[s] = blk;
+                            uint8_t *dst = smem + SL::kStagesOff + s * TL::kStageBytes;
+                            const size_t r = row0 + static_cast<size_t>(blk) * kBlock;
+                            mbar_arrive_expect_tx(&full[s], TL::kStageBytes);
+                            tma_load_1d(dst, static_cast<const uint8_t *>(a.k) + r * TL::kRowBytes,
+                                        TL::kKBytes, &full[s], pol);
+                            tma_load_1d(dst + TL::kKBytes,
+                                        static_cast<const uint8_t *>(a.v) + r * TL::kRowBytes,
+                                        TL::kKBytes, &full[s], pol);
+                            if constexpr (DT == KVD_INT8) {
+                                tma_load_1d(dst + 2 * TL::kKBytes, a.k_scale + r, kBlock * 4,
+                                            &full[s], pol);
+                                tma_load_1d(dst + 2 * TL::kKBytes + kBlock * 4, a.v_scale + r,
+                                            kBlock * 4, &full[s], pol);
+                            }
+                        } else {
+                            // an id outside the cache: report it, skip the block
+                            stage_blk[s] = -1;
+                            report_status(a.dev_status, KVD_ERR_INVALID);
+                            mbar_arrive(&full[s]);
+                        }
+                        issued = i + 1;
+                    } else {
+                        *abort_flag = 1;
+                        report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                    }
+                }
+                ok = __shfl_sync(kFull, ok, 0);
+                if (!ok) break;
+            }
+        }
+        if (lane == 0) *issued_s = issued;
+    } else {
+        // ------------------------------------------------------ consumers
+        float *pw = pw_all + warp * 32;
+        if constexpr (DT == KVD_INT8) {
+            QRegsI8<GC> qr;
+            load_qregs_i8<GC>(q_s, lane >> 2, lane & 3, qr);
+            for (int i = 0; i < n; ++i) {
+                const int s = i % TL::kStages;
+                const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
+                if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                const int blk = stage_blk[s];
+                if (blk >= 0) {
+                    const int n_valid = min(kBlock, a.len - blk * kBlock);
+                    consume_int8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, coef,
+                                     qr, pw, warp, lane, st);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+        } else {
+            QRegsF16<GC> qr;
+            load_qregs_f16<GC>(q_s, lane & 7, qr);
+            for (int i = 0; i < n; ++i) {
+                const int s = i % TL::kStages;
+                const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
+                if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                const int blk = stage_blk[s];
+                if (blk >= 0) {
+                    const int n_valid = min(kBlock, a.len - blk * kBlock);
+                    consume_f16<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, qr, pw,
+                                    warp, lane, st);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+        }
+        // per-warp totals: l summed over the lanes of each head
+        if constexpr (DT == KVD_INT8) {
+            st.l += __shfl_xor_sync(kFull, st.l, 4);
+            st.l += __shfl_xor_sync(kFull, st.l, 8);
+            st.l += __shfl_xor_sync(kFull, st.l, 16);
+        } else {
+            st.l += __shfl_xor_sync(kFull, st.l, 8);
+            st.l += __shfl_xor_sync(kFull, st.l, 16);
+        }
+    }
+    __syncthreads();  // (A) every stage consumed: the ring becomes the merge area
+    const bool aborted = *abort_flag != 0;
+    if (!aborted && warp < kConsumerWarps) {
+        float *mg = reinterpret_cast<float *>(smem + SL::kStagesOff);
+        constexpr int lph = (DT == KVD_INT8 ? 4 : 8) / GC;
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            float *row = mg + (warp * GC + h) * kPartStride;
+            if (lane == h * lph) {
+                row[0] = st.m;
+                row[1] = st.l;
+            }
+            *reinterpret_cast<float4 *>(row + kAccOff + 4 * lane) =
+                make_float4(st.acc[h][0], st.acc[h][1], st.acc[h][2], st.acc[h][3]);
+        }
+    }
+    __syncthreads();  // (B) merge area written
+    if (aborted) {
+        // wind down: wait (bounded) for the copies still landing in the ring
+        if (warp == kConsumerWarps && lane == 0) {
+            const int issued = *issued_s;
+            volatile int never = 0;
+            for (int i = max(0, issued - TL::kStages); i < issued; ++i)
+                (void)mbar_wait(&full[i % TL::kStages], (i / TL::kStages) & 1, &never);
+        }
+        return;
+    }
+
+    // ---- CTA merge of the 8 warp states: thread (h, d)
+    const float *mg = reinterpret_cast<const float *>(smem + SL::kStagesOff);
+    const bool single = a.splits == 1;
+    float *part = a.partials + (static_cast<size_t>(prob) * a.splits + split) * GC * kPartStride;
+    for (int o = tid; o < GC * kHeadDim; o += kThreads) {
+        const int h = o / kHeadDim, d = o % kHeadDim;
+        float M = kNegBig;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg[(w * GC + h) * kPartStride]);
+        float L = 0.0f, A = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float *row = mg + (w * GC + h) * kPartStride;
+            const float sc = exp2f(row[0] - M);
+            L = fmaf(sc, row[1], L);
+            A = fmaf(sc, row[kAccOff + d], A);
+        }
+        if (single) {
+            a.out[(static_cast<size_t>(b) * a.H + h0 + h) * kHeadDim + d] = L > 0.0f ? A / L : 0.0f;
+        } else {
+            float *pr = part + h * kPartStride;
+            if (d == 0) {
+                pr[0] = M;
+                pr[1] = L;
+            }
+            pr[kAccOff + d] = A;
+        }
+    }
+    if (single) return;
+
+    // ---- the last CTA of this problem to arrive merges all splits
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&a.counters[prob], 1u);
+        *last_flag = prev == static_cast<unsigned>(a.splits - 1);
+    }
+    __syncthreads();
+    if (!*last_flag) return;
+    __threadfence();
+    const float *p0 = a.partials + static_cast<size_t>(prob) * a.splits * GC * kPartStride;
+    for (int o = tid; o < GC * kHeadDim; o += kThreads) {
+        const int h = o / kHeadDim, d = o % kHeadDim;
+        float M = kNegBig;
+        for (int s = 0; s < a.splits; ++s)
+            M = fmaxf(M, __ldcg(p0 + (static_cast<size_t>(s) * GC + h) * kPartStride));
+        float L = 0.0f, A = 0.0f;
+        for (int s = 0; s < a.splits; ++s) {
+            const float *pr = p0 + (static_cast<size_t>(s) * GC + h) * kPartStride;
+            const float sc = exp2f(__ldcg(pr) - M);
+            L = fmaf(sc, __ldcg(pr + 1), L);
+            A = fmaf(sc, __ldcg(pr + kAccOff + d), A);
+        }
+        a.out[(static_cast<size_t>(b) * a.H + h0 + h) * kHeadDim + d] = L > 0.0f ? A / L : 0.0f;
+    }
+    if (tid == 0) a.counters[prob] = 0u;  // leave the counter ready for the next call
+}
+
+// ----------------------------------------------------------------------------
+// Test export: exact int32 q.k dots of every cached token, computed with the
+// decode kernel's query quantization and row-dot routines.
+template <int GC>
+__global__ void __launch_bounds__(256) qk_debug_kernel(DecodeArgs a, int32_t *dots,
+                                                       int8_t *q_codes, float *q_scales) {
+    __shared__ __align__(16) int8_t ks[kBlock * kHeadDim];
+    __shared__ __align__(16) uint32_t q_s[GC * 32];
+    __shared__ float coef[GC];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int blk = blockIdx.x;
+    const int prob = blockIdx.y;
+    const int sub = prob % a.subgroups;
+    const int bg = prob / a.subgroups;
+    const int b = bg / a.Hkv, g = bg % a.Hkv;
+    const int h0 = g * a.G + sub * GC;
+    load_query<KVD_INT8, GC>(a, b, h0, warp, lane, q_s, coef, blk == 0 ? q_codes : nullptr,
+                             q_scales);
+    const int8_t *src = static_cast<const int8_t *>(a.k) +
+                        (static_cast<size_t>(bg) * a.max_seq + static_cast<size_t>(blk) * kBlock) *
+                            kHeadDim;
+    for (int i = tid; i < kBlock * kHeadDim / 16; i += 256)
+        reinterpret_cast<uint4 *>(ks)[i] = reinterpret_cast<const uint4 *>(src)[i];
+    __syncthreads();
+    QRegsI8<GC> qr;
+    const int t = lane >> 2, c = lane & 3;
+    load_qregs_i8<GC>(q_s, t, c, qr);
+    const int tok = 8 * warp + t;
+    const int dot = qk_int8_row<GC>(ks + tok * kHeadDim, qr, t, c);
+    const int hq = (c * GC) >> 2;
+    const int pos = blk * kBlock + tok;
+    if ((c % (4 / GC)) == 0 && pos < a.len)
+        dots[(static_cast<size_t>(b) * a.H + h0 + hq) * a.len + pos] = dot;
+}
+
+template <int DT, int GC, bool DENSE>
+cudaError_t launch_decode_t(const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
+    using SL = SmemLayout<DT, GC>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SL::kTotal);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch_ex(decode_kernel<DT, GC, DENSE>, dim3(a.splits, P_sub), dim3(kThreads),
+                     SL::kTotal, st, pdl, a);
+}
+
+template <int DT, bool DENSE>
+cudaError_t launch_decode_gc(int gc, const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
+    switch (gc) {
+        case 1: return launch_decode_t<DT, 1, DENSE>(a, P_sub, st, pdl);
+        case 2: return launch_decode_t<DT, 2, DENSE>(a, P_sub, st, pdl);
+        default: return launch_decode_t<DT, 4, DENSE>(a, P_sub, st, pdl);
+    }
+}
+
+}  // namespace
+
+DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count) {
+    DecodePlan p;
+    p.heads_per_cta = g.G < 4 ? g.G : 4;
+    p.subgroups = g.G / p.heads_per_cta;
+    const long P = static_cast<long>(g.B) * g.Hkv * p.subgroups;
+    const long target = static_cast<long>(sm_count) * 2;  // two CTAs per SM
+    long s = P >= target ? 1 : target / P;
+    const long by_work = (static_cast<long>(max_blocks) + 3) / 4;  // >= 4 blocks per split
+    if (s > by_work) s = by_work;
+    if (s < 1) s = 1;
+    if (s > 256) s = 256;
+    p.splits = static_cast<int>(s);
+    return p;
+}
+
+size_t decode_partials_bytes(const Geom &g, const DecodePlan &p) {
+    if (p.splits <= 1) return 0;
+    return static_cast<size_t>(g.B) * g.Hkv * p.subgroups * p.splits * p.heads_per_cta *
+           kPartStride * sizeof(float);
+}
+
+cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p,
+                          const float *q, float scale, const int32_t *sel_idx,
+                          const int32_t *sel_cnt, float *out, float *partials,
+                          uint32_t *counters, cudaStream_t st, bool pdl) {
+    DecodeArgs a;
+    a.k = c.k;
+    a.v = c.v;
+    a.k_scale = c.k_scale;
+    a.v_scale = c.v_scale;
+    a.q = q;
+    a.out = out;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.partials = partials;
+    a.counters = counters;
+    a.dev_status = c.dev_status;
+    a.Hkv = g.Hkv;
+    a.H = g.H;
+    a.G = g.G;
+    a.max_seq = g.max_seq;
+    a.nbmax = g.nbmax;
+    a.len = g.len;
+    a.NB = g.NB;
+    a.splits = p.splits;
+    a.subgroups = p.subgroups;
+    a.scale_log2 = scale * kLog2e;
+    const int P_sub = g.B * g.Hkv * p.subgroups;
+    const bool dense = sel_idx == nullptr;
+    if (g.dtype == KVD_INT8)
+        return dense ? launch_decode_gc<KVD_INT8, true>(p.heads_per_cta, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_INT8, false>(p.heads_per_cta, a, P_sub, st, pdl);
+    return dense ? launch_decode_gc<KVD_F16, true>(p.heads_per_cta, a, P_sub, st, pdl)
+                 : launch_decode_gc<KVD_F16, false>(p.heads_per_cta, a, P_sub, st, pdl);
+}
+
+cudaError_t launch_qk_debug(const kvd_cache &c, const Geom &g, const float *q, int32_t *dots,
+                            int8_t *q_codes, float *q_scales, cudaStream_t st) {
+    DecodeArgs a = {};
+    a.k = c.k;
+    a.q = q;
+    a.Hkv = g.Hkv;
+    a.H = g.H;
+    a.G = g.G;
+    a.max_seq = g.max_seq;
+    a.nbmax = g.nbmax;
+    a.len = g.len;
+    a.NB = g.NB;
+    a.scale_log2 = 1.0f;
+    const int gc = g.G < 4 ? g.G : 4;
+    a.subgroups = g.G / gc;
+    dim3 grid(g.NB, g.B * g.Hkv * a.subgroups);
+    switch (gc) {
+        case 1: qk_debug_kernel<1><<<grid, 256, 0, st>>>(a, dots, q_codes, q_scales); break;
+        case 2: qk_debug_kernel<2><<<grid, 256, 0, st>>>(a, dots, q_codes, q_scales); break;
+        default: qk_debug_kernel<4><<<grid, 256, 0, st>>>(a, dots, q_codes, q_scales); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kvd

@@ -1,0 +1,70 @@
+// internal.h -- launchers shared between the kernel translation units and the
+// C-ABI front end (api.cu).  Arguments are already validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "kvdecode.h"
+
+namespace kvd {
+
+// Geometry shared by the launchers (all sizes validated).
+struct Geom {
+    int dtype, B, Hkv, max_seq, len;  // len = tokens to read / after append
+    int H, G;                         // query heads, group size
+    int NB;                           // ceil(len / 64)
+    int nbmax;                        // max_seq / 64
+};
+
+// Decode split plan: grid = (splits, B * Hkv * subgroups).
+struct DecodePlan {
+    int heads_per_cta;  // query heads handled by one CTA (<= 4)
+    int subgroups;      // G / heads_per_cta
+    int splits;         // CTAs per (sequence, KV head, subgroup)
+};
+
+DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count);
+size_t decode_partials_bytes(const Geom &g, const DecodePlan &p);
+int device_sm_count();
+
+cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_new, int n_new,
+                          cudaStream_t st, bool pdl);
+
+cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int k_sel,
+                          int sink_tokens, int recent_tokens, int32_t *sel_idx,
+                          int32_t *sel_cnt, uint32_t *keys, cudaStream_t st, bool pdl);
+
+cudaError_t launch_scores_debug(const kvd_cache &c, const Geom &g, const float *q, float *ub,
+                                cudaStream_t st);
+
+cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p,
+                          const float *q, float scale, const int32_t *sel_idx,
+                          const int32_t *sel_cnt, float *out, float *partials,
+                          uint32_t *counters, cudaStream_t st, bool pdl);
+
+cudaError_t launch_qk_debug(const kvd_cache &c, const Geom &g, const float *q, int32_t *dots,
+                            int8_t *q_codes, float *q_scales, cudaStream_t st);
+
+// Launch helper: cudaLaunchKernelEx with optional programmatic stream
+// serialization (the kernel must call pdl_wait() before reading upstream data).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t st, bool pdl, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace kvd

@@ -1,0 +1,181 @@
+"""The C ABI library loads and rejects bad arguments on the host (no GPU).
+
+Every call below fails validation, so nothing reaches the CUDA runtime; a
+call that passed validation on a machine without a GPU would return
+KVD_ERR_CUDA, which these tests would flag.
+"""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import long_context_decode_kv_gb300 as kvd
+from long_context_decode_kv_gb300 import CacheStruct
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvdecode.h")
+
+OK, INVALID, UNSUPPORTED, CAPACITY, CUDA, TIMEOUT, WORKSPACE = range(7)
+FAKE = 0x7f0000000000  # aligned, never dereferenced on the host
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from long_context_decode_kv_gb300 import build
+    build.build()
+
+
+def _cache(dtype=kvd.INT8, B=1, Hkv=8, D=128, max_seq=4096, blk=64, length=1000, **kw):
+    s = CacheStruct(dtype, B, Hkv, D, max_seq, blk, length, 0, FAKE, FAKE + 0x100000,
+                    FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x400000, FAKE + 0x500000, None)
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+def test_header_symbols_exported():
+    decl = re.findall(r"^KVD_API\s+[\w\s\*]+?\b(kvd_\w+)\s*\(", open(HEADER).read(), re.M)
+    assert len(decl) >= 12
+    L = C.CDLL(kvd.LIB_PATH)
+    for name in decl:
+        assert hasattr(L, name), name
+    assert set(decl) == set(kvd.EXPORTS)
+
+
+def test_abi_version_and_status_strings():
+    v = int(re.search(r"#define KVD_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert kvd.lib().kvd_abi_version() == v
+    for code in range(7):
+        assert kvd.status_string(code) and kvd.status_string(code) != "unknown status"
+    assert kvd.status_string(99) == "unknown status"
+
+
+def test_selected_count_matches_oracle_rule():
+    import oracle
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        L = int(rng.integers(1, 5000))
+        k = int(rng.integers(0, 100))
+        sink = int(rng.integers(0, 300))
+        rec = int(rng.integers(0, 300))
+        nb = (L + 63) // 64
+        sel, _ = oracle.select(L, 64, np.zeros(nb), k, sink, rec)
+        assert kvd.selected_count(L, k, sink, rec) == len(sel)
+    assert kvd.selected_count(0, 1, 0, 0) == -1
+    assert kvd.selected_count(10, -1, 0, 0) == -1
+    assert kvd.selected_count(10, 1, 0, 0, block=32) == -1
+
+
+def _ws(s, n_heads=32):
+    return int(kvd.lib().kvd_workspace_bytes(C.byref(s), n_heads))
+
+
+def test_workspace_bytes():
+    s = _cache()
+    n = _ws(s)
+    assert n > 0 and n % 256 == 0
+    assert _ws(_cache(max_seq=8192)) > n           # grows with capacity
+    assert _ws(s, 33) == 0                          # 33 % 8 != 0
+    assert _ws(_cache(D=64)) == 0
+    assert _ws(_cache(dtype=7)) == 0
+
+
+def _select(s, n_heads=32, k_sel=4, sink=4, recent=64, ws_bytes=None, q=FAKE, ws=FAKE):
+    ws_bytes = _ws(_cache()) if ws_bytes is None else ws_bytes
+    return kvd.lib().kvd_select_blocks(C.byref(s), q, n_heads, k_sel, sink, recent, FAKE, FAKE,
+                                       ws, ws_bytes, None)
+
+
+def test_select_validation():
+    assert _select(_cache(D=64)) == UNSUPPORTED
+    assert _select(_cache(blk=32)) == UNSUPPORTED
+    assert _select(_cache(), n_heads=12) == INVALID
+    assert _select(_cache(), n_heads=24) == UNSUPPORTED      # group of 3
+    assert _select(_cache(length=0)) == INVALID
+    assert _select(_cache(), k_sel=-1) == INVALID
+    assert _select(_cache(), sink=-1) == INVALID
+    assert _select(_cache(), recent=-1) == INVALID
+    assert _select(_cache(), q=FAKE + 4) == INVALID          # misaligned q
+    assert _select(_cache(), q=None) == INVALID
+    assert _select(_cache(), ws_bytes=16) == WORKSPACE
+    assert _select(_cache(), ws=FAKE + 8) == WORKSPACE
+    assert _select(_cache(), ws=None) == WORKSPACE
+    assert _select(_cache(k=FAKE + 2)) == INVALID
+    assert _select(_cache(kmin=None)) == INVALID
+    assert _select(_cache(k_scale=None)) == INVALID
+    assert _select(_cache(max_seq=100)) == INVALID           # not a multiple of 64
+    assert _select(_cache(length=5000)) == INVALID           # len > max_seq
+    assert _select(_cache(reserved=1)) == INVALID
+    big = _cache(max_seq=64 * 49153, length=64 * 49153)
+    assert _select(big, ws_bytes=_ws(big)) == UNSUPPORTED     # too many blocks to select
+
+
+def test_decode_validation():
+    L = kvd.lib()
+    s = _cache()
+    n = _ws(s)
+    assert L.kvd_decode_attn(C.byref(_cache(length=0)), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE,
+                             FAKE, n, None) == INVALID
+    assert L.kvd_decode_attn(C.byref(s), FAKE, 32, 0.1, None, FAKE, 10, FAKE, FAKE, n,
+                             None) == INVALID
+    assert L.kvd_decode_attn(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, -1, FAKE, FAKE, n,
+                             None) == INVALID
+    assert L.kvd_decode_attn(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE + 4, FAKE, n,
+                             None) == INVALID
+    assert L.kvd_decode_attn(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, FAKE, n - 256,
+                             None) == WORKSPACE
+    assert L.kvd_decode_attn_dense(C.byref(s), FAKE, 30, 0.1, FAKE, FAKE, n, None) == INVALID
+    assert L.kvd_decode_attn_dense(C.byref(_cache(head_dim=256)), FAKE, 32, 0.1, FAKE, FAKE, n,
+                                   None) == UNSUPPORTED
+    assert L.kvd_decode_attn_dense(C.byref(s), FAKE, 32, 0.1, FAKE, None, n, None) == WORKSPACE
+
+
+def test_append_validation():
+    L = kvd.lib()
+    s = _cache(length=4090)
+    assert L.kvd_kv_append(C.byref(s), FAKE, FAKE, 7, None) == CAPACITY
+    assert s.len == 4090
+    assert L.kvd_kv_append(C.byref(s), FAKE, FAKE, -1, None) == INVALID
+    assert L.kvd_kv_append(C.byref(s), FAKE, FAKE, 0, None) == OK      # no-op, no launch
+    assert s.len == 4090
+    assert L.kvd_kv_append(C.byref(s), FAKE + 2, FAKE, 1, None) == INVALID
+    assert L.kvd_kv_append(C.byref(s), None, FAKE, 1, None) == INVALID
+    assert L.kvd_kv_append(C.byref(_cache(dtype=3)), FAKE, FAKE, 1, None) == INVALID
+    assert L.kvd_kv_append(C.byref(None if False else _cache(n_kv_heads=0)), FAKE, FAKE, 1,
+                           None) == INVALID
+
+
+def test_step_validation():
+    L = kvd.lib()
+    s = _cache(length=4096)
+    n = _ws(s)
+    assert L.kvd_decode_step(C.byref(s), FAKE, FAKE, FAKE, 32, 0.1, 4, 4, 64, None, None, FAKE,
+                             FAKE, n, None) == CAPACITY
+    s = _cache()
+    assert L.kvd_decode_step(C.byref(s), FAKE, FAKE, FAKE, 32, 0.1, 4, -4, 64, None, None, FAKE,
+                             FAKE, n, None) == INVALID
+    assert L.kvd_decode_step(C.byref(s), FAKE, FAKE, FAKE, 32, 0.1, 4, 4, 64, None, None, FAKE,
+                             FAKE, 64, None) == WORKSPACE
+    assert s.len == 1000
+    assert L.kvd_decode_step_host(C.byref(s), None, FAKE, FAKE, 32, 0.1, 4, 4, 64, None, None,
+                                  FAKE, FAKE, n, None) == INVALID
+
+
+def test_debug_validation():
+    L = kvd.lib()
+    assert L.kvd_debug_qk_int8(C.byref(_cache(dtype=kvd.F16)), FAKE, 32, FAKE, FAKE, FAKE,
+                               None) == INVALID
+    assert L.kvd_debug_scores(C.byref(_cache(length=0)), FAKE, 32, FAKE, None) == INVALID
+    assert L.kvd_debug_scores(C.byref(_cache()), FAKE, 32, None, None) == INVALID
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import importlib
+    mod = importlib.reload(kvd)
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(ImportError):
+        mod.lib()
+    importlib.reload(kvd)

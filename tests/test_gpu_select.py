@@ -1,0 +1,125 @@
+"""GPU Quest bounds and block selection vs the oracle.
+
+Bar: bounds within f32 rounding of the fp64 bound; selected sets identical
+except inside the tie window around the K-th bound (see gpu_util).
+"""
+import numpy as np
+import pytest
+import torch
+
+import long_context_decode_kv_gb300 as kvd
+import oracle
+from gpu_util import check_selection, dev, make_pair, oracle_scores, seeded
+
+pytestmark = pytest.mark.gpu
+
+
+def _q(B, H, seed, scale=1.0):
+    return seeded((B, H, 128), seed, scale=scale, dtype=torch.float32)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8])
+def test_scores_match_oracle(G, dtype):
+    B, Hkv, L = 2, 2, 1000
+    k = seeded((B, L, Hkv, 128), 31) + 0.5
+    v = seeded((B, L, Hkv, 128), 32)
+    gc, oc = make_pair(dtype, k, v)
+    q = _q(B, Hkv * G, 33)
+    nb = (L + 63) // 64
+    ub = torch.empty(B, Hkv, nb, device=dev())
+    kvd.debug_scores(gc, q, ub)
+    torch.cuda.synchronize()
+    qn = q.cpu().numpy()
+    for b in range(B):
+        for g in range(Hkv):
+            want, _, mag = oracle_scores(oc, qn, b, g, G, L)
+            got = ub[b, g].cpu().double().numpy()
+            assert np.all(np.abs(got - want) <= 4e-6 * np.maximum(np.abs(want), mag) + 1e-30)
+
+
+CASES = [
+    # L, k_sel, sink, recent
+    (512, 4, 4, 64),
+    (512, 0, 4, 64),
+    (512, 6, 4, 64),
+    (512, 100, 0, 0),
+    (500, 2, 65, 1),
+    (1, 3, 0, 0),
+    (130, 1, 0, 0),
+    (5000, 17, 4, 256),
+    (5000, 60, 0, 1),
+    (20000, 77, 128, 640),
+]
+
+
+@pytest.mark.parametrize("L,k_sel,sink,recent", CASES)
+@pytest.mark.parametrize("G", [1, 4])
+def test_select_matches_oracle(L, k_sel, sink, recent, G):
+    B, Hkv = 2, 2
+    k = seeded((B, L, Hkv, 128), 41 + L)
+    v = seeded((B, L, Hkv, 128), 42)
+    gc, oc = make_pair(kvd.F16, k, v)
+    q = _q(B, Hkv * G, 43)
+    ws = kvd.make_workspace(gc, Hkv * G)
+    sel_idx = torch.full((B, Hkv, gc.max_seq // 64), -7, dtype=torch.int32, device=dev())
+    sel_cnt = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev())
+    kvd.select_blocks(gc, q, k_sel, sink, recent, sel_idx, sel_cnt, ws)
+    torch.cuda.synchronize()
+    check_selection(sel_idx, sel_cnt, oc, q.cpu().numpy(), k_sel, sink, recent, G)
+    assert np.all(sel_cnt.cpu().numpy() == kvd.selected_count(L, k_sel, sink, recent))
+
+
+def test_exact_ties_go_to_lower_index():
+    # every block identical => every bound equal (bit-identical f32 sums):
+    # the top-K must be the lowest-index candidates
+    B, Hkv, L, G = 1, 2, 64 * 40, 4
+    row = seeded((1, 64, Hkv, 128), 5)
+    k = row.repeat(1, 40, 1, 1).contiguous()
+    v = seeded((B, L, Hkv, 128), 6)
+    gc, oc = make_pair(kvd.F16, k, v)
+    q = _q(B, Hkv * G, 7)
+    ws = kvd.make_workspace(gc, Hkv * G)
+    sel_idx = torch.zeros((B, Hkv, gc.max_seq // 64), dtype=torch.int32, device=dev())
+    sel_cnt = torch.zeros((B, Hkv), dtype=torch.int32, device=dev())
+    kvd.select_blocks(gc, q, 5, 1, 64, sel_idx, sel_cnt, ws)
+    torch.cuda.synchronize()
+    for g in range(Hkv):
+        assert sel_idx[0, g, :sel_cnt[0, g]].cpu().tolist() == [0, 1, 2, 3, 4, 5, 39]
+
+
+def test_needle_blocks_survive_selection():
+    # retrieval gate of the Quest page: every planted needle's block has to be
+    # among the selected ones (needle keys lie along the group's query direction)
+    from long_context_decode_kv_gb300 import synth
+    w = synth.QWEN3_32K.with_(L=8192, k_sel=32)
+    q, k, v, needles = synth.make_workload(w, device=dev())
+    gc = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev())
+    kvd.kv_append(gc, k, v)
+    ws = kvd.make_workspace(gc, w.H)
+    sel_idx = torch.zeros((w.B, w.Hkv, gc.max_seq // 64), dtype=torch.int32, device=dev())
+    sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev())
+    kvd.select_blocks(gc, q, w.k_sel, w.sink_tokens, w.recent_tokens, sel_idx, sel_cnt, ws)
+    torch.cuda.synchronize()
+    for g in range(w.Hkv):
+        sel = set(sel_idx[0, g, :sel_cnt[0, g]].cpu().tolist())
+        for p in needles[0, g].cpu().tolist():
+            assert p // 64 in sel
+
+
+def test_select_repeatable_and_workspace_reuse():
+    B, Hkv, L, G = 3, 2, 3000, 4
+    k = seeded((B, L, Hkv, 128), 51)
+    gc, oc = make_pair(kvd.INT8, k, k)
+    q = _q(B, Hkv * G, 52)
+    ws = kvd.make_workspace(gc, Hkv * G)
+    outs = []
+    for _ in range(3):
+        sel_idx = torch.zeros((B, Hkv, gc.max_seq // 64), dtype=torch.int32, device=dev())
+        sel_cnt = torch.zeros((B, Hkv), dtype=torch.int32, device=dev())
+        kvd.select_blocks(gc, q, 9, 4, 64, sel_idx, sel_cnt, ws)
+        outs.append((sel_idx.clone(), sel_cnt.clone()))
+    torch.cuda.synchronize()
+    for a, b in outs[1:]:
+        assert torch.equal(a, outs[0][0]) and torch.equal(b, outs[0][1])
+    check_selection(outs[0][0], outs[0][1], oc, q.cpu().numpy(), 9, 4, 64, G)

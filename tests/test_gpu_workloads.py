@@ -1,0 +1,171 @@
+"""The decode workloads at full size, run the way the benchmark runs them
+(one whole decode step through the C ABI: append the step's token, select,
+attend), checked against the oracle on sampled (sequence, KV head) problems
+and, for the small ones, everywhere.
+
+Per sampled problem: cache rows (codes, scales) of the needles, of random
+positions and of the step's token bit-exact; every block bound equal; the
+selection identical up to the tie window; the G query heads' outputs within
+the stated tolerance and within 1e-4.  Every planted needle's block must be
+selected (all problems).
+"""
+import numpy as np
+import pytest
+import torch
+
+import long_context_decode_kv_gb300 as kvd
+import oracle
+from long_context_decode_kv_gb300 import synth
+from gpu_util import TOL, assert_outputs, check_selection, dev, rel_l2_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _build(w):
+    q, k, v, needles = synth.make_workload(w, device=dev())
+    gc = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev())
+    kvd.kv_append(gc, k, v)
+    return q, k, v, needles, gc
+
+
+def _oracle_problem(w, k, v, b, g, kn, vn):
+    oc = oracle.OracleCache(w.dtype, 1, 1, w.D, w.L + 64, 64)
+    oc.append(k[b:b + 1, :, g:g + 1].contiguous().cpu().numpy(),
+              v[b:b + 1, :, g:g + 1].contiguous().cpu().numpy())
+    oc.append(kn[b:b + 1, :, g:g + 1].cpu().numpy(), vn[b:b + 1, :, g:g + 1].cpu().numpy())
+    return oc
+
+
+def _check_rows(gc, oc, b, g, rows):
+    rows = np.asarray(sorted(set(int(r) for r in rows)))
+    if gc.dtype == kvd.INT8:
+        assert np.array_equal(gc.k[b, g, rows].cpu().numpy(), oc.K[0, 0, rows])
+        assert np.array_equal(gc.v[b, g, rows].cpu().numpy(), oc.V[0, 0, rows])
+        assert np.array_equal(gc.k_scale[b, g, rows].cpu().numpy().view(np.uint32),
+                              oc.ks[0, 0, rows].view(np.uint32))
+        assert np.array_equal(gc.v_scale[b, g, rows].cpu().numpy().view(np.uint32),
+                              oc.vs[0, 0, rows].view(np.uint32))
+    else:
+        assert np.array_equal(gc.k[b, g, rows].cpu().view(torch.int16).numpy(),
+                              oc.K[0, 0, rows].view(np.int16))
+    nb = (oc.len + 63) // 64
+    assert np.array_equal(gc.kmin[b, g, :nb].cpu().float().numpy(),
+                          oc.kmin[0, 0, :nb].astype(np.float32))
+    assert np.array_equal(gc.kmax[b, g, :nb].cpu().float().numpy(),
+                          oc.kmax[0, 0, :nb].astype(np.float32))
+
+
+def _run(w, samples, dense_too=False):
+    q, k, v, needles, gc = _build(w)
+    kn, vn = synth.make_step_token(w, 0, device=dev())
+    ws = kvd.make_workspace(gc, w.H)
+    nbmax = gc.max_seq // 64
+    sel_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev())
+    sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev())
+    out = torch.empty(w.B, w.H, w.D, device=dev())
+    kvd.decode_step(gc, q, kn, vn, w.scale, w.k_sel, w.sink_tokens, w.recent_tokens, out, ws,
+                    sel_idx=sel_idx, sel_cnt=sel_cnt)
+    dense = None
+    if dense_too:
+        dense = torch.empty_like(out)
+        kvd.decode_attn_dense(gc, q, w.scale, dense, ws)
+    torch.cuda.synchronize()
+    assert gc.device_status() == 0
+    L1 = w.L + 1
+    assert torch.all(sel_cnt == kvd.selected_count(L1, w.k_sel, w.sink_tokens, w.recent_tokens))
+    # needle recall, every problem
+    idx, cnt = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            sel = set(idx[b, g, :cnt[b, g]].tolist())
+            for p in needles[b, g].cpu().tolist():
+                assert p // 64 in sel, (b, g, p)
+    rng = np.random.default_rng(w.seed)
+    qn = q.cpu().numpy()
+    G = w.G
+    worst = 0.0
+    for b, g in samples:
+        oc = _oracle_problem(w, k, v, b, g, kn, vn)
+        rows = list(needles[b, g].cpu().numpy()) + list(rng.integers(0, w.L, 64)) + [w.L]
+        _check_rows(gc, oc, b, g, rows)
+        qg = qn[b:b + 1, g * G:(g + 1) * G]
+        check_selection(sel_idx[b:b + 1, g:g + 1], sel_cnt[b:b + 1, g:g + 1], oc, qg,
+                        w.k_sel, w.sink_tokens, w.recent_tokens, G)
+        ref, o_idx, o_cnt = oc.decode(qg, w.scale, k_sel=w.k_sel, sink_tokens=w.sink_tokens,
+                                      recent_tokens=w.recent_tokens)
+        if set(o_idx[0, 0, :o_cnt[0, 0]]) == set(idx[b, g, :cnt[b, g]]):
+            worst = max(worst, assert_outputs(out[b, g * G:(g + 1) * G], ref[0], w.dtype,
+                                              f"{w.name} b{b} g{g}"))
+        if dense is not None:
+            dref, _, _ = oc.decode(qg, w.scale, dense=True)
+            assert_outputs(dense[b, g * G:(g + 1) * G], dref[0], w.dtype,
+                           f"{w.name} dense b{b} g{g}")
+    return worst
+
+
+def test_tiny_512_f16_everywhere():
+    w = synth.TINY
+    q, k, v, _, gc = _build(w)
+    oc = oracle.OracleCache(w.dtype, w.B, w.Hkv, w.D, w.L + 64, 64)
+    oc.append(k.cpu().numpy(), v.cpu().numpy())
+    ws = kvd.make_workspace(gc, w.H)
+    nbmax = gc.max_seq // 64
+    for k_sel in (w.k_sel, 10 ** 6):
+        sel_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev())
+        sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev())
+        kvd.select_blocks(gc, q, k_sel, w.sink_tokens, w.recent_tokens, sel_idx, sel_cnt, ws)
+        out = torch.empty(w.B, w.H, w.D, device=dev())
+        kvd.decode_attn(gc, q, w.scale, sel_idx, sel_cnt, w.NB, out, ws)
+        torch.cuda.synchronize()
+        check_selection(sel_idx, sel_cnt, oc, q.cpu().numpy(), k_sel, w.sink_tokens,
+                        w.recent_tokens, w.G)
+        ref, _, cnt = oc.decode(q.cpu().numpy(), w.scale, k_sel=k_sel,
+                                sink_tokens=w.sink_tokens, recent_tokens=w.recent_tokens)
+        assert int(cnt[0, 0]) == (6 if k_sel == w.k_sel else 8)
+        assert_outputs(out, ref, w.dtype, f"tiny k_sel={k_sel}")
+    dense = torch.empty(w.B, w.H, w.D, device=dev())
+    kvd.decode_attn_dense(gc, q, w.scale, dense, ws)
+    torch.cuda.synchronize()
+    ref, _, _ = oc.decode(q.cpu().numpy(), w.scale, dense=True)
+    assert_outputs(dense, ref, w.dtype, "tiny dense")
+
+
+@pytest.mark.parametrize("w", synth.INT8_DENSE, ids=lambda w: w.name)
+def test_int8_dense_everywhere(w):
+    q, k, v, _, gc = _build(w)
+    oc = oracle.OracleCache(w.dtype, w.B, w.Hkv, w.D, w.L + 64, 64)
+    oc.append(k.cpu().numpy(), v.cpu().numpy())
+    ws = kvd.make_workspace(gc, w.H)
+    out = torch.empty(w.B, w.H, w.D, device=dev())
+    kvd.decode_attn_dense(gc, q, w.scale, out, ws)
+    torch.cuda.synchronize()
+    # codes and scales of the whole cache
+    assert np.array_equal(gc.k[:, :, :w.L].cpu().numpy(), oc.K[:, :, :w.L])
+    assert np.array_equal(gc.v_scale[:, :, :w.L].cpu().numpy().view(np.uint32),
+                          oc.vs[:, :, :w.L].view(np.uint32))
+    ref, _, _ = oc.decode(q.cpu().numpy(), w.scale, dense=True)
+    assert_outputs(out, ref, w.dtype, w.name)
+    # cpu-attn "Correctness": against fp32 attention with the unquantized query on
+    # the dequantized cache (query rounding included): median of the heads
+    errs = []
+    qn = q.cpu().numpy()
+    for h in range(w.H):
+        f = oracle.attend_dequant(qn[0, h], oc.K[0, h], oc.V[0, h], oc.ks[0, h], oc.vs[0, h],
+                                  w.L, 64, w.scale)
+        errs.append(rel_l2_rows(out[0, h:h + 1], f[None])[0])
+    assert np.median(errs) < TOL[kvd.INT8]
+
+
+def test_qwen3_gqa_32k_f16_every_problem():
+    w = synth.QWEN3_32K
+    _run(w, [(0, g) for g in range(w.Hkv)], dense_too=True)
+
+
+def test_ctx128k_batch8_int8_sampled():
+    w = synth.CTX128K_B8
+    _run(w, [(0, 0), (3, 5), (7, 7)], dense_too=True)
+
+
+def test_ctx1m_int8_sampled():
+    w = synth.CTX1M
+    _run(w, [(0, 0), (0, 6)], dense_too=True)
