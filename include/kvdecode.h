@@ -67,10 +67,12 @@ typedef enum { KVD_F16 = 0, KVD_INT8 = 1 } kvd_kv_dtype;
  *   k, v        [batch, n_kv_heads, max_seq, head_dim]   f16 or int8 codes
  *   k_scale,    [batch, n_kv_heads, max_seq]              f32, int8 only
  *   v_scale                                               (NULL for f16)
- *   kmin, kmax  [batch, n_kv_heads, max_seq / block, head_dim]  f16
- * kmin/kmax is the per-(KV head, block) channel-wise key envelope [QUEST
- * Method: "Store kmin[head_dim], kmax[head_dim] per block"], always taken
- * from the f16 keys before quantization [QUEST All-KV-types composition].
+ *   kbounds     [batch, n_kv_heads, max_seq / block, head_dim, 2]  f16
+ * kbounds holds the per-(KV head, block) channel-wise key envelope [QUEST
+ * Method: "Store kmin[head_dim], kmax[head_dim] per block"] as interleaved
+ * pairs: kbounds[..., d, 0] = kmin[d], kbounds[..., d, 1] = kmax[d] (one
+ * contiguous 512-byte row per block).  It is always taken from the f16 keys
+ * before quantization [QUEST All-KV-types composition].
  * int8 rows hold per-token per-head absmax codes [CPUATT Method]: scale =
  * absmax/127 (f32), code = round-half-even(x / scale) clamped to +-127, and
  * a row whose scale is 0 holds zero codes.
@@ -94,8 +96,7 @@ typedef struct kvd_cache {
     void *v;
     float *k_scale;
     float *v_scale;
-    void *kmin;
-    void *kmax;
+    void *kbounds;
     int32_t *dev_status;
 } kvd_cache;
 

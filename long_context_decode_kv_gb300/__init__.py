@@ -50,8 +50,7 @@ class CacheStruct(C.Structure):
                 ("head_dim", C.c_int32), ("max_seq", C.c_int32), ("block", C.c_int32),
                 ("len", C.c_int32), ("reserved", C.c_int32),
                 ("k", C.c_void_p), ("v", C.c_void_p), ("k_scale", C.c_void_p),
-                ("v_scale", C.c_void_p), ("kmin", C.c_void_p), ("kmax", C.c_void_p),
-                ("dev_status", C.c_void_p)]
+                ("v_scale", C.c_void_p), ("kbounds", C.c_void_p), ("dev_status", C.c_void_p)]
 
 
 _lib = None
@@ -112,7 +111,7 @@ class KVCache:
 
     k, v      [B, Hkv, max_seq, 128]  float16 or int8
     k_scale   [B, Hkv, max_seq]       float32 (int8 only)
-    kmin/kmax [B, Hkv, max_seq // 64, 128] float16
+    kbounds   [B, Hkv, max_seq // 64, 128, 2] float16: (kmin, kmax) per channel
     status    [1] int32 device word for device-side faults
     """
 
@@ -130,10 +129,8 @@ class KVCache:
             self.t = {
                 "k": torch.empty(batch, n_kv_heads, max_seq, head_dim, dtype=kvt, device=dev),
                 "v": torch.empty(batch, n_kv_heads, max_seq, head_dim, dtype=kvt, device=dev),
-                "kmin": torch.empty(batch, n_kv_heads, nb, head_dim, dtype=torch.float16,
-                                    device=dev),
-                "kmax": torch.empty(batch, n_kv_heads, nb, head_dim, dtype=torch.float16,
-                                    device=dev),
+                "kbounds": torch.empty(batch, n_kv_heads, nb, head_dim, 2, dtype=torch.float16,
+                                       device=dev),
                 "status": torch.zeros(1, dtype=torch.int32, device=dev),
             }
             if dtype == INT8:
@@ -144,8 +141,17 @@ class KVCache:
         self.s = CacheStruct(dtype, batch, n_kv_heads, head_dim, max_seq, block, 0, 0,
                              _ptr(self.t["k"]), _ptr(self.t["v"]),
                              _ptr(self.t.get("k_scale")), _ptr(self.t.get("v_scale")),
-                             _ptr(self.t["kmin"]), _ptr(self.t["kmax"]),
-                             _ptr(self.t.get("status")))
+                             _ptr(self.t["kbounds"]), _ptr(self.t.get("status")))
+
+    @property
+    def kmin(self) -> torch.Tensor:
+        """View [B, Hkv, max_seq // 64, 128] of the per-block channel minima."""
+        return self.t["kbounds"][..., 0]
+
+    @property
+    def kmax(self) -> torch.Tensor:
+        """View [B, Hkv, max_seq // 64, 128] of the per-block channel maxima."""
+        return self.t["kbounds"][..., 1]
 
     @property
     def len(self) -> int:

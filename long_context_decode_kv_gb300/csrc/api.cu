@@ -46,7 +46,7 @@ kvd_status check_cache(const kvd_cache *c) {
     if (c->max_seq < kBlock || c->max_seq % kBlock != 0) return KVD_ERR_INVALID;
     if (c->len < 0 || c->len > c->max_seq) return KVD_ERR_INVALID;
     if (c->reserved != 0) return KVD_ERR_INVALID;
-    const void *ptrs[4] = {c->k, c->v, c->kmin, c->kmax};
+    const void *ptrs[3] = {c->k, c->v, c->kbounds};
     for (const void *p : ptrs)
         if (!p || !aligned(p, 16)) return KVD_ERR_INVALID;
     if (c->dtype == KVD_INT8) {
@@ -143,15 +143,15 @@ void forced_range(int len, int sink, int recent, int *se, int *rb) {
 
 kvd_status select_impl(const kvd_cache *c, const float *q, int n_heads, int k_sel, int sink,
                        int recent, int32_t *sel_idx, int32_t *sel_cnt, void *ws,
-                       const WsLayout &w, cudaStream_t st) {
+                       const WsLayout &w, cudaStream_t st, bool in_step = false) {
     const Geom g = make_geom(c, n_heads, c->len);
     return cuda_status(launch_select(*c, g, q, k_sel, sink, recent, sel_idx, sel_cnt,
-                                     ws_at<uint32_t>(ws, w.keys), st, true));
+                                     ws_at<uint32_t>(ws, w.keys), st, true, in_step));
 }
 
 kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float scale,
                        const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel, float *out,
-                       void *ws, const WsLayout &w, cudaStream_t st) {
+                       void *ws, const WsLayout &w, cudaStream_t st, bool in_step = false) {
     const Geom g = make_geom(c, n_heads, c->len);
     const bool dense = sel_idx == nullptr;
     int max_blocks = dense ? g.NB : max_sel;
@@ -160,7 +160,7 @@ kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float sc
     const DecodePlan p = plan_decode(g, max_blocks, device_sm_count());
     return cuda_status(launch_decode(*c, g, p, q, scale, sel_idx, sel_cnt, out,
                                      ws_at<float>(ws, w.partials),
-                                     ws_at<uint32_t>(ws, w.counters), st, true));
+                                     ws_at<uint32_t>(ws, w.counters), st, true, in_step));
 }
 
 kvd_status check_select_args(const kvd_cache *c, int n_heads, int k_sel, int sink, int recent) {
@@ -297,16 +297,16 @@ kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
     cache->len += 1;
     if (dense)
         return decode_impl(cache, q, n_heads, softmax_scale, nullptr, nullptr, 0, out, workspace,
-                           w, st);
+                           w, st, true);
     if (!sel_idx) sel_idx = ws_at<int32_t>(workspace, w.sel_idx);
     if (!sel_cnt) sel_cnt = ws_at<int32_t>(workspace, w.sel_cnt);
     s = select_impl(cache, q, n_heads, k_sel, sink_tokens, recent_tokens, sel_idx, sel_cnt,
-                    workspace, w, st);
+                    workspace, w, st, true);
     if (s != KVD_OK) return s;
     const int max_sel =
         kvd_selected_count(cache->len, kBlock, k_sel, sink_tokens, recent_tokens);
     return decode_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_cnt, max_sel, out,
-                       workspace, w, st);
+                       workspace, w, st, true);
 }
 
 kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host, const void *k_new_host,

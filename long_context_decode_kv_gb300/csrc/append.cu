@@ -26,15 +26,6 @@ __device__ __forceinline__ void load_half4(const __half *p, float (&x)[4]) {
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
 }
 
-__device__ __forceinline__ void store_half4(__half *p, const float (&x)[4]) {
-    __half2 a = __floats2half2_rn(x[0], x[1]);
-    __half2 b = __floats2half2_rn(x[2], x[3]);
-    uint2 w;
-    w.x = *reinterpret_cast<uint32_t *>(&a);
-    w.y = *reinterpret_cast<uint32_t *>(&b);
-    *reinterpret_cast<uint2 *>(p) = w;
-}
-
 template <int DT>
 __global__ void __launch_bounds__(32 * kAppendWarps)
 append_kernel(kvd_cache c, const __half *__restrict__ k_new, const __half *__restrict__ v_new,
@@ -85,21 +76,27 @@ append_kernel(kvd_cache c, const __half *__restrict__ k_new, const __half *__res
             }
         }
     }
+    // bounds row of the block: (kmin, kmax) pairs of channels 4*lane .. 4*lane+3
     const size_t nbmax = static_cast<size_t>(c.max_seq / kBlock);
-    const size_t bidx = ((static_cast<size_t>(b) * c.n_kv_heads + h) * nbmax + blk) * kHeadDim +
-                        4 * lane;
-    __half *kmin = static_cast<__half *>(c.kmin) + bidx;
-    __half *kmax = static_cast<__half *>(c.kmax) + bidx;
+    const size_t bidx = (((static_cast<size_t>(b) * c.n_kv_heads + h) * nbmax + blk) * kHeadDim +
+                         4 * lane) * 2;
+    __half2 *bounds = reinterpret_cast<__half2 *>(static_cast<__half *>(c.kbounds) + bidx);
     if (merge) {
-        float om[4], oM[4];
-        load_half4(kmin, om);
-        load_half4(kmax, oM);
+        const uint4 old = *reinterpret_cast<const uint4 *>(bounds);
+        const __half2 *o2 = reinterpret_cast<const __half2 *>(&old);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) { mn[j] = fminf(mn[j], om[j]); mx[j] = fmaxf(mx[j], oM[j]); }
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(o2[j]);
+            mn[j] = fminf(mn[j], f.x);
+            mx[j] = fmaxf(mx[j], f.y);
+        }
     }
     // every value is an f16 already, so the conversions back are exact
-    store_half4(kmin, mn);
-    store_half4(kmax, mx);
+    uint4 w;
+    __half2 *w2 = reinterpret_cast<__half2 *>(&w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w2[j] = __floats2half2_rn(mn[j], mx[j]);
+    *reinterpret_cast<uint4 *>(bounds) = w;
 }
 
 }  // namespace

@@ -34,17 +34,23 @@ int device_sm_count();
 cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_new, int n_new,
                           cudaStream_t st, bool pdl);
 
+// after_step_append: launched right after the one-token append of a decode
+// step (so scoring may overlap that append when the token's block is forced).
 cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int k_sel,
                           int sink_tokens, int recent_tokens, int32_t *sel_idx,
-                          int32_t *sel_cnt, uint32_t *keys, cudaStream_t st, bool pdl);
+                          int32_t *sel_cnt, uint32_t *keys, cudaStream_t st, bool pdl,
+                          bool after_step_append);
 
 cudaError_t launch_scores_debug(const kvd_cache &c, const Geom &g, const float *q, float *ub,
                                 cudaStream_t st);
 
+// early_q: the query may be read before the upstream kernels complete (true
+// only when the caller's own earlier kernels in the same chain wrote nothing
+// the query depends on, as inside kvd_decode_step).
 cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p,
                           const float *q, float scale, const int32_t *sel_idx,
                           const int32_t *sel_cnt, float *out, float *partials,
-                          uint32_t *counters, cudaStream_t st, bool pdl);
+                          uint32_t *counters, cudaStream_t st, bool pdl, bool early_q);
 
 cudaError_t launch_qk_debug(const kvd_cache &c, const Geom &g, const float *q, int32_t *dots,
                             int8_t *q_codes, float *q_scales, cudaStream_t st);

@@ -29,7 +29,7 @@ def _built():
 
 def _cache(dtype=kvd.INT8, B=1, Hkv=8, D=128, max_seq=4096, blk=64, length=1000, **kw):
     s = CacheStruct(dtype, B, Hkv, D, max_seq, blk, length, 0, FAKE, FAKE + 0x100000,
-                    FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x400000, FAKE + 0x500000, None)
+                    FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x400000, None)
     for k, v in kw.items():
         setattr(s, k, v)
     return s
@@ -103,7 +103,7 @@ def test_select_validation():
     assert _select(_cache(), ws=FAKE + 8) == WORKSPACE
     assert _select(_cache(), ws=None) == WORKSPACE
     assert _select(_cache(k=FAKE + 2)) == INVALID
-    assert _select(_cache(kmin=None)) == INVALID
+    assert _select(_cache(kbounds=None)) == INVALID
     assert _select(_cache(k_scale=None)) == INVALID
     assert _select(_cache(max_seq=100)) == INVALID           # not a multiple of 64
     assert _select(_cache(length=5000)) == INVALID           # len > max_seq

