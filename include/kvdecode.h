@@ -180,6 +180,33 @@ KVD_API kvd_status kvd_decode_attn_dense(const kvd_cache *cache, const float *q,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* kvd_decode_attn without a workspace: the paper has no counterpart; this  */
+/* is a convenience of this library.  Same arguments, arithmetic and output */
+/* as kvd_decode_attn, minus workspace/workspace_bytes.                     */
+/*   For callers that cannot allocate device memory when they decode: a    */
+/*   plugin that an engine hands only its input and output buffers, or     */
+/*   code whose device memory is owned by another allocator.  The split     */
+/*   partials and arrival counters live in one array of                     */
+/*   KVD_STATIC_SCRATCH_BYTES compiled into the library; every GPU that     */
+/*   loads the library holds that array until the process exits.  The call */
+/*   allocates nothing (no cudaMalloc/cudaFree, no library allocator).      */
+/*   The first call on a device looks up the array's device address (once  */
+/*   per device, with that device current); make that first call before    */
+/*   any stream capture.  Each call zeroes the counters on `stream` before  */
+/*   its kernel.  All calls on a device share the array: two calls that    */
+/*   may overlap on the GPU (different streams, no ordering) race and give  */
+/*   wrong outputs; order them on one stream or with events.                */
+/* Errors: as kvd_decode_attn; WORKSPACE when this call's partials and      */
+/* counters would pass KVD_STATIC_SCRATCH_BYTES (on a 152-SM GPU every      */
+/* accepted shape needs under 0.7 MiB, so WORKSPACE does not occur there).  */
+/* ---------------------------------------------------------------------- */
+#define KVD_STATIC_SCRATCH_BYTES (1u << 20)
+KVD_API kvd_status kvd_decode_attn_static(const kvd_cache *cache, const float *q,
+                                  int32_t n_heads, float softmax_scale,
+                                  const int32_t *sel_idx, const int32_t *sel_cnt,
+                                  int32_t max_sel, float *out, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* One whole decode step on device buffers: append one token per sequence */
 /* (k_new, v_new: [batch, 1, n_kv_heads, head_dim] f16), then select and   */
 /* attend over the len+1 cached tokens.  Equivalent to kvd_kv_append,      */

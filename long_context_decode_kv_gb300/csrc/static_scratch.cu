@@ -1,0 +1,117 @@
+// static_scratch.cu -- kvd_decode_attn_static: the split-KV decode of
+// kvd_decode_attn with its scratch (split partials and per-problem arrival
+// counters) held in a fixed device array inside the library, so the caller
+// passes no workspace and nothing is allocated per call.
+//
+// Why it exists: some callers cannot allocate device memory when they call
+// the decode -- a plugin inside a host engine that hands it only the input and
+// output buffers and owns every allocation itself, or code running where a
+// cudaMalloc would synchronize the device or fail because the memory pool is
+// already carved up.  They pay with a fixed KVD_STATIC_SCRATCH_BYTES on every
+// GPU that loads the library, and with one rule: calls that share the array
+// must not run at the same time on the GPU.
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvd {
+namespace {
+
+static_assert(KVD_STATIC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-byte regions");
+
+// Shared by every kvd_decode_attn_static call on a device; each GPU that
+// loads the library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_static_scratch[KVD_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void *g_scratch_addr[kMaxDevices] = {};  // device address, per device ordinal
+
+// In host code g_static_scratch names a host-side stand-in; the array's device
+// address is asked of the runtime once per device, with that device current.
+cudaError_t scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+bool aligned_to(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// The argument rules of kvd_decode_attn, minus the workspace.
+kvd_status check_args(const kvd_cache *c, const float *q, int n_heads, const int32_t *sel_idx,
+                      const int32_t *sel_cnt, int max_sel, const float *out) {
+    if (!c) return KVD_ERR_INVALID;
+    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8) return KVD_ERR_INVALID;
+    if (c->batch < 1 || c->n_kv_heads < 1) return KVD_ERR_INVALID;
+    if (c->head_dim != kHeadDim || c->block != kBlock) return KVD_ERR_UNSUPPORTED;
+    if (c->max_seq < kBlock || c->max_seq % kBlock != 0) return KVD_ERR_INVALID;
+    if (c->len < 0 || c->len > c->max_seq || c->reserved != 0) return KVD_ERR_INVALID;
+    const void *ptrs[3] = {c->k, c->v, c->kbounds};
+    for (const void *p : ptrs)
+        if (!p || !aligned_to(p, 16)) return KVD_ERR_INVALID;
+    if (c->dtype == KVD_INT8 && (!c->k_scale || !c->v_scale || !aligned_to(c->k_scale, 16) ||
+                                 !aligned_to(c->v_scale, 16)))
+        return KVD_ERR_INVALID;
+    if (c->dev_status && !aligned_to(c->dev_status, 4)) return KVD_ERR_INVALID;
+    if (static_cast<long long>(c->batch) * c->n_kv_heads * 16 > 65535) return KVD_ERR_UNSUPPORTED;
+    if (n_heads < 1 || n_heads % c->n_kv_heads != 0) return KVD_ERR_INVALID;
+    const int G = n_heads / c->n_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return KVD_ERR_UNSUPPORTED;
+    if (c->len < 1 || max_sel < 0) return KVD_ERR_INVALID;
+    if (!q || !aligned_to(q, 16) || !out || !aligned_to(out, 16)) return KVD_ERR_INVALID;
+    if (!sel_idx || !aligned_to(sel_idx, 4) || !sel_cnt || !aligned_to(sel_cnt, 4))
+        return KVD_ERR_INVALID;
+    return KVD_OK;
+}
+
+}  // namespace
+}  // namespace kvd
+
+using namespace kvd;
+
+extern "C" kvd_status kvd_decode_attn_static(const kvd_cache *cache, const float *q,
+                                             int32_t n_heads, float softmax_scale,
+                                             const int32_t *sel_idx, const int32_t *sel_cnt,
+                                             int32_t max_sel, float *out, void *stream) {
+    const kvd_status s = check_args(cache, q, n_heads, sel_idx, sel_cnt, max_sel, out);
+    if (s != KVD_OK) return s;
+
+    Geom g;
+    g.dtype = cache->dtype;
+    g.B = cache->batch;
+    g.Hkv = cache->n_kv_heads;
+    g.max_seq = cache->max_seq;
+    g.len = cache->len;
+    g.H = n_heads;
+    g.G = n_heads / cache->n_kv_heads;
+    g.NB = (cache->len + kBlock - 1) / kBlock;
+    g.nbmax = cache->max_seq / kBlock;
+    int max_blocks = max_sel < g.NB ? max_sel : g.NB;
+    if (max_blocks < 1) max_blocks = 1;
+    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count());
+    const size_t counter_bytes =
+        round256(static_cast<size_t>(g.B) * g.Hkv * p.subgroups * sizeof(uint32_t));
+    if (counter_bytes + decode_partials_bytes(g, p) > KVD_STATIC_SCRATCH_BYTES)
+        return KVD_ERR_WORKSPACE;
+
+    void *base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return KVD_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The array holds what the last call left there; the arrival counters must
+    // start at zero (the partials are written before they are read).
+    if (cudaMemsetAsync(base, 0, counter_bytes, st) != cudaSuccess) return KVD_ERR_CUDA;
+    uint32_t *counters = static_cast<uint32_t *>(base);
+    float *partials = reinterpret_cast<float *>(static_cast<unsigned char *>(base) + counter_bytes);
+    const cudaError_t e = launch_decode(*cache, g, p, q, softmax_scale, sel_idx, sel_cnt, out,
+                                        partials, counters, st, false, false);
+    return e == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
