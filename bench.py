@@ -159,14 +159,17 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x, world):
+    """Max of a host number over all ranks (NCCL: through the GPU; gloo: CPU)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -180,18 +183,32 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload):
-    """dram bytes per decode-kernel launch from the committed ncu summary,
-    valid only while the kernel sources are unchanged since the capture."""
+def measured_traffic(workload, tokens):
+    """DRAM bytes (read + write) of one decode-kernel launch, from the committed
+    ncu summary: bytes per attended token measured on a capture of this
+    workload's recipe (at the context the summary names), times the tokens this
+    launch attends.  Valid only while the kernel sources are unchanged since the
+    capture (the summary line carries their digest); None otherwise."""
     path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
     if not os.path.exists(path):
         return None
     digest = source_digest()
     for line in open(path):
         parts = line.split()
-        if len(parts) == 3 and parts[0] == workload and parts[1] == digest:
-            return float(parts[2])
+        if len(parts) == 5 and parts[0] == workload and parts[2] == digest:
+            return float(parts[3]) / float(parts[4]) * tokens
     return None
+
+
+def launches_per_step(w, L1):
+    """Kernels one sparse step launches: append, score (only when a top-K has
+    to be found among the candidates), top-K/compaction, decode."""
+    nb = (L1 + 63) // 64
+    se = min(nb, (w.sink_tokens + 63) // 64)
+    rb = max(se, max(0, L1 - w.recent_tokens) // 64) if w.recent_tokens > 0 else nb
+    n_cand = rb - se
+    keff = min(w.k_sel, n_cand)
+    return 4 if 0 < keff < n_cand else 3
 
 
 # --------------------------------------------------------------------------
@@ -226,9 +243,10 @@ def oracle_leg(w, q, k, v, steps, problem=(0, 0)):
 
 
 def run_reference(args, w):
-    world, rank, _ = dist_setup(args.gpus)
-    if rank != 0:
+    # the oracle runs on rank 0's host cores only; other ranks exit without work
+    if int(os.environ.get("RANK", "0")) != 0:
         return
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     q, k, v, _ = synth.make_workload(w, device="cuda")
     steps = max(1, args.steps)
     for _ in range(max(0, min(args.warmup, 1))):
@@ -262,8 +280,15 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--context", type=int, default=None,
+                    help="run the workload's recipe at this context instead (a multiple "
+                         "of 64; a smaller case for profiling)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
+    if args.context is not None:
+        if args.context < 64 or args.context % 64:
+            ap.error("--context must be a positive multiple of 64")
+        w = w.with_(L=args.context)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -401,7 +426,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "decode_kernel (kvd_decode_attn)", "bytes": dbytes,
-                     "us": dec_us, "traffic": measured_traffic(w.name)},
+                     "us": dec_us, "traffic": measured_traffic(w.name, tokens),
+                     "tokens_attended": tokens},
         "breakdown_us": {"append": statistics.mean(app_ms) * 1e3,
                          "select": statistics.mean(sel_ms) * 1e3, "decode": dec_us,
                          "step": us_step, "dense_step": statistics.mean(dense_ms) * 1e3},
@@ -411,7 +437,7 @@ def main():
         "needles_selected": needle_ok,
         "e2e": {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,  # append, select, decode per step
+        "gpu_launches": launches_per_step(w, L1) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,

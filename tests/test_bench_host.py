@@ -1,0 +1,79 @@
+"""Host logic of bench.py on CPU: the max-over-ranks and barrier used by the
+multi-process run (gloo, world size 2), the launch count it claims per step,
+and the reading of the committed traffic summary."""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from long_context_decode_kv_gb300 import synth  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        m = bench.max_over_ranks(10.0 + 3.5 * rank, world)
+        with open(os.path.join(out_dir, f"r{rank}"), "w") as f:
+            f.write(repr(m))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2(tmp_path):
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, str(tmp_path))) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert [float(open(tmp_path / f"r{r}").read()) for r in range(2)] == [13.5, 13.5]
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(7.25, 1) == 7.25
+
+
+@pytest.mark.parametrize("name,expect", [
+    ("ctx1m_int8", 4), ("ctx128k_b8_int8", 4), ("qwen3_4b_gqa_32k_f16", 4),
+    ("tiny_512_f16", 4), ("int8_dense_2048", 3),
+])
+def test_launches_per_step(name, expect):
+    w = synth.WORKLOADS[name]
+    assert bench.launches_per_step(w, w.L + 1) == expect
+
+
+def test_all_candidates_taken_skips_scoring():
+    w = synth.TINY.with_(k_sel=1000)
+    assert bench.launches_per_step(w, w.L + 1) == 3
+
+
+def test_traffic_scaled_per_token(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "decode_kernel_traffic.txt").write_text(
+        "# workload context digest dram_bytes tokens\n"
+        "ctx1m_int8 262144 abc 1000 10\n"
+        "ctx1m_int8 262144 old 9999 10\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_digest", lambda: "abc")
+    assert bench.measured_traffic("ctx1m_int8", 25) == 2500.0
+    assert bench.measured_traffic("ctx128k_b8_int8", 25) is None
+    monkeypatch.setattr(bench, "source_digest", lambda: "new")
+    assert bench.measured_traffic("ctx1m_int8", 25) is None
