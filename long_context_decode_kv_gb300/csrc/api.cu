@@ -81,7 +81,8 @@ Geom make_geom(const kvd_cache *c, int n_heads, int len) {
 
 // Workspace regions (byte offsets; every region 256-byte aligned).
 struct WsLayout {
-    size_t counters, partials, keys, sel_idx, sel_cnt, q, k_new, v_new, out, total;
+    size_t counters, partials, keys, sel_hist, sel_ticket, sel_idx, sel_cnt, q, k_new, v_new,
+        out, total;
     DecodePlan plan;
 };
 
@@ -96,8 +97,16 @@ WsLayout ws_layout(const kvd_cache *c, int n_heads) {
     off += align_up(P * w.plan.subgroups * sizeof(uint32_t));
     w.partials = off;
     off += align_up(decode_partials_bytes(g, w.plan));
-    w.keys = off;
-    off += align_up(P * g.nbmax * sizeof(uint32_t));
+    w.keys = off;  // key rows padded to 16 bytes
+    off += align_up(P * ((g.nbmax + 3) / 4 * 4) * sizeof(uint32_t));
+    // top-digit histograms and tickets: only problems split over several
+    // CTAs use them, and there are fewer of those than 2 * SMs
+    const size_t sms = static_cast<size_t>(device_sm_count());
+    const size_t hrows = P < 2 * sms ? P : 2 * sms;
+    w.sel_hist = off;
+    off += align_up(hrows * select_hist_bytes());
+    w.sel_ticket = off;
+    off += align_up(hrows * sizeof(unsigned));
     w.sel_idx = off;
     off += align_up(P * g.nbmax * sizeof(int32_t));
     w.sel_cnt = off;
@@ -145,8 +154,12 @@ kvd_status select_impl(const kvd_cache *c, const float *q, int n_heads, int k_se
                        int recent, int32_t *sel_idx, int32_t *sel_cnt, void *ws,
                        const WsLayout &w, cudaStream_t st, bool in_step = false) {
     const Geom g = make_geom(c, n_heads, c->len);
-    return cuda_status(launch_select(*c, g, q, k_sel, sink, recent, sel_idx, sel_cnt,
-                                     ws_at<uint32_t>(ws, w.keys), st, true, in_step));
+    SelScratch scr;
+    scr.keys = ws_at<uint32_t>(ws, w.keys);
+    scr.hist = ws_at<int>(ws, w.sel_hist);
+    scr.ticket = ws_at<unsigned>(ws, w.sel_ticket);
+    return cuda_status(launch_select(*c, g, q, k_sel, sink, recent, sel_idx, sel_cnt, scr, st,
+                                     true, in_step));
 }
 
 kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float scale,

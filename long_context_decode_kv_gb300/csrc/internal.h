@@ -34,11 +34,20 @@ int device_sm_count();
 cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_new, int n_new,
                           cudaStream_t st, bool pdl);
 
+// Scratch of the selection (workspace regions; hist and ticket are zero
+// between calls, and every completed call leaves them zero).
+struct SelScratch {
+    uint32_t *keys;    // [B*Hkv][round_up(candidates, 4)] keys
+    int *hist;         // [min(B*Hkv, 2*SMs)][select_hist_bytes()/4] top-digit histograms
+    unsigned *ticket;  // [min(B*Hkv, 2*SMs)] arrival counters
+};
+size_t select_hist_bytes();
+
 // after_step_append: launched right after the one-token append of a decode
 // step (so scoring may overlap that append when the token's block is forced).
 cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int k_sel,
                           int sink_tokens, int recent_tokens, int32_t *sel_idx,
-                          int32_t *sel_cnt, uint32_t *keys, cudaStream_t st, bool pdl,
+                          int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st, bool pdl,
                           bool after_step_append);
 
 cudaError_t launch_scores_debug(const kvd_cache &c, const Geom &g, const float *q, float *ub,
@@ -70,6 +79,24 @@ cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Cooperative launch: every CTA of the grid is resident at once (the launch
+// fails otherwise), as kernels whose CTAs wait on one another require.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -12,16 +12,20 @@
 // Equal bounds go to the lower block index; the top-K budget counts only the
 // blocks that are not forced.
 //
-// score_kernel: streams the bounds (512 B per block) of a contiguous range of
-// candidate blocks through a TMA ring in shared memory, over every SM, and
-// writes one order-preserving u32 key per block (or the f32 bound itself,
-// for the test export).
+// select_kernel: the candidate blocks of a problem (sequence, KV head) are
+// split over X CTAs.  Each CTA streams the bounds (512 B per block) of its
+// range through a TMA ring in shared memory, turns every block's group bound
+// into an order-preserving u32 key (written to global scratch), and
+// histograms the keys' top 11 bits in shared memory.  It adds that
+// histogram into the problem's global one and takes a ticket; the last CTA
+// of the problem to arrive finishes the selection alone: the keff-th largest
+// key T by radix select (the top digit from the global histogram, then bits
+// 20-10 and 9-0 over the problem's keys, held in shared memory), then the
+// ascending list written warp by warp in index order.  No CTA waits for
+// another, so problems finish while others are still being scored.
 //
-// topk_kernel: one 1024-thread CTA per (sequence, KV head) holds the keys
-// (L2-resident) in shared memory, finds the K-th largest key with
-// range-adaptive 12-bit radix passes, and writes the ascending list: forced
-// sink blocks, the taken candidates (larger keys, then the lowest-index
-// blocks equal to the K-th key), forced recent blocks.
+// fill_kernel: the selections that need no bounds (no candidates to rank:
+// K_SEL = 0, or at least as large as the candidate count).
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,17 +36,22 @@ constexpr unsigned kFullMask = 0xffffffffu;
 
 constexpr int kScoreWarps = 8;                       // consumers; warp 8 produces
 constexpr int kScoreThreads = 32 * (kScoreWarps + 1);
+constexpr int kConsumerThreads = 32 * kScoreWarps;
 constexpr int kScoreSlots = 4;                       // blocks per warp per stage (8 lanes each)
 constexpr int kStageBlocks = kScoreWarps * kScoreSlots;  // 32
 constexpr int kBoundRowBytes = kHeadDim * 2 * 2;      // (kmin, kmax) f16 pairs: 512 B
-constexpr int kScoreStages = 4;
+constexpr int kScoreStages = 6;
 constexpr int kScoreStageBytes = kStageBlocks * kBoundRowBytes;  // 16 KiB
 
-constexpr int kMaxSelectBlocks = 49152;  // candidate keys held in shared memory
-constexpr int kDigitBits = 12;
-constexpr int kBins = 1 << kDigitBits;
+constexpr int kMaxSelectBlocks = 49152;
+constexpr int kMaxCtasPerProblem = 1024;
+
+// Radix digits of a key, from the top: bits 31-21, 20-10, 9-0.
+constexpr int kShift1 = 21, kShift2 = 10;
+constexpr int kH1 = 1 << 11, kH2 = 1 << 11, kH3 = 1 << 10;
 
 enum TopkMode { kTakeNone = 0, kTakeAll = 1, kTakeTopK = 2 };
+enum SelMode { kExport = 0, kSelect = 1 };
 
 // ------------------------------------------------------ bound math ---
 // Scoring lane layout: 16 lanes per block; lane e (0..15) of a block holds
@@ -150,33 +159,115 @@ __device__ __forceinline__ float group_bound(const float *q_s,
     return best;
 }
 
-// CTA (x, p) of score_kernel: candidate blocks [x*R, min(n, (x+1)*R)) of
-// problem p = (sequence, KV head), i.e. cache blocks blk_lo + j.  Their
-// bounds stream through a TMA ring (stages of 32 blocks; warp 8 produces,
-// warps 0..7 consume, warp w scoring blocks 4w..4w+3 of each stage two at a
-// time).  keys != nullptr: keys[p*n + j] = order-preserving key of the bound;
-// ub != nullptr: ub[p*n + j] = the f32 bound (test export).
-template <int G>
-__global__ void __launch_bounds__(kScoreThreads, 2)
-score_kernel(const float *__restrict__ q, const __half *__restrict__ kbounds, int Hkv, int H,
-             int nbmax, int blk_lo, int n,
-             int R, uint32_t *__restrict__ keys, float *__restrict__ ub,
-             int32_t *__restrict__ dev_status, int overlap) {
+struct SelArgs {
+    const float *q;
+    const __half *kbounds;
+    int Hkv, H, nbmax;
+    int se, n, R;          // candidates: blocks se .. se+n-1; R per CTA
+    uint32_t *keys;        // [P][ldk] keys (scratch)
+    int ldk;
+    float *ub;             // kExport: [P][n] bounds
+    int *hist;             // [P][kH1] top-digit histograms (zero between calls)
+    unsigned *ticket;      // [P] arrival counters (zero between calls)
+    int32_t *sel_idx, *sel_cnt;
+    int NB, rb, keff;
+    int32_t *dev_status;
+    int overlap;
+};
+
+__device__ __forceinline__ int warp_inclusive_scan(int x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+struct RadixShared {
+    uint64_t kbar;  // bulk copy of the keys (last CTA)
+    int wsum[kScoreWarps + 1];
+    int digit, above, last;
+};
+
+// Digit of the krem-th largest key from a shared-memory histogram of NBINS
+// bins (left zeroed); krem becomes the rank within that digit.  The consumer
+// thread t owns the digits NBINS-1-c*t .. NBINS-c*(t+1) (c = NBINS/256,
+// descending).  All threads call it.
+template <int NBINS>
+__device__ int radix_digit(int *hist, int &krem, RadixShared &rs) {
+    constexpr int c = NBINS / kConsumerThreads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __syncthreads();  // histogram complete
+    int cnt[c];
+    int here = 0;
+    if (warp < kScoreWarps) {
+        const int base = NBINS - c * (tid + 1);
+        int v[c];
+#pragma unroll
+        for (int i = 0; i < c; i += 4) {
+            int4 *h4 = reinterpret_cast<int4 *>(hist + base + i);
+            const int4 w = *h4;
+            *h4 = make_int4(0, 0, 0, 0);
+            v[i] = w.x; v[i + 1] = w.y; v[i + 2] = w.z; v[i + 3] = w.w;
+        }
+#pragma unroll
+        for (int jj = 0; jj < c; ++jj) {
+            cnt[jj] = v[c - 1 - jj];
+            here += cnt[jj];
+        }
+    }
+    const int incl = warp_inclusive_scan(here, lane);
+    if (lane == 31 && warp < kScoreWarps) rs.wsum[warp] = incl;
+    __syncthreads();
+    if (warp < kScoreWarps) {
+        const int wv = lane < kScoreWarps ? rs.wsum[lane] : 0;
+        const int winc = warp_inclusive_scan(wv, lane);
+        const int wex = __shfl_sync(kFullMask, winc - wv, warp);
+        const int above = wex + incl - here;
+        if (above < krem && krem <= above + here) {
+            int acc = above;
+#pragma unroll
+            for (int jj = 0; jj < c; ++jj) {
+                if (krem <= acc + cnt[jj]) {
+                    rs.digit = NBINS - 1 - c * tid - jj;
+                    rs.above = acc;
+                    break;
+                }
+                acc += cnt[jj];
+            }
+        }
+    }
+    __syncthreads();
+    krem -= rs.above;
+    return rs.digit;
+}
+
+constexpr int kRingKeys = kScoreStages * kScoreStageBytes / 4;  // keys that fit the ring
+
+// CTA (x, p): candidate blocks j in [x*R, min(n, (x+1)*R)) of problem p,
+// i.e. cache blocks se + j.  Their bounds stream through a TMA ring (stages
+// of 32 blocks; warp 8 produces, warps 0..7 consume, warp w scoring blocks
+// 4w..4w+3 of each stage two at a time).
+template <int G, int MODE>
+__global__ void __launch_bounds__(kScoreThreads, 2) select_kernel(SelArgs a) {
     constexpr int NH = G < 4 ? G : 4;
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ RadixShared rs;
+    __shared__ int s_abort, s_issued;
     uint8_t *ring = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kScoreStages * kScoreStageBytes);
     uint64_t *empty = full + kScoreStages;
     float *q_s = reinterpret_cast<float *>(empty + kScoreStages);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(q_s + G * kHeadDim);
-    int *issued_s = const_cast<int *>(abort_flag) + 1;
+    int *hist_l = reinterpret_cast<int *>(q_s + G * kHeadDim);  // kH1 ints (kSelect)
+    volatile int *abort_flag = &s_abort;
 
     const int p = blockIdx.y;
-    const int b = p / Hkv, g = p % Hkv;
+    const int b = p / a.Hkv, g = p % a.Hkv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int half = lane >> 4, e = lane & 15;
-    const int j0 = blockIdx.x * R;
-    const int j1 = min(n, j0 + R);
+    const int j0 = blockIdx.x * a.R;
+    const int j1 = min(a.n, j0 + a.R);
     const int nstage = (j1 - j0 + kStageBlocks - 1) / kStageBlocks;
 
     if (tid == 0) {
@@ -184,21 +275,23 @@ score_kernel(const float *__restrict__ q, const __half *__restrict__ kbounds, in
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kScoreWarps);
         }
-        *abort_flag = 0;
-        *issued_s = 0;
+        mbar_init(&rs.kbar, 1);
+        s_abort = 0;
+        s_issued = 0;
         fence_barrier_init();
     }
+    if (MODE == kSelect)
+        for (int i = tid; i < kH1; i += kScoreThreads) hist_l[i] = 0;
+    __syncthreads();
     // overlap: inside a decode step whose appended token lands in a forced
     // block, the candidate bounds and the query are complete before the
     // upstream append runs, so scoring overlaps it; the grid-dependency wait
-    // then moves to the end, so this grid still completes after the append.
-    if (!overlap) pdl_wait();
-    const float *qg = q + (static_cast<size_t>(b) * H + static_cast<size_t>(g) * G) * kHeadDim;
-    for (int i = tid; i < G * kHeadDim; i += blockDim.x) q_s[i] = qg[i];
-    __syncthreads();
+    // then comes before anything shared with earlier kernels is written.
+    if (!a.overlap) pdl_wait();
     pdl_launch_dependents();
 
-    const size_t base = static_cast<size_t>(p) * nbmax + blk_lo;  // row of candidate 0
+    // ================================================= phase 1: keys
+    const size_t base = static_cast<size_t>(p) * a.nbmax + a.se;  // row of candidate 0
     if (warp == kScoreWarps) {
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
@@ -207,21 +300,26 @@ score_kernel(const float *__restrict__ q, const __half *__restrict__ kbounds, in
                 const int s = si % kScoreStages;
                 if (si >= kScoreStages &&
                     !mbar_wait(&empty[s], ((si / kScoreStages) - 1) & 1, abort_flag)) {
-                    *abort_flag = 1;
-                    report_status(dev_status, KVD_ERR_TIMEOUT);
+                    s_abort = 1;
+                    report_status(a.dev_status, KVD_ERR_TIMEOUT);
                     break;
                 }
                 const int jb = j0 + si * kStageBlocks;
                 const int cnt = min(kStageBlocks, j1 - jb);
                 const uint32_t bytes = static_cast<uint32_t>(cnt) * kBoundRowBytes;
                 mbar_arrive_expect_tx(&full[s], bytes);
-                tma_load_1d(ring + s * kScoreStageBytes, kbounds + (base + jb) * kHeadDim * 2,
+                tma_load_1d(ring + s * kScoreStageBytes, a.kbounds + (base + jb) * kHeadDim * 2,
                             bytes, &full[s], pol);
                 issued = si + 1;
             }
-            *issued_s = issued;
+            s_issued = issued;
         }
     } else {
+        // the producer's first copies are in flight while the query loads
+        const float *qg =
+            a.q + (static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * G) * kHeadDim;
+        for (int i = tid; i < G * kHeadDim; i += kConsumerThreads) q_s[i] = qg[i];
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
         float2 qreg[NH][8];
         if constexpr (G <= 4) load_qpairs<NH>(q_s, 0, e, qreg);
         const int sw = chunk_swap(e);
@@ -230,8 +328,8 @@ score_kernel(const float *__restrict__ q, const __half *__restrict__ kbounds, in
             const bool ok = mbar_wait(&full[s], (si / kScoreStages) & 1, abort_flag);
             if (!__all_sync(kFullMask, ok)) {
                 if (lane == 0) {
-                    *abort_flag = 1;
-                    report_status(dev_status, KVD_ERR_TIMEOUT);
+                    s_abort = 1;
+                    report_status(a.dev_status, KVD_ERR_TIMEOUT);
                 }
                 break;
             }
@@ -264,279 +362,254 @@ score_kernel(const float *__restrict__ q, const __half *__restrict__ kbounds, in
 #pragma unroll
             for (int ps = 0; ps < 2; ++ps) {
                 if (jr[ps] < j1 && e == 0) {
-                    const size_t o = static_cast<size_t>(p) * n + jr[ps];
-                    if (keys) keys[o] = float_to_key(sc[ps]);
-                    if (ub) ub[o] = sc[ps];
-                }
-            }
-        }
-    }
-    __syncthreads();
-    if (*abort_flag && warp == kScoreWarps && lane == 0) {
-        // wind down: wait (bounded) for the copies still landing in the ring
-        const int issued = *issued_s;
-        volatile int never = 0;
-        for (int i = max(0, issued - kScoreStages); i < issued; ++i)
-            (void)mbar_wait(&full[i % kScoreStages], (i / kScoreStages) & 1, &never);
-    }
-    if (overlap) pdl_wait();
-}
-
-// ------------------------------------------------------------- top-K ---
-constexpr int kTopkThreads = 1024;
-
-struct TopkArgs {
-    const uint32_t *keys;   // [P, rb - se] candidate keys (score_kernel)
-    int32_t *sel_idx, *sel_cnt;
-    int nbmax, NB;
-    int se, rb;        // forced: [0, se) and [rb, NB); candidates [se, rb)
-    int keff, mode;    // candidates to take, TopkMode
-};
-
-// Exclusive scan of one int per thread over a 1024-thread CTA; *total gets
-// the sum.  All threads must call it.
-__device__ __forceinline__ int cta_exclusive_scan(int v, int *warp_sums, int *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFullMask, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        const int w = warp_sums[lane];
-        int s = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFullMask, s, o);
-            if (lane >= o) s += y;
-        }
-        warp_sums[lane] = s - w;  // exclusive prefix of the warp totals
-        if (lane == 31) *total = s;
-    }
-    __syncthreads();
-    const int r = warp_sums[warp] + x - v;
-    __syncthreads();
-    return r;
-}
-
-// One CTA per (sequence, KV head).  Thread t owns the C = ceil(n / 1024)
-// consecutive candidates [tC, tC + C); their keys sit in shared memory
-// transposed (key tC + i at i*1024 + t), so that every shared access below is
-// conflict-free.  The K-th largest key T comes from range-adaptive 12-bit
-// radix passes; the ascending list then needs one CTA scan of the packed
-// per-thread counts of keys above and equal to T.
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
-    extern __shared__ __align__(16) uint32_t s_keys[];
-    __shared__ int hist[kBins];
-    __shared__ int warp_sums[32];
-    __shared__ int s_total;
-    __shared__ uint32_t s_red[2][32];
-    __shared__ int s_digit, s_above;
-    const int n_cand = a.rb - a.se;
-    const int n_keys = a.mode == kTakeTopK ? n_cand : 0;
-    const int C = (n_cand + kTopkThreads - 1) / kTopkThreads;  // candidates per thread
-    const int p = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c0 = min(n_cand, tid * C), c1 = min(n_cand, c0 + C);
-    pdl_wait();
-    pdl_launch_dependents();
-
-    const uint32_t *kp = a.keys + static_cast<size_t>(p) * n_keys;
-    uint32_t kmn = 0xffffffffu, kmx = 0u;
-    if (a.mode == kTakeTopK) {
-        for (int j = c0; j < c1; ++j) {
-            const uint32_t k = __ldcg(kp + j);
-            s_keys[(j - c0) * kTopkThreads + tid] = k;
-            kmn = min(kmn, k);
-            kmx = max(kmx, k);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        kmn = min(kmn, __shfl_xor_sync(kFullMask, kmn, o));
-        kmx = max(kmx, __shfl_xor_sync(kFullMask, kmx, o));
-    }
-    if (lane == 0) {
-        s_red[0][warp] = kmn;
-        s_red[1][warp] = kmx;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        kmn = s_red[0][lane];
-        kmx = s_red[1][lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            kmn = min(kmn, __shfl_xor_sync(kFullMask, kmn, o));
-            kmx = max(kmx, __shfl_xor_sync(kFullMask, kmx, o));
-        }
-        if (lane == 0) {
-            s_red[0][0] = kmn;
-            s_red[1][0] = kmx;
-        }
-    }
-    __syncthreads();
-    kmn = s_red[0][0];
-    kmx = s_red[1][0];
-
-    // ---- T = the keff-th largest key; need_eq = keys equal to T to take.
-    // Digits of 12 bits from the top of the bits where the keys differ.
-    uint32_t T = 0u;
-    int need_eq = 0;
-    if (a.mode == kTakeTopK) {
-        const uint32_t diff = kmn ^ kmx;
-        if (diff == 0u) {
-            T = kmn;
-            need_eq = a.keff;
-        } else {
-            const int nbits = 32 - __clz(diff);
-            uint32_t mask = nbits >= 32 ? 0u : (0xffffffffu << nbits);
-            uint32_t prefix = kmn & mask;
-            int krem = a.keff;
-            for (int hi = nbits; hi > 0; hi -= kDigitBits) {
-                const int lo = hi > kDigitBits ? hi - kDigitBits : 0;
-                const int nb = 1 << (hi - lo);
-                const uint32_t dmask = static_cast<uint32_t>(nb - 1);
-                for (int i = tid; i < nb; i += kTopkThreads) hist[i] = 0;
-                __syncthreads();
-                for (int i = 0; i < c1 - c0; ++i) {
-                    const uint32_t k = s_keys[i * kTopkThreads + tid];
-                    if ((k & mask) == prefix) atomicAdd(&hist[(k >> lo) & dmask], 1);
-                }
-                __syncthreads();
-                // thread t owns the 4 digits nb-1-4t .. nb-4-4t (descending order)
-                int c4[4];
-                int here = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int d = nb - 1 - 4 * tid - j;
-                    c4[j] = d >= 0 ? hist[d] : 0;
-                    here += c4[j];
-                }
-                const int above = cta_exclusive_scan(here, warp_sums, &s_total);
-                if (above < krem && krem <= above + here) {
-                    int acc = above;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (krem <= acc + c4[j]) {
-                            s_digit = nb - 1 - 4 * tid - j;
-                            s_above = acc;
-                            break;
-                        }
-                        acc += c4[j];
+                    if constexpr (MODE == kSelect) {
+                        const uint32_t key = float_to_key(sc[ps]);
+                        a.keys[static_cast<size_t>(p) * a.ldk + jr[ps]] = key;
+                        atomicAdd(&hist_l[key >> kShift1], 1);
+                    } else {
+                        a.ub[static_cast<size_t>(p) * a.n + jr[ps]] = sc[ps];
                     }
                 }
-                __syncthreads();
-                prefix |= static_cast<uint32_t>(s_digit) << lo;
-                mask |= dmask << lo;
-                krem -= s_above;
-                __syncthreads();
             }
-            T = prefix;
-            need_eq = krem;
         }
+    }
+    __syncthreads();
+    if (s_abort) {
+        if (warp == kScoreWarps && lane == 0) {
+            // wind down: wait (bounded) for the copies still landing in the ring
+            const int issued = s_issued;
+            volatile int never = 0;
+            for (int i = max(0, issued - kScoreStages); i < issued; ++i)
+                (void)mbar_wait(&full[i % kScoreStages], (i / kScoreStages) & 1, &never);
+        }
+        if (a.overlap) pdl_wait();
+        return;
+    }
+    if (a.overlap) pdl_wait();  // the upstream kernels are complete past here
+    if constexpr (MODE == kExport) return;
+
+    // ================================================= phase 2: ticket
+    const int X = gridDim.x;
+    const int n = a.n;
+    const uint32_t *kp = a.keys + static_cast<size_t>(p) * a.ldk;
+    const bool in_smem = n <= kRingKeys;
+    uint32_t *s_keys = reinterpret_cast<uint32_t *>(ring);
+    if (X > 1) {
+        int *hg = a.hist + static_cast<size_t>(p) * kH1;
+        for (int i = tid; i < kH1; i += kScoreThreads) {
+            const int v = hist_l[i];
+            if (v != 0) {
+                atomicAdd(&hg[i], v);
+                hist_l[i] = 0;
+            }
+        }
+    }
+    __threadfence();  // this CTA's keys (and histogram counts) are out
+    __syncthreads();
+    if (X > 1) {
+        if (tid == 0)
+            rs.last = atomicAdd(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
+        __syncthreads();
+        if (!rs.last) return;
+        // the last CTA of the problem: every key and histogram count is in
+        __threadfence();
+    }
+    if (in_smem && warp == kScoreWarps) {
+        // the problem's keys (L2-resident) into the ring by bulk copies; they
+        // were written by ordinary stores, so order those before the async proxy
+        const uint32_t bytes = static_cast<uint32_t>(a.ldk) * 4u;
+        const uint32_t off = static_cast<uint32_t>(lane) * kScoreStageBytes;
+        asm volatile("fence.proxy.async;" ::: "memory");
+        if (lane == 0) mbar_arrive_expect_tx(&rs.kbar, bytes);
+        __syncwarp();
+        if (off < bytes)
+            tma_load_1d(ring + off, reinterpret_cast<const uint8_t *>(kp) + off,
+                        min(static_cast<uint32_t>(kScoreStageBytes), bytes - off), &rs.kbar,
+                        l2_policy_evict_first());
+    }
+    if (X > 1) {
+        int *hg = a.hist + static_cast<size_t>(p) * kH1;
+        for (int i = tid * 4; i < kH1; i += kScoreThreads * 4) {
+            int4 *src = reinterpret_cast<int4 *>(hg + i);
+            *reinterpret_cast<int4 *>(hist_l + i) = __ldcg(src);
+            __stcg(src, make_int4(0, 0, 0, 0));
+        }
+        if (tid == 0) a.ticket[p] = 0u;
     }
 
-    // ---- ascending list: sink blocks, taken candidates, recent blocks
+    // ================================================= phase 3: T
+    int krem = a.keff;
+    const int d1 = radix_digit<kH1>(hist_l, krem, rs);
+    if (in_smem && !mbar_wait(&rs.kbar, 0, abort_flag)) s_abort = 1;
+    if (__syncthreads_or(s_abort)) {
+        if (tid == 0) {
+            report_status(a.dev_status, KVD_ERR_TIMEOUT);
+            a.sel_cnt[p] = 0;
+            volatile int never = 0;
+            if (in_smem) (void)mbar_wait(&rs.kbar, 0, &never);  // copies in flight
+        }
+        return;
+    }
+    // pass over the keys, four at a time: thread t takes keys 4q..4q+3 for
+    // q = t, t + 288, ...
+    const int nq = (n + 3) / 4;
+    auto quad_at = [&](int q) -> uint4 {
+        return in_smem ? reinterpret_cast<const uint4 *>(s_keys)[q]
+                       : __ldcg(reinterpret_cast<const uint4 *>(kp) + q);
+    };
+    for (int q = tid; q < nq; q += kScoreThreads) {
+        const uint4 w = quad_at(q);
+        const uint32_t k4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (4 * q + u < n && (k4[u] >> kShift1) == static_cast<uint32_t>(d1))
+                atomicAdd(&hist_l[(k4[u] >> kShift2) & (kH2 - 1)], 1);
+    }
+    const int d2 = radix_digit<kH2>(hist_l, krem, rs);
+    const uint32_t pre2 = (static_cast<uint32_t>(d1) << (kShift1 - kShift2)) |
+                          static_cast<uint32_t>(d2);
+    for (int q = tid; q < nq; q += kScoreThreads) {
+        const uint4 w = quad_at(q);
+        const uint32_t k4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (4 * q + u < n && (k4[u] >> kShift2) == pre2)
+                atomicAdd(&hist_l[k4[u] & (kH3 - 1)], 1);
+    }
+    const int d3 = radix_digit<kH3>(hist_l, krem, rs);
+    const uint32_t T = (pre2 << kShift2) | static_cast<uint32_t>(d3);
+    const int need_eq = krem;  // keys equal to T to take, lowest index first
+
+    // ================================================= phase 4: the list
+    // bitmaps of the keys above / equal to T, one 32-bit word per 32
+    // consecutive candidates (a warp ballot each)
+    const int nw = (n + 31) / 32;
+    uint32_t *gtw = in_smem ? reinterpret_cast<uint32_t *>(hist_l) : s_keys;
+    uint32_t *eqw = gtw + nw;
+    constexpr int kWarps = kScoreWarps + 1;
+    for (int wi = warp; wi < nw; wi += kWarps) {
+        const int j = 32 * wi + lane;
+        const uint32_t k = j < n ? (in_smem ? s_keys[j] : __ldcg(kp + j)) : 0u;
+        const unsigned gm = __ballot_sync(kFullMask, j < n && k > T);
+        const unsigned em = __ballot_sync(kFullMask, j < n && k == T);
+        if (lane == 0) {
+            gtw[wi] = gm;
+            eqw[wi] = em;
+        }
+    }
+    __syncthreads();
+    // thread t owns words [t*wpt, (t+1)*wpt): an exclusive scan of the
+    // packed counts (above | equal << 16; both below 2^16) orders them
+    const int wpt = (nw + kScoreThreads - 1) / kScoreThreads;
+    const int w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+    unsigned mine = 0;
+    for (int wi = w0; wi < w1; ++wi)
+        mine += static_cast<unsigned>(__popc(gtw[wi])) | (static_cast<unsigned>(__popc(eqw[wi])) << 16);
+    const unsigned incl = static_cast<unsigned>(warp_inclusive_scan(static_cast<int>(mine), lane));
+    if (lane == 31) rs.wsum[warp] = static_cast<int>(incl);
+    __syncthreads();
+    unsigned before = incl - mine;
+    for (int w = 0; w < warp; ++w) before += static_cast<unsigned>(rs.wsum[w]);
+    int g_before = static_cast<int>(before & 0xffffu), e_before = static_cast<int>(before >> 16);
     int32_t *dst = a.sel_idx + static_cast<size_t>(p) * a.nbmax;
-    for (int j = tid; j < a.se; j += kTopkThreads) dst[j] = j;
-    int gt_here = 0, eq_here = 0;
-    if (a.mode == kTakeAll) {
-        gt_here = c1 - c0;
-    } else if (a.mode == kTakeTopK) {
-        for (int i = 0; i < c1 - c0; ++i) {
-            const uint32_t k = s_keys[i * kTopkThreads + tid];
-            gt_here += k > T;
-            eq_here += k == T;
+    for (int wi = w0; wi < w1; ++wi) {
+        const uint32_t gm = gtw[wi], em = eqw[wi];
+        uint32_t take = gm;
+        int r = min(max(need_eq - e_before, 0), __popc(em));  // equal keys taken here
+        for (uint32_t m = em; r > 0; --r) {
+            take |= m & (0u - m);  // lowest remaining equal key
+            m &= m - 1;
         }
+        int o = a.se + g_before + min(e_before, need_eq);
+        for (uint32_t m = take; m; m &= m - 1) dst[o++] = a.se + 32 * wi + (__ffs(m) - 1);
+        g_before += __popc(gm);
+        e_before += __popc(em);
     }
-    // counts stay below 2^16 (n <= 49152): greater in the low half, equal in the high
-    const int pre = cta_exclusive_scan(gt_here | (eq_here << 16), warp_sums, &s_total);
-    const int tot = s_total;
-    const int gt_pre = pre & 0xffff, eq_pre = pre >> 16;
-    // equal keys are taken in index order: the first need_eq of them
-    int o = a.se + gt_pre + min(eq_pre, need_eq);
-    if (a.mode == kTakeAll) {
-        for (int j = c0; j < c1; ++j) dst[o++] = a.se + j;
-    } else if (a.mode == kTakeTopK) {
-        int r = eq_pre;
-        for (int i = 0; i < c1 - c0; ++i) {
-            const uint32_t k = s_keys[i * kTopkThreads + tid];
-            const bool take = k > T || (k == T && r < need_eq);
-            r += k == T;
-            if (take) dst[o++] = a.se + c0 + i;
-        }
-    }
-    const int taken = (tot & 0xffff) + min(tot >> 16, need_eq);
-    for (int j = a.rb + tid; j < a.NB; j += kTopkThreads) dst[a.se + taken + (j - a.rb)] = j;
-    if (tid == 0) a.sel_cnt[p] = a.se + taken + (a.NB - a.rb);
+    for (int j = tid; j < a.se; j += kScoreThreads) dst[j] = j;
+    for (int j = a.rb + tid; j < a.NB; j += kScoreThreads) dst[a.se + a.keff + (j - a.rb)] = j;
+    if (tid == 0) a.sel_cnt[p] = a.se + a.keff + (a.NB - a.rb);
 }
 
-constexpr int score_smem_bytes(int G) {
-    return kScoreStages * kScoreStageBytes + 2 * kScoreStages * 8 + G * kHeadDim * 4 + 16;
+// Selections that rank nothing: sink blocks, all candidates (take_all) or
+// none, recent blocks.
+__global__ void __launch_bounds__(256) fill_kernel(int32_t *sel_idx, int32_t *sel_cnt, int nbmax,
+                                                   int NB, int se, int rb, int take_all) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int p = blockIdx.x;
+    int32_t *dst = sel_idx + static_cast<size_t>(p) * nbmax;
+    const int n_take = take_all ? rb - se : 0;
+    for (int j = threadIdx.x; j < se + n_take; j += blockDim.x) dst[j] = j;
+    for (int j = rb + threadIdx.x; j < NB; j += blockDim.x) dst[se + n_take + (j - rb)] = j;
+    if (threadIdx.x == 0) sel_cnt[p] = se + n_take + (NB - rb);
 }
 
 template <int G>
-cudaError_t launch_score(const kvd_cache &c, const Geom &g, const float *q, int blk_lo, int n,
-                         uint32_t *keys, float *ub, cudaStream_t st, bool pdl, bool overlap) {
-    static bool attr_set = false;
-    constexpr int smem = score_smem_bytes(G);
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            score_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    // blocks per CTA: about two CTAs per SM in total, at least one stage each
-    const long P = static_cast<long>(g.B) * g.Hkv;
-    const long want = 2L * device_sm_count();
-    long R = (static_cast<long>(n) * P + want - 1) / want;
-    R = (R + kStageBlocks - 1) / kStageBlocks * kStageBlocks;
-    if (R < kStageBlocks) R = kStageBlocks;
-    dim3 grid(static_cast<unsigned>((n + R - 1) / R), static_cast<unsigned>(P));
-    return launch_ex(score_kernel<G>, grid, dim3(kScoreThreads), smem, st, pdl, q,
-                     static_cast<const __half *>(c.kbounds), g.Hkv, g.H, g.nbmax, blk_lo, n,
-                     static_cast<int>(R), keys, ub, c.dev_status, overlap ? 1 : 0);
+constexpr int select_smem_bytes() {
+    return kScoreStages * kScoreStageBytes + 2 * kScoreStages * 8 + G * kHeadDim * 4 +
+           kH1 * 4;
 }
 
-cudaError_t launch_score_any(const kvd_cache &c, const Geom &g, const float *q, int blk_lo,
-                             int n, uint32_t *keys, float *ub, cudaStream_t st, bool pdl,
-                             bool overlap) {
-    switch (g.G) {
-        case 1: return launch_score<1>(c, g, q, blk_lo, n, keys, ub, st, pdl, overlap);
-        case 2: return launch_score<2>(c, g, q, blk_lo, n, keys, ub, st, pdl, overlap);
-        case 4: return launch_score<4>(c, g, q, blk_lo, n, keys, ub, st, pdl, overlap);
-        case 8: return launch_score<8>(c, g, q, blk_lo, n, keys, ub, st, pdl, overlap);
-        case 16: return launch_score<16>(c, g, q, blk_lo, n, keys, ub, st, pdl, overlap);
+template <int G, int MODE>
+cudaError_t launch_select_t(const SelArgs &a0, int P, cudaStream_t st, bool pdl) {
+    constexpr int smem = select_smem_bytes<G>();
+    static int occupancy = 0;
+    if (occupancy == 0) {
+        cudaError_t e = cudaFuncSetAttribute(select_kernel<G, MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_kernel<G, MODE>,
+                                                          kScoreThreads, smem);
+        if (e != cudaSuccess) return e;
+        occupancy = occ > 0 ? occ : 1;
+    }
+    SelArgs a = a0;
+    // CTAs per problem: about as many as fit on the GPU at once, split evenly
+    const long cap = static_cast<long>(occupancy) * device_sm_count();
+    long X = cap / P;
+    if (X > kMaxCtasPerProblem) X = kMaxCtasPerProblem;
+    if (X < 1) X = 1;
+    long R = (static_cast<long>(a.n) + X - 1) / X;
+    X = (a.n + R - 1) / R;
+    a.R = static_cast<int>(R);
+    const dim3 grid(static_cast<unsigned>(X), static_cast<unsigned>(P));
+    return launch_ex(select_kernel<G, MODE>, grid, dim3(kScoreThreads), smem, st, pdl, a);
+}
+
+template <int MODE>
+cudaError_t launch_select_any(const SelArgs &a, int G, int P, cudaStream_t st, bool pdl) {
+    switch (G) {
+        case 1: return launch_select_t<1, MODE>(a, P, st, pdl);
+        case 2: return launch_select_t<2, MODE>(a, P, st, pdl);
+        case 4: return launch_select_t<4, MODE>(a, P, st, pdl);
+        case 8: return launch_select_t<8, MODE>(a, P, st, pdl);
+        case 16: return launch_select_t<16, MODE>(a, P, st, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_topk(const TopkArgs &a, int P, int n_cand, cudaStream_t st, bool pdl) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMaxSelectBlocks * static_cast<int>(sizeof(uint32_t)));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    // transposed key layout: ceil(n / 1024) * 1024 slots (<= kMaxSelectBlocks)
-    const size_t slots = (static_cast<size_t>(n_cand) + kTopkThreads - 1) / kTopkThreads *
-                         kTopkThreads;
-    const size_t smem = (a.mode == kTakeTopK ? slots : 0) * sizeof(uint32_t);
-    return launch_ex(topk_kernel, dim3(P), dim3(kTopkThreads), smem, st, pdl, a);
+SelArgs base_args(const kvd_cache &c, const Geom &g, const float *q) {
+    SelArgs a = {};
+    a.q = q;
+    a.kbounds = static_cast<const __half *>(c.kbounds);
+    a.Hkv = g.Hkv;
+    a.H = g.H;
+    a.nbmax = g.nbmax;
+    a.NB = g.NB;
+    a.dev_status = c.dev_status;
+    return a;
 }
 
 }  // namespace
 
 int max_select_blocks() { return kMaxSelectBlocks; }
 
+size_t select_hist_bytes() { return kH1 * sizeof(int); }
+
 cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int k_sel,
                           int sink_tokens, int recent_tokens, int32_t *sel_idx,
-                          int32_t *sel_cnt, uint32_t *keys, cudaStream_t st, bool pdl,
+                          int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st, bool pdl,
                           bool after_step_append) {
     const int NB = g.NB;
     int se = (sink_tokens + kBlock - 1) / kBlock;
@@ -550,30 +623,34 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
     if (rb < se) rb = se;
     const int n_cand = rb - se;
     const int keff = k_sel < n_cand ? k_sel : n_cand;
-    TopkArgs a;
-    a.keys = keys;
+    const int P = g.B * g.Hkv;
+    if (!(keff > 0 && keff < n_cand))
+        return launch_ex(fill_kernel, dim3(P), dim3(256), 0, st, pdl, sel_idx, sel_cnt, g.nbmax,
+                         NB, se, rb, keff > 0 ? 1 : 0);
+    SelArgs a = base_args(c, g, q);
+    a.se = se;
+    a.n = n_cand;
+    a.keys = scr.keys;
+    a.ldk = (n_cand + 3) / 4 * 4;
+    a.hist = scr.hist;
+    a.ticket = scr.ticket;
     a.sel_idx = sel_idx;
     a.sel_cnt = sel_cnt;
-    a.nbmax = g.nbmax;
-    a.NB = NB;
-    a.se = se;
     a.rb = rb;
     a.keff = keff;
-    a.mode = (keff > 0 && keff < n_cand) ? kTakeTopK : (keff == 0 ? kTakeNone : kTakeAll);
-    if (a.mode == kTakeTopK) {
-        // the appended token's block is the last one; it is never a candidate
-        // while the recent window is non-empty
-        const bool overlap = after_step_append && recent_tokens > 0;
-        const cudaError_t e =
-            launch_score_any(c, g, q, se, n_cand, keys, nullptr, st, pdl, overlap);
-        if (e != cudaSuccess) return e;
-    }
-    return launch_topk(a, g.B * g.Hkv, n_cand, st, pdl);
+    // the appended token's block is the last one; it is never a candidate
+    // while the recent window is non-empty
+    a.overlap = (after_step_append && recent_tokens > 0) ? 1 : 0;
+    return launch_select_any<kSelect>(a, g.G, P, st, pdl);
 }
 
 cudaError_t launch_scores_debug(const kvd_cache &c, const Geom &g, const float *q, float *ub,
                                 cudaStream_t st) {
-    return launch_score_any(c, g, q, 0, g.NB, nullptr, ub, st, false, false);
+    SelArgs a = base_args(c, g, q);
+    a.se = 0;
+    a.n = g.NB;
+    a.ub = ub;
+    return launch_select_any<kExport>(a, g.G, g.B * g.Hkv, st, false);
 }
 
 }  // namespace kvd

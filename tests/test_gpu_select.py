@@ -123,3 +123,19 @@ def test_select_repeatable_and_workspace_reuse():
     for a, b in outs[1:]:
         assert torch.equal(a, outs[0][0]) and torch.equal(b, outs[0][1])
     check_selection(outs[0][0], outs[0][1], oc, q.cpu().numpy(), 9, 4, 64, G)
+
+
+@pytest.mark.parametrize("B,Hkv,L,k_sel", [(24, 8, 3000, 9), (40, 8, 700, 3)])
+def test_select_one_cta_per_problem(B, Hkv, L, k_sel):
+    # more problems than SMs: each (sequence, KV head) is ranked by one CTA
+    # (no barriers between CTAs); fewer problems split over several CTAs
+    G = 4
+    k = seeded((B, L, Hkv, 128), 61 + B)
+    gc, oc = make_pair(kvd.F16, k, k)
+    q = _q(B, Hkv * G, 62)
+    ws = kvd.make_workspace(gc, Hkv * G)
+    sel_idx = torch.full((B, Hkv, gc.max_seq // 64), -7, dtype=torch.int32, device=dev())
+    sel_cnt = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev())
+    kvd.select_blocks(gc, q, k_sel, 4, 64, sel_idx, sel_cnt, ws)
+    torch.cuda.synchronize()
+    check_selection(sel_idx, sel_cnt, oc, q.cpu().numpy(), k_sel, 4, 64, G)
