@@ -201,14 +201,10 @@ def measured_traffic(workload, tokens):
 
 
 def launches_per_step(w, L1):
-    """Kernels one sparse step launches: append, score (only when a top-K has
-    to be found among the candidates), top-K/compaction, decode."""
-    nb = (L1 + 63) // 64
-    se = min(nb, (w.sink_tokens + 63) // 64)
-    rb = max(se, max(0, L1 - w.recent_tokens) // 64) if w.recent_tokens > 0 else nb
-    n_cand = rb - se
-    keff = min(w.k_sel, n_cand)
-    return 4 if 0 < keff < n_cand else 3
+    """Kernels one sparse step launches: append, the selection (scoring and
+    top-K in one kernel, or the fill kernel when nothing has to be ranked),
+    decode."""
+    return 3
 
 
 # --------------------------------------------------------------------------

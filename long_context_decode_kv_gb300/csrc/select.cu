@@ -453,10 +453,10 @@ __global__ void __launch_bounds__(kScoreThreads, 2) select_kernel(SelArgs a) {
     // pass over the keys, four at a time: thread t takes keys 4q..4q+3 for
     // q = t, t + 288, ...
     const int nq = (n + 3) / 4;
-    auto quad_at = [&](int q) -> uint4 {
-        return in_smem ? reinterpret_cast<const uint4 *>(s_keys)[q]
-                       : __ldcg(reinterpret_cast<const uint4 *>(kp) + q);
-    };
+    // the keys: shared memory, or L2 for a problem too large for the ring (one
+    // pointer, so every pass issues a single load per key)
+    const uint32_t *ksrc = in_smem ? s_keys : kp;
+    auto quad_at = [&](int q) -> uint4 { return reinterpret_cast<const uint4 *>(ksrc)[q]; };
     for (int q = tid; q < nq; q += kScoreThreads) {
         const uint4 w = quad_at(q);
         const uint32_t k4[4] = {w.x, w.y, w.z, w.w};
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) select_kernel(SelArgs a) {
     constexpr int kWarps = kScoreWarps + 1;
     for (int wi = warp; wi < nw; wi += kWarps) {
         const int j = 32 * wi + lane;
-        const uint32_t k = j < n ? (in_smem ? s_keys[j] : __ldcg(kp + j)) : 0u;
+        const uint32_t k = j < n ? ksrc[j] : 0u;
         const unsigned gm = __ballot_sync(kFullMask, j < n && k > T);
         const unsigned em = __ballot_sync(kFullMask, j < n && k == T);
         if (lane == 0) {

@@ -51,17 +51,11 @@ def test_single_rank_is_identity():
     assert bench.max_over_ranks(7.25, 1) == 7.25
 
 
-@pytest.mark.parametrize("name,expect", [
-    ("ctx1m_int8", 4), ("ctx128k_b8_int8", 4), ("qwen3_4b_gqa_32k_f16", 4),
-    ("tiny_512_f16", 4), ("int8_dense_2048", 3),
-])
-def test_launches_per_step(name, expect):
+@pytest.mark.parametrize("name", ["ctx1m_int8", "ctx128k_b8_int8", "tiny_512_f16",
+                                  "int8_dense_2048"])
+def test_launches_per_step(name):
+    # append, selection, decode: the selection is one kernel whether it ranks or not
     w = synth.WORKLOADS[name]
-    assert bench.launches_per_step(w, w.L + 1) == expect
-
-
-def test_all_candidates_taken_skips_scoring():
-    w = synth.TINY.with_(k_sel=1000)
     assert bench.launches_per_step(w, w.L + 1) == 3
 
 
