@@ -83,6 +83,7 @@ Geom make_geom(const kvd_cache *c, int n_heads, int len) {
 struct WsLayout {
     size_t counters, partials, keys, sel_hist, sel_ticket, sel_idx, sel_cnt, q, k_new, v_new,
         out, total;
+    int hist_rows;
     DecodePlan plan;
 };
 
@@ -103,6 +104,7 @@ WsLayout ws_layout(const kvd_cache *c, int n_heads) {
     // CTAs use them, and there are fewer of those than 2 * SMs
     const size_t sms = static_cast<size_t>(device_sm_count());
     const size_t hrows = P < 2 * sms ? P : 2 * sms;
+    w.hist_rows = static_cast<int>(hrows);
     w.sel_hist = off;
     off += align_up(hrows * select_hist_bytes());
     w.sel_ticket = off;
@@ -150,16 +152,23 @@ void forced_range(int len, int sink, int recent, int *se, int *rb) {
     *rb = r;
 }
 
-kvd_status select_impl(const kvd_cache *c, const float *q, int n_heads, int k_sel, int sink,
-                       int recent, int32_t *sel_idx, int32_t *sel_cnt, void *ws,
-                       const WsLayout &w, cudaStream_t st, bool in_step = false) {
-    const Geom g = make_geom(c, n_heads, c->len);
+SelScratch sel_scratch(void *ws, const WsLayout &w) {
     SelScratch scr;
     scr.keys = ws_at<uint32_t>(ws, w.keys);
     scr.hist = ws_at<int>(ws, w.sel_hist);
     scr.ticket = ws_at<unsigned>(ws, w.sel_ticket);
+    scr.hist_rows = w.hist_rows;
+    return scr;
+}
+
+// tok: inside a decode step, the token to append first (c->len already counts it)
+kvd_status select_impl(const kvd_cache *c, const float *q, int n_heads, int k_sel, int sink,
+                       int recent, int32_t *sel_idx, int32_t *sel_cnt, void *ws,
+                       const WsLayout &w, cudaStream_t st, const StepToken *tok = nullptr) {
+    const Geom g = make_geom(c, n_heads, c->len);
+    const SelScratch scr = sel_scratch(ws, w);
     return cuda_status(launch_select(*c, g, q, k_sel, sink, recent, sel_idx, sel_cnt, scr, st,
-                                     true, in_step));
+                                     true, tok));
 }
 
 kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float scale,
@@ -306,16 +315,24 @@ kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
     const WsLayout w = ws_layout(cache, n_heads);
     if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (launch_append(*cache, k_new, v_new, 1, st, true) != cudaSuccess) return KVD_ERR_CUDA;
-    cache->len += 1;
-    if (dense)
+    if (dense) {
+        if (launch_append(*cache, k_new, v_new, 1, st, true) != cudaSuccess) return KVD_ERR_CUDA;
+        cache->len += 1;
         return decode_impl(cache, q, n_heads, softmax_scale, nullptr, nullptr, 0, out, workspace,
                            w, st, true);
+    }
     if (!sel_idx) sel_idx = ws_at<int32_t>(workspace, w.sel_idx);
     if (!sel_cnt) sel_cnt = ws_at<int32_t>(workspace, w.sel_cnt);
+    // the selection appends the token (in its own kernel when the token's
+    // block is forced, else by an append launch just before)
+    const StepToken tok = {k_new, v_new, cache->len};
+    cache->len += 1;
     s = select_impl(cache, q, n_heads, k_sel, sink_tokens, recent_tokens, sel_idx, sel_cnt,
-                    workspace, w, st, true);
-    if (s != KVD_OK) return s;
+                    workspace, w, st, &tok);
+    if (s != KVD_OK) {
+        cache->len -= 1;
+        return s;
+    }
     const int max_sel =
         kvd_selected_count(cache->len, kBlock, k_sel, sink_tokens, recent_tokens);
     return decode_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_cnt, max_sel, out,

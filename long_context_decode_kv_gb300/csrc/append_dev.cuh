@@ -1,0 +1,94 @@
+// append_dev.cuh -- one warp appends the new tokens of one (sequence, KV head)
+// that fall in one cache block, and updates that block's key envelope.
+//
+// "Sparse Attention -- Quest-style block-selector for long-context decode
+// (#551)", S2/S3 "Fill op" and "All-KV-types composition (bug-747)": for every
+// block the new tokens touch, reduce the channel-wise min and max of the new
+// f16 keys; merge (min/max) into a block that already held tokens, overwrite
+// a block that starts in the new range.  Bounds always come from the f16 keys
+// before quantization.  "cpu-attn", Method: K and V are quantized per token
+// per head (absmax int8) at append time.
+//
+// Lane l owns channels 4l..4l+3, so every row is read as one coalesced
+// 256-byte line.
+#pragma once
+
+#include "common.cuh"
+
+namespace kvd {
+
+__device__ __forceinline__ void load_half4(const __half *p, float (&x)[4]) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+// Tokens [max(lo, len0), min(lo + 64, len0 + n_new)) of cache block blk of
+// (sequence b, KV head h), taken from k_new / v_new [B, n_new, Hkv, 128] f16.
+template <int DT>
+__device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __half *k_new,
+                                                  const __half *v_new, int n_new, int len0,
+                                                  int blk, int b, int h, int lane) {
+    const long lo = static_cast<long>(blk) * kBlock;
+    const long nlo = lo > len0 ? lo : len0;
+    const long nhi = (lo + kBlock) < (static_cast<long>(len0) + n_new) ? (lo + kBlock)
+                                                                      : (static_cast<long>(len0) + n_new);
+    const bool merge = lo < len0;
+    const size_t row0 = (static_cast<size_t>(b) * c.n_kv_heads + h) * c.max_seq;
+
+    float mn[4], mx[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { mn[j] = __int_as_float(0x7f800000); mx[j] = -mn[j]; }
+
+    for (long t = nlo; t < nhi; ++t) {
+        const size_t src = ((static_cast<size_t>(b) * n_new + (t - len0)) * c.n_kv_heads + h) *
+                               kHeadDim + 4 * lane;
+        float kx[4], vx[4];
+        load_half4(k_new + src, kx);
+        load_half4(v_new + src, vx);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { mn[j] = fminf(mn[j], kx[j]); mx[j] = fmaxf(mx[j], kx[j]); }
+        const size_t dst = (row0 + t) * kHeadDim + 4 * lane;
+        if (DT == KVD_F16) {
+            // verbatim copy of the f16 bits
+            *reinterpret_cast<uint2 *>(static_cast<__half *>(c.k) + dst) =
+                *reinterpret_cast<const uint2 *>(k_new + src);
+            *reinterpret_cast<uint2 *>(static_cast<__half *>(c.v) + dst) =
+                *reinterpret_cast<const uint2 *>(v_new + src);
+        } else {
+            float ks, vs;
+            const uint32_t kc = quantize_row_warp(kx, &ks);
+            const uint32_t vc = quantize_row_warp(vx, &vs);
+            *reinterpret_cast<uint32_t *>(static_cast<int8_t *>(c.k) + dst) = kc;
+            *reinterpret_cast<uint32_t *>(static_cast<int8_t *>(c.v) + dst) = vc;
+            if (lane == 0) {
+                c.k_scale[row0 + t] = ks;
+                c.v_scale[row0 + t] = vs;
+            }
+        }
+    }
+    // bounds row of the block: (kmin, kmax) pairs of channels 4*lane .. 4*lane+3
+    const size_t nbmax = static_cast<size_t>(c.max_seq / kBlock);
+    const size_t bidx = (((static_cast<size_t>(b) * c.n_kv_heads + h) * nbmax + blk) * kHeadDim +
+                         4 * lane) * 2;
+    __half2 *bounds = reinterpret_cast<__half2 *>(static_cast<__half *>(c.kbounds) + bidx);
+    if (merge) {
+        const uint4 old = *reinterpret_cast<const uint4 *>(bounds);
+        const __half2 *o2 = reinterpret_cast<const __half2 *>(&old);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(o2[j]);
+            mn[j] = fminf(mn[j], f.x);
+            mx[j] = fmaxf(mx[j], f.y);
+        }
+    }
+    // every value is an f16 already, so the conversions back are exact
+    uint4 w;
+    __half2 *w2 = reinterpret_cast<__half2 *>(&w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w2[j] = __floats2half2_rn(mn[j], mx[j]);
+    *reinterpret_cast<uint4 *>(bounds) = w;
+}
+
+}  // namespace kvd

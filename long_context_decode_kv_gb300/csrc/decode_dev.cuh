@@ -1,0 +1,774 @@
+// decode_dev.cuh -- device side of the split-KV decode (decode_kernel).
+// selected KV blocks (or all of them for the dense arm).
+//
+// "Sparse Attention -- Quest-style block-selector for long-context decode
+// (#551)", S3 "FA-VEC block-skip": unselected blocks are skipped before the
+// K read, the q.k product and the V accumulation; the long-context decode hot
+// path is the vector kernel, not MMA -- no tensor cores: the work is 2-4
+// multiply-adds per byte read, so HBM bandwidth bounds it.
+// "cpu-attn", Method: int8 rows with per-token scales, exact int32 q.k dots
+// on the query quantized once per head, f32 softmax and f32 accumulation.
+// "SCSA", Mechanism: an online-softmax (max, sum, accumulator) gauge over an
+// ascending sweep, merged across splits.
+//
+// CTA = (split s of the block list, sequence b, KV head g, head subgroup).
+// Warp 8 is the producer: one lane streams each listed 64-token block (K, V
+// and, for int8, both scale rows) into a ring of shared-memory stages with
+// 1-D TMA bulk copies completing on an mbarrier.  Warps 0..7 form two
+// consumer groups that take alternate blocks (so twice as many warps hide
+// each other's latencies); within a group warp w owns tokens 16w..16w+15 of
+// the block and keeps its own online-softmax state for the CTA's query heads,
+// so no CTA-wide barrier is needed per block.  PV runs on packed f32x2 FMAs.
+// At the end the 8 warp states merge in shared memory and the CTA writes a
+// partial (m, l, acc[128]) per head; the last CTA of the problem to arrive
+// merges all splits.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvd {
+namespace {
+
+
+constexpr int kGroups = 2;                                 // consumer groups
+constexpr int kWarpsPerGroup = 4;
+constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;   // warps 0..7
+constexpr int kTokensPerWarp = kBlock / kWarpsPerGroup;    // 16
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+// Partial rows: m, l, two pad words, acc[128] (acc 16-byte aligned).
+constexpr int kPartStride = kHeadDim + 4;
+constexpr int kAccOff = 4;
+constexpr int kMaxSplits = 256;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int DT>
+struct Tile;
+template <>
+struct Tile<KVD_INT8> {
+    static constexpr int kRowBytes = kHeadDim;                        // int8 codes
+    static constexpr int kKBytes = kBlock * kRowBytes;                // 8192
+    static constexpr int kStageBytes = 2 * kKBytes + 2 * kBlock * 4;  // + both scale rows
+    static constexpr int kStages = 6;   // a multiple of kGroups
+    static constexpr int kMinCtas = 2;
+};
+template <>
+struct Tile<KVD_F16> {
+    static constexpr int kRowBytes = 2 * kHeadDim;                    // f16
+    static constexpr int kKBytes = kBlock * kRowBytes;                // 16384
+    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kStages = 4;   // a multiple of kGroups
+    static constexpr int kMinCtas = 1;
+};
+
+struct DecodeArgs {
+    const void *k, *v;
+    const float *k_scale, *v_scale;
+    const float *q;
+    float *out;
+    const int32_t *sel_idx, *sel_cnt;
+    float *partials;
+    uint32_t *counters;
+    int32_t *dev_status;
+    int Hkv, H, G, max_seq, nbmax, len, NB, splits, subgroups;
+    float scale_log2;  // softmax_scale * log2(e): logits live in base 2
+    int early_q;       // q is complete before the upstream kernels finish
+};
+
+template <int DT, int GC>
+struct SmemLayout {
+    static constexpr int kStageBytes = Tile<DT>::kStageBytes;
+    static constexpr int kStages = Tile<DT>::kStages;
+    static constexpr int kStagesOff = 0;
+    static constexpr int kRing = kStages * kStageBytes;
+    // after the loop the ring holds the warp merge, then the split weights
+    static constexpr int kMergeBytes = kConsumerWarps * GC * kPartStride * 4;
+    static constexpr int kWeightBytes = kMaxSplits * 4 * 4;
+    static constexpr int kScratch = kMergeBytes > kWeightBytes ? kMergeBytes : kWeightBytes;
+    static constexpr int kBarOff = (kRing > kScratch ? kRing : kScratch);
+    static constexpr int kFullOff = kBarOff;
+    static constexpr int kEmptyOff = kFullOff + 8 * kStages;
+    static constexpr int kBlkOff = kEmptyOff + 8 * kStages;
+    static constexpr int kQOff = (kBlkOff + 4 * kStages + 15) / 16 * 16;
+    static constexpr int kQBytes = GC * kHeadDim * 4;  // f32 q (f16 cache) or codes
+    static constexpr int kCoefOff = kQOff + kQBytes;
+    static constexpr int kPwOff = kCoefOff + 16;
+    // [warp][16 tokens][4 heads] pairs (p, p)
+    static constexpr int kPwBytes = kConsumerWarps * kTokensPerWarp * 4 * 2 * 4;
+    static constexpr int kLOff = kPwOff + kPwBytes;  // split merge: L per head
+    static constexpr int kFlagOff = kLOff + 16;
+    static constexpr int kTotal = kFlagOff + 16;
+};
+
+// ----------------------------------------------------------------------------
+// int32 reductions over the 4 quarter lanes (lane bits 0..1) returning to each
+// lane the total of head (c * GC) / 4.
+template <int GC>
+__device__ __forceinline__ int reduce4_scatter(int (&v)[GC], int c) {
+    if constexpr (GC == 4) {
+        const bool up = (c & 2) != 0;
+        int k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+        const int s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
+        k0 += __shfl_xor_sync(kFull, s0, 2);
+        k1 += __shfl_xor_sync(kFull, s1, 2);
+        const bool lo = (c & 1) != 0;
+        int k = lo ? k1 : k0;
+        k += __shfl_xor_sync(kFull, lo ? k0 : k1, 1);
+        return k;
+    } else if constexpr (GC == 2) {
+        const bool up = (c & 2) != 0;
+        int k = up ? v[1] : v[0];
+        k += __shfl_xor_sync(kFull, up ? v[0] : v[1], 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    } else {
+        int k = v[0];
+        k += __shfl_xor_sync(kFull, k, 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    }
+}
+
+// f32 version over the 8 eighth lanes (lane bits 0..2): head (e * GC) / 8.
+template <int GC>
+__device__ __forceinline__ float reduce8_scatter(float (&v)[GC], int e) {
+    if constexpr (GC == 4) {
+        const bool up = (e & 4) != 0;
+        float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+        const float s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
+        k0 += __shfl_xor_sync(kFull, s0, 4);
+        k1 += __shfl_xor_sync(kFull, s1, 4);
+        const bool mid = (e & 2) != 0;
+        float k = mid ? k1 : k0;
+        k += __shfl_xor_sync(kFull, mid ? k0 : k1, 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    } else if constexpr (GC == 2) {
+        const bool up = (e & 4) != 0;
+        float k = up ? v[1] : v[0];
+        k += __shfl_xor_sync(kFull, up ? v[0] : v[1], 4);
+        k += __shfl_xor_sync(kFull, k, 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    } else {
+        float k = v[0];
+        k += __shfl_xor_sync(kFull, k, 4);
+        k += __shfl_xor_sync(kFull, k, 2);
+        k += __shfl_xor_sync(kFull, k, 1);
+        return k;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Query prologue, one warp per head hh < GC of the CTA.
+//  int8: the row is quantized like a cache row (absmax, per head, once); the
+//        packed codes go to q_s ([GC][32] words) and the logit coefficient
+//        q_scale * softmax_scale * log2(e) to coef[hh].
+//  f16:  q * softmax_scale * log2(e) in f32 goes to q_s ([GC][128] floats).
+template <int DT, int GC>
+__device__ __forceinline__ void load_query(const DecodeArgs &a, int b, int h0, int warp, int lane,
+                                           uint32_t *q_s, float *coef, int8_t *q_codes_out,
+                                           float *q_scales_out) {
+    if (warp >= GC) return;
+    const int hq = h0 + warp;
+    const float4 x4 = *reinterpret_cast<const float4 *>(
+        a.q + (static_cast<size_t>(b) * a.H + hq) * kHeadDim + 4 * lane);
+    const float x[4] = {x4.x, x4.y, x4.z, x4.w};
+    if constexpr (DT == KVD_INT8) {
+        float s;
+        const uint32_t packed = quantize_row_warp(x, &s);
+        q_s[warp * 32 + lane] = packed;
+        if (lane == 0) coef[warp] = s * a.scale_log2;
+        if (q_codes_out) {
+            *reinterpret_cast<uint32_t *>(q_codes_out +
+                                          (static_cast<size_t>(b) * a.H + hq) * kHeadDim +
+                                          4 * lane) = packed;
+            if (lane == 0) q_scales_out[static_cast<size_t>(b) * a.H + hq] = s;
+        }
+    } else {
+        float *qf = reinterpret_cast<float *>(q_s) + warp * kHeadDim + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qf[j] = x[j] * a.scale_log2;
+    }
+}
+
+// int8 QK mapping: lane = 4 t + c (t: token slot 0..7, c: quarter 0..3 of the
+// 128 channels).  The lane reads 16-byte chunks 2c and 2c+1 of its token row,
+// odd tokens in swapped order so that the 8 lanes of each quarter-warp hit
+// distinct banks.  qr holds the matching query words in that order.
+template <int GC>
+struct QRegsI8 {
+    uint32_t w[GC][8];
+};
+
+template <int GC>
+__device__ __forceinline__ void load_qregs_i8(const uint32_t *q_s, int t, int c, QRegsI8<GC> &r) {
+#pragma unroll
+    for (int h = 0; h < GC; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int chunk = 2 * c + (i ^ (t & 1));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r.w[h][4 * i + j] = q_s[h * 32 + 4 * chunk + j];
+        }
+}
+
+// Exact int32 dot of one token row with the query of head (c*GC)/4.
+template <int GC>
+__device__ __forceinline__ int qk_int8_row(const int8_t *row, const QRegsI8<GC> &r, int t, int c) {
+    const uint4 ka = *reinterpret_cast<const uint4 *>(row + 16 * (2 * c + (t & 1)));
+    const uint4 kb = *reinterpret_cast<const uint4 *>(row + 16 * (2 * c + 1 - (t & 1)));
+    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+    int d[GC];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        int s = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            s = __dp4a(static_cast<int>(kw[j]), static_cast<int>(r.w[h][j]), s);
+        d[h] = s;
+    }
+    return reduce4_scatter<GC>(d, c);
+}
+
+// f16 QK mapping: lane = 8 t4 + e (t4: token slot 0..3 per pass, e: eighth
+// 0..7 of the channels).  The lane reads chunks 2e and 2e+1 (8 halves each) of
+// its token row, lanes e >= 4 in swapped order (bank-conflict free).  The
+// query pairs are held in that order.
+template <int GC>
+struct QRegsF16 {
+    float2 f[GC][8];
+};
+
+template <int GC>
+__device__ __forceinline__ void load_qregs_f16(const uint32_t *q_s, int e, QRegsF16<GC> &r) {
+    const float *qf = reinterpret_cast<const float *>(q_s);
+#pragma unroll
+    for (int h = 0; h < GC; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int chunk = 2 * e + (i ^ (e >> 2));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                r.f[h][4 * i + j] = make_float2(qf[h * kHeadDim + 8 * chunk + 2 * j],
+                                                qf[h * kHeadDim + 8 * chunk + 2 * j + 1]);
+        }
+}
+
+template <int GC>
+__device__ __forceinline__ float qk_f16_row(const __half *row, const QRegsF16<GC> &r, int e) {
+    const uint4 ka = *reinterpret_cast<const uint4 *>(row + 8 * (2 * e + (e >> 2)));
+    const uint4 kb = *reinterpret_cast<const uint4 *>(row + 8 * (2 * e + 1 - (e >> 2)));
+    float2 kf[8];
+    const __half2 *ha = reinterpret_cast<const __half2 *>(&ka);
+    const __half2 *hb = reinterpret_cast<const __half2 *>(&kb);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        kf[i] = __half22float2(ha[i]);
+        kf[4 + i] = __half22float2(hb[i]);
+    }
+    float d[GC];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        float2 s = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s = __ffma2_rn(r.f[h][j], kf[j], s);
+        d[h] = s.x + s.y;
+    }
+    return reduce8_scatter<GC>(d, e);
+}
+
+// Running softmax state of one consumer warp for the CTA's GC heads.
+template <int GC>
+struct WarpState {
+    float m;             // running max (base-2 logits) of this lane's QK head
+    float l;             // this lane's share of the running sum
+    float2 acc[GC][2];   // channels 4*lane .. 4*lane+3 of every head, as pairs
+};
+
+template <int GC>
+__device__ __forceinline__ void rescale(WarpState<GC> &st, float alpha_own, int lanes_per_head) {
+    if (__any_sync(kFull, alpha_own != 1.0f)) {
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            const float al = __shfl_sync(kFull, alpha_own, h * lanes_per_head);
+            const float2 a2 = make_float2(al, al);
+            st.acc[h][0] = __fmul2_rn(st.acc[h][0], a2);
+            st.acc[h][1] = __fmul2_rn(st.acc[h][1], a2);
+        }
+    }
+}
+
+// acc[h] += p[h] * v (4 channels) for one token; pw_tok holds (p, p) pairs.
+template <int GC>
+__device__ __forceinline__ void pv_token(WarpState<GC> &st, const float *pw_tok, float2 v01,
+                                         float2 v23) {
+    if constexpr (GC >= 2) {
+        const float4 p01 = *reinterpret_cast<const float4 *>(pw_tok);
+        const float2 pa = make_float2(p01.x, p01.y), pb = make_float2(p01.z, p01.w);
+        st.acc[0][0] = __ffma2_rn(v01, pa, st.acc[0][0]);
+        st.acc[0][1] = __ffma2_rn(v23, pa, st.acc[0][1]);
+        st.acc[1][0] = __ffma2_rn(v01, pb, st.acc[1][0]);
+        st.acc[1][1] = __ffma2_rn(v23, pb, st.acc[1][1]);
+        if constexpr (GC == 4) {
+            const float4 p23 = *reinterpret_cast<const float4 *>(pw_tok + 4);
+            const float2 pc = make_float2(p23.x, p23.y), pd = make_float2(p23.z, p23.w);
+            st.acc[2][0] = __ffma2_rn(v01, pc, st.acc[2][0]);
+            st.acc[2][1] = __ffma2_rn(v23, pc, st.acc[2][1]);
+            st.acc[3][0] = __ffma2_rn(v01, pd, st.acc[3][0]);
+            st.acc[3][1] = __ffma2_rn(v23, pd, st.acc[3][1]);
+        }
+    } else {
+        const float2 pa = *reinterpret_cast<const float2 *>(pw_tok);
+        st.acc[0][0] = __ffma2_rn(v01, pa, st.acc[0][0]);
+        st.acc[0][1] = __ffma2_rn(v23, pa, st.acc[0][1]);
+    }
+}
+
+// Four signed bytes -> two exact float pairs (see s8x4_to_f32 in common.cuh).
+__device__ __forceinline__ void s8x4_to_f32x2(uint32_t w, float2 &f01, float2 &f23) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+    f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651))),
+                     bias);
+    f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653))),
+                     bias);
+}
+
+// One stage (64-token block) for one consumer warp (wg = its index in the
+// group), int8 cache: two QK passes of 8 tokens, one softmax update, 16
+// tokens of PV.
+template <int GC>
+__device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, const float *coef,
+                                             const QRegsI8<GC> &qr, float *pw, int wg, int lane,
+                                             WarpState<GC> &st) {
+    const int8_t *Ks = reinterpret_cast<const int8_t *>(stage);
+    const int8_t *Vs = Ks + Tile<KVD_INT8>::kKBytes;
+    const float *ksc = reinterpret_cast<const float *>(stage + 2 * Tile<KVD_INT8>::kKBytes);
+    const float *vsc = ksc + kBlock;
+    const int t = lane >> 2, c = lane & 3;
+    const int tok0 = kTokensPerWarp * wg + t, tok1 = tok0 + 8;
+    const int hq = (c * GC) >> 2;
+    const float ninf = -__int_as_float(0x7f800000);
+    const int d0 = qk_int8_row<GC>(Ks + tok0 * kHeadDim, qr, t, c);
+    const int d1 = qk_int8_row<GC>(Ks + tok1 * kHeadDim, qr, t, c);
+    const float cf = coef[hq];
+    const float x0 = tok0 < n_valid ? static_cast<float>(d0) * cf * ksc[tok0] : ninf;
+    const float x1 = tok1 < n_valid ? static_cast<float>(d1) * cf * ksc[tok1] : ninf;
+    float bm = fmaxf(x0, x1);
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+    const float m_new = fmaxf(st.m, bm);
+    const float alpha = exp2f(st.m - m_new);
+    const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
+    st.l = st.l * alpha + (p0 + p1);
+    st.m = m_new;
+    constexpr int lph = 4 / GC;  // lanes per head among the quarters
+    if ((c % lph) == 0) {
+        const float w0 = tok0 < n_valid ? p0 * vsc[tok0] : 0.0f;
+        const float w1 = tok1 < n_valid ? p1 * vsc[tok1] : 0.0f;
+        *reinterpret_cast<float2 *>(pw + (t * 4 + hq) * 2) = make_float2(w0, w0);
+        *reinterpret_cast<float2 *>(pw + ((t + 8) * 4 + hq) * 2) = make_float2(w1, w1);
+    }
+    rescale<GC>(st, alpha, lph);
+    __syncwarp();
+    const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
+    const int8_t *vrow = Vs + kTokensPerWarp * wg * kHeadDim + 4 * lane;
+    if (nt == kTokensPerWarp) {
+#pragma unroll
+        for (int t2 = 0; t2 < kTokensPerWarp; ++t2) {
+            float2 f01, f23;
+            s8x4_to_f32x2(*reinterpret_cast<const uint32_t *>(vrow + t2 * kHeadDim), f01, f23);
+            pv_token<GC>(st, pw + t2 * 8, f01, f23);
+        }
+    } else {
+        for (int t2 = 0; t2 < nt; ++t2) {
+            float2 f01, f23;
+            s8x4_to_f32x2(*reinterpret_cast<const uint32_t *>(vrow + t2 * kHeadDim), f01, f23);
+            pv_token<GC>(st, pw + t2 * 8, f01, f23);
+        }
+    }
+}
+
+// One stage for one consumer warp (wg = its index in the group), f16 cache:
+// four QK passes of 4 tokens.
+template <int GC>
+__device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
+                                            const QRegsF16<GC> &qr, float *pw, int wg,
+                                            int lane, WarpState<GC> &st) {
+    const __half *Ks = reinterpret_cast<const __half *>(stage);
+    const __half *Vs = Ks + kBlock * kHeadDim;
+    const int t4 = lane >> 3, e = lane & 7;
+    const int hq = (e * GC) >> 3;
+    const float ninf = -__int_as_float(0x7f800000);
+    float x[4];
+#pragma unroll
+    for (int ps = 0; ps < 4; ++ps) {
+        const int tok = kTokensPerWarp * wg + 4 * ps + t4;
+        const float d = qk_f16_row<GC>(Ks + tok * kHeadDim, qr, e);
+        x[ps] = tok < n_valid ? d : ninf;
+    }
+    float bm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+    const float m_new = fmaxf(st.m, bm);
+    const float alpha = exp2f(st.m - m_new);
+    float p[4];
+#pragma unroll
+    for (int ps = 0; ps < 4; ++ps) p[ps] = exp2f(x[ps] - m_new);
+    st.l = st.l * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+    st.m = m_new;
+    constexpr int lph = 8 / GC;
+    if ((e % lph) == 0) {
+#pragma unroll
+        for (int ps = 0; ps < 4; ++ps)
+            *reinterpret_cast<float2 *>(pw + ((4 * ps + t4) * 4 + hq) * 2) =
+                make_float2(p[ps], p[ps]);
+    }
+    rescale<GC>(st, alpha, lph);
+    __syncwarp();
+    const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
+    const __half *vrow = Vs + kTokensPerWarp * wg * kHeadDim + 4 * lane;
+#pragma unroll 4
+    for (int t2 = 0; t2 < nt; ++t2) {
+        const uint2 vw = *reinterpret_cast<const uint2 *>(vrow + t2 * kHeadDim);
+        const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
+        const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
+        pv_token<GC>(st, pw + t2 * 8, v01, v23);
+    }
+}
+
+template <int DT, int GC, bool DENSE>
+__device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *smem) {
+    using SL = SmemLayout<DT, GC>;
+    using TL = Tile<DT>;
+    static_assert(TL::kStages % kGroups == 0, "stages must split evenly over the groups");
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + SL::kFullOff);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + SL::kEmptyOff);
+    int *stage_blk = reinterpret_cast<int *>(smem + SL::kBlkOff);
+    uint32_t *q_s = reinterpret_cast<uint32_t *>(smem + SL::kQOff);
+    float *coef = reinterpret_cast<float *>(smem + SL::kCoefOff);
+    float *pw_all = reinterpret_cast<float *>(smem + SL::kPwOff);
+    float *l_tot = reinterpret_cast<float *>(smem + SL::kLOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SL::kFlagOff);
+    int *last_flag = reinterpret_cast<int *>(smem + SL::kFlagOff + 4);
+    int *issued_s = reinterpret_cast<int *>(smem + SL::kFlagOff + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // prob = ((b * Hkv) + g) * subgroups + sub
+    const int sub = prob % a.subgroups;
+    const int bg = prob / a.subgroups;  // b * Hkv + g
+    const int b = bg / a.Hkv, g = bg % a.Hkv;
+    const int h0 = g * a.G + sub * GC;
+
+    if (tid == 0) {
+        for (int i = 0; i < TL::kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kWarpsPerGroup);
+        }
+        *abort_flag = 0;
+        *issued_s = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // Inside a decode step the query was written before the step's first
+    // kernel, so it may be read while the selection is still finishing.
+    if (a.early_q) load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
+    pdl_wait();  // upstream kernels (append, select) are complete past here
+    if (!a.early_q) load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
+    int cnt = DENSE ? a.NB : a.sel_cnt[bg];
+    cnt = max(0, min(cnt, a.NB));
+    const int beg = static_cast<int>((static_cast<long long>(split) * cnt) / a.splits);
+    const int end = static_cast<int>((static_cast<long long>(split + 1) * cnt) / a.splits);
+    const int n = end - beg;
+    __syncthreads();
+    pdl_launch_dependents();
+
+    const size_t row0 = static_cast<size_t>(bg) * a.max_seq;  // first token row of (b, g)
+    WarpState<GC> st;
+    st.m = kNegBig;
+    st.l = 0.0f;
+#pragma unroll
+    for (int h = 0; h < GC; ++h) st.acc[h][0] = st.acc[h][1] = make_float2(0.0f, 0.0f);
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        const uint64_t pol = l2_policy_evict_first();
+        const int32_t *list = a.sel_idx + static_cast<size_t>(bg) * a.nbmax + beg;
+        int issued = 0;
+        bool ok = true;
+        for (int i0 = 0; i0 < n && ok; i0 += 32) {
+            int mine = 0;
+            if (i0 + lane < n) mine = DENSE ? beg + i0 + lane : list[i0 + lane];
+            const int m = min(32, n - i0);
+            for (int j = 0; j < m; ++j) {
+                const int blk = __shfl_sync(kFull, mine, j);
+                const int i = i0 + j;
+                const int s = i % TL::kStages;
+                if (lane == 0) {
+                    if (i >= TL::kStages)
+                        ok = mbar_wait(&empty[s], ((i / TL::kStages) - 1) & 1, abort_flag);
+                    if (ok) {
+                        if (blk >= 0 && blk < a.NB) {
+                            stage_blk[s] = blk;
+                            uint8_t *dst = smem + SL::kStagesOff + s * TL::kStageBytes;
+                            const size_t r = row0 + static_cast<size_t>(blk) * kBlock;
+                            mbar_arrive_expect_tx(&full[s], TL::kStageBytes);
+                            tma_load_1d(dst, static_cast<const uint8_t *>(a.k) + r * TL::kRowBytes,
+                                        TL::kKBytes, &full[s], pol);
+                            tma_load_1d(dst + TL::kKBytes,
+                                        static_cast<const uint8_t *>(a.v) + r * TL::kRowBytes,
+                                        TL::kKBytes, &full[s], pol);
+                            if constexpr (DT == KVD_INT8) {
+                                tma_load_1d(dst + 2 * TL::kKBytes, a.k_scale + r, kBlock * 4,
+                                            &full[s], pol);
+                                tma_load_1d(dst + 2 * TL::kKBytes + kBlock * 4, a.v_scale + r,
+                                            kBlock * 4, &full[s], pol);
+                            }
+                        } else {
+                            // an id outside the cache: report it, skip the block
+                            stage_blk[s] = -1;
+                            report_status(a.dev_status, KVD_ERR_INVALID);
+                            mbar_arrive(&full[s]);
+                        }
+                        issued = i + 1;
+                    } else {
+                        *abort_flag = 1;
+                        report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                    }
+                }
+                ok = __shfl_sync(kFull, ok, 0);
+                if (!ok) break;
+            }
+        }
+        if (lane == 0) *issued_s = issued;
+    } else {
+        // ------------------------------------------------------ consumers
+        float *pw = pw_all + warp * (kTokensPerWarp * 4 * 2);
+        const int group = warp / kWarpsPerGroup, wg = warp % kWarpsPerGroup;
+        if constexpr (DT == KVD_INT8) {
+            QRegsI8<GC> qr;
+            load_qregs_i8<GC>(q_s, lane >> 2, lane & 3, qr);
+            for (int i = group; i < n; i += kGroups) {
+                const int s = i % TL::kStages;
+                const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
+                if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                const int blk = stage_blk[s];
+                if (blk >= 0) {
+                    const int n_valid = min(kBlock, a.len - blk * kBlock);
+                    consume_int8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, coef,
+                                     qr, pw, wg, lane, st);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+        } else {
+            QRegsF16<GC> qr;
+            load_qregs_f16<GC>(q_s, lane & 7, qr);
+            for (int i = group; i < n; i += kGroups) {
+                const int s = i % TL::kStages;
+                const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
+                if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                const int blk = stage_blk[s];
+                if (blk >= 0) {
+                    const int n_valid = min(kBlock, a.len - blk * kBlock);
+                    consume_f16<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, qr, pw,
+                                    wg, lane, st);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+        }
+        // per-warp totals: l summed over the lanes of each head
+        if constexpr (DT == KVD_INT8) {
+            st.l += __shfl_xor_sync(kFull, st.l, 4);
+            st.l += __shfl_xor_sync(kFull, st.l, 8);
+            st.l += __shfl_xor_sync(kFull, st.l, 16);
+        } else {
+            st.l += __shfl_xor_sync(kFull, st.l, 8);
+            st.l += __shfl_xor_sync(kFull, st.l, 16);
+        }
+    }
+    __syncthreads();  // (A) every stage consumed: the ring becomes scratch
+    const bool aborted = *abort_flag != 0;
+    if (!aborted && warp < kConsumerWarps) {
+        float *mg = reinterpret_cast<float *>(smem + SL::kStagesOff);
+        constexpr int lph = (DT == KVD_INT8 ? 4 : 8) / GC;
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            float *row = mg + (warp * GC + h) * kPartStride;
+            if (lane == h * lph) {
+                row[0] = st.m;
+                row[1] = st.l;
+            }
+            *reinterpret_cast<float4 *>(row + kAccOff + 4 * lane) =
+                make_float4(st.acc[h][0].x, st.acc[h][0].y, st.acc[h][1].x, st.acc[h][1].y);
+        }
+    }
+    __syncthreads();  // (B) merge area written
+    if (aborted) {
+        // wind down: wait (bounded) for the copies still landing in the ring
+        if (warp == kConsumerWarps && lane == 0) {
+            const int issued = *issued_s;
+            volatile int never = 0;
+            for (int i = max(0, issued - TL::kStages); i < issued; ++i)
+                (void)mbar_wait(&full[i % TL::kStages], (i / TL::kStages) & 1, &never);
+        }
+        return;
+    }
+
+    // ---- CTA merge of the warp states: thread (h, 4 channels)
+    const float *mg = reinterpret_cast<const float *>(smem + SL::kStagesOff);
+    const bool single = a.splits == 1;
+    float *part = a.partials + (static_cast<size_t>(prob) * a.splits + split) * GC * kPartStride;
+    if (tid < GC * 32) {
+        const int h = tid >> 5, d4 = tid & 31;
+        float M = kNegBig;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg[(w * GC + h) * kPartStride]);
+        float L = 0.0f;
+        float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float *row = mg + (w * GC + h) * kPartStride;
+            const float sc = exp2f(row[0] - M);
+            L = fmaf(sc, row[1], L);
+            const float4 r4 = *reinterpret_cast<const float4 *>(row + kAccOff + 4 * d4);
+            A.x = fmaf(sc, r4.x, A.x);
+            A.y = fmaf(sc, r4.y, A.y);
+            A.z = fmaf(sc, r4.z, A.z);
+            A.w = fmaf(sc, r4.w, A.w);
+        }
+        if (single) {
+            const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+            *reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(b) * a.H + h0 + h) *
+                                                    kHeadDim + 4 * d4) =
+                make_float4(A.x * inv, A.y * inv, A.z * inv, A.w * inv);
+        } else {
+            float *pr = part + h * kPartStride;
+            if (d4 == 0) {
+                pr[0] = M;
+                pr[1] = L;
+            }
+            *reinterpret_cast<float4 *>(pr + kAccOff + 4 * d4) = A;
+        }
+    }
+    if (single) return;
+
+    // ---- the last CTA of this problem to arrive merges all splits
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&a.counters[prob], 1u);
+        *last_flag = prev == static_cast<unsigned>(a.splits - 1);
+    }
+    __syncthreads();
+    if (!*last_flag) return;
+    __threadfence();
+    const int S = a.splits;
+    const float *p0 = a.partials + static_cast<size_t>(prob) * S * GC * kPartStride;
+    float *ms = reinterpret_cast<float *>(smem + SL::kStagesOff);  // [S][GC] maxima -> weights
+    for (int i = tid; i < S * GC; i += kThreads)
+        ms[i] = __ldcg(p0 + static_cast<size_t>(i) * kPartStride);
+    __syncthreads();
+    if (warp < GC) {
+        const int h = warp;
+        float M = kNegBig;
+        for (int s = lane; s < S; s += 32) M = fmaxf(M, ms[s * GC + h]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        float L = 0.0f;
+        for (int s = lane; s < S; s += 32) {
+            const float wgt = exp2f(ms[s * GC + h] - M);
+            ms[s * GC + h] = wgt;
+            L = fmaf(wgt, __ldcg(p0 + static_cast<size_t>(s * GC + h) * kPartStride + 1), L);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+        if (lane == 0) l_tot[h] = L;
+    }
+    __syncthreads();
+    if (tid < GC * 32) {
+        const int h = tid >> 5, d4 = tid & 31;
+        const float *col = p0 + h * kPartStride + kAccOff + 4 * d4;
+        float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        int s = 0;
+        for (; s + 8 <= S; s += 8) {
+            float4 r[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                r[u] = __ldcg(reinterpret_cast<const float4 *>(
+                    col + static_cast<size_t>(s + u) * GC * kPartStride));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float wgt = ms[(s + u) * GC + h];
+                A.x = fmaf(wgt, r[u].x, A.x);
+                A.y = fmaf(wgt, r[u].y, A.y);
+                A.z = fmaf(wgt, r[u].z, A.z);
+                A.w = fmaf(wgt, r[u].w, A.w);
+            }
+        }
+        for (; s < S; ++s) {
+            const float4 r = __ldcg(reinterpret_cast<const float4 *>(
+                col + static_cast<size_t>(s) * GC * kPartStride));
+            const float wgt = ms[s * GC + h];
+            A.x = fmaf(wgt, r.x, A.x);
+            A.y = fmaf(wgt, r.y, A.y);
+            A.z = fmaf(wgt, r.z, A.z);
+            A.w = fmaf(wgt, r.w, A.w);
+        }
+        const float L = l_tot[h];
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        *reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(b) * a.H + h0 + h) * kHeadDim +
+                                    4 * d4) = make_float4(A.x * inv, A.y * inv, A.z * inv,
+                                                          A.w * inv);
+    }
+    if (tid == 0) a.counters[prob] = 0u;  // leave the counter ready for the next call
+}
+
+DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan &p,
+                            const float *q, float scale, const int32_t *sel_idx,
+                            const int32_t *sel_cnt, float *out, float *partials,
+                            uint32_t *counters, bool early_q) {
+    DecodeArgs a = {};
+    a.early_q = early_q ? 1 : 0;
+    a.k = c.k;
+    a.v = c.v;
+    a.k_scale = c.k_scale;
+    a.v_scale = c.v_scale;
+    a.q = q;
+    a.out = out;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.partials = partials;
+    a.counters = counters;
+    a.dev_status = c.dev_status;
+    a.Hkv = g.Hkv;
+    a.H = g.H;
+    a.G = g.G;
+    a.max_seq = g.max_seq;
+    a.nbmax = g.nbmax;
+    a.len = g.len;
+    a.NB = g.NB;
+    a.splits = p.splits;
+    a.subgroups = p.subgroups;
+    a.scale_log2 = scale * kLog2e;
+    return a;
+}
+
+}  // namespace
+}  // namespace kvd

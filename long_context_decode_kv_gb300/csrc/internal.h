@@ -38,17 +38,26 @@ cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_n
 // between calls, and every completed call leaves them zero).
 struct SelScratch {
     uint32_t *keys;    // [B*Hkv][round_up(candidates, 4)] keys
-    int *hist;         // [min(B*Hkv, 2*SMs)][select_hist_bytes()/4] top-digit histograms
-    unsigned *ticket;  // [min(B*Hkv, 2*SMs)] arrival counters
+    int *hist;         // [hist_rows][select_hist_bytes()/4] top-digit histograms
+    unsigned *ticket;  // [hist_rows] arrival counters
+    int hist_rows;     // problems that may split over several CTAs need a row each
 };
 size_t select_hist_bytes();
 
-// after_step_append: launched right after the one-token append of a decode
-// step (so scoring may overlap that append when the token's block is forced).
+// The one token a decode step appends ([B, 1, Hkv, 128] f16 each) and the
+// cache length before it.
+struct StepToken {
+    const void *k_new, *v_new;
+    int len0;
+};
+
+// tok: inside a decode step, the token to append before the selection (g and
+// c.len then describe the cache after it); the selection kernel appends it
+// when the token's block is forced, else a separate append launch does.
 cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int k_sel,
                           int sink_tokens, int recent_tokens, int32_t *sel_idx,
                           int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st, bool pdl,
-                          bool after_step_append);
+                          const StepToken *tok);
 
 cudaError_t launch_scores_debug(const kvd_cache &c, const Geom &g, const float *q, float *ub,
                                 cudaStream_t st);

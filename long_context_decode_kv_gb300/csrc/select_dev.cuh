@@ -1,0 +1,614 @@
+// select_dev.cuh -- device side of the Quest block selection: block bounds,
+// GQA max, top-K with the sink and recent blocks forced in.  Used by
+// select_kernel (select.cu) and by the scoring items of the persistent step
+// kernel (step.cu).
+//
+// "Sparse Attention -- Quest-style block-selector for long-context decode
+// (#551)":
+//  - Method, "Per-query upper bound": UB_h(j) = sum_d max(q_d kmin_j[d],
+//    q_d kmax_j[d]) (kmax where q_d > 0, kmin where q_d < 0);
+//  - S2/S3 selector op: the group's query heads reduce to one bound per
+//    (KV head, block) by a max, so the whole group shares one block set;
+//  - Method, "Top-K block selection": the top-K_SEL blocks by bound plus the
+//    recent window and the attention-sink block.
+// Equal bounds go to the lower block index; the top-K budget counts only the
+// blocks that are not forced.
+//
+// select_kernel: the candidate blocks of a problem (sequence, KV head) are
+// split over X CTAs.  Each CTA streams the bounds (512 B per block) of its
+// range through a TMA ring in shared memory, turns every block's group bound
+// into an order-preserving u32 key (written to global scratch), and
+// histograms the keys' top 11 bits in shared memory.  It adds that
+// histogram into the problem's global one and takes a ticket; the last CTA
+// of the problem to arrive finishes the selection alone: the keff-th largest
+// key T by radix select (the top digit from the global histogram, then bits
+// 20-10 and 9-0 over the problem's keys, held in shared memory), then the
+// ascending list written warp by warp in index order.  No CTA waits for
+// another, so problems finish while others are still being scored.
+#pragma once
+
+#include "append_dev.cuh"
+#include "common.cuh"
+#include "internal.h"
+
+namespace kvd {
+namespace {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+constexpr int kScoreWarps = 16;                      // consumers; warp 16 produces
+constexpr int kScoreThreads = 32 * (kScoreWarps + 1);
+constexpr int kConsumerThreads = 32 * kScoreWarps;
+constexpr int kScoreSlots = 4;                       // blocks per warp per stage (8 lanes each)
+constexpr int kStageBlocks = kScoreWarps * kScoreSlots;  // 64
+constexpr int kBoundRowBytes = kHeadDim * 2 * 2;      // (kmin, kmax) f16 pairs: 512 B
+constexpr int kScoreStages = 6;
+constexpr int kScoreStageBytes = kStageBlocks * kBoundRowBytes;  // 32 KiB
+
+constexpr int kMaxSelectBlocks = 49152;
+constexpr int kMaxCtasPerProblem = 1024;
+
+// Radix digits of a key, from the top: bits 31-21, 20-10, 9-0.
+constexpr int kShift1 = 21, kShift2 = 10;
+constexpr int kH1 = 1 << 11, kH2 = 1 << 11, kH3 = 1 << 10;
+
+enum TopkMode { kTakeNone = 0, kTakeAll = 1, kTakeTopK = 2 };
+enum SelMode { kExport = 0, kSelect = 1 };
+
+// ------------------------------------------------------ bound math ---
+// Scoring lane layout: 16 lanes per block; lane e (0..15) of a block holds
+// channels [8e, 8e+8), as (kmin, kmax) pairs.  A warp scores two blocks at a
+// time.  Per channel and head the bound's term is one packed FMA:
+//   max(q*kmin, q*kmax) = min(q,0)*kmin + max(q,0)*kmax   (exact: the other
+// product is a signed zero), accumulated as a pair and summed at the end.
+
+// The 16-byte chunk order of lane e: lanes 4..7 (mod 8) take their two
+// chunks swapped so that the 8 lanes of a quarter-warp hit distinct banks.
+__device__ __forceinline__ int chunk_swap(int e) { return (e >> 2) & 1; }
+
+// Query pairs (min(q,0), max(q,0)) of this lane's 8 channels, in the order
+// the lane reads its bound pairs.
+template <int NH>
+__device__ __forceinline__ void load_qpairs(const float *q_s, int h0, int e,
+                                            float2 (&qp)[NH][8]) {
+    const int sw = chunk_swap(e);
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = ((i >> 2) ^ sw) * 4 + (i & 3);  // channel within the lane's 8
+            const float x = q_s[(h0 + hh) * kHeadDim + 8 * e + c];
+            qp[hh][i] = make_float2(fminf(x, 0.0f), fmaxf(x, 0.0f));
+        }
+}
+
+// Sum over the 16 lanes of a block (lane bits 0..3) of NH per-head partials,
+// returning to each lane the full sum of head (e * NH) / 16 (NH in 1, 2, 4).
+template <int NH>
+__device__ __forceinline__ float reduce16_scatter(float (&v)[NH], int e) {
+    if constexpr (NH == 4) {
+        const bool up = (e & 8) != 0;
+        float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+        const float s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
+        k0 += __shfl_xor_sync(kFullMask, s0, 8);
+        k1 += __shfl_xor_sync(kFullMask, s1, 8);
+        const bool mid = (e & 4) != 0;
+        float k = mid ? k1 : k0;
+        k += __shfl_xor_sync(kFullMask, mid ? k0 : k1, 4);
+        k += __shfl_xor_sync(kFullMask, k, 2);
+        k += __shfl_xor_sync(kFullMask, k, 1);
+        return k;
+    } else if constexpr (NH == 2) {
+        const bool up = (e & 8) != 0;
+        float k = up ? v[1] : v[0];
+        k += __shfl_xor_sync(kFullMask, up ? v[0] : v[1], 8);
+        k += __shfl_xor_sync(kFullMask, k, 4);
+        k += __shfl_xor_sync(kFullMask, k, 2);
+        k += __shfl_xor_sync(kFullMask, k, 1);
+        return k;
+    } else {
+        float k = v[0];
+        k += __shfl_xor_sync(kFullMask, k, 8);
+        k += __shfl_xor_sync(kFullMask, k, 4);
+        k += __shfl_xor_sync(kFullMask, k, 2);
+        k += __shfl_xor_sync(kFullMask, k, 1);
+        return k;
+    }
+}
+
+// Max over the NH heads spread over the block's lanes (after reduce16_scatter).
+template <int NH>
+__device__ __forceinline__ float max_over_heads(float s) {
+    if constexpr (NH == 4) {
+        s = fmaxf(s, __shfl_xor_sync(kFullMask, s, 4));
+        s = fmaxf(s, __shfl_xor_sync(kFullMask, s, 8));
+    } else if constexpr (NH == 2) {
+        s = fmaxf(s, __shfl_xor_sync(kFullMask, s, 8));
+    }
+    return s;
+}
+
+// Bound of one head over the lane's 8 channels: kb holds (kmin, kmax) pairs.
+__device__ __forceinline__ float head_bound8(const float2 *qp, const float2 *kb) {
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = __ffma2_rn(qp[i], kb[i], acc);
+    return acc.x + acc.y;
+}
+
+// Group bound of one block from this lane's 8 channels: the max over the
+// group's heads of each head's bound.
+template <int G>
+__device__ __forceinline__ float group_bound(const float *q_s,
+                                             const float2 (&qreg)[G < 4 ? G : 4][8],
+                                             const float2 *kb, int e) {
+    constexpr int NH = G < 4 ? G : 4;
+    float best = kNegBig;
+#pragma unroll 1
+    for (int h0 = 0; h0 < G; h0 += NH) {
+        float part[NH];
+        if constexpr (G <= 4) {
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) part[hh] = head_bound8(qreg[hh], kb);
+        } else {
+            float2 qv[NH][8];
+            load_qpairs<NH>(q_s, h0, e, qv);
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) part[hh] = head_bound8(qv[hh], kb);
+        }
+        best = fmaxf(best, max_over_heads<NH>(reduce16_scatter<NH>(part, e)));
+    }
+    return best;
+}
+
+struct SelArgs {
+    const float *q;
+    const __half *kbounds;
+    int Hkv, H, nbmax;
+    int se, n, R;          // candidates: blocks se .. se+n-1; R per CTA
+    uint32_t *keys;        // [P][ldk] keys (scratch)
+    int ldk;
+    float *ub;             // kExport: [P][n] bounds
+    int *hist;             // [P][kH1] top-digit histograms (zero between calls)
+    unsigned *ticket;      // [P] arrival counters (zero between calls)
+    int32_t *sel_idx, *sel_cnt;
+    int NB, rb, keff;
+    int32_t *dev_status;
+    int overlap;
+    // decode step: the token to append (app_k non-null), fused here because
+    // its block is forced (never scored); app_cache.len is the length before
+    kvd_cache app_cache;
+    const __half *app_k, *app_v;
+};
+
+__device__ __forceinline__ int warp_inclusive_scan(int x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+struct RadixShared {
+    uint64_t kbar;  // bulk copy of the keys (last CTA)
+    int wsum[kScoreWarps + 1];
+    int digit, above, last;
+};
+
+// Digit of the krem-th largest key from a shared-memory histogram of NBINS
+// bins (left zeroed); krem becomes the rank within that digit.  The consumer
+// thread t owns the digits NBINS-1-c*t .. NBINS-c*(t+1) (c = NBINS/256,
+// descending).  All threads call it.
+template <int NBINS>
+__device__ int radix_digit(int *hist, int &krem, RadixShared &rs) {
+    constexpr int c = NBINS / kConsumerThreads;
+    static_assert(c >= 1 && (c < 4 || c % 4 == 0), "bins per thread");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __syncthreads();  // histogram complete
+    int cnt[c];
+    int here = 0;
+    if (warp < kScoreWarps) {
+        const int base = NBINS - c * (tid + 1);
+        int v[c];
+        if constexpr (c % 4 == 0) {
+            // 4 bins per 16-byte access (base is a multiple of 4)
+#pragma unroll
+            for (int i = 0; i < c; i += 4) {
+                int4 *h4 = reinterpret_cast<int4 *>(hist + base + i);
+                const int4 w = *h4;
+                *h4 = make_int4(0, 0, 0, 0);
+                v[i] = w.x; v[i + 1] = w.y; v[i + 2] = w.z; v[i + 3] = w.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < c; ++i) {
+                v[i] = hist[base + i];
+                hist[base + i] = 0;
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < c; ++jj) {
+            cnt[jj] = v[c - 1 - jj];
+            here += cnt[jj];
+        }
+    }
+    const int incl = warp_inclusive_scan(here, lane);
+    if (lane == 31 && warp < kScoreWarps) rs.wsum[warp] = incl;
+    __syncthreads();
+    if (warp < kScoreWarps) {
+        const int wv = lane < kScoreWarps ? rs.wsum[lane] : 0;
+        const int winc = warp_inclusive_scan(wv, lane);
+        const int wex = __shfl_sync(kFullMask, winc - wv, warp);
+        const int above = wex + incl - here;
+        if (above < krem && krem <= above + here) {
+            int acc = above;
+#pragma unroll
+            for (int jj = 0; jj < c; ++jj) {
+                if (krem <= acc + cnt[jj]) {
+                    rs.digit = NBINS - 1 - c * tid - jj;
+                    rs.above = acc;
+                    break;
+                }
+                acc += cnt[jj];
+            }
+        }
+    }
+    __syncthreads();
+    krem -= rs.above;
+    return rs.digit;
+}
+
+struct SelShared {
+    RadixShared rs;
+    int abort, issued;
+};
+
+// Count, into hist, the digit (key >> DSHIFT) & (NBINS - 1) of every key
+// whose bits above MSHIFT equal match; every other key counts in the spare
+// bin hist[NBINS], so each key takes one atomic and no branch (a branch per
+// key costs more than the atomic).  Keys are read 16 per thread per round
+// into registers before any atomic is issued, so the loads overlap and the
+// shared atomics pipeline.
+template <int MSHIFT, int DSHIFT, int NBINS>
+__device__ __forceinline__ void radix_count(const uint32_t *keys, int n, uint32_t match,
+                                            int *hist) {
+    const int nq = (n + 3) / 4;
+    const uint4 *k4p = reinterpret_cast<const uint4 *>(keys);
+    for (int q0 = threadIdx.x; q0 < nq; q0 += 4 * kScoreThreads) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int q = q0 + u * kScoreThreads;
+            w[u] = q < nq ? k4p[q] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = 4 * (q0 + u * kScoreThreads);
+            const uint32_t kk[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const bool hit = j + c < n && (kk[c] >> MSHIFT) == match;
+                atomicAdd(&hist[hit ? static_cast<int>((kk[c] >> DSHIFT) & (NBINS - 1)) : NBINS],
+                          1);
+            }
+        }
+    }
+}
+
+// Keys the last CTA keeps in shared memory: as many as fit the ring, and few
+// enough that the two bitmaps of its list (2 * n / 32 words) fit the kH1
+// histogram ints; a larger problem is read from L2 and its bitmaps use the ring.
+constexpr int kRingKeys = (kScoreStages * kScoreStageBytes / 4) < 16 * kH1
+                              ? kScoreStages * kScoreStageBytes / 4
+                              : 16 * kH1;
+
+// Phases 3-4 of the last CTA of a problem: bits 20-0 of T by two counting
+// passes over the problem's keys, then the ascending list from bitmaps of
+// the keys above and equal to T.  ksrc: the keys (shared memory when
+// IN_SMEM, else global); words: shared scratch for 2 * ceil(n / 32) words.
+template <bool IN_SMEM>
+__device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n, int d1, int krem,
+                                              const uint32_t *ksrc, int *hist_l,
+                                              uint32_t *words, RadixShared &rs) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    radix_count<kShift1, kShift2, kH2>(ksrc, n, static_cast<uint32_t>(d1), hist_l);
+    const int d2 = radix_digit<kH2>(hist_l, krem, rs);
+    const uint32_t pre2 = (static_cast<uint32_t>(d1) << (kShift1 - kShift2)) |
+                          static_cast<uint32_t>(d2);
+    radix_count<kShift2, 0, kH3>(ksrc, n, pre2, hist_l);
+    const int d3 = radix_digit<kH3>(hist_l, krem, rs);
+    const uint32_t T = (pre2 << kShift2) | static_cast<uint32_t>(d3);
+    const int need_eq = krem;  // keys equal to T to take, lowest index first
+
+    // ================================================= phase 4: the list
+    // bitmaps of the keys above / equal to T, one 32-bit word per 32
+    // consecutive candidates (a warp ballot each)
+    const int nw = (n + 31) / 32;
+    uint32_t *gtw = words;
+    uint32_t *eqw = gtw + nw;
+    constexpr int kWarps = kScoreWarps + 1;
+    for (int w0 = warp; w0 < nw; w0 += 4 * kWarps) {
+        uint32_t k4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = 32 * (w0 + u * kWarps) + lane;
+            k4[u] = j < n ? ksrc[j] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int wi = w0 + u * kWarps;
+            const int j = 32 * wi + lane;
+            const unsigned gm = __ballot_sync(kFullMask, j < n && k4[u] > T);
+            const unsigned em = __ballot_sync(kFullMask, j < n && k4[u] == T);
+            if (lane == 0 && wi < nw) {
+                gtw[wi] = gm;
+                eqw[wi] = em;
+            }
+        }
+    }
+    __syncthreads();
+    // thread t owns words [t*wpt, (t+1)*wpt): an exclusive scan of the
+    // packed counts (above | equal << 16; both below 2^16) orders them
+    const int wpt = (nw + kScoreThreads - 1) / kScoreThreads;
+    const int w0 = min(nw, tid * wpt), w1 = min(nw, w0 + wpt);
+    unsigned mine = 0;
+    for (int wi = w0; wi < w1; ++wi)
+        mine += static_cast<unsigned>(__popc(gtw[wi])) | (static_cast<unsigned>(__popc(eqw[wi])) << 16);
+    const unsigned incl = static_cast<unsigned>(warp_inclusive_scan(static_cast<int>(mine), lane));
+    if (lane == 31) rs.wsum[warp] = static_cast<int>(incl);
+    __syncthreads();
+    unsigned before = incl - mine;
+    for (int w = 0; w < warp; ++w) before += static_cast<unsigned>(rs.wsum[w]);
+    int g_before = static_cast<int>(before & 0xffffu), e_before = static_cast<int>(before >> 16);
+    int32_t *dst = a.sel_idx + static_cast<size_t>(p) * a.nbmax;
+    for (int wi = w0; wi < w1; ++wi) {
+        const uint32_t gm = gtw[wi], em = eqw[wi];
+        uint32_t take = gm;
+        int r = min(max(need_eq - e_before, 0), __popc(em));  // equal keys taken here
+        for (uint32_t m = em; r > 0; --r) {
+            take |= m & (0u - m);  // lowest remaining equal key
+            m &= m - 1;
+        }
+        int o = a.se + g_before + min(e_before, need_eq);
+        for (uint32_t m = take; m; m &= m - 1) dst[o++] = a.se + 32 * wi + (__ffs(m) - 1);
+        g_before += __popc(gm);
+        e_before += __popc(em);
+    }
+    for (int j = tid; j < a.se; j += kScoreThreads) dst[j] = j;
+    for (int j = a.rb + tid; j < a.NB; j += kScoreThreads) dst[a.se + a.keff + (j - a.rb)] = j;
+    if (tid == 0) a.sel_cnt[p] = a.se + a.keff + (a.NB - a.rb);
+}
+
+// CTA (x, p): candidate blocks j in [x*R, min(n, (x+1)*R)) of problem p,
+// i.e. cache blocks se + j.  Their bounds stream through a TMA ring (stages
+// of 64 blocks; warp 16 produces, warps 0..15 consume, warp w scoring blocks
+// 4w..4w+3 of each stage two at a time).
+template <int G, int MODE>
+__device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, uint8_t *smem,
+                            SelShared &ss) {
+    constexpr int NH = G < 4 ? G : 4;
+    RadixShared &rs = ss.rs;
+    int &s_abort = ss.abort;
+    int &s_issued = ss.issued;
+    uint8_t *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kScoreStages * kScoreStageBytes);
+    uint64_t *empty = full + kScoreStages;
+    float *q_s = reinterpret_cast<float *>(empty + kScoreStages);
+    int *hist_l = reinterpret_cast<int *>(q_s + G * kHeadDim);  // kH1 ints (kSelect)
+    volatile int *abort_flag = &s_abort;
+
+    const int b = p / a.Hkv, g = p % a.Hkv;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = lane >> 4, e = lane & 15;
+    const int j0 = x_tile * a.R;
+    const int j1 = min(a.n, j0 + a.R);
+    const int nstage = (j1 - j0 + kStageBlocks - 1) / kStageBlocks;
+
+    if (tid == 0) {
+        for (int i = 0; i < kScoreStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kScoreWarps);
+        }
+        mbar_init(&rs.kbar, 1);
+        s_abort = 0;
+        s_issued = 0;
+        fence_barrier_init();
+    }
+    if (MODE == kSelect)
+        for (int i = tid; i < kH1; i += kScoreThreads) hist_l[i] = 0;
+    __syncthreads();
+    // overlap: inside a decode step whose appended token lands in a forced
+    // block, the candidate bounds and the query are complete before the
+    // upstream append runs, so scoring overlaps it; the grid-dependency wait
+    // then comes before anything shared with earlier kernels is written.
+    if (!a.overlap) pdl_wait();
+    pdl_launch_dependents();
+
+    // ================================================= phase 1: keys
+    const size_t base = static_cast<size_t>(p) * a.nbmax + a.se;  // row of candidate 0
+    if (warp == kScoreWarps) {
+        if (lane == 0) {
+            const uint64_t pol = l2_policy_evict_first();
+            int issued = 0;
+            for (int si = 0; si < nstage; ++si) {
+                const int s = si % kScoreStages;
+                if (si >= kScoreStages &&
+                    !mbar_wait(&empty[s], ((si / kScoreStages) - 1) & 1, abort_flag)) {
+                    s_abort = 1;
+                    report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                    break;
+                }
+                const int jb = j0 + si * kStageBlocks;
+                const int cnt = min(kStageBlocks, j1 - jb);
+                const uint32_t bytes = static_cast<uint32_t>(cnt) * kBoundRowBytes;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                tma_load_1d(ring + s * kScoreStageBytes, a.kbounds + (base + jb) * kHeadDim * 2,
+                            bytes, &full[s], pol);
+                issued = si + 1;
+            }
+            s_issued = issued;
+        }
+    } else {
+        // the producer's first copies are in flight while the query loads
+        const float *qg =
+            a.q + (static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * G) * kHeadDim;
+        for (int i = tid; i < G * kHeadDim; i += kConsumerThreads) q_s[i] = qg[i];
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+        float2 qreg[NH][8];
+        if constexpr (G <= 4) load_qpairs<NH>(q_s, 0, e, qreg);
+        const int sw = chunk_swap(e);
+        for (int si = 0; si < nstage; ++si) {
+            const int s = si % kScoreStages;
+            const bool ok = mbar_wait(&full[s], (si / kScoreStages) & 1, abort_flag);
+            if (!__all_sync(kFullMask, ok)) {
+                if (lane == 0) {
+                    s_abort = 1;
+                    report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                }
+                break;
+            }
+            const uint8_t *st = ring + s * kScoreStageBytes;
+            float sc[2];
+            int jr[2];
+#pragma unroll
+            for (int ps = 0; ps < 2; ++ps) {
+                const int k = warp * kScoreSlots + 2 * ps + half;  // block within the stage
+                jr[ps] = j0 + si * kStageBlocks + k;
+                float2 kb[8];
+                if (jr[ps] < j1) {
+                    const uint4 *row = reinterpret_cast<const uint4 *>(st + k * kBoundRowBytes);
+                    const uint4 c0 = row[2 * e + sw], c1 = row[2 * e + 1 - sw];
+                    const __half2 *h0 = reinterpret_cast<const __half2 *>(&c0);
+                    const __half2 *h1 = reinterpret_cast<const __half2 *>(&c1);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        kb[i] = __half22float2(h0[i]);
+                        kb[4 + i] = __half22float2(h1[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) kb[i] = make_float2(0.0f, 0.0f);
+                }
+                sc[ps] = group_bound<G>(q_s, qreg, kb, e);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+#pragma unroll
+            for (int ps = 0; ps < 2; ++ps) {
+                if (jr[ps] < j1 && e == 0) {
+                    if constexpr (MODE == kSelect) {
+                        const uint32_t key = float_to_key(sc[ps]);
+                        a.keys[static_cast<size_t>(p) * a.ldk + jr[ps]] = key;
+                        atomicAdd(&hist_l[key >> kShift1], 1);
+                    } else {
+                        a.ub[static_cast<size_t>(p) * a.n + jr[ps]] = sc[ps];
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (s_abort) {
+        if (warp == kScoreWarps && lane == 0) {
+            // wind down: wait (bounded) for the copies still landing in the ring
+            const int issued = s_issued;
+            volatile int never = 0;
+            for (int i = max(0, issued - kScoreStages); i < issued; ++i)
+                (void)mbar_wait(&full[i % kScoreStages], (i / kScoreStages) & 1, &never);
+        }
+        if (a.overlap) pdl_wait();
+        return;
+    }
+    if (a.overlap) pdl_wait();  // the upstream kernels are complete past here
+    if (a.app_k && x_tile == 0 && warp == 0) {
+        // the decode step's token for (b, g): after the dependency wait, as the
+        // previous step's kernels may still read the row it replaces
+        const int len0 = a.app_cache.len;
+        if (a.app_cache.dtype == KVD_F16)
+            append_block_warp<KVD_F16>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b,
+                                       g, lane);
+        else
+            append_block_warp<KVD_INT8>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b,
+                                        g, lane);
+    }
+    if constexpr (MODE == kExport) return;
+
+    // ================================================= phase 2: ticket
+    const int X = n_tiles;
+    const int n = a.n;
+    const uint32_t *kp = a.keys + static_cast<size_t>(p) * a.ldk;
+    const bool in_smem = n <= kRingKeys;
+    uint32_t *s_keys = reinterpret_cast<uint32_t *>(ring);
+    if (X > 1) {
+        int *hg = a.hist + static_cast<size_t>(p) * kH1;
+        for (int i = tid; i < kH1; i += kScoreThreads) {
+            const int v = hist_l[i];
+            if (v != 0) {
+                atomicAdd(&hg[i], v);
+                hist_l[i] = 0;
+            }
+        }
+    }
+    __threadfence();  // this CTA's keys (and histogram counts) are out
+    __syncthreads();
+    if (X > 1) {
+        if (tid == 0)
+            rs.last = atomicAdd(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
+        __syncthreads();
+        if (!rs.last) return;
+        // the last CTA of the problem: every key and histogram count is in
+        __threadfence();
+    }
+    if (in_smem && warp == kScoreWarps) {
+        // the problem's keys (L2-resident) into the ring by bulk copies; they
+        // were written by ordinary stores, so order those before the async proxy
+        const uint32_t bytes = static_cast<uint32_t>(a.ldk) * 4u;
+        const uint32_t off = static_cast<uint32_t>(lane) * kScoreStageBytes;
+        asm volatile("fence.proxy.async;" ::: "memory");
+        if (lane == 0) mbar_arrive_expect_tx(&rs.kbar, bytes);
+        __syncwarp();
+        if (off < bytes)
+            tma_load_1d(ring + off, reinterpret_cast<const uint8_t *>(kp) + off,
+                        min(static_cast<uint32_t>(kScoreStageBytes), bytes - off), &rs.kbar,
+                        l2_policy_evict_first());
+    }
+    if (X > 1) {
+        int *hg = a.hist + static_cast<size_t>(p) * kH1;
+        for (int i = tid * 4; i < kH1; i += kScoreThreads * 4) {
+            int4 *src = reinterpret_cast<int4 *>(hg + i);
+            *reinterpret_cast<int4 *>(hist_l + i) = __ldcg(src);
+            __stcg(src, make_int4(0, 0, 0, 0));
+        }
+        if (tid == 0) a.ticket[p] = 0u;
+    }
+
+    // ================================================= phase 3: T
+    int krem = a.keff;
+    const int d1 = radix_digit<kH1>(hist_l, krem, rs);
+    if (in_smem && !mbar_wait(&rs.kbar, 0, abort_flag)) s_abort = 1;
+    if (__syncthreads_or(s_abort)) {
+        if (tid == 0) {
+            report_status(a.dev_status, KVD_ERR_TIMEOUT);
+            a.sel_cnt[p] = 0;
+            volatile int never = 0;
+            if (in_smem) (void)mbar_wait(&rs.kbar, 0, &never);  // copies in flight
+        }
+        return;
+    }
+    // the rest reads the keys from shared memory, or from L2 for a problem too
+    // large for the ring; each variant is compiled with its address space known
+    if (in_smem)
+        select_finish<true>(a, p, n, d1, krem, s_keys, hist_l, reinterpret_cast<uint32_t *>(hist_l), rs);
+    else
+        select_finish<false>(a, p, n, d1, krem, kp, hist_l, s_keys, rs);
+}
+
+template <int G>
+constexpr int select_smem_bytes() {
+    return kScoreStages * kScoreStageBytes + 2 * kScoreStages * 8 + G * kHeadDim * 4 +
+           kH1 * 4 + 64;  // + the spare bin of the counting passes
+}
+
+}  // namespace
+}  // namespace kvd

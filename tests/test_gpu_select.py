@@ -9,7 +9,7 @@ import torch
 
 import long_context_decode_kv_gb300 as kvd
 import oracle
-from gpu_util import check_selection, dev, make_pair, oracle_scores, seeded
+from gpu_util import TIE_REL, check_selection, dev, make_pair, oracle_scores, seeded
 
 pytestmark = pytest.mark.gpu
 
@@ -139,3 +139,33 @@ def test_select_one_cta_per_problem(B, Hkv, L, k_sel):
     kvd.select_blocks(gc, q, k_sel, 4, 64, sel_idx, sel_cnt, ws)
     torch.cuda.synchronize()
     check_selection(sel_idx, sel_cnt, oc, q.cpu().numpy(), k_sel, 4, 64, G)
+
+
+@pytest.mark.parametrize("nb,k_sel,G", [(36000, 700, 4), (49000, 2048, 8)])
+def test_select_large_problem_keys_from_l2(nb, k_sel, G):
+    # more candidates than the ranking CTA keeps in shared memory: it reads
+    # the keys from L2.  Only bounds matter to the selection, so they are
+    # written directly (kmin <= kmax per channel) instead of appending tokens.
+    B, Hkv = 1, 1
+    L = nb * 64 - 17
+    gc = kvd.KVCache(kvd.INT8, B, Hkv, nb * 64, device=dev())
+    a = seeded((B, Hkv, nb, 128), 81, scale=2.0)
+    d = seeded((B, Hkv, nb, 128), 82).abs()
+    gc.t["kbounds"][..., 0] = a
+    gc.t["kbounds"][..., 1] = (a.float() + d.float()).half()
+    gc.len = L
+    q = _q(B, Hkv * G, 83)
+    ws = kvd.make_workspace(gc, Hkv * G)
+    sel_idx = torch.full((B, Hkv, nb), -7, dtype=torch.int32, device=dev())
+    sel_cnt = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev())
+    kvd.select_blocks(gc, q, k_sel, 4, 256, sel_idx, sel_cnt, ws)
+    torch.cuda.synchronize()
+    kmin = gc.kmin[0, 0].cpu().numpy()
+    kmax = gc.kmax[0, 0].cpu().numpy()
+    ub, _, mag = oracle.block_scores(q[0].cpu().numpy(), kmin, kmax)
+    want, kth = oracle.select(L, 64, ub, k_sel, 4, 256)
+    n = int(sel_cnt[0, 0])
+    got = sel_idx[0, 0, :n].cpu().numpy()
+    assert n == len(want) and np.all(np.diff(got) > 0)
+    for j in set(got.tolist()) ^ set(want.tolist()):
+        assert abs(ub[j] - kth) <= TIE_REL * max(abs(kth), mag[j]), (j, ub[j], kth)
