@@ -240,6 +240,36 @@ def oracle_leg(w, q, k, v, steps, problem=(0, 0)):
                    f"x {n_prob} problems")}
 
 
+def oracle_leg_all_cores(w, q, k, v, steps):
+    """The same oracle step on all host cores: as many (KV head) problems of
+    sequence 0 as there are threads, one per OpenMP thread; the step time is
+    scaled by the number of such batches the workload's B*Hkv problems make."""
+    import oracle
+    threads = max(1, oracle.threads_available())
+    hk = min(w.Hkv, threads)
+    G = w.G
+    oc = oracle.OracleCache(w.dtype, 1, hk, w.D, w.L + 64, 64)
+    oc.append(k[0:1, :, :hk].contiguous().cpu().numpy(), v[0:1, :, :hk].contiguous().cpu().numpy())
+    qg = q[0:1, :hk * G].cpu().numpy()
+    times = []
+    for s in range(steps):
+        kn, vn = synth.make_step_token(w, s, device="cpu")
+        t0 = time.perf_counter()
+        oc.len = w.L
+        oc.append(kn[0:1, :, :hk].numpy(), vn[0:1, :, :hk].numpy())
+        oc.decode(qg, w.scale, k_sel=w.k_sel, sink_tokens=w.sink_tokens,
+                  recent_tokens=w.recent_tokens, n_threads=threads)
+        times.append(time.perf_counter() - t0)
+    n_prob = w.B * w.Hkv
+    batches = -(-n_prob // hk)
+    used = min(threads, hk)
+    return statistics.median(times) * 1e6 * batches, {
+        "kind": "oracle", "cores": used,
+        "sample": (f"{hk} of {n_prob} (sequence, KV head) problems of {w.name} at once on "
+                   f"{used} threads, {steps} steps (append + select + attend, fp64), median "
+                   f"step time x {batches} batch(es)")}
+
+
 def run_reference(args, w):
     # the oracle runs on rank 0's host cores only; other ranks exit without work
     if int(os.environ.get("RANK", "0")) != 0:
@@ -272,6 +302,64 @@ def config_of(w):
             "parallelism": "replicas"}
 
 
+def run_sweep(args):
+    """Sparse and dense decode steps (append + select + attend, as in the bench
+    line) over a sweep of workloads; one JSON line per point."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    points = synth.context_sweep() if args.sweep == "context" else synth.coverage_sweep()
+    steps, warm = max(1, args.steps), max(3, args.warmup)
+    for w in points:
+        q, k, v, _ = synth.make_workload(w, device=dev)
+        cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev)
+        kvd.kv_append(cache, k, v)
+        del k, v
+        ws = kvd.make_workspace(cache, w.H)
+        nbmax = cache.max_seq // 64
+        sel_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev)
+        sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev)
+        out = torch.empty(w.B, w.H, w.D, device=dev)
+        toks = [synth.make_step_token(w, s, device=dev) for s in range(8)]
+
+        def step(i, dense):
+            cache.len = w.L
+            kn, vn = toks[i % len(toks)]
+            kvd.decode_step(cache, q, kn, vn, w.scale, -1 if dense else w.k_sel,
+                            w.sink_tokens, w.recent_tokens, out, ws, sel_idx=sel_idx,
+                            sel_cnt=sel_cnt)
+
+        res = {}
+        for dense in (False, True):
+            ms = []
+            for i in range(warm + steps):
+                flush.fill_(i & 0xFF)
+                drain.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                step(i, dense)
+                e1.record(stream)
+                if i >= warm:
+                    ms.append((e0, e1))
+            torch.cuda.synchronize()
+            res[dense] = statistics.mean(a.elapsed_time(b) for a, b in ms) * 1e3
+        L1 = w.L + 1
+        n_sel = int(sel_cnt.sum().item())
+        tokens = attended_tokens(sel_idx, sel_cnt, L1) if n_sel else 0
+        print(json.dumps({
+            "sweep": args.sweep, "workload": w.name, "context": w.L, "batch": w.B,
+            "kv_dtype": "int8" if w.dtype == kvd.INT8 else "f16", "k_sel": w.k_sel,
+            "coverage": n_sel / (w.B * w.Hkv) / ((L1 + 63) // 64),
+            "sparse_step_us": res[False], "dense_step_us": res[True],
+            "dense_over_sparse": res[True] / res[False],
+            "effective_kv_gbs": step_bytes(w, tokens, n_sel, L1) / (res[False] * 1e-6) / 1e9,
+            "steps": steps, "l2": "write + read flush between steps"}), flush=True)
+        del cache, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -283,7 +371,13 @@ def main():
     ap.add_argument("--context", type=int, default=None,
                     help="run the workload's recipe at this context instead (a multiple "
                          "of 64; a smaller case for profiling)")
+    ap.add_argument("--sweep", choices=["context", "coverage"], default=None,
+                    help="instead of the bench line: sparse vs dense decode steps over the "
+                         "context sweep (16K..1M, 25%% coverage) or the 128K x 8 coverage "
+                         "sweep, one JSON line per point")
     args = ap.parse_args()
+    if args.sweep:
+        return run_sweep(args)
     w = synth.WORKLOADS[args.workload]
     if args.context is not None:
         if args.context < 64 or args.context % 64:
@@ -306,7 +400,7 @@ def main():
     sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev)
     out = torch.empty(w.B, w.H, w.D, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def flush_l2(i):
         flush.fill_(i & 0xFF)
@@ -411,9 +505,12 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         try:
-            v_cpu, cpu = oracle_leg(w, q, k, v, 3)
-            cpu["value"] = v_cpu
+            v_all, cpu = oracle_leg_all_cores(w, q, k, v, 3)
+            v_one, one = oracle_leg(w, q, k, v, 3)
+            cpu["value"] = v_all
             cpu["unit"] = "us/step"
+            cpu["value_1_thread"] = v_one
+            cpu["sample_1_thread"] = one["sample"]
         except Exception as e:  # the baseline must not hide the GPU number
             cpu = {"kind": "oracle", "value": None, "error": str(e)[:200]}
 

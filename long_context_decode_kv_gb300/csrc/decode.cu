@@ -7,7 +7,7 @@ namespace kvd {
 namespace {
 
 template <int DT, int GC, bool DENSE>
-__global__ void __launch_bounds__(kThreads, Tile<DT>::kMinCtas) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(Tile<DT>::kThreads, Tile<DT>::kMinCtas) decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     decode_body<DT, GC, DENSE>(a, blockIdx.x, blockIdx.y, smem);
 }
@@ -58,7 +58,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, int P_sub, cudaStream_t st, boo
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_ex(decode_kernel<DT, GC, DENSE>, dim3(a.splits, P_sub), dim3(kThreads),
+    return launch_ex(decode_kernel<DT, GC, DENSE>, dim3(a.splits, P_sub), dim3(Tile<DT>::kThreads),
                      SL::kTotal, st, pdl, a);
 }
 

@@ -12,16 +12,16 @@
 // ascending sweep, merged across splits.
 //
 // CTA = (split s of the block list, sequence b, KV head g, head subgroup).
-// Warp 8 is the producer: one lane streams each listed 64-token block (K, V
-// and, for int8, both scale rows) into a ring of shared-memory stages with
-// 1-D TMA bulk copies completing on an mbarrier.  Warps 0..7 form two
-// consumer groups that take alternate blocks (so twice as many warps hide
-// each other's latencies); within a group warp w owns tokens 16w..16w+15 of
-// the block and keeps its own online-softmax state for the CTA's query heads,
-// so no CTA-wide barrier is needed per block.  PV runs on packed f32x2 FMAs.
-// At the end the 8 warp states merge in shared memory and the CTA writes a
-// partial (m, l, acc[128]) per head; the last CTA of the problem to arrive
-// merges all splits.
+// The last warp is the producer: one lane streams each
+// listed 64-token block (K, V and, for int8, both scale rows) into a ring of
+// shared-memory stages with 1-D TMA bulk copies completing on an mbarrier.
+// The other warps form two consumer groups of four that take blocks in turn,
+// so more warps hide each other's latencies; within a group warp w owns
+// tokens 16w..16w+15 of the block and keeps its own online-softmax state for
+// the CTA's query heads, so no CTA-wide barrier is needed per block.  PV runs
+// on packed f32x2 FMAs.  At the end the warp states merge in shared memory
+// and the CTA writes a partial (m, l, acc[128]) per head; the last CTA of the
+// problem to arrive merges all splits.
 #pragma once
 
 #include "common.cuh"
@@ -31,11 +31,8 @@ namespace kvd {
 namespace {
 
 
-constexpr int kGroups = 2;                                 // consumer groups
 constexpr int kWarpsPerGroup = 4;
-constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;   // warps 0..7
 constexpr int kTokensPerWarp = kBlock / kWarpsPerGroup;    // 16
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
 // Partial rows: m, l, two pad words, acc[128] (acc 16-byte aligned).
 constexpr int kPartStride = kHeadDim + 4;
 constexpr int kAccOff = 4;
@@ -49,16 +46,22 @@ struct Tile<KVD_INT8> {
     static constexpr int kRowBytes = kHeadDim;                        // int8 codes
     static constexpr int kKBytes = kBlock * kRowBytes;                // 8192
     static constexpr int kStageBytes = 2 * kKBytes + 2 * kBlock * 4;  // + both scale rows
+    static constexpr int kGroups = 2;   // consumer groups (4 warps each)
     static constexpr int kStages = 6;   // a multiple of kGroups
     static constexpr int kMinCtas = 2;
+    static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
 };
 template <>
 struct Tile<KVD_F16> {
     static constexpr int kRowBytes = 2 * kHeadDim;                    // f16
     static constexpr int kKBytes = kBlock * kRowBytes;                // 16384
     static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kGroups = 2;
     static constexpr int kStages = 4;   // a multiple of kGroups
     static constexpr int kMinCtas = 1;
+    static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
 };
 
 struct DecodeArgs {
@@ -82,7 +85,7 @@ struct SmemLayout {
     static constexpr int kStagesOff = 0;
     static constexpr int kRing = kStages * kStageBytes;
     // after the loop the ring holds the warp merge, then the split weights
-    static constexpr int kMergeBytes = kConsumerWarps * GC * kPartStride * 4;
+    static constexpr int kMergeBytes = Tile<DT>::kConsumerWarps * GC * kPartStride * 4;
     static constexpr int kWeightBytes = kMaxSplits * 4 * 4;
     static constexpr int kScratch = kMergeBytes > kWeightBytes ? kMergeBytes : kWeightBytes;
     static constexpr int kBarOff = (kRing > kScratch ? kRing : kScratch);
@@ -94,7 +97,7 @@ struct SmemLayout {
     static constexpr int kCoefOff = kQOff + kQBytes;
     static constexpr int kPwOff = kCoefOff + 16;
     // [warp][16 tokens][4 heads] pairs (p, p)
-    static constexpr int kPwBytes = kConsumerWarps * kTokensPerWarp * 4 * 2 * 4;
+    static constexpr int kPwBytes = Tile<DT>::kConsumerWarps * kTokensPerWarp * 4 * 2 * 4;
     static constexpr int kLOff = kPwOff + kPwBytes;  // split merge: L per head
     static constexpr int kFlagOff = kLOff + 16;
     static constexpr int kTotal = kFlagOff + 16;
@@ -445,7 +448,7 @@ template <int DT, int GC, bool DENSE>
 __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *smem) {
     using SL = SmemLayout<DT, GC>;
     using TL = Tile<DT>;
-    static_assert(TL::kStages % kGroups == 0, "stages must split evenly over the groups");
+    static_assert(TL::kStages % TL::kGroups == 0, "stages must split evenly over the groups");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + SL::kFullOff);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + SL::kEmptyOff);
     int *stage_blk = reinterpret_cast<int *>(smem + SL::kBlkOff);
@@ -493,7 +496,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     st.l = 0.0f;
 #pragma unroll
     for (int h = 0; h < GC; ++h) st.acc[h][0] = st.acc[h][1] = make_float2(0.0f, 0.0f);
-    if (warp == kConsumerWarps) {
+    if (warp == TL::kConsumerWarps) {
         // ------------------------------------------------------ producer
         const uint64_t pol = l2_policy_evict_first();
         const int32_t *list = a.sel_idx + static_cast<size_t>(bg) * a.nbmax + beg;
@@ -551,7 +554,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         if constexpr (DT == KVD_INT8) {
             QRegsI8<GC> qr;
             load_qregs_i8<GC>(q_s, lane >> 2, lane & 3, qr);
-            for (int i = group; i < n; i += kGroups) {
+            for (int i = group; i < n; i += TL::kGroups) {
                 const int s = i % TL::kStages;
                 const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
                 if (!__all_sync(kFull, ok)) {
@@ -573,7 +576,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         } else {
             QRegsF16<GC> qr;
             load_qregs_f16<GC>(q_s, lane & 7, qr);
-            for (int i = group; i < n; i += kGroups) {
+            for (int i = group; i < n; i += TL::kGroups) {
                 const int s = i % TL::kStages;
                 const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
                 if (!__all_sync(kFull, ok)) {
@@ -605,7 +608,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     }
     __syncthreads();  // (A) every stage consumed: the ring becomes scratch
     const bool aborted = *abort_flag != 0;
-    if (!aborted && warp < kConsumerWarps) {
+    if (!aborted && warp < TL::kConsumerWarps) {
         float *mg = reinterpret_cast<float *>(smem + SL::kStagesOff);
         constexpr int lph = (DT == KVD_INT8 ? 4 : 8) / GC;
 #pragma unroll
@@ -622,7 +625,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     __syncthreads();  // (B) merge area written
     if (aborted) {
         // wind down: wait (bounded) for the copies still landing in the ring
-        if (warp == kConsumerWarps && lane == 0) {
+        if (warp == TL::kConsumerWarps && lane == 0) {
             const int issued = *issued_s;
             volatile int never = 0;
             for (int i = max(0, issued - TL::kStages); i < issued; ++i)
@@ -639,11 +642,11 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         const int h = tid >> 5, d4 = tid & 31;
         float M = kNegBig;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg[(w * GC + h) * kPartStride]);
+        for (int w = 0; w < TL::kConsumerWarps; ++w) M = fmaxf(M, mg[(w * GC + h) * kPartStride]);
         float L = 0.0f;
         float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < TL::kConsumerWarps; ++w) {
             const float *row = mg + (w * GC + h) * kPartStride;
             const float sc = exp2f(row[0] - M);
             L = fmaf(sc, row[1], L);
@@ -682,7 +685,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     const int S = a.splits;
     const float *p0 = a.partials + static_cast<size_t>(prob) * S * GC * kPartStride;
     float *ms = reinterpret_cast<float *>(smem + SL::kStagesOff);  // [S][GC] maxima -> weights
-    for (int i = tid; i < S * GC; i += kThreads)
+    for (int i = tid; i < S * GC; i += TL::kThreads)
         ms[i] = __ldcg(p0 + static_cast<size_t>(i) * kPartStride);
     __syncthreads();
     if (warp < GC) {

@@ -43,7 +43,8 @@ cudaError_t launch_select_t(const SelArgs &a0, int P, cudaStream_t st, bool pdl)
         occupancy = occ > 0 ? occ : 1;
     }
     SelArgs a = a0;
-    // CTAs per problem: about as many as fit on the GPU at once, split evenly
+    // CTAs per problem: as many as fit on the GPU at once, split evenly (a
+    // small problem still gains from many CTAs streaming its bounds)
     const long cap = static_cast<long>(occupancy) * device_sm_count();
     long X = cap / P;
     if (X > kMaxCtasPerProblem) X = kMaxCtasPerProblem;

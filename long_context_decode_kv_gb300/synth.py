@@ -59,7 +59,7 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-def _coverage_budget(L: int, block: int, frac: float, sink: int, recent: int) -> int:
+def coverage_budget(L: int, block: int, frac: float, sink: int, recent: int) -> int:
     """Top-K budget so that forced + top-K blocks make `frac` of all blocks."""
     nb = (L + block - 1) // block
     se = min(nb, (sink + block - 1) // block)
@@ -77,7 +77,7 @@ INT8_DENSE = tuple(
     for L in (512, 2048, 8192))
 QWEN3_32K = Workload("qwen3_4b_gqa_32k_f16", B=1, H=32, Hkv=8, D=128, L=32768, dtype=F16,
                      keys="gqa_needles", n_needles=16, sink_tokens=4, recent_tokens=64,
-                     k_sel=_coverage_budget(32768, 64, 0.25, 4, 64), seed=1236)
+                     k_sel=coverage_budget(32768, 64, 0.25, 4, 64), seed=1236)
 CTX128K_B8 = Workload("ctx128k_b8_int8", B=8, H=32, Hkv=8, D=128, L=131072, dtype=INT8,
                       keys="gqa_needles", n_needles=16, sink_tokens=4, recent_tokens=256,
                       k_sel=131072 // 64 // 16, seed=1237)
@@ -86,6 +86,25 @@ CTX1M = Workload("ctx1m_int8", B=1, H=32, Hkv=8, D=128, L=1 << 20, dtype=INT8,
                  k_sel=1024, seed=1238)
 
 WORKLOADS = {w.name: w for w in (TINY, *INT8_DENSE, QWEN3_32K, CTX128K_B8, CTX1M)}
+
+
+def context_sweep(frac: float = 0.25):
+    """The 32K GQA recipe (f16, per-head mean offsets, 16 needles) at 16K..1M
+    context, each at `frac` block coverage (forced blocks included)."""
+    out = []
+    for L in (16384, 32768, 131072, 1 << 20):
+        k_sel = coverage_budget(L, 64, frac, QWEN3_32K.sink_tokens, QWEN3_32K.recent_tokens)
+        out.append(QWEN3_32K.with_(name=f"gqa_f16_{L // 1024}k_cov{round(frac * 100)}", L=L,
+                                   k_sel=k_sel))
+    return out
+
+
+def coverage_sweep():
+    """The 128K x 8 int8 recipe with K_SEL = NB * c, c = 1/64 .. 1/2 (plus the
+    sink and recent blocks)."""
+    nb = CTX128K_B8.NB
+    return [CTX128K_B8.with_(name=f"ctx128k_b8_int8_c1_{d}", k_sel=nb // d)
+            for d in (64, 32, 16, 8, 4, 2)]
 
 
 def _gen(device, seed: int) -> torch.Generator:
