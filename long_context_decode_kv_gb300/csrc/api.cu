@@ -81,9 +81,9 @@ Geom make_geom(const kvd_cache *c, int n_heads, int len) {
 
 // Workspace regions (byte offsets; every region 256-byte aligned).
 struct WsLayout {
-    size_t counters, partials, keys, sel_hist, sel_ticket, sel_idx, sel_cnt, q, k_new, v_new,
+    size_t counters, partials, keys, sel_range, sel_ticket, sel_idx, sel_cnt, q, k_new, v_new,
         out, total;
-    int hist_rows;
+    int range_rows;
     DecodePlan plan;
 };
 
@@ -100,13 +100,13 @@ WsLayout ws_layout(const kvd_cache *c, int n_heads) {
     off += align_up(decode_partials_bytes(g, w.plan));
     w.keys = off;  // key rows padded to 16 bytes
     off += align_up(P * ((g.nbmax + 3) / 4 * 4) * sizeof(uint32_t));
-    // top-digit histograms and tickets: only problems split over several
-    // CTAs use them, and there are fewer of those than 2 * SMs
+    // key ranges and tickets: only problems split over several CTAs use
+    // them, and there are fewer of those than 2 * SMs
     const size_t sms = static_cast<size_t>(device_sm_count());
     const size_t hrows = P < 2 * sms ? P : 2 * sms;
-    w.hist_rows = static_cast<int>(hrows);
-    w.sel_hist = off;
-    off += align_up(hrows * select_hist_bytes());
+    w.range_rows = static_cast<int>(hrows);
+    w.sel_range = off;
+    off += align_up(hrows * 2 * sizeof(unsigned));
     w.sel_ticket = off;
     off += align_up(hrows * sizeof(unsigned));
     w.sel_idx = off;
@@ -155,9 +155,9 @@ void forced_range(int len, int sink, int recent, int *se, int *rb) {
 SelScratch sel_scratch(void *ws, const WsLayout &w) {
     SelScratch scr;
     scr.keys = ws_at<uint32_t>(ws, w.keys);
-    scr.hist = ws_at<int>(ws, w.sel_hist);
+    scr.range = ws_at<unsigned>(ws, w.sel_range);
     scr.ticket = ws_at<unsigned>(ws, w.sel_ticket);
-    scr.hist_rows = w.hist_rows;
+    scr.range_rows = w.range_rows;
     return scr;
 }
 

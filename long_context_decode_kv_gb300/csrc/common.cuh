@@ -117,6 +117,16 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Arrival on a GPU-scope counter by one thread right after a CTA barrier.
+// The release covers every store the CTA made before the barrier, and the
+// acquire every store that earlier arrivals released; a barrier after the
+// call extends the acquire to the whole CTA.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void report_status(int32_t *dev_status, int code) {
     if (dev_status) atomicCAS(reinterpret_cast<int *>(dev_status), 0, code);
 }

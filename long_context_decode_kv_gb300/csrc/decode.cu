@@ -86,6 +86,7 @@ DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count) {
     if (s < 1) s = 1;
     if (s > kMaxSplits) s = kMaxSplits;
     p.splits = static_cast<int>(s);
+    p.blocks = max_blocks;
     return p;
 }
 

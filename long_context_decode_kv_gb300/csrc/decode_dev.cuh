@@ -38,6 +38,8 @@ constexpr int kPartStride = kHeadDim + 4;
 constexpr int kAccOff = 4;
 constexpr int kMaxSplits = 256;
 constexpr unsigned kFull = 0xffffffffu;
+// Stage marker that ends a consumer group's loop.
+constexpr int kEndMark = -2;
 
 template <int DT>
 struct Tile;
@@ -71,9 +73,10 @@ struct DecodeArgs {
     float *out;
     const int32_t *sel_idx, *sel_cnt;
     float *partials;
-    uint32_t *counters;
+    uint32_t *counters;  // [problems] split arrivals
     int32_t *dev_status;
     int Hkv, H, G, max_seq, nbmax, len, NB, splits, subgroups;
+    int plan_blocks;     // list length the splits were planned for (<= NB)
     float scale_log2;  // softmax_scale * log2(e): logits live in base 2
     int early_q;       // q is complete before the upstream kernels finish
 };
@@ -86,7 +89,8 @@ struct SmemLayout {
     static constexpr int kRing = kStages * kStageBytes;
     // after the loop the ring holds the warp merge, then the split weights
     static constexpr int kMergeBytes = Tile<DT>::kConsumerWarps * GC * kPartStride * 4;
-    static constexpr int kWeightBytes = kMaxSplits * 4 * 4;
+    // split merge: (m, l) and the accumulators of every thread part
+    static constexpr int kWeightBytes = Tile<DT>::kConsumerWarps * 32 * (16 + 8);
     static constexpr int kScratch = kMergeBytes > kWeightBytes ? kMergeBytes : kWeightBytes;
     static constexpr int kBarOff = (kRing > kScratch ? kRing : kScratch);
     static constexpr int kFullOff = kBarOff;
@@ -481,14 +485,9 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     // kernel, so it may be read while the selection is still finishing.
     if (a.early_q) load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
     pdl_wait();  // upstream kernels (append, select) are complete past here
-    if (!a.early_q) load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
+    pdl_launch_dependents();
     int cnt = DENSE ? a.NB : a.sel_cnt[bg];
     cnt = max(0, min(cnt, a.NB));
-    const int beg = static_cast<int>((static_cast<long long>(split) * cnt) / a.splits);
-    const int end = static_cast<int>((static_cast<long long>(split + 1) * cnt) / a.splits);
-    const int n = end - beg;
-    __syncthreads();
-    pdl_launch_dependents();
 
     const size_t row0 = static_cast<size_t>(bg) * a.max_seq;  // first token row of (b, g)
     WarpState<GC> st;
@@ -498,17 +497,32 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     for (int h = 0; h < GC; ++h) st.acc[h][0] = st.acc[h][1] = make_float2(0.0f, 0.0f);
     if (warp == TL::kConsumerWarps) {
         // ------------------------------------------------------ producer
+        // The split's list positions: its share [pb, pe) of the planned
+        // length, then (only when sel_cnt passes that length) every
+        // splits-th position beyond it, from plan_blocks + split on.
         const uint64_t pol = l2_policy_evict_first();
-        const int32_t *list = a.sel_idx + static_cast<size_t>(bg) * a.nbmax + beg;
-        int issued = 0;
+        const int32_t *list = a.sel_idx + static_cast<size_t>(bg) * a.nbmax;
+        const int S = a.splits, MB = a.plan_blocks;
+        const int pb = static_cast<int>((static_cast<long long>(split) * MB) / S);
+        const int pe = static_cast<int>((static_cast<long long>(split + 1) * MB) / S);
+        // the share's first list entries, read while cnt is in flight (pe <= NB <= nbmax)
+        int pre = 0;
+        if (!DENSE && lane < pe - pb) pre = list[pb + lane];
+        const int n_own = max(0, min(pe, cnt) - pb);
+        const int x0 = MB + split;
+        const int n = n_own + (cnt > x0 ? (cnt - x0 + S - 1) / S : 0);
+        int i = 0;  // stage sequence number
         bool ok = true;
         for (int i0 = 0; i0 < n && ok; i0 += 32) {
-            int mine = 0;
-            if (i0 + lane < n) mine = DENSE ? beg + i0 + lane : list[i0 + lane];
             const int m = min(32, n - i0);
+            const int idx = i0 + lane;
+            int mine = 0;
+            if (idx < n) {
+                const int pos = idx < n_own ? pb + idx : x0 + (idx - n_own) * S;
+                mine = DENSE ? pos : (i0 == 0 && idx < n_own ? pre : list[pos]);
+            }
             for (int j = 0; j < m; ++j) {
                 const int blk = __shfl_sync(kFull, mine, j);
-                const int i = i0 + j;
                 const int s = i % TL::kStages;
                 if (lane == 0) {
                     if (i >= TL::kStages)
@@ -536,7 +550,6 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                             report_status(a.dev_status, KVD_ERR_INVALID);
                             mbar_arrive(&full[s]);
                         }
-                        issued = i + 1;
                     } else {
                         *abort_flag = 1;
                         report_status(a.dev_status, KVD_ERR_TIMEOUT);
@@ -544,17 +557,38 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 }
                 ok = __shfl_sync(kFull, ok, 0);
                 if (!ok) break;
+                ++i;
             }
+        }
+        const int issued = i;
+        // one end marker per consumer group (stages i, i+1, ...)
+        for (int j = 0; j < TL::kGroups && ok; ++j, ++i) {
+            const int s = i % TL::kStages;
+            if (lane == 0) {
+                if (i >= TL::kStages)
+                    ok = mbar_wait(&empty[s], ((i / TL::kStages) - 1) & 1, abort_flag);
+                if (ok) {
+                    stage_blk[s] = kEndMark;
+                    mbar_arrive(&full[s]);
+                } else {
+                    *abort_flag = 1;
+                    report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                }
+            }
+            ok = __shfl_sync(kFull, ok, 0);
         }
         if (lane == 0) *issued_s = issued;
     } else {
         // ------------------------------------------------------ consumers
+        if (!a.early_q) load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
+        // the query words and coefficients are visible to every consumer warp
+        asm volatile("bar.sync 1, %0;" ::"r"(TL::kConsumerWarps * 32) : "memory");
         float *pw = pw_all + warp * (kTokensPerWarp * 4 * 2);
         const int group = warp / kWarpsPerGroup, wg = warp % kWarpsPerGroup;
         if constexpr (DT == KVD_INT8) {
             QRegsI8<GC> qr;
             load_qregs_i8<GC>(q_s, lane >> 2, lane & 3, qr);
-            for (int i = group; i < n; i += TL::kGroups) {
+            for (int i = group;; i += TL::kGroups) {
                 const int s = i % TL::kStages;
                 const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
                 if (!__all_sync(kFull, ok)) {
@@ -565,6 +599,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     break;
                 }
                 const int blk = stage_blk[s];
+                if (blk == kEndMark) break;
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
                     consume_int8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, coef,
@@ -576,7 +611,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         } else {
             QRegsF16<GC> qr;
             load_qregs_f16<GC>(q_s, lane & 7, qr);
-            for (int i = group; i < n; i += TL::kGroups) {
+            for (int i = group;; i += TL::kGroups) {
                 const int s = i % TL::kStages;
                 const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
                 if (!__all_sync(kFull, ok)) {
@@ -587,6 +622,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     break;
                 }
                 const int blk = stage_blk[s];
+                if (blk == kEndMark) break;
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
                     consume_f16<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, qr, pw,
@@ -673,68 +709,85 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     if (single) return;
 
     // ---- the last CTA of this problem to arrive merges all splits
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(&a.counters[prob], 1u);
-        *last_flag = prev == static_cast<unsigned>(a.splits - 1);
-    }
+    __syncthreads();  // every partial store of the CTA precedes the release
+    if (tid == 0)
+        *last_flag = atomic_add_acq_rel_gpu(&a.counters[prob], 1u) ==
+                     static_cast<unsigned>(a.splits - 1);
     __syncthreads();
     if (!*last_flag) return;
-    __threadfence();
+    // Thread (part, h, 4 channels) merges the splits of its part online:
+    // one batch of loads (maxima, sums, accumulators of kMergeBatch splits)
+    // in flight at a time, rescaled onto the running maximum.  The parts
+    // then merge in shared memory (the ring).
     const int S = a.splits;
     const float *p0 = a.partials + static_cast<size_t>(prob) * S * GC * kPartStride;
-    float *ms = reinterpret_cast<float *>(smem + SL::kStagesOff);  // [S][GC] maxima -> weights
-    for (int i = tid; i < S * GC; i += TL::kThreads)
-        ms[i] = __ldcg(p0 + static_cast<size_t>(i) * kPartStride);
-    __syncthreads();
-    if (warp < GC) {
-        const int h = warp;
-        float M = kNegBig;
-        for (int s = lane; s < S; s += 32) M = fmaxf(M, ms[s * GC + h]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        float L = 0.0f;
-        for (int s = lane; s < S; s += 32) {
-            const float wgt = exp2f(ms[s * GC + h] - M);
-            ms[s * GC + h] = wgt;
-            L = fmaf(wgt, __ldcg(p0 + static_cast<size_t>(s * GC + h) * kPartStride + 1), L);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
-        if (lane == 0) l_tot[h] = L;
-    }
-    __syncthreads();
-    if (tid < GC * 32) {
-        const int h = tid >> 5, d4 = tid & 31;
-        const float *col = p0 + h * kPartStride + kAccOff + 4 * d4;
+    constexpr int kParts = TL::kConsumerWarps / GC;
+    constexpr int kMergeBatch = 10;
+    float *mrow = reinterpret_cast<float *>(smem + SL::kStagesOff);  // [kParts][GC] m, l
+    float4 *arow = reinterpret_cast<float4 *>(mrow + 2 * TL::kConsumerWarps * 4);
+    if (warp < TL::kConsumerWarps) {
+        const int hd = tid % (GC * 32), part = tid / (GC * 32);
+        const int h = hd >> 5, d4 = hd & 31;
+        const int s_beg = (S * part) / kParts, s_end = (S * (part + 1)) / kParts;
+        const float *base = p0 + h * kPartStride;
+        float M = kNegBig, L = 0.0f;
         float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        int s = 0;
-        for (; s + 8 <= S; s += 8) {
-            float4 r[8];
+        for (int s0 = s_beg; s0 < s_end; s0 += kMergeBatch) {
+            float m[kMergeBatch], l[kMergeBatch];
+            float4 r[kMergeBatch];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                r[u] = __ldcg(reinterpret_cast<const float4 *>(
-                    col + static_cast<size_t>(s + u) * GC * kPartStride));
+            for (int u = 0; u < kMergeBatch; ++u) {
+                const float *row = base + static_cast<size_t>(s0 + u) * GC * kPartStride;
+                const bool in = s0 + u < s_end;
+                m[u] = in ? __ldcg(row) : kNegBig;
+                l[u] = in ? __ldcg(row + 1) : 0.0f;
+                r[u] = in ? __ldcg(reinterpret_cast<const float4 *>(row + kAccOff + 4 * d4))
+                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+            float mb = M;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float wgt = ms[(s + u) * GC + h];
+            for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, m[u]);
+            const float al = exp2f(M - mb);
+            L *= al;
+            A.x *= al;
+            A.y *= al;
+            A.z *= al;
+            A.w *= al;
+#pragma unroll
+            for (int u = 0; u < kMergeBatch; ++u) {
+                const float wgt = exp2f(m[u] - mb);
+                L = fmaf(wgt, l[u], L);
                 A.x = fmaf(wgt, r[u].x, A.x);
                 A.y = fmaf(wgt, r[u].y, A.y);
                 A.z = fmaf(wgt, r[u].z, A.z);
                 A.w = fmaf(wgt, r[u].w, A.w);
             }
+            M = mb;
         }
-        for (; s < S; ++s) {
-            const float4 r = __ldcg(reinterpret_cast<const float4 *>(
-                col + static_cast<size_t>(s) * GC * kPartStride));
-            const float wgt = ms[s * GC + h];
+        if (d4 == 0) {
+            mrow[(part * GC + h) * 2] = M;
+            mrow[(part * GC + h) * 2 + 1] = L;
+        }
+        arow[tid] = A;
+    }
+    __syncthreads();
+    if (tid < GC * 32) {
+        const int h = tid >> 5, d4 = tid & 31;
+        float M = kNegBig;
+#pragma unroll
+        for (int pt = 0; pt < kParts; ++pt) M = fmaxf(M, mrow[(pt * GC + h) * 2]);
+        float L = 0.0f;
+        float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int pt = 0; pt < kParts; ++pt) {
+            const float wgt = exp2f(mrow[(pt * GC + h) * 2] - M);
+            L = fmaf(wgt, mrow[(pt * GC + h) * 2 + 1], L);
+            const float4 r = arow[pt * GC * 32 + tid];
             A.x = fmaf(wgt, r.x, A.x);
             A.y = fmaf(wgt, r.y, A.y);
             A.z = fmaf(wgt, r.z, A.z);
             A.w = fmaf(wgt, r.w, A.w);
         }
-        const float L = l_tot[h];
         const float inv = L > 0.0f ? 1.0f / L : 0.0f;
         *reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(b) * a.H + h0 + h) * kHeadDim +
                                     4 * d4) = make_float4(A.x * inv, A.y * inv, A.z * inv,
@@ -769,6 +822,7 @@ DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan 
     a.NB = g.NB;
     a.splits = p.splits;
     a.subgroups = p.subgroups;
+    a.plan_blocks = p.blocks;
     a.scale_log2 = scale * kLog2e;
     return a;
 }

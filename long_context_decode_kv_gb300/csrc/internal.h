@@ -20,11 +20,14 @@ struct Geom {
     int nbmax;                        // max_seq / 64
 };
 
-// Decode split plan: grid = (splits, B * Hkv * subgroups).
+// Decode split plan: grid = (splits, B * Hkv * subgroups).  Split s attends
+// the list positions [s * blocks / splits, (s + 1) * blocks / splits), and
+// positions past `blocks` (a sel_cnt above the planned bound) round-robin.
 struct DecodePlan {
     int heads_per_cta;  // query heads handled by one CTA (<= 4)
     int subgroups;      // G / heads_per_cta
     int splits;         // CTAs per (sequence, KV head, subgroup)
+    int blocks;         // list length planned for (max_sel, at most NB)
 };
 
 DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count);
@@ -34,15 +37,14 @@ int device_sm_count();
 cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_new, int n_new,
                           cudaStream_t st, bool pdl);
 
-// Scratch of the selection (workspace regions; hist and ticket are zero
+// Scratch of the selection (workspace regions; range and ticket are zero
 // between calls, and every completed call leaves them zero).
 struct SelScratch {
     uint32_t *keys;    // [B*Hkv][round_up(candidates, 4)] keys
-    int *hist;         // [hist_rows][select_hist_bytes()/4] top-digit histograms
-    unsigned *ticket;  // [hist_rows] arrival counters
-    int hist_rows;     // problems that may split over several CTAs need a row each
+    unsigned *range;   // [range_rows][2] key range of the problem (max, ~min)
+    unsigned *ticket;  // [range_rows] arrival counters
+    int range_rows;    // problems that may split over several CTAs need a row each
 };
-size_t select_hist_bytes();
 
 // The one token a decode step appends ([B, 1, Hkv, 128] f16 each) and the
 // cache length before it.

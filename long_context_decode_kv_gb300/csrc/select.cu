@@ -84,8 +84,6 @@ SelArgs base_args(const kvd_cache &c, const Geom &g, const float *q) {
 
 int max_select_blocks() { return kMaxSelectBlocks; }
 
-size_t select_hist_bytes() { return kH1 * sizeof(int); }
-
 cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int k_sel,
                           int sink_tokens, int recent_tokens, int32_t *sel_idx,
                           int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st, bool pdl,
@@ -122,7 +120,7 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
     a.n = n_cand;
     a.keys = scr.keys;
     a.ldk = (n_cand + 3) / 4 * 4;
-    a.hist = scr.hist;
+    a.range = scr.range;
     a.ticket = scr.ticket;
     a.sel_idx = sel_idx;
     a.sel_cnt = sel_cnt;

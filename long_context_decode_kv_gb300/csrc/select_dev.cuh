@@ -17,14 +17,15 @@
 // select_kernel: the candidate blocks of a problem (sequence, KV head) are
 // split over X CTAs.  Each CTA streams the bounds (512 B per block) of its
 // range through a TMA ring in shared memory, turns every block's group bound
-// into an order-preserving u32 key (written to global scratch), and
-// histograms the keys' top 11 bits in shared memory.  It adds that
-// histogram into the problem's global one and takes a ticket; the last CTA
-// of the problem to arrive finishes the selection alone: the keff-th largest
-// key T by radix select (the top digit from the global histogram, then bits
-// 20-10 and 9-0 over the problem's keys, held in shared memory), then the
-// ascending list written warp by warp in index order.  No CTA waits for
-// another, so problems finish while others are still being scored.
+// into an order-preserving u32 key (written to global scratch), and folds
+// the keys' range [kmin, kmax] into the problem's.  It then takes a ticket;
+// the last CTA of the problem to arrive finishes the selection alone, with
+// the problem's keys in shared memory: the keff-th largest key T by a radix
+// select whose first digit bins (key - kmin) over the keys' actual range
+// (bounds of one problem are close together, so the top bits of the keys
+// barely differ), one pass that marks the keys above T's bin and collects
+// the few keys inside it, digits of those keys' low bits, then the
+// ascending list written in index order.  No CTA waits for another.
 #pragma once
 
 #include "append_dev.cuh"
@@ -48,9 +49,24 @@ constexpr int kScoreStageBytes = kStageBlocks * kBoundRowBytes;  // 32 KiB
 constexpr int kMaxSelectBlocks = 49152;
 constexpr int kMaxCtasPerProblem = 1024;
 
-// Radix digits of a key, from the top: bits 31-21, 20-10, 9-0.
-constexpr int kShift1 = 21, kShift2 = 10;
-constexpr int kH1 = 1 << 11, kH2 = 1 << 11, kH3 = 1 << 10;
+// Radix select over v = key - kmin: the first digit is v >> shift with
+// shift the least that leaves at most kBins1 bins; later digits take up to
+// kSubBits of the bits below.
+constexpr int kBins1Bits = 11;
+constexpr int kBins1 = 1 << kBins1Bits;
+constexpr int kSubBits = 11;
+constexpr int kSubBins = 1 << kSubBits;
+// Keys the last CTA keeps in shared memory (the rest of the ring is its
+// scratch); a larger problem's keys are read from L2.
+constexpr int kRingKeys = 32768;
+constexpr int kMaxWords = (kMaxSelectBlocks + 31) / 32;
+// Keys of the threshold bin collected for the later digits, and the most
+// that are ranked directly (against each other) instead.
+constexpr int kCandCap = 2560;
+constexpr int kRankMax = 256;
+constexpr int kScratchBytes = kBins1 * 4 + 2 * kMaxWords * 4 + kCandCap * 8;
+static_assert(kRingKeys * 4 + kScratchBytes <= kScoreStages * kScoreStageBytes,
+              "keys and tail scratch must fit the ring");
 
 enum TopkMode { kTakeNone = 0, kTakeAll = 1, kTakeTopK = 2 };
 enum SelMode { kExport = 0, kSelect = 1 };
@@ -169,7 +185,7 @@ struct SelArgs {
     uint32_t *keys;        // [P][ldk] keys (scratch)
     int ldk;
     float *ub;             // kExport: [P][n] bounds
-    int *hist;             // [P][kH1] top-digit histograms (zero between calls)
+    unsigned *range;       // [P][2] max key, ~min key (zero between calls)
     unsigned *ticket;      // [P] arrival counters (zero between calls)
     int32_t *sel_idx, *sel_cnt;
     int NB, rb, keff;
@@ -194,6 +210,8 @@ struct RadixShared {
     uint64_t kbar;  // bulk copy of the keys (last CTA)
     int wsum[kScoreWarps + 1];
     int digit, above, last;
+    unsigned kmin, kmax;  // the CTA's, then the problem's, key range
+    int ccount;           // keys collected from the threshold bin
 };
 
 // Digit of the krem-th largest key from a shared-memory histogram of NBINS
@@ -264,15 +282,15 @@ struct SelShared {
     int abort, issued;
 };
 
-// Count, into hist, the digit (key >> DSHIFT) & (NBINS - 1) of every key
-// whose bits above MSHIFT equal match; every other key counts in the spare
-// bin hist[NBINS], so each key takes one atomic and no branch (a branch per
-// key costs more than the atomic).  Keys are read 16 per thread per round
-// into registers before any atomic is issued, so the loads overlap and the
-// shared atomics pipeline.
-template <int MSHIFT, int DSHIFT, int NBINS>
-__device__ __forceinline__ void radix_count(const uint32_t *keys, int n, uint32_t match,
-                                            int *hist) {
+// Count, into hist, the digit ((key - kmin) >> lo) & dmask of every key
+// j < n whose bits above hi, (key - kmin) >> hi, equal prefix (hi < 32).
+// PADDED: the row's keys up to the next multiple of 4 are counted too.
+// Keys are read 16 per thread per round into registers before any atomic is
+// issued, so the loads overlap and the shared atomics pipeline.
+template <bool ALL, bool PADDED = false>
+__device__ __forceinline__ void count_digits(const uint32_t *keys, int n, uint32_t kmin, int hi,
+                                             uint32_t prefix, int lo, uint32_t dmask,
+                                             int *hist) {
     const int nq = (n + 3) / 4;
     const uint4 *k4p = reinterpret_cast<const uint4 *>(keys);
     for (int q0 = threadIdx.x; q0 < nq; q0 += 4 * kScoreThreads) {
@@ -288,66 +306,24 @@ __device__ __forceinline__ void radix_count(const uint32_t *keys, int n, uint32_
             const uint32_t kk[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const bool hit = j + c < n && (kk[c] >> MSHIFT) == match;
-                atomicAdd(&hist[hit ? static_cast<int>((kk[c] >> DSHIFT) & (NBINS - 1)) : NBINS],
-                          1);
+                const uint32_t v = kk[c] - kmin;
+                // padded rows: whole 16-byte groups of the row count (the
+                // padding keys are taken back out by the caller)
+                if ((PADDED ? j < 4 * nq : j + c < n) && (ALL || (v >> hi) == prefix))
+                    atomicAdd(&hist[(v >> lo) & dmask], 1);
             }
         }
     }
 }
 
-// Keys the last CTA keeps in shared memory: as many as fit the ring, and few
-// enough that the two bitmaps of its list (2 * n / 32 words) fit the kH1
-// histogram ints; a larger problem is read from L2 and its bitmaps use the ring.
-constexpr int kRingKeys = (kScoreStages * kScoreStageBytes / 4) < 16 * kH1
-                              ? kScoreStages * kScoreStageBytes / 4
-                              : 16 * kH1;
-
-// Phases 3-4 of the last CTA of a problem: bits 20-0 of T by two counting
-// passes over the problem's keys, then the ascending list from bitmaps of
-// the keys above and equal to T.  ksrc: the keys (shared memory when
-// IN_SMEM, else global); words: shared scratch for 2 * ceil(n / 32) words.
-template <bool IN_SMEM>
-__device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n, int d1, int krem,
-                                              const uint32_t *ksrc, int *hist_l,
-                                              uint32_t *words, RadixShared &rs) {
+// Phase 4: the ascending list from the bitmaps of the keys above T (gtw)
+// and equal to T (eqw; the need_eq lowest-index ones are taken), plus the
+// forced sink and recent blocks, and the count.
+__device__ __forceinline__ void select_write_list(const SelArgs &a, int p, int n,
+                                                  const uint32_t *gtw, const uint32_t *eqw,
+                                                  int need_eq, RadixShared &rs) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    radix_count<kShift1, kShift2, kH2>(ksrc, n, static_cast<uint32_t>(d1), hist_l);
-    const int d2 = radix_digit<kH2>(hist_l, krem, rs);
-    const uint32_t pre2 = (static_cast<uint32_t>(d1) << (kShift1 - kShift2)) |
-                          static_cast<uint32_t>(d2);
-    radix_count<kShift2, 0, kH3>(ksrc, n, pre2, hist_l);
-    const int d3 = radix_digit<kH3>(hist_l, krem, rs);
-    const uint32_t T = (pre2 << kShift2) | static_cast<uint32_t>(d3);
-    const int need_eq = krem;  // keys equal to T to take, lowest index first
-
-    // ================================================= phase 4: the list
-    // bitmaps of the keys above / equal to T, one 32-bit word per 32
-    // consecutive candidates (a warp ballot each)
     const int nw = (n + 31) / 32;
-    uint32_t *gtw = words;
-    uint32_t *eqw = gtw + nw;
-    constexpr int kWarps = kScoreWarps + 1;
-    for (int w0 = warp; w0 < nw; w0 += 4 * kWarps) {
-        uint32_t k4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = 32 * (w0 + u * kWarps) + lane;
-            k4[u] = j < n ? ksrc[j] : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int wi = w0 + u * kWarps;
-            const int j = 32 * wi + lane;
-            const unsigned gm = __ballot_sync(kFullMask, j < n && k4[u] > T);
-            const unsigned em = __ballot_sync(kFullMask, j < n && k4[u] == T);
-            if (lane == 0 && wi < nw) {
-                gtw[wi] = gm;
-                eqw[wi] = em;
-            }
-        }
-    }
-    __syncthreads();
     // thread t owns words [t*wpt, (t+1)*wpt): an exclusive scan of the
     // packed counts (above | equal << 16; both below 2^16) orders them
     const int wpt = (nw + kScoreThreads - 1) / kScoreThreads;
@@ -380,6 +356,161 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n, in
     if (tid == 0) a.sel_cnt[p] = a.se + a.keff + (a.NB - a.rb);
 }
 
+// Phases 3-4 of the last CTA of a problem, with the problem's key range
+// [kmin, kmax] in rs: the keff-th largest key T, then the ascending list
+// from bitmaps of the keys above and equal to T.  ksrc: the keys (shared
+// memory when IN_SMEM, else global); scratch: kScratchBytes of shared memory
+// whose histogram part is zero.
+template <bool IN_SMEM>
+__device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n,
+                                              const uint32_t *ksrc, uint8_t *scratch,
+                                              RadixShared &rs) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kWarps = kScoreWarps + 1;
+    int *hist = reinterpret_cast<int *>(scratch);
+    uint32_t *gtw = reinterpret_cast<uint32_t *>(scratch + kBins1 * 4);  // [nw] keys above T
+    const int nw = (n + 31) / 32;
+    uint32_t *eqw = gtw + nw;                                           // [nw] keys equal to T
+    uint32_t *ck = gtw + 2 * kMaxWords;                                 // threshold-bin keys
+    int *ci = reinterpret_cast<int *>(ck + kCandCap);                   // and their indices
+    const uint32_t kmin = rs.kmin;
+    const uint32_t range = rs.kmax - kmin;
+    const int bits = range ? 32 - __clz(static_cast<int>(range)) : 0;
+    const int shift = bits > kBins1Bits ? bits - kBins1Bits : 0;
+
+    // ---- digit 1: the bin v >> shift of T (krem: keys still to take from it)
+    count_digits<true, IN_SMEM>(ksrc, n, kmin, 31, 0u, shift, kBins1 - 1, hist);
+    int krem = a.keff;
+    if (IN_SMEM && tid == 0) atomicAdd(&hist[0], n - (n + 3) / 4 * 4);  // padding keys (kmin)
+    if (tid == 0) rs.ccount = 0;
+    const int d1 = radix_digit<kBins1>(hist, krem, rs);
+
+    // ---- one pass: keys in bins above d1 are in; keys in bin d1 are collected.
+    // Thread t builds word t (keys 32t .. 32t+31) in registers, reading its
+    // eight 16-byte chunks in a rotated order so that the eight lanes of a
+    // quarter-warp hit distinct banks; a warp scan places the collected keys.
+    // bin d1 holds the keys in [k_lo, k_hi): v >> shift == d1
+    const uint64_t k_lo64 = static_cast<uint64_t>(kmin) + (static_cast<uint64_t>(d1) << shift);
+    const uint64_t k_hi64 = k_lo64 + (1ull << shift);
+    const uint32_t k_lo = static_cast<uint32_t>(k_lo64);          // <= kmax
+    const bool none_above = k_hi64 > 0xffffffffull;
+    const uint32_t k_hi = none_above ? 0xffffffffu : static_cast<uint32_t>(k_hi64);
+    for (int w0 = 0; w0 < nw; w0 += kScoreThreads) {
+        const int wi = w0 + tid;
+        uint32_t gmask = 0u, cmask = 0u;
+        if (wi < nw) {
+            uint32_t lmask = 0u;
+            const uint4 *k4 = reinterpret_cast<const uint4 *>(ksrc + 32 * wi);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int ch = (i + wi) & 7;
+                const int jb = 32 * wi + 4 * ch;
+                const uint4 w = jb < n ? k4[ch] : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t kk[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (kk[e] >= k_hi) gmask |= 1u << (4 * ch + e);
+                    if (kk[e] >= k_lo) lmask |= 1u << (4 * ch + e);
+                }
+            }
+            // keys past n (padding or beyond the row) are dropped here
+            const int valid = n - 32 * wi;
+            const uint32_t vmask = valid >= 32 ? 0xffffffffu : ((1u << valid) - 1u);
+            if (none_above) gmask = 0u;
+            gmask &= vmask;
+            cmask = lmask & ~gmask & vmask;
+            gtw[wi] = gmask;
+            eqw[wi] = 0u;
+        }
+        const int cn = __popc(cmask);
+        if (__any_sync(kFullMask, cn != 0)) {
+            const int incl = warp_inclusive_scan(cn, lane);
+            int at = 0;
+            if (lane == 31) at = atomicAdd(&rs.ccount, incl);
+            at = __shfl_sync(kFullMask, at, 31) + incl - cn;
+            for (uint32_t mm = cmask; mm; mm &= mm - 1u, ++at) {
+                const int j = 32 * wi + (__ffs(mm) - 1);
+                if (at < kCandCap) {
+                    ck[at] = ksrc[j];
+                    ci[at] = j;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int m = rs.ccount;
+    const bool compact = m <= kCandCap;
+    if (m <= kRankMax) {
+        // few keys in the bin: each one's rank among them (key descending,
+        // index ascending) decides it; the krem best join the list
+        for (int c = warp; c < m; c += kWarps) {
+            const uint32_t kc = ck[c];
+            const int jc = ci[c];
+            int beats = 0;
+            for (int o = lane; o < m; o += 32) {
+                const uint32_t ko = ck[o];
+                beats += ko > kc || (ko == kc && ci[o] < jc);
+            }
+            beats = __reduce_add_sync(kFullMask, beats);
+            if (lane == 0 && beats < krem) atomicOr(&gtw[jc >> 5], 1u << (jc & 31));
+        }
+        __syncthreads();
+        select_write_list(a, p, n, gtw, eqw, 0, rs);
+        return;
+    }
+
+    // ---- the bits of v below the bin, kSubBits at a time, over bin d1's keys
+    // (the collected ones, or every key again when too many were in the bin)
+    uint32_t prefix = static_cast<uint32_t>(d1);
+    int hi = shift;
+    while (hi > 0) {
+        const int db = hi < kSubBits ? hi : kSubBits;
+        const int lo = hi - db;
+        const uint32_t dmask = (1u << db) - 1u;
+        if (compact) {
+            for (int c = tid; c < m; c += kScoreThreads) {
+                const uint32_t v = ck[c] - kmin;
+                if ((v >> hi) == prefix) atomicAdd(&hist[(v >> lo) & dmask], 1);
+            }
+        } else {
+            count_digits<false>(ksrc, n, kmin, hi, prefix, lo, dmask, hist);
+        }
+        const int d = radix_digit<kSubBins>(hist, krem, rs);
+        prefix = (prefix << db) | static_cast<uint32_t>(d);
+        hi = lo;
+    }
+    const uint32_t T = kmin + prefix;
+    const int need_eq = krem;  // keys equal to T to take, lowest index first
+
+    // ---- bin d1's keys above / equal to T join the bitmaps
+    if (compact) {
+        for (int c = tid; c < m; c += kScoreThreads) {
+            const uint32_t k = ck[c];
+            const int j = ci[c];
+            if (k > T)
+                atomicOr(&gtw[j >> 5], 1u << (j & 31));
+            else if (k == T)
+                atomicOr(&eqw[j >> 5], 1u << (j & 31));
+        }
+    } else {
+        for (int wi = warp; wi < nw; wi += kWarps) {
+            const int j = 32 * wi + lane;
+            const uint32_t k = j < n ? ksrc[j] : 0u;
+            const bool inbin = j < n && ((k - kmin) >> shift) == static_cast<uint32_t>(d1);
+            const unsigned gm = __ballot_sync(kFullMask, inbin && k > T);
+            const unsigned em = __ballot_sync(kFullMask, inbin && k == T);
+            if (lane == 0) {
+                gtw[wi] |= gm;
+                eqw[wi] = em;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ================================================= phase 4: the list
+    select_write_list(a, p, n, gtw, eqw, need_eq, rs);
+}
+
 // CTA (x, p): candidate blocks j in [x*R, min(n, (x+1)*R)) of problem p,
 // i.e. cache blocks se + j.  Their bounds stream through a TMA ring (stages
 // of 64 blocks; warp 16 produces, warps 0..15 consume, warp w scoring blocks
@@ -395,7 +526,6 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kScoreStages * kScoreStageBytes);
     uint64_t *empty = full + kScoreStages;
     float *q_s = reinterpret_cast<float *>(empty + kScoreStages);
-    int *hist_l = reinterpret_cast<int *>(q_s + G * kHeadDim);  // kH1 ints (kSelect)
     volatile int *abort_flag = &s_abort;
 
     const int b = p / a.Hkv, g = p % a.Hkv;
@@ -413,10 +543,10 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
         mbar_init(&rs.kbar, 1);
         s_abort = 0;
         s_issued = 0;
+        rs.kmin = 0xffffffffu;
+        rs.kmax = 0u;
         fence_barrier_init();
     }
-    if (MODE == kSelect)
-        for (int i = tid; i < kH1; i += kScoreThreads) hist_l[i] = 0;
     __syncthreads();
     // overlap: inside a decode step whose appended token lands in a forced
     // block, the candidate bounds and the query are complete before the
@@ -458,6 +588,7 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
         float2 qreg[NH][8];
         if constexpr (G <= 4) load_qpairs<NH>(q_s, 0, e, qreg);
         const int sw = chunk_swap(e);
+        uint32_t tmin = 0xffffffffu, tmax = 0u;  // range of this thread's keys
         for (int si = 0; si < nstage; ++si) {
             const int s = si % kScoreStages;
             const bool ok = mbar_wait(&full[s], (si / kScoreStages) & 1, abort_flag);
@@ -500,11 +631,20 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
                     if constexpr (MODE == kSelect) {
                         const uint32_t key = float_to_key(sc[ps]);
                         a.keys[static_cast<size_t>(p) * a.ldk + jr[ps]] = key;
-                        atomicAdd(&hist_l[key >> kShift1], 1);
+                        tmin = min(tmin, key);
+                        tmax = max(tmax, key);
                     } else {
                         a.ub[static_cast<size_t>(p) * a.n + jr[ps]] = sc[ps];
                     }
                 }
+            }
+        }
+        if constexpr (MODE == kSelect) {
+            tmin = __reduce_min_sync(kFullMask, tmin);
+            tmax = __reduce_max_sync(kFullMask, tmax);
+            if (lane == 0) {
+                atomicMin(&rs.kmin, tmin);
+                atomicMax(&rs.kmax, tmax);
             }
         }
     }
@@ -539,27 +679,20 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
     const int n = a.n;
     const uint32_t *kp = a.keys + static_cast<size_t>(p) * a.ldk;
     const bool in_smem = n <= kRingKeys;
-    uint32_t *s_keys = reinterpret_cast<uint32_t *>(ring);
     if (X > 1) {
-        int *hg = a.hist + static_cast<size_t>(p) * kH1;
-        for (int i = tid; i < kH1; i += kScoreThreads) {
-            const int v = hist_l[i];
-            if (v != 0) {
-                atomicAdd(&hg[i], v);
-                hist_l[i] = 0;
-            }
+        // this CTA's key range into the problem's (max key, ~min key: both
+        // zero-based maxima), then the ticket; its release covers the keys
+        __syncthreads();
+        if (tid == 0) {
+            unsigned *rg = a.range + 2 * static_cast<size_t>(p);
+            atomicMax(rg, rs.kmax);
+            atomicMax(rg + 1, ~rs.kmin);
+            rs.last = atomic_add_acq_rel_gpu(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
         }
-    }
-    __threadfence();  // this CTA's keys (and histogram counts) are out
-    __syncthreads();
-    if (X > 1) {
-        if (tid == 0)
-            rs.last = atomicAdd(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
         __syncthreads();
         if (!rs.last) return;
-        // the last CTA of the problem: every key and histogram count is in
-        __threadfence();
     }
+    // the last CTA of the problem: every key is in
     if (in_smem && warp == kScoreWarps) {
         // the problem's keys (L2-resident) into the ring by bulk copies; they
         // were written by ordinary stores, so order those before the async proxy
@@ -573,20 +706,26 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
                         min(static_cast<uint32_t>(kScoreStageBytes), bytes - off), &rs.kbar,
                         l2_policy_evict_first());
     }
-    if (X > 1) {
-        int *hg = a.hist + static_cast<size_t>(p) * kH1;
-        for (int i = tid * 4; i < kH1; i += kScoreThreads * 4) {
-            int4 *src = reinterpret_cast<int4 *>(hg + i);
-            *reinterpret_cast<int4 *>(hist_l + i) = __ldcg(src);
-            __stcg(src, make_int4(0, 0, 0, 0));
-        }
-        if (tid == 0) a.ticket[p] = 0u;
+    // tail scratch: the ring past the keys (the histogram part zeroed)
+    uint8_t *scratch = ring + (in_smem ? kRingKeys * 4 : 0);
+    {
+        int4 *h4 = reinterpret_cast<int4 *>(scratch);
+        for (int i = tid; i < kBins1 / 4; i += kScoreThreads) h4[i] = make_int4(0, 0, 0, 0);
+    }
+    if (X > 1 && tid == 0) {
+        unsigned *rg = a.range + 2 * static_cast<size_t>(p);
+        rs.kmax = __ldcg(rg);
+        rs.kmin = ~__ldcg(rg + 1);
+        __stcg(rg, 0u);  // leave the words ready for the next call
+        __stcg(rg + 1, 0u);
+        a.ticket[p] = 0u;
     }
 
     // ================================================= phase 3: T
-    int krem = a.keff;
-    const int d1 = radix_digit<kH1>(hist_l, krem, rs);
     if (in_smem && !mbar_wait(&rs.kbar, 0, abort_flag)) s_abort = 1;
+    // the row's padding keys (up to 3 past n) read as kmin: bin 0, taken back out
+    if (in_smem && tid < a.ldk - n && !s_abort)
+        reinterpret_cast<uint32_t *>(ring)[n + tid] = rs.kmin;
     if (__syncthreads_or(s_abort)) {
         if (tid == 0) {
             report_status(a.dev_status, KVD_ERR_TIMEOUT);
@@ -599,15 +738,14 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
     // the rest reads the keys from shared memory, or from L2 for a problem too
     // large for the ring; each variant is compiled with its address space known
     if (in_smem)
-        select_finish<true>(a, p, n, d1, krem, s_keys, hist_l, reinterpret_cast<uint32_t *>(hist_l), rs);
+        select_finish<true>(a, p, n, reinterpret_cast<const uint32_t *>(ring), scratch, rs);
     else
-        select_finish<false>(a, p, n, d1, krem, kp, hist_l, s_keys, rs);
+        select_finish<false>(a, p, n, kp, scratch, rs);
 }
 
 template <int G>
 constexpr int select_smem_bytes() {
-    return kScoreStages * kScoreStageBytes + 2 * kScoreStages * 8 + G * kHeadDim * 4 +
-           kH1 * 4 + 64;  // + the spare bin of the counting passes
+    return kScoreStages * kScoreStageBytes + 2 * kScoreStages * 8 + G * kHeadDim * 4;
 }
 
 }  // namespace

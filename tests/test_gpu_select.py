@@ -169,3 +169,47 @@ def test_select_large_problem_keys_from_l2(nb, k_sel, G):
     assert n == len(want) and np.all(np.diff(got) > 0)
     for j in set(got.tolist()) ^ set(want.tolist()):
         assert abs(ub[j] - kth) <= TIE_REL * max(abs(kth), mag[j]), (j, ub[j], kth)
+
+
+@pytest.mark.parametrize("cluster,nb", [(1000, 8192), (3000, 8192), (3000, 40000)])
+def test_select_crowded_threshold_bin(cluster, nb):
+    # Bounds are written so that each block's bound is one chosen f16 value
+    # (q = e_0, channel 0's kmin = kmax = value, every other channel 0):
+    # two outliers far above the rest, `cluster` blocks at 1 + 2^-10,
+    # `cluster` at exactly 1, the rest at 0.5, in seeded order.  The K-th
+    # pick lands among the exact ties at 1, which one bin of the first radix
+    # digit holds together with the 1 + 2^-10 keys.  With 1000 per value the
+    # bin's keys are collected and refined apart; with 3000 there are too
+    # many to collect and the refinement re-reads every key (40000 blocks:
+    # from L2).  Exact ties leave no freedom: the list must equal the
+    # oracle's, lowest indices first.
+    B, Hkv, G = 1, 1, 1
+    L = nb * 64 - 17
+    gc = kvd.KVCache(kvd.F16, B, Hkv, nb * 64, device=dev())
+    cand = np.arange(1, nb - 5)  # clear of the sink block and the recent window
+    rng = np.random.default_rng(91)
+    perm = rng.permutation(cand)
+    vals = np.full(nb, 0.5, np.float16)
+    vals[perm[:2]] = 60000.0
+    vals[perm[2:2 + cluster]] = 1.0 + 2.0 ** -10
+    vals[perm[2 + cluster:2 + 2 * cluster]] = 1.0
+    kb = torch.zeros((B, Hkv, nb, 128, 2), dtype=torch.float16)
+    kb[0, 0, :, 0, 0] = torch.from_numpy(vals)
+    kb[0, 0, :, 0, 1] = torch.from_numpy(vals)
+    gc.t["kbounds"].copy_(kb.to(dev()))
+    gc.len = L
+    q = torch.zeros((B, Hkv * G, 128), dtype=torch.float32, device=dev())
+    q[..., 0] = 1.0
+    k_sel = 2 + cluster + cluster // 2
+    ws = kvd.make_workspace(gc, Hkv * G)
+    sel_idx = torch.full((B, Hkv, nb), -7, dtype=torch.int32, device=dev())
+    sel_cnt = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev())
+    for _ in range(2):  # the second call runs on the scratch the first left
+        kvd.select_blocks(gc, q, k_sel, 4, 256, sel_idx, sel_cnt, ws)
+        torch.cuda.synchronize()
+        ub, _, _ = oracle.block_scores(q[0].cpu().numpy(), gc.kmin[0, 0].cpu().numpy(),
+                                       gc.kmax[0, 0].cpu().numpy())
+        want, kth = oracle.select(L, 64, ub, k_sel, 4, 256)
+        assert kth == 1.0
+        n = int(sel_cnt[0, 0])
+        assert sel_idx[0, 0, :n].cpu().numpy().tolist() == want.tolist()
