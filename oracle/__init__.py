@@ -48,6 +48,9 @@ def lib():
         L.orc_qk_int8.argtypes = [i, C.c_long, p, p, p]
         L.orc_attend_int8.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, p]
         L.orc_attend_dequant.argtypes = [i, i, i, p, p, C.c_float, d, p, p, p, p, p, i, p]
+        L.orc_sparse_v_keep.argtypes = [C.c_long, p, p, d, p]
+        L.orc_attend_f16_sv.argtypes = [i, i, i, p, d, p, p, p, i, d, p, p]
+        L.orc_attend_int8_sv.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
         L.orc_decode.argtypes = [p, i, p, d, i, i, i, i, p, p, p, i]
         L.orc_decode.restype = i
         L.orc_num_threads_available.restype = i
@@ -234,10 +237,51 @@ def attend_dequant(q, K, V, ks, vs, L, blk, scale, sel=None, q_code=None, q_scal
     return out
 
 
+def sparse_v_keep(tok, lg, eps):
+    """Sparse-V keep mask (eps mode) of attended positions tok with logits lg."""
+    tok = _c(tok, np.int64)
+    lg = _c(lg, np.float64)
+    keep = np.zeros(max(tok.size, 1), np.int32)
+    lib().orc_sparse_v_keep(tok.size, _ptr(tok), _ptr(lg), float(eps), _ptr(keep))
+    return keep[:tok.size].astype(bool)
+
+
+def attend_f16_sv(q, K, V, L, blk, scale, eps, sel=None):
+    """attend_f16 with sparse-V (eps mode): (out [D], dropped mass share)."""
+    q = _c(q, np.float32)
+    K = _c(K, np.float16)
+    V = _c(V, np.float16)
+    D = q.size
+    s, n = _sel_args(sel)
+    out = np.zeros(D, np.float64)
+    dropped = C.c_double()
+    lib().orc_attend_f16_sv(D, L, blk, _ptr(q), float(scale), _ptr(K), _ptr(V), _ptr(s), n,
+                            float(eps), _ptr(out), C.byref(dropped))
+    return out, dropped.value
+
+
+def attend_int8_sv(q_code, q_scale, K, V, ks, vs, L, blk, scale, eps, sel=None):
+    """attend_int8 with sparse-V (eps mode): (out [D], dropped mass share)."""
+    q_code = _c(q_code, np.int8)
+    K = _c(K, np.int8)
+    V = _c(V, np.int8)
+    ks = _c(ks, np.float32)
+    vs = _c(vs, np.float32)
+    D = q_code.size
+    s, n = _sel_args(sel)
+    out = np.zeros(D, np.float64)
+    dropped = C.c_double()
+    lib().orc_attend_int8_sv(D, L, blk, _ptr(q_code), float(q_scale), float(scale), _ptr(K),
+                             _ptr(V), _ptr(ks), _ptr(vs), _ptr(s), n, float(eps), _ptr(out),
+                             C.byref(dropped))
+    return out, dropped.value
+
+
 def threads_available() -> int:
     return lib().orc_num_threads_available()
 
 
 __all__ = ["F16", "INT8", "OracleCache", "half_to_double", "quantize_row", "block_scores",
            "forced_range", "select", "attend_f16", "qk_int8", "attend_int8", "attend_dequant",
+           "sparse_v_keep", "attend_f16_sv", "attend_int8_sv",
            "threads_available", "lib"]

@@ -17,6 +17,8 @@
  *           "Usage", "Correctness", "Requirements and limits".
  *  [SCSA]   "SCSA: Self-Calibrating Subquadratic Attention", section
  *           "2. Mechanism" (sink / recent suffix always attended exactly).
+ *  The sparse-V (eps mode) functions follow [QUEST] "Adaptive tau (the eps
+ *  mode)" and "Compose" item 3.
  *
  * Readings taken where the pages are silent (each is listed in the design
  * notes with its reason):
@@ -30,6 +32,8 @@
  *  R5  the bound uses the raw f32 query (no softmax scale: a positive factor
  *      does not change the ranking) on both cache types.
  *  R6  attention over an empty token set returns the zero vector.
+ *  R7  sparse-V (eps mode): the mean weight a position is compared with is
+ *      taken over its 16-token chunk of the attended positions.
  *
  * Every floating-point step runs in IEEE binary64 unless a step of the
  * method fixes f32 (the quantizer's scale and quotient, R1).  Build with
@@ -335,6 +339,120 @@ void orc_attend_f16(int D, int L, int blk, const float *q, double scale,
     }
     if (n > 0)
         for (int d = 0; d < D; ++d) out[d] /= Z;   /* R6: empty set -> 0 */
+    free(lg);
+    free(tok);
+}
+
+/* ------------------------------------------------------------------ */
+/* Sparse-V, eps mode  ["Sparse Attention -- Quest-style block-selector */
+/* ...", section "Adaptive tau (the eps mode)" and "Compose" item 3]:   */
+/* inside the attended blocks, the V term of a position is dropped when */
+/* its weight is below eps times the mean weight around it, so that the */
+/* dropped share of the softmax mass stays below eps.  The positions    */
+/* stay in the softmax denominator.                                      */
+/* Reading R7 (the page leaves the extent of its running sums to the    */
+/* kernel): the mean is taken over the position's chunk, the attended   */
+/* positions t with the same t / ORC_SV_CHUNK:                          */
+/*   m_c = max_{t in c} s_t,  p_t = exp(s_t - m_c),                     */
+/*   keep V_t  iff  not (p_t < eps * (sum_{u in c} p_u) / |c|).         */
+/* keep[i] is set for the i-th position of the list tok[0..n).          */
+/* ------------------------------------------------------------------ */
+#define ORC_SV_CHUNK 16
+
+void orc_sparse_v_keep(long n, const long *tok, const double *lg, double eps, int *keep)
+{
+    long i = 0;
+    while (i < n) {
+        long j = i;
+        while (j < n && tok[j] / ORC_SV_CHUNK == tok[i] / ORC_SV_CHUNK) ++j;
+        double m = -INFINITY;
+        for (long u = i; u < j; ++u)
+            if (lg[u] > m) m = lg[u];
+        double sum = 0.0;
+        for (long u = i; u < j; ++u) sum += exp(lg[u] - m);
+        double thr = eps * sum / (double)(j - i);
+        for (long u = i; u < j; ++u) keep[u] = !(exp(lg[u] - m) < thr);
+        i = j;
+    }
+}
+
+/* Attention of one head with sparse-V (eps mode) over an f16 cache: as */
+/* orc_attend_f16, the numerator summing only the kept positions.       */
+/* dropped (optional): the dropped share of the softmax mass.           */
+void orc_attend_f16_sv(int D, int L, int blk, const float *q, double scale,
+                       const uint16_t *K, const uint16_t *V, const int *sel, int n_sel,
+                       double eps, double *out, double *dropped)
+{
+    long cap = (long)L + 1;
+    long *tok = (long *)malloc(sizeof(long) * (size_t)cap);
+    long n = token_list(L, blk, sel, n_sel, tok);
+    double *lg = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    int *keep = (int *)calloc((size_t)(n > 0 ? n : 1), sizeof(int));
+    double M = -INFINITY;
+    for (long i = 0; i < n; ++i) {
+        const uint16_t *k = K + (size_t)tok[i] * D;
+        double s = 0.0;
+        for (int d = 0; d < D; ++d) s += (double)q[d] * orc_half_to_double(k[d]);
+        lg[i] = scale * s;
+        if (lg[i] > M) M = lg[i];
+    }
+    orc_sparse_v_keep(n, tok, lg, eps, keep);
+    double Z = 0.0, Zd = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        double w = exp(lg[i] - M);
+        Z += w;
+        if (!keep[i]) {
+            Zd += w;
+            continue;
+        }
+        const uint16_t *vr = V + (size_t)tok[i] * D;
+        for (int d = 0; d < D; ++d) out[d] += w * orc_half_to_double(vr[d]);
+    }
+    if (n > 0)
+        for (int d = 0; d < D; ++d) out[d] /= Z;
+    if (dropped) *dropped = n > 0 ? Zd / Z : 0.0;
+    free(keep);
+    free(lg);
+    free(tok);
+}
+
+/* The same over an absmax-int8 cache (logits as orc_attend_int8).      */
+void orc_attend_int8_sv(int D, int L, int blk, const int8_t *qc, float q_scale, double scale,
+                        const int8_t *K, const int8_t *V, const float *ks, const float *vs,
+                        const int *sel, int n_sel, double eps, double *out, double *dropped)
+{
+    long cap = (long)L + 1;
+    long *tok = (long *)malloc(sizeof(long) * (size_t)cap);
+    long n = token_list(L, blk, sel, n_sel, tok);
+    double *lg = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    int *keep = (int *)calloc((size_t)(n > 0 ? n : 1), sizeof(int));
+    double M = -INFINITY;
+    for (long i = 0; i < n; ++i) {
+        int64_t dot = 0;
+        const int8_t *k = K + (size_t)tok[i] * D;
+        for (int d = 0; d < D; ++d) dot += (int64_t)qc[d] * (int64_t)k[d];
+        lg[i] = scale * ((double)dot * (double)q_scale * (double)ks[tok[i]]);
+        if (lg[i] > M) M = lg[i];
+    }
+    orc_sparse_v_keep(n, tok, lg, eps, keep);
+    double Z = 0.0, Zd = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        double w = exp(lg[i] - M);
+        Z += w;
+        if (!keep[i]) {
+            Zd += w;
+            continue;
+        }
+        double vsc = (double)vs[tok[i]];
+        const int8_t *vr = V + (size_t)tok[i] * D;
+        for (int d = 0; d < D; ++d) out[d] += w * vsc * (double)vr[d];
+    }
+    if (n > 0)
+        for (int d = 0; d < D; ++d) out[d] /= Z;
+    if (dropped) *dropped = n > 0 ? Zd / Z : 0.0;
+    free(keep);
     free(lg);
     free(tok);
 }

@@ -50,6 +50,14 @@ MUTANTS = {
     "partial_block_overrun": ("t < (long)(sel[i] + 1) * blk && t < L; ++t)",
                               "t < (long)(sel[i] + 1) * blk; ++t)"),
     "half_subnormal_exp": ("mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);"),
+    # sparse-V (eps mode)
+    "sv_one_scope_for_all": ("while (j < n && tok[j] / ORC_SV_CHUNK == tok[i] / ORC_SV_CHUNK) ++j;",
+                             "while (j < n) ++j;"),
+    "sv_le_not_lt": ("keep[u] = !(exp(lg[u] - m) < thr);", "keep[u] = !(exp(lg[u] - m) <= thr);"),
+    "sv_sum_not_mean": ("double thr = eps * sum / (double)(j - i);", "double thr = eps * sum;"),
+    "sv_dropped_out_of_denominator": (
+        "            Zd += w;\n            continue;\n        }\n        const uint16_t *vr",
+        "            Zd += w;\n            Z -= w;\n            continue;\n        }\n        const uint16_t *vr"),
 }
 
 
@@ -66,7 +74,8 @@ def _run_mutant(name, old, new, tmp):
                     "-ffp-contract=off", "-o", lib, cfile, "-lm"], check=True)
     env = dict(os.environ, ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_sparse_v.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return name, r.returncode
 
