@@ -360,6 +360,55 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+SPARSE_V_EPS = (0.0, 0.05, 0.5, 2.0)
+
+
+def run_sparse_v_sweep(args):
+    """Decode attention alone with sparse-V (eps mode) at several eps, on the
+    selection of the workloads' decode step; one JSON line per point."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    steps, warm = max(1, args.steps), max(3, args.warmup)
+    for name in ("ctx1m_int8", "qwen3_4b_gqa_32k_f16"):
+        w = synth.WORKLOADS[name]
+        q, k, v, _ = synth.make_workload(w, device=dev)
+        cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev)
+        kvd.kv_append(cache, k, v)
+        del k, v
+        ws = kvd.make_workspace(cache, w.H)
+        nbmax = cache.max_seq // 64
+        sel_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev)
+        sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev)
+        kvd.select_blocks(cache, q, w.k_sel, w.sink_tokens, w.recent_tokens, sel_idx, sel_cnt, ws)
+        max_sel = kvd.selected_count(w.L, w.k_sel, w.sink_tokens, w.recent_tokens)
+        out = torch.empty(w.B, w.H, w.D, device=dev)
+        base = None
+        for eps in SPARSE_V_EPS:
+            ms = []
+            for i in range(warm + steps):
+                flush.fill_(i & 0xFF)
+                drain.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                kvd.decode_attn_sv(cache, q, w.scale, sel_idx, sel_cnt, max_sel, eps, out, ws)
+                e1.record(stream)
+                if i >= warm:
+                    ms.append((e0, e1))
+            torch.cuda.synchronize()
+            us = statistics.mean(a.elapsed_time(b) for a, b in ms) * 1e3
+            base = us if base is None else base
+            print(json.dumps({
+                "sweep": "sparse_v", "workload": w.name, "context": w.L,
+                "kv_dtype": "int8" if w.dtype == kvd.INT8 else "f16", "eps": eps,
+                "decode_us": us, "vs_eps0": us / base, "steps": steps,
+                "l2": "write + read flush between steps"}), flush=True)
+        del cache, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -371,11 +420,14 @@ def main():
     ap.add_argument("--context", type=int, default=None,
                     help="run the workload's recipe at this context instead (a multiple "
                          "of 64; a smaller case for profiling)")
-    ap.add_argument("--sweep", choices=["context", "coverage"], default=None,
+    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v"], default=None,
                     help="instead of the bench line: sparse vs dense decode steps over the "
                          "context sweep (16K..1M, 25%% coverage) or the 128K x 8 coverage "
-                         "sweep, one JSON line per point")
+                         "sweep, or decode attention with sparse-V at several eps; one JSON "
+                         "line per point")
     args = ap.parse_args()
+    if args.sweep == "sparse_v":
+        return run_sparse_v_sweep(args)
     if args.sweep:
         return run_sweep(args)
     w = synth.WORKLOADS[args.workload]

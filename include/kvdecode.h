@@ -180,6 +180,33 @@ KVD_API kvd_status kvd_decode_attn_dense(const kvd_cache *cache, const float *q,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* Decode attention with sparse-V in eps mode  [QUEST "Adaptive tau (the   */
+/* eps mode)", "Compose" item 3: inside the attended blocks, skip the V    */
+/* work of positions whose weight is negligible, so that the dropped share */
+/* of the softmax mass stays below eps].                                    */
+/*   As kvd_decode_attn (sel_idx/sel_cnt/max_sel as there), or over every  */
+/*   block when sel_idx is NULL (then sel_cnt and max_sel are ignored),     */
+/*   except that, for each query head, the V term of position t is left out */
+/*   of the numerator when                                                  */
+/*     p_t < sparse_v_eps * mean_{u in c} p_u,   p_u = exp(s_u - max_c s)   */
+/*   where c is t's chunk: the attended positions u with u / 16 == t / 16   */
+/*   (a 16-token quarter of a 64-token block).  Every position stays in the */
+/*   softmax denominator, so out_h = sum_{kept t} w_t v_t / sum_{all t} w_t */
+/*   and the dropped share of sum_t w_t is below sparse_v_eps.              */
+/*   sparse_v_eps = 0 gives kvd_decode_attn's (or the dense call's) output  */
+/*   bit for bit; values above 16 drop every V term (out = 0).               */
+/*   The comparison runs in f32 on the GPU: a position whose p_t lies within */
+/*   rounding of the threshold may fall on either side.                     */
+/* Errors: as kvd_decode_attn; INVALID also for a negative, NaN or infinite */
+/* sparse_v_eps.                                                            */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_decode_attn_sv(const kvd_cache *cache, const float *q, int32_t n_heads,
+                              float softmax_scale, const int32_t *sel_idx,
+                              const int32_t *sel_cnt, int32_t max_sel, float sparse_v_eps,
+                              float *out, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* kvd_decode_attn without a workspace: the paper has no counterpart; this  */
 /* is a convenience of this library.  Same arguments, arithmetic and output */
 /* as kvd_decode_attn, minus workspace/workspace_bytes.                     */

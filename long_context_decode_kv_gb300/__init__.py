@@ -35,7 +35,7 @@ STATUS = {0: "KVD_OK", 1: "KVD_ERR_INVALID", 2: "KVD_ERR_UNSUPPORTED", 3: "KVD_E
 EXPORTS = ("kvd_kv_append", "kvd_select_blocks", "kvd_decode_attn", "kvd_decode_attn_dense",
            "kvd_decode_step", "kvd_decode_step_host", "kvd_workspace_bytes",
            "kvd_selected_count", "kvd_status_string", "kvd_abi_version", "kvd_debug_qk_int8",
-           "kvd_debug_scores", "kvd_decode_attn_static")
+           "kvd_debug_scores", "kvd_decode_attn_static", "kvd_decode_attn_sv")
 
 
 class KvdError(RuntimeError):
@@ -71,6 +71,8 @@ def lib():
         L.kvd_decode_attn.argtypes = [cp, p, i32, C.c_float, p, p, i32, p, p, sz, p]
         L.kvd_decode_attn_dense.argtypes = [cp, p, i32, C.c_float, p, p, sz, p]
         L.kvd_decode_attn_static.argtypes = [cp, p, i32, C.c_float, p, p, i32, p, p]
+        L.kvd_decode_attn_sv.argtypes = [cp, p, i32, C.c_float, p, p, i32, C.c_float, p, p, sz,
+                                         p]
         L.kvd_decode_step.argtypes = [cp, p, p, p, i32, C.c_float, i32, i32, i32, p, p, p, p,
                                       sz, p]
         L.kvd_decode_step_host.argtypes = [cp, p, p, p, i32, C.c_float, i32, i32, i32, p, p, p,
@@ -229,6 +231,16 @@ def decode_attn_static(cache: KVCache, q: torch.Tensor, softmax_scale: float,
         _ptr(sel_cnt), int(max_sel), _ptr(out), _stream(q, stream)))
 
 
+def decode_attn_sv(cache: KVCache, q: torch.Tensor, softmax_scale: float, sel_idx,
+                   sel_cnt, max_sel: int, sparse_v_eps: float, out: torch.Tensor,
+                   workspace: torch.Tensor, stream=None):
+    """decode_attn with sparse-V in eps mode; sel_idx None attends every block."""
+    _check("kvd_decode_attn_sv", lib().kvd_decode_attn_sv(
+        cache.ref(), _ptr(q), int(q.shape[1]), float(softmax_scale), _ptr(sel_idx),
+        _ptr(sel_cnt), int(max_sel), float(sparse_v_eps), _ptr(out), _ptr(workspace),
+        workspace.numel(), _stream(q, stream)))
+
+
 def decode_attn_dense(cache: KVCache, q: torch.Tensor, softmax_scale: float, out: torch.Tensor,
                       workspace: torch.Tensor, stream=None):
     _check("kvd_decode_attn_dense", lib().kvd_decode_attn_dense(
@@ -271,5 +283,6 @@ def debug_scores(cache: KVCache, q: torch.Tensor, ub: torch.Tensor, stream=None)
 
 __all__ = ["F16", "INT8", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
            "workspace_bytes", "make_workspace", "selected_count", "status_string", "kv_append",
-           "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static", "decode_step",
+           "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
+           "decode_attn_sv", "decode_step",
            "decode_step_host", "debug_qk_int8", "debug_scores", "synth", "EXPORTS"]

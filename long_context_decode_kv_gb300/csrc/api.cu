@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points of libkvdecode.so: argument checks on
 // the host, workspace layout, and kernel dispatch on the caller's stream.
+#include <cmath>
 #include <cstring>
 
 #include "common.cuh"
@@ -173,7 +174,8 @@ kvd_status select_impl(const kvd_cache *c, const float *q, int n_heads, int k_se
 
 kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float scale,
                        const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel, float *out,
-                       void *ws, const WsLayout &w, cudaStream_t st, bool in_step = false) {
+                       void *ws, const WsLayout &w, cudaStream_t st, bool in_step = false,
+                       float sv_eps = 0.0f) {
     const Geom g = make_geom(c, n_heads, c->len);
     const bool dense = sel_idx == nullptr;
     int max_blocks = dense ? g.NB : max_sel;
@@ -182,7 +184,8 @@ kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float sc
     const DecodePlan p = plan_decode(g, max_blocks, device_sm_count());
     return cuda_status(launch_decode(*c, g, p, q, scale, sel_idx, sel_cnt, out,
                                      ws_at<float>(ws, w.partials),
-                                     ws_at<uint32_t>(ws, w.counters), st, true, in_step));
+                                     ws_at<uint32_t>(ws, w.counters), st, true, in_step,
+                                     sv_eps));
 }
 
 kvd_status check_select_args(const kvd_cache *c, int n_heads, int k_sel, int sink, int recent) {
@@ -277,6 +280,28 @@ kvd_status kvd_decode_attn(const kvd_cache *cache, const float *q, int32_t n_hea
     if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
     return decode_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_cnt, max_sel, out,
                        workspace, w, static_cast<cudaStream_t>(stream));
+}
+
+kvd_status kvd_decode_attn_sv(const kvd_cache *cache, const float *q, int32_t n_heads,
+                              float softmax_scale, const int32_t *sel_idx,
+                              const int32_t *sel_cnt, int32_t max_sel, float sparse_v_eps,
+                              float *out, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (cache->len < 1) return KVD_ERR_INVALID;
+    if (!(sparse_v_eps >= 0.0f) || !std::isfinite(sparse_v_eps)) return KVD_ERR_INVALID;
+    if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
+    if (sel_idx) {
+        if (max_sel < 0 || !aligned(sel_idx, 4) || !sel_cnt || !aligned(sel_cnt, 4))
+            return KVD_ERR_INVALID;
+    }
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    return decode_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_idx ? sel_cnt : nullptr,
+                       sel_idx ? max_sel : 0, out, workspace, w,
+                       static_cast<cudaStream_t>(stream), false, sparse_v_eps);
 }
 
 kvd_status kvd_decode_attn_dense(const kvd_cache *cache, const float *q, int32_t n_heads,

@@ -99,9 +99,10 @@ size_t decode_partials_bytes(const Geom &g, const DecodePlan &p) {
 cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p,
                           const float *q, float scale, const int32_t *sel_idx,
                           const int32_t *sel_cnt, float *out, float *partials,
-                          uint32_t *counters, cudaStream_t st, bool pdl, bool early_q) {
+                          uint32_t *counters, cudaStream_t st, bool pdl, bool early_q,
+                          float sv_eps) {
     const DecodeArgs a = make_decode_args(c, g, p, q, scale, sel_idx, sel_cnt, out, partials,
-                                          counters, early_q);
+                                          counters, early_q, sv_eps);
     const int P_sub = g.B * g.Hkv * p.subgroups;
     const bool dense = sel_idx == nullptr;
     if (g.dtype == KVD_INT8)

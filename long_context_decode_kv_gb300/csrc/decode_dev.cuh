@@ -77,6 +77,7 @@ struct DecodeArgs {
     int32_t *dev_status;
     int Hkv, H, G, max_seq, nbmax, len, NB, splits, subgroups;
     int plan_blocks;     // list length the splits were planned for (<= NB)
+    float sv_eps;        // sparse-V (eps mode): 0 = every V term accumulated
     float scale_log2;  // softmax_scale * log2(e): logits live in base 2
     int early_q;       // q is complete before the upstream kernels finish
 };
@@ -332,6 +333,43 @@ __device__ __forceinline__ void pv_token(WarpState<GC> &st, const float *pw_tok,
     }
 }
 
+// Bits b*w of x (b = 0..n-1) that have any of their w bits set, packed into
+// bits 0..n-1: which tokens of a ballot (w lanes per token) are live.
+template <int N, int W>
+__device__ __forceinline__ uint32_t any_per_group(uint32_t x) {
+    uint32_t r = 0;
+#pragma unroll
+    for (int b = 0; b < N; ++b)
+        if ((x >> (W * b)) & ((1u << W) - 1u)) r |= 1u << b;
+    return r;
+}
+
+// Sparse-V, eps mode ("Sparse Attention -- Quest-style block-selector ...",
+// "Adaptive tau (the eps mode)"): a position's V term is dropped when its
+// weight is below eps times the mean weight of its 16-token chunk (the
+// warp's share of the block), both relative to the chunk's maximum, so the
+// dropped share of the softmax mass stays below eps.  The position stays in
+// the softmax denominator.  x: this lane's base-2 logits of NT tokens (-inf
+// past the valid ones), bm: the chunk maximum of the lane's head, nvc: the
+// chunk's valid tokens; the reduction runs over the lanes of one head
+// (lane bits RED0 and up).  Returns, per token, whether V is kept.
+template <int NT, int RED0>
+__device__ __forceinline__ void sparse_v_keep(const float (&x)[NT], float bm, int nvc, float eps,
+                                              bool (&keep)[NT]) {
+    float c[NT];
+    float cs = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        c[i] = exp2f(x[i] - bm);
+        cs += c[i];
+    }
+#pragma unroll
+    for (int o = RED0; o < 32; o <<= 1) cs += __shfl_xor_sync(kFull, cs, o);
+    const float thr = nvc > 0 ? eps * cs / static_cast<float>(nvc) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) keep[i] = !(c[i] < thr);
+}
+
 // Four signed bytes -> two exact float pairs (see s8x4_to_f32 in common.cuh).
 __device__ __forceinline__ void s8x4_to_f32x2(uint32_t w, float2 &f01, float2 &f23) {
     const uint32_t u = w ^ 0x80808080u;
@@ -350,7 +388,7 @@ __device__ __forceinline__ void s8x4_to_f32x2(uint32_t w, float2 &f01, float2 &f
 template <int GC>
 __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, const float *coef,
                                              const QRegsI8<GC> &qr, float *pw, int wg, int lane,
-                                             WarpState<GC> &st) {
+                                             WarpState<GC> &st, float sv_eps) {
     const int8_t *Ks = reinterpret_cast<const int8_t *>(stage);
     const int8_t *Vs = Ks + Tile<KVD_INT8>::kKBytes;
     const float *ksc = reinterpret_cast<const float *>(stage + 2 * Tile<KVD_INT8>::kKBytes);
@@ -373,10 +411,20 @@ __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, 
     const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
     st.l = st.l * alpha + (p0 + p1);
     st.m = m_new;
+    bool keep[2] = {true, true};
+    uint32_t live = 0xffffu;  // tokens whose V some head still needs
+    if (sv_eps > 0.0f) {
+        const float xs[2] = {x0, x1};
+        sparse_v_keep<2, 4>(xs, bm, min(max(n_valid - kTokensPerWarp * wg, 0), kTokensPerWarp),
+                            sv_eps, keep);
+        const uint32_t b0 = __ballot_sync(kFull, keep[0] && tok0 < n_valid);  // lane 4t + c
+        const uint32_t b1 = __ballot_sync(kFull, keep[1] && tok1 < n_valid);
+        live = any_per_group<8, 4>(b0) | (any_per_group<8, 4>(b1) << 8);
+    }
     constexpr int lph = 4 / GC;  // lanes per head among the quarters
     if ((c % lph) == 0) {
-        const float w0 = tok0 < n_valid ? p0 * vsc[tok0] : 0.0f;
-        const float w1 = tok1 < n_valid ? p1 * vsc[tok1] : 0.0f;
+        const float w0 = tok0 < n_valid && keep[0] ? p0 * vsc[tok0] : 0.0f;
+        const float w1 = tok1 < n_valid && keep[1] ? p1 * vsc[tok1] : 0.0f;
         *reinterpret_cast<float2 *>(pw + (t * 4 + hq) * 2) = make_float2(w0, w0);
         *reinterpret_cast<float2 *>(pw + ((t + 8) * 4 + hq) * 2) = make_float2(w1, w1);
     }
@@ -384,7 +432,15 @@ __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, 
     __syncwarp();
     const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
     const int8_t *vrow = Vs + kTokensPerWarp * wg * kHeadDim + 4 * lane;
-    if (nt == kTokensPerWarp) {
+    if (live != 0xffffu) {
+        // sparse-V dropped some tokens for every head: only the live ones
+        for (uint32_t m = live; m; m &= m - 1u) {
+            const int t2 = __ffs(m) - 1;
+            float2 f01, f23;
+            s8x4_to_f32x2(*reinterpret_cast<const uint32_t *>(vrow + t2 * kHeadDim), f01, f23);
+            pv_token<GC>(st, pw + t2 * 8, f01, f23);
+        }
+    } else if (nt == kTokensPerWarp) {
 #pragma unroll
         for (int t2 = 0; t2 < kTokensPerWarp; ++t2) {
             float2 f01, f23;
@@ -405,7 +461,7 @@ __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, 
 template <int GC>
 __device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
                                             const QRegsF16<GC> &qr, float *pw, int wg,
-                                            int lane, WarpState<GC> &st) {
+                                            int lane, WarpState<GC> &st, float sv_eps) {
     const __half *Ks = reinterpret_cast<const __half *>(stage);
     const __half *Vs = Ks + kBlock * kHeadDim;
     const int t4 = lane >> 3, e = lane & 7;
@@ -428,17 +484,42 @@ __device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
     for (int ps = 0; ps < 4; ++ps) p[ps] = exp2f(x[ps] - m_new);
     st.l = st.l * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
     st.m = m_new;
+    bool keep[4] = {true, true, true, true};
+    uint32_t live = 0xffffu;  // tokens whose V some head still needs
+    if (sv_eps > 0.0f) {
+        sparse_v_keep<4, 8>(x, bm, min(max(n_valid - kTokensPerWarp * wg, 0), kTokensPerWarp),
+                            sv_eps, keep);
+        live = 0u;
+#pragma unroll
+        for (int ps = 0; ps < 4; ++ps) {
+            const int tok = kTokensPerWarp * wg + 4 * ps + t4;
+            const uint32_t bp = __ballot_sync(kFull, keep[ps] && tok < n_valid);  // lane 8 t4 + e
+            live |= any_per_group<4, 8>(bp) << (4 * ps);
+        }
+    }
     constexpr int lph = 8 / GC;
     if ((e % lph) == 0) {
 #pragma unroll
-        for (int ps = 0; ps < 4; ++ps)
-            *reinterpret_cast<float2 *>(pw + ((4 * ps + t4) * 4 + hq) * 2) =
-                make_float2(p[ps], p[ps]);
+        for (int ps = 0; ps < 4; ++ps) {
+            const float w = keep[ps] ? p[ps] : 0.0f;
+            *reinterpret_cast<float2 *>(pw + ((4 * ps + t4) * 4 + hq) * 2) = make_float2(w, w);
+        }
     }
     rescale<GC>(st, alpha, lph);
     __syncwarp();
     const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
     const __half *vrow = Vs + kTokensPerWarp * wg * kHeadDim + 4 * lane;
+    if (live != 0xffffu) {
+        // sparse-V dropped some tokens for every head: only the live ones
+        for (uint32_t m = live; m; m &= m - 1u) {
+            const int t2 = __ffs(m) - 1;
+            const uint2 vw = *reinterpret_cast<const uint2 *>(vrow + t2 * kHeadDim);
+            const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
+            const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
+            pv_token<GC>(st, pw + t2 * 8, v01, v23);
+        }
+        return;
+    }
 #pragma unroll 4
     for (int t2 = 0; t2 < nt; ++t2) {
         const uint2 vw = *reinterpret_cast<const uint2 *>(vrow + t2 * kHeadDim);
@@ -603,7 +684,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
                     consume_int8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, coef,
-                                     qr, pw, wg, lane, st);
+                                     qr, pw, wg, lane, st, a.sv_eps);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -626,7 +707,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
                     consume_f16<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, qr, pw,
-                                    wg, lane, st);
+                                    wg, lane, st, a.sv_eps);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -799,8 +880,9 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
 DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan &p,
                             const float *q, float scale, const int32_t *sel_idx,
                             const int32_t *sel_cnt, float *out, float *partials,
-                            uint32_t *counters, bool early_q) {
+                            uint32_t *counters, bool early_q, float sv_eps) {
     DecodeArgs a = {};
+    a.sv_eps = sv_eps;
     a.early_q = early_q ? 1 : 0;
     a.k = c.k;
     a.v = c.v;

@@ -66,11 +66,13 @@ cudaError_t launch_scores_debug(const kvd_cache &c, const Geom &g, const float *
 
 // early_q: the query may be read before the upstream kernels complete (true
 // only when the caller's own earlier kernels in the same chain wrote nothing
-// the query depends on, as inside kvd_decode_step).
+// the query depends on, as inside kvd_decode_step).  sv_eps > 0: sparse-V in
+// eps mode (0: every V term is accumulated).
 cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p,
                           const float *q, float scale, const int32_t *sel_idx,
                           const int32_t *sel_cnt, float *out, float *partials,
-                          uint32_t *counters, cudaStream_t st, bool pdl, bool early_q);
+                          uint32_t *counters, cudaStream_t st, bool pdl, bool early_q,
+                          float sv_eps = 0.0f);
 
 cudaError_t launch_qk_debug(const kvd_cache &c, const Geom &g, const float *q, int32_t *dots,
                             int8_t *q_codes, float *q_scales, cudaStream_t st);
