@@ -22,6 +22,8 @@ from . import build as _build
 
 F16 = 0
 INT8 = 1
+Q8_0 = 2
+QGROUP = 32
 
 _lib = None
 
@@ -49,6 +51,10 @@ def lib():
         L.orc_attend_int8.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, p]
         L.orc_attend_dequant.argtypes = [i, i, i, p, p, C.c_float, d, p, p, p, p, p, i, p]
         L.orc_sparse_v_keep.argtypes = [C.c_long, p, p, d, p]
+        L.orc_double_to_half.argtypes = [d]
+        L.orc_double_to_half.restype = C.c_uint16
+        L.orc_quantize_group32.argtypes = [p, i, p, p]
+        L.orc_attend_q8_0.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
         L.orc_attend_f16_sv.argtypes = [i, i, i, p, d, p, p, p, i, d, p, p]
         L.orc_attend_int8_sv.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
         L.orc_decode.argtypes = [p, i, p, d, i, i, i, i, p, p, p, i]
@@ -70,7 +76,8 @@ class _OrcCache(C.Structure):
     _fields_ = [("dtype", C.c_int), ("B", C.c_int), ("Hkv", C.c_int), ("D", C.c_int),
                 ("max_seq", C.c_int), ("blk", C.c_int), ("len", C.c_int),
                 ("K", C.c_void_p), ("V", C.c_void_p), ("ks", C.c_void_p), ("vs", C.c_void_p),
-                ("kmin", C.c_void_p), ("kmax", C.c_void_p)]
+                ("kmin", C.c_void_p), ("kmax", C.c_void_p), ("kd", C.c_void_p),
+                ("vd", C.c_void_p)]
 
 
 def half_to_double(h) -> float:
@@ -90,8 +97,9 @@ def quantize_row(x):
 class OracleCache:
     """Head-major cache held in numpy arrays, filled by the oracle's own append.
 
-    K, V: [B, Hkv, max_seq, D] (float16 or int8); ks, vs: [B, Hkv, max_seq]
-    float32 (int8 only); kmin, kmax: [B, Hkv, max_seq // blk, D] float16.
+    K, V: [B, Hkv, max_seq, D] (float16, or int8 codes); ks, vs: [B, Hkv,
+    max_seq] float32 (int8 only); kd, vd: [B, Hkv, max_seq, D // 32] float16
+    group scales (q8_0 only); kmin, kmax: [B, Hkv, max_seq // blk, D] float16.
     """
 
     def __init__(self, dtype: int, B: int, Hkv: int, D: int, max_seq: int, blk: int = 64):
@@ -103,6 +111,9 @@ class OracleCache:
         self.V = np.zeros((B, Hkv, max_seq, D), kvt)
         self.ks = np.zeros((B, Hkv, max_seq), np.float32) if dtype == INT8 else None
         self.vs = np.zeros((B, Hkv, max_seq), np.float32) if dtype == INT8 else None
+        q8 = dtype == Q8_0
+        self.kd = np.zeros((B, Hkv, max_seq, D // QGROUP), np.float16) if q8 else None
+        self.vd = np.zeros((B, Hkv, max_seq, D // QGROUP), np.float16) if q8 else None
         nb = max_seq // blk
         self.kmin = np.zeros((B, Hkv, nb, D), np.float16)
         self.kmax = np.zeros((B, Hkv, nb, D), np.float16)
@@ -110,7 +121,7 @@ class OracleCache:
     def _struct(self):
         s = _OrcCache(self.dtype, self.B, self.Hkv, self.D, self.max_seq, self.blk, self.len,
                       _ptr(self.K), _ptr(self.V), _ptr(self.ks), _ptr(self.vs),
-                      _ptr(self.kmin), _ptr(self.kmax))
+                      _ptr(self.kmin), _ptr(self.kmax), _ptr(self.kd), _ptr(self.vd))
         return s
 
     def append(self, k_new, v_new):
@@ -237,6 +248,37 @@ def attend_dequant(q, K, V, ks, vs, L, blk, scale, sel=None, q_code=None, q_scal
     return out
 
 
+def double_to_half(x) -> np.float16:
+    """Nearest binary16 (ties to even), from the oracle's own rounding."""
+    return np.array([lib().orc_double_to_half(float(x))], np.uint16).view(np.float16)[0]
+
+
+def quantize_group32(x):
+    """q8_0 codes of a row (length a multiple of 32) and its float16 group scales."""
+    x = _c(x, np.float32)
+    code = np.zeros(x.size, np.int8)
+    d = np.zeros(x.size // QGROUP, np.uint16)
+    lib().orc_quantize_group32(_ptr(x), x.size, _ptr(code), _ptr(d))
+    return code, d.view(np.float16)
+
+
+def attend_q8_0(q_code, q_scale, K, V, kd, vd, L, blk, scale, sel=None, eps=0.0):
+    """q8_0 attention of one head (sparse-V at eps): (out [D], dropped mass share)."""
+    q_code = _c(q_code, np.int8)
+    K = _c(K, np.int8)
+    V = _c(V, np.int8)
+    kd = _c(kd, np.float16)
+    vd = _c(vd, np.float16)
+    D = q_code.size
+    s, n = _sel_args(sel)
+    out = np.zeros(D, np.float64)
+    dropped = C.c_double()
+    lib().orc_attend_q8_0(D, L, blk, _ptr(q_code), float(q_scale), float(scale), _ptr(K),
+                          _ptr(V), _ptr(kd), _ptr(vd), _ptr(s), n, float(eps), _ptr(out),
+                          C.byref(dropped))
+    return out, dropped.value
+
+
 def sparse_v_keep(tok, lg, eps):
     """Sparse-V keep mask (eps mode) of attended positions tok with logits lg."""
     tok = _c(tok, np.int64)
@@ -283,5 +325,6 @@ def threads_available() -> int:
 
 __all__ = ["F16", "INT8", "OracleCache", "half_to_double", "quantize_row", "block_scores",
            "forced_range", "select", "attend_f16", "qk_int8", "attend_int8", "attend_dequant",
-           "sparse_v_keep", "attend_f16_sv", "attend_int8_sv",
+           "sparse_v_keep", "attend_f16_sv", "attend_int8_sv", "Q8_0", "QGROUP",
+           "double_to_half", "quantize_group32", "attend_q8_0",
            "threads_available", "lib"]

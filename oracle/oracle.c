@@ -34,6 +34,10 @@
  *  R6  attention over an empty token set returns the zero vector.
  *  R7  sparse-V (eps mode): the mean weight a position is compared with is
  *      taken over its 16-token chunk of the attended positions.
+ *  R8  q8_0 (named, not defined, by the pages): per 32-channel group an f16
+ *      scale fl16(fl32(amax/127)) and codes round-half-even(fl32(x/d))
+ *      clamped to +-127; the query is quantized per row as for int8, and the
+ *      logit sums the exact per-group dots times the group scales.
  *
  * Every floating-point step runs in IEEE binary64 unless a step of the
  * method fixes f32 (the quantizer's scale and quotient, R1).  Build with
@@ -49,6 +53,8 @@
 
 #define ORC_F16 0
 #define ORC_INT8 1
+#define ORC_Q8_0 2
+#define ORC_QGROUP 32
 
 /* ------------------------------------------------------------------ */
 /* binary16 -> binary64, exact.  Written from the IEEE 754 binary16     */
@@ -67,6 +73,36 @@ double orc_half_to_double(uint16_t h)
     else
         mag = ldexp((double)(f + 1024), e - 25); /* (1024+f) * 2^(e-15-10) */
     return sign ? -mag : mag;
+}
+
+/* ------------------------------------------------------------------ */
+/* binary64 -> binary16, rounded to nearest, ties to even, from the      */
+/* same layout: a normal half holds (1024 + f) * 2^(e-25) for e = 1..30, */
+/* a subnormal f * 2^-24; magnitudes from 65520 up round to infinity.   */
+/* Scaling by a power of two is exact in binary64, so rounding the       */
+/* scaled value to an integer rounds the value itself.                  */
+/* ------------------------------------------------------------------ */
+uint16_t orc_double_to_half(double x)
+{
+    uint16_t sign = (uint16_t)(signbit(x) ? 0x8000 : 0);
+    double a = fabs(x);
+    if (isnan(x)) return 0x7e00;
+    if (a == 0.0) return sign;
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00);
+    int k;
+    (void)frexp(a, &k);              /* a = m * 2^k, m in [0.5, 1): a in [2^(k-1), 2^k) */
+    int e = k - 1;                   /* a in [2^e, 2^(e+1)) */
+    if (e < -14) {                   /* subnormal range: units of 2^-24 */
+        double n = nearbyint(ldexp(a, 24));
+        return (uint16_t)(sign | (uint16_t)n);  /* n == 1024 is the smallest normal */
+    }
+    double n = nearbyint(ldexp(a, 10 - e));      /* in [1024, 2048] */
+    if (n == 2048.0) {
+        n = 1024.0;
+        ++e;
+    }
+    if (e > 15) return (uint16_t)(sign | 0x7c00);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(n - 1024.0));
 }
 
 /* ------------------------------------------------------------------ */
@@ -97,9 +133,40 @@ void orc_quantize_row(const float *x, int n, int8_t *code, float *scale)
 }
 
 /* ------------------------------------------------------------------ */
+/* q8_0: absmax int8 per group of 32 channels with a binary16 scale     */
+/* (the llama.cpp cache type of [QUEST] "All-KV-types composition" and  */
+/* "The decode win lives on quantized KV"; R8):                          */
+/*   d_g = fl16(fl32(amax_g / 127)),                                     */
+/*   code = round-half-even(fl32(x / d_g)) clamped to +-127 (0 if d_g=0) */
+/* d: n / 32 binary16 bits.                                               */
+/* ------------------------------------------------------------------ */
+void orc_quantize_group32(const float *x, int n, int8_t *code, uint16_t *d)
+{
+    for (int g = 0; g < n / ORC_QGROUP; ++g) {
+        const float *xg = x + g * ORC_QGROUP;
+        double amax = 0.0;
+        for (int i = 0; i < ORC_QGROUP; ++i) {
+            double a = fabs((double)xg[i]);
+            if (a > amax) amax = a;
+        }
+        float s32 = (float)(amax / 127.0);
+        d[g] = orc_double_to_half((double)s32);
+        double dg = orc_half_to_double(d[g]);
+        for (int i = 0; i < ORC_QGROUP; ++i) {
+            if (dg == 0.0) { code[g * ORC_QGROUP + i] = 0; continue; }
+            float qg = (float)((double)xg[i] / dg);
+            double rq = nearbyint((double)qg);  /* ties to even */
+            rq = rq > 127.0 ? 127.0 : (rq < -127.0 ? -127.0 : rq);
+            code[g * ORC_QGROUP + i] = (int8_t)rq;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* Cache description (layouts of the head-major cache).                */
 /*   K, V     [B, Hkv, max_seq, D]   f16 bits or int8 codes            */
 /*   ks, vs   [B, Hkv, max_seq]      f32 (int8 cache only)             */
+/*   kd, vd   [B, Hkv, max_seq, D/32] f16 bits (q8_0 cache only)       */
 /*   kmin/kmax[B, Hkv, max_seq/blk, D] f16 bits                        */
 /* ------------------------------------------------------------------ */
 typedef struct {
@@ -107,6 +174,7 @@ typedef struct {
     void *K, *V;
     float *ks, *vs;
     uint16_t *kmin, *kmax;
+    uint16_t *kd, *vd;
 } orc_cache;
 
 static size_t row_index(const orc_cache *c, int b, int h, long t)
@@ -147,6 +215,12 @@ int orc_append(orc_cache *c, const uint16_t *k_new, const uint16_t *v_new, int n
                 if (c->dtype == ORC_F16) {
                     memcpy((uint16_t *)c->K + r * D, kin, sizeof(uint16_t) * D);
                     memcpy((uint16_t *)c->V + r * D, vin, sizeof(uint16_t) * D);
+                } else if (c->dtype == ORC_Q8_0) {
+                    const int ng = D / ORC_QGROUP;
+                    for (int d = 0; d < D; ++d) row[d] = (float)orc_half_to_double(kin[d]);
+                    orc_quantize_group32(row, D, (int8_t *)c->K + r * D, c->kd + r * ng);
+                    for (int d = 0; d < D; ++d) row[d] = (float)orc_half_to_double(vin[d]);
+                    orc_quantize_group32(row, D, (int8_t *)c->V + r * D, c->vd + r * ng);
                 } else {
                     for (int d = 0; d < D; ++d) row[d] = (float)orc_half_to_double(kin[d]);
                     orc_quantize_row(row, D, (int8_t *)c->K + r * D, &c->ks[r]);
@@ -458,6 +532,61 @@ void orc_attend_int8_sv(int D, int L, int blk, const int8_t *qc, float q_scale, 
 }
 
 /* ------------------------------------------------------------------ */
+/* q8_0 attention of one query head (R8), with sparse-V at eps (eps = 0 */
+/* keeps every V term):                                                  */
+/*   logit_t = softmax_scale * q_scale * sum_g d_g(k_t) * dot_g(t),      */
+/*   dot_g(t) = sum_{d in group g} q_code[d] * k_code_t[d]  (exact)      */
+/*   out[d]  = sum_t softmax(logit)_t * d_g(v_t) * v_code_t[d]           */
+/* qc/q_scale: the head's query quantized per row (orc_quantize_row).   */
+/* kd, vd: [max_seq, D/32] binary16 bits of one (seq, KV head).          */
+/* ------------------------------------------------------------------ */
+void orc_attend_q8_0(int D, int L, int blk, const int8_t *qc, float q_scale, double scale,
+                     const int8_t *K, const int8_t *V, const uint16_t *kd, const uint16_t *vd,
+                     const int *sel, int n_sel, double eps, double *out, double *dropped)
+{
+    const int ng = D / ORC_QGROUP;
+    long cap = (long)L + 1;
+    long *tok = (long *)malloc(sizeof(long) * (size_t)cap);
+    long n = token_list(L, blk, sel, n_sel, tok);
+    double *lg = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    int *keep = (int *)calloc((size_t)(n > 0 ? n : 1), sizeof(int));
+    double M = -INFINITY;
+    for (long i = 0; i < n; ++i) {
+        const int8_t *k = K + (size_t)tok[i] * D;
+        double acc = 0.0;
+        for (int g = 0; g < ng; ++g) {
+            int64_t dot = 0;
+            for (int d = g * ORC_QGROUP; d < (g + 1) * ORC_QGROUP; ++d)
+                dot += (int64_t)qc[d] * (int64_t)k[d];
+            acc += orc_half_to_double(kd[(size_t)tok[i] * ng + g]) * (double)dot;
+        }
+        lg[i] = scale * (double)q_scale * acc;
+        if (lg[i] > M) M = lg[i];
+    }
+    orc_sparse_v_keep(n, tok, lg, eps, keep);
+    double Z = 0.0, Zd = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        double w = exp(lg[i] - M);
+        Z += w;
+        if (!keep[i]) {
+            Zd += w;
+            continue;
+        }
+        const int8_t *vq = V + (size_t)tok[i] * D;
+        for (int d = 0; d < D; ++d)
+            out[d] += w * orc_half_to_double(vd[(size_t)tok[i] * ng + d / ORC_QGROUP]) *
+                      (double)vq[d];
+    }
+    if (n > 0)
+        for (int d = 0; d < D; ++d) out[d] /= Z;
+    if (dropped) *dropped = n > 0 ? Zd / Z : 0.0;
+    free(keep);
+    free(lg);
+    free(tok);
+}
+
+/* ------------------------------------------------------------------ */
 /* Exact integer q.k dots  [CPUATT Method "Logit dots are exact int32"].*/
 /*   dot_t = sum_d q_code[d] * k_code_t[d]   (|dot| <= D*127*127)       */
 /* ------------------------------------------------------------------ */
@@ -592,6 +721,14 @@ int orc_decode(const orc_cache *c, int H, const float *q, double scale, int k_se
             if (c->dtype == ORC_F16) {
                 orc_attend_f16(D, L, c->blk, qh, scale, (const uint16_t *)c->K + r0 * D,
                                (const uint16_t *)c->V + r0 * D, sel, n_sel, o);
+            } else if (c->dtype == ORC_Q8_0) {
+                int8_t *qc = (int8_t *)malloc((size_t)D);
+                float qs;
+                orc_quantize_row(qh, D, qc, &qs);
+                orc_attend_q8_0(D, L, c->blk, qc, qs, scale, (const int8_t *)c->K + r0 * D,
+                                (const int8_t *)c->V + r0 * D, c->kd + r0 * (D / ORC_QGROUP),
+                                c->vd + r0 * (D / ORC_QGROUP), sel, n_sel, 0.0, o, NULL);
+                free(qc);
             } else {
                 int8_t *qc = (int8_t *)malloc((size_t)D);
                 float qs;

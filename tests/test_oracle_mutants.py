@@ -58,6 +58,15 @@ MUTANTS = {
     "sv_dropped_out_of_denominator": (
         "            Zd += w;\n            continue;\n        }\n        const uint16_t *vr",
         "            Zd += w;\n            Z -= w;\n            continue;\n        }\n        const uint16_t *vr"),
+    # q8_0
+    "half_round_down": ("double n = nearbyint(ldexp(a, 10 - e));", "double n = floor(ldexp(a, 10 - e));"),
+    "q8_codes_from_unrounded_scale": ("double dg = orc_half_to_double(d[g]);", "double dg = (double)s32;"),
+    "q8_amax_of_first_group": ("double a = fabs((double)xg[i]);", "double a = fabs((double)x[i]);"),
+    "q8_logit_group0_scale": ("acc += orc_half_to_double(kd[(size_t)tok[i] * ng + g]) * (double)dot;",
+                              "acc += orc_half_to_double(kd[(size_t)tok[i] * ng]) * (double)dot;"),
+    "q8_value_scale_wrong_group": (
+        "out[d] += w * orc_half_to_double(vd[(size_t)tok[i] * ng + d / ORC_QGROUP]) *",
+        "out[d] += w * orc_half_to_double(vd[(size_t)tok[i] * ng + (d / ORC_QGROUP + 1) % ng]) *"),
 }
 
 
@@ -75,7 +84,8 @@ def _run_mutant(name, old, new, tmp):
     env = dict(os.environ, ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_sparse_v.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_sparse_v.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_q8_0.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return name, r.returncode
 
