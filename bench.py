@@ -57,8 +57,17 @@ def peaks():
 
 
 def kv_bytes_per_token(dtype):
-    # K row + V row (+ one f32 scale each for int8)
-    return 2 * 128 + 2 * 4 if dtype == kvd.INT8 else 2 * 2 * 128
+    # K row + V row, plus one f32 scale each (int8) or four f16 group scales
+    # each (q8_0)
+    if dtype == kvd.INT8:
+        return 2 * 128 + 2 * 4
+    if dtype == kvd.Q8_0:
+        return 2 * 128 + 2 * 4 * 2
+    return 2 * 2 * 128
+
+
+def dtype_name(dtype):
+    return {kvd.F16: "f16", kvd.INT8: "int8", kvd.Q8_0: "q8_0"}[dtype]
 
 
 def attended_tokens(sel_idx, sel_cnt, L):
@@ -87,7 +96,7 @@ def step_bytes(w, tokens, n_sel_total, L1):
     P = w.B * w.Hkv
     scored = P * n_cand * 2 * 128 * 2
     keys = P * n_cand * 4 * 2
-    row_out = 2 * 128 + 2 * 4 if w.dtype == kvd.INT8 else 2 * 2 * 128
+    row_out = kv_bytes_per_token(w.dtype)
     append = P * (2 * 128 * 2 + row_out + 2 * 128 * 2)
     return decode_kernel_bytes(w, tokens, n_sel_total) + scored + keys + append
 
@@ -293,7 +302,7 @@ def run_reference(args, w):
 
 def config_of(w):
     return {"workload": w.name, "batch": w.B, "n_heads": w.H, "n_kv_heads": w.Hkv,
-            "head_dim": w.D, "context": w.L, "kv_dtype": "int8" if w.dtype == kvd.INT8 else "f16",
+            "head_dim": w.D, "context": w.L, "kv_dtype": dtype_name(w.dtype),
             "block": 64, "k_sel": w.k_sel, "sink_tokens": w.sink_tokens,
             "recent_tokens": w.recent_tokens, "keys": w.keys, "n_needles": w.n_needles,
             "step": "append 1 token + select + sparse attend (kvd_decode_step)",
@@ -350,7 +359,7 @@ def run_sweep(args):
         tokens = attended_tokens(sel_idx, sel_cnt, L1) if n_sel else 0
         print(json.dumps({
             "sweep": args.sweep, "workload": w.name, "context": w.L, "batch": w.B,
-            "kv_dtype": "int8" if w.dtype == kvd.INT8 else "f16", "k_sel": w.k_sel,
+            "kv_dtype": dtype_name(w.dtype), "k_sel": w.k_sel,
             "coverage": n_sel / (w.B * w.Hkv) / ((L1 + 63) // 64),
             "sparse_step_us": res[False], "dense_step_us": res[True],
             "dense_over_sparse": res[True] / res[False],
@@ -402,7 +411,7 @@ def run_sparse_v_sweep(args):
             base = us if base is None else base
             print(json.dumps({
                 "sweep": "sparse_v", "workload": w.name, "context": w.L,
-                "kv_dtype": "int8" if w.dtype == kvd.INT8 else "f16", "eps": eps,
+                "kv_dtype": dtype_name(w.dtype), "eps": eps,
                 "decode_us": us, "vs_eps0": us / base, "steps": steps,
                 "l2": "write + read flush between steps"}), flush=True)
         del cache, ws
@@ -572,7 +581,7 @@ def main():
         "metric": "us_per_decode_step", "value": us_step, "unit": "us/step",
         "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": us_step / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8" if w.dtype == kvd.INT8 else "f16", "data": "synthetic",
+        "dtype": dtype_name(w.dtype), "data": "synthetic",
         "config": config_of(w),
         "effective_kv_gbs": eff_step,
         "effective_kv_frac": eff_step / peak,

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define KVD_ABI_VERSION 1
+#define KVD_ABI_VERSION 2
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -57,7 +57,7 @@ typedef enum {
     KVD_ERR_WORKSPACE = 6     /* workspace NULL, misaligned or too small */
 } kvd_status;
 
-typedef enum { KVD_F16 = 0, KVD_INT8 = 1 } kvd_kv_dtype;
+typedef enum { KVD_F16 = 0, KVD_INT8 = 1, KVD_Q8_0 = 2 } kvd_kv_dtype;
 
 /*
  * The cache: a plain descriptor of caller-owned device memory.
@@ -65,8 +65,9 @@ typedef enum { KVD_F16 = 0, KVD_INT8 = 1 } kvd_kv_dtype;
  * Layout is head-major, so one block of `block` tokens of one (sequence,
  * KV head) is one contiguous run of memory:
  *   k, v        [batch, n_kv_heads, max_seq, head_dim]   f16 or int8 codes
- *   k_scale,    [batch, n_kv_heads, max_seq]              f32, int8 only
- *   v_scale                                               (NULL for f16)
+ *   k_scale,    int8: [batch, n_kv_heads, max_seq] f32;
+ *   v_scale     q8_0: [batch, n_kv_heads, max_seq, head_dim / 32] f16
+ *               (NULL for f16)
  *   kbounds     [batch, n_kv_heads, max_seq / block, head_dim, 2]  f16
  * kbounds holds the per-(KV head, block) channel-wise key envelope [QUEST
  * Method: "Store kmin[head_dim], kmax[head_dim] per block"] as interleaved
@@ -76,6 +77,11 @@ typedef enum { KVD_F16 = 0, KVD_INT8 = 1 } kvd_kv_dtype;
  * int8 rows hold per-token per-head absmax codes [CPUATT Method]: scale =
  * absmax/127 (f32), code = round-half-even(x / scale) clamped to +-127, and
  * a row whose scale is 0 holds zero codes.
+ * q8_0 rows hold the same codes per group of 32 channels (the llama.cpp
+ * cache type of [QUEST] "All-KV-types composition"), each group with its
+ * own f16 scale d = fl16(fl32(absmax_group / 127)); code = round-half-even
+ * of the f32 quotient x / d, clamped to +-127 (zero codes when d is 0).
+ * The bounds come from the f16 keys on every cache type.
  *
  * `len` (tokens cached; the same for every sequence) is host state, advanced
  * by kvd_kv_append.  Rows at or beyond `len` are never read by a decode
@@ -94,8 +100,8 @@ typedef struct kvd_cache {
     int32_t reserved;     /* must be 0 */
     void *k;
     void *v;
-    float *k_scale;
-    float *v_scale;
+    void *k_scale;        /* f32 (int8) or f16 (q8_0) scales, see above */
+    void *v_scale;
     void *kbounds;
     int32_t *dev_status;
 } kvd_cache;
@@ -152,6 +158,9 @@ KVD_API kvd_status kvd_select_blocks(const kvd_cache *cache, const float *q, int
 /*     int8: q is quantized once per head like a cache row; logit_t =      */
 /*           dot_int32(q_code, k_code_t) * q_scale * k_scale_t * softmax_scale */
 /*           and v_t = v_scale_t * v_code_t                                 */
+/*     q8_0: q as for int8; logit_t = q_scale * softmax_scale *             */
+/*           sum_g d_g(k_t) * dot_int32 over group g (32 channels), and     */
+/*           v_t[c] = d_g(v_t) * v_code_t[c] with g = c / 32                */
 /*     out_h = sum_t softmax(logit)_t * v_t       (f32 accumulation)       */
 /*   An empty selection gives a zero output row.                           */
 /*   out: device [batch, n_heads, head_dim] f32.                            */

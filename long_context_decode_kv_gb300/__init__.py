@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(PKG, "libkvdecode.so")
 
 F16 = 0
 INT8 = 1
+Q8_0 = 2
 BLOCK = 64
 HEAD_DIM = 128
 
@@ -112,8 +113,9 @@ def _stream(t: torch.Tensor, stream=None):
 class KVCache:
     """Caller-owned cache tensors plus the C descriptor that points at them.
 
-    k, v      [B, Hkv, max_seq, 128]  float16 or int8
-    k_scale   [B, Hkv, max_seq]       float32 (int8 only)
+    k, v      [B, Hkv, max_seq, 128]  float16 or int8 codes
+    k_scale   [B, Hkv, max_seq]       float32 (int8), or
+              [B, Hkv, max_seq, 4]    float16 group scales (q8_0); same for v_scale
     kbounds   [B, Hkv, max_seq // 64, 128, 2] float16: (kmin, kmax) per channel
     status    [1] int32 device word for device-side faults
     """
@@ -141,6 +143,12 @@ class KVCache:
                                                 device=dev)
                 self.t["v_scale"] = torch.empty(batch, n_kv_heads, max_seq, dtype=torch.float32,
                                                 device=dev)
+            elif dtype == Q8_0:
+                ng = head_dim // 32
+                self.t["k_scale"] = torch.empty(batch, n_kv_heads, max_seq, ng,
+                                                dtype=torch.float16, device=dev)
+                self.t["v_scale"] = torch.empty(batch, n_kv_heads, max_seq, ng,
+                                                dtype=torch.float16, device=dev)
         self.s = CacheStruct(dtype, batch, n_kv_heads, head_dim, max_seq, block, 0, 0,
                              _ptr(self.t["k"]), _ptr(self.t["v"]),
                              _ptr(self.t.get("k_scale")), _ptr(self.t.get("v_scale")),
@@ -281,7 +289,7 @@ def debug_scores(cache: KVCache, q: torch.Tensor, ub: torch.Tensor, stream=None)
         cache.ref(), _ptr(q), int(q.shape[1]), _ptr(ub), _stream(q, stream)))
 
 
-__all__ = ["F16", "INT8", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
+__all__ = ["F16", "INT8", "Q8_0", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
            "workspace_bytes", "make_workspace", "selected_count", "status_string", "kv_append",
            "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
            "decode_attn_sv", "decode_step",

@@ -7,7 +7,8 @@
 // f16 keys; merge (min/max) into a block that already held tokens, overwrite
 // a block that starts in the new range.  Bounds always come from the f16 keys
 // before quantization.  "cpu-attn", Method: K and V are quantized per token
-// per head (absmax int8) at append time.
+// per head (absmax int8) at append time; the q8_0 type quantizes each group
+// of 32 channels with its own f16 scale instead.
 //
 // Lane l owns channels 4l..4l+3, so every row is read as one coalesced
 // 256-byte line.
@@ -56,6 +57,17 @@ __device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __ha
                 *reinterpret_cast<const uint2 *>(k_new + src);
             *reinterpret_cast<uint2 *>(static_cast<__half *>(c.v) + dst) =
                 *reinterpret_cast<const uint2 *>(v_new + src);
+        } else if (DT == KVD_Q8_0) {
+            __half kd, vd;
+            const uint32_t kc = quantize_group32_warp(kx, &kd);
+            const uint32_t vc = quantize_group32_warp(vx, &vd);
+            *reinterpret_cast<uint32_t *>(static_cast<int8_t *>(c.k) + dst) = kc;
+            *reinterpret_cast<uint32_t *>(static_cast<int8_t *>(c.v) + dst) = vc;
+            if ((lane & 7) == 0) {  // one lane per 32-channel group
+                const size_t si = (row0 + t) * (kHeadDim / 32) + (lane >> 3);
+                static_cast<__half *>(c.k_scale)[si] = kd;
+                static_cast<__half *>(c.v_scale)[si] = vd;
+            }
         } else {
             float ks, vs;
             const uint32_t kc = quantize_row_warp(kx, &ks);
@@ -63,8 +75,8 @@ __device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __ha
             *reinterpret_cast<uint32_t *>(static_cast<int8_t *>(c.k) + dst) = kc;
             *reinterpret_cast<uint32_t *>(static_cast<int8_t *>(c.v) + dst) = vc;
             if (lane == 0) {
-                c.k_scale[row0 + t] = ks;
-                c.v_scale[row0 + t] = vs;
+                static_cast<float *>(c.k_scale)[row0 + t] = ks;
+                static_cast<float *>(c.v_scale)[row0 + t] = vs;
             }
         }
     }

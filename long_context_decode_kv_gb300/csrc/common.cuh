@@ -151,6 +151,32 @@ __device__ __forceinline__ void s8x4_to_f32(uint32_t w, float (&f)[4]) {
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
 }
 
+// q8_0 quantization of one 128-wide row held 4 values per lane by a full
+// warp: the 8 lanes 8g..8g+7 hold group g (channels 32g..32g+31).  The
+// group's scale is d = fl16(absmax/127) (the IEEE f32 quotient rounded to
+// f16), code = round-half-even(x/d) in f32, clamped to +-127, and a zero
+// scale gives zero codes.  Returns the packed codes of the lane's 4 values
+// and writes the group's scale to *d (all lanes of the group).
+__device__ __forceinline__ uint32_t quantize_group32_warp(const float (&x)[4], __half *d) {
+    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const __half dh = __float2half_rn(__fdiv_rn(a, 127.0f));
+    *d = dh;
+    const float s = __half2float(dh);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int c = 0;
+        if (s != 0.0f) {
+            const float r = rintf(__fdiv_rn(x[j], s));
+            c = static_cast<int>(fminf(fmaxf(r, -127.0f), 127.0f));
+        }
+        packed |= (static_cast<uint32_t>(c) & 0xffu) << (8 * j);
+    }
+    return packed;
+}
+
 // Absmax int8 quantization of one 128-wide row held 4 values per lane by a
 // full warp (lane l holds x[4l..4l+3]).  scale = absmax/127 (IEEE f32
 // division), code = round-half-even(x/scale) clamped to +-127, and a zero

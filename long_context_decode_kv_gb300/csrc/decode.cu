@@ -78,7 +78,9 @@ DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count) {
     p.heads_per_cta = g.G < 4 ? g.G : 4;
     p.subgroups = g.G / p.heads_per_cta;
     const long P = static_cast<long>(g.B) * g.Hkv * p.subgroups;
-    const int per_sm = g.dtype == KVD_INT8 ? Tile<KVD_INT8>::kMinCtas : Tile<KVD_F16>::kMinCtas;
+    const int per_sm = g.dtype == KVD_F16    ? Tile<KVD_F16>::kMinCtas
+                       : g.dtype == KVD_Q8_0 ? Tile<KVD_Q8_0>::kMinCtas
+                                             : Tile<KVD_INT8>::kMinCtas;
     const long target = static_cast<long>(sm_count) * per_sm;  // one wave of resident CTAs
     long s = P >= target ? 1 : target / P;
     const long by_work = (static_cast<long>(max_blocks) + 3) / 4;  // >= 4 blocks per split
@@ -108,6 +110,9 @@ cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p
     if (g.dtype == KVD_INT8)
         return dense ? launch_decode_gc<KVD_INT8, true>(p.heads_per_cta, a, P_sub, st, pdl)
                      : launch_decode_gc<KVD_INT8, false>(p.heads_per_cta, a, P_sub, st, pdl);
+    if (g.dtype == KVD_Q8_0)
+        return dense ? launch_decode_gc<KVD_Q8_0, true>(p.heads_per_cta, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_Q8_0, false>(p.heads_per_cta, a, P_sub, st, pdl);
     return dense ? launch_decode_gc<KVD_F16, true>(p.heads_per_cta, a, P_sub, st, pdl)
                  : launch_decode_gc<KVD_F16, false>(p.heads_per_cta, a, P_sub, st, pdl);
 }

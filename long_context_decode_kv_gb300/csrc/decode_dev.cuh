@@ -55,6 +55,18 @@ struct Tile<KVD_INT8> {
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
 };
 template <>
+struct Tile<KVD_Q8_0> {
+    static constexpr int kRowBytes = kHeadDim;                        // int8 codes
+    static constexpr int kKBytes = kBlock * kRowBytes;                // 8192
+    static constexpr int kScaleBytes = kBlock * (kHeadDim / 32) * 2;  // f16 group scales: 512
+    static constexpr int kStageBytes = 2 * kKBytes + 2 * kScaleBytes;
+    static constexpr int kGroups = 2;
+    static constexpr int kStages = 6;   // a multiple of kGroups
+    static constexpr int kMinCtas = 2;
+    static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+};
+template <>
 struct Tile<KVD_F16> {
     static constexpr int kRowBytes = 2 * kHeadDim;                    // f16
     static constexpr int kKBytes = kBlock * kRowBytes;                // 16384
@@ -68,7 +80,7 @@ struct Tile<KVD_F16> {
 
 struct DecodeArgs {
     const void *k, *v;
-    const float *k_scale, *v_scale;
+    const void *k_scale, *v_scale;  // f32 per token (int8) or f16 per group (q8_0)
     const float *q;
     float *out;
     const int32_t *sel_idx, *sel_cnt;
@@ -109,28 +121,28 @@ struct SmemLayout {
 };
 
 // ----------------------------------------------------------------------------
-// int32 reductions over the 4 quarter lanes (lane bits 0..1) returning to each
-// lane the total of head (c * GC) / 4.
-template <int GC>
-__device__ __forceinline__ int reduce4_scatter(int (&v)[GC], int c) {
+// Reductions (int32 or f32) over the 4 quarter lanes (lane bits 0..1)
+// returning to each lane the total of head (c * GC) / 4.
+template <int GC, typename T>
+__device__ __forceinline__ T reduce4_scatter(T (&v)[GC], int c) {
     if constexpr (GC == 4) {
         const bool up = (c & 2) != 0;
-        int k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
-        const int s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
+        T k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+        const T s0 = up ? v[0] : v[2], s1 = up ? v[1] : v[3];
         k0 += __shfl_xor_sync(kFull, s0, 2);
         k1 += __shfl_xor_sync(kFull, s1, 2);
         const bool lo = (c & 1) != 0;
-        int k = lo ? k1 : k0;
+        T k = lo ? k1 : k0;
         k += __shfl_xor_sync(kFull, lo ? k0 : k1, 1);
         return k;
     } else if constexpr (GC == 2) {
         const bool up = (c & 2) != 0;
-        int k = up ? v[1] : v[0];
+        T k = up ? v[1] : v[0];
         k += __shfl_xor_sync(kFull, up ? v[0] : v[1], 2);
         k += __shfl_xor_sync(kFull, k, 1);
         return k;
     } else {
-        int k = v[0];
+        T k = v[0];
         k += __shfl_xor_sync(kFull, k, 2);
         k += __shfl_xor_sync(kFull, k, 1);
         return k;
@@ -182,7 +194,7 @@ __device__ __forceinline__ void load_query(const DecodeArgs &a, int b, int h0, i
     const float4 x4 = *reinterpret_cast<const float4 *>(
         a.q + (static_cast<size_t>(b) * a.H + hq) * kHeadDim + 4 * lane);
     const float x[4] = {x4.x, x4.y, x4.z, x4.w};
-    if constexpr (DT == KVD_INT8) {
+    if constexpr (DT != KVD_F16) {
         float s;
         const uint32_t packed = quantize_row_warp(x, &s);
         q_s[warp * 32 + lane] = packed;
@@ -235,6 +247,27 @@ __device__ __forceinline__ int qk_int8_row(const int8_t *row, const QRegsI8<GC> 
         for (int j = 0; j < 8; ++j)
             s = __dp4a(static_cast<int>(kw[j]), static_cast<int>(r.w[h][j]), s);
         d[h] = s;
+    }
+    return reduce4_scatter<GC>(d, c);
+}
+
+// q8_0: the lane's quarter c of the channels is exactly the cache's group c,
+// so its exact int32 dot takes the group's key scale before the quarters
+// are summed (in f32) into the logit of head (c*GC)/4.
+template <int GC>
+__device__ __forceinline__ float qk_q8_row(const int8_t *row, const QRegsI8<GC> &r, int t, int c,
+                                           float kscale) {
+    const uint4 ka = *reinterpret_cast<const uint4 *>(row + 16 * (2 * c + (t & 1)));
+    const uint4 kb = *reinterpret_cast<const uint4 *>(row + 16 * (2 * c + 1 - (t & 1)));
+    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+    float d[GC];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        int s = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            s = __dp4a(static_cast<int>(kw[j]), static_cast<int>(r.w[h][j]), s);
+        d[h] = static_cast<float>(s) * kscale;  // |s| <= 32*127*127: exact in f32
     }
     return reduce4_scatter<GC>(d, c);
 }
@@ -456,6 +489,83 @@ __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, 
     }
 }
 
+// One stage for one consumer warp, q8_0 cache: as consume_int8, with the
+// key scales per (token, group) inside the logit and the value scale of the
+// lane's group (lanes 8g..8g+7 hold channels of group g) applied to the
+// converted values.
+template <int GC>
+__device__ __forceinline__ void consume_q8(const uint8_t *stage, int n_valid, const float *coef,
+                                           const QRegsI8<GC> &qr, float *pw, int wg, int lane,
+                                           WarpState<GC> &st, float sv_eps) {
+    using TQ = Tile<KVD_Q8_0>;
+    const int8_t *Ks = reinterpret_cast<const int8_t *>(stage);
+    const int8_t *Vs = Ks + TQ::kKBytes;
+    const __half *kd = reinterpret_cast<const __half *>(stage + 2 * TQ::kKBytes);  // [64][4]
+    const __half *vd = kd + kBlock * (kHeadDim / 32);
+    const int t = lane >> 2, c = lane & 3;
+    const int tok0 = kTokensPerWarp * wg + t, tok1 = tok0 + 8;
+    const int hq = (c * GC) >> 2;
+    const float ninf = -__int_as_float(0x7f800000);
+    const float dot0 = qk_q8_row<GC>(Ks + tok0 * kHeadDim, qr, t, c,
+                                     __half2float(kd[tok0 * (kHeadDim / 32) + c]));
+    const float dot1 = qk_q8_row<GC>(Ks + tok1 * kHeadDim, qr, t, c,
+                                     __half2float(kd[tok1 * (kHeadDim / 32) + c]));
+    const float cf = coef[hq];
+    const float x0 = tok0 < n_valid ? dot0 * cf : ninf;
+    const float x1 = tok1 < n_valid ? dot1 * cf : ninf;
+    float bm = fmaxf(x0, x1);
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+    const float m_new = fmaxf(st.m, bm);
+    const float alpha = exp2f(st.m - m_new);
+    const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
+    st.l = st.l * alpha + (p0 + p1);
+    st.m = m_new;
+    bool keep[2] = {true, true};
+    uint32_t live = 0xffffu;
+    if (sv_eps > 0.0f) {
+        const float xs[2] = {x0, x1};
+        sparse_v_keep<2, 4>(xs, bm, min(max(n_valid - kTokensPerWarp * wg, 0), kTokensPerWarp),
+                            sv_eps, keep);
+        const uint32_t b0 = __ballot_sync(kFull, keep[0] && tok0 < n_valid);
+        const uint32_t b1 = __ballot_sync(kFull, keep[1] && tok1 < n_valid);
+        live = any_per_group<8, 4>(b0) | (any_per_group<8, 4>(b1) << 8);
+    }
+    constexpr int lph = 4 / GC;
+    if ((c % lph) == 0) {
+        const float w0 = tok0 < n_valid && keep[0] ? p0 : 0.0f;
+        const float w1 = tok1 < n_valid && keep[1] ? p1 : 0.0f;
+        *reinterpret_cast<float2 *>(pw + (t * 4 + hq) * 2) = make_float2(w0, w0);
+        *reinterpret_cast<float2 *>(pw + ((t + 8) * 4 + hq) * 2) = make_float2(w1, w1);
+    }
+    rescale<GC>(st, alpha, lph);
+    __syncwarp();
+    const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
+    const int8_t *vrow = Vs + kTokensPerWarp * wg * kHeadDim + 4 * lane;
+    const __half *vdl = vd + kTokensPerWarp * wg * (kHeadDim / 32) + (lane >> 3);
+    if (live != 0xffffu || nt != kTokensPerWarp) {
+        uint32_t m = live & ((nt >= 32 ? 0u : (1u << max(nt, 0))) - 1u);
+        for (; m; m &= m - 1u) {
+            const int t2 = __ffs(m) - 1;
+            float2 f01, f23;
+            s8x4_to_f32x2(*reinterpret_cast<const uint32_t *>(vrow + t2 * kHeadDim), f01, f23);
+            const float dv = __half2float(vdl[t2 * (kHeadDim / 32)]);
+            const float2 d2 = make_float2(dv, dv);
+            pv_token<GC>(st, pw + t2 * 8, __fmul2_rn(f01, d2), __fmul2_rn(f23, d2));
+        }
+    } else {
+#pragma unroll
+        for (int t2 = 0; t2 < kTokensPerWarp; ++t2) {
+            float2 f01, f23;
+            s8x4_to_f32x2(*reinterpret_cast<const uint32_t *>(vrow + t2 * kHeadDim), f01, f23);
+            const float dv = __half2float(vdl[t2 * (kHeadDim / 32)]);
+            const float2 d2 = make_float2(dv, dv);
+            pv_token<GC>(st, pw + t2 * 8, __fmul2_rn(f01, d2), __fmul2_rn(f23, d2));
+        }
+    }
+}
+
 // One stage for one consumer warp (wg = its index in the group), f16 cache:
 // four QK passes of 4 tokens.
 template <int GC>
@@ -620,10 +730,22 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                                         static_cast<const uint8_t *>(a.v) + r * TL::kRowBytes,
                                         TL::kKBytes, &full[s], pol);
                             if constexpr (DT == KVD_INT8) {
-                                tma_load_1d(dst + 2 * TL::kKBytes, a.k_scale + r, kBlock * 4,
-                                            &full[s], pol);
-                                tma_load_1d(dst + 2 * TL::kKBytes + kBlock * 4, a.v_scale + r,
+                                tma_load_1d(dst + 2 * TL::kKBytes,
+                                            static_cast<const float *>(a.k_scale) + r,
                                             kBlock * 4, &full[s], pol);
+                                tma_load_1d(dst + 2 * TL::kKBytes + kBlock * 4,
+                                            static_cast<const float *>(a.v_scale) + r,
+                                            kBlock * 4, &full[s], pol);
+                            } else if constexpr (DT == KVD_Q8_0) {
+                                constexpr int kSB = Tile<KVD_Q8_0>::kScaleBytes;
+                                tma_load_1d(dst + 2 * TL::kKBytes,
+                                            static_cast<const __half *>(a.k_scale) +
+                                                r * (kHeadDim / 32),
+                                            kSB, &full[s], pol);
+                                tma_load_1d(dst + 2 * TL::kKBytes + kSB,
+                                            static_cast<const __half *>(a.v_scale) +
+                                                r * (kHeadDim / 32),
+                                            kSB, &full[s], pol);
                             }
                         } else {
                             // an id outside the cache: report it, skip the block
@@ -666,7 +788,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         asm volatile("bar.sync 1, %0;" ::"r"(TL::kConsumerWarps * 32) : "memory");
         float *pw = pw_all + warp * (kTokensPerWarp * 4 * 2);
         const int group = warp / kWarpsPerGroup, wg = warp % kWarpsPerGroup;
-        if constexpr (DT == KVD_INT8) {
+        if constexpr (DT != KVD_F16) {
             QRegsI8<GC> qr;
             load_qregs_i8<GC>(q_s, lane >> 2, lane & 3, qr);
             for (int i = group;; i += TL::kGroups) {
@@ -683,8 +805,12 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 if (blk == kEndMark) break;
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
-                    consume_int8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, coef,
-                                     qr, pw, wg, lane, st, a.sv_eps);
+                    if constexpr (DT == KVD_INT8)
+                        consume_int8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
+                                         coef, qr, pw, wg, lane, st, a.sv_eps);
+                    else
+                        consume_q8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
+                                       coef, qr, pw, wg, lane, st, a.sv_eps);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -714,7 +840,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
             }
         }
         // per-warp totals: l summed over the lanes of each head
-        if constexpr (DT == KVD_INT8) {
+        if constexpr (DT != KVD_F16) {
             st.l += __shfl_xor_sync(kFull, st.l, 4);
             st.l += __shfl_xor_sync(kFull, st.l, 8);
             st.l += __shfl_xor_sync(kFull, st.l, 16);
@@ -727,7 +853,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     const bool aborted = *abort_flag != 0;
     if (!aborted && warp < TL::kConsumerWarps) {
         float *mg = reinterpret_cast<float *>(smem + SL::kStagesOff);
-        constexpr int lph = (DT == KVD_INT8 ? 4 : 8) / GC;
+        constexpr int lph = (DT != KVD_F16 ? 4 : 8) / GC;
 #pragma unroll
         for (int h = 0; h < GC; ++h) {
             float *row = mg + (warp * GC + h) * kPartStride;

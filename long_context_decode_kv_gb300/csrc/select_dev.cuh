@@ -665,7 +665,10 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
         // the decode step's token for (b, g): after the dependency wait, as the
         // previous step's kernels may still read the row it replaces
         const int len0 = a.app_cache.len;
-        if (a.app_cache.dtype == KVD_F16)
+        if (a.app_cache.dtype == KVD_Q8_0)
+            append_block_warp<KVD_Q8_0>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b,
+                                        g, lane);
+        else if (a.app_cache.dtype == KVD_F16)
             append_block_warp<KVD_F16>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b,
                                        g, lane);
         else

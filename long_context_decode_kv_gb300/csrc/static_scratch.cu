@@ -50,7 +50,8 @@ bool aligned_to(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p)
 kvd_status check_args(const kvd_cache *c, const float *q, int n_heads, const int32_t *sel_idx,
                       const int32_t *sel_cnt, int max_sel, const float *out) {
     if (!c) return KVD_ERR_INVALID;
-    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8) return KVD_ERR_INVALID;
+    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8 && c->dtype != KVD_Q8_0)
+        return KVD_ERR_INVALID;
     if (c->batch < 1 || c->n_kv_heads < 1) return KVD_ERR_INVALID;
     if (c->head_dim != kHeadDim || c->block != kBlock) return KVD_ERR_UNSUPPORTED;
     if (c->max_seq < kBlock || c->max_seq % kBlock != 0) return KVD_ERR_INVALID;
@@ -58,7 +59,7 @@ kvd_status check_args(const kvd_cache *c, const float *q, int n_heads, const int
     const void *ptrs[3] = {c->k, c->v, c->kbounds};
     for (const void *p : ptrs)
         if (!p || !aligned_to(p, 16)) return KVD_ERR_INVALID;
-    if (c->dtype == KVD_INT8 && (!c->k_scale || !c->v_scale || !aligned_to(c->k_scale, 16) ||
+    if (c->dtype != KVD_F16 && (!c->k_scale || !c->v_scale || !aligned_to(c->k_scale, 16) ||
                                  !aligned_to(c->v_scale, 16)))
         return KVD_ERR_INVALID;
     if (c->dev_status && !aligned_to(c->dev_status, 4)) return KVD_ERR_INVALID;

@@ -1,4 +1,4 @@
-"""GPU append (f16 copy / int8 absmax quantization + block envelope) vs the oracle.
+"""GPU append (f16 copy / int8 or q8_0 absmax quantization + block envelope) vs the oracle.
 
 Bar: cache rows, codes and scales bit-exact; bounds equal as numbers.
 """
@@ -23,6 +23,13 @@ def _compare(gc, oc):
                            torch.from_numpy(oc.K[:, :, :L].view(np.int16)))
         assert torch.equal(gc.v[:, :, :L].cpu().view(torch.int16),
                            torch.from_numpy(oc.V[:, :, :L].view(np.int16)))
+    elif gc.dtype == kvd.Q8_0:
+        assert np.array_equal(gc.k[:, :, :L].cpu().numpy(), oc.K[:, :, :L])
+        assert np.array_equal(gc.v[:, :, :L].cpu().numpy(), oc.V[:, :, :L])
+        assert np.array_equal(gc.k_scale[:, :, :L].cpu().numpy().view(np.uint16),
+                              oc.kd[:, :, :L].view(np.uint16))
+        assert np.array_equal(gc.v_scale[:, :, :L].cpu().numpy().view(np.uint16),
+                              oc.vd[:, :, :L].view(np.uint16))
     else:
         assert np.array_equal(gc.k[:, :, :L].cpu().numpy(), oc.K[:, :, :L])
         assert np.array_equal(gc.v[:, :, :L].cpu().numpy(), oc.V[:, :, :L])
@@ -36,7 +43,7 @@ def _compare(gc, oc):
                           oc.kmax[:, :, :nb].astype(np.float32))
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
 @pytest.mark.parametrize("L,chunks", [
     (1, None), (63, None), (64, None), (65, None), (300, None),
     (300, [1] * 70 + [230]), (1000, [63, 2, 64, 1, 870]), (4160, [4096, 1, 63]),
@@ -49,8 +56,9 @@ def test_append_matches_oracle(dtype, L, chunks):
     _compare(gc, oc)
 
 
+@pytest.mark.parametrize("dtype", [kvd.INT8, kvd.Q8_0])
 @pytest.mark.parametrize("dist", ["outliers", "tiny", "ties", "zeros"])
-def test_int8_quantization_edge_values(dist):
+def test_int8_quantization_edge_values(dist, dtype):
     B, L, Hkv = 1, 256, 2
     k = seeded((B, L, Hkv, 128), 7).float()
     v = seeded((B, L, Hkv, 128), 8).float()
@@ -70,7 +78,7 @@ def test_int8_quantization_edge_values(dist):
     else:
         k[:, :10] = 0
         v[:, 5:20] = 0
-    gc, oc = make_pair(kvd.INT8, k.half(), v.half())
+    gc, oc = make_pair(dtype, k.half(), v.half())
     _compare(gc, oc)
 
 

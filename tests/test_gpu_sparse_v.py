@@ -35,6 +35,10 @@ def _logits(dtype, oc, qh, b, g, tok, scale):
         K = oc.K[b, g, tok].astype(np.float64)
         return scale * (K @ qh.astype(np.float64))
     qc, qs = oracle.quantize_row(qh)
+    if dtype == kvd.Q8_0:
+        K = oc.K[b, g, tok].astype(np.float64) * np.repeat(
+            oc.kd[b, g, tok].astype(np.float64), 32, axis=1)
+        return (K @ qc.astype(np.float64)) * float(qs) * scale
     dots = oracle.qk_int8(qc, oc.K[b, g, tok])
     return dots.astype(np.float64) * float(qs) * oc.ks[b, g, tok].astype(np.float64) * scale
 
@@ -58,12 +62,19 @@ def _reference(dtype, oc, q_np, b, g, G, L, sel, eps, scale):
     tok = _tokens(L, sel)
     if dtype == kvd.F16:
         vrows = oc.V[b, g, tok].astype(np.float64)
+    elif dtype == kvd.Q8_0:
+        vrows = oc.V[b, g, tok].astype(np.float64) * np.repeat(
+            oc.vd[b, g, tok].astype(np.float64), 32, axis=1)
     else:
         vrows = oc.V[b, g, tok].astype(np.float64) * oc.vs[b, g, tok, None].astype(np.float64)
     for h in range(G):
         qh = q_np[b, g * G + h]
         if dtype == kvd.F16:
             o, d = oracle.attend_f16_sv(qh, oc.K[b, g], oc.V[b, g], L, 64, scale, eps, sel=sel)
+        elif dtype == kvd.Q8_0:
+            qc, qs = oracle.quantize_row(qh)
+            o, d = oracle.attend_q8_0(qc, qs, oc.K[b, g], oc.V[b, g], oc.kd[b, g], oc.vd[b, g],
+                                      L, 64, scale, sel=sel, eps=eps)
         else:
             qc, qs = oracle.quantize_row(qh)
             o, d = oracle.attend_int8_sv(qc, qs, oc.K[b, g], oc.V[b, g], oc.ks[b, g],
@@ -90,7 +101,7 @@ def _case(dtype, B, Hkv, G, L, seed):
     return gc, oc, q
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
 @pytest.mark.parametrize("eps", [0.05, 0.5, 2.0])
 @pytest.mark.parametrize("sparse", [True, False])
 def test_sparse_v_matches_oracle(dtype, eps, sparse):
@@ -124,7 +135,7 @@ def test_sparse_v_matches_oracle(dtype, eps, sparse):
         assert min(dropped) > 0.0  # the rule did drop something in every head
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
 def test_eps_zero_is_bit_identical(dtype):
     B, Hkv, G, L = 1, 8, 4, 9000
     gc, oc, q = _case(dtype, B, Hkv, G, L, 350)
