@@ -599,7 +599,9 @@ def main():
         "coverage": n_sel_total / (w.B * w.Hkv) / ((L1 + 63) // 64),
         "needles_selected": needle_ok,
         "e2e": {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "host_buffers": "pinned; the kernels read q, k, v and write out in place "
+                                "over the host link (no staging copies)"},
         "gpu_launches": launches_per_step(w, L1) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": wall,

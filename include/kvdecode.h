@@ -261,10 +261,13 @@ KVD_API kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void 
 /* ---------------------------------------------------------------------- */
 /* kvd_decode_step with HOST inputs and output: q_host ([batch, n_heads,   */
 /* head_dim] f32), k_new_host/v_new_host ([batch, 1, n_kv_heads, head_dim] */
-/* f16) are copied into the workspace, the step runs, and the output is   */
-/* copied to out_host ([batch, n_heads, head_dim] f32), all enqueued on    */
-/* `stream`.  Host buffers should be page-locked for the copies to be      */
-/* asynchronous; out_host is valid once the stream has finished.          */
+/* f16) in, out_host ([batch, n_heads, head_dim] f32) out, all enqueued on */
+/* `stream`.  A buffer in page-locked host memory that CUDA maps into the  */
+/* device's address space (16-byte aligned) is read or written in place by */
+/* the kernels, over the host link; any other buffer is staged through    */
+/* the workspace with cudaMemcpyAsync (pageable memory makes those copies   */
+/* synchronous).  out_host is valid once the stream has finished, and the  */
+/* host must not change the inputs before then.                             */
 /* ---------------------------------------------------------------------- */
 KVD_API kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host,
                                 const void *k_new_host, const void *v_new_host,

@@ -365,6 +365,30 @@ kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
                        workspace, w, st, true);
 }
 
+}  // extern "C"
+
+namespace kvd {
+namespace {
+
+// The device-side address of host buffer p when the GPU can reach it
+// directly: pinned host memory mapped into the device's address space (on a
+// Grace host the kernels then read and write it over the chip-to-chip link).
+// nullptr for pageable or unknown memory, or an address not 16-byte aligned.
+void *device_view(const void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // not a CUDA-known pointer: clear the error
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+    return aligned(at.devicePointer, 16) ? at.devicePointer : nullptr;
+}
+
+}  // namespace
+}  // namespace kvd
+
+extern "C" {
+
 kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host, const void *k_new_host,
                                 const void *v_new_host, int32_t n_heads, float softmax_scale,
                                 int32_t k_sel, int32_t sink_tokens, int32_t recent_tokens,
@@ -379,19 +403,34 @@ kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host, const voi
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t qb = static_cast<size_t>(cache->batch) * n_heads * kHeadDim * sizeof(float);
     const size_t kb = static_cast<size_t>(cache->batch) * cache->n_kv_heads * kHeadDim * 2;
-    float *q_dev = ws_at<float>(workspace, w.q);
-    void *k_dev = ws_at<void>(workspace, w.k_new);
-    void *v_dev = ws_at<void>(workspace, w.v_new);
-    float *o_dev = ws_at<float>(workspace, w.out);
-    if (cudaMemcpyAsync(q_dev, q_host, qb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(k_dev, k_new_host, kb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(v_dev, v_new_host, kb, cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return KVD_ERR_CUDA;
+    // Buffers the GPU can reach directly are used in place by the kernels;
+    // the others are staged through the workspace by copies on the stream.
+    float *q_dev = static_cast<float *>(device_view(q_host));
+    void *k_dev = device_view(k_new_host);
+    void *v_dev = device_view(v_new_host);
+    float *o_map = static_cast<float *>(device_view(out_host));
+    if (!q_dev) {
+        q_dev = ws_at<float>(workspace, w.q);
+        if (cudaMemcpyAsync(q_dev, q_host, qb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return KVD_ERR_CUDA;
+    }
+    if (!k_dev) {
+        k_dev = ws_at<void>(workspace, w.k_new);
+        if (cudaMemcpyAsync(k_dev, k_new_host, kb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return KVD_ERR_CUDA;
+    }
+    if (!v_dev) {
+        v_dev = ws_at<void>(workspace, w.v_new);
+        if (cudaMemcpyAsync(v_dev, v_new_host, kb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return KVD_ERR_CUDA;
+    }
+    float *o_dev = o_map ? o_map : ws_at<float>(workspace, w.out);
     s = kvd_decode_step(cache, q_dev, k_dev, v_dev, n_heads, softmax_scale, k_sel, sink_tokens,
                         recent_tokens, sel_idx, sel_cnt, o_dev, workspace, workspace_bytes,
                         stream);
     if (s != KVD_OK) return s;
-    if (cudaMemcpyAsync(out_host, o_dev, qb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (!o_map &&
+        cudaMemcpyAsync(out_host, o_dev, qb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return KVD_ERR_CUDA;
     return KVD_OK;
 }

@@ -1,16 +1,10 @@
 // decode.cu -- decode launches: decode_kernel (split-KV decode over the
-// selected or all blocks; decode_dev.cuh), the int8 q.k test export, and the
-// split plan.
+// selected or all blocks; decode_dev.cuh) without sparse-V, the int8 q.k test
+// export, and the split plan.  decode_sv.cu holds the sparse-V kernels.
 #include "decode_dev.cuh"
 
 namespace kvd {
 namespace {
-
-template <int DT, int GC, bool DENSE>
-__global__ void __launch_bounds__(Tile<DT>::kThreads, Tile<DT>::kMinCtas) decode_kernel(DecodeArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    decode_body<DT, GC, DENSE>(a, blockIdx.x, blockIdx.y, smem);
-}
 
 // ----------------------------------------------------------------------------
 // Test export: exact int32 q.k dots of every cached token, computed with the
@@ -47,30 +41,6 @@ __global__ void __launch_bounds__(256) qk_debug_kernel(DecodeArgs a, int32_t *do
         dots[(static_cast<size_t>(b) * a.H + h0 + hq) * a.len + pos] = dot;
 }
 
-template <int DT, int GC, bool DENSE>
-cudaError_t launch_decode_t(const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
-    using SL = SmemLayout<DT, GC>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SL::kTotal);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    return launch_ex(decode_kernel<DT, GC, DENSE>, dim3(a.splits, P_sub), dim3(Tile<DT>::kThreads),
-                     SL::kTotal, st, pdl, a);
-}
-
-template <int DT, bool DENSE>
-cudaError_t launch_decode_gc(int gc, const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
-    switch (gc) {
-        case 1: return launch_decode_t<DT, 1, DENSE>(a, P_sub, st, pdl);
-        case 2: return launch_decode_t<DT, 2, DENSE>(a, P_sub, st, pdl);
-        default: return launch_decode_t<DT, 4, DENSE>(a, P_sub, st, pdl);
-    }
-}
-
 }  // namespace
 
 DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count) {
@@ -103,18 +73,11 @@ cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p
                           const int32_t *sel_cnt, float *out, float *partials,
                           uint32_t *counters, cudaStream_t st, bool pdl, bool early_q,
                           float sv_eps) {
-    const DecodeArgs a = make_decode_args(c, g, p, q, scale, sel_idx, sel_cnt, out, partials,
-                                          counters, early_q, sv_eps);
-    const int P_sub = g.B * g.Hkv * p.subgroups;
-    const bool dense = sel_idx == nullptr;
-    if (g.dtype == KVD_INT8)
-        return dense ? launch_decode_gc<KVD_INT8, true>(p.heads_per_cta, a, P_sub, st, pdl)
-                     : launch_decode_gc<KVD_INT8, false>(p.heads_per_cta, a, P_sub, st, pdl);
-    if (g.dtype == KVD_Q8_0)
-        return dense ? launch_decode_gc<KVD_Q8_0, true>(p.heads_per_cta, a, P_sub, st, pdl)
-                     : launch_decode_gc<KVD_Q8_0, false>(p.heads_per_cta, a, P_sub, st, pdl);
-    return dense ? launch_decode_gc<KVD_F16, true>(p.heads_per_cta, a, P_sub, st, pdl)
-                 : launch_decode_gc<KVD_F16, false>(p.heads_per_cta, a, P_sub, st, pdl);
+    if (sv_eps > 0.0f)
+        return launch_decode_sv(c, g, p, q, scale, sel_idx, sel_cnt, out, partials, counters,
+                                st, pdl, early_q, sv_eps);
+    return launch_decode_any<false>(c, g, p, q, scale, sel_idx, sel_cnt, out, partials,
+                                    counters, st, pdl, early_q, 0.0f);
 }
 
 cudaError_t launch_qk_debug(const kvd_cache &c, const Geom &g, const float *q, int32_t *dots,

@@ -418,7 +418,7 @@ __device__ __forceinline__ void s8x4_to_f32x2(uint32_t w, float2 &f01, float2 &f
 // One stage (64-token block) for one consumer warp (wg = its index in the
 // group), int8 cache: two QK passes of 8 tokens, one softmax update, 16
 // tokens of PV.
-template <int GC>
+template <int GC, bool SV>
 __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, const float *coef,
                                              const QRegsI8<GC> &qr, float *pw, int wg, int lane,
                                              WarpState<GC> &st, float sv_eps) {
@@ -446,7 +446,7 @@ __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, 
     st.m = m_new;
     bool keep[2] = {true, true};
     uint32_t live = 0xffffu;  // tokens whose V some head still needs
-    if (sv_eps > 0.0f) {
+    if constexpr (SV) {
         const float xs[2] = {x0, x1};
         sparse_v_keep<2, 4>(xs, bm, min(max(n_valid - kTokensPerWarp * wg, 0), kTokensPerWarp),
                             sv_eps, keep);
@@ -465,7 +465,7 @@ __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, 
     __syncwarp();
     const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
     const int8_t *vrow = Vs + kTokensPerWarp * wg * kHeadDim + 4 * lane;
-    if (live != 0xffffu) {
+    if (SV && live != 0xffffu) {
         // sparse-V dropped some tokens for every head: only the live ones
         for (uint32_t m = live; m; m &= m - 1u) {
             const int t2 = __ffs(m) - 1;
@@ -493,7 +493,7 @@ __device__ __forceinline__ void consume_int8(const uint8_t *stage, int n_valid, 
 // key scales per (token, group) inside the logit and the value scale of the
 // lane's group (lanes 8g..8g+7 hold channels of group g) applied to the
 // converted values.
-template <int GC>
+template <int GC, bool SV>
 __device__ __forceinline__ void consume_q8(const uint8_t *stage, int n_valid, const float *coef,
                                            const QRegsI8<GC> &qr, float *pw, int wg, int lane,
                                            WarpState<GC> &st, float sv_eps) {
@@ -524,7 +524,7 @@ __device__ __forceinline__ void consume_q8(const uint8_t *stage, int n_valid, co
     st.m = m_new;
     bool keep[2] = {true, true};
     uint32_t live = 0xffffu;
-    if (sv_eps > 0.0f) {
+    if constexpr (SV) {
         const float xs[2] = {x0, x1};
         sparse_v_keep<2, 4>(xs, bm, min(max(n_valid - kTokensPerWarp * wg, 0), kTokensPerWarp),
                             sv_eps, keep);
@@ -568,7 +568,7 @@ __device__ __forceinline__ void consume_q8(const uint8_t *stage, int n_valid, co
 
 // One stage for one consumer warp (wg = its index in the group), f16 cache:
 // four QK passes of 4 tokens.
-template <int GC>
+template <int GC, bool SV>
 __device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
                                             const QRegsF16<GC> &qr, float *pw, int wg,
                                             int lane, WarpState<GC> &st, float sv_eps) {
@@ -596,7 +596,7 @@ __device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
     st.m = m_new;
     bool keep[4] = {true, true, true, true};
     uint32_t live = 0xffffu;  // tokens whose V some head still needs
-    if (sv_eps > 0.0f) {
+    if constexpr (SV) {
         sparse_v_keep<4, 8>(x, bm, min(max(n_valid - kTokensPerWarp * wg, 0), kTokensPerWarp),
                             sv_eps, keep);
         live = 0u;
@@ -619,7 +619,7 @@ __device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
     __syncwarp();
     const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
     const __half *vrow = Vs + kTokensPerWarp * wg * kHeadDim + 4 * lane;
-    if (live != 0xffffu) {
+    if (SV && live != 0xffffu) {
         // sparse-V dropped some tokens for every head: only the live ones
         for (uint32_t m = live; m; m &= m - 1u) {
             const int t2 = __ffs(m) - 1;
@@ -639,7 +639,7 @@ __device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
     }
 }
 
-template <int DT, int GC, bool DENSE>
+template <int DT, int GC, bool DENSE, bool SV>
 __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *smem) {
     using SL = SmemLayout<DT, GC>;
     using TL = Tile<DT>;
@@ -806,11 +806,11 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
                     if constexpr (DT == KVD_INT8)
-                        consume_int8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
-                                         coef, qr, pw, wg, lane, st, a.sv_eps);
+                        consume_int8<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes,
+                                             n_valid, coef, qr, pw, wg, lane, st, a.sv_eps);
                     else
-                        consume_q8<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
-                                       coef, qr, pw, wg, lane, st, a.sv_eps);
+                        consume_q8<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
+                                           coef, qr, pw, wg, lane, st, a.sv_eps);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -832,8 +832,8 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 if (blk == kEndMark) break;
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
-                    consume_f16<GC>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid, qr, pw,
-                                    wg, lane, st, a.sv_eps);
+                    consume_f16<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
+                                        qr, pw, wg, lane, st, a.sv_eps);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -1033,6 +1033,64 @@ DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan 
     a.plan_blocks = p.blocks;
     a.scale_log2 = scale * kLog2e;
     return a;
+}
+
+
+// ----------------------------------------------------------------------------
+// The kernel and its launchers.  SV (sparse-V) kernels are instantiated by
+// their own translation unit, so the plain kernels carry none of that code:
+// after an L2 flush every instruction of a kernel comes from HBM again, and
+// a shorter instruction stream starts sooner.
+template <int DT, int GC, bool DENSE, bool SV>
+__global__ void __launch_bounds__(Tile<DT>::kThreads, Tile<DT>::kMinCtas)
+    decode_kernel(DecodeArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    decode_body<DT, GC, DENSE, SV>(a, blockIdx.x, blockIdx.y, smem);
+}
+
+template <int DT, int GC, bool DENSE, bool SV>
+cudaError_t launch_decode_t(const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
+    using SL = SmemLayout<DT, GC>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE, SV>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SL::kTotal);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch_ex(decode_kernel<DT, GC, DENSE, SV>, dim3(a.splits, P_sub),
+                     dim3(Tile<DT>::kThreads), SL::kTotal, st, pdl, a);
+}
+
+template <int DT, bool DENSE, bool SV>
+cudaError_t launch_decode_gc(int gc, const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
+    switch (gc) {
+        case 1: return launch_decode_t<DT, 1, DENSE, SV>(a, P_sub, st, pdl);
+        case 2: return launch_decode_t<DT, 2, DENSE, SV>(a, P_sub, st, pdl);
+        default: return launch_decode_t<DT, 4, DENSE, SV>(a, P_sub, st, pdl);
+    }
+}
+
+template <bool SV>
+cudaError_t launch_decode_any(const kvd_cache &c, const Geom &g, const DecodePlan &p,
+                              const float *q, float scale, const int32_t *sel_idx,
+                              const int32_t *sel_cnt, float *out, float *partials,
+                              uint32_t *counters, cudaStream_t st, bool pdl, bool early_q,
+                              float sv_eps) {
+    const DecodeArgs a = make_decode_args(c, g, p, q, scale, sel_idx, sel_cnt, out, partials,
+                                          counters, early_q, sv_eps);
+    const int P_sub = g.B * g.Hkv * p.subgroups;
+    const bool dense = sel_idx == nullptr;
+    const int gc = p.heads_per_cta;
+    if (g.dtype == KVD_INT8)
+        return dense ? launch_decode_gc<KVD_INT8, true, SV>(gc, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_INT8, false, SV>(gc, a, P_sub, st, pdl);
+    if (g.dtype == KVD_Q8_0)
+        return dense ? launch_decode_gc<KVD_Q8_0, true, SV>(gc, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_Q8_0, false, SV>(gc, a, P_sub, st, pdl);
+    return dense ? launch_decode_gc<KVD_F16, true, SV>(gc, a, P_sub, st, pdl)
+                 : launch_decode_gc<KVD_F16, false, SV>(gc, a, P_sub, st, pdl);
 }
 
 }  // namespace

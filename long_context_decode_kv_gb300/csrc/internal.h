@@ -74,6 +74,13 @@ cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p
                           uint32_t *counters, cudaStream_t st, bool pdl, bool early_q,
                           float sv_eps = 0.0f);
 
+// The sparse-V (sv_eps > 0) kernels behind launch_decode (decode_sv.cu).
+cudaError_t launch_decode_sv(const kvd_cache &c, const Geom &g, const DecodePlan &p,
+                             const float *q, float scale, const int32_t *sel_idx,
+                             const int32_t *sel_cnt, float *out, float *partials,
+                             uint32_t *counters, cudaStream_t st, bool pdl, bool early_q,
+                             float sv_eps);
+
 cudaError_t launch_qk_debug(const kvd_cache &c, const Geom &g, const float *q, int32_t *dots,
                             int8_t *q_codes, float *q_scales, cudaStream_t st);
 

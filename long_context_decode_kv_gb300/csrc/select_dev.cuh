@@ -511,6 +511,29 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n,
     select_write_list(a, p, n, gtw, eqw, need_eq, rs);
 }
 
+// Out of line: code the common path does not run stays off its instruction
+// stream (after an L2 flush each kernel's instructions come from HBM again).
+// The decode step's token, appended by one warp of the first tile.
+__device__ __noinline__ void fused_append(const SelArgs &a, int b, int g, int lane) {
+    const int len0 = a.app_cache.len;
+    if (a.app_cache.dtype == KVD_Q8_0)
+        append_block_warp<KVD_Q8_0>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
+                                    lane);
+    else if (a.app_cache.dtype == KVD_F16)
+        append_block_warp<KVD_F16>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
+                                   lane);
+    else
+        append_block_warp<KVD_INT8>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
+                                    lane);
+}
+
+// The tail of a problem too large for its keys to fit the ring.
+__device__ __noinline__ void select_finish_from_l2(const SelArgs &a, int p, int n,
+                                                   const uint32_t *keys, uint8_t *scratch,
+                                                   RadixShared &rs) {
+    select_finish<false>(a, p, n, keys, scratch, rs);
+}
+
 // CTA (x, p): candidate blocks j in [x*R, min(n, (x+1)*R)) of problem p,
 // i.e. cache blocks se + j.  Their bounds stream through a TMA ring (stages
 // of 64 blocks; warp 16 produces, warps 0..15 consume, warp w scoring blocks
@@ -664,16 +687,7 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
     if (a.app_k && x_tile == 0 && warp == 0) {
         // the decode step's token for (b, g): after the dependency wait, as the
         // previous step's kernels may still read the row it replaces
-        const int len0 = a.app_cache.len;
-        if (a.app_cache.dtype == KVD_Q8_0)
-            append_block_warp<KVD_Q8_0>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b,
-                                        g, lane);
-        else if (a.app_cache.dtype == KVD_F16)
-            append_block_warp<KVD_F16>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b,
-                                       g, lane);
-        else
-            append_block_warp<KVD_INT8>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b,
-                                        g, lane);
+        fused_append(a, b, g, lane);
     }
     if constexpr (MODE == kExport) return;
 
@@ -743,7 +757,7 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
     if (in_smem)
         select_finish<true>(a, p, n, reinterpret_cast<const uint32_t *>(ring), scratch, rs);
     else
-        select_finish<false>(a, p, n, kp, scratch, rs);
+        select_finish_from_l2(a, p, n, kp, scratch, rs);
 }
 
 template <int G>

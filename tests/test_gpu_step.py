@@ -62,8 +62,11 @@ def test_steps_match_oracle(dtype, sparse):
         assert_outputs(out, ref, dtype, f"step {s}")
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8])
-def test_host_step_equals_device_step(dtype):
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
+def test_host_step_equals_device_step(dtype, pinned):
+    # pinned (device-mapped) host buffers are used in place by the kernels,
+    # pageable ones are staged by copies; either way the step is the device one
     B, Hkv, G, L0 = 1, 8, 4, 5000
     k = seeded((B, L0, Hkv, 128), 181)
     v = seeded((B, L0, Hkv, 128), 182)
@@ -77,8 +80,11 @@ def test_host_step_equals_device_step(dtype):
         vn = seeded((B, 1, Hkv, 128), 199 + s)
         out_d = torch.empty(B, Hkv * G, 128, device=dev())
         kvd.decode_step(a, q, kn, vn, scale_for(), 20, 4, 128, out_d, wa)
-        qh, kh, vh = q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()
-        out_h = torch.empty(B, Hkv * G, 128).pin_memory()
+        pin = {"all": (1, 1, 1, 1), "none": (0, 0, 0, 0), "mixed": (1, 0, 1, 0)}[pinned]
+        qh, kh, vh = (t.cpu().pin_memory() if p else t.cpu().clone()
+                      for t, p in zip((q, kn, vn), pin[:3]))
+        out_h = torch.empty(B, Hkv * G, 128)
+        out_h = out_h.pin_memory() if pin[3] else out_h
         kvd.decode_step_host(b, qh, kh, vh, scale_for(), 20, 4, 128, out_h, wb)
         torch.cuda.synchronize()
         assert torch.equal(out_d.cpu(), out_h)
