@@ -684,12 +684,13 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
         return;
     }
     if (a.overlap) pdl_wait();  // the upstream kernels are complete past here
-    if (a.app_k && x_tile == 0 && warp == 0) {
-        // the decode step's token for (b, g): after the dependency wait, as the
-        // previous step's kernels may still read the row it replaces
-        fused_append(a, b, g, lane);
-    }
     if constexpr (MODE == kExport) return;
+    // The decode step's token for (b, g) is appended by warp 0 of the first
+    // tile, after the dependency wait (the previous step's kernels may still
+    // read the row it replaces) and off the way to the ranking: once the
+    // tile's ticket shows another CTA ranks, else after its own ranking.  The
+    // step's decode kernel waits for this whole grid, so it sees the token.
+    const bool appends = a.app_k && x_tile == 0 && warp == 0;
 
     // ================================================= phase 2: ticket
     const int X = n_tiles;
@@ -707,7 +708,10 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
             rs.last = atomic_add_acq_rel_gpu(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
         }
         __syncthreads();
-        if (!rs.last) return;
+        if (!rs.last) {
+            if (appends) fused_append(a, b, g, lane);
+            return;
+        }
     }
     // the last CTA of the problem: every key is in
     if (in_smem && warp == kScoreWarps) {
@@ -750,6 +754,7 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
             volatile int never = 0;
             if (in_smem) (void)mbar_wait(&rs.kbar, 0, &never);  // copies in flight
         }
+        if (appends) fused_append(a, b, g, lane);
         return;
     }
     // the rest reads the keys from shared memory, or from L2 for a problem too
@@ -758,6 +763,7 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
         select_finish<true>(a, p, n, reinterpret_cast<const uint32_t *>(ring), scratch, rs);
     else
         select_finish_from_l2(a, p, n, kp, scratch, rs);
+    if (appends) fused_append(a, b, g, lane);
 }
 
 template <int G>
