@@ -23,6 +23,7 @@ from . import build as _build
 F16 = 0
 INT8 = 1
 Q8_0 = 2
+Q4_0 = 3
 QGROUP = 32
 
 _lib = None
@@ -55,6 +56,8 @@ def lib():
         L.orc_double_to_half.restype = C.c_uint16
         L.orc_quantize_group32.argtypes = [p, i, p, p]
         L.orc_attend_q8_0.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
+        L.orc_quantize_q4_0.argtypes = [p, i, p, p]
+        L.orc_attend_q4_0.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
         L.orc_attend_f16_sv.argtypes = [i, i, i, p, d, p, p, p, i, d, p, p]
         L.orc_attend_int8_sv.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
         L.orc_decode.argtypes = [p, i, p, d, i, i, i, i, p, p, p, i]
@@ -106,12 +109,13 @@ class OracleCache:
         assert max_seq % blk == 0
         self.dtype, self.B, self.Hkv, self.D = dtype, B, Hkv, D
         self.max_seq, self.blk, self.len = max_seq, blk, 0
-        kvt = np.float16 if dtype == F16 else np.int8
-        self.K = np.zeros((B, Hkv, max_seq, D), kvt)
-        self.V = np.zeros((B, Hkv, max_seq, D), kvt)
+        kvt = np.float16 if dtype == F16 else (np.uint8 if dtype == Q4_0 else np.int8)
+        width = D // 2 if dtype == Q4_0 else D
+        self.K = np.zeros((B, Hkv, max_seq, width), kvt)
+        self.V = np.zeros((B, Hkv, max_seq, width), kvt)
         self.ks = np.zeros((B, Hkv, max_seq), np.float32) if dtype == INT8 else None
         self.vs = np.zeros((B, Hkv, max_seq), np.float32) if dtype == INT8 else None
-        q8 = dtype == Q8_0
+        q8 = dtype in (Q8_0, Q4_0)
         self.kd = np.zeros((B, Hkv, max_seq, D // QGROUP), np.float16) if q8 else None
         self.vd = np.zeros((B, Hkv, max_seq, D // QGROUP), np.float16) if q8 else None
         nb = max_seq // blk
@@ -262,6 +266,32 @@ def quantize_group32(x):
     return code, d.view(np.float16)
 
 
+def quantize_q4_0(x):
+    """q4_0 packed codes ([n // 2] uint8) of a row and its float16 group scales."""
+    x = _c(x, np.float32)
+    packed = np.zeros(x.size // 2, np.uint8)
+    d = np.zeros(x.size // QGROUP, np.uint16)
+    lib().orc_quantize_q4_0(_ptr(x), x.size, _ptr(packed), _ptr(d))
+    return packed, d.view(np.float16)
+
+
+def attend_q4_0(q_code, q_scale, K, V, kd, vd, L, blk, scale, sel=None, eps=0.0):
+    """q4_0 attention of one head (sparse-V at eps): (out [D], dropped mass share)."""
+    q_code = _c(q_code, np.int8)
+    K = _c(K, np.uint8)
+    V = _c(V, np.uint8)
+    kd = _c(kd, np.float16)
+    vd = _c(vd, np.float16)
+    D = q_code.size
+    s, n = _sel_args(sel)
+    out = np.zeros(D, np.float64)
+    dropped = C.c_double()
+    lib().orc_attend_q4_0(D, L, blk, _ptr(q_code), float(q_scale), float(scale), _ptr(K),
+                          _ptr(V), _ptr(kd), _ptr(vd), _ptr(s), n, float(eps), _ptr(out),
+                          C.byref(dropped))
+    return out, dropped.value
+
+
 def attend_q8_0(q_code, q_scale, K, V, kd, vd, L, blk, scale, sel=None, eps=0.0):
     """q8_0 attention of one head (sparse-V at eps): (out [D], dropped mass share)."""
     q_code = _c(q_code, np.int8)
@@ -326,5 +356,6 @@ def threads_available() -> int:
 __all__ = ["F16", "INT8", "OracleCache", "half_to_double", "quantize_row", "block_scores",
            "forced_range", "select", "attend_f16", "qk_int8", "attend_int8", "attend_dequant",
            "sparse_v_keep", "attend_f16_sv", "attend_int8_sv", "Q8_0", "QGROUP",
-           "double_to_half", "quantize_group32", "attend_q8_0",
+           "double_to_half", "quantize_group32", "attend_q8_0", "Q4_0", "quantize_q4_0",
+           "attend_q4_0",
            "threads_available", "lib"]

@@ -34,6 +34,9 @@
  *  R6  attention over an empty token set returns the zero vector.
  *  R7  sparse-V (eps mode): the mean weight a position is compared with is
  *      taken over its 16-token chunk of the attended positions.
+ *  R9  q4_0 (named, not defined, by the pages): per 32-channel group the
+ *      f16 scale fl16(fl32(m/-8)) of the largest-magnitude value m, codes
+ *      clamp(round-half-even(fl32(x/d)) + 8, 0, 15), two per byte.
  *  R8  q8_0 (named, not defined, by the pages): per 32-channel group an f16
  *      scale fl16(fl32(amax/127)) and codes round-half-even(fl32(x/d))
  *      clamped to +-127; the query is quantized per row as for int8, and the
@@ -54,6 +57,7 @@
 #define ORC_F16 0
 #define ORC_INT8 1
 #define ORC_Q8_0 2
+#define ORC_Q4_0 3
 #define ORC_QGROUP 32
 
 /* ------------------------------------------------------------------ */
@@ -163,10 +167,54 @@ void orc_quantize_group32(const float *x, int n, int8_t *code, uint16_t *d)
 }
 
 /* ------------------------------------------------------------------ */
+/* q4_0: 4-bit codes per group of 32 channels with a binary16 scale     */
+/* (the llama.cpp cache type named by [QUEST] "All-KV-types            */
+/* composition"; R9).  m is the group's value of largest magnitude (the */
+/* first one in channel order); d = fl16(fl32(m / -8)), so m maps to    */
+/* -8; code = clamp(round-half-even(fl32(x / d)) + 8, 0, 15) (all 8 if  */
+/* d = 0); the value is d * (code - 8).  Byte i of a group holds         */
+/* channels 2i (low nibble) and 2i+1 (high nibble).                      */
+/* packed: n / 2 bytes; d: n / 32 binary16 bits.                          */
+/* ------------------------------------------------------------------ */
+void orc_quantize_q4_0(const float *x, int n, uint8_t *packed, uint16_t *d)
+{
+    for (int g = 0; g < n / ORC_QGROUP; ++g) {
+        const float *xg = x + g * ORC_QGROUP;
+        double amax = 0.0, m = 0.0;
+        for (int i = 0; i < ORC_QGROUP; ++i) {
+            double mag = fabs((double)xg[i]);
+            if (mag > amax) {
+                amax = mag;
+                m = (double)xg[i];
+            }
+        }
+        float s32 = (float)(m / -8.0);
+        d[g] = orc_double_to_half((double)s32);
+        double dq = orc_half_to_double(d[g]);
+        int c4[ORC_QGROUP];
+        for (int i = 0; i < ORC_QGROUP; ++i) {
+            if (dq == 0.0) { c4[i] = 8; continue; }
+            float qt = (float)((double)xg[i] / dq);
+            double r4 = nearbyint((double)qt) + 8.0;   /* ties to even */
+            c4[i] = (int)(r4 < 0.0 ? 0.0 : (r4 > 15.0 ? 15.0 : r4));
+        }
+        for (int i = 0; i < ORC_QGROUP / 2; ++i)
+            packed[g * (ORC_QGROUP / 2) + i] = (uint8_t)(c4[2 * i] | (c4[2 * i + 1] << 4));
+    }
+}
+
+/* The 4-bit code of channel c of a packed row. */
+static int q4_code(const uint8_t *row, int c)
+{
+    return (row[c / 2] >> (4 * (c & 1))) & 15;
+}
+
+/* ------------------------------------------------------------------ */
 /* Cache description (layouts of the head-major cache).                */
 /*   K, V     [B, Hkv, max_seq, D]   f16 bits or int8 codes            */
 /*   ks, vs   [B, Hkv, max_seq]      f32 (int8 cache only)             */
-/*   kd, vd   [B, Hkv, max_seq, D/32] f16 bits (q8_0 cache only)       */
+/*   kd, vd   [B, Hkv, max_seq, D/32] f16 bits (q8_0, q4_0 caches)      */
+/*   K, V of a q4_0 cache: [B, Hkv, max_seq, D/2] packed 4-bit codes     */
 /*   kmin/kmax[B, Hkv, max_seq/blk, D] f16 bits                        */
 /* ------------------------------------------------------------------ */
 typedef struct {
@@ -215,6 +263,12 @@ int orc_append(orc_cache *c, const uint16_t *k_new, const uint16_t *v_new, int n
                 if (c->dtype == ORC_F16) {
                     memcpy((uint16_t *)c->K + r * D, kin, sizeof(uint16_t) * D);
                     memcpy((uint16_t *)c->V + r * D, vin, sizeof(uint16_t) * D);
+                } else if (c->dtype == ORC_Q4_0) {
+                    const int ng = D / ORC_QGROUP;
+                    for (int d = 0; d < D; ++d) row[d] = (float)orc_half_to_double(kin[d]);
+                    orc_quantize_q4_0(row, D, (uint8_t *)c->K + r * (D / 2), c->kd + r * ng);
+                    for (int d = 0; d < D; ++d) row[d] = (float)orc_half_to_double(vin[d]);
+                    orc_quantize_q4_0(row, D, (uint8_t *)c->V + r * (D / 2), c->vd + r * ng);
                 } else if (c->dtype == ORC_Q8_0) {
                     const int ng = D / ORC_QGROUP;
                     for (int d = 0; d < D; ++d) row[d] = (float)orc_half_to_double(kin[d]);
@@ -587,6 +641,60 @@ void orc_attend_q8_0(int D, int L, int blk, const int8_t *qc, float q_scale, dou
 }
 
 /* ------------------------------------------------------------------ */
+/* q4_0 attention of one query head (R9), with sparse-V at eps:         */
+/*   logit_t = softmax_scale * q_scale * sum_g d_g(k_t) * dot_g(t),      */
+/*   dot_g(t) = sum_{c in g} q_code[c] * (k_code_t[c] - 8)   (exact)     */
+/*   out[c]  = sum_t softmax(logit)_t * d_g(v_t) * (v_code_t[c] - 8)     */
+/* K, V: [max_seq, D/2] packed rows; kd, vd: [max_seq, D/32] binary16.  */
+/* ------------------------------------------------------------------ */
+void orc_attend_q4_0(int D, int L, int blk, const int8_t *qc, float q_scale, double scale,
+                     const uint8_t *K, const uint8_t *V, const uint16_t *kd,
+                     const uint16_t *vd, const int *sel, int n_sel, double eps, double *out,
+                     double *dropped)
+{
+    const int ng = D / ORC_QGROUP;
+    long cap = (long)L + 1;
+    long *tok = (long *)malloc(sizeof(long) * (size_t)cap);
+    long n = token_list(L, blk, sel, n_sel, tok);
+    double *lg = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    int *keep = (int *)calloc((size_t)(n > 0 ? n : 1), sizeof(int));
+    double M = -INFINITY;
+    for (long i = 0; i < n; ++i) {
+        const uint8_t *k = K + (size_t)tok[i] * (D / 2);
+        double sum = 0.0;
+        for (int g = 0; g < ng; ++g) {
+            int64_t dot = 0;
+            for (int c = g * ORC_QGROUP; c < (g + 1) * ORC_QGROUP; ++c)
+                dot += (int64_t)qc[c] * (int64_t)(q4_code(k, c) - 8);
+            sum += orc_half_to_double(kd[(size_t)tok[i] * ng + g]) * (double)dot;
+        }
+        lg[i] = scale * (double)q_scale * sum;
+        if (lg[i] > M) M = lg[i];
+    }
+    orc_sparse_v_keep(n, tok, lg, eps, keep);
+    double Z = 0.0, Zd = 0.0;
+    for (int c = 0; c < D; ++c) out[c] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        double w = exp(lg[i] - M);
+        Z += w;
+        if (!keep[i]) {
+            Zd += w;
+            continue;
+        }
+        const uint8_t *v4 = V + (size_t)tok[i] * (D / 2);
+        for (int c = 0; c < D; ++c)
+            out[c] += w * orc_half_to_double(vd[(size_t)tok[i] * ng + c / ORC_QGROUP]) *
+                      (double)(q4_code(v4, c) - 8);
+    }
+    if (n > 0)
+        for (int c = 0; c < D; ++c) out[c] /= Z;
+    if (dropped) *dropped = n > 0 ? Zd / Z : 0.0;
+    free(keep);
+    free(lg);
+    free(tok);
+}
+
+/* ------------------------------------------------------------------ */
 /* Exact integer q.k dots  [CPUATT Method "Logit dots are exact int32"].*/
 /*   dot_t = sum_d q_code[d] * k_code_t[d]   (|dot| <= D*127*127)       */
 /* ------------------------------------------------------------------ */
@@ -721,6 +829,14 @@ int orc_decode(const orc_cache *c, int H, const float *q, double scale, int k_se
             if (c->dtype == ORC_F16) {
                 orc_attend_f16(D, L, c->blk, qh, scale, (const uint16_t *)c->K + r0 * D,
                                (const uint16_t *)c->V + r0 * D, sel, n_sel, o);
+            } else if (c->dtype == ORC_Q4_0) {
+                int8_t *qc = (int8_t *)malloc((size_t)D);
+                float qs;
+                orc_quantize_row(qh, D, qc, &qs);
+                orc_attend_q4_0(D, L, c->blk, qc, qs, scale, (const uint8_t *)c->K + r0 * (D / 2),
+                                (const uint8_t *)c->V + r0 * (D / 2), c->kd + r0 * (D / ORC_QGROUP),
+                                c->vd + r0 * (D / ORC_QGROUP), sel, n_sel, 0.0, o, NULL);
+                free(qc);
             } else if (c->dtype == ORC_Q8_0) {
                 int8_t *qc = (int8_t *)malloc((size_t)D);
                 float qs;

@@ -67,6 +67,15 @@ MUTANTS = {
     "q8_value_scale_wrong_group": (
         "out[d] += w * orc_half_to_double(vd[(size_t)tok[i] * ng + d / ORC_QGROUP]) *",
         "out[d] += w * orc_half_to_double(vd[(size_t)tok[i] * ng + (d / ORC_QGROUP + 1) % ng]) *"),
+    # q4_0
+    "q4_scale_positive": ("float s32 = (float)(m / -8.0);", "float s32 = (float)(m / 8.0);"),
+    "q4_max_by_value": ("            if (mag > amax) {\n                amax = mag;\n                m = (double)xg[i];",
+                        "            if (mag > amax) {\n                amax = mag;\n                m = fabs((double)xg[i]);"),
+    "q4_nibbles_swapped": ("packed[g * (ORC_QGROUP / 2) + i] = (uint8_t)(c4[2 * i] | (c4[2 * i + 1] << 4));",
+                           "packed[g * (ORC_QGROUP / 2) + i] = (uint8_t)(c4[2 * i + 1] | (c4[2 * i] << 4));"),
+    "q4_no_offset_in_dot": ("dot += (int64_t)qc[c] * (int64_t)(q4_code(k, c) - 8);",
+                            "dot += (int64_t)qc[c] * (int64_t)q4_code(k, c);"),
+    "q4_round_half_up": ("double r4 = nearbyint((double)qt) + 8.0;", "double r4 = floor((double)qt + 0.5) + 8.0;"),
 }
 
 
@@ -85,7 +94,8 @@ def _run_mutant(name, old, new, tmp):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_sparse_v.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_q8_0.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_q8_0.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_q4_0.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return name, r.returncode
 
