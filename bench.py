@@ -58,16 +58,18 @@ def peaks():
 
 def kv_bytes_per_token(dtype):
     # K row + V row, plus one f32 scale each (int8) or four f16 group scales
-    # each (q8_0)
+    # each (q8_0, q4_0; a q4_0 row is 64 bytes)
     if dtype == kvd.INT8:
         return 2 * 128 + 2 * 4
     if dtype == kvd.Q8_0:
         return 2 * 128 + 2 * 4 * 2
+    if dtype == kvd.Q4_0:
+        return 2 * 64 + 2 * 4 * 2
     return 2 * 2 * 128
 
 
 def dtype_name(dtype):
-    return {kvd.F16: "f16", kvd.INT8: "int8", kvd.Q8_0: "q8_0"}[dtype]
+    return {kvd.F16: "f16", kvd.INT8: "int8", kvd.Q8_0: "q8_0", kvd.Q4_0: "q4_0"}[dtype]
 
 
 def attended_tokens(sel_idx, sel_cnt, L):

@@ -57,16 +57,17 @@ typedef enum {
     KVD_ERR_WORKSPACE = 6     /* workspace NULL, misaligned or too small */
 } kvd_status;
 
-typedef enum { KVD_F16 = 0, KVD_INT8 = 1, KVD_Q8_0 = 2 } kvd_kv_dtype;
+typedef enum { KVD_F16 = 0, KVD_INT8 = 1, KVD_Q8_0 = 2, KVD_Q4_0 = 3 } kvd_kv_dtype;
 
 /*
  * The cache: a plain descriptor of caller-owned device memory.
  *
  * Layout is head-major, so one block of `block` tokens of one (sequence,
  * KV head) is one contiguous run of memory:
- *   k, v        [batch, n_kv_heads, max_seq, head_dim]   f16 or int8 codes
+ *   k, v        [batch, n_kv_heads, max_seq, head_dim]   f16 or int8 codes,
+ *               or [.., head_dim / 2] bytes of 4-bit codes (q4_0)
  *   k_scale,    int8: [batch, n_kv_heads, max_seq] f32;
- *   v_scale     q8_0: [batch, n_kv_heads, max_seq, head_dim / 32] f16
+ *   v_scale     q8_0, q4_0: [batch, n_kv_heads, max_seq, head_dim / 32] f16
  *               (NULL for f16)
  *   kbounds     [batch, n_kv_heads, max_seq / block, head_dim, 2]  f16
  * kbounds holds the per-(KV head, block) channel-wise key envelope [QUEST
@@ -81,6 +82,11 @@ typedef enum { KVD_F16 = 0, KVD_INT8 = 1, KVD_Q8_0 = 2 } kvd_kv_dtype;
  * cache type of [QUEST] "All-KV-types composition"), each group with its
  * own f16 scale d = fl16(fl32(absmax_group / 127)); code = round-half-even
  * of the f32 quotient x / d, clamped to +-127 (zero codes when d is 0).
+ * q4_0 rows hold 4-bit codes per group of 32 channels: m is the group's
+ * value of largest magnitude (the first in channel order), the f16 scale is
+ * d = fl16(fl32(m / -8)), code = clamp(round-half-even(fl32(x / d)) + 8,
+ * 0, 15) (all 8 when d is 0), and the value is d * (code - 8); byte i of a
+ * group holds channels 2i (low nibble) and 2i+1 (high nibble).
  * The bounds come from the f16 keys on every cache type.
  *
  * `len` (tokens cached; the same for every sequence) is host state, advanced
@@ -161,6 +167,7 @@ KVD_API kvd_status kvd_select_blocks(const kvd_cache *cache, const float *q, int
 /*     q8_0: q as for int8; logit_t = q_scale * softmax_scale *             */
 /*           sum_g d_g(k_t) * dot_int32 over group g (32 channels), and     */
 /*           v_t[c] = d_g(v_t) * v_code_t[c] with g = c / 32                */
+/*     q4_0: as q8_0 with (code - 8) in place of the code                   */
 /*     out_h = sum_t softmax(logit)_t * v_t       (f32 accumulation)       */
 /*   An empty selection gives a zero output row.                           */
 /*   out: device [batch, n_heads, head_dim] f32.                            */

@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(PKG, "libkvdecode.so")
 F16 = 0
 INT8 = 1
 Q8_0 = 2
+Q4_0 = 3
 BLOCK = 64
 HEAD_DIM = 128
 
@@ -113,9 +114,10 @@ def _stream(t: torch.Tensor, stream=None):
 class KVCache:
     """Caller-owned cache tensors plus the C descriptor that points at them.
 
-    k, v      [B, Hkv, max_seq, 128]  float16 or int8 codes
+    k, v      [B, Hkv, max_seq, 128]  float16 or int8 codes, or
+              [B, Hkv, max_seq, 64]   uint8 pairs of 4-bit codes (q4_0)
     k_scale   [B, Hkv, max_seq]       float32 (int8), or
-              [B, Hkv, max_seq, 4]    float16 group scales (q8_0); same for v_scale
+              [B, Hkv, max_seq, 4]    float16 group scales (q8_0, q4_0); same for v_scale
     kbounds   [B, Hkv, max_seq // 64, 128, 2] float16: (kmin, kmax) per channel
     status    [1] int32 device word for device-side faults
     """
@@ -129,11 +131,13 @@ class KVCache:
         if tensors is not None:
             self.t = dict(tensors)
         else:
-            kvt = torch.float16 if dtype == F16 else torch.int8
+            kvt = (torch.float16 if dtype == F16 else
+                   torch.uint8 if dtype == Q4_0 else torch.int8)
+            width = head_dim // 2 if dtype == Q4_0 else head_dim  # q4_0: two codes a byte
             nb = max_seq // block if block > 0 else 0
             self.t = {
-                "k": torch.empty(batch, n_kv_heads, max_seq, head_dim, dtype=kvt, device=dev),
-                "v": torch.empty(batch, n_kv_heads, max_seq, head_dim, dtype=kvt, device=dev),
+                "k": torch.empty(batch, n_kv_heads, max_seq, width, dtype=kvt, device=dev),
+                "v": torch.empty(batch, n_kv_heads, max_seq, width, dtype=kvt, device=dev),
                 "kbounds": torch.empty(batch, n_kv_heads, nb, head_dim, 2, dtype=torch.float16,
                                        device=dev),
                 "status": torch.zeros(1, dtype=torch.int32, device=dev),
@@ -143,7 +147,7 @@ class KVCache:
                                                 device=dev)
                 self.t["v_scale"] = torch.empty(batch, n_kv_heads, max_seq, dtype=torch.float32,
                                                 device=dev)
-            elif dtype == Q8_0:
+            elif dtype in (Q8_0, Q4_0):
                 ng = head_dim // 32
                 self.t["k_scale"] = torch.empty(batch, n_kv_heads, max_seq, ng,
                                                 dtype=torch.float16, device=dev)
@@ -289,7 +293,7 @@ def debug_scores(cache: KVCache, q: torch.Tensor, ub: torch.Tensor, stream=None)
         cache.ref(), _ptr(q), int(q.shape[1]), _ptr(ub), _stream(q, stream)))
 
 
-__all__ = ["F16", "INT8", "Q8_0", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
+__all__ = ["F16", "INT8", "Q8_0", "Q4_0", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
            "workspace_bytes", "make_workspace", "selected_count", "status_string", "kv_append",
            "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
            "decode_attn_sv", "decode_step",

@@ -40,7 +40,8 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 kvd_status check_cache(const kvd_cache *c) {
     if (!c) return KVD_ERR_INVALID;
-    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8 && c->dtype != KVD_Q8_0)
+    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8 && c->dtype != KVD_Q8_0 &&
+        c->dtype != KVD_Q4_0)
         return KVD_ERR_INVALID;
     if (c->batch < 1 || c->n_kv_heads < 1) return KVD_ERR_INVALID;
     if (c->head_dim != kHeadDim) return KVD_ERR_UNSUPPORTED;
@@ -51,7 +52,7 @@ kvd_status check_cache(const kvd_cache *c) {
     const void *ptrs[3] = {c->k, c->v, c->kbounds};
     for (const void *p : ptrs)
         if (!p || !aligned(p, 16)) return KVD_ERR_INVALID;
-    if (c->dtype == KVD_INT8 || c->dtype == KVD_Q8_0) {
+    if (c->dtype != KVD_F16) {
         if (!c->k_scale || !c->v_scale || !aligned(c->k_scale, 16) || !aligned(c->v_scale, 16))
             return KVD_ERR_INVALID;
     }

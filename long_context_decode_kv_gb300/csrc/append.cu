@@ -43,6 +43,9 @@ cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_n
     if (c.dtype == KVD_Q8_0)
         return launch_ex(append_kernel<KVD_Q8_0>, grid, block, 0, st, pdl, c, kn, vn, n_new,
                          len0, first, n_aff);
+    if (c.dtype == KVD_Q4_0)
+        return launch_ex(append_kernel<KVD_Q4_0>, grid, block, 0, st, pdl, c, kn, vn, n_new,
+                         len0, first, n_aff);
     return launch_ex(append_kernel<KVD_INT8>, grid, block, 0, st, pdl, c, kn, vn, n_new, len0,
                      first, n_aff);
 }

@@ -57,6 +57,20 @@ __device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __ha
                 *reinterpret_cast<const uint2 *>(k_new + src);
             *reinterpret_cast<uint2 *>(static_cast<__half *>(c.v) + dst) =
                 *reinterpret_cast<const uint2 *>(v_new + src);
+        } else if (DT == KVD_Q4_0) {
+            __half kd, vd;
+            const uint32_t kc = quantize_q4_0_warp(kx, &kd, lane);
+            const uint32_t vc = quantize_q4_0_warp(vx, &vd, lane);
+            const size_t dst4 = (row0 + t) * (kHeadDim / 2) + 2 * lane;  // 2 bytes per lane
+            *reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(c.k) + dst4) =
+                static_cast<uint16_t>(kc);
+            *reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(c.v) + dst4) =
+                static_cast<uint16_t>(vc);
+            if ((lane & 7) == 0) {  // one lane per 32-channel group
+                const size_t si = (row0 + t) * (kHeadDim / 32) + (lane >> 3);
+                static_cast<__half *>(c.k_scale)[si] = kd;
+                static_cast<__half *>(c.v_scale)[si] = vd;
+            }
         } else if (DT == KVD_Q8_0) {
             __half kd, vd;
             const uint32_t kc = quantize_group32_warp(kx, &kd);

@@ -177,6 +177,51 @@ __device__ __forceinline__ uint32_t quantize_group32_warp(const float (&x)[4], _
     return packed;
 }
 
+// q4_0 quantization of one 128-wide row held 4 values per lane by a full
+// warp (group g = lanes 8g..8g+7).  m is the group's value of largest
+// magnitude, the first one in channel order; the scale is d = fl16(m/-8)
+// (the IEEE f32 quotient rounded to f16); code = round-half-even(x/d) + 8 in
+// f32, clamped to [0, 15] (8 when d is 0).  Returns the lane's two bytes:
+// channel 4l in the low nibble of the first, 4l+1 in its high nibble, and
+// so on; writes the group's scale to *d.
+__device__ __forceinline__ uint32_t quantize_q4_0_warp(const float (&x)[4], __half *d,
+                                                       int lane) {
+    float mag = -1.0f, m = 0.0f;
+    int idx = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (fabsf(x[j]) > mag) {
+            mag = fabsf(x[j]);
+            m = x[j];
+            idx = 4 * lane + j;
+        }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, mag, o);
+        const float ov = __shfl_xor_sync(0xffffffffu, m, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (om > mag || (om == mag && oi < idx)) {
+            mag = om;
+            m = ov;
+            idx = oi;
+        }
+    }
+    const __half dh = __float2half_rn(__fdiv_rn(m, -8.0f));
+    *d = dh;
+    const float s = __half2float(dh);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        int c = 8;
+        if (s != 0.0f) {
+            const float r = rintf(__fdiv_rn(x[j], s)) + 8.0f;
+            c = static_cast<int>(fminf(fmaxf(r, 0.0f), 15.0f));
+        }
+        packed |= static_cast<uint32_t>(c) << (4 * j);
+    }
+    return packed;  // 16 bits: channels 4l .. 4l+3, low nibble first
+}
+
 // Absmax int8 quantization of one 128-wide row held 4 values per lane by a
 // full warp (lane l holds x[4l..4l+3]).  scale = absmax/127 (IEEE f32
 // division), code = round-half-even(x/scale) clamped to +-127, and a zero

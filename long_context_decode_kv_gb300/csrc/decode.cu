@@ -50,6 +50,7 @@ DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count) {
     const long P = static_cast<long>(g.B) * g.Hkv * p.subgroups;
     const int per_sm = g.dtype == KVD_F16    ? Tile<KVD_F16>::kMinCtas
                        : g.dtype == KVD_Q8_0 ? Tile<KVD_Q8_0>::kMinCtas
+                       : g.dtype == KVD_Q4_0 ? Tile<KVD_Q4_0>::kMinCtas
                                              : Tile<KVD_INT8>::kMinCtas;
     const long target = static_cast<long>(sm_count) * per_sm;  // one wave of resident CTAs
     long s = P >= target ? 1 : target / P;

@@ -67,6 +67,18 @@ struct Tile<KVD_Q8_0> {
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
 };
 template <>
+struct Tile<KVD_Q4_0> {
+    static constexpr int kRowBytes = kHeadDim / 2;                    // 4-bit codes
+    static constexpr int kKBytes = kBlock * kRowBytes;                // 4096
+    static constexpr int kScaleBytes = kBlock * (kHeadDim / 32) * 2;  // f16 group scales: 512
+    static constexpr int kStageBytes = 2 * kKBytes + 2 * kScaleBytes;
+    static constexpr int kGroups = 2;
+    static constexpr int kStages = 10;  // a multiple of kGroups
+    static constexpr int kMinCtas = 2;
+    static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+};
+template <>
 struct Tile<KVD_F16> {
     static constexpr int kRowBytes = 2 * kHeadDim;                    // f16
     static constexpr int kKBytes = kBlock * kRowBytes;                // 16384
@@ -112,7 +124,8 @@ struct SmemLayout {
     static constexpr int kQOff = (kBlkOff + 4 * kStages + 15) / 16 * 16;
     static constexpr int kQBytes = GC * kHeadDim * 4;  // f32 q (f16 cache) or codes
     static constexpr int kCoefOff = kQOff + kQBytes;
-    static constexpr int kPwOff = kCoefOff + 16;
+    static constexpr int kQsumOff = kCoefOff + 16;  // q4_0: [GC][4] group sums of the codes
+    static constexpr int kPwOff = kQsumOff + 64;
     // [warp][16 tokens][4 heads] pairs (p, p)
     static constexpr int kPwBytes = Tile<DT>::kConsumerWarps * kTokensPerWarp * 4 * 2 * 4;
     static constexpr int kLOff = kPwOff + kPwBytes;  // split merge: L per head
@@ -199,6 +212,14 @@ __device__ __forceinline__ void load_query(const DecodeArgs &a, int b, int h0, i
         const uint32_t packed = quantize_row_warp(x, &s);
         q_s[warp * 32 + lane] = packed;
         if (lane == 0) coef[warp] = s * a.scale_log2;
+        if constexpr (DT == KVD_Q4_0) {
+            // sum of the head's codes over each 32-channel group (lanes 8g..8g+7)
+            int qs = __dp4a(static_cast<int>(packed), 0x01010101, 0);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) qs += __shfl_xor_sync(kFull, qs, o);
+            if ((lane & 7) == 0)
+                reinterpret_cast<int *>(coef + 4)[warp * 4 + (lane >> 3)] = qs;
+        }
         if (q_codes_out) {
             *reinterpret_cast<uint32_t *>(q_codes_out +
                                           (static_cast<size_t>(b) * a.H + hq) * kHeadDim +
@@ -270,6 +291,73 @@ __device__ __forceinline__ float qk_q8_row(const int8_t *row, const QRegsI8<GC> 
         d[h] = static_cast<float>(s) * kscale;  // |s| <= 32*127*127: exact in f32
     }
     return reduce4_scatter<GC>(d, c);
+}
+
+// q4_0: lane (t, c) reads its token row's 16 bytes of group c (32 channels,
+// two per byte).  Its word i holds channels 8i..8i+7 of the group; the low
+// nibbles are channels 8i, 8i+2, 8i+4, 8i+6 and the high ones the odd
+// channels, so the query words are held in that even/odd order.  The codes
+// (0..15) are non-negative as signed bytes, so dp4a gives sum(q * code), and
+// q * (code - 8) subtracts 8 times the group's query sum.
+template <int GC>
+struct QRegsQ4 {
+    uint32_t lo[GC][4], hi[GC][4];
+    int qsum[GC];  // sum of the head's codes over this lane's group
+};
+
+template <int GC>
+__device__ __forceinline__ void load_qregs_q4(const uint32_t *q_s, const int *qsum_s, int c,
+                                              QRegsQ4<GC> &r) {
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w0 = q_s[h * 32 + 8 * c + 2 * i];      // channels 8i .. 8i+3
+            const uint32_t w1 = q_s[h * 32 + 8 * c + 2 * i + 1];  // channels 8i+4 .. 8i+7
+            r.lo[h][i] = __byte_perm(w0, w1, 0x6420);
+            r.hi[h][i] = __byte_perm(w0, w1, 0x7531);
+        }
+        r.qsum[h] = qsum_s[h * 4 + c];
+    }
+}
+
+template <int GC>
+__device__ __forceinline__ float qk_q4_row(const uint8_t *row, const QRegsQ4<GC> &r, int c,
+                                           float kscale) {
+    const uint4 kw = *reinterpret_cast<const uint4 *>(row + 16 * c);
+    const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
+    uint32_t lo[4], hi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        lo[i] = w[i] & 0x0f0f0f0fu;
+        hi[i] = (w[i] >> 4) & 0x0f0f0f0fu;
+    }
+    float d[GC];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        int s = -8 * r.qsum[h];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            s = __dp4a(static_cast<int>(lo[i]), static_cast<int>(r.lo[h][i]), s);
+            s = __dp4a(static_cast<int>(hi[i]), static_cast<int>(r.hi[h][i]), s);
+        }
+        d[h] = static_cast<float>(s) * kscale;  // |s| <= 32*127*8: exact in f32
+    }
+    return reduce4_scatter<GC>(d, c);
+}
+
+// Two 4-bit codes per byte of w16 (channels 4l .. 4l+3 of the lane) -> the
+// exact floats code - 8, as pairs.
+__device__ __forceinline__ void u4x4_to_f32x2(uint32_t w16, float2 &f01, float2 &f23) {
+    const uint32_t lo = w16 & 0x0f0fu;         // codes of channels 4l and 4l+2
+    const uint32_t hi = (w16 >> 4) & 0x0f0fu;  // codes of channels 4l+1 and 4l+3
+    const float2 bias = make_float2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
+    f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650)),
+                                 __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650))),
+                     bias);
+    f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7651)),
+                                 __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7651))),
+                     bias);
 }
 
 // f16 QK mapping: lane = 8 t4 + e (t4: token slot 0..3 per pass, e: eighth
@@ -566,6 +654,83 @@ __device__ __forceinline__ void consume_q8(const uint8_t *stage, int n_valid, co
     }
 }
 
+// One stage for one consumer warp, q4_0 cache: consume_q8 with the 4-bit
+// rows unpacked in registers.
+template <int GC, bool SV>
+__device__ __forceinline__ void consume_q4(const uint8_t *stage, int n_valid, const float *coef,
+                                           const QRegsQ4<GC> &qr, float *pw, int wg, int lane,
+                                           WarpState<GC> &st, float sv_eps) {
+    using TQ = Tile<KVD_Q4_0>;
+    const uint8_t *Ks = stage;
+    const uint8_t *Vs = Ks + TQ::kKBytes;
+    const __half *kd = reinterpret_cast<const __half *>(stage + 2 * TQ::kKBytes);  // [64][4]
+    const __half *vd = kd + kBlock * (kHeadDim / 32);
+    const int t = lane >> 2, c = lane & 3;
+    const int tok0 = kTokensPerWarp * wg + t, tok1 = tok0 + 8;
+    const int hq = (c * GC) >> 2;
+    const float ninf = -__int_as_float(0x7f800000);
+    const float dot0 = qk_q4_row<GC>(Ks + tok0 * TQ::kRowBytes, qr, c,
+                                     __half2float(kd[tok0 * (kHeadDim / 32) + c]));
+    const float dot1 = qk_q4_row<GC>(Ks + tok1 * TQ::kRowBytes, qr, c,
+                                     __half2float(kd[tok1 * (kHeadDim / 32) + c]));
+    const float cf = coef[hq];
+    const float x0 = tok0 < n_valid ? dot0 * cf : ninf;
+    const float x1 = tok1 < n_valid ? dot1 * cf : ninf;
+    float bm = fmaxf(x0, x1);
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
+    const float m_new = fmaxf(st.m, bm);
+    const float alpha = exp2f(st.m - m_new);
+    const float p0 = exp2f(x0 - m_new), p1 = exp2f(x1 - m_new);
+    st.l = st.l * alpha + (p0 + p1);
+    st.m = m_new;
+    bool keep[2] = {true, true};
+    uint32_t live = 0xffffu;
+    if constexpr (SV) {
+        const float xs[2] = {x0, x1};
+        sparse_v_keep<2, 4>(xs, bm, min(max(n_valid - kTokensPerWarp * wg, 0), kTokensPerWarp),
+                            sv_eps, keep);
+        const uint32_t b0 = __ballot_sync(kFull, keep[0] && tok0 < n_valid);
+        const uint32_t b1 = __ballot_sync(kFull, keep[1] && tok1 < n_valid);
+        live = any_per_group<8, 4>(b0) | (any_per_group<8, 4>(b1) << 8);
+    }
+    constexpr int lph = 4 / GC;
+    if ((c % lph) == 0) {
+        const float w0 = tok0 < n_valid && keep[0] ? p0 : 0.0f;
+        const float w1 = tok1 < n_valid && keep[1] ? p1 : 0.0f;
+        *reinterpret_cast<float2 *>(pw + (t * 4 + hq) * 2) = make_float2(w0, w0);
+        *reinterpret_cast<float2 *>(pw + ((t + 8) * 4 + hq) * 2) = make_float2(w1, w1);
+    }
+    rescale<GC>(st, alpha, lph);
+    __syncwarp();
+    const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
+    const uint8_t *vrow = Vs + kTokensPerWarp * wg * TQ::kRowBytes + 2 * lane;
+    const __half *vdl = vd + kTokensPerWarp * wg * (kHeadDim / 32) + (lane >> 3);
+    if ((SV && live != 0xffffu) || nt != kTokensPerWarp) {
+        uint32_t m = live & ((1u << max(nt, 0)) - 1u);
+        for (; m; m &= m - 1u) {
+            const int t2 = __ffs(m) - 1;
+            float2 f01, f23;
+            u4x4_to_f32x2(*reinterpret_cast<const uint16_t *>(vrow + t2 * TQ::kRowBytes), f01,
+                          f23);
+            const float dv = __half2float(vdl[t2 * (kHeadDim / 32)]);
+            const float2 d2 = make_float2(dv, dv);
+            pv_token<GC>(st, pw + t2 * 8, __fmul2_rn(f01, d2), __fmul2_rn(f23, d2));
+        }
+    } else {
+#pragma unroll
+        for (int t2 = 0; t2 < kTokensPerWarp; ++t2) {
+            float2 f01, f23;
+            u4x4_to_f32x2(*reinterpret_cast<const uint16_t *>(vrow + t2 * TQ::kRowBytes), f01,
+                          f23);
+            const float dv = __half2float(vdl[t2 * (kHeadDim / 32)]);
+            const float2 d2 = make_float2(dv, dv);
+            pv_token<GC>(st, pw + t2 * 8, __fmul2_rn(f01, d2), __fmul2_rn(f23, d2));
+        }
+    }
+}
+
 // One stage for one consumer warp (wg = its index in the group), f16 cache:
 // four QK passes of 4 tokens.
 template <int GC, bool SV>
@@ -736,8 +901,8 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                                 tma_load_1d(dst + 2 * TL::kKBytes + kBlock * 4,
                                             static_cast<const float *>(a.v_scale) + r,
                                             kBlock * 4, &full[s], pol);
-                            } else if constexpr (DT == KVD_Q8_0) {
-                                constexpr int kSB = Tile<KVD_Q8_0>::kScaleBytes;
+                            } else if constexpr (DT == KVD_Q8_0 || DT == KVD_Q4_0) {
+                                constexpr int kSB = TL::kScaleBytes;
                                 tma_load_1d(dst + 2 * TL::kKBytes,
                                             static_cast<const __half *>(a.k_scale) +
                                                 r * (kHeadDim / 32),
@@ -788,7 +953,30 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         asm volatile("bar.sync 1, %0;" ::"r"(TL::kConsumerWarps * 32) : "memory");
         float *pw = pw_all + warp * (kTokensPerWarp * 4 * 2);
         const int group = warp / kWarpsPerGroup, wg = warp % kWarpsPerGroup;
-        if constexpr (DT != KVD_F16) {
+        if constexpr (DT == KVD_Q4_0) {
+            QRegsQ4<GC> qr;
+            load_qregs_q4<GC>(q_s, reinterpret_cast<const int *>(coef + 4), lane & 3, qr);
+            for (int i = group;; i += TL::kGroups) {
+                const int s = i % TL::kStages;
+                const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
+                if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                    }
+                    break;
+                }
+                const int blk = stage_blk[s];
+                if (blk == kEndMark) break;
+                if (blk >= 0) {
+                    const int n_valid = min(kBlock, a.len - blk * kBlock);
+                    consume_q4<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
+                                       coef, qr, pw, wg, lane, st, a.sv_eps);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+        } else if constexpr (DT != KVD_F16) {
             QRegsI8<GC> qr;
             load_qregs_i8<GC>(q_s, lane >> 2, lane & 3, qr);
             for (int i = group;; i += TL::kGroups) {
@@ -1089,6 +1277,9 @@ cudaError_t launch_decode_any(const kvd_cache &c, const Geom &g, const DecodePla
     if (g.dtype == KVD_Q8_0)
         return dense ? launch_decode_gc<KVD_Q8_0, true, SV>(gc, a, P_sub, st, pdl)
                      : launch_decode_gc<KVD_Q8_0, false, SV>(gc, a, P_sub, st, pdl);
+    if (g.dtype == KVD_Q4_0)
+        return dense ? launch_decode_gc<KVD_Q4_0, true, SV>(gc, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_Q4_0, false, SV>(gc, a, P_sub, st, pdl);
     return dense ? launch_decode_gc<KVD_F16, true, SV>(gc, a, P_sub, st, pdl)
                  : launch_decode_gc<KVD_F16, false, SV>(gc, a, P_sub, st, pdl);
 }

@@ -519,6 +519,9 @@ __device__ __noinline__ void fused_append(const SelArgs &a, int b, int g, int la
     if (a.app_cache.dtype == KVD_Q8_0)
         append_block_warp<KVD_Q8_0>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
                                     lane);
+    else if (a.app_cache.dtype == KVD_Q4_0)
+        append_block_warp<KVD_Q4_0>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
+                                    lane);
     else if (a.app_cache.dtype == KVD_F16)
         append_block_warp<KVD_F16>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
                                    lane);

@@ -50,7 +50,8 @@ bool aligned_to(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p)
 kvd_status check_args(const kvd_cache *c, const float *q, int n_heads, const int32_t *sel_idx,
                       const int32_t *sel_cnt, int max_sel, const float *out) {
     if (!c) return KVD_ERR_INVALID;
-    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8 && c->dtype != KVD_Q8_0)
+    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8 && c->dtype != KVD_Q8_0 &&
+        c->dtype != KVD_Q4_0)
         return KVD_ERR_INVALID;
     if (c->batch < 1 || c->n_kv_heads < 1) return KVD_ERR_INVALID;
     if (c->head_dim != kHeadDim || c->block != kBlock) return KVD_ERR_UNSUPPORTED;

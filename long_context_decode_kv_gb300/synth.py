@@ -25,6 +25,7 @@ import torch
 F16 = 0
 INT8 = 1
 Q8_0 = 2
+Q4_0 = 3
 
 
 @dataclasses.dataclass(frozen=True)
@@ -86,10 +87,12 @@ CTX1M = Workload("ctx1m_int8", B=1, H=32, Hkv=8, D=128, L=1 << 20, dtype=INT8,
                  keys="drift_needles", n_needles=64, sink_tokens=4, recent_tokens=1024,
                  k_sel=1024, seed=1238)
 
-# the 1M recipe on a group-quantized (q8_0) cache: same keys, same selection
+# the 1M recipe on group-quantized (q8_0, q4_0) caches: same keys, same selection
 CTX1M_Q8 = CTX1M.with_(name="ctx1m_q8_0", dtype=Q8_0)
+CTX1M_Q4 = CTX1M.with_(name="ctx1m_q4_0", dtype=Q4_0)
 
-WORKLOADS = {w.name: w for w in (TINY, *INT8_DENSE, QWEN3_32K, CTX128K_B8, CTX1M, CTX1M_Q8)}
+WORKLOADS = {w.name: w for w in (TINY, *INT8_DENSE, QWEN3_32K, CTX128K_B8, CTX1M, CTX1M_Q8,
+                                 CTX1M_Q4)}
 
 
 def context_sweep(frac: float = 0.25):

@@ -19,7 +19,7 @@ import torch
 import long_context_decode_kv_gb300 as kvd
 import oracle
 
-TOL = {kvd.F16: 2e-3, kvd.INT8: 8e-3, kvd.Q8_0: 8e-3}
+TOL = {kvd.F16: 2e-3, kvd.INT8: 8e-3, kvd.Q8_0: 8e-3, kvd.Q4_0: 8e-3}
 TIGHT = 1e-4
 TIE_REL = 1e-5
 

@@ -105,6 +105,9 @@ def test_select_validation():
     assert _select(_cache(k=FAKE + 2)) == INVALID
     assert _select(_cache(kbounds=None)) == INVALID
     assert _select(_cache(k_scale=None)) == INVALID
+    for dt in (kvd.Q8_0, kvd.Q4_0):                         # group scales required
+        assert _select(_cache(dtype=dt, k_scale=None)) == INVALID
+        assert _select(_cache(dtype=dt, v_scale=None)) == INVALID
     assert _select(_cache(max_seq=100)) == INVALID           # not a multiple of 64
     assert _select(_cache(length=5000)) == INVALID           # len > max_seq
     assert _select(_cache(reserved=1)) == INVALID
@@ -142,7 +145,7 @@ def test_append_validation():
     assert s.len == 4090
     assert L.kvd_kv_append(C.byref(s), FAKE + 2, FAKE, 1, None) == INVALID
     assert L.kvd_kv_append(C.byref(s), None, FAKE, 1, None) == INVALID
-    assert L.kvd_kv_append(C.byref(_cache(dtype=3)), FAKE, FAKE, 1, None) == INVALID
+    assert L.kvd_kv_append(C.byref(_cache(dtype=7)), FAKE, FAKE, 1, None) == INVALID
     assert L.kvd_kv_append(C.byref(None if False else _cache(n_kv_heads=0)), FAKE, FAKE, 1,
                            None) == INVALID
 

@@ -23,7 +23,7 @@ def _compare(gc, oc):
                            torch.from_numpy(oc.K[:, :, :L].view(np.int16)))
         assert torch.equal(gc.v[:, :, :L].cpu().view(torch.int16),
                            torch.from_numpy(oc.V[:, :, :L].view(np.int16)))
-    elif gc.dtype == kvd.Q8_0:
+    elif gc.dtype in (kvd.Q8_0, kvd.Q4_0):
         assert np.array_equal(gc.k[:, :, :L].cpu().numpy(), oc.K[:, :, :L])
         assert np.array_equal(gc.v[:, :, :L].cpu().numpy(), oc.V[:, :, :L])
         assert np.array_equal(gc.k_scale[:, :, :L].cpu().numpy().view(np.uint16),
@@ -43,7 +43,7 @@ def _compare(gc, oc):
                           oc.kmax[:, :, :nb].astype(np.float32))
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 @pytest.mark.parametrize("L,chunks", [
     (1, None), (63, None), (64, None), (65, None), (300, None),
     (300, [1] * 70 + [230]), (1000, [63, 2, 64, 1, 870]), (4160, [4096, 1, 63]),
@@ -56,7 +56,7 @@ def test_append_matches_oracle(dtype, L, chunks):
     _compare(gc, oc)
 
 
-@pytest.mark.parametrize("dtype", [kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 @pytest.mark.parametrize("dist", ["outliers", "tiny", "ties", "zeros"])
 def test_int8_quantization_edge_values(dist, dtype):
     B, L, Hkv = 1, 256, 2

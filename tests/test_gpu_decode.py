@@ -36,7 +36,7 @@ def _sparse(gc, q, scale, sel_idx, sel_cnt, max_sel, ws=None):
     return out
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 @pytest.mark.parametrize("B,Hkv,G,L", [
     (1, 1, 1, 1), (1, 2, 1, 63), (1, 8, 1, 512), (2, 2, 4, 1000), (1, 8, 4, 4097),
     (1, 2, 2, 777), (1, 1, 8, 2000), (1, 1, 16, 300), (40, 8, 4, 200), (3, 1, 4, 20000),
@@ -51,7 +51,7 @@ def test_dense_matches_oracle(dtype, B, Hkv, G, L):
     assert_outputs(out, ref, dtype, f"dense {dtype} B{B} Hkv{Hkv} G{G} L{L}")
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 @pytest.mark.parametrize("L,k_sel,sink,recent", [
     (512, 4, 4, 64), (1000, 3, 0, 1), (5000, 20, 4, 256), (20000, 50, 64, 1000),
 ])
@@ -69,7 +69,7 @@ def test_sparse_with_oracle_selection(dtype, L, k_sel, sink, recent):
     assert_outputs(out, ref, dtype, f"sparse {dtype} L{L}")
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 def test_select_all_equals_dense(dtype):
     # gate ladder plumbing anchor: K_SEL = n_blocks => sparse == dense
     B, Hkv, G, L = 2, 4, 4, 3333

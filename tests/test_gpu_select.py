@@ -19,7 +19,7 @@ def _q(B, H, seed, scale=1.0):
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 def test_scores_match_oracle(G, dtype):
     B, Hkv, L = 2, 2, 1000
     k = seeded((B, L, Hkv, 128), 31) + 0.5

@@ -30,13 +30,23 @@ def _tokens(L, sel):
         else np.zeros(0, np.int64)
 
 
+def _codes(dtype, rows):
+    """Integer code values of cache rows: int8 codes, or 4-bit codes minus 8."""
+    if dtype == kvd.Q4_0:
+        out = np.empty(rows.shape[:-1] + (rows.shape[-1] * 2,), np.float64)
+        out[..., 0::2] = (rows & 15).astype(np.float64) - 8
+        out[..., 1::2] = (rows >> 4).astype(np.float64) - 8
+        return out
+    return rows.astype(np.float64)
+
+
 def _logits(dtype, oc, qh, b, g, tok, scale):
     if dtype == kvd.F16:
         K = oc.K[b, g, tok].astype(np.float64)
         return scale * (K @ qh.astype(np.float64))
     qc, qs = oracle.quantize_row(qh)
-    if dtype == kvd.Q8_0:
-        K = oc.K[b, g, tok].astype(np.float64) * np.repeat(
+    if dtype in (kvd.Q8_0, kvd.Q4_0):
+        K = _codes(dtype, oc.K[b, g, tok]) * np.repeat(
             oc.kd[b, g, tok].astype(np.float64), 32, axis=1)
         return (K @ qc.astype(np.float64)) * float(qs) * scale
     dots = oracle.qk_int8(qc, oc.K[b, g, tok])
@@ -62,8 +72,8 @@ def _reference(dtype, oc, q_np, b, g, G, L, sel, eps, scale):
     tok = _tokens(L, sel)
     if dtype == kvd.F16:
         vrows = oc.V[b, g, tok].astype(np.float64)
-    elif dtype == kvd.Q8_0:
-        vrows = oc.V[b, g, tok].astype(np.float64) * np.repeat(
+    elif dtype in (kvd.Q8_0, kvd.Q4_0):
+        vrows = _codes(dtype, oc.V[b, g, tok]) * np.repeat(
             oc.vd[b, g, tok].astype(np.float64), 32, axis=1)
     else:
         vrows = oc.V[b, g, tok].astype(np.float64) * oc.vs[b, g, tok, None].astype(np.float64)
@@ -71,10 +81,11 @@ def _reference(dtype, oc, q_np, b, g, G, L, sel, eps, scale):
         qh = q_np[b, g * G + h]
         if dtype == kvd.F16:
             o, d = oracle.attend_f16_sv(qh, oc.K[b, g], oc.V[b, g], L, 64, scale, eps, sel=sel)
-        elif dtype == kvd.Q8_0:
+        elif dtype in (kvd.Q8_0, kvd.Q4_0):
             qc, qs = oracle.quantize_row(qh)
-            o, d = oracle.attend_q8_0(qc, qs, oc.K[b, g], oc.V[b, g], oc.kd[b, g], oc.vd[b, g],
-                                      L, 64, scale, sel=sel, eps=eps)
+            att = oracle.attend_q8_0 if dtype == kvd.Q8_0 else oracle.attend_q4_0
+            o, d = att(qc, qs, oc.K[b, g], oc.V[b, g], oc.kd[b, g], oc.vd[b, g], L, 64, scale,
+                       sel=sel, eps=eps)
         else:
             qc, qs = oracle.quantize_row(qh)
             o, d = oracle.attend_int8_sv(qc, qs, oc.K[b, g], oc.V[b, g], oc.ks[b, g],
@@ -101,7 +112,7 @@ def _case(dtype, B, Hkv, G, L, seed):
     return gc, oc, q
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 @pytest.mark.parametrize("eps", [0.05, 0.5, 2.0])
 @pytest.mark.parametrize("sparse", [True, False])
 def test_sparse_v_matches_oracle(dtype, eps, sparse):
@@ -135,7 +146,7 @@ def test_sparse_v_matches_oracle(dtype, eps, sparse):
         assert min(dropped) > 0.0  # the rule did drop something in every head
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 def test_eps_zero_is_bit_identical(dtype):
     B, Hkv, G, L = 1, 8, 4, 9000
     gc, oc, q = _case(dtype, B, Hkv, G, L, 350)

@@ -11,7 +11,7 @@ from gpu_util import assert_outputs, check_selection, dev, make_pair, scale_for,
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 @pytest.mark.parametrize("sparse", [True, False])
 def test_steps_match_oracle(dtype, sparse):
     B, Hkv, G, L0, steps = 2, 2, 4, 1980, 6      # merges into block 30, then opens block 31
@@ -47,11 +47,11 @@ def test_steps_match_oracle(dtype, sparse):
                         if dtype == kvd.F16:
                             ref[b, hq] = oracle.attend_f16(qn[b, hq], oc.K[b, g], oc.V[b, g],
                                                            oc.len, 64, scale_for(), sel=sel)
-                        elif dtype == kvd.Q8_0:
+                        elif dtype in (kvd.Q8_0, kvd.Q4_0):
                             c, qs = oracle.quantize_row(qn[b, hq])
-                            ref[b, hq] = oracle.attend_q8_0(c, qs, oc.K[b, g], oc.V[b, g],
-                                                            oc.kd[b, g], oc.vd[b, g], oc.len, 64,
-                                                            scale_for(), sel=sel)[0]
+                            att = oracle.attend_q8_0 if dtype == kvd.Q8_0 else oracle.attend_q4_0
+                            ref[b, hq] = att(c, qs, oc.K[b, g], oc.V[b, g], oc.kd[b, g],
+                                             oc.vd[b, g], oc.len, 64, scale_for(), sel=sel)[0]
                         else:
                             c, qs = oracle.quantize_row(qn[b, hq])
                             ref[b, hq] = oracle.attend_int8(c, qs, oc.K[b, g], oc.V[b, g],
@@ -62,7 +62,7 @@ def test_steps_match_oracle(dtype, sparse):
         assert_outputs(out, ref, dtype, f"step {s}")
 
 
-@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0])
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 @pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
 def test_host_step_equals_device_step(dtype, pinned):
     # pinned (device-mapped) host buffers are used in place by the kernels,
