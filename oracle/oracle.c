@@ -34,13 +34,13 @@
  *  R6  attention over an empty token set returns the zero vector.
  *  R7  sparse-V (eps mode): the mean weight a position is compared with is
  *      taken over its 16-token chunk of the attended positions.
- *  R9  q4_0 (named, not defined, by the pages): per 32-channel group the
- *      f16 scale fl16(fl32(m/-8)) of the largest-magnitude value m, codes
- *      clamp(round-half-even(fl32(x/d)) + 8, 0, 15), two per byte.
  *  R8  q8_0 (named, not defined, by the pages): per 32-channel group an f16
  *      scale fl16(fl32(amax/127)) and codes round-half-even(fl32(x/d))
  *      clamped to +-127; the query is quantized per row as for int8, and the
  *      logit sums the exact per-group dots times the group scales.
+ *  R9  q4_0 (named, not defined, by the pages): per 32-channel group the
+ *      f16 scale fl16(fl32(m/-8)) of the largest-magnitude value m, codes
+ *      clamp(round-half-even(fl32(x/d)) + 8, 0, 15), two per byte.
  *
  * Every floating-point step runs in IEEE binary64 unless a step of the
  * method fixes f32 (the quantizer's scale and quotient, R1).  Build with
