@@ -60,6 +60,8 @@ def lib():
         L.orc_attend_q4_0.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
         L.orc_attend_f16_sv.argtypes = [i, i, i, p, d, p, p, p, i, d, p, p]
         L.orc_attend_int8_sv.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
+        L.orc_block_moments.argtypes = [i, i, i, p, p]
+        L.orc_attend_tail.argtypes = [i, i, i, p, p, d, p, p, p, i, p, p, p]
         L.orc_decode.argtypes = [p, i, p, d, i, i, i, i, p, p, p, i]
         L.orc_decode.restype = i
         L.orc_num_threads_available.restype = i
@@ -139,6 +141,34 @@ class OracleCache:
         if rc != 0:
             raise ValueError("append passes max_seq")
         self.len = s.len
+
+    def rows(self, b: int, h: int):
+        """The stored K and V rows [len, D] of (sequence b, KV head h) in binary64."""
+        L = self.len
+        sk = self.ks if self.dtype == INT8 else self.kd
+        sv = self.vs if self.dtype == INT8 else self.vd
+        return (dequant_rows(self.dtype, self.K[b, h, :L], None if sk is None else sk[b, h, :L]),
+                dequant_rows(self.dtype, self.V[b, h, :L], None if sv is None else sv[b, h, :L]))
+
+    def moments(self, b: int, h: int):
+        """Block means (mK, mV), float16 [ceil(len / blk), D], of (b, h)'s stored rows."""
+        K, V = self.rows(b, h)
+        return block_moments(K, self.blk), block_moments(V, self.blk)
+
+    def attend_tail(self, b: int, h: int, q, scale: float, sel):
+        """One query head over KV head h: the listed blocks exactly, the rest by
+        their moment tail.  The exact logits take the query as the cache type's
+        decode does (int8 codes for the quantized types); the tail takes it raw."""
+        K, V = self.rows(b, h)
+        mK, mV = self.moments(b, h)
+        q = _c(q, np.float32)
+        if self.dtype == F16:
+            q_exact = q.astype(np.float64)
+        else:
+            qc, qs = quantize_row(q)
+            q_exact = qc.astype(np.float64) * float(qs)
+        return attend_tail(q_exact, q.astype(np.float64), K, V, self.len, self.blk, scale, sel,
+                           mK, mV)
 
     def decode(self, q, scale: float, k_sel: int = 0, sink_tokens: int = 0,
                recent_tokens: int = 0, dense: bool = False, n_threads: int = 1):
@@ -349,6 +379,55 @@ def attend_int8_sv(q_code, q_scale, K, V, ks, vs, L, blk, scale, eps, sel=None):
     return out, dropped.value
 
 
+def dequant_rows(dtype, rows, scales=None):
+    """Stored cache rows as binary64 values (every product is exact in binary64):
+    f16 as is; int8 codes times their row's f32 scale; q8_0 codes times their
+    32-channel group's f16 scale; q4_0 4-bit codes less 8 times that scale (the
+    low nibble of byte i is channel 2i, the high nibble channel 2i + 1)."""
+    rows = np.asarray(rows)
+    if dtype == F16:
+        return rows.astype(np.float16).astype(np.float64)
+    if dtype == INT8:
+        return rows.astype(np.float64) * np.asarray(scales, np.float32).astype(np.float64)[..., None]
+    if dtype == Q4_0:
+        r = rows.astype(np.int64)
+        codes = np.empty(rows.shape[:-1] + (rows.shape[-1] * 2,), np.float64)
+        codes[..., 0::2] = (r & 15) - 8
+        codes[..., 1::2] = (r >> 4) - 8
+    else:
+        codes = rows.astype(np.float64)
+    d = np.asarray(scales, np.float16).astype(np.float64)
+    return codes * np.repeat(d, QGROUP, axis=-1)
+
+
+def block_moments(X, blk):
+    """Float16 means of the blocks of rows X [L, D] (binary64): [ceil(L / blk), D]."""
+    X = _c(X, np.float64)
+    L, D = X.shape
+    nb = (L + blk - 1) // blk
+    mean = np.zeros((max(nb, 1), D), np.uint16)
+    lib().orc_block_moments(D, L, blk, _ptr(X), _ptr(mean))
+    return mean[:nb].view(np.float16)
+
+
+def attend_tail(q_exact, q_tail, K, V, L, blk, scale, sel, mK, mV):
+    """Exact attention over the listed blocks plus the moment tail of every other
+    block of [0, L): out [D] binary64.  K, V: [L, D] binary64 rows; mK, mV: the
+    float16 block means."""
+    q_exact = _c(q_exact, np.float64)
+    q_tail = _c(q_tail, np.float64)
+    K = _c(K, np.float64)
+    V = _c(V, np.float64)
+    mK = _c(mK, np.float16)
+    mV = _c(mV, np.float16)
+    D = q_exact.size
+    s, n = _sel_args(np.zeros(0, np.int32) if sel is None else sel)
+    out = np.zeros(D, np.float64)
+    lib().orc_attend_tail(D, L, blk, _ptr(q_exact), _ptr(q_tail), float(scale), _ptr(K),
+                          _ptr(V), _ptr(s), max(n, 0), _ptr(mK), _ptr(mV), _ptr(out))
+    return out
+
+
 def threads_available() -> int:
     return lib().orc_num_threads_available()
 
@@ -357,5 +436,5 @@ __all__ = ["F16", "INT8", "OracleCache", "half_to_double", "quantize_row", "bloc
            "forced_range", "select", "attend_f16", "qk_int8", "attend_int8", "attend_dequant",
            "sparse_v_keep", "attend_f16_sv", "attend_int8_sv", "Q8_0", "QGROUP",
            "double_to_half", "quantize_group32", "attend_q8_0", "Q4_0", "quantize_q4_0",
-           "attend_q4_0",
+           "attend_q4_0", "dequant_rows", "block_moments", "attend_tail",
            "threads_available", "lib"]

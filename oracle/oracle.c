@@ -16,7 +16,8 @@
  *  [CPUATT] "cpu-attn" (Hugging Face kernels card), sections "Method",
  *           "Usage", "Correctness", "Requirements and limits".
  *  [SCSA]   "SCSA: Self-Calibrating Subquadratic Attention", section
- *           "2. Mechanism" (sink / recent suffix always attended exactly).
+ *           "2. Mechanism" (sink / recent suffix always attended exactly;
+ *           the moment tail of the groups not read exactly).
  *  The sparse-V (eps mode) functions follow [QUEST] "Adaptive tau (the eps
  *  mode)" and "Compose" item 3.
  *
@@ -41,6 +42,10 @@
  *  R9  q4_0 (named, not defined, by the pages): per 32-channel group the
  *      f16 scale fl16(fl32(m/-8)) of the largest-magnitude value m, codes
  *      clamp(round-half-even(fl32(x/d)) + 8, 0, 15), two per byte.
+ *  R10 moment tail on Quest blocks: every block of [0, L) that the
+ *      selection leaves out contributes m_j exp(scale q . c_K) at c_V, with
+ *      c_K, c_V the means of the block's stored (dequantized) keys and
+ *      values rounded to f16 and q the unquantized f32 query.
  *
  * Every floating-point step runs in IEEE binary64 unless a step of the
  * method fixes f32 (the quantizer's scale and quotient, R1).  Build with
@@ -782,6 +787,94 @@ void orc_attend_dequant(int D, int L, int blk, const float *q, const int8_t *q_c
         for (int d = 0; d < D; ++d) out[d] /= Z;
     free(lg);
     free(tok);
+}
+
+/* ------------------------------------------------------------------ */
+/* Moment tail  [SCSA "2. Mechanism", per-query steps "Moment tail" and */
+/* "Output"; applied to Quest blocks as reading R10]: a group of keys   */
+/* that is not read exactly still contributes, through its member count */
+/* m, key centroid c_K and value mean c_V, the term m * exp(a) at c_V   */
+/* inside the shared softmax normalizer, a = scale * q . c_K.           */
+/* ------------------------------------------------------------------ */
+
+/* The per-block means of rows X [L][D] (binary64; the cache's stored    */
+/* rows, dequantized), each rounded once to binary16: block j holds the  */
+/* m_j = min(blk, L - j * blk) rows j * blk .. j * blk + m_j - 1.        */
+/* mean: [ceil(L / blk)][D] binary16 bit patterns.                       */
+void orc_block_moments(int D, int L, int blk, const double *X, uint16_t *mean)
+{
+    int nb = (L + blk - 1) / blk;
+    for (int j = 0; j < nb; ++j) {
+        int lo = j * blk;
+        int m = L - lo < blk ? L - lo : blk;
+        for (int d = 0; d < D; ++d) {
+            double sum = 0.0;
+            for (int t = lo; t < lo + m; ++t) sum += X[(size_t)t * D + d];
+            mean[(size_t)j * D + d] = orc_double_to_half(sum / (double)m);
+        }
+    }
+}
+
+/* Attention of one query head over the tokens of the listed blocks,     */
+/* exactly, plus the moment tail of every other block of [0, L).         */
+/* q_exact: the query the exact logits use (the f32 query, or for the    */
+/* quantized cache types its dequantized int8 codes); q_tail: the f32    */
+/* query (R10).  K, V: [L][D] the cache's rows in binary64 (dequantized). */
+/* mK, mV: [ceil(L / blk)][D] binary16 block means (orc_block_moments).  */
+/* Terms:                                                                */
+/*   listed token t:   x_t = scale * q_exact . K_t,           value V_t  */
+/*   unlisted block j: x_j = scale * q_tail . mK_j + ln m_j,  value mV_j */
+/*   out = sum_i exp(x_i - M) value_i / sum_i exp(x_i - M),  M = max x.  */
+/* ------------------------------------------------------------------ */
+void orc_attend_tail(int D, int L, int blk, const double *q_exact, const double *q_tail,
+                     double scale, const double *K, const double *V, const int *sel,
+                     int n_sel, const uint16_t *mK, const uint16_t *mV, double *out)
+{
+    int nb = (L + blk - 1) / blk;
+    char *listed = (char *)calloc((size_t)(nb > 0 ? nb : 1), 1);
+    for (int i = 0; i < n_sel; ++i)
+        if (sel[i] >= 0 && sel[i] < nb) listed[sel[i]] = 1;
+    long n_terms = (long)L + nb;
+    double *x = (double *)malloc(sizeof(double) * (size_t)(n_terms > 0 ? n_terms : 1));
+    const double **val = (const double **)malloc(sizeof(double *) * (size_t)(n_terms > 0 ? n_terms : 1));
+    double *tail_val = (double *)malloc(sizeof(double) * (size_t)(nb > 0 ? nb : 1) * D);
+    long n = 0;
+    for (int j = 0; j < nb; ++j) {
+        int lo = j * blk;
+        int mj = L - lo < blk ? L - lo : blk;
+        if (listed[j]) {
+            for (int t = lo; t < lo + mj; ++t) {
+                double s = 0.0;
+                for (int d = 0; d < D; ++d) s += q_exact[d] * K[(size_t)t * D + d];
+                x[n] = scale * s;
+                val[n++] = V + (size_t)t * D;
+            }
+        } else {
+            double s = 0.0;
+            for (int d = 0; d < D; ++d)
+                s += q_tail[d] * orc_half_to_double(mK[(size_t)j * D + d]);
+            for (int d = 0; d < D; ++d)
+                tail_val[(size_t)j * D + d] = orc_half_to_double(mV[(size_t)j * D + d]);
+            x[n] = scale * s + log((double)mj);
+            val[n++] = tail_val + (size_t)j * D;
+        }
+    }
+    double M = -INFINITY;
+    for (long i = 0; i < n; ++i)
+        if (x[i] > M) M = x[i];
+    double Z = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (long i = 0; i < n; ++i) {
+        double w = exp(x[i] - M);
+        Z += w;
+        for (int d = 0; d < D; ++d) out[d] += w * val[i][d];
+    }
+    if (n > 0)
+        for (int d = 0; d < D; ++d) out[d] /= Z;
+    free(tail_val);
+    free(val);
+    free(x);
+    free(listed);
 }
 
 /* ------------------------------------------------------------------ */

@@ -76,6 +76,20 @@ MUTANTS = {
     "q4_no_offset_in_dot": ("dot += (int64_t)qc[c] * (int64_t)(q4_code(k, c) - 8);",
                             "dot += (int64_t)qc[c] * (int64_t)q4_code(k, c);"),
     "q4_round_half_up": ("double r4 = nearbyint((double)qt) + 8.0;", "double r4 = floor((double)qt + 0.5) + 8.0;"),
+    # moment tail (R10)
+    "tail_without_count": ("x[n] = scale * s + log((double)mj);", "x[n] = scale * s;"),
+    "tail_full_block_count": ("x[n] = scale * s + log((double)mj);",
+                              "x[n] = scale * s + log((double)blk);"),
+    "tail_without_scale": ("x[n] = scale * s + log((double)mj);", "x[n] = s + log((double)mj);"),
+    "tail_ignores_listing": ("if (sel[i] >= 0 && sel[i] < nb) listed[sel[i]] = 1;",
+                             "if (sel[i] >= 0 && sel[i] < nb) listed[sel[i]] = 0;"),
+    "tail_value_is_key_mean": (
+        "tail_val[(size_t)j * D + d] = orc_half_to_double(mV[(size_t)j * D + d]);",
+        "tail_val[(size_t)j * D + d] = orc_half_to_double(mK[(size_t)j * D + d]);"),
+    "moment_divides_by_blk": ("mean[(size_t)j * D + d] = orc_double_to_half(sum / (double)m);",
+                              "mean[(size_t)j * D + d] = orc_double_to_half(sum / (double)blk);"),
+    "moment_skips_first_row": ("for (int t = lo; t < lo + m; ++t) sum += X[(size_t)t * D + d];",
+                               "for (int t = lo + 1; t < lo + m; ++t) sum += X[(size_t)t * D + d];"),
 }
 
 
@@ -95,7 +109,8 @@ def _run_mutant(name, old, new, tmp):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_sparse_v.py"),
                         os.path.join(ROOT, "tests", "test_oracle_q8_0.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_q4_0.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_q4_0.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_tail.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return name, r.returncode
 
