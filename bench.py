@@ -420,6 +420,74 @@ def run_sparse_v_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_tail_sweep(args):
+    """Decode attention over the step's selection, without and with the moment
+    tail of the blocks it leaves out, at the workload's K_SEL and a quarter of
+    it: device time (write + read L2 flush between calls) and the relative L2
+    error of each output against dense attention; one JSON line per point."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    steps, warm = max(1, args.steps), max(3, args.warmup)
+
+    def timed_us(fn):
+        ms = []
+        for i in range(warm + steps):
+            flush.fill_(i & 0xFF)
+            drain.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= warm:
+                ms.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ms) * 1e3
+
+    def rel_err(x, ref):
+        e = ((x - ref).norm(dim=-1) / ref.norm(dim=-1)).flatten()
+        return float(e.median()), float(e.max())
+
+    for name in ("ctx1m_int8", "qwen3_4b_gqa_32k_f16"):
+        w = synth.WORKLOADS[name]
+        q, k, v, _ = synth.make_workload(w, device=dev)
+        cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev, moments=True)
+        kvd.kv_append(cache, k, v)
+        del k, v
+        ws = kvd.make_workspace(cache, w.H)
+        nbmax = cache.max_seq // 64
+        dense = torch.empty(w.B, w.H, w.D, device=dev)
+        kvd.decode_attn_dense(cache, q, w.scale, dense, ws)
+        for k_sel in (w.k_sel, w.k_sel // 4):
+            sel_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev)
+            sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev)
+            kvd.select_blocks(cache, q, k_sel, w.sink_tokens, w.recent_tokens, sel_idx, sel_cnt,
+                              ws)
+            max_sel = kvd.selected_count(w.L, k_sel, w.sink_tokens, w.recent_tokens)
+            plain = torch.empty_like(dense)
+            tail = torch.empty_like(dense)
+            us_plain = timed_us(lambda: kvd.decode_attn(cache, q, w.scale, sel_idx, sel_cnt,
+                                                        max_sel, plain, ws))
+            us_tail = timed_us(lambda: kvd.decode_attn_tail(cache, q, w.scale, sel_idx, sel_cnt,
+                                                            max_sel, tail, ws))
+            assert cache.device_status() == 0, "device-side fault reported"
+            nb = (w.L + 63) // 64
+            print(json.dumps({
+                "sweep": "tail", "workload": w.name, "context": w.L,
+                "kv_dtype": dtype_name(w.dtype), "k_sel": k_sel,
+                "coverage": max_sel / nb, "decode_us": us_plain, "decode_tail_us": us_tail,
+                "tail_moment_bytes": w.B * w.Hkv * nb * 512,
+                "err_vs_dense_median": rel_err(plain, dense)[0],
+                "err_vs_dense_max": rel_err(plain, dense)[1],
+                "tail_err_vs_dense_median": rel_err(tail, dense)[0],
+                "tail_err_vs_dense_max": rel_err(tail, dense)[1], "steps": steps,
+                "l2": "write + read flush between calls"}), flush=True)
+        del cache, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,14 +499,17 @@ def main():
     ap.add_argument("--context", type=int, default=None,
                     help="run the workload's recipe at this context instead (a multiple "
                          "of 64; a smaller case for profiling)")
-    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v"], default=None,
+    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v", "tail"],
+                    default=None,
                     help="instead of the bench line: sparse vs dense decode steps over the "
                          "context sweep (16K..1M, 25%% coverage) or the 128K x 8 coverage "
-                         "sweep, or decode attention with sparse-V at several eps; one JSON "
-                         "line per point")
+                         "sweep, decode attention with sparse-V at several eps, or decode "
+                         "attention with the moment tail; one JSON line per point")
     args = ap.parse_args()
     if args.sweep == "sparse_v":
         return run_sparse_v_sweep(args)
+    if args.sweep == "tail":
+        return run_tail_sweep(args)
     if args.sweep:
         return run_sweep(args)
     w = synth.WORKLOADS[args.workload]

@@ -11,6 +11,8 @@
  *           (bug-747)".
  *  [CPUATT] "cpu-attn" (Hugging Face kernels card): "Usage", "Method",
  *           "Correctness", "Requirements and limits".
+ *  [SCSA]   "SCSA: Self-Calibrating Subquadratic Attention": "2. Mechanism"
+ *           (the moment tail of the key groups not read exactly).
  *
  * Conventions for every entry point
  *  - All device memory is allocated and owned by the caller.  The library
@@ -38,7 +40,7 @@
 extern "C" {
 #endif
 
-#define KVD_ABI_VERSION 2
+#define KVD_ABI_VERSION 3
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -94,6 +96,14 @@ typedef enum { KVD_F16 = 0, KVD_INT8 = 1, KVD_Q8_0 = 2, KVD_Q4_0 = 3 } kvd_kv_dt
  * call's arithmetic (they may hold anything).
  * `dev_status` may be NULL; if set it is one device int32 that kernels set
  * to a kvd_status code when a bounded device wait runs out.
+ * `moments` may be NULL; if set, [batch, n_kv_heads, max_seq / block, 2,
+ * head_dim] f16: per block the mean of its stored keys, then of its stored
+ * values (dequantized: code * scale for int8, code * d for q8_0, (code - 8)
+ * * d for q4_0), over the block's tokens below len, each channel's f32 sum
+ * in token order divided by the count and rounded to f16.  kvd_kv_append
+ * and kvd_decode_step keep them for every block they write; they feed the
+ * moment tail of kvd_decode_attn_tail.  Rewinding len inside a block and
+ * appending again recomputes that block's means from its rows.
  */
 typedef struct kvd_cache {
     int32_t dtype;        /* kvd_kv_dtype */
@@ -110,6 +120,7 @@ typedef struct kvd_cache {
     void *v_scale;
     void *kbounds;
     int32_t *dev_status;
+    void *moments;        /* optional block means (moment tail), see above */
 } kvd_cache;
 
 /* ---------------------------------------------------------------------- */
@@ -119,7 +130,9 @@ typedef struct kvd_cache {
 /* Writes rows len .. len+n_new-1 (f16 verbatim, or int8 codes + scales)   */
 /* and the bounds of every block those rows touch: a block that already   */
 /* held tokens is min/max-merged, a block that starts in the new range is  */
-/* overwritten.  On KVD_OK, cache->len += n_new (host side; the kernels    */
+/* overwritten.  With cache->moments set, the key and value means of every */
+/* touched block are recomputed over its rows below the new len.          */
+/* On KVD_OK, cache->len += n_new (host side; the kernels                  */
 /* are only enqueued).  n_new == 0 is a no-op.                             */
 /* Errors: INVALID, UNSUPPORTED, CAPACITY (len + n_new > max_seq), CUDA.   */
 /* ---------------------------------------------------------------------- */
@@ -221,6 +234,34 @@ KVD_API kvd_status kvd_decode_attn_sv(const kvd_cache *cache, const float *q, in
                               const int32_t *sel_cnt, int32_t max_sel, float sparse_v_eps,
                               float *out, void *workspace, size_t workspace_bytes,
                               void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Decode attention over the selected blocks plus the moment tail of every */
+/* other block  [SCSA "2. Mechanism": a group that is not read exactly     */
+/* contributes its count m times exp(a), a = softmax_scale * q . c_K, at   */
+/* its value mean c_V, inside the shared normalizer; here the groups are   */
+/* the Quest blocks the selection leaves out].                              */
+/*   As kvd_decode_attn (same arguments), plus, for each query head h and   */
+/*   each block j < NB = ceil(len / block) not listed in its row:           */
+/*     term weight m_j * exp(softmax_scale * q_h . c_K(j)), value c_V(j)    */
+/*   with m_j = min(block, len - j * block), c_K/c_V the f16 block means of */
+/*   cache->moments, and q_h the f32 query (unquantized on every cache      */
+/*   type).  out_h = (sum over listed tokens w_t v_t + sum over the other   */
+/*   blocks of their terms) / (the same sum of weights).                    */
+/*   Every listed row must be strictly ascending (as kvd_select_blocks      */
+/*   writes it); otherwise a block may be counted both ways or not at all  */
+/*   (wrong output, no fault).  Every row listing all NB blocks gives        */
+/*   kvd_decode_attn's output bit for bit.                                   */
+/*   Each launch reads all NB moment rows (512 bytes per block and KV head) */
+/*   besides the listed blocks.                                              */
+/* Errors: as kvd_decode_attn; INVALID also when cache->moments is NULL or  */
+/* misaligned, or sel_idx/sel_cnt is NULL.                                  */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_decode_attn_tail(const kvd_cache *cache, const float *q,
+                                int32_t n_heads, float softmax_scale,
+                                const int32_t *sel_idx, const int32_t *sel_cnt,
+                                int32_t max_sel, float *out, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* kvd_decode_attn without a workspace: the paper has no counterpart; this  */

@@ -37,7 +37,8 @@ STATUS = {0: "KVD_OK", 1: "KVD_ERR_INVALID", 2: "KVD_ERR_UNSUPPORTED", 3: "KVD_E
 EXPORTS = ("kvd_kv_append", "kvd_select_blocks", "kvd_decode_attn", "kvd_decode_attn_dense",
            "kvd_decode_step", "kvd_decode_step_host", "kvd_workspace_bytes",
            "kvd_selected_count", "kvd_status_string", "kvd_abi_version", "kvd_debug_qk_int8",
-           "kvd_debug_scores", "kvd_decode_attn_static", "kvd_decode_attn_sv")
+           "kvd_debug_scores", "kvd_decode_attn_static", "kvd_decode_attn_sv",
+           "kvd_decode_attn_tail")
 
 
 class KvdError(RuntimeError):
@@ -52,7 +53,8 @@ class CacheStruct(C.Structure):
                 ("head_dim", C.c_int32), ("max_seq", C.c_int32), ("block", C.c_int32),
                 ("len", C.c_int32), ("reserved", C.c_int32),
                 ("k", C.c_void_p), ("v", C.c_void_p), ("k_scale", C.c_void_p),
-                ("v_scale", C.c_void_p), ("kbounds", C.c_void_p), ("dev_status", C.c_void_p)]
+                ("v_scale", C.c_void_p), ("kbounds", C.c_void_p), ("dev_status", C.c_void_p),
+                ("moments", C.c_void_p)]
 
 
 _lib = None
@@ -75,6 +77,7 @@ def lib():
         L.kvd_decode_attn_static.argtypes = [cp, p, i32, C.c_float, p, p, i32, p, p]
         L.kvd_decode_attn_sv.argtypes = [cp, p, i32, C.c_float, p, p, i32, C.c_float, p, p, sz,
                                          p]
+        L.kvd_decode_attn_tail.argtypes = [cp, p, i32, C.c_float, p, p, i32, p, p, sz, p]
         L.kvd_decode_step.argtypes = [cp, p, p, p, i32, C.c_float, i32, i32, i32, p, p, p, p,
                                       sz, p]
         L.kvd_decode_step_host.argtypes = [cp, p, p, p, i32, C.c_float, i32, i32, i32, p, p, p,
@@ -120,11 +123,13 @@ class KVCache:
               [B, Hkv, max_seq, 4]    float16 group scales (q8_0, q4_0); same for v_scale
     kbounds   [B, Hkv, max_seq // 64, 128, 2] float16: (kmin, kmax) per channel
     status    [1] int32 device word for device-side faults
+    moments   [B, Hkv, max_seq // 64, 2, 128] float16 block means of K then V
+              (only with moments=True: the moment tail of decode_attn_tail)
     """
 
     def __init__(self, dtype: int, batch: int, n_kv_heads: int, max_seq: int,
                  head_dim: int = HEAD_DIM, block: int = BLOCK, device="cuda",
-                 tensors: Optional[dict] = None):
+                 tensors: Optional[dict] = None, moments: bool = False):
         self.dtype, self.batch, self.n_kv_heads = dtype, batch, n_kv_heads
         self.head_dim, self.max_seq, self.block = head_dim, max_seq, block
         dev = torch.device(device)
@@ -153,10 +158,14 @@ class KVCache:
                                                 dtype=torch.float16, device=dev)
                 self.t["v_scale"] = torch.empty(batch, n_kv_heads, max_seq, ng,
                                                 dtype=torch.float16, device=dev)
+            if moments:
+                self.t["moments"] = torch.empty(batch, n_kv_heads, nb, 2, head_dim,
+                                                dtype=torch.float16, device=dev)
         self.s = CacheStruct(dtype, batch, n_kv_heads, head_dim, max_seq, block, 0, 0,
                              _ptr(self.t["k"]), _ptr(self.t["v"]),
                              _ptr(self.t.get("k_scale")), _ptr(self.t.get("v_scale")),
-                             _ptr(self.t["kbounds"]), _ptr(self.t.get("status")))
+                             _ptr(self.t["kbounds"]), _ptr(self.t.get("status")),
+                             _ptr(self.t.get("moments")))
 
     @property
     def kmin(self) -> torch.Tensor:
@@ -253,6 +262,16 @@ def decode_attn_sv(cache: KVCache, q: torch.Tensor, softmax_scale: float, sel_id
         workspace.numel(), _stream(q, stream)))
 
 
+def decode_attn_tail(cache: KVCache, q: torch.Tensor, softmax_scale: float, sel_idx, sel_cnt,
+                     max_sel: int, out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """decode_attn plus the moment tail of every block the lists leave out
+    (needs a cache made with moments=True)."""
+    _check("kvd_decode_attn_tail", lib().kvd_decode_attn_tail(
+        cache.ref(), _ptr(q), int(q.shape[1]), float(softmax_scale), _ptr(sel_idx),
+        _ptr(sel_cnt), int(max_sel), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(q, stream)))
+
+
 def decode_attn_dense(cache: KVCache, q: torch.Tensor, softmax_scale: float, out: torch.Tensor,
                       workspace: torch.Tensor, stream=None):
     _check("kvd_decode_attn_dense", lib().kvd_decode_attn_dense(
@@ -296,5 +315,5 @@ def debug_scores(cache: KVCache, q: torch.Tensor, ub: torch.Tensor, stream=None)
 __all__ = ["F16", "INT8", "Q8_0", "Q4_0", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
            "workspace_bytes", "make_workspace", "selected_count", "status_string", "kv_append",
            "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
-           "decode_attn_sv", "decode_step",
+           "decode_attn_sv", "decode_attn_tail", "decode_step",
            "decode_step_host", "debug_qk_int8", "debug_scores", "synth", "EXPORTS"]

@@ -57,6 +57,7 @@ kvd_status check_cache(const kvd_cache *c) {
             return KVD_ERR_INVALID;
     }
     if (c->dev_status && !aligned(c->dev_status, 4)) return KVD_ERR_INVALID;
+    if (c->moments && !aligned(c->moments, 16)) return KVD_ERR_INVALID;
     if (static_cast<long long>(c->batch) * c->n_kv_heads * 16 > 65535) return KVD_ERR_UNSUPPORTED;
     return KVD_OK;
 }
@@ -190,6 +191,24 @@ kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float sc
                                      sv_eps));
 }
 
+// The listed blocks plus the moment tail of the others.  The split grid is
+// planned for the larger of the two streams: the listed blocks, or the
+// moment rows counted as one block per 32 rows (about the same bytes).
+kvd_status decode_tail_impl(const kvd_cache *c, const float *q, int n_heads, float scale,
+                            const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel,
+                            float *out, void *ws, const WsLayout &w, cudaStream_t st) {
+    const Geom g = make_geom(c, n_heads, c->len);
+    int max_blocks = max_sel < g.NB ? max_sel : g.NB;
+    if (max_blocks < 1) max_blocks = 1;
+    const int tail_work = (g.NB + 31) / 32;
+    DecodePlan p = plan_decode(g, max_blocks > tail_work ? max_blocks : tail_work,
+                               device_sm_count());
+    p.blocks = max_blocks;
+    return cuda_status(launch_decode_tail(*c, g, p, q, scale, sel_idx, sel_cnt, out,
+                                          ws_at<float>(ws, w.partials),
+                                          ws_at<uint32_t>(ws, w.counters), st, true));
+}
+
 kvd_status check_select_args(const kvd_cache *c, int n_heads, int k_sel, int sink, int recent) {
     kvd_status s = check_cache(c);
     if (s != KVD_OK) return s;
@@ -304,6 +323,23 @@ kvd_status kvd_decode_attn_sv(const kvd_cache *cache, const float *q, int32_t n_
     return decode_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_idx ? sel_cnt : nullptr,
                        sel_idx ? max_sel : 0, out, workspace, w,
                        static_cast<cudaStream_t>(stream), false, sparse_v_eps);
+}
+
+kvd_status kvd_decode_attn_tail(const kvd_cache *cache, const float *q, int32_t n_heads,
+                                float softmax_scale, const int32_t *sel_idx,
+                                const int32_t *sel_cnt, int32_t max_sel, float *out,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (cache->len < 1 || max_sel < 0 || !cache->moments) return KVD_ERR_INVALID;
+    if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
+    if (!sel_idx || !aligned(sel_idx, 4) || !sel_cnt || !aligned(sel_cnt, 4))
+        return KVD_ERR_INVALID;
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    return decode_tail_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_cnt, max_sel, out,
+                            workspace, w, static_cast<cudaStream_t>(stream));
 }
 
 kvd_status kvd_decode_attn_dense(const kvd_cache *cache, const float *q, int32_t n_heads,

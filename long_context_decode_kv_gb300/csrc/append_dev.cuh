@@ -8,7 +8,7 @@
 // a block that starts in the new range.  Bounds always come from the f16 keys
 // before quantization.  "cpu-attn", Method: K and V are quantized per token
 // per head (absmax int8) at append time; the q8_0 type quantizes each group
-// of 32 channels with its own f16 scale instead.
+// of 32 channels with its own f16 scale instead, and q4_0 to 4-bit codes.
 //
 // Lane l owns channels 4l..4l+3, so every row is read as one coalesced
 // 256-byte line.
@@ -25,9 +25,89 @@ __device__ __forceinline__ void load_half4(const __half *p, float (&x)[4]) {
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
 }
 
+// Channels 4 lane .. 4 lane + 3 of stored row r of K (is_v false) or V, as
+// the decode reads them: f16 as is, int8 code * row scale, q8_0 code * group
+// scale, q4_0 (code - 8) * group scale, each product one f32 rounding.
+template <int DT>
+__device__ __forceinline__ void load_row4(const kvd_cache &c, bool is_v, size_t r, int lane,
+                                          float (&x)[4]) {
+    const void *base = is_v ? c.v : c.k;
+    const void *scl = is_v ? c.v_scale : c.k_scale;
+    if constexpr (DT == KVD_F16) {
+        load_half4(static_cast<const __half *>(base) + r * kHeadDim + 4 * lane, x);
+    } else if constexpr (DT == KVD_Q4_0) {
+        const uint32_t b = *reinterpret_cast<const uint16_t *>(
+            static_cast<const uint8_t *>(base) + r * (kHeadDim / 2) + 2 * lane);
+        const float d = __half2float(static_cast<const __half *>(scl)[r * (kHeadDim / 32) +
+                                                                      (lane >> 3)]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            x[j] = static_cast<float>(static_cast<int>((b >> (4 * j)) & 15u) - 8) * d;
+    } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(static_cast<const int8_t *>(base) +
+                                                               r * kHeadDim + 4 * lane);
+        const float s = DT == KVD_INT8
+                            ? static_cast<const float *>(scl)[r]
+                            : __half2float(static_cast<const __half *>(scl)[r * (kHeadDim / 32) +
+                                                                            (lane >> 3)]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            x[j] = static_cast<float>(static_cast<int8_t>(w >> (8 * j))) * s;
+    }
+}
+
+// "SCSA: Self-Calibrating Subquadratic Attention", "2. Mechanism": a group
+// of keys read only through its moments keeps its member count, key centroid
+// and value mean.  Here the group is a cache block: its f16 key and value
+// means over the stored rows [lo, hi) (the rows' f32 sum in token order over
+// the count, rounded once), recomputed from the rows whenever the block
+// grows, so they never depend on how the rows were appended.
+template <int DT>
+__device__ __forceinline__ void block_means_warp(const kvd_cache &c, size_t row0, int blk,
+                                                 long lo, long hi, int lane) {
+    float sk[4] = {0.0f, 0.0f, 0.0f, 0.0f}, sv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    constexpr int kBatch = 8;  // rows whose loads are in flight together
+    for (long t0 = lo; t0 < hi; t0 += kBatch) {
+        float xk[kBatch][4], xv[kBatch][4];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (t0 + u < hi) {
+                load_row4<DT>(c, false, row0 + t0 + u, lane, xk[u]);
+                load_row4<DT>(c, true, row0 + t0 + u, lane, xv[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (t0 + u < hi) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    sk[j] += xk[u][j];
+                    sv[j] += xv[u][j];
+                }
+            }
+        }
+    }
+    const float n = static_cast<float>(hi - lo);
+    uint2 mk, mv;
+    __half *k4 = reinterpret_cast<__half *>(&mk);
+    __half *v4 = reinterpret_cast<__half *>(&mv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        k4[j] = __float2half_rn(__fdiv_rn(sk[j], n));
+        v4[j] = __float2half_rn(__fdiv_rn(sv[j], n));
+    }
+    const size_t nbmax = static_cast<size_t>(c.max_seq / kBlock);
+    __half *rec = static_cast<__half *>(c.moments) +
+                  ((row0 / c.max_seq) * nbmax + blk) * (2 * kHeadDim);
+    *reinterpret_cast<uint2 *>(rec + 4 * lane) = mk;
+    *reinterpret_cast<uint2 *>(rec + kHeadDim + 4 * lane) = mv;
+}
+
 // Tokens [max(lo, len0), min(lo + 64, len0 + n_new)) of cache block blk of
 // (sequence b, KV head h), taken from k_new / v_new [B, n_new, Hkv, 128] f16.
-template <int DT>
+// MEANS: also the block's means when the cache keeps them (callers that
+// never see such a cache leave that code out).
+template <int DT, bool MEANS = true>
 __device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __half *k_new,
                                                   const __half *v_new, int n_new, int len0,
                                                   int blk, int b, int h, int lane) {
@@ -115,6 +195,10 @@ __device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __ha
 #pragma unroll
     for (int j = 0; j < 4; ++j) w2[j] = __floats2half2_rn(mn[j], mx[j]);
     *reinterpret_cast<uint4 *>(bounds) = w;
+    if (MEANS && c.moments) {
+        __syncwarp();  // the group scales written by other lanes are visible
+        block_means_warp<DT>(c, row0, blk, lo, nhi, lane);
+    }
 }
 
 }  // namespace kvd

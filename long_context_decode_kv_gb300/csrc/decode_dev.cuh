@@ -40,6 +40,12 @@ constexpr int kMaxSplits = 256;
 constexpr unsigned kFull = 0xffffffffu;
 // Stage marker that ends a consumer group's loop.
 constexpr int kEndMark = -2;
+// Moment-tail stages carry kTailBase - chunk (chunk >= 0) as their block.
+constexpr int kTailBase = -16;
+// One block's moment row: the f16 key mean, then the f16 value mean.
+constexpr int kMomentBytes = 2 * kHeadDim * 2;
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
 template <int DT>
 struct Tile;
@@ -50,6 +56,7 @@ struct Tile<KVD_INT8> {
     static constexpr int kStageBytes = 2 * kKBytes + 2 * kBlock * 4;  // + both scale rows
     static constexpr int kGroups = 2;   // consumer groups (4 warps each)
     static constexpr int kStages = 6;   // a multiple of kGroups
+    static constexpr int kTailRecs = 32;  // moment rows per tail stage
     static constexpr int kMinCtas = 2;
     static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
@@ -62,6 +69,7 @@ struct Tile<KVD_Q8_0> {
     static constexpr int kStageBytes = 2 * kKBytes + 2 * kScaleBytes;
     static constexpr int kGroups = 2;
     static constexpr int kStages = 6;   // a multiple of kGroups
+    static constexpr int kTailRecs = 32;
     static constexpr int kMinCtas = 2;
     static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
@@ -74,6 +82,7 @@ struct Tile<KVD_Q4_0> {
     static constexpr int kStageBytes = 2 * kKBytes + 2 * kScaleBytes;
     static constexpr int kGroups = 2;
     static constexpr int kStages = 10;  // a multiple of kGroups
+    static constexpr int kTailRecs = 16;  // 8 KiB of a 9 KiB stage
     static constexpr int kMinCtas = 2;
     static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
@@ -85,6 +94,7 @@ struct Tile<KVD_F16> {
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kGroups = 2;
     static constexpr int kStages = 4;   // a multiple of kGroups
+    static constexpr int kTailRecs = 32;
     static constexpr int kMinCtas = 1;
     static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
@@ -93,6 +103,7 @@ struct Tile<KVD_F16> {
 struct DecodeArgs {
     const void *k, *v;
     const void *k_scale, *v_scale;  // f32 per token (int8) or f16 per group (q8_0)
+    const __half *moments;          // block means (moment tail), or null
     const float *q;
     float *out;
     const int32_t *sel_idx, *sel_cnt;
@@ -106,14 +117,17 @@ struct DecodeArgs {
     int early_q;       // q is complete before the upstream kernels finish
 };
 
-template <int DT, int GC>
+template <int DT, int GC, bool TAIL = false>
 struct SmemLayout {
     static constexpr int kStageBytes = Tile<DT>::kStageBytes;
     static constexpr int kStages = Tile<DT>::kStages;
     static constexpr int kStagesOff = 0;
     static constexpr int kRing = kStages * kStageBytes;
+    static_assert(Tile<DT>::kTailRecs * kMomentBytes <= kStageBytes, "tail stage overflows");
+    // merge rows: one state per consumer warp and head (two with the tail)
+    static constexpr int kRows = (TAIL ? 2 : 1) * Tile<DT>::kConsumerWarps;
     // after the loop the ring holds the warp merge, then the split weights
-    static constexpr int kMergeBytes = Tile<DT>::kConsumerWarps * GC * kPartStride * 4;
+    static constexpr int kMergeBytes = kRows * GC * kPartStride * 4;
     // split merge: (m, l) and the accumulators of every thread part
     static constexpr int kWeightBytes = Tile<DT>::kConsumerWarps * 32 * (16 + 8);
     static constexpr int kScratch = kMergeBytes > kWeightBytes ? kMergeBytes : kWeightBytes;
@@ -130,7 +144,9 @@ struct SmemLayout {
     static constexpr int kPwBytes = Tile<DT>::kConsumerWarps * kTokensPerWarp * 4 * 2 * 4;
     static constexpr int kLOff = kPwOff + kPwBytes;  // split merge: L per head
     static constexpr int kFlagOff = kLOff + 16;
-    static constexpr int kTotal = kFlagOff + 16;
+    // moment tail: the listed-block mask of each stage
+    static constexpr int kMaskOff = kFlagOff + 16;
+    static constexpr int kTotal = kMaskOff + (TAIL ? 4 * kStages : 0);
 };
 
 // ----------------------------------------------------------------------------
@@ -804,9 +820,219 @@ __device__ __forceinline__ void consume_f16(const uint8_t *stage, int n_valid,
     }
 }
 
-template <int DT, int GC, bool DENSE, bool SV>
+// ----------------------------------------------------------------------------
+// Moment tail  ("SCSA: Self-Calibrating Subquadratic Attention", "2.
+// Mechanism": a group of keys that is not read exactly contributes its count
+// m times exp(a), a = scale * q . c_K, at its value mean c_V, inside the
+// shared softmax normalizer).  Here the groups are the cache blocks the list
+// leaves out.  Each split streams the moment rows of its share of all blocks
+// through the same ring after its listed blocks; the producer marks which
+// rows are listed (the list must be ascending), and the consumers fold the
+// others into a second online softmax state per warp, merged with the exact
+// states at the end.
+
+// First position p in the ascending list[0, n) with list[p] >= target (n when
+// none), by a 32-way search: one round of loads per factor of 32.
+__device__ __forceinline__ int first_at_least(const int32_t *list, int n, int target, int lane) {
+    int lo = 0, hi = n;
+    while (hi - lo > 32) {
+        const int step = (hi - lo + 31) / 32;
+        const int p = lo + lane * step;
+        const int v = p < hi ? list[p] : 0x7fffffff;
+        const int k = __popc(__ballot_sync(kFull, v < target));
+        if (k == 0) return lo;
+        const int nhi = lo + k * step;
+        lo += (k - 1) * step + 1;
+        hi = nhi < hi ? nhi : hi;
+    }
+    const int p = lo + lane;
+    const int v = p < hi ? list[p] : 0x7fffffff;
+    return lo + __popc(__ballot_sync(kFull, v < target));
+}
+
+// Producer: the moment rows of chunks [c0, c1) of this split (chunk c holds
+// blocks [c R, c R + R)), each stage tagged with its chunk and the mask of
+// its listed blocks.  The list is walked once, 32 entries per load: ent holds
+// entries cur .. cur + 31, of which the first o lanes are used up.
+// i: the stage sequence number, advanced per stage.
+template <int DT>
+__device__ __forceinline__ bool produce_tail(const DecodeArgs &a, int split, int bg, int cnt,
+                                             const int32_t *list, int &i, uint64_t *full,
+                                             uint64_t *empty, int *stage_blk,
+                                             uint32_t *stage_mask, uint8_t *ring,
+                                             volatile int *abort_flag, int lane, uint64_t pol) {
+    using TL = Tile<DT>;
+    constexpr int R = TL::kTailRecs;
+    const int nch = (a.NB + R - 1) / R;
+    const int c0 = static_cast<int>((static_cast<long long>(split) * nch) / a.splits);
+    const int c1 = static_cast<int>((static_cast<long long>(split + 1) * nch) / a.splits);
+    if (c0 >= c1) return true;
+    const __half *mom = a.moments + static_cast<size_t>(bg) * a.nbmax * (2 * kHeadDim);
+    int cur = first_at_least(list, cnt, c0 * R, lane);
+    int ent = cur + lane < cnt ? list[cur + lane] : 0x7fffffff;
+    int o = 0;
+    bool ok = true;
+    for (int c = c0; c < c1; ++c) {
+        const int lo = c * R, hi = lo + R;
+        uint32_t m = 0;
+        for (;;) {
+            const bool live = lane >= o;
+            const bool in = live && ent >= lo && ent < hi;
+            m |= __reduce_or_sync(kFull, in ? 1u << (ent - lo) : 0u);
+            o += __popc(__ballot_sync(kFull, live && ent < hi));
+            if (o < 32) break;
+            cur += 32;  // the batch is used up: the next 32 entries
+            o = 0;
+            ent = cur + lane < cnt ? list[cur + lane] : 0x7fffffff;
+        }
+        const int s = i % TL::kStages;
+        if (lane == 0) {
+            if (i >= TL::kStages)
+                ok = mbar_wait(&empty[s], ((i / TL::kStages) - 1) & 1, abort_flag);
+            if (ok) {
+                const int nrec = min(R, a.NB - lo);
+                stage_blk[s] = kTailBase - c;
+                stage_mask[s] = m;
+                mbar_arrive_expect_tx(&full[s], nrec * kMomentBytes);
+                tma_load_1d(ring + s * TL::kStageBytes,
+                            mom + static_cast<size_t>(lo) * (2 * kHeadDim), nrec * kMomentBytes,
+                            &full[s], pol);
+            } else {
+                *abort_flag = 1;
+                report_status(a.dev_status, KVD_ERR_TIMEOUT);
+            }
+        }
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) break;
+        ++i;
+    }
+    return ok;
+}
+
+// Sum over the 32 lanes of each of v[0..N) (N a power of two <= 32), left
+// scattered: lane l receives the total of index l >> (5 - log2 N).
+template <int N>
+__device__ __forceinline__ float reduce_scatter_n(float (&v)[N], int lane) {
+#pragma unroll
+    for (int len = N, o = 16; len > 1; len >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < len / 2; ++j) {
+            const float keep = up ? v[len / 2 + j] : v[j];
+            const float send = up ? v[j] : v[len / 2 + j];
+            v[j] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int o = 16 >> ilog2(N); o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+// Lanes per (record, head) value of a warp's tail stage.
+template <int DT, int GC>
+constexpr int tail_shift() {
+    return 5 - ilog2(Tile<DT>::kTailRecs / kWarpsPerGroup * GC);
+}
+
+// Consumer: the tail stages of this warp's group, from stage i (already
+// waited for) to the group's end marker.  Warp wg takes records
+// [wg RW, wg RW + RW) of each stage; ts.m and ts.l belong to the lane's head
+// h = (lane >> SH) % GC, ts.acc to channels 4 lane .. 4 lane + 3 of every head.
+template <int DT, int GC>
+__device__ __forceinline__ void tail_loop(const DecodeArgs &a, int b, int h0, int i,
+                                       uint64_t *full, uint64_t *empty, const int *stage_blk,
+                                       const uint32_t *stage_mask, const uint8_t *ring, float *pw,
+                                       int wg, int lane, volatile int *abort_flag,
+                                       WarpState<GC> &ts) {
+    using TL = Tile<DT>;
+    constexpr int R = TL::kTailRecs, RW = R / kWarpsPerGroup, N = RW * GC;
+    constexpr int SH = tail_shift<DT, GC>(), LGC = ilog2(GC);
+    float qf[GC][4];  // the f32 query in base-2 logit units
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        const float4 v = *reinterpret_cast<const float4 *>(
+            a.q + (static_cast<size_t>(b) * a.H + h0 + h) * kHeadDim + 4 * lane);
+        qf[h][0] = v.x * a.scale_log2;
+        qf[h][1] = v.y * a.scale_log2;
+        qf[h][2] = v.z * a.scale_log2;
+        qf[h][3] = v.w * a.scale_log2;
+    }
+    const int idx = lane >> SH, r_own = idx / GC, h_own = idx % GC;
+    for (bool first = true;; i += TL::kGroups, first = false) {
+        const int s = i % TL::kStages;
+        if (!first) {
+            const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
+            if (!__all_sync(kFull, ok)) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    report_status(a.dev_status, KVD_ERR_TIMEOUT);
+                }
+                return;
+            }
+        }
+        const int code = stage_blk[s];
+        if (code == kEndMark) return;
+        const int j0 = (kTailBase - code) * R + wg * RW;  // block of this warp's first record
+        const uint32_t listed = stage_mask[s] >> (wg * RW);
+        const uint8_t *rec = ring + s * TL::kStageBytes + wg * RW * kMomentBytes;
+        uint32_t vm = 0;  // records to fold: present and not listed
+#pragma unroll
+        for (int r = 0; r < RW; ++r)
+            if (j0 + r < a.NB && !((listed >> r) & 1u)) vm |= 1u << r;
+        if (vm) {
+            float d[N];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(rec + r * kMomentBytes + 8 * lane);
+                const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+                const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+#pragma unroll
+                for (int h = 0; h < GC; ++h)
+                    d[r * GC + h] = fmaf(qf[h][3], k23.y,
+                                         fmaf(qf[h][2], k23.x,
+                                              fmaf(qf[h][1], k01.y, qf[h][0] * k01.x)));
+            }
+            float x = reduce_scatter_n<N>(d, lane);
+            const int j = j0 + r_own;
+            const int m = min(kBlock, a.len - j * kBlock);
+            x = ((vm >> r_own) & 1u) ? x + (m == kBlock ? 6.0f : log2f(static_cast<float>(m)))
+                                     : -INFINITY;
+            // over this warp's records of the lane's head (lane bits above LGC + SH)
+            float mx = x;
+#pragma unroll
+            for (int o = 1 << (SH + LGC); o < 32; o <<= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+            const float m_new = fmaxf(ts.m, mx);
+            const float alpha = exp2f(ts.m - m_new);
+            const float p = exp2f(x - m_new);
+            float ps = p;
+#pragma unroll
+            for (int o = 1 << (SH + LGC); o < 32; o <<= 1) ps += __shfl_xor_sync(kFull, ps, o);
+            ts.l = fmaf(ts.l, alpha, ps);
+            ts.m = m_new;
+            if ((lane & ((1 << SH) - 1)) == 0)
+                *reinterpret_cast<float2 *>(pw + r_own * 8 + 2 * h_own) = make_float2(p, p);
+            rescale<GC>(ts, alpha, 1 << SH);
+            __syncwarp();
+            for (uint32_t mm = vm; mm; mm &= mm - 1u) {
+                const int r = __ffs(mm) - 1;
+                const uint2 w = *reinterpret_cast<const uint2 *>(rec + r * kMomentBytes +
+                                                                 2 * kHeadDim + 8 * lane);
+                const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+                const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+                pv_token<GC>(ts, pw + r * 8, v01, v23);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL>
 __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *smem) {
-    using SL = SmemLayout<DT, GC>;
+    static_assert(!TAIL || (!DENSE && !SV), "the moment tail runs on a listed selection alone");
+    using SL = SmemLayout<DT, GC, TAIL>;
     using TL = Tile<DT>;
     static_assert(TL::kStages % TL::kGroups == 0, "stages must split evenly over the groups");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + SL::kFullOff);
@@ -819,6 +1045,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SL::kFlagOff);
     int *last_flag = reinterpret_cast<int *>(smem + SL::kFlagOff + 4);
     int *issued_s = reinterpret_cast<int *>(smem + SL::kFlagOff + 8);
+    uint32_t *stage_mask = reinterpret_cast<uint32_t *>(smem + SL::kMaskOff);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // prob = ((b * Hkv) + g) * subgroups + sub
@@ -851,6 +1078,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     st.l = 0.0f;
 #pragma unroll
     for (int h = 0; h < GC; ++h) st.acc[h][0] = st.acc[h][1] = make_float2(0.0f, 0.0f);
+    WarpState<GC> ts = st;  // the moment tail's state (TAIL only)
     if (warp == TL::kConsumerWarps) {
         // ------------------------------------------------------ producer
         // The split's list positions: its share [pb, pe) of the planned
@@ -928,6 +1156,11 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 ++i;
             }
         }
+        if constexpr (TAIL) {
+            if (ok)
+                ok = produce_tail<DT>(a, split, bg, cnt, list, i, full, empty, stage_blk,
+                                      stage_mask, smem + SL::kStagesOff, abort_flag, lane, pol);
+        }
         const int issued = i;
         // one end marker per consumer group (stages i, i+1, ...)
         for (int j = 0; j < TL::kGroups && ok; ++j, ++i) {
@@ -953,10 +1186,12 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         asm volatile("bar.sync 1, %0;" ::"r"(TL::kConsumerWarps * 32) : "memory");
         float *pw = pw_all + warp * (kTokensPerWarp * 4 * 2);
         const int group = warp / kWarpsPerGroup, wg = warp % kWarpsPerGroup;
+        int i = group;         // stage sequence number of this group
+        bool at_tail = false;  // stage i is the group's first moment-tail stage
         if constexpr (DT == KVD_Q4_0) {
             QRegsQ4<GC> qr;
             load_qregs_q4<GC>(q_s, reinterpret_cast<const int *>(coef + 4), lane & 3, qr);
-            for (int i = group;; i += TL::kGroups) {
+            for (;; i += TL::kGroups) {
                 const int s = i % TL::kStages;
                 const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
                 if (!__all_sync(kFull, ok)) {
@@ -968,6 +1203,10 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 }
                 const int blk = stage_blk[s];
                 if (blk == kEndMark) break;
+                if (TAIL && blk <= kTailBase) {
+                    at_tail = true;
+                    break;
+                }
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
                     consume_q4<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
@@ -979,7 +1218,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         } else if constexpr (DT != KVD_F16) {
             QRegsI8<GC> qr;
             load_qregs_i8<GC>(q_s, lane >> 2, lane & 3, qr);
-            for (int i = group;; i += TL::kGroups) {
+            for (;; i += TL::kGroups) {
                 const int s = i % TL::kStages;
                 const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
                 if (!__all_sync(kFull, ok)) {
@@ -991,6 +1230,10 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 }
                 const int blk = stage_blk[s];
                 if (blk == kEndMark) break;
+                if (TAIL && blk <= kTailBase) {
+                    at_tail = true;
+                    break;
+                }
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
                     if constexpr (DT == KVD_INT8)
@@ -1006,7 +1249,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         } else {
             QRegsF16<GC> qr;
             load_qregs_f16<GC>(q_s, lane & 7, qr);
-            for (int i = group;; i += TL::kGroups) {
+            for (;; i += TL::kGroups) {
                 const int s = i % TL::kStages;
                 const bool ok = mbar_wait(&full[s], (i / TL::kStages) & 1, abort_flag);
                 if (!__all_sync(kFull, ok)) {
@@ -1018,6 +1261,10 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 }
                 const int blk = stage_blk[s];
                 if (blk == kEndMark) break;
+                if (TAIL && blk <= kTailBase) {
+                    at_tail = true;
+                    break;
+                }
                 if (blk >= 0) {
                     const int n_valid = min(kBlock, a.len - blk * kBlock);
                     consume_f16<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
@@ -1026,6 +1273,11 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
+        }
+        if constexpr (TAIL) {
+            if (at_tail)
+                tail_loop<DT, GC>(a, b, h0, i, full, empty, stage_blk, stage_mask,
+                                  smem + SL::kStagesOff, pw, wg, lane, abort_flag, ts);
         }
         // per-warp totals: l summed over the lanes of each head
         if constexpr (DT != KVD_F16) {
@@ -1052,6 +1304,19 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
             *reinterpret_cast<float4 *>(row + kAccOff + 4 * lane) =
                 make_float4(st.acc[h][0].x, st.acc[h][0].y, st.acc[h][1].x, st.acc[h][1].y);
         }
+        if constexpr (TAIL) {
+            constexpr int SH = tail_shift<DT, GC>();
+#pragma unroll
+            for (int h = 0; h < GC; ++h) {
+                float *row = mg + ((TL::kConsumerWarps + warp) * GC + h) * kPartStride;
+                if (lane == (h << SH)) {
+                    row[0] = ts.m;
+                    row[1] = ts.l;
+                }
+                *reinterpret_cast<float4 *>(row + kAccOff + 4 * lane) = make_float4(
+                    ts.acc[h][0].x, ts.acc[h][0].y, ts.acc[h][1].x, ts.acc[h][1].y);
+            }
+        }
     }
     __syncthreads();  // (B) merge area written
     if (aborted) {
@@ -1073,11 +1338,11 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         const int h = tid >> 5, d4 = tid & 31;
         float M = kNegBig;
 #pragma unroll
-        for (int w = 0; w < TL::kConsumerWarps; ++w) M = fmaxf(M, mg[(w * GC + h) * kPartStride]);
+        for (int w = 0; w < SL::kRows; ++w) M = fmaxf(M, mg[(w * GC + h) * kPartStride]);
         float L = 0.0f;
         float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-        for (int w = 0; w < TL::kConsumerWarps; ++w) {
+        for (int w = 0; w < SL::kRows; ++w) {
             const float *row = mg + (w * GC + h) * kPartStride;
             const float sc = exp2f(row[0] - M);
             L = fmaf(sc, row[1], L);
@@ -1229,34 +1494,34 @@ DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan 
 // their own translation unit, so the plain kernels carry none of that code:
 // after an L2 flush every instruction of a kernel comes from HBM again, and
 // a shorter instruction stream starts sooner.
-template <int DT, int GC, bool DENSE, bool SV>
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL>
 __global__ void __launch_bounds__(Tile<DT>::kThreads, Tile<DT>::kMinCtas)
     decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    decode_body<DT, GC, DENSE, SV>(a, blockIdx.x, blockIdx.y, smem);
+    decode_body<DT, GC, DENSE, SV, TAIL>(a, blockIdx.x, blockIdx.y, smem);
 }
 
-template <int DT, int GC, bool DENSE, bool SV>
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL>
 cudaError_t launch_decode_t(const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
-    using SL = SmemLayout<DT, GC>;
+    using SL = SmemLayout<DT, GC, TAIL>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE, SV>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE, SV, TAIL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SL::kTotal);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_ex(decode_kernel<DT, GC, DENSE, SV>, dim3(a.splits, P_sub),
+    return launch_ex(decode_kernel<DT, GC, DENSE, SV, TAIL>, dim3(a.splits, P_sub),
                      dim3(Tile<DT>::kThreads), SL::kTotal, st, pdl, a);
 }
 
-template <int DT, bool DENSE, bool SV>
+template <int DT, bool DENSE, bool SV, bool TAIL>
 cudaError_t launch_decode_gc(int gc, const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
     switch (gc) {
-        case 1: return launch_decode_t<DT, 1, DENSE, SV>(a, P_sub, st, pdl);
-        case 2: return launch_decode_t<DT, 2, DENSE, SV>(a, P_sub, st, pdl);
-        default: return launch_decode_t<DT, 4, DENSE, SV>(a, P_sub, st, pdl);
+        case 1: return launch_decode_t<DT, 1, DENSE, SV, TAIL>(a, P_sub, st, pdl);
+        case 2: return launch_decode_t<DT, 2, DENSE, SV, TAIL>(a, P_sub, st, pdl);
+        default: return launch_decode_t<DT, 4, DENSE, SV, TAIL>(a, P_sub, st, pdl);
     }
 }
 
@@ -1272,16 +1537,16 @@ cudaError_t launch_decode_any(const kvd_cache &c, const Geom &g, const DecodePla
     const bool dense = sel_idx == nullptr;
     const int gc = p.heads_per_cta;
     if (g.dtype == KVD_INT8)
-        return dense ? launch_decode_gc<KVD_INT8, true, SV>(gc, a, P_sub, st, pdl)
-                     : launch_decode_gc<KVD_INT8, false, SV>(gc, a, P_sub, st, pdl);
+        return dense ? launch_decode_gc<KVD_INT8, true, SV, false>(gc, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_INT8, false, SV, false>(gc, a, P_sub, st, pdl);
     if (g.dtype == KVD_Q8_0)
-        return dense ? launch_decode_gc<KVD_Q8_0, true, SV>(gc, a, P_sub, st, pdl)
-                     : launch_decode_gc<KVD_Q8_0, false, SV>(gc, a, P_sub, st, pdl);
+        return dense ? launch_decode_gc<KVD_Q8_0, true, SV, false>(gc, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_Q8_0, false, SV, false>(gc, a, P_sub, st, pdl);
     if (g.dtype == KVD_Q4_0)
-        return dense ? launch_decode_gc<KVD_Q4_0, true, SV>(gc, a, P_sub, st, pdl)
-                     : launch_decode_gc<KVD_Q4_0, false, SV>(gc, a, P_sub, st, pdl);
-    return dense ? launch_decode_gc<KVD_F16, true, SV>(gc, a, P_sub, st, pdl)
-                 : launch_decode_gc<KVD_F16, false, SV>(gc, a, P_sub, st, pdl);
+        return dense ? launch_decode_gc<KVD_Q4_0, true, SV, false>(gc, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_Q4_0, false, SV, false>(gc, a, P_sub, st, pdl);
+    return dense ? launch_decode_gc<KVD_F16, true, SV, false>(gc, a, P_sub, st, pdl)
+                 : launch_decode_gc<KVD_F16, false, SV, false>(gc, a, P_sub, st, pdl);
 }
 
 }  // namespace

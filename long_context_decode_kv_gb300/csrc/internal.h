@@ -80,6 +80,12 @@ cudaError_t launch_decode_sv(const kvd_cache &c, const Geom &g, const DecodePlan
                              const int32_t *sel_cnt, float *out, float *partials,
                              uint32_t *counters, cudaStream_t st, bool pdl, bool early_q,
                              float sv_eps);
+// The listed blocks exactly plus the moment tail of every other block
+// (decode_tail.cu); c.moments must be set.
+cudaError_t launch_decode_tail(const kvd_cache &c, const Geom &g, const DecodePlan &p,
+                               const float *q, float scale, const int32_t *sel_idx,
+                               const int32_t *sel_cnt, float *out, float *partials,
+                               uint32_t *counters, cudaStream_t st, bool pdl);
 
 cudaError_t launch_qk_debug(const kvd_cache &c, const Geom &g, const float *q, int32_t *dots,
                             int8_t *q_codes, float *q_scales, cudaStream_t st);

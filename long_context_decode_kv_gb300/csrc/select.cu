@@ -105,7 +105,9 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
     // forced (a recent window) and there is a top-K to find; otherwise it is
     // appended by its own launch first
     const bool topk = keff > 0 && keff < n_cand;
-    const bool fuse = tok && topk && recent_tokens > 0;
+    // the fused append writes rows and bounds only: a cache that keeps block
+    // means appends through the append kernel, which recomputes them
+    const bool fuse = tok && topk && recent_tokens > 0 && c.moments == nullptr;
     if (tok && !fuse) {
         kvd_cache c0 = c;
         c0.len = tok->len0;

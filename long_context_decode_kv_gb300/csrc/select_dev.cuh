@@ -515,19 +515,16 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n,
 // stream (after an L2 flush each kernel's instructions come from HBM again).
 // The decode step's token, appended by one warp of the first tile.
 __device__ __noinline__ void fused_append(const SelArgs &a, int b, int g, int lane) {
-    const int len0 = a.app_cache.len;
-    if (a.app_cache.dtype == KVD_Q8_0)
-        append_block_warp<KVD_Q8_0>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
-                                    lane);
-    else if (a.app_cache.dtype == KVD_Q4_0)
-        append_block_warp<KVD_Q4_0>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
-                                    lane);
-    else if (a.app_cache.dtype == KVD_F16)
-        append_block_warp<KVD_F16>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
-                                   lane);
+    const int len0 = a.app_cache.len, blk = len0 / kBlock;
+    const kvd_cache &c = a.app_cache;
+    if (c.dtype == KVD_Q8_0)
+        append_block_warp<KVD_Q8_0, false>(c, a.app_k, a.app_v, 1, len0, blk, b, g, lane);
+    else if (c.dtype == KVD_Q4_0)
+        append_block_warp<KVD_Q4_0, false>(c, a.app_k, a.app_v, 1, len0, blk, b, g, lane);
+    else if (c.dtype == KVD_F16)
+        append_block_warp<KVD_F16, false>(c, a.app_k, a.app_v, 1, len0, blk, b, g, lane);
     else
-        append_block_warp<KVD_INT8>(a.app_cache, a.app_k, a.app_v, 1, len0, len0 / kBlock, b, g,
-                                    lane);
+        append_block_warp<KVD_INT8, false>(c, a.app_k, a.app_v, 1, len0, blk, b, g, lane);
 }
 
 // The tail of a problem too large for its keys to fit the ring.

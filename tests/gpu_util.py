@@ -32,11 +32,11 @@ def round_up(x, m=64):
     return (x + m - 1) // m * m
 
 
-def make_pair(dtype, k, v, max_seq=None, chunks=None):
+def make_pair(dtype, k, v, max_seq=None, chunks=None, moments=False):
     """GPU cache and oracle cache filled from k, v ([B, L, Hkv, D] f16, on the GPU)."""
     B, L, Hkv, D = k.shape
     max_seq = max_seq or round_up(max(L, 1) + 64)
-    gc = kvd.KVCache(dtype, B, Hkv, max_seq, device=dev())
+    gc = kvd.KVCache(dtype, B, Hkv, max_seq, device=dev(), moments=moments)
     oc = oracle.OracleCache(dtype, B, Hkv, D, max_seq, 64)
     chunks = chunks or [L]
     s = 0

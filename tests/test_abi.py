@@ -135,6 +135,26 @@ def test_decode_validation():
     assert L.kvd_decode_attn_dense(C.byref(s), FAKE, 32, 0.1, FAKE, None, n, None) == WORKSPACE
 
 
+def test_decode_tail_validation():
+    L = kvd.lib()
+    s = _cache(moments=FAKE + 0x500000)
+    n = _ws(s)
+    tail = L.kvd_decode_attn_tail
+    assert tail(C.byref(_cache()), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, FAKE, n,
+                None) == INVALID                                   # no moments kept
+    assert tail(C.byref(_cache(moments=FAKE + 8)), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, FAKE,
+                n, None) == INVALID                                # misaligned moments
+    assert tail(C.byref(s), FAKE, 32, 0.1, None, FAKE, 10, FAKE, FAKE, n, None) == INVALID
+    assert tail(C.byref(s), FAKE, 32, 0.1, FAKE, None, 10, FAKE, FAKE, n, None) == INVALID
+    assert tail(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, -1, FAKE, FAKE, n, None) == INVALID
+    assert tail(C.byref(_cache(moments=FAKE + 0x500000, length=0)), FAKE, 32, 0.1, FAKE, FAKE,
+                10, FAKE, FAKE, n, None) == INVALID
+    assert tail(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, FAKE, n - 256,
+                None) == WORKSPACE
+    # a cache that keeps moments is otherwise an ordinary cache
+    assert _select(_cache(moments=FAKE + 8)) == INVALID
+
+
 def test_append_validation():
     L = kvd.lib()
     s = _cache(length=4090)
