@@ -173,3 +173,25 @@ def test_tail_moves_toward_dense(k_sel):
     e_sparse = ((sparse - dense).norm(dim=-1) / dense.norm(dim=-1)).median().item()
     e_tail = ((tail - dense).norm(dim=-1) / dense.norm(dim=-1)).median().item()
     assert e_tail < e_sparse, (e_tail, e_sparse)
+
+
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8])
+@pytest.mark.parametrize("k_sel", [3, -1])
+def test_decode_steps_keep_block_means(dtype, k_sel):
+    # a decode step appends through the append kernel when the cache keeps
+    # block means (sparse and dense arms), so the means stay current
+    B, Hkv, G, L = 1, 2, 4, 64 * 6 + 60
+    k = seeded((B, L, Hkv, 128), 31)
+    v = seeded((B, L, Hkv, 128), 32)
+    gc, oc = make_pair(dtype, k, v, moments=True)
+    ws = kvd.make_workspace(gc, Hkv * G)
+    out = torch.empty((B, Hkv * G, 128), device=dev())
+    for step in range(6):  # crosses into a new block
+        q = seeded((B, Hkv * G, 128), 40 + step, dtype=torch.float32)
+        kn = seeded((B, 1, Hkv, 128), 50 + step)
+        vn = seeded((B, 1, Hkv, 128), 60 + step)
+        kvd.decode_step(gc, q, kn, vn, scale_for(), k_sel, 4, 64, out, ws)
+        oc.append(kn.cpu().numpy(), vn.cpu().numpy())
+    torch.cuda.synchronize()
+    assert gc.len == oc.len
+    _moments_close(gc, oc, f"steps {dtype} {k_sel}")
