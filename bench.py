@@ -187,12 +187,18 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+# The files the decode kernel's translation unit is compiled from.
+DECODE_SOURCES = ("long_context_decode_kv_gb300/csrc/decode.cu",
+                  "long_context_decode_kv_gb300/csrc/decode_dev.cuh",
+                  "long_context_decode_kv_gb300/csrc/common.cuh",
+                  "long_context_decode_kv_gb300/csrc/internal.h",
+                  "include/kvdecode.h")
+
+
 def source_digest():
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "long_context_decode_kv_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 

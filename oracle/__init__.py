@@ -61,6 +61,10 @@ def lib():
         L.orc_attend_f16_sv.argtypes = [i, i, i, p, d, p, p, p, i, d, p, p]
         L.orc_attend_int8_sv.argtypes = [i, i, i, p, C.c_float, d, p, p, p, p, p, i, d, p, p]
         L.orc_block_moments.argtypes = [i, i, i, p, p]
+        L.orc_append_f32.argtypes = [p, p, p, i]
+        L.orc_append_f32.restype = i
+        L.orc_double_to_half_dir.argtypes = [d, i]
+        L.orc_double_to_half_dir.restype = C.c_uint16
         L.orc_attend_tail.argtypes = [i, i, i, p, p, d, p, p, p, i, p, p, p]
         L.orc_decode.argtypes = [p, i, p, d, i, i, i, i, p, p, p, i]
         L.orc_decode.restype = i
@@ -138,6 +142,18 @@ class OracleCache:
         assert k_new.shape == (self.B, n_new, self.Hkv, self.D) == v_new.shape
         s = self._struct()
         rc = lib().orc_append(C.byref(s), _ptr(k_new), _ptr(v_new), n_new)
+        if rc != 0:
+            raise ValueError("append passes max_seq")
+        self.len = s.len
+
+    def append_f32(self, k_new, v_new):
+        """k_new, v_new: [B, n_new, Hkv, D] float32 (reading R11)."""
+        k_new = _c(k_new, np.float32)
+        v_new = _c(v_new, np.float32)
+        n_new = k_new.shape[1]
+        assert k_new.shape == (self.B, n_new, self.Hkv, self.D) == v_new.shape
+        s = self._struct()
+        rc = lib().orc_append_f32(C.byref(s), _ptr(k_new), _ptr(v_new), n_new)
         if rc != 0:
             raise ValueError("append passes max_seq")
         self.len = s.len
@@ -285,6 +301,12 @@ def attend_dequant(q, K, V, ks, vs, L, blk, scale, sel=None, q_code=None, q_scal
 def double_to_half(x) -> np.float16:
     """Nearest binary16 (ties to even), from the oracle's own rounding."""
     return np.array([lib().orc_double_to_half(float(x))], np.uint16).view(np.float16)[0]
+
+
+def double_to_half_dir(x, direction: int) -> np.float16:
+    """The binary16 nearest x toward -inf (direction < 0) or +inf (> 0)."""
+    return np.array([lib().orc_double_to_half_dir(float(x), int(direction))],
+                    np.uint16).view(np.float16)[0]
 
 
 def quantize_group32(x):
@@ -436,5 +458,5 @@ __all__ = ["F16", "INT8", "OracleCache", "half_to_double", "quantize_row", "bloc
            "forced_range", "select", "attend_f16", "qk_int8", "attend_int8", "attend_dequant",
            "sparse_v_keep", "attend_f16_sv", "attend_int8_sv", "Q8_0", "QGROUP",
            "double_to_half", "quantize_group32", "attend_q8_0", "Q4_0", "quantize_q4_0",
-           "attend_q4_0", "dequant_rows", "block_moments", "attend_tail",
+           "attend_q4_0", "dequant_rows", "block_moments", "attend_tail", "double_to_half_dir",
            "threads_available", "lib"]

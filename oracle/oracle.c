@@ -46,6 +46,9 @@
  *      selection leaves out contributes m_j exp(scale q . c_K) at c_V, with
  *      c_K, c_V the means of the block's stored (dequantized) keys and
  *      values rounded to f16 and q the unquantized f32 query.
+ *  R11 f32 append input: the f16 cache stores the nearest f16 of each
+ *      value; the quantized caches quantize the f32 values and round the
+ *      f32 keys' block envelope outward to f16.
  *
  * Every floating-point step runs in IEEE binary64 unless a step of the
  * method fixes f32 (the quantizer's scale and quotient, R1).  Build with
@@ -318,6 +321,107 @@ int orc_append(orc_cache *c, const uint16_t *k_new, const uint16_t *v_new, int n
             }
         }
     free(row);
+    c->len += n_new;
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Binary16 rounding toward -inf (dir < 0) or +inf (dir > 0): the f16   */
+/* nearest below or above x, x itself when it is an f16.  From the      */
+/* nearest f16 (orc_double_to_half) stepped once to its neighbour when  */
+/* it lies on the wrong side of x.                                       */
+/* ------------------------------------------------------------------ */
+uint16_t orc_double_to_half_dir(double x, int dir)
+{
+    uint16_t h = orc_double_to_half(x);
+    double y = orc_half_to_double(h);
+    int toward_pos;
+    if (dir < 0 && y > x) toward_pos = 0;
+    else if (dir > 0 && y < x) toward_pos = 1;
+    else return h;
+    int neg = (h & 0x8000) != 0;
+    if ((h & 0x7fff) == 0)                       /* +-0: the smallest subnormal */
+        return toward_pos ? 0x0001 : 0x8001;
+    if (neg == toward_pos) return (uint16_t)(h - 1);  /* magnitude shrinks */
+    return (uint16_t)(h + 1);                         /* magnitude grows */
+}
+
+/* ------------------------------------------------------------------ */
+/* Append with f32 input  [CPUATT Usage: the cache takes f32 K/V per    */
+/* token; QUEST All-KV-types composition: bounds from the keys before   */
+/* quantization].  Reading R11:                                          */
+/*  - the f16 cache stores each value's nearest f16, so it is exactly   */
+/*    orc_append of those f16 values;                                    */
+/*  - the quantized caches quantize the f32 values themselves, and a    */
+/*    block's bounds are the f32 keys' envelope rounded outward to f16   */
+/*    (kmin toward -inf, kmax toward +inf), merged as usual, so they    */
+/*    still bound every key.                                             */
+/* k_new, v_new: [B, n_new, Hkv, D] f32.  Returns 0, or -1 past max_seq. */
+/* ------------------------------------------------------------------ */
+int orc_append_f32(orc_cache *c, const float *k_new, const float *v_new, int n_new)
+{
+    if (n_new < 0 || (long)c->len + n_new > c->max_seq) return -1;
+    const int D = c->D;
+    const size_t n_all = (size_t)c->B * (size_t)n_new * c->Hkv * D;
+    if (c->dtype == ORC_F16) {
+        uint16_t *kh = (uint16_t *)malloc(sizeof(uint16_t) * (n_all ? n_all : 1));
+        uint16_t *vh = (uint16_t *)malloc(sizeof(uint16_t) * (n_all ? n_all : 1));
+        for (size_t i = 0; i < n_all; ++i) {
+            kh[i] = orc_double_to_half((double)k_new[i]);
+            vh[i] = orc_double_to_half((double)v_new[i]);
+        }
+        int rc = orc_append(c, kh, vh, n_new);
+        free(vh);
+        free(kh);
+        return rc;
+    }
+    const int ng = D / ORC_QGROUP;
+    for (int b = 0; b < c->B; ++b)
+        for (int h = 0; h < c->Hkv; ++h) {
+            for (int i = 0; i < n_new; ++i) {
+                const float *kx = k_new + (((size_t)b * n_new + i) * c->Hkv + h) * D;
+                const float *vx = v_new + (((size_t)b * n_new + i) * c->Hkv + h) * D;
+                size_t r = row_index(c, b, h, (long)c->len + i);
+                if (c->dtype == ORC_Q4_0) {
+                    orc_quantize_q4_0(kx, D, (uint8_t *)c->K + r * (D / 2), c->kd + r * ng);
+                    orc_quantize_q4_0(vx, D, (uint8_t *)c->V + r * (D / 2), c->vd + r * ng);
+                } else if (c->dtype == ORC_Q8_0) {
+                    orc_quantize_group32(kx, D, (int8_t *)c->K + r * D, c->kd + r * ng);
+                    orc_quantize_group32(vx, D, (int8_t *)c->V + r * D, c->vd + r * ng);
+                } else {
+                    orc_quantize_row(kx, D, (int8_t *)c->K + r * D, &c->ks[r]);
+                    orc_quantize_row(vx, D, (int8_t *)c->V + r * D, &c->vs[r]);
+                }
+            }
+            if (n_new == 0) continue;
+            int q0 = c->len / c->blk, q1 = (c->len + n_new - 1) / c->blk;
+            for (int q = q0; q <= q1; ++q) {
+                long first = (long)q * c->blk;
+                long t0 = first > c->len ? first : c->len;
+                long t1 = first + c->blk < (long)c->len + n_new ? first + c->blk
+                                                                 : (long)c->len + n_new;
+                int held = first < c->len;       /* block held tokens already */
+                uint16_t *lo16 = c->kmin + bound_index(c, b, h, q);
+                uint16_t *hi16 = c->kmax + bound_index(c, b, h, q);
+                for (int d = 0; d < D; ++d) {
+                    double xmin = INFINITY, xmax = -INFINITY;
+                    for (long t = t0; t < t1; ++t) {
+                        double x = (double)k_new[(((size_t)b * n_new + (t - c->len)) * c->Hkv
+                                                  + h) * D + d];
+                        if (x < xmin) xmin = x;
+                        if (x > xmax) xmax = x;
+                    }
+                    uint16_t dn = orc_double_to_half_dir(xmin, -1);
+                    uint16_t up = orc_double_to_half_dir(xmax, +1);
+                    if (held) {
+                        if (orc_half_to_double(lo16[d]) < orc_half_to_double(dn)) dn = lo16[d];
+                        if (orc_half_to_double(hi16[d]) > orc_half_to_double(up)) up = hi16[d];
+                    }
+                    lo16[d] = dn;
+                    hi16[d] = up;
+                }
+            }
+        }
     c->len += n_new;
     return 0;
 }

@@ -90,6 +90,14 @@ MUTANTS = {
                               "mean[(size_t)j * D + d] = orc_double_to_half(sum / (double)blk);"),
     "moment_skips_first_row": ("for (int t = lo; t < lo + m; ++t) sum += X[(size_t)t * D + d];",
                                "for (int t = lo + 1; t < lo + m; ++t) sum += X[(size_t)t * D + d];"),
+    # f32 append input (R11)
+    "f32_bounds_to_nearest": ("uint16_t dn = orc_double_to_half_dir(xmin, -1);",
+                              "uint16_t dn = orc_double_to_half(xmin);"),
+    "f32_bounds_overwrite": ("int held = first < c->len;", "int held = 0;"),
+    "half_dir_wrong_step": ("if (neg == toward_pos) return (uint16_t)(h - 1);",
+                            "if (neg == toward_pos) return (uint16_t)(h + 1);"),
+    "f32_values_as_keys": ("orc_quantize_row(vx, D, (int8_t *)c->V + r * D, &c->vs[r]);",
+                           "orc_quantize_row(kx, D, (int8_t *)c->V + r * D, &c->vs[r]);"),
 }
 
 
@@ -110,7 +118,8 @@ def _run_mutant(name, old, new, tmp):
                         os.path.join(ROOT, "tests", "test_oracle_sparse_v.py"),
                         os.path.join(ROOT, "tests", "test_oracle_q8_0.py"),
                         os.path.join(ROOT, "tests", "test_oracle_q4_0.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_tail.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_tail.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_append_f32.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return name, r.returncode
 
