@@ -140,6 +140,22 @@ KVD_API kvd_status kvd_kv_append(kvd_cache *cache, const void *k_new, const void
                          int32_t n_new, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* kvd_kv_append from f32 input  [CPUATT Usage: the cache takes each       */
+/* token's K and V as f32; QUEST All-KV-types composition: the bounds come */
+/* from the keys before quantization].                                      */
+/*   k_new, v_new: device, [batch, n_new, n_kv_heads, head_dim] f32.         */
+/*   f16 cache: stores each value's nearest f16 (ties to even), exactly as  */
+/*   kvd_kv_append of those f16 values would.                               */
+/*   int8 / q8_0 / q4_0: the rows are quantized from the f32 values; a       */
+/*   block's bounds are the f32 keys' channel envelope rounded outward to   */
+/*   f16 (kmin toward -inf, kmax toward +inf), merged as usual, so they     */
+/*   hold every key.  Block means (when kept) come from the stored rows.    */
+/* Errors and len: as kvd_kv_append.                                        */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_kv_append_f32(kvd_cache *cache, const float *k_new, const float *v_new,
+                             int32_t n_new, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* Quest block selection for one query token per sequence  [QUEST Method   */
 /* "Per-query upper bound", "Top-K block selection"; S2/S3 selector op:    */
 /* "GQA -> max UB over the query group per KV-head"].                      */

@@ -38,7 +38,7 @@ EXPORTS = ("kvd_kv_append", "kvd_select_blocks", "kvd_decode_attn", "kvd_decode_
            "kvd_decode_step", "kvd_decode_step_host", "kvd_workspace_bytes",
            "kvd_selected_count", "kvd_status_string", "kvd_abi_version", "kvd_debug_qk_int8",
            "kvd_debug_scores", "kvd_decode_attn_static", "kvd_decode_attn_sv",
-           "kvd_decode_attn_tail")
+           "kvd_decode_attn_tail", "kvd_kv_append_f32")
 
 
 class KvdError(RuntimeError):
@@ -71,6 +71,7 @@ def lib():
         p, i32, sz = C.c_void_p, C.c_int32, C.c_size_t
         cp = C.POINTER(CacheStruct)
         L.kvd_kv_append.argtypes = [cp, p, p, i32, p]
+        L.kvd_kv_append_f32.argtypes = [cp, p, p, i32, p]
         L.kvd_select_blocks.argtypes = [cp, p, i32, i32, i32, i32, p, p, p, sz, p]
         L.kvd_decode_attn.argtypes = [cp, p, i32, C.c_float, p, p, i32, p, p, sz, p]
         L.kvd_decode_attn_dense.argtypes = [cp, p, i32, C.c_float, p, p, sz, p]
@@ -225,6 +226,13 @@ def kv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=N
                                                 int(k_new.shape[1]), _stream(k_new, stream)))
 
 
+def kv_append_f32(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
+    """k_new, v_new: [B, n_new, Hkv, 128] float32 on the cache's device."""
+    _check("kvd_kv_append_f32", lib().kvd_kv_append_f32(cache.ref(), _ptr(k_new), _ptr(v_new),
+                                                        int(k_new.shape[1]),
+                                                        _stream(k_new, stream)))
+
+
 def select_blocks(cache: KVCache, q: torch.Tensor, k_sel: int, sink_tokens: int,
                   recent_tokens: int, sel_idx: torch.Tensor, sel_cnt: torch.Tensor,
                   workspace: torch.Tensor, stream=None):
@@ -314,6 +322,6 @@ def debug_scores(cache: KVCache, q: torch.Tensor, ub: torch.Tensor, stream=None)
 
 __all__ = ["F16", "INT8", "Q8_0", "Q4_0", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
            "workspace_bytes", "make_workspace", "selected_count", "status_string", "kv_append",
-           "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
+           "kv_append_f32", "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
            "decode_attn_sv", "decode_attn_tail", "decode_step",
            "decode_step_host", "debug_qk_int8", "debug_scores", "synth", "EXPORTS"]

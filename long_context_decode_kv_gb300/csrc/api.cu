@@ -256,19 +256,37 @@ size_t kvd_workspace_bytes(const kvd_cache *cache, int32_t n_heads) {
     return ws_layout(cache, n_heads).total;
 }
 
-kvd_status kvd_kv_append(kvd_cache *cache, const void *k_new, const void *v_new, int32_t n_new,
-                         void *stream) {
+}  // extern "C"
+
+namespace {
+
+kvd_status append_impl(kvd_cache *cache, const void *k_new, const void *v_new, int32_t n_new,
+                       void *stream, bool f32_in) {
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
     if (n_new < 0) return KVD_ERR_INVALID;
     if (n_new == 0) return KVD_OK;
     if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVD_ERR_INVALID;
     if (static_cast<long long>(cache->len) + n_new > cache->max_seq) return KVD_ERR_CAPACITY;
-    const cudaError_t e =
-        launch_append(*cache, k_new, v_new, n_new, static_cast<cudaStream_t>(stream), true);
+    const cudaError_t e = launch_append(*cache, k_new, v_new, n_new,
+                                        static_cast<cudaStream_t>(stream), true, f32_in);
     if (e != cudaSuccess) return KVD_ERR_CUDA;
     cache->len += n_new;
     return KVD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvd_status kvd_kv_append(kvd_cache *cache, const void *k_new, const void *v_new, int32_t n_new,
+                         void *stream) {
+    return append_impl(cache, k_new, v_new, n_new, stream, false);
+}
+
+kvd_status kvd_kv_append_f32(kvd_cache *cache, const float *k_new, const float *v_new,
+                             int32_t n_new, void *stream) {
+    return append_impl(cache, k_new, v_new, n_new, stream, true);
 }
 
 kvd_status kvd_select_blocks(const kvd_cache *cache, const float *q, int32_t n_heads,

@@ -25,6 +25,13 @@ __device__ __forceinline__ void load_half4(const __half *p, float (&x)[4]) {
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
 }
 
+__device__ __forceinline__ void load_in4(const __half *p, float (&x)[4]) { load_half4(p, x); }
+
+__device__ __forceinline__ void load_in4(const float *p, float (&x)[4]) {
+    const float4 w = *reinterpret_cast<const float4 *>(p);
+    x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+}
+
 // Channels 4 lane .. 4 lane + 3 of stored row r of K (is_v false) or V, as
 // the decode reads them: f16 as is, int8 code * row scale, q8_0 code * group
 // scale, q4_0 (code - 8) * group scale, each product one f32 rounding.
@@ -104,13 +111,18 @@ __device__ __forceinline__ void block_means_warp(const kvd_cache &c, size_t row0
 }
 
 // Tokens [max(lo, len0), min(lo + 64, len0 + n_new)) of cache block blk of
-// (sequence b, KV head h), taken from k_new / v_new [B, n_new, Hkv, 128] f16.
+// (sequence b, KV head h), taken from k_new / v_new [B, n_new, Hkv, 128] of
+// IN (f16, or f32 as "cpu-attn" Usage feeds its cache).  f32 input: the f16
+// cache stores each value's nearest f16 (and bounds those); the quantized
+// caches quantize the f32 values, and round the keys' envelope outward to f16
+// so that the bounds still hold every key.
 // MEANS: also the block's means when the cache keeps them (callers that
 // never see such a cache leave that code out).
-template <int DT, bool MEANS = true>
-__device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __half *k_new,
-                                                  const __half *v_new, int n_new, int len0,
+template <int DT, bool MEANS = true, typename IN = __half>
+__device__ __forceinline__ void append_block_warp(const kvd_cache &c, const IN *k_new,
+                                                  const IN *v_new, int n_new, int len0,
                                                   int blk, int b, int h, int lane) {
+    constexpr bool kF32In = sizeof(IN) == 4;
     const long lo = static_cast<long>(blk) * kBlock;
     const long nlo = lo > len0 ? lo : len0;
     const long nhi = (lo + kBlock) < (static_cast<long>(len0) + n_new) ? (lo + kBlock)
@@ -126,17 +138,33 @@ __device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __ha
         const size_t src = ((static_cast<size_t>(b) * n_new + (t - len0)) * c.n_kv_heads + h) *
                                kHeadDim + 4 * lane;
         float kx[4], vx[4];
-        load_half4(k_new + src, kx);
-        load_half4(v_new + src, vx);
+        load_in4(k_new + src, kx);
+        load_in4(v_new + src, vx);
+        if (kF32In && DT == KVD_F16) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // the f16 cache holds the nearest f16
+                kx[j] = __half2float(__float2half_rn(kx[j]));
+                vx[j] = __half2float(__float2half_rn(vx[j]));
+            }
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) { mn[j] = fminf(mn[j], kx[j]); mx[j] = fmaxf(mx[j], kx[j]); }
         const size_t dst = (row0 + t) * kHeadDim + 4 * lane;
         if (DT == KVD_F16) {
-            // verbatim copy of the f16 bits
-            *reinterpret_cast<uint2 *>(static_cast<__half *>(c.k) + dst) =
-                *reinterpret_cast<const uint2 *>(k_new + src);
-            *reinterpret_cast<uint2 *>(static_cast<__half *>(c.v) + dst) =
-                *reinterpret_cast<const uint2 *>(v_new + src);
+            if constexpr (kF32In) {  // the rounded values (exact in f16)
+                uint2 kw, vw;
+                *reinterpret_cast<__half2 *>(&kw.x) = __floats2half2_rn(kx[0], kx[1]);
+                *reinterpret_cast<__half2 *>(&kw.y) = __floats2half2_rn(kx[2], kx[3]);
+                *reinterpret_cast<__half2 *>(&vw.x) = __floats2half2_rn(vx[0], vx[1]);
+                *reinterpret_cast<__half2 *>(&vw.y) = __floats2half2_rn(vx[2], vx[3]);
+                *reinterpret_cast<uint2 *>(static_cast<__half *>(c.k) + dst) = kw;
+                *reinterpret_cast<uint2 *>(static_cast<__half *>(c.v) + dst) = vw;
+            } else {  // verbatim copy of the f16 bits
+                *reinterpret_cast<uint2 *>(static_cast<__half *>(c.k) + dst) =
+                    *reinterpret_cast<const uint2 *>(k_new + src);
+                *reinterpret_cast<uint2 *>(static_cast<__half *>(c.v) + dst) =
+                    *reinterpret_cast<const uint2 *>(v_new + src);
+            }
         } else if (DT == KVD_Q4_0) {
             __half kd, vd;
             const uint32_t kc = quantize_q4_0_warp(kx, &kd, lane);
@@ -189,11 +217,18 @@ __device__ __forceinline__ void append_block_warp(const kvd_cache &c, const __ha
             mx[j] = fmaxf(mx[j], f.y);
         }
     }
-    // every value is an f16 already, so the conversions back are exact
     uint4 w;
     __half2 *w2 = reinterpret_cast<__half2 *>(&w);
+    if (kF32In && DT != KVD_F16) {
+        // f32 keys: the envelope rounded outward (exact for the old f16 bounds)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w2[j] = __floats2half2_rn(mn[j], mx[j]);
+        for (int j = 0; j < 4; ++j)
+            w2[j] = __halves2half2(__float2half_rd(mn[j]), __float2half_ru(mx[j]));
+    } else {
+        // every value is an f16 already, so the conversions back are exact
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w2[j] = __floats2half2_rn(mn[j], mx[j]);
+    }
     *reinterpret_cast<uint4 *>(bounds) = w;
     if (MEANS && c.moments) {
         __syncwarp();  // the group scales written by other lanes are visible

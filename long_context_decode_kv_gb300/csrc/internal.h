@@ -35,7 +35,7 @@ size_t decode_partials_bytes(const Geom &g, const DecodePlan &p);
 int device_sm_count();
 
 cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_new, int n_new,
-                          cudaStream_t st, bool pdl);
+                          cudaStream_t st, bool pdl, bool f32_in = false);
 
 // Scratch of the selection (workspace regions; range and ticket are zero
 // between calls, and every completed call leaves them zero).

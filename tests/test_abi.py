@@ -166,6 +166,12 @@ def test_append_validation():
     assert L.kvd_kv_append(C.byref(s), FAKE + 2, FAKE, 1, None) == INVALID
     assert L.kvd_kv_append(C.byref(s), None, FAKE, 1, None) == INVALID
     assert L.kvd_kv_append(C.byref(_cache(dtype=7)), FAKE, FAKE, 1, None) == INVALID
+    s = _cache(length=4090)
+    assert L.kvd_kv_append_f32(C.byref(s), FAKE, FAKE, 7, None) == CAPACITY
+    assert L.kvd_kv_append_f32(C.byref(s), FAKE + 8, FAKE, 1, None) == INVALID
+    assert L.kvd_kv_append_f32(C.byref(s), FAKE, None, 1, None) == INVALID
+    assert L.kvd_kv_append_f32(C.byref(s), FAKE, FAKE, 0, None) == OK
+    assert s.len == 4090
     assert L.kvd_kv_append(C.byref(None if False else _cache(n_kv_heads=0)), FAKE, FAKE, 1,
                            None) == INVALID
 

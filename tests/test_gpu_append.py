@@ -122,3 +122,47 @@ def test_bounds_merge_equals_recompute_over_many_small_appends():
     nb = 4
     assert torch.equal(a.kmin[:, :, :nb].float(), b.kmin[:, :, :nb].float())
     assert torch.equal(a.kmax[:, :, :nb].float(), b.kmax[:, :, :nb].float())
+
+
+def _make_pair_f32(dtype, k, v, chunks, moments=False):
+    B, L, Hkv, D = k.shape
+    max_seq = (L + 64 + 63) // 64 * 64
+    gc = kvd.KVCache(dtype, B, Hkv, max_seq, device=dev(), moments=moments)
+    oc = oracle.OracleCache(dtype, B, Hkv, D, max_seq, 64)
+    kh, vh = k.cpu().numpy(), v.cpu().numpy()
+    s = 0
+    for n in chunks:
+        kvd.kv_append_f32(gc, k[:, s:s + n].contiguous(), v[:, s:s + n].contiguous())
+        oc.append_f32(kh[:, s:s + n], vh[:, s:s + n])
+        s += n
+    torch.cuda.synchronize()
+    assert gc.len == oc.len == L
+    return gc, oc
+
+
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
+@pytest.mark.parametrize("chunks", [[300], [1] * 70 + [230], [63, 2, 64, 1, 170]])
+def test_append_f32_matches_oracle(dtype, chunks):
+    # f32 input: rows, codes, scales and the outward-rounded bounds bit-exact
+    B, Hkv, L = 2, 3, sum(chunks)
+    k = seeded((B, L, Hkv, 128), 900, scale=3.0, dtype=torch.float32)
+    v = seeded((B, L, Hkv, 128), 901, dtype=torch.float32)
+    k[0, :5, 0, :4] = torch.tensor([1e-6, -1e-6, 3e4, -7e4])  # subnormal, large, past f16
+    gc, oc = _make_pair_f32(dtype, k, v, chunks)
+    _compare(gc, oc)
+
+
+def test_append_f32_f16_cache_equals_f16_input():
+    # the f16 cache stores the nearest f16 of each f32 value: the same cache as
+    # appending those f16 values
+    B, Hkv, L = 1, 2, 200
+    k = seeded((B, L, Hkv, 128), 910, scale=2.0, dtype=torch.float32)
+    v = seeded((B, L, Hkv, 128), 911, dtype=torch.float32)
+    a = kvd.KVCache(kvd.F16, B, Hkv, 256, device=dev())
+    b = kvd.KVCache(kvd.F16, B, Hkv, 256, device=dev())
+    kvd.kv_append_f32(a, k, v)
+    kvd.kv_append(b, k.half(), v.half())
+    torch.cuda.synchronize()
+    for name in ("k", "v", "kbounds"):
+        assert torch.equal(getattr(a, name)[:, :, :L].view(torch.int16),
+                           getattr(b, name)[:, :, :L].view(torch.int16)), name
