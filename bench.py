@@ -494,6 +494,88 @@ def run_tail_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_gqa_sweep(args):
+    """The GQA-shared selection against one selection per query head, at the
+    workload's K_SEL: device time of select and decode (write + read L2 flush
+    before each call), the K/V bytes each decode reads, the distinct blocks
+    the heads of a group pick, and each output's relative L2 error against
+    dense attention; one JSON line per workload."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    steps, warm = max(1, args.steps), max(3, args.warmup)
+
+    def timed_us(fn):
+        ms = []
+        for i in range(warm + steps):
+            flush.fill_(i & 0xFF)
+            drain.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= warm:
+                ms.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ms) * 1e3
+
+    def rel_err(x, ref):
+        e = ((x - ref).norm(dim=-1) / ref.norm(dim=-1)).flatten()
+        return float(e.median()), float(e.max())
+
+    for name in ("qwen3_4b_gqa_32k_f16", "ctx1m_int8"):
+        w = synth.WORKLOADS[name]
+        q, k, v, _ = synth.make_workload(w, device=dev)
+        cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev)
+        kvd.kv_append(cache, k, v)
+        del k, v
+        ws = kvd.make_workspace(cache, w.H)
+        nbmax = cache.max_seq // 64
+        dense = torch.empty(w.B, w.H, w.D, device=dev)
+        kvd.decode_attn_dense(cache, q, w.scale, dense, ws)
+        s_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev)
+        s_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev)
+        h_idx = torch.zeros((w.B, w.H, nbmax), dtype=torch.int32, device=dev)
+        h_cnt = torch.zeros((w.B, w.H), dtype=torch.int32, device=dev)
+        args_sel = (w.k_sel, w.sink_tokens, w.recent_tokens)
+        us_sel_s = timed_us(lambda: kvd.select_blocks(cache, q, *args_sel, s_idx, s_cnt, ws))
+        us_sel_h = timed_us(lambda: kvd.select_blocks_per_head(cache, q, *args_sel, h_idx,
+                                                                h_cnt, ws))
+        max_sel = kvd.selected_count(w.L, *args_sel)
+        shared, per_head = torch.empty_like(dense), torch.empty_like(dense)
+        us_dec_s = timed_us(lambda: kvd.decode_attn(cache, q, w.scale, s_idx, s_cnt, max_sel,
+                                                    shared, ws))
+        us_dec_h = timed_us(lambda: kvd.decode_attn_per_head(cache, q, w.scale, h_idx, h_cnt,
+                                                             max_sel, per_head, ws))
+        assert cache.device_status() == 0, "device-side fault reported"
+        blk_bytes = 64 * kv_bytes_per_token(w.dtype)
+        si, sc = s_idx.cpu().numpy(), s_cnt.cpu().numpy()
+        hi, hc = h_idx.cpu().numpy(), h_cnt.cpu().numpy()
+        shared_blocks = int(sc.sum())
+        head_blocks = int(hc.sum())
+        union = sum(len(set().union(*[set(hi[b, g * w.G + j, :hc[b, g * w.G + j]].tolist())
+                                      for j in range(w.G)]))
+                    for b in range(w.B) for g in range(w.Hkv))
+        print(json.dumps({
+            "sweep": "gqa", "workload": w.name, "context": w.L, "group": w.G,
+            "kv_dtype": dtype_name(w.dtype), "k_sel": w.k_sel,
+            "shared": {"select_us": us_sel_s, "decode_us": us_dec_s,
+                       "kv_bytes": shared_blocks * blk_bytes,
+                       "err_vs_dense_median": rel_err(shared, dense)[0],
+                       "err_vs_dense_max": rel_err(shared, dense)[1]},
+            "per_head": {"select_us": us_sel_h, "decode_us": us_dec_h,
+                         "kv_bytes": head_blocks * blk_bytes,
+                         "distinct_blocks_per_group_vs_shared": union / shared_blocks,
+                         "err_vs_dense_median": rel_err(per_head, dense)[0],
+                         "err_vs_dense_max": rel_err(per_head, dense)[1]},
+            "bytes_per_head_over_shared": head_blocks / shared_blocks, "steps": steps,
+            "l2": "write + read flush between calls"}), flush=True)
+        del cache, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -505,17 +587,20 @@ def main():
     ap.add_argument("--context", type=int, default=None,
                     help="run the workload's recipe at this context instead (a multiple "
                          "of 64; a smaller case for profiling)")
-    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v", "tail"],
+    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v", "tail", "gqa"],
                     default=None,
                     help="instead of the bench line: sparse vs dense decode steps over the "
                          "context sweep (16K..1M, 25%% coverage) or the 128K x 8 coverage "
                          "sweep, decode attention with sparse-V at several eps, or decode "
-                         "attention with the moment tail; one JSON line per point")
+                         "attention with the moment tail, or the GQA-shared selection "
+                         "against one per query head; one JSON line per point")
     args = ap.parse_args()
     if args.sweep == "sparse_v":
         return run_sparse_v_sweep(args)
     if args.sweep == "tail":
         return run_tail_sweep(args)
+    if args.sweep == "gqa":
+        return run_gqa_sweep(args)
     if args.sweep:
         return run_sweep(args)
     w = synth.WORKLOADS[args.workload]

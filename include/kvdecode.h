@@ -13,6 +13,8 @@
  *           "Correctness", "Requirements and limits".
  *  [SCSA]   "SCSA: Self-Calibrating Subquadratic Attention": "2. Mechanism"
  *           (the moment tail of the key groups not read exactly).
+ *  [CERT]   "Certified Sparse Attention via Perturbed Retrieval": Appendix
+ *           Table 4 (GQA-shared scan against one scan per query head).
  *
  * Conventions for every entry point
  *  - All device memory is allocated and owned by the caller.  The library
@@ -182,6 +184,37 @@ KVD_API kvd_status kvd_select_blocks(const kvd_cache *cache, const float *q, int
                              int32_t k_sel, int32_t sink_tokens, int32_t recent_tokens,
                              int32_t *sel_idx, int32_t *sel_cnt,
                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Per-query-head selection: the ablation of the GQA-shared one  [CERT      */
+/* Appendix Table 4: one scan per query head against the GQA-shared scan;   */
+/* QUEST "GQA": the shared block set avoids per-head divergence].           */
+/*   As kvd_select_blocks, except that query head h ranks the blocks by its  */
+/*   own bound UB_h(j) (no maximum over the group), and its list is row      */
+/*   (b, h) of sel_idx [batch, n_heads, max_seq / block] int32, its count    */
+/*   sel_cnt[b, h] ([batch, n_heads] int32).  Forced blocks and ties as      */
+/*   there.  One launch per head of a group.                                  */
+/* Errors: as kvd_select_blocks.                                              */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_select_blocks_per_head(const kvd_cache *cache, const float *q,
+                                      int32_t n_heads, int32_t k_sel, int32_t sink_tokens,
+                                      int32_t recent_tokens, int32_t *sel_idx,
+                                      int32_t *sel_cnt, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Decode attention over lists per query head (kvd_select_blocks_per_head's  */
+/* rows): as kvd_decode_attn, with query head h attending the blocks of row  */
+/* (b, h) of sel_idx [batch, n_heads, max_seq / block] (sel_cnt [batch,      */
+/* n_heads]).  Each CTA serves one query head, so a block listed for several */
+/* heads of a group is read once per head.                                    */
+/* Errors: as kvd_decode_attn.                                                */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_decode_attn_per_head(const kvd_cache *cache, const float *q,
+                                    int32_t n_heads, float softmax_scale,
+                                    const int32_t *sel_idx, const int32_t *sel_cnt,
+                                    int32_t max_sel, float *out, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* Split-KV decode attention over selected blocks only  [QUEST S3 FA-VEC   */

@@ -38,7 +38,8 @@ EXPORTS = ("kvd_kv_append", "kvd_select_blocks", "kvd_decode_attn", "kvd_decode_
            "kvd_decode_step", "kvd_decode_step_host", "kvd_workspace_bytes",
            "kvd_selected_count", "kvd_status_string", "kvd_abi_version", "kvd_debug_qk_int8",
            "kvd_debug_scores", "kvd_decode_attn_static", "kvd_decode_attn_sv",
-           "kvd_decode_attn_tail", "kvd_kv_append_f32")
+           "kvd_decode_attn_tail", "kvd_kv_append_f32", "kvd_select_blocks_per_head",
+           "kvd_decode_attn_per_head")
 
 
 class KvdError(RuntimeError):
@@ -78,6 +79,8 @@ def lib():
         L.kvd_decode_attn_static.argtypes = [cp, p, i32, C.c_float, p, p, i32, p, p]
         L.kvd_decode_attn_sv.argtypes = [cp, p, i32, C.c_float, p, p, i32, C.c_float, p, p, sz,
                                          p]
+        L.kvd_select_blocks_per_head.argtypes = [cp, p, i32, i32, i32, i32, p, p, p, sz, p]
+        L.kvd_decode_attn_per_head.argtypes = [cp, p, i32, C.c_float, p, p, i32, p, p, sz, p]
         L.kvd_decode_attn_tail.argtypes = [cp, p, i32, C.c_float, p, p, i32, p, p, sz, p]
         L.kvd_decode_step.argtypes = [cp, p, p, p, i32, C.c_float, i32, i32, i32, p, p, p, p,
                                       sz, p]
@@ -270,6 +273,26 @@ def decode_attn_sv(cache: KVCache, q: torch.Tensor, softmax_scale: float, sel_id
         workspace.numel(), _stream(q, stream)))
 
 
+def select_blocks_per_head(cache: KVCache, q: torch.Tensor, k_sel: int, sink_tokens: int,
+                           recent_tokens: int, sel_idx: torch.Tensor, sel_cnt: torch.Tensor,
+                           workspace: torch.Tensor, stream=None):
+    """Selection per query head: sel_idx [B, H, max_seq // 64], sel_cnt [B, H] int32."""
+    _check("kvd_select_blocks_per_head", lib().kvd_select_blocks_per_head(
+        cache.ref(), _ptr(q), int(q.shape[1]), int(k_sel), int(sink_tokens),
+        int(recent_tokens), _ptr(sel_idx), _ptr(sel_cnt), _ptr(workspace), workspace.numel(),
+        _stream(q, stream)))
+
+
+def decode_attn_per_head(cache: KVCache, q: torch.Tensor, softmax_scale: float, sel_idx,
+                         sel_cnt, max_sel: int, out: torch.Tensor, workspace: torch.Tensor,
+                         stream=None):
+    """decode_attn over lists per query head (select_blocks_per_head's rows)."""
+    _check("kvd_decode_attn_per_head", lib().kvd_decode_attn_per_head(
+        cache.ref(), _ptr(q), int(q.shape[1]), float(softmax_scale), _ptr(sel_idx),
+        _ptr(sel_cnt), int(max_sel), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(q, stream)))
+
+
 def decode_attn_tail(cache: KVCache, q: torch.Tensor, softmax_scale: float, sel_idx, sel_cnt,
                      max_sel: int, out: torch.Tensor, workspace: torch.Tensor, stream=None):
     """decode_attn plus the moment tail of every block the lists leave out
@@ -323,5 +346,6 @@ def debug_scores(cache: KVCache, q: torch.Tensor, ub: torch.Tensor, stream=None)
 __all__ = ["F16", "INT8", "Q8_0", "Q4_0", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
            "workspace_bytes", "make_workspace", "selected_count", "status_string", "kv_append",
            "kv_append_f32", "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
-           "decode_attn_sv", "decode_attn_tail", "decode_step",
+           "decode_attn_sv", "decode_attn_tail", "select_blocks_per_head",
+           "decode_attn_per_head", "decode_step",
            "decode_step_host", "debug_qk_int8", "debug_scores", "synth", "EXPORTS"]

@@ -98,8 +98,8 @@ WsLayout ws_layout(const kvd_cache *c, int n_heads) {
     w.plan = plan_decode(g, g.nbmax, device_sm_count());
     const size_t P = static_cast<size_t>(g.B) * g.Hkv;
     size_t off = 0;
-    w.counters = off;
-    off += align_up(P * w.plan.subgroups * sizeof(uint32_t));
+    w.counters = off;  // one per query head: enough for one-head-per-CTA plans too
+    off += align_up(static_cast<size_t>(g.B) * g.H * sizeof(uint32_t));
     w.partials = off;
     off += align_up(decode_partials_bytes(g, w.plan));
     w.keys = off;  // key rows padded to 16 bytes
@@ -207,6 +207,19 @@ kvd_status decode_tail_impl(const kvd_cache *c, const float *q, int n_heads, flo
     return cuda_status(launch_decode_tail(*c, g, p, q, scale, sel_idx, sel_cnt, out,
                                           ws_at<float>(ws, w.partials),
                                           ws_at<uint32_t>(ws, w.counters), st, true));
+}
+
+// Lists per query head (an ablation of the GQA-shared selection).
+kvd_status decode_per_head_impl(const kvd_cache *c, const float *q, int n_heads, float scale,
+                                const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel,
+                                float *out, void *ws, const WsLayout &w, cudaStream_t st) {
+    const Geom g = make_geom(c, n_heads, c->len);
+    int max_blocks = max_sel < g.NB ? max_sel : g.NB;
+    if (max_blocks < 1) max_blocks = 1;
+    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), true);
+    return cuda_status(launch_decode_per_head(*c, g, p, q, scale, sel_idx, sel_cnt, out,
+                                              ws_at<float>(ws, w.partials),
+                                              ws_at<uint32_t>(ws, w.counters), st, true));
 }
 
 kvd_status check_select_args(const kvd_cache *c, int n_heads, int k_sel, int sink, int recent) {
@@ -341,6 +354,41 @@ kvd_status kvd_decode_attn_sv(const kvd_cache *cache, const float *q, int32_t n_
     return decode_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_idx ? sel_cnt : nullptr,
                        sel_idx ? max_sel : 0, out, workspace, w,
                        static_cast<cudaStream_t>(stream), false, sparse_v_eps);
+}
+
+kvd_status kvd_select_blocks_per_head(const kvd_cache *cache, const float *q, int32_t n_heads,
+                                      int32_t k_sel, int32_t sink_tokens,
+                                      int32_t recent_tokens, int32_t *sel_idx,
+                                      int32_t *sel_cnt, void *workspace, size_t workspace_bytes,
+                                      void *stream) {
+    kvd_status s = check_select_args(cache, n_heads, k_sel, sink_tokens, recent_tokens);
+    if (s != KVD_OK) return s;
+    if (!q || !aligned(q, 16)) return KVD_ERR_INVALID;
+    if (!sel_idx || !aligned(sel_idx, 4) || !sel_cnt || !aligned(sel_cnt, 4))
+        return KVD_ERR_INVALID;
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    const Geom g = make_geom(cache, n_heads, cache->len);
+    return cuda_status(launch_select_per_head(*cache, g, q, k_sel, sink_tokens, recent_tokens,
+                                              sel_idx, sel_cnt, sel_scratch(workspace, w),
+                                              static_cast<cudaStream_t>(stream), true));
+}
+
+kvd_status kvd_decode_attn_per_head(const kvd_cache *cache, const float *q, int32_t n_heads,
+                                    float softmax_scale, const int32_t *sel_idx,
+                                    const int32_t *sel_cnt, int32_t max_sel, float *out,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+    kvd_status s = check_cache(cache);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (cache->len < 1 || max_sel < 0) return KVD_ERR_INVALID;
+    if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
+    if (!sel_idx || !aligned(sel_idx, 4) || !sel_cnt || !aligned(sel_cnt, 4))
+        return KVD_ERR_INVALID;
+    const WsLayout w = ws_layout(cache, n_heads);
+    if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
+    return decode_per_head_impl(cache, q, n_heads, softmax_scale, sel_idx, sel_cnt, max_sel,
+                                out, workspace, w, static_cast<cudaStream_t>(stream));
 }
 
 kvd_status kvd_decode_attn_tail(const kvd_cache *cache, const float *q, int32_t n_heads,

@@ -43,9 +43,9 @@ __global__ void __launch_bounds__(256) qk_debug_kernel(DecodeArgs a, int32_t *do
 
 }  // namespace
 
-DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count) {
+DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_head) {
     DecodePlan p;
-    p.heads_per_cta = g.G < 4 ? g.G : 4;
+    p.heads_per_cta = one_head ? 1 : g.G < 4 ? g.G : 4;
     p.subgroups = g.G / p.heads_per_cta;
     const long P = static_cast<long>(g.B) * g.Hkv * p.subgroups;
     const int per_sm = g.dtype == KVD_F16    ? Tile<KVD_F16>::kMinCtas
@@ -79,6 +79,23 @@ cudaError_t launch_decode(const kvd_cache &c, const Geom &g, const DecodePlan &p
                                 st, pdl, early_q, sv_eps);
     return launch_decode_any<false>(c, g, p, q, scale, sel_idx, sel_cnt, out, partials,
                                     counters, st, pdl, early_q, 0.0f);
+}
+
+cudaError_t launch_decode_per_head(const kvd_cache &c, const Geom &g, const DecodePlan &p,
+                                   const float *q, float scale, const int32_t *sel_idx,
+                                   const int32_t *sel_cnt, float *out, float *partials,
+                                   uint32_t *counters, cudaStream_t st, bool pdl) {
+    DecodeArgs a = make_decode_args(c, g, p, q, scale, sel_idx, sel_cnt, out, partials,
+                                    counters, false, 0.0f);
+    a.per_head = 1;  // p.heads_per_cta is 1: CTA problem b * H + h reads list row b * H + h
+    const int P_sub = g.B * g.Hkv * p.subgroups;
+    if (g.dtype == KVD_INT8)
+        return launch_decode_t<KVD_INT8, 1, false, false, false>(a, P_sub, st, pdl);
+    if (g.dtype == KVD_Q8_0)
+        return launch_decode_t<KVD_Q8_0, 1, false, false, false>(a, P_sub, st, pdl);
+    if (g.dtype == KVD_Q4_0)
+        return launch_decode_t<KVD_Q4_0, 1, false, false, false>(a, P_sub, st, pdl);
+    return launch_decode_t<KVD_F16, 1, false, false, false>(a, P_sub, st, pdl);
 }
 
 cudaError_t launch_qk_debug(const kvd_cache &c, const Geom &g, const float *q, int32_t *dots,

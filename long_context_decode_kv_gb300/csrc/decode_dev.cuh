@@ -115,6 +115,7 @@ struct DecodeArgs {
     float sv_eps;        // sparse-V (eps mode): 0 = every V term accumulated
     float scale_log2;  // softmax_scale * log2(e): logits live in base 2
     int early_q;       // q is complete before the upstream kernels finish
+    int per_head;      // lists per query head ([B, H] rows; one head per CTA)
 };
 
 template <int DT, int GC, bool TAIL = false>
@@ -1069,7 +1070,9 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     if (a.early_q) load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
     pdl_wait();  // upstream kernels (append, select) are complete past here
     pdl_launch_dependents();
-    int cnt = DENSE ? a.NB : a.sel_cnt[bg];
+    // the list row: the KV head's, or with per-head lists the CTA's one head's
+    const int lrow = a.per_head ? prob : bg;
+    int cnt = DENSE ? a.NB : a.sel_cnt[lrow];
     cnt = max(0, min(cnt, a.NB));
 
     const size_t row0 = static_cast<size_t>(bg) * a.max_seq;  // first token row of (b, g)
@@ -1085,7 +1088,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         // length, then (only when sel_cnt passes that length) every
         // splits-th position beyond it, from plan_blocks + split on.
         const uint64_t pol = l2_policy_evict_first();
-        const int32_t *list = a.sel_idx + static_cast<size_t>(bg) * a.nbmax;
+        const int32_t *list = a.sel_idx + static_cast<size_t>(lrow) * a.nbmax;
         const int S = a.splits, MB = a.plan_blocks;
         const int pb = static_cast<int>((static_cast<long long>(split) * MB) / S);
         const int pe = static_cast<int>((static_cast<long long>(split + 1) * MB) / S);

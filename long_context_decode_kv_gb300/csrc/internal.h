@@ -30,7 +30,8 @@ struct DecodePlan {
     int blocks;         // list length planned for (max_sel, at most NB)
 };
 
-DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count);
+// one_head: one query head per CTA (lists per query head).
+DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_head = false);
 size_t decode_partials_bytes(const Geom &g, const DecodePlan &p);
 int device_sm_count();
 
@@ -60,6 +61,11 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
                           int sink_tokens, int recent_tokens, int32_t *sel_idx,
                           int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st, bool pdl,
                           const StepToken *tok);
+// Per-query-head selection (sel_idx [B, H, nbmax], sel_cnt [B, H]).
+cudaError_t launch_select_per_head(const kvd_cache &c, const Geom &g, const float *q, int k_sel,
+                                   int sink_tokens, int recent_tokens, int32_t *sel_idx,
+                                   int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st,
+                                   bool pdl);
 
 cudaError_t launch_scores_debug(const kvd_cache &c, const Geom &g, const float *q, float *ub,
                                 cudaStream_t st);
@@ -80,6 +86,13 @@ cudaError_t launch_decode_sv(const kvd_cache &c, const Geom &g, const DecodePlan
                              const int32_t *sel_cnt, float *out, float *partials,
                              uint32_t *counters, cudaStream_t st, bool pdl, bool early_q,
                              float sv_eps);
+// Decode over lists per query head (sel_idx [B, H, nbmax], sel_cnt [B, H]);
+// p planned with one_head.
+cudaError_t launch_decode_per_head(const kvd_cache &c, const Geom &g, const DecodePlan &p,
+                                   const float *q, float scale, const int32_t *sel_idx,
+                                   const int32_t *sel_cnt, float *out, float *partials,
+                                   uint32_t *counters, cudaStream_t st, bool pdl);
+
 // The listed blocks exactly plus the moment tail of every other block
 // (decode_tail.cu); c.moments must be set.
 cudaError_t launch_decode_tail(const kvd_cache &c, const Geom &g, const DecodePlan &p,

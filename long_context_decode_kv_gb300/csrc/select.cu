@@ -77,6 +77,8 @@ SelArgs base_args(const kvd_cache &c, const Geom &g, const float *q) {
     a.nbmax = g.nbmax;
     a.NB = g.NB;
     a.dev_status = c.dev_status;
+    a.head_sub = -1;
+    a.G_all = g.G;
     return a;
 }
 
@@ -139,6 +141,49 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
     // upstream kernels finish
     a.overlap = fuse ? 1 : 0;
     return launch_select_any<kSelect>(a, g.G, P, st, pdl);
+}
+
+// Per-query-head selection: query head h of KV head g ranks the blocks by its
+// own bound, not the group's maximum.  One launch per head of the group, each
+// a G = 1 selection over the B * Hkv problems (the same scratch, reused in
+// stream order), writing rows [B, H] of sel_idx / sel_cnt.
+cudaError_t launch_select_per_head(const kvd_cache &c, const Geom &g, const float *q, int k_sel,
+                                   int sink_tokens, int recent_tokens, int32_t *sel_idx,
+                                   int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st,
+                                   bool pdl) {
+    const int NB = g.NB;
+    int se = (sink_tokens + kBlock - 1) / kBlock;
+    if (se > NB) se = NB;
+    int rb = NB;
+    if (recent_tokens > 0) {
+        long start = static_cast<long>(g.len) - recent_tokens;
+        if (start < 0) start = 0;
+        rb = static_cast<int>(start / kBlock);
+    }
+    if (rb < se) rb = se;
+    const int n_cand = rb - se;
+    const int keff = k_sel < n_cand ? k_sel : n_cand;
+    const int P = g.B * g.Hkv;
+    if (!(keff > 0 && keff < n_cand))  // nothing to rank: every head gets the same list
+        return launch_ex(fill_kernel, dim3(P * g.G), dim3(256), 0, st, pdl, sel_idx, sel_cnt,
+                         g.nbmax, NB, se, rb, keff > 0 ? 1 : 0);
+    SelArgs a = base_args(c, g, q);
+    a.se = se;
+    a.n = n_cand;
+    a.keys = scr.keys;
+    a.ldk = (n_cand + 3) / 4 * 4;
+    a.range = scr.range;
+    a.ticket = scr.ticket;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.rb = rb;
+    a.keff = keff;
+    for (int sub = 0; sub < g.G; ++sub) {
+        a.head_sub = sub;
+        const cudaError_t e = launch_select_any<kSelect>(a, 1, P, st, pdl);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_scores_debug(const kvd_cache &c, const Geom &g, const float *q, float *ub,

@@ -191,11 +191,21 @@ struct SelArgs {
     int NB, rb, keff;
     int32_t *dev_status;
     int overlap;
+    // per-query-head selection (an ablation of the GQA-shared one): this
+    // launch serves query head head_sub of every group of G_all heads, and
+    // problem p writes list row p * G_all + head_sub; head_sub < 0: shared
+    int head_sub, G_all;
     // decode step: the token to append (app_k non-null), fused here because
     // its block is forced (never scored); app_cache.len is the length before
     kvd_cache app_cache;
     const __half *app_k, *app_v;
 };
+
+// The list row problem p writes.
+__device__ __forceinline__ size_t sel_row(const SelArgs &a, int p) {
+    return a.head_sub < 0 ? static_cast<size_t>(p)
+                          : static_cast<size_t>(p) * a.G_all + a.head_sub;
+}
 
 __device__ __forceinline__ int warp_inclusive_scan(int x, int lane) {
 #pragma unroll
@@ -337,7 +347,7 @@ __device__ __forceinline__ void select_write_list(const SelArgs &a, int p, int n
     unsigned before = incl - mine;
     for (int w = 0; w < warp; ++w) before += static_cast<unsigned>(rs.wsum[w]);
     int g_before = static_cast<int>(before & 0xffffu), e_before = static_cast<int>(before >> 16);
-    int32_t *dst = a.sel_idx + static_cast<size_t>(p) * a.nbmax;
+    int32_t *dst = a.sel_idx + sel_row(a, p) * a.nbmax;
     for (int wi = w0; wi < w1; ++wi) {
         const uint32_t gm = gtw[wi], em = eqw[wi];
         uint32_t take = gm;
@@ -353,7 +363,7 @@ __device__ __forceinline__ void select_write_list(const SelArgs &a, int p, int n
     }
     for (int j = tid; j < a.se; j += kScoreThreads) dst[j] = j;
     for (int j = a.rb + tid; j < a.NB; j += kScoreThreads) dst[a.se + a.keff + (j - a.rb)] = j;
-    if (tid == 0) a.sel_cnt[p] = a.se + a.keff + (a.NB - a.rb);
+    if (tid == 0) a.sel_cnt[sel_row(a, p)] = a.se + a.keff + (a.NB - a.rb);
 }
 
 // Phases 3-4 of the last CTA of a problem, with the problem's key range
@@ -604,8 +614,9 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
         }
     } else {
         // the producer's first copies are in flight while the query loads
-        const float *qg =
-            a.q + (static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * G) * kHeadDim;
+        const size_t h0 = a.head_sub < 0 ? static_cast<size_t>(g) * G
+                                         : static_cast<size_t>(g) * a.G_all + a.head_sub;
+        const float *qg = a.q + (static_cast<size_t>(b) * a.H + h0) * kHeadDim;
         for (int i = tid; i < G * kHeadDim; i += kConsumerThreads) q_s[i] = qg[i];
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
         float2 qreg[NH][8];
@@ -750,7 +761,7 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
     if (__syncthreads_or(s_abort)) {
         if (tid == 0) {
             report_status(a.dev_status, KVD_ERR_TIMEOUT);
-            a.sel_cnt[p] = 0;
+            a.sel_cnt[sel_row(a, p)] = 0;
             volatile int never = 0;
             if (in_smem) (void)mbar_wait(&rs.kbar, 0, &never);  // copies in flight
         }

@@ -151,6 +151,16 @@ def test_decode_tail_validation():
                 10, FAKE, FAKE, n, None) == INVALID
     assert tail(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, FAKE, n - 256,
                 None) == WORKSPACE
+    # per-head selection and decode validate like the shared calls
+    ph = L.kvd_select_blocks_per_head
+    assert ph(C.byref(s), FAKE, 12, 4, 4, 64, FAKE, FAKE, FAKE, n, None) == INVALID
+    assert ph(C.byref(s), FAKE, 32, -1, 4, 64, FAKE, FAKE, FAKE, n, None) == INVALID
+    assert ph(C.byref(s), FAKE, 32, 4, 4, 64, None, FAKE, FAKE, n, None) == INVALID
+    assert ph(C.byref(s), FAKE, 32, 4, 4, 64, FAKE, FAKE, FAKE, 16, None) == WORKSPACE
+    pd = L.kvd_decode_attn_per_head
+    assert pd(C.byref(s), FAKE, 32, 0.1, FAKE, None, 10, FAKE, FAKE, n, None) == INVALID
+    assert pd(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, -1, FAKE, FAKE, n, None) == INVALID
+    assert pd(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, None, n, None) == WORKSPACE
     # a cache that keeps moments is otherwise an ordinary cache
     assert _select(_cache(moments=FAKE + 8)) == INVALID
 
