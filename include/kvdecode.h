@@ -106,6 +106,16 @@ typedef enum { KVD_F16 = 0, KVD_INT8 = 1, KVD_Q8_0 = 2, KVD_Q4_0 = 3 } kvd_kv_dt
  * and kvd_decode_step keep them for every block they write; they feed the
  * moment tail of kvd_decode_attn_tail.  Rewinding len inside a block and
  * appending again recomputes that block's means from its rows.
+ * `seq_lens` may be NULL (every sequence holds len tokens); if set, a device
+ * int32 [batch] with sequence b's own length, 0 <= seq_lens[b] <= len, and
+ * `len` is the batch's maximum (it sizes the grids).  Every call then works
+ * per sequence: kvd_kv_append writes sequence b's new rows from position
+ * seq_lens[b] (the caller adds n_new to seq_lens afterwards; the library
+ * never writes it), the selection ranks blocks below ceil(seq_lens[b] / block)
+ * with the recent window ending at seq_lens[b], and the decode calls attend
+ * tokens below seq_lens[b] (a sequence of length 0 gets a zero output).
+ * kvd_decode_step, kvd_decode_step_host and kvd_debug_scores do not take it
+ * (UNSUPPORTED).
  */
 typedef struct kvd_cache {
     int32_t dtype;        /* kvd_kv_dtype */
@@ -123,6 +133,7 @@ typedef struct kvd_cache {
     void *kbounds;
     int32_t *dev_status;
     void *moments;        /* optional block means (moment tail), see above */
+    const int32_t *seq_lens;  /* optional per-sequence lengths, see above */
 } kvd_cache;
 
 /* ---------------------------------------------------------------------- */

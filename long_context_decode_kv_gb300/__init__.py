@@ -55,7 +55,7 @@ class CacheStruct(C.Structure):
                 ("len", C.c_int32), ("reserved", C.c_int32),
                 ("k", C.c_void_p), ("v", C.c_void_p), ("k_scale", C.c_void_p),
                 ("v_scale", C.c_void_p), ("kbounds", C.c_void_p), ("dev_status", C.c_void_p),
-                ("moments", C.c_void_p)]
+                ("moments", C.c_void_p), ("seq_lens", C.c_void_p)]
 
 
 _lib = None
@@ -129,6 +129,8 @@ class KVCache:
     status    [1] int32 device word for device-side faults
     moments   [B, Hkv, max_seq // 64, 2, 128] float16 block means of K then V
               (only with moments=True: the moment tail of decode_attn_tail)
+    seq_lens  optional [B] int32 device tensor of per-sequence lengths (each at
+              most len; len is then the batch's maximum); see set_seq_lens
     """
 
     def __init__(self, dtype: int, batch: int, n_kv_heads: int, max_seq: int,
@@ -170,6 +172,25 @@ class KVCache:
                              _ptr(self.t.get("k_scale")), _ptr(self.t.get("v_scale")),
                              _ptr(self.t["kbounds"]), _ptr(self.t.get("status")),
                              _ptr(self.t.get("moments")))
+
+    def set_seq_lens(self, seq_lens: Optional[torch.Tensor]):
+        """Give every sequence its own length (an int32 [B] device tensor the
+        caller owns and advances after each append), or None for one length."""
+        if seq_lens is not None:
+            assert seq_lens.dtype == torch.int32 and seq_lens.shape == (self.batch,)
+            self.t["seq_lens"] = seq_lens
+        else:
+            self.t.pop("seq_lens", None)
+        self.s.seq_lens = _ptr(seq_lens)
+
+    def view(self, b: int) -> "KVCache":
+        """Sequence b alone, as a batch-1 cache over the same memory (one
+        sequence's rows, scales, bounds and means are contiguous slices)."""
+        t = {k: v[b:b + 1] for k, v in self.t.items() if k not in ("status", "seq_lens")}
+        t["status"] = self.t["status"]
+        c = KVCache(self.dtype, 1, self.n_kv_heads, self.max_seq, self.head_dim, self.block,
+                    device=self.t["k"].device, tensors=t)
+        return c
 
     @property
     def kmin(self) -> torch.Tensor:

@@ -58,6 +58,7 @@ kvd_status check_cache(const kvd_cache *c) {
     }
     if (c->dev_status && !aligned(c->dev_status, 4)) return KVD_ERR_INVALID;
     if (c->moments && !aligned(c->moments, 16)) return KVD_ERR_INVALID;
+    if (c->seq_lens && !aligned(c->seq_lens, 4)) return KVD_ERR_INVALID;
     if (static_cast<long long>(c->batch) * c->n_kv_heads * 16 > 65535) return KVD_ERR_UNSUPPORTED;
     return KVD_OK;
 }
@@ -430,6 +431,7 @@ kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (cache->seq_lens) return KVD_ERR_UNSUPPORTED;  // one length per cache in a step
     if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
     if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVD_ERR_INVALID;
     if (cache->len + 1 > cache->max_seq) return KVD_ERR_CAPACITY;
@@ -499,6 +501,7 @@ kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host, const voi
                                 void *workspace, size_t workspace_bytes, void *stream) {
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
+    if (cache->seq_lens) return KVD_ERR_UNSUPPORTED;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
     if (!q_host || !k_new_host || !v_new_host || !out_host) return KVD_ERR_INVALID;
     const WsLayout w = ws_layout(cache, n_heads);
@@ -556,6 +559,7 @@ kvd_status kvd_debug_scores(const kvd_cache *cache, const float *q, int32_t n_he
                             void *stream) {
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
+    if (cache->seq_lens) return KVD_ERR_UNSUPPORTED;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
     if (cache->len < 1) return KVD_ERR_INVALID;
     if (!q || !aligned(q, 16) || !ub || !aligned(ub, 4)) return KVD_ERR_INVALID;

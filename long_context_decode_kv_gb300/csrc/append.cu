@@ -20,10 +20,16 @@ append_kernel(kvd_cache c, const IN *__restrict__ k_new, const IN *__restrict__ 
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int a = blockIdx.x * kAppendWarps + warp;
-    if (a >= n_aff) return;
     const int p = blockIdx.y;
-    append_block_warp<DT, true, IN>(c, k_new, v_new, n_new, len0, first_blk + a,
-                                    p / c.n_kv_heads, p % c.n_kv_heads, lane);
+    const int b = p / c.n_kv_heads;
+    if (c.seq_lens) {  // this sequence's own position: its touched blocks
+        len0 = seq_len_of(c.seq_lens, b, c.len, c.dev_status);
+        first_blk = len0 / kBlock;
+        n_aff = (len0 + n_new - 1) / kBlock - first_blk + 1;
+    }
+    if (a >= n_aff) return;
+    append_block_warp<DT, true, IN>(c, k_new, v_new, n_new, len0, first_blk + a, b,
+                                    p % c.n_kv_heads, lane);
 }
 
 template <typename IN>
@@ -32,7 +38,8 @@ cudaError_t launch_append_in(const kvd_cache &c, const void *k_new, const void *
     const int len0 = c.len;
     const int first = len0 / kBlock;
     const int last = (len0 + n_new - 1) / kBlock;
-    const int n_aff = last - first + 1;
+    // with per-sequence lengths a sequence's n_new rows touch at most this many
+    const int n_aff = c.seq_lens ? (n_new + kBlock - 1) / kBlock + 1 : last - first + 1;
     dim3 grid((n_aff + kAppendWarps - 1) / kAppendWarps, c.batch * c.n_kv_heads);
     dim3 block(32 * kAppendWarps);
     const IN *kn = static_cast<const IN *>(k_new);

@@ -131,6 +131,40 @@ __device__ __forceinline__ void report_status(int32_t *dev_status, int code) {
     if (dev_status) atomicCAS(reinterpret_cast<int *>(dev_status), 0, code);
 }
 
+// Sequence b's own length when the cache carries per-sequence lengths (one
+// outside [0, len] is reported and clamped), else the cache's len.
+__device__ __forceinline__ int seq_len_of(const int32_t *seq_lens, int b, int len,
+                                          int32_t *dev_status) {
+    if (!seq_lens) return len;
+    int l = seq_lens[b];
+    if (l < 0 || l > len) {
+        report_status(dev_status, KVD_ERR_INVALID);
+        l = l < 0 ? 0 : len;
+    }
+    return l;
+}
+
+// Quest forced blocks and candidates of a sequence of L tokens: sink blocks
+// [0, se), recent blocks [rb, NB), candidates [se, rb).
+struct ForcedRange {
+    int NB, se, rb;
+};
+__device__ __host__ __forceinline__ ForcedRange forced_range(int L, int sink_tokens,
+                                                             int recent_tokens) {
+    ForcedRange f;
+    f.NB = (L + kBlock - 1) / kBlock;
+    f.se = (sink_tokens + kBlock - 1) / kBlock;
+    if (f.se > f.NB) f.se = f.NB;
+    f.rb = f.NB;
+    if (recent_tokens > 0) {
+        long start = static_cast<long>(L) - recent_tokens;
+        if (start < 0) start = 0;
+        f.rb = static_cast<int>(start / kBlock);
+    }
+    if (f.rb < f.se) f.rb = f.se;
+    return f;
+}
+
 // ------------------------------------------------------------ numerics ---
 // Order-preserving map f32 -> u32 (larger float, larger key); -0 maps as +0.
 __device__ __forceinline__ uint32_t float_to_key(float f) {

@@ -116,6 +116,7 @@ struct DecodeArgs {
     float scale_log2;  // softmax_scale * log2(e): logits live in base 2
     int early_q;       // q is complete before the upstream kernels finish
     int per_head;      // lists per query head ([B, H] rows; one head per CTA)
+    const int32_t *seq_lens;  // per-sequence lengths (<= len), or null
 };
 
 template <int DT, int GC, bool TAIL = false>
@@ -857,14 +858,15 @@ __device__ __forceinline__ int first_at_least(const int32_t *list, int n, int ta
 // entries cur .. cur + 31, of which the first o lanes are used up.
 // i: the stage sequence number, advanced per stage.
 template <int DT>
-__device__ __forceinline__ bool produce_tail(const DecodeArgs &a, int split, int bg, int cnt,
+__device__ __forceinline__ bool produce_tail(const DecodeArgs &a, int NB, int split, int bg,
+                                             int cnt,
                                              const int32_t *list, int &i, uint64_t *full,
                                              uint64_t *empty, int *stage_blk,
                                              uint32_t *stage_mask, uint8_t *ring,
                                              volatile int *abort_flag, int lane, uint64_t pol) {
     using TL = Tile<DT>;
     constexpr int R = TL::kTailRecs;
-    const int nch = (a.NB + R - 1) / R;
+    const int nch = (NB + R - 1) / R;
     const int c0 = static_cast<int>((static_cast<long long>(split) * nch) / a.splits);
     const int c1 = static_cast<int>((static_cast<long long>(split + 1) * nch) / a.splits);
     if (c0 >= c1) return true;
@@ -891,7 +893,7 @@ __device__ __forceinline__ bool produce_tail(const DecodeArgs &a, int split, int
             if (i >= TL::kStages)
                 ok = mbar_wait(&empty[s], ((i / TL::kStages) - 1) & 1, abort_flag);
             if (ok) {
-                const int nrec = min(R, a.NB - lo);
+                const int nrec = min(R, NB - lo);
                 stage_blk[s] = kTailBase - c;
                 stage_mask[s] = m;
                 mbar_arrive_expect_tx(&full[s], nrec * kMomentBytes);
@@ -941,7 +943,8 @@ constexpr int tail_shift() {
 // [wg RW, wg RW + RW) of each stage; ts.m and ts.l belong to the lane's head
 // h = (lane >> SH) % GC, ts.acc to channels 4 lane .. 4 lane + 3 of every head.
 template <int DT, int GC>
-__device__ __forceinline__ void tail_loop(const DecodeArgs &a, int b, int h0, int i,
+__device__ __forceinline__ void tail_loop(const DecodeArgs &a, int len, int NB, int b, int h0,
+                                          int i,
                                        uint64_t *full, uint64_t *empty, const int *stage_blk,
                                        const uint32_t *stage_mask, const uint8_t *ring, float *pw,
                                        int wg, int lane, volatile int *abort_flag,
@@ -980,7 +983,7 @@ __device__ __forceinline__ void tail_loop(const DecodeArgs &a, int b, int h0, in
         uint32_t vm = 0;  // records to fold: present and not listed
 #pragma unroll
         for (int r = 0; r < RW; ++r)
-            if (j0 + r < a.NB && !((listed >> r) & 1u)) vm |= 1u << r;
+            if (j0 + r < NB && !((listed >> r) & 1u)) vm |= 1u << r;
         if (vm) {
             float d[N];
 #pragma unroll
@@ -996,7 +999,7 @@ __device__ __forceinline__ void tail_loop(const DecodeArgs &a, int b, int h0, in
             }
             float x = reduce_scatter_n<N>(d, lane);
             const int j = j0 + r_own;
-            const int m = min(kBlock, a.len - j * kBlock);
+            const int m = min(kBlock, len - j * kBlock);
             x = ((vm >> r_own) & 1u) ? x + (m == kBlock ? 6.0f : log2f(static_cast<float>(m)))
                                      : -INFINITY;
             // over this warp's records of the lane's head (lane bits above LGC + SH)
@@ -1072,8 +1075,11 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     pdl_launch_dependents();
     // the list row: the KV head's, or with per-head lists the CTA's one head's
     const int lrow = a.per_head ? prob : bg;
-    int cnt = DENSE ? a.NB : a.sel_cnt[lrow];
-    cnt = max(0, min(cnt, a.NB));
+    // this sequence's own length (per-sequence lengths) and blocks
+    const int len = seq_len_of(a.seq_lens, b, a.len, a.dev_status);
+    const int NB = (len + kBlock - 1) / kBlock;
+    int cnt = DENSE ? NB : a.sel_cnt[lrow];
+    cnt = max(0, min(cnt, NB));
 
     const size_t row0 = static_cast<size_t>(bg) * a.max_seq;  // first token row of (b, g)
     WarpState<GC> st;
@@ -1115,7 +1121,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     if (i >= TL::kStages)
                         ok = mbar_wait(&empty[s], ((i / TL::kStages) - 1) & 1, abort_flag);
                     if (ok) {
-                        if (blk >= 0 && blk < a.NB) {
+                        if (blk >= 0 && blk < NB) {
                             stage_blk[s] = blk;
                             uint8_t *dst = smem + SL::kStagesOff + s * TL::kStageBytes;
                             const size_t r = row0 + static_cast<size_t>(blk) * kBlock;
@@ -1161,7 +1167,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         }
         if constexpr (TAIL) {
             if (ok)
-                ok = produce_tail<DT>(a, split, bg, cnt, list, i, full, empty, stage_blk,
+                ok = produce_tail<DT>(a, NB, split, bg, cnt, list, i, full, empty, stage_blk,
                                       stage_mask, smem + SL::kStagesOff, abort_flag, lane, pol);
         }
         const int issued = i;
@@ -1211,7 +1217,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     break;
                 }
                 if (blk >= 0) {
-                    const int n_valid = min(kBlock, a.len - blk * kBlock);
+                    const int n_valid = min(kBlock, len - blk * kBlock);
                     consume_q4<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
                                        coef, qr, pw, wg, lane, st, a.sv_eps);
                 }
@@ -1238,7 +1244,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     break;
                 }
                 if (blk >= 0) {
-                    const int n_valid = min(kBlock, a.len - blk * kBlock);
+                    const int n_valid = min(kBlock, len - blk * kBlock);
                     if constexpr (DT == KVD_INT8)
                         consume_int8<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes,
                                              n_valid, coef, qr, pw, wg, lane, st, a.sv_eps);
@@ -1269,7 +1275,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     break;
                 }
                 if (blk >= 0) {
-                    const int n_valid = min(kBlock, a.len - blk * kBlock);
+                    const int n_valid = min(kBlock, len - blk * kBlock);
                     consume_f16<GC, SV>(smem + SL::kStagesOff + s * TL::kStageBytes, n_valid,
                                         qr, pw, wg, lane, st, a.sv_eps);
                 }
@@ -1279,7 +1285,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         }
         if constexpr (TAIL) {
             if (at_tail)
-                tail_loop<DT, GC>(a, b, h0, i, full, empty, stage_blk, stage_mask,
+                tail_loop<DT, GC>(a, len, NB, b, h0, i, full, empty, stage_blk, stage_mask,
                                   smem + SL::kStagesOff, pw, wg, lane, abort_flag, ts);
         }
         // per-warp totals: l summed over the lanes of each head
@@ -1484,6 +1490,7 @@ DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan 
     a.nbmax = g.nbmax;
     a.len = g.len;
     a.NB = g.NB;
+    a.seq_lens = c.seq_lens;
     a.splits = p.splits;
     a.subgroups = p.subgroups;
     a.plan_blocks = p.blocks;

@@ -28,6 +28,18 @@ __global__ void __launch_bounds__(256) fill_kernel(int32_t *sel_idx, int32_t *se
     if (threadIdx.x == 0) sel_cnt[p] = se + n_take + (NB - rb);
 }
 
+// fill_kernel under per-sequence lengths: each problem's own forced blocks
+// and candidates (every candidate when k_sel reaches the longest sequence's
+// count, none when k_sel is 0).
+__global__ void __launch_bounds__(256) fill_kernel_varlen(SelArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int p = blockIdx.x;
+    SelArgs v;
+    const int take = problem_args(a, p, v);
+    fill_list(v, p, take >= 1, threadIdx.x, blockDim.x);  // one row per problem of the grid
+}
+
 template <int G, int MODE>
 cudaError_t launch_select_t(const SelArgs &a0, int P, cudaStream_t st, bool pdl) {
     constexpr int smem = select_smem_bytes<G>();
@@ -68,6 +80,18 @@ cudaError_t launch_select_any(const SelArgs &a, int G, int P, cudaStream_t st, b
     }
 }
 
+// The selection kernel for P problems, with per-sequence geometry on the
+// device when the cache carries sequence lengths; per_head: one query head
+// of each group (a.head_sub).
+cudaError_t launch_select_mode(const SelArgs &a, int G, int P, cudaStream_t st, bool pdl,
+                               bool per_head = false) {
+    if (per_head)  // G = 1 problems: one head at a time
+        return a.seq_lens ? launch_select_t<1, kSelect | kVarlen | kPerHead>(a, P, st, pdl)
+                          : launch_select_t<1, kSelect | kPerHead>(a, P, st, pdl);
+    return a.seq_lens ? launch_select_any<kSelect | kVarlen>(a, G, P, st, pdl)
+                      : launch_select_any<kSelect>(a, G, P, st, pdl);
+}
+
 SelArgs base_args(const kvd_cache &c, const Geom &g, const float *q) {
     SelArgs a = {};
     a.q = q;
@@ -79,6 +103,30 @@ SelArgs base_args(const kvd_cache &c, const Geom &g, const float *q) {
     a.dev_status = c.dev_status;
     a.head_sub = -1;
     a.G_all = g.G;
+    a.seq_lens = c.seq_lens;
+    a.len_max = g.len;
+    return a;
+}
+
+// The arguments of a ranking selection over the longest sequence's geometry.
+SelArgs rank_args(const kvd_cache &c, const Geom &g, const float *q, const ForcedRange &f,
+                  int k_sel, int sink_tokens, int recent_tokens, int32_t *sel_idx,
+                  int32_t *sel_cnt, const SelScratch &scr) {
+    SelArgs a = base_args(c, g, q);
+    a.se = f.se;
+    a.n = f.rb - f.se;
+    a.keys = scr.keys;
+    a.ldk = (a.n + 3) / 4 * 4;
+    a.ldn = a.ldk;
+    a.range = scr.range;
+    a.ticket = scr.ticket;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.rb = f.rb;
+    a.keff = k_sel < a.n ? k_sel : a.n;
+    a.k_sel = k_sel;
+    a.sink_tokens = sink_tokens;
+    a.recent_tokens = recent_tokens;
     return a;
 }
 
@@ -90,17 +138,8 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
                           int sink_tokens, int recent_tokens, int32_t *sel_idx,
                           int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st, bool pdl,
                           const StepToken *tok) {
-    const int NB = g.NB;
-    int se = (sink_tokens + kBlock - 1) / kBlock;
-    if (se > NB) se = NB;
-    int rb = NB;
-    if (recent_tokens > 0) {
-        long start = static_cast<long>(g.len) - recent_tokens;
-        if (start < 0) start = 0;
-        rb = static_cast<int>(start / kBlock);
-    }
-    if (rb < se) rb = se;
-    const int n_cand = rb - se;
+    const ForcedRange f = forced_range(g.len, sink_tokens, recent_tokens);
+    const int n_cand = f.rb - f.se;
     const int keff = k_sel < n_cand ? k_sel : n_cand;
     const int P = g.B * g.Hkv;
     // a decode step's token rides in the selection kernel when its block is
@@ -116,20 +155,13 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
         const cudaError_t e = launch_append(c0, tok->k_new, tok->v_new, 1, st, pdl);
         if (e != cudaSuccess) return e;
     }
-    if (!topk)
+    SelArgs a = rank_args(c, g, q, f, k_sel, sink_tokens, recent_tokens, sel_idx, sel_cnt, scr);
+    if (!topk) {
+        if (c.seq_lens)  // shorter sequences may still rank: the same rule per problem
+            return launch_ex(fill_kernel_varlen, dim3(P), dim3(256), 0, st, pdl, a);
         return launch_ex(fill_kernel, dim3(P), dim3(256), 0, st, pdl, sel_idx, sel_cnt, g.nbmax,
-                         NB, se, rb, keff > 0 ? 1 : 0);
-    SelArgs a = base_args(c, g, q);
-    a.se = se;
-    a.n = n_cand;
-    a.keys = scr.keys;
-    a.ldk = (n_cand + 3) / 4 * 4;
-    a.range = scr.range;
-    a.ticket = scr.ticket;
-    a.sel_idx = sel_idx;
-    a.sel_cnt = sel_cnt;
-    a.rb = rb;
-    a.keff = keff;
+                         f.NB, f.se, f.rb, keff > 0 ? 1 : 0);
+    }
     if (fuse) {
         a.app_cache = c;
         a.app_cache.len = tok->len0;
@@ -140,7 +172,7 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
     // the recent window is non-empty, so scoring may start before the
     // upstream kernels finish
     a.overlap = fuse ? 1 : 0;
-    return launch_select_any<kSelect>(a, g.G, P, st, pdl);
+    return launch_select_mode(a, g.G, P, st, pdl);
 }
 
 // Per-query-head selection: query head h of KV head g ranks the blocks by its
@@ -151,36 +183,24 @@ cudaError_t launch_select_per_head(const kvd_cache &c, const Geom &g, const floa
                                    int sink_tokens, int recent_tokens, int32_t *sel_idx,
                                    int32_t *sel_cnt, const SelScratch &scr, cudaStream_t st,
                                    bool pdl) {
-    const int NB = g.NB;
-    int se = (sink_tokens + kBlock - 1) / kBlock;
-    if (se > NB) se = NB;
-    int rb = NB;
-    if (recent_tokens > 0) {
-        long start = static_cast<long>(g.len) - recent_tokens;
-        if (start < 0) start = 0;
-        rb = static_cast<int>(start / kBlock);
-    }
-    if (rb < se) rb = se;
-    const int n_cand = rb - se;
+    const ForcedRange f = forced_range(g.len, sink_tokens, recent_tokens);
+    const int n_cand = f.rb - f.se;
     const int keff = k_sel < n_cand ? k_sel : n_cand;
     const int P = g.B * g.Hkv;
-    if (!(keff > 0 && keff < n_cand))  // nothing to rank: every head gets the same list
+    SelArgs a = rank_args(c, g, q, f, k_sel, sink_tokens, recent_tokens, sel_idx, sel_cnt, scr);
+    if (!(keff > 0 && keff < n_cand)) {  // nothing to rank: every head gets the same list
+        if (c.seq_lens) {
+            a.head_sub = 0;
+            a.G_all = 1;  // rows are (b, h) = problem index over B * H
+            a.Hkv = g.H;  // problem b * H + h belongs to sequence b
+            return launch_ex(fill_kernel_varlen, dim3(P * g.G), dim3(256), 0, st, pdl, a);
+        }
         return launch_ex(fill_kernel, dim3(P * g.G), dim3(256), 0, st, pdl, sel_idx, sel_cnt,
-                         g.nbmax, NB, se, rb, keff > 0 ? 1 : 0);
-    SelArgs a = base_args(c, g, q);
-    a.se = se;
-    a.n = n_cand;
-    a.keys = scr.keys;
-    a.ldk = (n_cand + 3) / 4 * 4;
-    a.range = scr.range;
-    a.ticket = scr.ticket;
-    a.sel_idx = sel_idx;
-    a.sel_cnt = sel_cnt;
-    a.rb = rb;
-    a.keff = keff;
+                         g.nbmax, f.NB, f.se, f.rb, keff > 0 ? 1 : 0);
+    }
     for (int sub = 0; sub < g.G; ++sub) {
         a.head_sub = sub;
-        const cudaError_t e = launch_select_any<kSelect>(a, 1, P, st, pdl);
+        const cudaError_t e = launch_select_mode(a, 1, P, st, pdl, true);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

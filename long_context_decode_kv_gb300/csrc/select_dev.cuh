@@ -69,7 +69,11 @@ static_assert(kRingKeys * 4 + kScratchBytes <= kScoreStages * kScoreStageBytes,
               "keys and tail scratch must fit the ring");
 
 enum TopkMode { kTakeNone = 0, kTakeAll = 1, kTakeTopK = 2 };
-enum SelMode { kExport = 0, kSelect = 1 };
+// Modes: kExport (bounds out), kSelect, and kSelect with the flags kVarlen
+// (per-sequence lengths: each problem's own candidates, forced blocks and
+// budget, found on the device) and kPerHead (one query head of each group per
+// launch, head_sub; problem p writes list row p * G_all + head_sub).
+enum SelMode { kExport = 0, kSelect = 1, kVarlen = 2, kPerHead = 4 };
 
 // ------------------------------------------------------ bound math ---
 // Scoring lane layout: 16 lanes per block; lane e (0..15) of a block holds
@@ -191,21 +195,18 @@ struct SelArgs {
     int NB, rb, keff;
     int32_t *dev_status;
     int overlap;
-    // per-query-head selection (an ablation of the GQA-shared one): this
-    // launch serves query head head_sub of every group of G_all heads, and
-    // problem p writes list row p * G_all + head_sub; head_sub < 0: shared
+    // per-query-head selection (kPerHead, an ablation of the GQA-shared one):
+    // this launch serves query head head_sub of every group of G_all heads
     int head_sub, G_all;
+    int ldn;  // keys of a problem's row its last CTA copies: n rounded up to 4
+    // per-sequence lengths (kVarlen): the rules the host applies to len
+    const int32_t *seq_lens;
+    int len_max, k_sel, sink_tokens, recent_tokens;
     // decode step: the token to append (app_k non-null), fused here because
     // its block is forced (never scored); app_cache.len is the length before
     kvd_cache app_cache;
     const __half *app_k, *app_v;
 };
-
-// The list row problem p writes.
-__device__ __forceinline__ size_t sel_row(const SelArgs &a, int p) {
-    return a.head_sub < 0 ? static_cast<size_t>(p)
-                          : static_cast<size_t>(p) * a.G_all + a.head_sub;
-}
 
 __device__ __forceinline__ int warp_inclusive_scan(int x, int lane) {
 #pragma unroll
@@ -329,7 +330,7 @@ __device__ __forceinline__ void count_digits(const uint32_t *keys, int n, uint32
 // Phase 4: the ascending list from the bitmaps of the keys above T (gtw)
 // and equal to T (eqw; the need_eq lowest-index ones are taken), plus the
 // forced sink and recent blocks, and the count.
-__device__ __forceinline__ void select_write_list(const SelArgs &a, int p, int n,
+__device__ __forceinline__ void select_write_list(const SelArgs &a, size_t row, int n,
                                                   const uint32_t *gtw, const uint32_t *eqw,
                                                   int need_eq, RadixShared &rs) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -347,7 +348,7 @@ __device__ __forceinline__ void select_write_list(const SelArgs &a, int p, int n
     unsigned before = incl - mine;
     for (int w = 0; w < warp; ++w) before += static_cast<unsigned>(rs.wsum[w]);
     int g_before = static_cast<int>(before & 0xffffu), e_before = static_cast<int>(before >> 16);
-    int32_t *dst = a.sel_idx + sel_row(a, p) * a.nbmax;
+    int32_t *dst = a.sel_idx + row * a.nbmax;
     for (int wi = w0; wi < w1; ++wi) {
         const uint32_t gm = gtw[wi], em = eqw[wi];
         uint32_t take = gm;
@@ -363,7 +364,7 @@ __device__ __forceinline__ void select_write_list(const SelArgs &a, int p, int n
     }
     for (int j = tid; j < a.se; j += kScoreThreads) dst[j] = j;
     for (int j = a.rb + tid; j < a.NB; j += kScoreThreads) dst[a.se + a.keff + (j - a.rb)] = j;
-    if (tid == 0) a.sel_cnt[sel_row(a, p)] = a.se + a.keff + (a.NB - a.rb);
+    if (tid == 0) a.sel_cnt[row] = a.se + a.keff + (a.NB - a.rb);
 }
 
 // Phases 3-4 of the last CTA of a problem, with the problem's key range
@@ -372,7 +373,7 @@ __device__ __forceinline__ void select_write_list(const SelArgs &a, int p, int n
 // memory when IN_SMEM, else global); scratch: kScratchBytes of shared memory
 // whose histogram part is zero.
 template <bool IN_SMEM>
-__device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n,
+__device__ __forceinline__ void select_finish(const SelArgs &a, size_t row, int n,
                                               const uint32_t *ksrc, uint8_t *scratch,
                                               RadixShared &rs) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -465,7 +466,7 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n,
             if (lane == 0 && beats < krem) atomicOr(&gtw[jc >> 5], 1u << (jc & 31));
         }
         __syncthreads();
-        select_write_list(a, p, n, gtw, eqw, 0, rs);
+        select_write_list(a, row, n, gtw, eqw, 0, rs);
         return;
     }
 
@@ -518,7 +519,7 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, int p, int n,
     __syncthreads();
 
     // ================================================= phase 4: the list
-    select_write_list(a, p, n, gtw, eqw, need_eq, rs);
+    select_write_list(a, row, n, gtw, eqw, need_eq, rs);
 }
 
 // Out of line: code the common path does not run stays off its instruction
@@ -538,10 +539,93 @@ __device__ __noinline__ void fused_append(const SelArgs &a, int b, int g, int la
 }
 
 // The tail of a problem too large for its keys to fit the ring.
-__device__ __noinline__ void select_finish_from_l2(const SelArgs &a, int p, int n,
+__device__ __noinline__ void select_finish_from_l2(const SelArgs &a, size_t row, int n,
                                                    const uint32_t *keys, uint8_t *scratch,
                                                    RadixShared &rs) {
-    select_finish<false>(a, p, n, keys, scratch, rs);
+    select_finish<false>(a, row, n, keys, scratch, rs);
+}
+
+// Phases 3-4 by the last CTA of problem p: the problem's keys into the ring
+// (when they fit), the key range, then the radix select and the list.
+__device__ __forceinline__ void select_rank(const SelArgs &a, int p, size_t row, int n, int X,
+                                            const uint32_t *kp, bool in_smem, uint8_t *ring,
+                                            RadixShared &rs, int &s_abort) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int *abort_flag = &s_abort;
+    if (in_smem && warp == kScoreWarps) {
+        // the problem's keys (L2-resident) into the ring by bulk copies; they
+        // were written by ordinary stores, so order those before the async proxy
+        const uint32_t bytes = static_cast<uint32_t>(a.ldn) * 4u;
+        const uint32_t off = static_cast<uint32_t>(lane) * kScoreStageBytes;
+        asm volatile("fence.proxy.async;" ::: "memory");
+        if (lane == 0) mbar_arrive_expect_tx(&rs.kbar, bytes);
+        __syncwarp();
+        if (off < bytes)
+            tma_load_1d(ring + off, reinterpret_cast<const uint8_t *>(kp) + off,
+                        min(static_cast<uint32_t>(kScoreStageBytes), bytes - off), &rs.kbar,
+                        l2_policy_evict_first());
+    }
+    // tail scratch: the ring past the keys (the histogram part zeroed)
+    uint8_t *scratch = ring + (in_smem ? kRingKeys * 4 : 0);
+    {
+        int4 *h4 = reinterpret_cast<int4 *>(scratch);
+        for (int i = tid; i < kBins1 / 4; i += kScoreThreads) h4[i] = make_int4(0, 0, 0, 0);
+    }
+    if (X > 1 && tid == 0) {
+        unsigned *rg = a.range + 2 * static_cast<size_t>(p);
+        rs.kmax = __ldcg(rg);
+        rs.kmin = ~__ldcg(rg + 1);
+        __stcg(rg, 0u);  // leave the words ready for the next call
+        __stcg(rg + 1, 0u);
+        a.ticket[p] = 0u;
+    }
+
+    // ================================================= phase 3: T
+    if (in_smem && !mbar_wait(&rs.kbar, 0, abort_flag)) s_abort = 1;
+    // the row's padding keys (up to 3 past n) read as kmin: bin 0, taken back out
+    if (in_smem && tid < a.ldn - n && !s_abort)
+        reinterpret_cast<uint32_t *>(ring)[n + tid] = rs.kmin;
+    if (__syncthreads_or(s_abort)) {
+        if (tid == 0) {
+            report_status(a.dev_status, KVD_ERR_TIMEOUT);
+            a.sel_cnt[row] = 0;
+            volatile int never = 0;
+            if (in_smem) (void)mbar_wait(&rs.kbar, 0, &never);  // copies in flight
+        }
+        return;
+    }
+    // the rest reads the keys from shared memory, or from L2 for a problem too
+    // large for the ring; each variant is compiled with its address space known
+    if (in_smem)
+        select_finish<true>(a, row, n, reinterpret_cast<const uint32_t *>(ring), scratch, rs);
+    else
+        select_finish_from_l2(a, row, n, kp, scratch, rs);
+}
+
+// Problem p's own selection geometry under per-sequence lengths.  take: 0
+// ranks nothing beyond the forced blocks, 1 takes every candidate, 2 ranks.
+__device__ __forceinline__ int problem_args(const SelArgs &a, int p, SelArgs &v) {
+    v = a;
+    const int L = seq_len_of(a.seq_lens, p / a.Hkv, a.len_max, a.dev_status);
+    const ForcedRange f = forced_range(L, a.sink_tokens, a.recent_tokens);
+    v.NB = f.NB;
+    v.se = f.se;
+    v.rb = f.rb;
+    v.n = f.rb - f.se;
+    v.keff = a.k_sel < v.n ? a.k_sel : v.n;
+    v.ldn = (v.n + 3) / 4 * 4;
+    return v.keff == 0 ? 0 : v.keff == v.n ? 1 : 2;
+}
+
+// The list of a problem that ranks nothing: sink blocks, every candidate when
+// take_all, recent blocks; threads tid of nthr.
+__device__ __forceinline__ void fill_list(const SelArgs &v, size_t row, bool take_all, int tid,
+                                          int nthr) {
+    int32_t *dst = v.sel_idx + row * v.nbmax;
+    const int n_take = take_all ? v.rb - v.se : 0;
+    for (int j = tid; j < v.se + n_take; j += nthr) dst[j] = j;
+    for (int j = v.rb + tid; j < v.NB; j += nthr) dst[v.se + n_take + (j - v.rb)] = j;
+    if (tid == 0) v.sel_cnt[row] = v.se + n_take + (v.NB - v.rb);
 }
 
 // CTA (x, p): candidate blocks j in [x*R, min(n, (x+1)*R)) of problem p,
@@ -549,8 +633,17 @@ __device__ __noinline__ void select_finish_from_l2(const SelArgs &a, int p, int 
 // of 64 blocks; warp 16 produces, warps 0..15 consume, warp w scoring blocks
 // 4w..4w+3 of each stage two at a time).
 template <int G, int MODE>
-__device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, uint8_t *smem,
+__device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p, uint8_t *smem,
                             SelShared &ss) {
+    // per-sequence lengths: this problem's own geometry (a copy of the args)
+    constexpr bool kVar = (MODE & kVarlen) != 0, kOneHead = (MODE & kPerHead) != 0;
+    SelArgs av;
+    int take = 2;
+    if constexpr (kVar) take = problem_args(a_in, p, av);
+    const SelArgs &a = kVar ? av : a_in;
+    // the list row this problem writes
+    const size_t row = kOneHead ? static_cast<size_t>(p) * a_in.G_all + a_in.head_sub
+                                : static_cast<size_t>(p);
     constexpr int NH = G < 4 ? G : 4;
     RadixShared &rs = ss.rs;
     int &s_abort = ss.abort;
@@ -587,6 +680,12 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
     // then comes before anything shared with earlier kernels is written.
     if (!a.overlap) pdl_wait();
     pdl_launch_dependents();
+    if constexpr (kVar) {
+        if (take < 2) {  // nothing to rank in this sequence: the first CTA fills
+            if (x_tile == 0) fill_list(a, row, take == 1, tid, kScoreThreads);
+            return;
+        }
+    }
 
     // ================================================= phase 1: keys
     const size_t base = static_cast<size_t>(p) * a.nbmax + a.se;  // row of candidate 0
@@ -614,8 +713,8 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
         }
     } else {
         // the producer's first copies are in flight while the query loads
-        const size_t h0 = a.head_sub < 0 ? static_cast<size_t>(g) * G
-                                         : static_cast<size_t>(g) * a.G_all + a.head_sub;
+        const size_t h0 = kOneHead ? static_cast<size_t>(g) * a.G_all + a.head_sub
+                                   : static_cast<size_t>(g) * G;
         const float *qg = a.q + (static_cast<size_t>(b) * a.H + h0) * kHeadDim;
         for (int i = tid; i < G * kHeadDim; i += kConsumerThreads) q_s[i] = qg[i];
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
@@ -662,7 +761,7 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
 #pragma unroll
             for (int ps = 0; ps < 2; ++ps) {
                 if (jr[ps] < j1 && e == 0) {
-                    if constexpr (MODE == kSelect) {
+                    if constexpr (MODE != kExport) {
                         const uint32_t key = float_to_key(sc[ps]);
                         a.keys[static_cast<size_t>(p) * a.ldk + jr[ps]] = key;
                         tmin = min(tmin, key);
@@ -673,7 +772,7 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
                 }
             }
         }
-        if constexpr (MODE == kSelect) {
+        if constexpr (MODE != kExport) {
             tmin = __reduce_min_sync(kFullMask, tmin);
             tmax = __reduce_max_sync(kFullMask, tmax);
             if (lane == 0) {
@@ -719,63 +818,13 @@ __device__ void select_body(const SelArgs &a, int x_tile, int n_tiles, int p, ui
             rs.last = atomic_add_acq_rel_gpu(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
         }
         __syncthreads();
-        if (!rs.last) {
-            if (appends) fused_append(a, b, g, lane);
-            return;
-        }
     }
-    // the last CTA of the problem: every key is in
-    if (in_smem && warp == kScoreWarps) {
-        // the problem's keys (L2-resident) into the ring by bulk copies; they
-        // were written by ordinary stores, so order those before the async proxy
-        const uint32_t bytes = static_cast<uint32_t>(a.ldk) * 4u;
-        const uint32_t off = static_cast<uint32_t>(lane) * kScoreStageBytes;
-        asm volatile("fence.proxy.async;" ::: "memory");
-        if (lane == 0) mbar_arrive_expect_tx(&rs.kbar, bytes);
-        __syncwarp();
-        if (off < bytes)
-            tma_load_1d(ring + off, reinterpret_cast<const uint8_t *>(kp) + off,
-                        min(static_cast<uint32_t>(kScoreStageBytes), bytes - off), &rs.kbar,
-                        l2_policy_evict_first());
-    }
-    // tail scratch: the ring past the keys (the histogram part zeroed)
-    uint8_t *scratch = ring + (in_smem ? kRingKeys * 4 : 0);
-    {
-        int4 *h4 = reinterpret_cast<int4 *>(scratch);
-        for (int i = tid; i < kBins1 / 4; i += kScoreThreads) h4[i] = make_int4(0, 0, 0, 0);
-    }
-    if (X > 1 && tid == 0) {
-        unsigned *rg = a.range + 2 * static_cast<size_t>(p);
-        rs.kmax = __ldcg(rg);
-        rs.kmin = ~__ldcg(rg + 1);
-        __stcg(rg, 0u);  // leave the words ready for the next call
-        __stcg(rg + 1, 0u);
-        a.ticket[p] = 0u;
-    }
-
-    // ================================================= phase 3: T
-    if (in_smem && !mbar_wait(&rs.kbar, 0, abort_flag)) s_abort = 1;
-    // the row's padding keys (up to 3 past n) read as kmin: bin 0, taken back out
-    if (in_smem && tid < a.ldk - n && !s_abort)
-        reinterpret_cast<uint32_t *>(ring)[n + tid] = rs.kmin;
-    if (__syncthreads_or(s_abort)) {
-        if (tid == 0) {
-            report_status(a.dev_status, KVD_ERR_TIMEOUT);
-            a.sel_cnt[sel_row(a, p)] = 0;
-            volatile int never = 0;
-            if (in_smem) (void)mbar_wait(&rs.kbar, 0, &never);  // copies in flight
-        }
-        if (appends) fused_append(a, b, g, lane);
-        return;
-    }
-    // the rest reads the keys from shared memory, or from L2 for a problem too
-    // large for the ring; each variant is compiled with its address space known
-    if (in_smem)
-        select_finish<true>(a, p, n, reinterpret_cast<const uint32_t *>(ring), scratch, rs);
-    else
-        select_finish_from_l2(a, p, n, kp, scratch, rs);
+    // the last CTA of the problem (every key is in) ranks; the step's token is
+    // appended on one path out of every CTA
+    if (X == 1 || rs.last) select_rank(a, p, row, n, X, kp, in_smem, ring, rs, s_abort);
     if (appends) fused_append(a, b, g, lane);
 }
+
 
 template <int G>
 constexpr int select_smem_bytes() {
