@@ -48,6 +48,9 @@ constexpr int kScoreStageBytes = kStageBlocks * kBoundRowBytes;  // 32 KiB
 
 constexpr int kMaxSelectBlocks = 49152;
 constexpr int kMaxCtasPerProblem = 1024;
+// Problems of at most this many candidates are scored and ranked by one CTA
+// (select_small): no ticket, no key copy, no radix passes.
+constexpr int kSmallRank = 512;
 
 // Radix select over v = key - kmin: the first digit is v >> shift with
 // shift the least that leaves at most kBins1 bins; later digits take up to
@@ -545,6 +548,46 @@ __device__ __noinline__ void select_finish_from_l2(const SelArgs &a, size_t row,
     select_finish<false>(a, row, n, keys, scratch, rs);
 }
 
+// Exclusive count, over the CTA's threads in order, of flag (all threads
+// call; wsum: kScoreWarps + 1 ints of shared memory).
+__device__ __forceinline__ int block_exclusive_count(bool flag, int *wsum) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned m = __ballot_sync(kFullMask, flag);
+    if (lane == 0) wsum[warp] = __popc(m);
+    __syncthreads();
+    int before = __popc(m & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    __syncthreads();  // wsum free for the next call
+    return before;
+}
+
+// The list of a problem of n <= kSmallRank candidates whose keys (row kp)
+// this CTA wrote itself: thread t holds key t.  The keff-th largest key T is
+// built bit by bit from block-wide counts (count(key >= T | bit) >= keff
+// keeps the bit); keys above T are in, and of the keys equal to T the
+// lowest indices fill the rest.  All threads call.
+__device__ __forceinline__ void select_small(const SelArgs &a, size_t row, int n,
+                                             const uint32_t *kp, int *wsum) {
+    const int tid = threadIdx.x;
+    const bool have = tid < n;
+    const uint32_t key = have ? kp[tid] : 0u;
+    uint32_t T = 0u;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t c = T | (1u << bit);
+        if (__syncthreads_count(have && key >= c) >= a.keff) T = c;
+    }
+    const int n_gt = __syncthreads_count(have && key > T);
+    const bool eq = have && key == T;
+    const int eq_before = block_exclusive_count(eq, wsum);
+    const bool in = have && (key > T || (eq && eq_before < a.keff - n_gt));
+    const int pos = block_exclusive_count(in, wsum);
+    int32_t *dst = a.sel_idx + row * a.nbmax;
+    if (in) dst[a.se + pos] = a.se + tid;
+    for (int j = tid; j < a.se; j += kScoreThreads) dst[j] = j;
+    for (int j = a.rb + tid; j < a.NB; j += kScoreThreads) dst[a.se + a.keff + (j - a.rb)] = j;
+    if (tid == 0) a.sel_cnt[row] = a.se + a.keff + (a.NB - a.rb);
+}
+
 // Phases 3-4 by the last CTA of problem p: the problem's keys into the ring
 // (when they fit), the key range, then the radix select and the list.
 __device__ __forceinline__ void select_rank(const SelArgs &a, int p, size_t row, int n, int X,
@@ -821,7 +864,12 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
     }
     // the last CTA of the problem (every key is in) ranks; the step's token is
     // appended on one path out of every CTA
-    if (X == 1 || rs.last) select_rank(a, p, row, n, X, kp, in_smem, ring, rs, s_abort);
+    if (X == 1 && n <= kSmallRank) {
+        __syncthreads();  // this CTA's key stores are visible to all its threads
+        select_small(a, row, n, kp, rs.wsum);
+    } else if (X == 1 || rs.last) {
+        select_rank(a, p, row, n, X, kp, in_smem, ring, rs, s_abort);
+    }
     if (appends) fused_append(a, b, g, lane);
 }
 

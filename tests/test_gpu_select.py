@@ -50,6 +50,11 @@ CASES = [
     (5000, 17, 4, 256),
     (5000, 60, 0, 1),
     (20000, 77, 128, 640),
+    # at most 512 candidates rank in one CTA; more go through the radix tail
+    (32768, 100, 0, 0),     # 512 candidates
+    (32769, 100, 0, 0),     # 513
+    (40000, 300, 4, 256),
+    (70000, 9, 0, 0),
 ]
 
 
@@ -70,12 +75,13 @@ def test_select_matches_oracle(L, k_sel, sink, recent, G):
     assert np.all(sel_cnt.cpu().numpy() == kvd.selected_count(L, k_sel, sink, recent))
 
 
-def test_exact_ties_go_to_lower_index():
+@pytest.mark.parametrize("nb", [40, 600])
+def test_exact_ties_go_to_lower_index(nb):
     # every block identical => every bound equal (bit-identical f32 sums):
-    # the top-K must be the lowest-index candidates
-    B, Hkv, L, G = 1, 2, 64 * 40, 4
+    # the top-K must be the lowest-index candidates (one-CTA and radix paths)
+    B, Hkv, L, G = 1, 2, 64 * nb, 4
     row = seeded((1, 64, Hkv, 128), 5)
-    k = row.repeat(1, 40, 1, 1).contiguous()
+    k = row.repeat(1, nb, 1, 1).contiguous()
     v = seeded((B, L, Hkv, 128), 6)
     gc, oc = make_pair(kvd.F16, k, v)
     q = _q(B, Hkv * G, 7)
@@ -85,7 +91,7 @@ def test_exact_ties_go_to_lower_index():
     kvd.select_blocks(gc, q, 5, 1, 64, sel_idx, sel_cnt, ws)
     torch.cuda.synchronize()
     for g in range(Hkv):
-        assert sel_idx[0, g, :sel_cnt[0, g]].cpu().tolist() == [0, 1, 2, 3, 4, 5, 39]
+        assert sel_idx[0, g, :sel_cnt[0, g]].cpu().tolist() == [0, 1, 2, 3, 4, 5, nb - 1]
 
 
 def test_needle_blocks_survive_selection():
