@@ -60,7 +60,7 @@ cudaError_t launch_select_t(const SelArgs &a0, int P, cudaStream_t st, bool pdl)
     const long cap = static_cast<long>(occupancy) * device_sm_count();
     long X = cap / P;
     if (X > kMaxCtasPerProblem) X = kMaxCtasPerProblem;
-    if (X < 1 || (MODE != kExport && a.n <= kSmallRank)) X = 1;  // one CTA ranks alone
+    if (X < 1) X = 1;
     long R = (static_cast<long>(a.n) + X - 1) / X;
     X = (a.n + R - 1) / R;
     a.R = static_cast<int>(R);

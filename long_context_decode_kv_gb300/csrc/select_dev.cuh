@@ -48,8 +48,8 @@ constexpr int kScoreStageBytes = kStageBlocks * kBoundRowBytes;  // 32 KiB
 
 constexpr int kMaxSelectBlocks = 49152;
 constexpr int kMaxCtasPerProblem = 1024;
-// Problems of at most this many candidates are scored and ranked by one CTA
-// (select_small): no ticket, no key copy, no radix passes.
+// The last CTA of a problem of at most this many candidates ranks them one
+// key per thread (select_small): no key copy, no radix passes.
 constexpr int kSmallRank = 512;
 
 // Radix select over v = key - kmin: the first digit is v >> shift with
@@ -561,8 +561,8 @@ __device__ __forceinline__ int block_exclusive_count(bool flag, int *wsum) {
     return before;
 }
 
-// The list of a problem of n <= kSmallRank candidates whose keys (row kp)
-// this CTA wrote itself: thread t holds key t.  The keff-th largest key T is
+// The list of a problem of n <= kSmallRank candidates, by its last CTA once
+// every key of row kp is in: thread t holds key t.  The keff-th largest key T is
 // built bit by bit from block-wide counts (count(key >= T | bit) >= keff
 // keeps the bit); keys above T are in, and of the keys equal to T the
 // lowest indices fill the rest.  All threads call.
@@ -570,7 +570,7 @@ __device__ __forceinline__ void select_small(const SelArgs &a, size_t row, int n
                                              const uint32_t *kp, int *wsum) {
     const int tid = threadIdx.x;
     const bool have = tid < n;
-    const uint32_t key = have ? kp[tid] : 0u;
+    const uint32_t key = have ? __ldcg(kp + tid) : 0u;
     uint32_t T = 0u;
     for (int bit = 31; bit >= 0; --bit) {
         const uint32_t c = T | (1u << bit);
@@ -855,20 +855,25 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
         // zero-based maxima), then the ticket; its release covers the keys
         __syncthreads();
         if (tid == 0) {
-            unsigned *rg = a.range + 2 * static_cast<size_t>(p);
-            atomicMax(rg, rs.kmax);
-            atomicMax(rg + 1, ~rs.kmin);
+            if (n > kSmallRank) {  // the radix tail bins over the keys' range
+                unsigned *rg = a.range + 2 * static_cast<size_t>(p);
+                atomicMax(rg, rs.kmax);
+                atomicMax(rg + 1, ~rs.kmin);
+            }
             rs.last = atomic_add_acq_rel_gpu(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
         }
         __syncthreads();
     }
     // the last CTA of the problem (every key is in) ranks; the step's token is
     // appended on one path out of every CTA
-    if (X == 1 && n <= kSmallRank) {
-        __syncthreads();  // this CTA's key stores are visible to all its threads
-        select_small(a, row, n, kp, rs.wsum);
-    } else if (X == 1 || rs.last) {
-        select_rank(a, p, row, n, X, kp, in_smem, ring, rs, s_abort);
+    if (X == 1 || rs.last) {
+        if (n <= kSmallRank) {
+            __syncthreads();  // (X == 1) this CTA's key stores, seen by all its threads
+            if (X > 1 && tid == 0) a.ticket[p] = 0u;  // ready for the next call
+            select_small(a, row, n, kp, rs.wsum);
+        } else {
+            select_rank(a, p, row, n, X, kp, in_smem, ring, rs, s_abort);
+        }
     }
     if (appends) fused_append(a, b, g, lane);
 }
