@@ -114,8 +114,9 @@ typedef enum { KVD_F16 = 0, KVD_INT8 = 1, KVD_Q8_0 = 2, KVD_Q4_0 = 3 } kvd_kv_dt
  * never writes it), the selection ranks blocks below ceil(seq_lens[b] / block)
  * with the recent window ending at seq_lens[b], and the decode calls attend
  * tokens below seq_lens[b] (a sequence of length 0 gets a zero output).
- * kvd_decode_step, kvd_decode_step_host and kvd_debug_scores do not take it
- * (UNSUPPORTED).
+ * kvd_decode_step appends sequence b's token at seq_lens[b] and then selects
+ * and attends over its seq_lens[b] + 1 tokens (the caller adds 1 to seq_lens
+ * after the step).  kvd_debug_scores does not take it (UNSUPPORTED).
  */
 typedef struct kvd_cache {
     int32_t dtype;        /* kvd_kv_dtype */

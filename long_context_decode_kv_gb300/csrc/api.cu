@@ -81,6 +81,7 @@ Geom make_geom(const kvd_cache *c, int n_heads, int len) {
     g.G = n_heads / c->n_kv_heads;
     g.NB = (len + kBlock - 1) / kBlock;
     g.nbmax = c->max_seq / kBlock;
+    g.seq_add = 0;
     return g;
 }
 
@@ -170,7 +171,8 @@ SelScratch sel_scratch(void *ws, const WsLayout &w) {
 kvd_status select_impl(const kvd_cache *c, const float *q, int n_heads, int k_sel, int sink,
                        int recent, int32_t *sel_idx, int32_t *sel_cnt, void *ws,
                        const WsLayout &w, cudaStream_t st, const StepToken *tok = nullptr) {
-    const Geom g = make_geom(c, n_heads, c->len);
+    Geom g = make_geom(c, n_heads, c->len);
+    g.seq_add = tok ? 1 : 0;  // a step's token: seq_lens does not count it yet
     const SelScratch scr = sel_scratch(ws, w);
     return cuda_status(launch_select(*c, g, q, k_sel, sink, recent, sel_idx, sel_cnt, scr, st,
                                      true, tok));
@@ -180,7 +182,8 @@ kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float sc
                        const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel, float *out,
                        void *ws, const WsLayout &w, cudaStream_t st, bool in_step = false,
                        float sv_eps = 0.0f) {
-    const Geom g = make_geom(c, n_heads, c->len);
+    Geom g = make_geom(c, n_heads, c->len);
+    g.seq_add = in_step ? 1 : 0;  // the step's token: seq_lens does not count it yet
     const bool dense = sel_idx == nullptr;
     int max_blocks = dense ? g.NB : max_sel;
     if (max_blocks > g.NB) max_blocks = g.NB;
@@ -431,7 +434,6 @@ kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
-    if (cache->seq_lens) return KVD_ERR_UNSUPPORTED;  // one length per cache in a step
     if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
     if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVD_ERR_INVALID;
     if (cache->len + 1 > cache->max_seq) return KVD_ERR_CAPACITY;
@@ -501,7 +503,6 @@ kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host, const voi
                                 void *workspace, size_t workspace_bytes, void *stream) {
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
-    if (cache->seq_lens) return KVD_ERR_UNSUPPORTED;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
     if (!q_host || !k_new_host || !v_new_host || !out_host) return KVD_ERR_INVALID;
     const WsLayout w = ws_layout(cache, n_heads);

@@ -117,6 +117,7 @@ struct DecodeArgs {
     int early_q;       // q is complete before the upstream kernels finish
     int per_head;      // lists per query head ([B, H] rows; one head per CTA)
     const int32_t *seq_lens;  // per-sequence lengths (<= len), or null
+    int seq_add;              // tokens appended by this step that seq_lens lacks
 };
 
 template <int DT, int GC, bool TAIL = false>
@@ -1076,7 +1077,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     // the list row: the KV head's, or with per-head lists the CTA's one head's
     const int lrow = a.per_head ? prob : bg;
     // this sequence's own length (per-sequence lengths) and blocks
-    const int len = seq_len_of(a.seq_lens, b, a.len, a.dev_status);
+    const int len = seq_len_of(a.seq_lens, b, a.len - a.seq_add, a.dev_status) + a.seq_add;
     const int NB = (len + kBlock - 1) / kBlock;
     int cnt = DENSE ? NB : a.sel_cnt[lrow];
     cnt = max(0, min(cnt, NB));
@@ -1491,6 +1492,7 @@ DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan 
     a.len = g.len;
     a.NB = g.NB;
     a.seq_lens = c.seq_lens;
+    a.seq_add = g.seq_add;
     a.splits = p.splits;
     a.subgroups = p.subgroups;
     a.plan_blocks = p.blocks;

@@ -18,6 +18,7 @@ struct Geom {
     int H, G;                         // query heads, group size
     int NB;                           // ceil(len / 64)
     int nbmax;                        // max_seq / 64
+    int seq_add;  // tokens a decode step appended that the caller's seq_lens lacks
 };
 
 // Decode split plan: grid = (splits, B * Hkv * subgroups).  Split s attends

@@ -105,6 +105,7 @@ SelArgs base_args(const kvd_cache &c, const Geom &g, const float *q) {
     a.G_all = g.G;
     a.seq_lens = c.seq_lens;
     a.len_max = g.len;
+    a.seq_add = g.seq_add;
     return a;
 }
 
@@ -148,7 +149,9 @@ cudaError_t launch_select(const kvd_cache &c, const Geom &g, const float *q, int
     const bool topk = keff > 0 && keff < n_cand;
     // the fused append writes rows and bounds only: a cache that keeps block
     // means appends through the append kernel, which recomputes them
-    const bool fuse = tok && topk && recent_tokens > 0 && c.moments == nullptr;
+    // with per-sequence lengths some problems may rank nothing (filled without
+    // the fused path), so their tokens are appended by the append kernel too
+    const bool fuse = tok && topk && recent_tokens > 0 && c.moments == nullptr && !c.seq_lens;
     if (tok && !fuse) {
         kvd_cache c0 = c;
         c0.len = tok->len0;

@@ -205,6 +205,7 @@ struct SelArgs {
     // per-sequence lengths (kVarlen): the rules the host applies to len
     const int32_t *seq_lens;
     int len_max, k_sel, sink_tokens, recent_tokens;
+    int seq_add;  // tokens a decode step appended that seq_lens lacks
     // decode step: the token to append (app_k non-null), fused here because
     // its block is forced (never scored); app_cache.len is the length before
     kvd_cache app_cache;
@@ -649,7 +650,8 @@ __device__ __forceinline__ void select_rank(const SelArgs &a, int p, size_t row,
 // ranks nothing beyond the forced blocks, 1 takes every candidate, 2 ranks.
 __device__ __forceinline__ int problem_args(const SelArgs &a, int p, SelArgs &v) {
     v = a;
-    const int L = seq_len_of(a.seq_lens, p / a.Hkv, a.len_max, a.dev_status);
+    const int L =
+        seq_len_of(a.seq_lens, p / a.Hkv, a.len_max - a.seq_add, a.dev_status) + a.seq_add;
     const ForcedRange f = forced_range(L, a.sink_tokens, a.recent_tokens);
     v.NB = f.NB;
     v.se = f.se;

@@ -64,6 +64,7 @@ kvd_status check_args(const kvd_cache *c, const float *q, int n_heads, const int
                                  !aligned_to(c->v_scale, 16)))
         return KVD_ERR_INVALID;
     if (c->dev_status && !aligned_to(c->dev_status, 4)) return KVD_ERR_INVALID;
+    if (c->seq_lens && !aligned_to(c->seq_lens, 4)) return KVD_ERR_INVALID;
     if (static_cast<long long>(c->batch) * c->n_kv_heads * 16 > 65535) return KVD_ERR_UNSUPPORTED;
     if (n_heads < 1 || n_heads % c->n_kv_heads != 0) return KVD_ERR_INVALID;
     const int G = n_heads / c->n_kv_heads;
@@ -97,6 +98,7 @@ extern "C" kvd_status kvd_decode_attn_static(const kvd_cache *cache, const float
     g.G = n_heads / cache->n_kv_heads;
     g.NB = (cache->len + kBlock - 1) / kBlock;
     g.nbmax = cache->max_seq / kBlock;
+    g.seq_add = 0;
     int max_blocks = max_sel < g.NB ? max_sel : g.NB;
     if (max_blocks < 1) max_blocks = 1;
     const DecodePlan p = plan_decode(g, max_blocks, device_sm_count());

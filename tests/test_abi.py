@@ -163,8 +163,8 @@ def test_decode_tail_validation():
     assert pd(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, None, n, None) == WORKSPACE
     # per-sequence lengths: aligned, and not taken by the whole-step calls
     assert _select(_cache(seq_lens=FAKE + 2)) == INVALID
-    assert L.kvd_decode_step(C.byref(_cache(seq_lens=FAKE)), FAKE, FAKE, FAKE, 32, 0.1, 4, 4,
-                             64, None, None, FAKE, FAKE, n, None) == UNSUPPORTED
+    assert L.kvd_decode_step(C.byref(_cache(seq_lens=FAKE + 2)), FAKE, FAKE, FAKE, 32, 0.1, 4,
+                             4, 64, None, None, FAKE, FAKE, n, None) == INVALID
     assert L.kvd_debug_scores(C.byref(_cache(seq_lens=FAKE)), FAKE, 32, FAKE,
                               None) == UNSUPPORTED
     # a cache that keeps moments is otherwise an ordinary cache

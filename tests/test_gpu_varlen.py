@@ -185,3 +185,39 @@ def test_lengths_past_len_are_reported():
     kvd.decode_attn_dense(gc, q, scale_for(), out, ws)
     torch.cuda.synchronize()
     assert kvd.STATUS[gc.device_status()] == "KVD_ERR_INVALID"
+
+
+@pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8])
+@pytest.mark.parametrize("k_sel", [4, -1])
+def test_varlen_decode_steps(dtype, k_sel):
+    # kvd_decode_step appends each sequence's token at its own length and
+    # attends that length + 1; the caller then advances the lengths
+    Hkv, G = 2, 4
+    lens = [70, 1000, 0, 2389, 63]
+    gc, ocs, _, lens_t = _build(dtype, lens, Hkv, G, 800)
+    B = len(lens)
+    ws = kvd.make_workspace(gc, Hkv * G)
+    nbmax = gc.max_seq // 64
+    sel_idx = torch.zeros((B, Hkv, nbmax), dtype=torch.int32, device=dev())
+    sel_cnt = torch.zeros((B, Hkv), dtype=torch.int32, device=dev())
+    out = torch.empty((B, Hkv * G, 128), device=dev())
+    for step in range(3):
+        q = seeded((B, Hkv * G, 128), 810 + step, scale=2.0, dtype=torch.float32)
+        kn = seeded((B, 1, Hkv, 128), 820 + step)
+        vn = seeded((B, 1, Hkv, 128), 830 + step)
+        kvd.decode_step(gc, q, kn, vn, scale_for(), k_sel, 4, 64, out, ws, sel_idx, sel_cnt)
+        lens_t += 1
+        torch.cuda.synchronize()
+        assert gc.device_status() == 0
+        q_np = q.cpu().numpy()
+        idx, cnt = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
+        for b, oc in enumerate(ocs):
+            oc.append(kn[b:b + 1].cpu().numpy(), vn[b:b + 1].cpu().numpy())
+            for g in range(Hkv):
+                sel = None if k_sel < 0 else idx[b, g, :cnt[b, g]]
+                ref = np.stack([_oracle_head(dtype, oc, q_np[b, g * G + h], g, sel)
+                                for h in range(G)])
+                assert_outputs(out[b, g * G:(g + 1) * G], ref, dtype, f"step{step} b{b} g{g}")
+        if k_sel >= 0:
+            _check_lists(idx, cnt, ocs, q_np, k_sel, 4, 64, G)
+    assert gc.len == max(lens) + 3
