@@ -220,10 +220,18 @@ def measured_traffic(workload, tokens):
 
 
 def launches_per_step(w, L1):
-    """Kernels one sparse step launches: append, the selection (scoring and
-    top-K in one kernel, or the fill kernel when nothing has to be ranked),
-    decode."""
-    return 3
+    """Kernels one sparse step (kvd_decode_step) launches on a cache of L1
+    tokens after its append.  When there is a top-K to rank and the token's
+    block is forced (a recent window), the token is appended inside the
+    selection kernel: selection + decode.  Otherwise: append, then the
+    selection (or the fill kernel when nothing has to be ranked), then decode."""
+    nb = (L1 + 63) // 64
+    se = min((w.sink_tokens + 63) // 64, nb)
+    rb = nb if w.recent_tokens <= 0 else max(se, max(0, L1 - w.recent_tokens) // 64)
+    n_cand = rb - se
+    keff = min(w.k_sel, n_cand)
+    fused = 0 < keff < n_cand and w.recent_tokens > 0
+    return 2 if fused else 3
 
 
 # --------------------------------------------------------------------------

@@ -51,12 +51,15 @@ def test_single_rank_is_identity():
     assert bench.max_over_ranks(7.25, 1) == 7.25
 
 
-@pytest.mark.parametrize("name", ["ctx1m_int8", "ctx128k_b8_int8", "tiny_512_f16",
-                                  "int8_dense_2048"])
-def test_launches_per_step(name):
-    # append, selection, decode: the selection is one kernel whether it ranks or not
+@pytest.mark.parametrize("name,want", [("ctx1m_int8", 2), ("ctx128k_b8_int8", 2),
+                                       ("tiny_512_f16", 2), ("int8_dense_2048", 3)])
+def test_launches_per_step(name, want):
+    # a top-K to rank with a recent window: the token rides in the selection
+    # kernel (selection + decode); K_SEL = 0: append, fill, decode
     w = synth.WORKLOADS[name]
-    assert bench.launches_per_step(w, w.L + 1) == 3
+    assert bench.launches_per_step(w, w.L + 1) == want
+    # nothing to rank once K_SEL covers every candidate
+    assert bench.launches_per_step(w.with_(k_sel=10 ** 9), w.L + 1) == 3
 
 
 def test_traffic_scaled_per_token(tmp_path, monkeypatch):
