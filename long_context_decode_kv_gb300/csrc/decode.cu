@@ -43,12 +43,17 @@ __global__ void __launch_bounds__(256) qk_debug_kernel(DecodeArgs a, int32_t *do
 
 }  // namespace
 
-DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_head) {
+DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_head,
+                       bool allow_wide) {
     DecodePlan p;
     p.heads_per_cta = one_head ? 1 : g.G < 4 ? g.G : 4;
     p.subgroups = g.G / p.heads_per_cta;
     const long P = static_cast<long>(g.B) * g.Hkv * p.subgroups;
-    const int per_sm = g.dtype == KVD_F16    ? Tile<KVD_F16>::kMinCtas
+    // the wide tile when every problem still gets at least 4 CTAs with one CTA
+    // per SM (long single sequences); the f16 tile has no wide form
+    p.wide = allow_wide && g.dtype != KVD_F16 && P * 4 <= sm_count;
+    const int per_sm = p.wide                ? 1
+                       : g.dtype == KVD_F16  ? Tile<KVD_F16>::kMinCtas
                        : g.dtype == KVD_Q8_0 ? Tile<KVD_Q8_0>::kMinCtas
                        : g.dtype == KVD_Q4_0 ? Tile<KVD_Q4_0>::kMinCtas
                                              : Tile<KVD_INT8>::kMinCtas;

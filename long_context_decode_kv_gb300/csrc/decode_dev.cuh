@@ -100,6 +100,19 @@ struct Tile<KVD_F16> {
     static constexpr int kThreads = 32 * (kConsumerWarps + 1);
 };
 
+// The wide variant of a tile: twice the consumer groups and stages in one CTA
+// per SM.  With few problems (long single sequences) one CTA per SM keeps its
+// warps at one scheduling priority, where two CTAs per SM let the older one
+// finish its share first and the younger one set the launch's end.
+template <int DT, bool WIDE>
+struct TileW : Tile<DT> {
+    static constexpr int kGroups = (WIDE ? 2 : 1) * Tile<DT>::kGroups;
+    static constexpr int kStages = (WIDE ? 2 : 1) * Tile<DT>::kStages;
+    static constexpr int kMinCtas = WIDE ? 1 : Tile<DT>::kMinCtas;
+    static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+};
+
 struct DecodeArgs {
     const void *k, *v;
     const void *k_scale, *v_scale;  // f32 per token (int8) or f16 per group (q8_0)
@@ -120,19 +133,20 @@ struct DecodeArgs {
     int seq_add;              // tokens appended by this step that seq_lens lacks
 };
 
-template <int DT, int GC, bool TAIL = false>
+template <int DT, int GC, bool TAIL = false, bool WIDE = false>
 struct SmemLayout {
-    static constexpr int kStageBytes = Tile<DT>::kStageBytes;
-    static constexpr int kStages = Tile<DT>::kStages;
+    using T = TileW<DT, WIDE>;
+    static constexpr int kStageBytes = T::kStageBytes;
+    static constexpr int kStages = T::kStages;
     static constexpr int kStagesOff = 0;
     static constexpr int kRing = kStages * kStageBytes;
-    static_assert(Tile<DT>::kTailRecs * kMomentBytes <= kStageBytes, "tail stage overflows");
+    static_assert(T::kTailRecs * kMomentBytes <= kStageBytes, "tail stage overflows");
     // merge rows: one state per consumer warp and head (two with the tail)
-    static constexpr int kRows = (TAIL ? 2 : 1) * Tile<DT>::kConsumerWarps;
+    static constexpr int kRows = (TAIL ? 2 : 1) * T::kConsumerWarps;
     // after the loop the ring holds the warp merge, then the split weights
     static constexpr int kMergeBytes = kRows * GC * kPartStride * 4;
     // split merge: (m, l) and the accumulators of every thread part
-    static constexpr int kWeightBytes = Tile<DT>::kConsumerWarps * 32 * (16 + 8);
+    static constexpr int kWeightBytes = T::kConsumerWarps * 32 * (16 + 8);
     static constexpr int kScratch = kMergeBytes > kWeightBytes ? kMergeBytes : kWeightBytes;
     static constexpr int kBarOff = (kRing > kScratch ? kRing : kScratch);
     static constexpr int kFullOff = kBarOff;
@@ -144,7 +158,7 @@ struct SmemLayout {
     static constexpr int kQsumOff = kCoefOff + 16;  // q4_0: [GC][4] group sums of the codes
     static constexpr int kPwOff = kQsumOff + 64;
     // [warp][16 tokens][4 heads] pairs (p, p)
-    static constexpr int kPwBytes = Tile<DT>::kConsumerWarps * kTokensPerWarp * 4 * 2 * 4;
+    static constexpr int kPwBytes = T::kConsumerWarps * kTokensPerWarp * 4 * 2 * 4;
     static constexpr int kLOff = kPwOff + kPwBytes;  // split merge: L per head
     static constexpr int kFlagOff = kLOff + 16;
     // moment tail: the listed-block mask of each stage
@@ -1034,11 +1048,12 @@ __device__ __forceinline__ void tail_loop(const DecodeArgs &a, int len, int NB, 
     }
 }
 
-template <int DT, int GC, bool DENSE, bool SV, bool TAIL>
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE>
 __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *smem) {
     static_assert(!TAIL || (!DENSE && !SV), "the moment tail runs on a listed selection alone");
-    using SL = SmemLayout<DT, GC, TAIL>;
-    using TL = Tile<DT>;
+    static_assert(!(TAIL && WIDE), "the tail's stages are planned for the narrow tile");
+    using SL = SmemLayout<DT, GC, TAIL, WIDE>;
+    using TL = TileW<DT, WIDE>;
     static_assert(TL::kStages % TL::kGroups == 0, "stages must split evenly over the groups");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + SL::kFullOff);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + SL::kEmptyOff);
@@ -1506,34 +1521,34 @@ DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan 
 // their own translation unit, so the plain kernels carry none of that code:
 // after an L2 flush every instruction of a kernel comes from HBM again, and
 // a shorter instruction stream starts sooner.
-template <int DT, int GC, bool DENSE, bool SV, bool TAIL>
-__global__ void __launch_bounds__(Tile<DT>::kThreads, Tile<DT>::kMinCtas)
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE>
+__global__ void __launch_bounds__(TileW<DT, WIDE>::kThreads, TileW<DT, WIDE>::kMinCtas)
     decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    decode_body<DT, GC, DENSE, SV, TAIL>(a, blockIdx.x, blockIdx.y, smem);
+    decode_body<DT, GC, DENSE, SV, TAIL, WIDE>(a, blockIdx.x, blockIdx.y, smem);
 }
 
-template <int DT, int GC, bool DENSE, bool SV, bool TAIL>
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE = false>
 cudaError_t launch_decode_t(const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
-    using SL = SmemLayout<DT, GC, TAIL>;
+    using SL = SmemLayout<DT, GC, TAIL, WIDE>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE, SV, TAIL>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SL::kTotal);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_ex(decode_kernel<DT, GC, DENSE, SV, TAIL>, dim3(a.splits, P_sub),
-                     dim3(Tile<DT>::kThreads), SL::kTotal, st, pdl, a);
+    return launch_ex(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE>, dim3(a.splits, P_sub),
+                     dim3(TileW<DT, WIDE>::kThreads), SL::kTotal, st, pdl, a);
 }
 
-template <int DT, bool DENSE, bool SV, bool TAIL>
+template <int DT, bool DENSE, bool SV, bool TAIL, bool WIDE = false>
 cudaError_t launch_decode_gc(int gc, const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
     switch (gc) {
-        case 1: return launch_decode_t<DT, 1, DENSE, SV, TAIL>(a, P_sub, st, pdl);
-        case 2: return launch_decode_t<DT, 2, DENSE, SV, TAIL>(a, P_sub, st, pdl);
-        default: return launch_decode_t<DT, 4, DENSE, SV, TAIL>(a, P_sub, st, pdl);
+        case 1: return launch_decode_t<DT, 1, DENSE, SV, TAIL, WIDE>(a, P_sub, st, pdl);
+        case 2: return launch_decode_t<DT, 2, DENSE, SV, TAIL, WIDE>(a, P_sub, st, pdl);
+        default: return launch_decode_t<DT, 4, DENSE, SV, TAIL, WIDE>(a, P_sub, st, pdl);
     }
 }
 
@@ -1548,6 +1563,18 @@ cudaError_t launch_decode_any(const kvd_cache &c, const Geom &g, const DecodePla
     const int P_sub = g.B * g.Hkv * p.subgroups;
     const bool dense = sel_idx == nullptr;
     const int gc = p.heads_per_cta;
+    if constexpr (!SV) {
+        if (p.wide) {  // quantized caches only (plan_decode)
+            if (g.dtype == KVD_INT8)
+                return dense ? launch_decode_gc<KVD_INT8, true, false, false, true>(gc, a, P_sub, st, pdl)
+                             : launch_decode_gc<KVD_INT8, false, false, false, true>(gc, a, P_sub, st, pdl);
+            if (g.dtype == KVD_Q8_0)
+                return dense ? launch_decode_gc<KVD_Q8_0, true, false, false, true>(gc, a, P_sub, st, pdl)
+                             : launch_decode_gc<KVD_Q8_0, false, false, false, true>(gc, a, P_sub, st, pdl);
+            return dense ? launch_decode_gc<KVD_Q4_0, true, false, false, true>(gc, a, P_sub, st, pdl)
+                         : launch_decode_gc<KVD_Q4_0, false, false, false, true>(gc, a, P_sub, st, pdl);
+        }
+    }
     if (g.dtype == KVD_INT8)
         return dense ? launch_decode_gc<KVD_INT8, true, SV, false>(gc, a, P_sub, st, pdl)
                      : launch_decode_gc<KVD_INT8, false, SV, false>(gc, a, P_sub, st, pdl);

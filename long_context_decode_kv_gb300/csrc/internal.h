@@ -29,10 +29,13 @@ struct DecodePlan {
     int subgroups;      // G / heads_per_cta
     int splits;         // CTAs per (sequence, KV head, subgroup)
     int blocks;         // list length planned for (max_sel, at most NB)
+    bool wide;          // one CTA per SM with twice the consumer groups
 };
 
-// one_head: one query head per CTA (lists per query head).
-DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_head = false);
+// one_head: one query head per CTA (lists per query head).  allow_wide: the
+// plain kernels may take the wide tile (quantized caches, few problems).
+DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_head = false,
+                       bool allow_wide = false);
 size_t decode_partials_bytes(const Geom &g, const DecodePlan &p);
 int device_sm_count();
 

@@ -69,6 +69,24 @@ def test_sparse_with_oracle_selection(dtype, L, k_sel, sink, recent):
     assert_outputs(out, ref, dtype, f"sparse {dtype} L{L}")
 
 
+@pytest.mark.parametrize("dtype", [kvd.INT8, kvd.Q8_0, kvd.Q4_0])
+@pytest.mark.parametrize("B,Hkv", [(1, 8), (10, 4)])
+def test_sparse_both_tiles(dtype, B, Hkv):
+    # few problems take the wide tile (one CTA per SM, four consumer groups),
+    # many take two CTAs per SM: both against the oracle
+    L, G = 3000, 4
+    k = seeded((B, L, Hkv, 128), 91, scale=1.5)
+    v = seeded((B, L, Hkv, 128), 92)
+    gc, oc = make_pair(dtype, k, v)
+    q = _q(B, Hkv * G, 93, scale=2.0)
+    ref, o_idx, o_cnt = oc.decode(q.cpu().numpy(), scale_for(), k_sel=9, sink_tokens=4,
+                                  recent_tokens=128)
+    sel_idx = torch.from_numpy(o_idx).to(dev())
+    sel_cnt = torch.from_numpy(o_cnt).to(dev())
+    out = _sparse(gc, q, scale_for(), sel_idx, sel_cnt, int(o_cnt.max()))
+    assert_outputs(out, ref, dtype, f"sparse {dtype} B{B} Hkv{Hkv}")
+
+
 @pytest.mark.parametrize("dtype", [kvd.F16, kvd.INT8, kvd.Q8_0, kvd.Q4_0])
 def test_select_all_equals_dense(dtype):
     # gate ladder plumbing anchor: K_SEL = n_blocks => sparse == dense
