@@ -221,7 +221,7 @@ kvd_status decode_per_head_impl(const kvd_cache *c, const float *q, int n_heads,
     const Geom g = make_geom(c, n_heads, c->len);
     int max_blocks = max_sel < g.NB ? max_sel : g.NB;
     if (max_blocks < 1) max_blocks = 1;
-    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), true);
+    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), true, true);
     return cuda_status(launch_decode_per_head(*c, g, p, q, scale, sel_idx, sel_cnt, out,
                                               ws_at<float>(ws, w.partials),
                                               ws_at<uint32_t>(ws, w.counters), st, true));

@@ -94,6 +94,13 @@ cudaError_t launch_decode_per_head(const kvd_cache &c, const Geom &g, const Deco
                                     counters, false, 0.0f);
     a.per_head = 1;  // p.heads_per_cta is 1: CTA problem b * H + h reads list row b * H + h
     const int P_sub = g.B * g.Hkv * p.subgroups;
+    if (p.wide) {  // quantized caches only (plan_decode)
+        if (g.dtype == KVD_INT8)
+            return launch_decode_t<KVD_INT8, 1, false, false, false, true>(a, P_sub, st, pdl);
+        if (g.dtype == KVD_Q8_0)
+            return launch_decode_t<KVD_Q8_0, 1, false, false, false, true>(a, P_sub, st, pdl);
+        return launch_decode_t<KVD_Q4_0, 1, false, false, false, true>(a, P_sub, st, pdl);
+    }
     if (g.dtype == KVD_INT8)
         return launch_decode_t<KVD_INT8, 1, false, false, false>(a, P_sub, st, pdl);
     if (g.dtype == KVD_Q8_0)
