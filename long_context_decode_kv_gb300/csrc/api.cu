@@ -188,8 +188,7 @@ kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float sc
     int max_blocks = dense ? g.NB : max_sel;
     if (max_blocks > g.NB) max_blocks = g.NB;
     if (max_blocks < 1) max_blocks = 1;
-    // the wide tile only for the plain kernels (not sparse-V)
-    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), false, sv_eps == 0.0f);
+    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), false, true);
     return cuda_status(launch_decode(*c, g, p, q, scale, sel_idx, sel_cnt, out,
                                      ws_at<float>(ws, w.partials),
                                      ws_at<uint32_t>(ws, w.counters), st, true, in_step,
@@ -207,7 +206,7 @@ kvd_status decode_tail_impl(const kvd_cache *c, const float *q, int n_heads, flo
     if (max_blocks < 1) max_blocks = 1;
     const int tail_work = (g.NB + 31) / 32;
     DecodePlan p = plan_decode(g, max_blocks > tail_work ? max_blocks : tail_work,
-                               device_sm_count());
+                               device_sm_count(), false, true);
     p.blocks = max_blocks;
     return cuda_status(launch_decode_tail(*c, g, p, q, scale, sel_idx, sel_cnt, out,
                                           ws_at<float>(ws, w.partials),

@@ -872,14 +872,14 @@ __device__ __forceinline__ int first_at_least(const int32_t *list, int n, int ta
 // its listed blocks.  The list is walked once, 32 entries per load: ent holds
 // entries cur .. cur + 31, of which the first o lanes are used up.
 // i: the stage sequence number, advanced per stage.
-template <int DT>
+template <int DT, bool WIDE>
 __device__ __forceinline__ bool produce_tail(const DecodeArgs &a, int NB, int split, int bg,
                                              int cnt,
                                              const int32_t *list, int &i, uint64_t *full,
                                              uint64_t *empty, int *stage_blk,
                                              uint32_t *stage_mask, uint8_t *ring,
                                              volatile int *abort_flag, int lane, uint64_t pol) {
-    using TL = Tile<DT>;
+    using TL = TileW<DT, WIDE>;
     constexpr int R = TL::kTailRecs;
     const int nch = (NB + R - 1) / R;
     const int c0 = static_cast<int>((static_cast<long long>(split) * nch) / a.splits);
@@ -957,14 +957,14 @@ constexpr int tail_shift() {
 // waited for) to the group's end marker.  Warp wg takes records
 // [wg RW, wg RW + RW) of each stage; ts.m and ts.l belong to the lane's head
 // h = (lane >> SH) % GC, ts.acc to channels 4 lane .. 4 lane + 3 of every head.
-template <int DT, int GC>
+template <int DT, int GC, bool WIDE>
 __device__ __forceinline__ void tail_loop(const DecodeArgs &a, int len, int NB, int b, int h0,
                                           int i,
                                        uint64_t *full, uint64_t *empty, const int *stage_blk,
                                        const uint32_t *stage_mask, const uint8_t *ring, float *pw,
                                        int wg, int lane, volatile int *abort_flag,
                                        WarpState<GC> &ts) {
-    using TL = Tile<DT>;
+    using TL = TileW<DT, WIDE>;
     constexpr int R = TL::kTailRecs, RW = R / kWarpsPerGroup, N = RW * GC;
     constexpr int SH = tail_shift<DT, GC>(), LGC = ilog2(GC);
     float qf[GC][4];  // the f32 query in base-2 logit units
@@ -1051,7 +1051,6 @@ __device__ __forceinline__ void tail_loop(const DecodeArgs &a, int len, int NB, 
 template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE>
 __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *smem) {
     static_assert(!TAIL || (!DENSE && !SV), "the moment tail runs on a listed selection alone");
-    static_assert(!(TAIL && WIDE), "the tail's stages are planned for the narrow tile");
     using SL = SmemLayout<DT, GC, TAIL, WIDE>;
     using TL = TileW<DT, WIDE>;
     static_assert(TL::kStages % TL::kGroups == 0, "stages must split evenly over the groups");
@@ -1183,7 +1182,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         }
         if constexpr (TAIL) {
             if (ok)
-                ok = produce_tail<DT>(a, NB, split, bg, cnt, list, i, full, empty, stage_blk,
+                ok = produce_tail<DT, WIDE>(a, NB, split, bg, cnt, list, i, full, empty, stage_blk,
                                       stage_mask, smem + SL::kStagesOff, abort_flag, lane, pol);
         }
         const int issued = i;
@@ -1301,7 +1300,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         }
         if constexpr (TAIL) {
             if (at_tail)
-                tail_loop<DT, GC>(a, len, NB, b, h0, i, full, empty, stage_blk, stage_mask,
+                tail_loop<DT, GC, WIDE>(a, len, NB, b, h0, i, full, empty, stage_blk, stage_mask,
                                   smem + SL::kStagesOff, pw, wg, lane, abort_flag, ts);
         }
         // per-warp totals: l summed over the lanes of each head
@@ -1563,17 +1562,15 @@ cudaError_t launch_decode_any(const kvd_cache &c, const Geom &g, const DecodePla
     const int P_sub = g.B * g.Hkv * p.subgroups;
     const bool dense = sel_idx == nullptr;
     const int gc = p.heads_per_cta;
-    if constexpr (!SV) {
-        if (p.wide) {  // quantized caches only (plan_decode)
-            if (g.dtype == KVD_INT8)
-                return dense ? launch_decode_gc<KVD_INT8, true, false, false, true>(gc, a, P_sub, st, pdl)
-                             : launch_decode_gc<KVD_INT8, false, false, false, true>(gc, a, P_sub, st, pdl);
-            if (g.dtype == KVD_Q8_0)
-                return dense ? launch_decode_gc<KVD_Q8_0, true, false, false, true>(gc, a, P_sub, st, pdl)
-                             : launch_decode_gc<KVD_Q8_0, false, false, false, true>(gc, a, P_sub, st, pdl);
-            return dense ? launch_decode_gc<KVD_Q4_0, true, false, false, true>(gc, a, P_sub, st, pdl)
-                         : launch_decode_gc<KVD_Q4_0, false, false, false, true>(gc, a, P_sub, st, pdl);
-        }
+    if (p.wide) {  // quantized caches only (plan_decode)
+        if (g.dtype == KVD_INT8)
+            return dense ? launch_decode_gc<KVD_INT8, true, SV, false, true>(gc, a, P_sub, st, pdl)
+                         : launch_decode_gc<KVD_INT8, false, SV, false, true>(gc, a, P_sub, st, pdl);
+        if (g.dtype == KVD_Q8_0)
+            return dense ? launch_decode_gc<KVD_Q8_0, true, SV, false, true>(gc, a, P_sub, st, pdl)
+                         : launch_decode_gc<KVD_Q8_0, false, SV, false, true>(gc, a, P_sub, st, pdl);
+        return dense ? launch_decode_gc<KVD_Q4_0, true, SV, false, true>(gc, a, P_sub, st, pdl)
+                     : launch_decode_gc<KVD_Q4_0, false, SV, false, true>(gc, a, P_sub, st, pdl);
     }
     if (g.dtype == KVD_INT8)
         return dense ? launch_decode_gc<KVD_INT8, true, SV, false>(gc, a, P_sub, st, pdl)

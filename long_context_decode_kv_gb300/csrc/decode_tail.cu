@@ -16,6 +16,13 @@ cudaError_t launch_decode_tail(const kvd_cache &c, const Geom &g, const DecodePl
     a.moments = static_cast<const __half *>(c.moments);
     const int P_sub = g.B * g.Hkv * p.subgroups;
     const int gc = p.heads_per_cta;
+    if (p.wide) {  // quantized caches only (plan_decode)
+        if (g.dtype == KVD_INT8)
+            return launch_decode_gc<KVD_INT8, false, false, true, true>(gc, a, P_sub, st, pdl);
+        if (g.dtype == KVD_Q8_0)
+            return launch_decode_gc<KVD_Q8_0, false, false, true, true>(gc, a, P_sub, st, pdl);
+        return launch_decode_gc<KVD_Q4_0, false, false, true, true>(gc, a, P_sub, st, pdl);
+    }
     if (g.dtype == KVD_INT8)
         return launch_decode_gc<KVD_INT8, false, false, true>(gc, a, P_sub, st, pdl);
     if (g.dtype == KVD_Q8_0)

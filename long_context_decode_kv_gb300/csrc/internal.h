@@ -33,7 +33,8 @@ struct DecodePlan {
 };
 
 // one_head: one query head per CTA (lists per query head).  allow_wide: the
-// plain kernels may take the wide tile (quantized caches, few problems).
+// launch may take the wide tile (quantized caches, few problems); every
+// decode call allows it, so they all plan the same tile and splits.
 DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_head = false,
                        bool allow_wide = false);
 size_t decode_partials_bytes(const Geom &g, const DecodePlan &p);

@@ -101,7 +101,7 @@ extern "C" kvd_status kvd_decode_attn_static(const kvd_cache *cache, const float
     g.seq_add = 0;
     int max_blocks = max_sel < g.NB ? max_sel : g.NB;
     if (max_blocks < 1) max_blocks = 1;
-    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count());
+    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), false, true);
     const size_t counter_bytes =
         round256(static_cast<size_t>(g.B) * g.Hkv * p.subgroups * sizeof(uint32_t));
     if (counter_bytes + decode_partials_bytes(g, p) > KVD_STATIC_SCRATCH_BYTES)
