@@ -188,7 +188,9 @@ kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float sc
     int max_blocks = dense ? g.NB : max_sel;
     if (max_blocks > g.NB) max_blocks = g.NB;
     if (max_blocks < 1) max_blocks = 1;
-    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), false, true);
+    // the wide tile for listed blocks only: over every block (a long stream) the
+    // two-CTA tile keeps two producers per SM and streams faster
+    const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), false, !dense);
     return cuda_status(launch_decode(*c, g, p, q, scale, sel_idx, sel_cnt, out,
                                      ws_at<float>(ws, w.partials),
                                      ws_at<uint32_t>(ws, w.counters), st, true, in_step,
