@@ -49,9 +49,9 @@ DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_hea
     p.heads_per_cta = one_head ? 1 : g.G < 4 ? g.G : 4;
     p.subgroups = g.G / p.heads_per_cta;
     const long P = static_cast<long>(g.B) * g.Hkv * p.subgroups;
-    // the wide tile when every problem still gets at least 4 CTAs with one CTA
+    // the wide tile when every problem still gets at least 8 CTAs with one CTA
     // per SM (long single sequences); the f16 tile has no wide form
-    p.wide = allow_wide && g.dtype != KVD_F16 && P * 4 <= sm_count;
+    p.wide = allow_wide && g.dtype != KVD_F16 && P * 8 <= sm_count;
     const int per_sm = p.wide                ? 1
                        : g.dtype == KVD_F16  ? Tile<KVD_F16>::kMinCtas
                        : g.dtype == KVD_Q8_0 ? Tile<KVD_Q8_0>::kMinCtas
