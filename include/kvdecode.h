@@ -129,7 +129,7 @@ typedef struct kvd_cache {
     int32_t reserved;     /* must be 0 */
     void *k;
     void *v;
-    void *k_scale;        /* f32 (int8) or f16 (q8_0) scales, see above */
+    void *k_scale;        /* f32 (int8) or f16 (q8_0, q4_0) scales, see above */
     void *v_scale;
     void *kbounds;
     int32_t *dev_status;

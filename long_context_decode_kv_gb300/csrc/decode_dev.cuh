@@ -1,5 +1,5 @@
-// decode_dev.cuh -- device side of the split-KV decode (decode_kernel).
-// selected KV blocks (or all of them for the dense arm).
+// decode_dev.cuh -- device side of the split-KV decode (decode_kernel) over
+// the selected KV blocks (or all of them for the dense arm).
 //
 // "Sparse Attention -- Quest-style block-selector for long-context decode
 // (#551)", S3 "FA-VEC block-skip": unselected blocks are skipped before the
@@ -15,13 +15,16 @@
 // The last warp is the producer: one lane streams each
 // listed 64-token block (K, V and, for int8, both scale rows) into a ring of
 // shared-memory stages with 1-D TMA bulk copies completing on an mbarrier.
-// The other warps form two consumer groups of four that take blocks in turn,
-// so more warps hide each other's latencies; within a group warp w owns
+// The other warps form two consumer groups of four (four groups in the wide
+// tile, one CTA per SM) that take blocks in turn, so more warps hide each
+// other's latencies; within a group warp w owns
 // tokens 16w..16w+15 of the block and keeps its own online-softmax state for
 // the CTA's query heads, so no CTA-wide barrier is needed per block.  PV runs
 // on packed f32x2 FMAs.  At the end the warp states merge in shared memory
 // and the CTA writes a partial (m, l, acc[128]) per head; the last CTA of the
-// problem to arrive merges all splits.
+// problem to arrive merges all splits.  Variants: sparse-V (SV), the moment
+// tail of the unlisted blocks (TAIL), per-sequence lengths and per-head lists
+// (run-time arguments).
 #pragma once
 
 #include "common.cuh"
@@ -115,7 +118,7 @@ struct TileW : Tile<DT> {
 
 struct DecodeArgs {
     const void *k, *v;
-    const void *k_scale, *v_scale;  // f32 per token (int8) or f16 per group (q8_0)
+    const void *k_scale, *v_scale;  // f32 per token (int8) or f16 per group (q8_0, q4_0)
     const __half *moments;          // block means (moment tail), or null
     const float *q;
     float *out;

@@ -1,7 +1,6 @@
 // select_dev.cuh -- device side of the Quest block selection: block bounds,
 // GQA max, top-K with the sink and recent blocks forced in.  Used by
-// select_kernel (select.cu) and by the scoring items of the persistent step
-// kernel (step.cu).
+// select_kernel and fill_kernel_varlen (select.cu).
 //
 // "Sparse Attention -- Quest-style block-selector for long-context decode
 // (#551)":
@@ -26,6 +25,14 @@
 // barely differ), one pass that marks the keys above T's bin and collects
 // the few keys inside it, digits of those keys' low bits, then the
 // ascending list written in index order.  No CTA waits for another.
+// A problem of at most kSmallRank candidates skips the copy and the radix
+// passes: its last CTA holds one key per thread and builds T bit by bit from
+// block-wide counts (select_small).
+//
+// Modes (template MODE): kExport writes the bounds for the tests; kSelect
+// selects; kVarlen finds each problem's geometry from its own sequence length
+// on the device; kPerHead serves one query head of each group per launch
+// (lists per query head, the ablation of the shared block set).
 #pragma once
 
 #include "append_dev.cuh"

@@ -108,7 +108,8 @@ class OracleCache:
 
     K, V: [B, Hkv, max_seq, D] (float16, or int8 codes); ks, vs: [B, Hkv,
     max_seq] float32 (int8 only); kd, vd: [B, Hkv, max_seq, D // 32] float16
-    group scales (q8_0 only); kmin, kmax: [B, Hkv, max_seq // blk, D] float16.
+    group scales (q8_0 and q4_0; q4_0 rows are [.., D // 2] bytes of two codes);
+    kmin, kmax: [B, Hkv, max_seq // blk, D] float16.
     """
 
     def __init__(self, dtype: int, B: int, Hkv: int, D: int, max_seq: int, blk: int = 64):

@@ -1,6 +1,7 @@
 /*
  * oracle.c -- plain, slow, fp64 CPU oracle for Quest-style sparse decode
- * attention over an f16 or absmax-int8 KV cache.
+ * attention over an f16, absmax-int8, q8_0 or q4_0 KV cache, with the
+ * sparse-V (eps mode) and moment-tail variants.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
  * calls this file: only the tests, the smoke check and the benchmark's CPU
