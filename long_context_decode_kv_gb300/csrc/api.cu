@@ -458,35 +458,6 @@ kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
     }
     if (!sel_idx) sel_idx = ws_at<int32_t>(workspace, w.sel_idx);
     if (!sel_cnt) sel_cnt = ws_at<int32_t>(workspace, w.sel_cnt);
-    {
-        // A small f16 problem selects inside the decode kernel: the step is the
-        // token's append, then one decode launch.  The token's block is forced
-        // (a recent window), so the ranking never reads its bounds.
-        const int L1 = cache->len + 1;
-        const ForcedRange f = forced_range(L1, sink_tokens, recent_tokens);
-        const int n_cand = f.rb - f.se;
-        const int keff = k_sel < n_cand ? k_sel : n_cand;
-        const int G = n_heads / cache->n_kv_heads;
-        if (cache->dtype == KVD_F16 && !cache->seq_lens && G <= kFuseMaxGroup &&
-            recent_tokens > 0 && keff > 0 && keff < n_cand && n_cand <= kFuseMaxCandidates &&
-            f.NB <= kFuseMaxListBlocks) {
-            kvd_cache c0 = *cache;
-            if (launch_append(c0, k_new, v_new, 1, st, true) != cudaSuccess)
-                return KVD_ERR_CUDA;
-            cache->len += 1;
-            Geom g = make_geom(cache, n_heads, cache->len);
-            g.seq_add = 1;
-            const int max_sel =
-                kvd_selected_count(cache->len, kBlock, k_sel, sink_tokens, recent_tokens);
-            const DecodePlan p = plan_decode(g, max_sel < g.NB ? max_sel : g.NB,
-                                             device_sm_count());
-            return cuda_status(launch_decode_fused(*cache, g, p, q, softmax_scale, f.se, f.rb,
-                                                   keff, sel_idx, sel_cnt, out,
-                                                   ws_at<float>(workspace, w.partials),
-                                                   ws_at<uint32_t>(workspace, w.counters), st,
-                                                   true));
-        }
-    }
     // the selection appends the token (in its own kernel when the token's
     // block is forced, else by an append launch just before)
     const StepToken tok = {k_new, v_new, cache->len};

@@ -50,12 +50,6 @@ constexpr int kMomentBytes = 2 * kHeadDim * 2;
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
-// Selection inside the decode kernel (FUSE): small problems only (the
-// host's limits in internal.h).
-constexpr int kFuseMaxCand = kFuseMaxCandidates;  // ranked, two keys per thread
-constexpr int kFuseMaxBlocks = kFuseMaxListBlocks;  // the list in shared memory
-constexpr int kFuseMaxG = kFuseMaxGroup;          // query heads scored per block
-
 template <int DT>
 struct Tile;
 template <>
@@ -140,13 +134,9 @@ struct DecodeArgs {
     int per_head;      // lists per query head ([B, H] rows; one head per CTA)
     const int32_t *seq_lens;  // per-sequence lengths (<= len), or null
     int seq_add;              // tokens appended by this step that seq_lens lacks
-    // FUSE: the kernel selects itself (bounds in, the list out to sel_out_*)
-    const __half *kbounds;
-    int32_t *sel_out_idx, *sel_out_cnt;
-    int fuse_se, fuse_rb, fuse_keff;
 };
 
-template <int DT, int GC, bool TAIL = false, bool WIDE = false, bool FUSE = false>
+template <int DT, int GC, bool TAIL = false, bool WIDE = false>
 struct SmemLayout {
     using T = TileW<DT, WIDE>;
     static constexpr int kStageBytes = T::kStageBytes;
@@ -176,13 +166,7 @@ struct SmemLayout {
     static constexpr int kFlagOff = kLOff + 16;
     // moment tail: the listed-block mask of each stage
     static constexpr int kMaskOff = kFlagOff + 16;
-    // in-kernel selection: the ascending list, and warp totals of the scans
-    static constexpr int kListOff = kMaskOff + (TAIL ? 4 * kStages : 0);
-    static constexpr int kWsumOff = kListOff + (FUSE ? 4 * kFuseMaxBlocks : 0);
-    static constexpr int kTotal = kWsumOff + (FUSE ? 4 * 32 : 0);
-    // the selection's scratch (the group's query, the keys) lives in the ring
-    static_assert(!FUSE || kFuseMaxG * kHeadDim * 4 + kFuseMaxCand * 4 <= kRing,
-                  "selection scratch overflows the ring");
+    static constexpr int kTotal = kMaskOff + (TAIL ? 4 * kStages : 0);
 };
 
 // ----------------------------------------------------------------------------
@@ -1067,106 +1051,10 @@ __device__ __forceinline__ void tail_loop(const DecodeArgs &a, int len, int NB, 
     }
 }
 
-// ----------------------------------------------------------------------------
-// In-kernel selection for small problems ("Sparse Attention -- Quest-style
-// block-selector ...", Method: per-query upper bound, GQA max, top-K with the
-// sink and recent blocks forced in).  Every CTA of the problem ranks the same
-// keys, so none waits for another; the selection kernel's launch and ticket
-// drop out of the step.  At most kFuseMaxCand candidates, kFuseMaxG heads.
-
-// Exclusive count of flag over the CTA's threads in order, and the total
-// (all threads call; wsum: one int per warp).
-__device__ __forceinline__ int cta_exclusive_count(bool flag, int *wsum, int &total) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nw = blockDim.x >> 5;
-    const unsigned m = __ballot_sync(kFull, flag);
-    if (lane == 0) wsum[warp] = __popc(m);
-    __syncthreads();
-    int before = __popc(m & ((1u << lane) - 1u)), all = 0;
-    for (int w = 0; w < nw; ++w) {
-        const int c = wsum[w];
-        if (w < warp) before += c;
-        all += c;
-    }
-    __syncthreads();  // wsum free for the next call
-    total = all;
-    return before;
-}
-
-// The ascending list of (sequence b, KV head g) into list_s; returns its
-// length.  Candidates are blocks [se, rb) of the NB blocks: the group bound
-// UB(j) = max over the group's G heads of sum_d max(q_d kmin_j[d],
-// q_d kmax_j[d]) of each, the keff largest keys (ties to the lower index),
-// then the sink blocks [0, se) before and the recent blocks [rb, NB) after.
-// scratch: the ring, free until the stream starts.  All threads call.
-__device__ __noinline__ int fused_select(const DecodeArgs &a, int b, int g, int bg, int NB,
-                                         uint8_t *scratch, int32_t *list_s, int *wsum) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nthr = blockDim.x, nwarps = nthr >> 5;
-    const int G = a.G, se = a.fuse_se, rb = a.fuse_rb, keff = a.fuse_keff, n = rb - se;
-    float *qg = reinterpret_cast<float *>(scratch);                                  // [G][128]
-    uint32_t *keys = reinterpret_cast<uint32_t *>(scratch + kFuseMaxG * kHeadDim * 4);  // [n]
-    const float *qsrc = a.q + (static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * G) *
-                                  kHeadDim;
-    for (int i = tid; i < G * kHeadDim; i += nthr) qg[i] = qsrc[i];
-    __syncthreads();
-    // one warp per block: lane l reads the (kmin, kmax) pairs of channels 4l..4l+3
-    for (int jj = warp; jj < n; jj += nwarps) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(
-            a.kbounds + ((static_cast<size_t>(bg) * a.nbmax + se + jj) * kHeadDim + 4 * lane) * 2);
-        const __half2 *p2 = reinterpret_cast<const __half2 *>(&w);
-        float2 kb[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) kb[c] = __half22float2(p2[c]);  // (kmin, kmax)
-        float ub = -__int_as_float(0x7f800000);
-        for (int h = 0; h < G; ++h) {
-            const float4 q4 = *reinterpret_cast<const float4 *>(qg + h * kHeadDim + 4 * lane);
-            const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-            float sum = 0.0f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                sum = fmaf(fmaxf(qv[c], 0.0f), kb[c].y, fmaf(fminf(qv[c], 0.0f), kb[c].x, sum));
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-            ub = fmaxf(ub, sum);
-        }
-        if (lane == 0) keys[jj] = float_to_key(ub);
-    }
-    __syncthreads();
-    // the keff-th largest key T, bit by bit from CTA-wide counts; key j of
-    // thread t: j = t (slot 0) and j = t + nthr (slot 1)
-    const bool h0 = tid < n, h1 = tid + nthr < n;
-    const uint32_t k0 = h0 ? keys[tid] : 0u, k1 = h1 ? keys[tid + nthr] : 0u;
-    uint32_t T = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t c = T | (1u << bit);
-        const int ge = __syncthreads_count(h0 && k0 >= c) + __syncthreads_count(h1 && k1 >= c);
-        if (ge >= keff) T = c;
-    }
-    const int n_gt = __syncthreads_count(h0 && k0 > T) + __syncthreads_count(h1 && k1 > T);
-    const bool e0 = h0 && k0 == T, e1 = h1 && k1 == T;
-    int t0 = 0, t1 = 0;
-    const int r0 = cta_exclusive_count(e0, wsum, t0);
-    const int r1 = t0 + cta_exclusive_count(e1, wsum, t1);
-    const int need = keff - n_gt;  // keys equal to T to take, lowest index first
-    const bool i0 = h0 && (k0 > T || (e0 && r0 < need));
-    const bool i1 = h1 && (k1 > T || (e1 && r1 < need));
-    int s0 = 0, s1 = 0;
-    const int p0 = cta_exclusive_count(i0, wsum, s0);
-    const int p1 = s0 + cta_exclusive_count(i1, wsum, s1);
-    if (i0) list_s[se + p0] = se + tid;
-    if (i1) list_s[se + p1] = se + tid + nthr;
-    for (int j = tid; j < se; j += nthr) list_s[j] = j;
-    for (int j = rb + tid; j < NB; j += nthr) list_s[se + keff + (j - rb)] = j;
-    __syncthreads();  // the list is complete; the ring may take data
-    return se + keff + (NB - rb);
-}
-
-template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE, bool FUSE>
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE>
 __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *smem) {
     static_assert(!TAIL || (!DENSE && !SV), "the moment tail runs on a listed selection alone");
-    static_assert(!FUSE || (!DENSE && !SV && !TAIL && !WIDE), "in-kernel selection: plain only");
-    using SL = SmemLayout<DT, GC, TAIL, WIDE, FUSE>;
+    using SL = SmemLayout<DT, GC, TAIL, WIDE>;
     using TL = TileW<DT, WIDE>;
     static_assert(TL::kStages % TL::kGroups == 0, "stages must split evenly over the groups");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + SL::kFullOff);
@@ -1208,21 +1096,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
     // this sequence's own length (per-sequence lengths) and blocks
     const int len = seq_len_of(a.seq_lens, b, a.len - a.seq_add, a.dev_status) + a.seq_add;
     const int NB = (len + kBlock - 1) / kBlock;
-    int cnt;
-    const int32_t *list_src = a.sel_idx + static_cast<size_t>(lrow) * a.nbmax;
-    if constexpr (FUSE) {
-        int32_t *list_s = reinterpret_cast<int32_t *>(smem + SL::kListOff);
-        cnt = fused_select(a, b, g, bg, NB, smem + SL::kStagesOff, list_s,
-                           reinterpret_cast<int *>(smem + SL::kWsumOff));
-        if (split == 0 && sub == 0) {  // the list goes out for the caller too
-            int32_t *dst = a.sel_out_idx + static_cast<size_t>(bg) * a.nbmax;
-            for (int i = tid; i < cnt; i += blockDim.x) dst[i] = list_s[i];
-            if (tid == 0) a.sel_out_cnt[bg] = cnt;
-        }
-        list_src = list_s;
-    } else {
-        cnt = DENSE ? NB : a.sel_cnt[lrow];
-    }
+    int cnt = DENSE ? NB : a.sel_cnt[lrow];
     cnt = max(0, min(cnt, NB));
 
     const size_t row0 = static_cast<size_t>(bg) * a.max_seq;  // first token row of (b, g)
@@ -1238,7 +1112,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         // length, then (only when sel_cnt passes that length) every
         // splits-th position beyond it, from plan_blocks + split on.
         const uint64_t pol = l2_policy_evict_first();
-        const int32_t *list = list_src;
+        const int32_t *list = a.sel_idx + static_cast<size_t>(lrow) * a.nbmax;
         const int S = a.splits, MB = a.plan_blocks;
         const int pb = static_cast<int>((static_cast<long long>(split) * MB) / S);
         const int pe = static_cast<int>((static_cast<long long>(split + 1) * MB) / S);
@@ -1649,34 +1523,34 @@ DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan 
 // their own translation unit, so the plain kernels carry none of that code:
 // after an L2 flush every instruction of a kernel comes from HBM again, and
 // a shorter instruction stream starts sooner.
-template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE, bool FUSE>
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE>
 __global__ void __launch_bounds__(TileW<DT, WIDE>::kThreads, TileW<DT, WIDE>::kMinCtas)
     decode_kernel(DecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    decode_body<DT, GC, DENSE, SV, TAIL, WIDE, FUSE>(a, blockIdx.x, blockIdx.y, smem);
+    decode_body<DT, GC, DENSE, SV, TAIL, WIDE>(a, blockIdx.x, blockIdx.y, smem);
 }
 
-template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE = false, bool FUSE = false>
+template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE = false>
 cudaError_t launch_decode_t(const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
-    using SL = SmemLayout<DT, GC, TAIL, WIDE, FUSE>;
+    using SL = SmemLayout<DT, GC, TAIL, WIDE>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE, FUSE>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SL::kTotal);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_ex(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE, FUSE>, dim3(a.splits, P_sub),
+    return launch_ex(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE>, dim3(a.splits, P_sub),
                      dim3(TileW<DT, WIDE>::kThreads), SL::kTotal, st, pdl, a);
 }
 
-template <int DT, bool DENSE, bool SV, bool TAIL, bool WIDE = false, bool FUSE = false>
+template <int DT, bool DENSE, bool SV, bool TAIL, bool WIDE = false>
 cudaError_t launch_decode_gc(int gc, const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
     switch (gc) {
-        case 1: return launch_decode_t<DT, 1, DENSE, SV, TAIL, WIDE, FUSE>(a, P_sub, st, pdl);
-        case 2: return launch_decode_t<DT, 2, DENSE, SV, TAIL, WIDE, FUSE>(a, P_sub, st, pdl);
-        default: return launch_decode_t<DT, 4, DENSE, SV, TAIL, WIDE, FUSE>(a, P_sub, st, pdl);
+        case 1: return launch_decode_t<DT, 1, DENSE, SV, TAIL, WIDE>(a, P_sub, st, pdl);
+        case 2: return launch_decode_t<DT, 2, DENSE, SV, TAIL, WIDE>(a, P_sub, st, pdl);
+        default: return launch_decode_t<DT, 4, DENSE, SV, TAIL, WIDE>(a, P_sub, st, pdl);
     }
 }
 

@@ -98,20 +98,6 @@ cudaError_t launch_decode_per_head(const kvd_cache &c, const Geom &g, const Deco
                                    const int32_t *sel_cnt, float *out, float *partials,
                                    uint32_t *counters, cudaStream_t st, bool pdl);
 
-// Limits of the in-kernel selection (decode_fused.cu): group size,
-// candidates, blocks of the sequence.
-constexpr int kFuseMaxGroup = 8;
-constexpr int kFuseMaxCandidates = 512;
-constexpr int kFuseMaxListBlocks = 1024;
-
-// A decode that selects its own blocks (small f16 problems inside a step):
-// candidates [se, rb), keff of them; the list also goes to sel_idx / sel_cnt.
-cudaError_t launch_decode_fused(const kvd_cache &c, const Geom &g, const DecodePlan &p,
-                                const float *q, float scale, int se, int rb, int keff,
-                                int32_t *sel_idx, int32_t *sel_cnt, float *out,
-                                float *partials, uint32_t *counters, cudaStream_t st,
-                                bool pdl);
-
 // The listed blocks exactly plus the moment tail of every other block
 // (decode_tail.cu); c.moments must be set.
 cudaError_t launch_decode_tail(const kvd_cache &c, const Geom &g, const DecodePlan &p,
