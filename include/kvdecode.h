@@ -424,6 +424,17 @@ KVD_API kvd_status kvd_debug_qk_int8(const kvd_cache *cache, const float *q, int
 KVD_API kvd_status kvd_debug_scores(const kvd_cache *cache, const float *q, int32_t n_heads,
                             float *ub, void *stream);
 
+/* ---------------------------------------------------------------------- */
+/* Test export of the bounded-wait path: one kernel waits on an mbarrier    */
+/* phase that nothing completes, gives up after limit_us microseconds of    */
+/* wall time (the decode and selection kernels give up after 2 s), and      */
+/* writes KVD_ERR_TIMEOUT to *dev_status (a device int32) unless it holds a */
+/* code already.  The kernel then returns normally: the context stays       */
+/* usable.  Errors: INVALID (dev_status NULL or misaligned, limit_us 0 or   */
+/* above 1,000,000), CUDA.                                                  */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_debug_wait_timeout(int32_t *dev_status, int32_t limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

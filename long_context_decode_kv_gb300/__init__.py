@@ -39,7 +39,7 @@ EXPORTS = ("kvd_kv_append", "kvd_select_blocks", "kvd_decode_attn", "kvd_decode_
            "kvd_selected_count", "kvd_status_string", "kvd_abi_version", "kvd_debug_qk_int8",
            "kvd_debug_scores", "kvd_decode_attn_static", "kvd_decode_attn_sv",
            "kvd_decode_attn_tail", "kvd_kv_append_f32", "kvd_select_blocks_per_head",
-           "kvd_decode_attn_per_head")
+           "kvd_decode_attn_per_head", "kvd_debug_wait_timeout")
 
 
 class KvdError(RuntimeError):
@@ -95,6 +95,7 @@ def lib():
         L.kvd_abi_version.restype = i32
         L.kvd_debug_qk_int8.argtypes = [cp, p, i32, p, p, p, p]
         L.kvd_debug_scores.argtypes = [cp, p, i32, p, p]
+        L.kvd_debug_wait_timeout.argtypes = [p, i32, p]
         _lib = L
     return _lib
 
@@ -359,6 +360,12 @@ def debug_qk_int8(cache: KVCache, q: torch.Tensor, dots: torch.Tensor, q_codes: 
         _stream(q, stream)))
 
 
+def debug_wait_timeout(status: torch.Tensor, limit_us: int, stream=None):
+    """Run the bounded-wait path on a wait that nothing ends (status: int32 [1])."""
+    _check("kvd_debug_wait_timeout", lib().kvd_debug_wait_timeout(
+        _ptr(status), int(limit_us), _stream(status, stream)))
+
+
 def debug_scores(cache: KVCache, q: torch.Tensor, ub: torch.Tensor, stream=None):
     _check("kvd_debug_scores", lib().kvd_debug_scores(
         cache.ref(), _ptr(q), int(q.shape[1]), _ptr(ub), _stream(q, stream)))
@@ -369,4 +376,4 @@ __all__ = ["F16", "INT8", "Q8_0", "Q4_0", "BLOCK", "HEAD_DIM", "KVCache", "KvdEr
            "kv_append_f32", "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
            "decode_attn_sv", "decode_attn_tail", "select_blocks_per_head",
            "decode_attn_per_head", "decode_step",
-           "decode_step_host", "debug_qk_int8", "debug_scores", "synth", "EXPORTS"]
+           "decode_step_host", "debug_qk_int8", "debug_scores", "debug_wait_timeout", "synth", "EXPORTS"]

@@ -558,6 +558,13 @@ kvd_status kvd_debug_qk_int8(const kvd_cache *cache, const float *q, int32_t n_h
                                        static_cast<cudaStream_t>(stream)));
 }
 
+kvd_status kvd_debug_wait_timeout(int32_t *dev_status, int32_t limit_us, void *stream) {
+    if (!dev_status || !aligned(dev_status, 4)) return KVD_ERR_INVALID;
+    if (limit_us < 1 || limit_us > 1000000) return KVD_ERR_INVALID;
+    return cuda_status(launch_wait_probe(dev_status, static_cast<uint64_t>(limit_us) * 1000u,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 kvd_status kvd_debug_scores(const kvd_cache *cache, const float *q, int32_t n_heads, float *ub,
                             void *stream) {
     kvd_status s = check_cache(cache);

@@ -76,18 +76,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Returns false
-// when `abort_flag` (shared memory) becomes non-zero or the time limit passes.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort_flag) {
+// when `abort_flag` (shared memory) becomes non-zero or limit_ns of wall time
+// pass.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity,
+                                                volatile int *abort_flag, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 15u) == 0) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
         }
     }
+}
+
+// mbar_wait_limit with the kernels' limit, kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort_flag) {
+    return mbar_wait_limit(bar, parity, abort_flag, kWaitLimitNs);
 }
 
 // L2 policy for data read once per step (K/V blocks): evict first.

@@ -98,6 +98,9 @@ cudaError_t launch_decode_per_head(const kvd_cache &c, const Geom &g, const Deco
                                    const int32_t *sel_cnt, float *out, float *partials,
                                    uint32_t *counters, cudaStream_t st, bool pdl);
 
+// A kernel whose one mbarrier wait runs out after limit_ns (selftest.cu).
+cudaError_t launch_wait_probe(int32_t *status, uint64_t limit_ns, cudaStream_t st);
+
 // The listed blocks exactly plus the moment tail of every other block
 // (decode_tail.cu); c.moments must be set.
 cudaError_t launch_decode_tail(const kvd_cache &c, const Geom &g, const DecodePlan &p,

@@ -171,6 +171,14 @@ def test_decode_tail_validation():
     assert _select(_cache(moments=FAKE + 8)) == INVALID
 
 
+def test_wait_timeout_validation():
+    L = kvd.lib()
+    assert L.kvd_debug_wait_timeout(None, 1000, None) == INVALID
+    assert L.kvd_debug_wait_timeout(FAKE + 2, 1000, None) == INVALID
+    assert L.kvd_debug_wait_timeout(FAKE, 0, None) == INVALID
+    assert L.kvd_debug_wait_timeout(FAKE, 1000001, None) == INVALID
+
+
 def test_append_validation():
     L = kvd.lib()
     s = _cache(length=4090)
