@@ -56,16 +56,16 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def kv_bytes_per_token(dtype):
-    # K row + V row, plus one f32 scale each (int8) or four f16 group scales
-    # each (q8_0, q4_0; a q4_0 row is 64 bytes)
+def kv_bytes_per_token(dtype, D=128):
+    # K row + V row, plus one f32 scale each (int8) or D / 32 f16 group scales
+    # each (q8_0, q4_0; a q4_0 row is D / 2 bytes)
     if dtype == kvd.INT8:
-        return 2 * 128 + 2 * 4
+        return 2 * D + 2 * 4
     if dtype == kvd.Q8_0:
-        return 2 * 128 + 2 * 4 * 2
+        return 2 * D + 2 * (D // 32) * 2
     if dtype == kvd.Q4_0:
-        return 2 * 64 + 2 * 4 * 2
-    return 2 * 2 * 128
+        return 2 * (D // 2) + 2 * (D // 32) * 2
+    return 2 * 2 * D
 
 
 def dtype_name(dtype):
@@ -85,7 +85,8 @@ def attended_tokens(sel_idx, sel_cnt, L):
 
 def decode_kernel_bytes(w, tokens, n_sel_total):
     # selected rows (+ scales), the block lists, q in, out
-    return (tokens * kv_bytes_per_token(w.dtype) + n_sel_total * 4 + w.B * w.H * w.D * 4 * 2)
+    return (tokens * kv_bytes_per_token(w.dtype, w.D) + n_sel_total * 4 +
+            w.B * w.H * w.D * 4 * 2)
 
 
 def step_bytes(w, tokens, n_sel_total, L1):
@@ -96,10 +97,10 @@ def step_bytes(w, tokens, n_sel_total, L1):
     forced = kvd.selected_count(L1, 0, w.sink_tokens, w.recent_tokens)
     n_cand = nb - forced
     P = w.B * w.Hkv
-    scored = P * n_cand * 2 * 128 * 2
+    scored = P * n_cand * 2 * w.D * 2
     keys = P * n_cand * 4 * 2
-    row_out = kv_bytes_per_token(w.dtype)
-    append = P * (2 * 128 * 2 + row_out + 2 * 128 * 2)
+    row_out = kv_bytes_per_token(w.dtype, w.D)
+    append = P * (2 * w.D * 2 + row_out + 2 * w.D * 2)
     return decode_kernel_bytes(w, tokens, n_sel_total) + scored + keys + append
 
 
@@ -335,11 +336,12 @@ def run_sweep(args):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    points = synth.context_sweep() if args.sweep == "context" else synth.coverage_sweep()
+    points = {"context": synth.context_sweep, "coverage": synth.coverage_sweep,
+              "head_dim": synth.head_dim_sweep}[args.sweep]()
     steps, warm = max(1, args.steps), max(3, args.warmup)
     for w in points:
         q, k, v, _ = synth.make_workload(w, device=dev)
-        cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev)
+        cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, head_dim=w.D, device=dev)
         kvd.kv_append(cache, k, v)
         del k, v
         ws = kvd.make_workspace(cache, w.H)
@@ -375,11 +377,14 @@ def run_sweep(args):
         tokens = attended_tokens(sel_idx, sel_cnt, L1) if n_sel else 0
         print(json.dumps({
             "sweep": args.sweep, "workload": w.name, "context": w.L, "batch": w.B,
-            "kv_dtype": dtype_name(w.dtype), "k_sel": w.k_sel,
+            "kv_dtype": dtype_name(w.dtype), "head_dim": w.D, "k_sel": w.k_sel,
+            "kernels": "tuned (head dim 128)" if w.D == 128 else "general head dim",
             "coverage": n_sel / (w.B * w.Hkv) / ((L1 + 63) // 64),
             "sparse_step_us": res[False], "dense_step_us": res[True],
             "dense_over_sparse": res[True] / res[False],
             "effective_kv_gbs": step_bytes(w, tokens, n_sel, L1) / (res[False] * 1e-6) / 1e9,
+            "dense_kv_gbs": (w.B * w.Hkv * L1 * kv_bytes_per_token(w.dtype, w.D) /
+                             (res[True] * 1e-6) / 1e9),
             "steps": steps, "l2": "write + read flush between steps"}), flush=True)
         del cache, ws
         torch.cuda.empty_cache()
@@ -595,7 +600,8 @@ def main():
     ap.add_argument("--context", type=int, default=None,
                     help="run the workload's recipe at this context instead (a multiple "
                          "of 64; a smaller case for profiling)")
-    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v", "tail", "gqa"],
+    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v", "tail", "gqa",
+                                        "head_dim"],
                     default=None,
                     help="instead of the bench line: sparse vs dense decode steps over the "
                          "context sweep (16K..1M, 25%% coverage) or the 128K x 8 coverage "

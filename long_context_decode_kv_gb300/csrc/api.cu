@@ -44,7 +44,14 @@ kvd_status check_cache(const kvd_cache *c) {
         c->dtype != KVD_Q4_0)
         return KVD_ERR_INVALID;
     if (c->batch < 1 || c->n_kv_heads < 1) return KVD_ERR_INVALID;
-    if (c->head_dim != kHeadDim) return KVD_ERR_UNSUPPORTED;
+    if (c->head_dim != kHeadDim) {
+        // other head dims: multiples of 16 up to 1024, f16 and int8 caches,
+        // without block means or per-sequence lengths
+        if (c->head_dim < 16 || c->head_dim > 1024 || c->head_dim % 16 != 0)
+            return KVD_ERR_UNSUPPORTED;
+        if (c->dtype != KVD_F16 && c->dtype != KVD_INT8) return KVD_ERR_UNSUPPORTED;
+        if (c->moments || c->seq_lens) return KVD_ERR_UNSUPPORTED;
+    }
     if (c->block != kBlock) return KVD_ERR_UNSUPPORTED;
     if (c->max_seq < kBlock || c->max_seq % kBlock != 0) return KVD_ERR_INVALID;
     if (c->len < 0 || c->len > c->max_seq) return KVD_ERR_INVALID;
@@ -69,6 +76,9 @@ kvd_status check_heads(const kvd_cache *c, int n_heads) {
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return KVD_ERR_UNSUPPORTED;
     return KVD_OK;
 }
+
+// A head dim the general kernels serve (the tuned ones take 128).
+bool general_d(const kvd_cache *c) { return c->head_dim != kHeadDim; }
 
 Geom make_geom(const kvd_cache *c, int n_heads, int len) {
     Geom g;
@@ -102,8 +112,12 @@ WsLayout ws_layout(const kvd_cache *c, int n_heads) {
     size_t off = 0;
     w.counters = off;  // one per query head: enough for one-head-per-CTA plans too
     off += align_up(static_cast<size_t>(g.B) * g.H * sizeof(uint32_t));
+    const size_t D = static_cast<size_t>(c->head_dim);
     w.partials = off;
-    off += align_up(decode_partials_bytes(g, w.plan));
+    off += align_up(general_d(c) ? gd_partials_bytes(static_cast<int>(P), g.G, c->head_dim,
+                                                     gd_splits(static_cast<int>(P), g.nbmax,
+                                                               device_sm_count()))
+                                 : decode_partials_bytes(g, w.plan));
     w.keys = off;  // key rows padded to 16 bytes
     off += align_up(P * ((g.nbmax + 3) / 4 * 4) * sizeof(uint32_t));
     // key ranges and tickets: only problems split over several CTAs use
@@ -120,13 +134,13 @@ WsLayout ws_layout(const kvd_cache *c, int n_heads) {
     w.sel_cnt = off;
     off += align_up(P * sizeof(int32_t));
     w.q = off;
-    off += align_up(static_cast<size_t>(g.B) * g.H * kHeadDim * sizeof(float));
+    off += align_up(static_cast<size_t>(g.B) * g.H * D * sizeof(float));
     w.k_new = off;
-    off += align_up(P * kHeadDim * sizeof(__half));
+    off += align_up(P * D * sizeof(__half));
     w.v_new = off;
-    off += align_up(P * kHeadDim * sizeof(__half));
+    off += align_up(P * D * sizeof(__half));
     w.out = off;
-    off += align_up(static_cast<size_t>(g.B) * g.H * kHeadDim * sizeof(float));
+    off += align_up(static_cast<size_t>(g.B) * g.H * D * sizeof(float));
     w.total = off;
     return w;
 }
@@ -171,6 +185,15 @@ SelScratch sel_scratch(void *ws, const WsLayout &w) {
 kvd_status select_impl(const kvd_cache *c, const float *q, int n_heads, int k_sel, int sink,
                        int recent, int32_t *sel_idx, int32_t *sel_cnt, void *ws,
                        const WsLayout &w, cudaStream_t st, const StepToken *tok = nullptr) {
+    if (general_d(c)) {
+        if (tok && launch_append_gd(*c, tok->k_new, tok->v_new, 1, tok->len0, st, false) !=
+                       cudaSuccess)
+            return KVD_ERR_CUDA;
+        int se, rb;
+        forced_range(c->len, sink, recent, &se, &rb);
+        return cuda_status(launch_select_gd(*c, q, n_heads, k_sel, se, rb, sel_idx, sel_cnt,
+                                            ws_at<uint32_t>(ws, w.keys), st));
+    }
     Geom g = make_geom(c, n_heads, c->len);
     g.seq_add = tok ? 1 : 0;  // a step's token: seq_lens does not count it yet
     const SelScratch scr = sel_scratch(ws, w);
@@ -188,6 +211,11 @@ kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float sc
     int max_blocks = dense ? g.NB : max_sel;
     if (max_blocks > g.NB) max_blocks = g.NB;
     if (max_blocks < 1) max_blocks = 1;
+    if (general_d(c)) {
+        if (sv_eps > 0.0f) return KVD_ERR_UNSUPPORTED;
+        return cuda_status(launch_decode_gd(*c, q, n_heads, scale, sel_idx, sel_cnt, max_blocks,
+                                            out, ws_at<float>(ws, w.partials), st));
+    }
     // the wide tile for listed blocks only: over every block (a long stream) the
     // two-CTA tile keeps two producers per SM and streams faster
     const DecodePlan p = plan_decode(g, max_blocks, device_sm_count(), false, !dense);
@@ -287,8 +315,12 @@ kvd_status append_impl(kvd_cache *cache, const void *k_new, const void *v_new, i
     if (n_new == 0) return KVD_OK;
     if (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)) return KVD_ERR_INVALID;
     if (static_cast<long long>(cache->len) + n_new > cache->max_seq) return KVD_ERR_CAPACITY;
-    const cudaError_t e = launch_append(*cache, k_new, v_new, n_new,
-                                        static_cast<cudaStream_t>(stream), true, f32_in);
+    const cudaError_t e =
+        general_d(cache)
+            ? launch_append_gd(*cache, k_new, v_new, n_new, cache->len,
+                               static_cast<cudaStream_t>(stream), f32_in)
+            : launch_append(*cache, k_new, v_new, n_new, static_cast<cudaStream_t>(stream), true,
+                            f32_in);
     if (e != cudaSuccess) return KVD_ERR_CUDA;
     cache->len += n_new;
     return KVD_OK;
@@ -369,6 +401,7 @@ kvd_status kvd_select_blocks_per_head(const kvd_cache *cache, const float *q, in
                                       void *stream) {
     kvd_status s = check_select_args(cache, n_heads, k_sel, sink_tokens, recent_tokens);
     if (s != KVD_OK) return s;
+    if (general_d(cache)) return KVD_ERR_UNSUPPORTED;  // per-head lists: D = 128 only
     if (!q || !aligned(q, 16)) return KVD_ERR_INVALID;
     if (!sel_idx || !aligned(sel_idx, 4) || !sel_cnt || !aligned(sel_cnt, 4))
         return KVD_ERR_INVALID;
@@ -387,6 +420,7 @@ kvd_status kvd_decode_attn_per_head(const kvd_cache *cache, const float *q, int3
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (general_d(cache)) return KVD_ERR_UNSUPPORTED;  // per-head lists: D = 128 only
     if (cache->len < 1 || max_sel < 0) return KVD_ERR_INVALID;
     if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
     if (!sel_idx || !aligned(sel_idx, 4) || !sel_cnt || !aligned(sel_cnt, 4))
@@ -404,6 +438,7 @@ kvd_status kvd_decode_attn_tail(const kvd_cache *cache, const float *q, int32_t 
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (general_d(cache)) return KVD_ERR_UNSUPPORTED;  // block means: D = 128 only
     if (cache->len < 1 || max_sel < 0 || !cache->moments) return KVD_ERR_INVALID;
     if (!q || !aligned(q, 16) || !out || !aligned(out, 16)) return KVD_ERR_INVALID;
     if (!sel_idx || !aligned(sel_idx, 4) || !sel_cnt || !aligned(sel_cnt, 4))
@@ -451,7 +486,10 @@ kvd_status kvd_decode_step(kvd_cache *cache, const float *q, const void *k_new,
     if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dense) {
-        if (launch_append(*cache, k_new, v_new, 1, st, true) != cudaSuccess) return KVD_ERR_CUDA;
+        const cudaError_t e = general_d(cache)
+                                  ? launch_append_gd(*cache, k_new, v_new, 1, cache->len, st, false)
+                                  : launch_append(*cache, k_new, v_new, 1, st, true);
+        if (e != cudaSuccess) return KVD_ERR_CUDA;
         cache->len += 1;
         return decode_impl(cache, q, n_heads, softmax_scale, nullptr, nullptr, 0, out, workspace,
                            w, st, true);
@@ -510,8 +548,8 @@ kvd_status kvd_decode_step_host(kvd_cache *cache, const float *q_host, const voi
     const WsLayout w = ws_layout(cache, n_heads);
     if ((s = check_ws(workspace, workspace_bytes, w.total)) != KVD_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t qb = static_cast<size_t>(cache->batch) * n_heads * kHeadDim * sizeof(float);
-    const size_t kb = static_cast<size_t>(cache->batch) * cache->n_kv_heads * kHeadDim * 2;
+    const size_t qb = static_cast<size_t>(cache->batch) * n_heads * cache->head_dim * sizeof(float);
+    const size_t kb = static_cast<size_t>(cache->batch) * cache->n_kv_heads * cache->head_dim * 2;
     // Buffers the GPU can reach directly are used in place by the kernels;
     // the others are staged through the workspace by copies on the stream.
     float *q_dev = static_cast<float *>(device_view(q_host));
@@ -549,6 +587,7 @@ kvd_status kvd_debug_qk_int8(const kvd_cache *cache, const float *q, int32_t n_h
     kvd_status s = check_cache(cache);
     if (s != KVD_OK) return s;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (general_d(cache)) return KVD_ERR_UNSUPPORTED;  // the tuned decode only
     if (cache->dtype != KVD_INT8 || cache->len < 1) return KVD_ERR_INVALID;
     if (!q || !aligned(q, 16) || !dots || !aligned(dots, 4) || !q_codes ||
         !aligned(q_codes, 4) || !q_scales || !aligned(q_scales, 4))
@@ -571,6 +610,7 @@ kvd_status kvd_debug_scores(const kvd_cache *cache, const float *q, int32_t n_he
     if (s != KVD_OK) return s;
     if (cache->seq_lens) return KVD_ERR_UNSUPPORTED;
     if ((s = check_heads(cache, n_heads)) != KVD_OK) return s;
+    if (general_d(cache)) return KVD_ERR_UNSUPPORTED;  // the tuned scorer only
     if (cache->len < 1) return KVD_ERR_INVALID;
     if (!q || !aligned(q, 16) || !ub || !aligned(ub, 4)) return KVD_ERR_INVALID;
     const Geom g = make_geom(cache, n_heads, cache->len);

@@ -98,6 +98,21 @@ cudaError_t launch_decode_per_head(const kvd_cache &c, const Geom &g, const Deco
                                    const int32_t *sel_cnt, float *out, float *partials,
                                    uint32_t *counters, cudaStream_t st, bool pdl);
 
+// Head dims other than 128 (general_d.cu, general_d_decode.cu; f16 and int8
+// caches without block means or per-sequence lengths).  The append writes
+// tokens [len0, len0 + n_new); the selection takes the candidate range
+// [se, rb) and scratch keys rows of round_up(max_seq / 64, 4); the decode
+// writes the splits' partials (gd_partials_bytes) and then out.
+cudaError_t launch_append_gd(const kvd_cache &c, const void *k_new, const void *v_new,
+                             int n_new, int len0, cudaStream_t st, bool f32_in);
+cudaError_t launch_select_gd(const kvd_cache &c, const float *q, int n_heads, int k_sel, int se,
+                             int rb, int32_t *sel_idx, int32_t *sel_cnt, uint32_t *keys,
+                             cudaStream_t st);
+int gd_splits(int problems, int max_blocks, int sm_count);
+size_t gd_partials_bytes(int problems, int G, int D, int splits);
+cudaError_t launch_decode_gd(const kvd_cache &c, const float *q, int n_heads, float scale,
+                             const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
+                             float *out, float *partials, cudaStream_t st);
 // A kernel whose one mbarrier wait runs out after limit_ns (selftest.cu).
 cudaError_t launch_wait_probe(int32_t *status, uint64_t limit_ns, cudaStream_t st);
 

@@ -106,6 +106,19 @@ def context_sweep(frac: float = 0.25):
     return out
 
 
+def head_dim_sweep(frac: float = 0.25, L: int = 131072):
+    """The 32K GQA recipe at 128K context with head dims 64, 96, 128 and 256,
+    on f16 and int8 caches, each at `frac` block coverage.  Head dim 128
+    runs the tuned kernels, the others the general ones."""
+    k_sel = coverage_budget(L, 64, frac, QWEN3_32K.sink_tokens, QWEN3_32K.recent_tokens)
+    out = []
+    for dtype, dn in ((F16, "f16"), (INT8, "int8")):
+        for D in (64, 96, 128, 256):
+            out.append(QWEN3_32K.with_(name=f"gqa_{dn}_128k_d{D}_cov{round(frac * 100)}", L=L,
+                                       D=D, dtype=dtype, k_sel=k_sel))
+    return out
+
+
 def coverage_sweep():
     """The 128K x 8 int8 recipe with K_SEL = NB * c, c = 1/64 .. 1/2 (plus the
     sink and recent blocks)."""

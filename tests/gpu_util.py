@@ -36,7 +36,7 @@ def make_pair(dtype, k, v, max_seq=None, chunks=None, moments=False):
     """GPU cache and oracle cache filled from k, v ([B, L, Hkv, D] f16, on the GPU)."""
     B, L, Hkv, D = k.shape
     max_seq = max_seq or round_up(max(L, 1) + 64)
-    gc = kvd.KVCache(dtype, B, Hkv, max_seq, device=dev(), moments=moments)
+    gc = kvd.KVCache(dtype, B, Hkv, max_seq, head_dim=D, device=dev(), moments=moments)
     oc = oracle.OracleCache(dtype, B, Hkv, D, max_seq, 64)
     chunks = chunks or [L]
     s = 0

@@ -78,7 +78,7 @@ def test_workspace_bytes():
     assert n > 0 and n % 256 == 0
     assert _ws(_cache(max_seq=8192)) > n           # grows with capacity
     assert _ws(s, 33) == 0                          # 33 % 8 != 0
-    assert _ws(_cache(D=64)) == 0
+    assert _ws(_cache(D=72)) == 0                   # D not a multiple of 16
     assert _ws(_cache(dtype=7)) == 0
 
 
@@ -89,7 +89,12 @@ def _select(s, n_heads=32, k_sel=4, sink=4, recent=64, ws_bytes=None, q=FAKE, ws
 
 
 def test_select_validation():
-    assert _select(_cache(D=64)) == UNSUPPORTED
+    assert _select(_cache(D=72)) == UNSUPPORTED              # not a multiple of 16
+    assert _select(_cache(D=1040)) == UNSUPPORTED            # above 1024
+    assert _select(_cache(D=0)) == UNSUPPORTED
+    assert _select(_cache(dtype=kvd.Q8_0, D=64)) == UNSUPPORTED  # group types: D = 128
+    assert _select(_cache(D=64, moments=FAKE)) == UNSUPPORTED    # block means: D = 128
+    assert _select(_cache(D=64, seq_lens=FAKE)) == UNSUPPORTED   # per-sequence: D = 128
     assert _select(_cache(blk=32)) == UNSUPPORTED
     assert _select(_cache(), n_heads=12) == INVALID
     assert _select(_cache(), n_heads=24) == UNSUPPORTED      # group of 3
@@ -130,7 +135,7 @@ def test_decode_validation():
     assert L.kvd_decode_attn(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, FAKE, n - 256,
                              None) == WORKSPACE
     assert L.kvd_decode_attn_dense(C.byref(s), FAKE, 30, 0.1, FAKE, FAKE, n, None) == INVALID
-    assert L.kvd_decode_attn_dense(C.byref(_cache(head_dim=256)), FAKE, 32, 0.1, FAKE, FAKE, n,
+    assert L.kvd_decode_attn_dense(C.byref(_cache(head_dim=264)), FAKE, 32, 0.1, FAKE, FAKE, n,
                                    None) == UNSUPPORTED
     assert L.kvd_decode_attn_dense(C.byref(s), FAKE, 32, 0.1, FAKE, None, n, None) == WORKSPACE
 
@@ -169,6 +174,31 @@ def test_decode_tail_validation():
                               None) == UNSUPPORTED
     # a cache that keeps moments is otherwise an ordinary cache
     assert _select(_cache(moments=FAKE + 8)) == INVALID
+
+
+def test_general_head_dims():
+    L = kvd.lib()
+    for D in (16, 64, 80, 96, 256, 1024):
+        for dt in (kvd.F16, kvd.INT8):
+            s = _cache(dtype=dt, D=D)
+            need = L.kvd_workspace_bytes(C.byref(s), 32)
+            assert need > 0 and need % 256 == 0, (D, dt)
+            # validation runs first and still applies
+            assert _select(s, n_heads=24, ws_bytes=need) == UNSUPPORTED
+            assert _select(s, k_sel=-1, ws_bytes=need) == INVALID
+            assert _select(s, ws_bytes=need - 256) == WORKSPACE
+    big = L.kvd_workspace_bytes(C.byref(_cache(D=1024)), 32)
+    assert big > L.kvd_workspace_bytes(C.byref(_cache(D=64)), 32)
+    assert L.kvd_workspace_bytes(C.byref(_cache(D=72)), 32) == 0
+    s = _cache(D=64)
+    n = L.kvd_workspace_bytes(C.byref(s), 32)
+    # the calls only the D = 128 kernels serve
+    assert L.kvd_select_blocks_per_head(C.byref(s), FAKE, 32, 4, 4, 64, FAKE, FAKE, FAKE, n,
+                                        None) == UNSUPPORTED
+    assert L.kvd_decode_attn_per_head(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, FAKE, FAKE, n,
+                                      None) == UNSUPPORTED
+    assert L.kvd_debug_scores(C.byref(s), FAKE, 32, FAKE, None) == UNSUPPORTED
+    assert L.kvd_debug_qk_int8(C.byref(s), FAKE, 32, FAKE, FAKE, FAKE, None) == UNSUPPORTED
 
 
 def test_wait_timeout_validation():
