@@ -375,6 +375,28 @@ def run_sweep(args):
         L1 = w.L + 1
         n_sel = int(sel_cnt.sum().item())
         tokens = attended_tokens(sel_idx, sel_cnt, L1) if n_sel else 0
+        # the step's selection and sparse decode timed apart (same flush)
+        cache.len = L1
+        max_sel = kvd.selected_count(L1, w.k_sel, w.sink_tokens, w.recent_tokens)
+        calls = {"select": lambda: kvd.select_blocks(cache, q, w.k_sel, w.sink_tokens,
+                                                     w.recent_tokens, sel_idx, sel_cnt, ws),
+                 "decode": lambda: kvd.decode_attn(cache, q, w.scale, sel_idx, sel_cnt, max_sel,
+                                                   out, ws)}
+        part = {}
+        for name, fn in calls.items():
+            ms = []
+            for i in range(warm + steps):
+                flush.fill_(i & 0xFF)
+                drain.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                if i >= warm:
+                    ms.append((e0, e1))
+            torch.cuda.synchronize()
+            part[name] = statistics.mean(a.elapsed_time(b) for a, b in ms) * 1e3
+        assert cache.device_status() == 0, "device-side fault reported"
         print(json.dumps({
             "sweep": args.sweep, "workload": w.name, "context": w.L, "batch": w.B,
             "kv_dtype": dtype_name(w.dtype), "head_dim": w.D, "k_sel": w.k_sel,
@@ -382,6 +404,8 @@ def run_sweep(args):
             "coverage": n_sel / (w.B * w.Hkv) / ((L1 + 63) // 64),
             "sparse_step_us": res[False], "dense_step_us": res[True],
             "dense_over_sparse": res[True] / res[False],
+            "select_us": part["select"], "decode_us": part["decode"],
+            "decode_kv_gbs": decode_kernel_bytes(w, tokens, n_sel) / (part["decode"] * 1e-6) / 1e9,
             "effective_kv_gbs": step_bytes(w, tokens, n_sel, L1) / (res[False] * 1e-6) / 1e9,
             "dense_kv_gbs": (w.B * w.Hkv * L1 * kv_bytes_per_token(w.dtype, w.D) /
                              (res[True] * 1e-6) / 1e9),
@@ -600,6 +624,10 @@ def main():
     ap.add_argument("--context", type=int, default=None,
                     help="run the workload's recipe at this context instead (a multiple "
                          "of 64; a smaller case for profiling)")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="run the workload's recipe with this head dim instead (a multiple "
+                         "of 16 up to 1024; 128 runs the tuned kernels, others the general "
+                         "ones)")
     ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v", "tail", "gqa",
                                         "head_dim"],
                     default=None,
@@ -622,6 +650,10 @@ def main():
         if args.context < 64 or args.context % 64:
             ap.error("--context must be a positive multiple of 64")
         w = w.with_(L=args.context)
+    if args.head_dim is not None:
+        if not (16 <= args.head_dim <= 1024 and args.head_dim % 16 == 0):
+            ap.error("--head-dim must be a multiple of 16 in [16, 1024]")
+        w = w.with_(D=args.head_dim)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -631,7 +663,7 @@ def main():
     warmup = max(3, args.warmup)
 
     q, k, v, needles = synth.make_workload(w, device=dev)
-    cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, device=dev)
+    cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, head_dim=w.D, device=dev)
     kvd.kv_append(cache, k, v)
     ws = kvd.make_workspace(cache, w.H)
     nbmax = cache.max_seq // 64
@@ -766,8 +798,8 @@ def main():
         "step_bytes": sbytes,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "decode_kernel (kvd_decode_attn)", "bytes": dbytes,
-                     "us": dec_us, "traffic": measured_traffic(w.name, tokens),
+                     "kernel": ("decode_kernel" if w.D == 128 else "gd_decode_kernel") + " (kvd_decode_attn)", "bytes": dbytes,
+                     "us": dec_us, "traffic": measured_traffic(w.name, tokens) if w.D == 128 else None,
                      "tokens_attended": tokens},
         "breakdown_us": {"append": statistics.mean(app_ms) * 1e3,
                          "select": statistics.mean(sel_ms) * 1e3, "decode": dec_us,

@@ -116,7 +116,7 @@ WsLayout ws_layout(const kvd_cache *c, int n_heads) {
     w.partials = off;
     off += align_up(general_d(c) ? gd_partials_bytes(static_cast<int>(P), g.G, c->head_dim,
                                                      gd_splits(static_cast<int>(P), g.nbmax,
-                                                               device_sm_count()))
+                                                               device_sm_count(), 0))
                                  : decode_partials_bytes(g, w.plan));
     w.keys = off;  // key rows padded to 16 bytes
     off += align_up(P * ((g.nbmax + 3) / 4 * 4) * sizeof(uint32_t));

@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kRankThreads = 1024;
 constexpr int kScoreWarps = 8;
-constexpr int kScoreBlocksPerCta = 64;
+constexpr int kScoreBlocksPerCta = 16;  // two per warp: many loads in flight
 
 __device__ __forceinline__ float in_value(const __half *p, size_t i) { return __half2float(p[i]); }
 __device__ __forceinline__ float in_value(const float *p, size_t i) { return p[i]; }
@@ -121,7 +121,7 @@ __device__ __forceinline__ uint32_t gd_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Keys of blocks [64 * blockIdx.x, +64) of problem p = blockIdx.y (sequence
+// Keys of blocks [16 * blockIdx.x, +16) of problem p = blockIdx.y (sequence
 // p / Hkv, KV head p % Hkv): warp w scores blocks w, w + 8, ..; lane l takes
 // channels l, l + 32, .. of the G query heads (query in shared memory).
 template <int G>
@@ -219,14 +219,31 @@ __global__ void __launch_bounds__(kRankThreads) gd_rank_kernel(const uint32_t *k
                 if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
             }
             __syncthreads();
-            if (tid == 0) {
-                int above = 0, bin = 255;
-                for (; bin > 0; --bin) {
-                    if (above + static_cast<int>(hist[bin]) >= need) break;
-                    above += static_cast<int>(hist[bin]);
+            if (tid < 32) {
+                // the bin holding the need-th largest: lane l sums bins
+                // 8 (31 - l) .. +7, an inclusive scan over lanes counts the
+                // keys from the top, and the first lane to reach need walks
+                // its own 8 bins downward
+                const int lo = 8 * (31 - tid);
+                int own = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) own += static_cast<int>(hist[lo + i]);
+                int incl = own;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
                 }
-                s_need = need - above;
-                s_prefix = prefix | (static_cast<uint32_t>(bin) << shift);
+                const unsigned reach = __ballot_sync(0xffffffffu, incl >= need);
+                if (tid == __ffs(reach) - 1) {
+                    int above = incl - own, bin = lo + 7;
+                    for (; bin > lo; --bin) {
+                        if (above + static_cast<int>(hist[bin]) >= need) break;
+                        above += static_cast<int>(hist[bin]);
+                    }
+                    s_need = need - above;
+                    s_prefix = prefix | (static_cast<uint32_t>(bin) << shift);
+                }
             }
             __syncthreads();
             need = s_need;

@@ -108,7 +108,7 @@ cudaError_t launch_append_gd(const kvd_cache &c, const void *k_new, const void *
 cudaError_t launch_select_gd(const kvd_cache &c, const float *q, int n_heads, int k_sel, int se,
                              int rb, int32_t *sel_idx, int32_t *sel_cnt, uint32_t *keys,
                              cudaStream_t st);
-int gd_splits(int problems, int max_blocks, int sm_count);
+int gd_splits(int problems, int max_blocks, int sm_count, int per_sm);
 size_t gd_partials_bytes(int problems, int G, int D, int splits);
 cudaError_t launch_decode_gd(const kvd_cache &c, const float *q, int n_heads, float scale,
                              const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
