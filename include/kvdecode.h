@@ -54,7 +54,8 @@ extern "C" {
 typedef enum {
     KVD_OK = 0,
     KVD_ERR_INVALID = 1,      /* bad argument: NULL/misaligned pointer, bad size */
-    KVD_ERR_UNSUPPORTED = 2,  /* legal but not built: head_dim != 128, block != 64, ... */
+    KVD_ERR_UNSUPPORTED = 2,  /* legal but not built: block != 64, a head_dim that is not
+                                 a multiple of 16 in [16, 1024], ... */
     KVD_ERR_CAPACITY = 3,     /* append would pass max_seq */
     KVD_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
     KVD_ERR_TIMEOUT = 5,      /* device only: a bounded wait ran out (dev_status) */
@@ -74,8 +75,8 @@ typedef enum { KVD_F16 = 0, KVD_INT8 = 1, KVD_Q8_0 = 2, KVD_Q4_0 = 3 } kvd_kv_dt
  *   v_scale     q8_0, q4_0: [batch, n_kv_heads, max_seq, head_dim / 32] f16
  *               (NULL for f16)
  *   kbounds     [batch, n_kv_heads, max_seq / block, head_dim, 2]  f16
- * kbounds holds the per-(KV head, block) channel-wise key envelope [QUEST
- * Method: "Store kmin[head_dim], kmax[head_dim] per block"] as interleaved
+ * kbounds holds the per-(KV head, block) channel-wise key envelope (QUEST,
+ * Method: one minimum and one maximum per channel for every block) as interleaved
  * pairs: kbounds[..., d, 0] = kmin[d], kbounds[..., d, 1] = kmax[d] (one
  * contiguous 512-byte row per block).  It is always taken from the f16 keys
  * before quantization [QUEST All-KV-types composition].
@@ -122,7 +123,12 @@ typedef struct kvd_cache {
     int32_t dtype;        /* kvd_kv_dtype */
     int32_t batch;        /* independent sequences, >= 1 */
     int32_t n_kv_heads;   /* Hkv >= 1 */
-    int32_t head_dim;     /* D; only 128 is built */
+    int32_t head_dim;     /* D: 128 (every cache type and call), or any other multiple
+                             of 16 up to 1024 ("cpu-attn", Requirements and limits)
+                             for f16 and int8 caches without moments or seq_lens,
+                             through kvd_kv_append(_f32), kvd_select_blocks,
+                             kvd_decode_attn(_dense), kvd_decode_step(_host) and
+                             kvd_workspace_bytes; other calls return UNSUPPORTED */
     int32_t max_seq;      /* capacity in tokens, a multiple of `block` */
     int32_t block;        /* B_SEL; only 64 is built [QUEST Knobs: default 64] */
     int32_t len;          /* tokens currently cached, 0 <= len <= max_seq */
@@ -415,7 +421,7 @@ KVD_API int32_t kvd_abi_version(void);
 /* by the same device routines the decode and select kernels use.         */
 /*   kvd_debug_qk_int8: dots [batch, n_heads, len] int32, q_codes [batch,   */
 /*   n_heads, head_dim] int8, q_scales [batch, n_heads] f32 (int8 cache     */
-/*   only)  [CPUATT Method "Logit dots are exact int32"].                   */
+/*   only)  [CPUATT Method: integer logit dots, exact].                      */
 /*   kvd_debug_scores: ub [batch, n_kv_heads, NB] f32, the group bound UB(j)*/
 /*   of every block j < NB = ceil(len / block)  [QUEST Method].             */
 /* ---------------------------------------------------------------------- */

@@ -805,7 +805,7 @@ void orc_attend_q4_0(int D, int L, int blk, const int8_t *qc, float q_scale, dou
 }
 
 /* ------------------------------------------------------------------ */
-/* Exact integer q.k dots  [CPUATT Method "Logit dots are exact int32"].*/
+/* Exact integer q.k dots  [CPUATT Method: integer logit dots, exact].     */
 /*   dot_t = sum_d q_code[d] * k_code_t[d]   (|dot| <= D*127*127)       */
 /* ------------------------------------------------------------------ */
 void orc_qk_int8(int D, long n, const int8_t *qc, const int8_t *K, int64_t *dots)
@@ -855,8 +855,8 @@ void orc_attend_int8(int D, int L, int blk, const int8_t *qc, float q_scale, dou
 
 /* ------------------------------------------------------------------ */
 /* Attention over float rows (dequantized cache)  [CPUATT Correctness:  */
-/* "fp32 attention on the dequantized cache"].  q: [D] f32; K, V: the   */
-/* int8 rows times their scales, formed here in binary64.               */
+/* the reference is float attention over the dequantized rows].  q: [D] */
+/* f32; K, V: the int8 rows times their scales, formed here in binary64. */
 /* With q_code != NULL the query is the dequantized int8 query          */
 /* (q_scale * q_code) instead of q.                                      */
 /* ------------------------------------------------------------------ */
