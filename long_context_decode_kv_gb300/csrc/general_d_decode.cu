@@ -97,7 +97,9 @@ __host__ __device__ constexpr int stage_bytes(int D, int elt, int T, bool scales
     return 2 * T * D * elt + (scales ? 2 * T * 4 : 0);
 }
 
-template <int DT, int G>
+// DC: the head dim fixed at compile time (its loops then fold), or 0 to read
+// it from the cache.
+template <int DT, int G, int DC>
 __global__ void __launch_bounds__(kThreads, G <= 2 ? 4 : (G <= 4 ? 3 : (G <= 8 ? 2 : 1)))
 gd_decode_kernel(kvd_cache c, const float *q, int H,
                                                              float scale_log2,
@@ -107,7 +109,7 @@ gd_decode_kernel(kvd_cache c, const float *q, int H,
     constexpr int kElt = DT == KVD_F16 ? 2 : 1;
     constexpr bool kScales = DT != KVD_F16;
     extern __shared__ __align__(16) float smem[];
-    const int D = c.head_dim;
+    const int D = DC > 0 ? DC : c.head_dim;
     const int T = tile_tokens(D, kElt), TPB = kBlock / T;
     const int SB = stage_bytes(D, kElt, T, kScales);
     float *sc = smem;               // [G][64] scores, then weights
@@ -471,7 +473,7 @@ __global__ void __launch_bounds__(128) gd_merge_kernel(const float *part_acc,
     }
 }
 
-template <int DT, int G>
+template <int DT, int G, int DC = 0>
 cudaError_t decode_g(const kvd_cache &c, const float *q, int H, float scale_log2,
                      const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
                      float *partials, int *splits_out, cudaStream_t st) {
@@ -480,7 +482,7 @@ cudaError_t decode_g(const kvd_cache &c, const float *q, int H, float scale_log2
     const size_t smem = (static_cast<size_t>(G) * (kBlock + 4) + static_cast<size_t>(G) * c.head_dim) *
                             sizeof(float) +
                         static_cast<size_t>(kStages) * stage_bytes(c.head_dim, kElt, T, DT != KVD_F16);
-    auto kern = gd_decode_kernel<DT, G>;
+    auto kern = gd_decode_kernel<DT, G, DC>;
     // one wave: the CTAs that fit on every SM at once, shared by the problems
     static LaunchCache lc;
     int occ = 0;
@@ -500,7 +502,15 @@ template <int DT>
 cudaError_t decode_dt(const kvd_cache &c, const float *q, int H, float scale_log2,
                       const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
                       float *partials, int *splits, cudaStream_t st) {
-    switch (H / c.n_kv_heads) {
+    // common head dims (64, 96, 256) of GQA groups of 4 and 8, with folded loops
+    const int G = H / c.n_kv_heads;
+    if (c.head_dim == 64 && G == 4) return decode_g<DT, 4, 64>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
+    if (c.head_dim == 64 && G == 8) return decode_g<DT, 8, 64>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
+    if (c.head_dim == 96 && G == 4) return decode_g<DT, 4, 96>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
+    if (c.head_dim == 96 && G == 8) return decode_g<DT, 8, 96>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
+    if (c.head_dim == 256 && G == 4) return decode_g<DT, 4, 256>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
+    if (c.head_dim == 256 && G == 8) return decode_g<DT, 8, 256>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
+    switch (G) {
         case 1: return decode_g<DT, 1>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
         case 2: return decode_g<DT, 2>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
         case 4: return decode_g<DT, 4>(c, q, H, scale_log2, sel_idx, sel_cnt, max_blocks, partials, splits, st);
