@@ -122,11 +122,13 @@ def _stream(t: torch.Tensor, stream=None):
 class KVCache:
     """Caller-owned cache tensors plus the C descriptor that points at them.
 
-    k, v      [B, Hkv, max_seq, 128]  float16 or int8 codes, or
-              [B, Hkv, max_seq, 64]   uint8 pairs of 4-bit codes (q4_0)
+    k, v      [B, Hkv, max_seq, D]    float16 or int8 codes, or
+              [B, Hkv, max_seq, D/2]  uint8 pairs of 4-bit codes (q4_0); D = head_dim:
+              128, or any multiple of 16 up to 1024 for f16 / int8 caches without
+              moments or seq_lens
     k_scale   [B, Hkv, max_seq]       float32 (int8), or
               [B, Hkv, max_seq, 4]    float16 group scales (q8_0, q4_0); same for v_scale
-    kbounds   [B, Hkv, max_seq // 64, 128, 2] float16: (kmin, kmax) per channel
+    kbounds   [B, Hkv, max_seq // 64, D, 2] float16: (kmin, kmax) per channel
     status    [1] int32 device word for device-side faults
     moments   [B, Hkv, max_seq // 64, 2, 128] float16 block means of K then V
               (only with moments=True: the moment tail of decode_attn_tail)
@@ -246,13 +248,13 @@ def status_string(code: int) -> str:
 
 
 def kv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
-    """k_new, v_new: [B, n_new, Hkv, 128] float16 on the cache's device."""
+    """k_new, v_new: [B, n_new, Hkv, D] float16 on the cache's device."""
     _check("kvd_kv_append", lib().kvd_kv_append(cache.ref(), _ptr(k_new), _ptr(v_new),
                                                 int(k_new.shape[1]), _stream(k_new, stream)))
 
 
 def kv_append_f32(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None):
-    """k_new, v_new: [B, n_new, Hkv, 128] float32 on the cache's device."""
+    """k_new, v_new: [B, n_new, Hkv, D] float32 on the cache's device."""
     _check("kvd_kv_append_f32", lib().kvd_kv_append_f32(cache.ref(), _ptr(k_new), _ptr(v_new),
                                                         int(k_new.shape[1]),
                                                         _stream(k_new, stream)))

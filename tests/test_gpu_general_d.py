@@ -10,7 +10,8 @@ largest (1024), with group sizes 1 to 16.
   * selection: identical to the oracle's top-K up to the tie window;
   * decode: within the cache type's bar and 1e-4 of the oracle's attention
     on the GPU's lists, sparse and dense, and bit-identical on a repeat;
-  * decode steps: three kvd_decode_step calls, sparse and dense.
+  * decode steps: three kvd_decode_step calls, sparse and dense, and the
+    host-buffer step (pinned, pageable, mixed) equal to the device step.
 """
 import numpy as np
 import pytest
@@ -18,8 +19,7 @@ import torch
 
 import long_context_decode_kv_gb300 as kvd
 import oracle
-from gpu_util import (TIE_REL, assert_outputs, check_selection, dev, make_pair, scale_for,
-                      seeded)
+from gpu_util import assert_outputs, check_selection, dev, make_pair, scale_for, seeded
 
 pytestmark = pytest.mark.gpu
 DTYPES = [kvd.F16, kvd.INT8]
@@ -216,3 +216,33 @@ def test_decode_steps(dtype, D, G, dense):
         else:
             check_selection(sel_idx, sel_cnt, oc, q.cpu().numpy(), k_sel, 4, 64, G)
             _check_outputs(dtype, gc, oc, q, out, G, D, sel_idx, sel_cnt, f"step {step}")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("D,pinned", [(96, "none"), (256, "mixed"), (48, "all")])
+def test_host_step_equals_device_step(dtype, D, pinned):
+    # the host-buffer step stages (or maps) D-channel rows and equals the
+    # device step bit for bit
+    B, Hkv, G, L0 = 2, 2, 4, 64 * 9 + 7
+    k = seeded((B, L0, Hkv, D), 41 + D)
+    v = seeded((B, L0, Hkv, D), 42 + D)
+    a, _ = make_pair(dtype, k, v, max_seq=64 * 11)
+    b, _ = make_pair(dtype, k, v, max_seq=64 * 11)
+    wa = kvd.make_workspace(a, Hkv * G)
+    wb = kvd.make_workspace(b, Hkv * G)
+    for s in range(3):
+        q = seeded((B, Hkv * G, D), 50 + s, dtype=torch.float32)
+        kn = seeded((B, 1, Hkv, D), 60 + s)
+        vn = seeded((B, 1, Hkv, D), 70 + s)
+        out_d = torch.empty(B, Hkv * G, D, device=dev())
+        kvd.decode_step(a, q, kn, vn, scale_for(D), 3, 4, 64, out_d, wa)
+        pin = {"all": (1, 1, 1, 1), "none": (0, 0, 0, 0), "mixed": (1, 0, 1, 0)}[pinned]
+        qh, kh, vh = (t.cpu().pin_memory() if p else t.cpu().clone()
+                      for t, p in zip((q, kn, vn), pin[:3]))
+        out_h = torch.empty(B, Hkv * G, D)
+        out_h = out_h.pin_memory() if pin[3] else out_h
+        kvd.decode_step_host(b, qh, kh, vh, scale_for(D), 3, 4, 64, out_h, wb)
+        torch.cuda.synchronize()
+        assert torch.equal(out_d.cpu(), out_h)
+    assert a.len == b.len == L0 + 3
+    assert a.device_status() == b.device_status() == 0
