@@ -199,6 +199,9 @@ def test_general_head_dims():
                                       None) == UNSUPPORTED
     assert L.kvd_debug_scores(C.byref(s), FAKE, 32, FAKE, None) == UNSUPPORTED
     assert L.kvd_debug_qk_int8(C.byref(s), FAKE, 32, FAKE, FAKE, FAKE, None) == UNSUPPORTED
+    # sparse-V with eps > 0 is a tuned-kernel mode (refused before any launch)
+    assert L.kvd_decode_attn_sv(C.byref(s), FAKE, 32, 0.1, FAKE, FAKE, 10, 0.5, FAKE, FAKE, n,
+                                None) == UNSUPPORTED
 
 
 def test_wait_timeout_validation():
