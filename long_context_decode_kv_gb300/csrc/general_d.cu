@@ -155,12 +155,14 @@ __device__ __forceinline__ uint32_t gd_key(float x) {
 // Keys of blocks [16 * blockIdx.x, +16) of problem p = blockIdx.y (sequence
 // p / Hkv, KV head p % Hkv): warp w scores blocks w, w + 8, ..; lane l takes
 // channels l, l + 32, .. of the G query heads (query in shared memory).
-template <int G>
+// DC: the head dim fixed at compile time (its loops then fold), or 0 to read
+// it from the cache.
+template <int G, int DC>
 __global__ void __launch_bounds__(kScoreWarps * 32) gd_score_kernel(kvd_cache c, const float *q,
                                                                     int H, int NB, uint32_t *keys,
                                                                     int key_stride) {
     extern __shared__ float sq[];  // [G][D]
-    const int D = c.head_dim;
+    const int D = DC > 0 ? DC : c.head_dim;
     const int p = blockIdx.y, b = p / c.n_kv_heads, h = p % c.n_kv_heads;
     const float *qp = q + (static_cast<size_t>(b) * H + static_cast<size_t>(h) * G) * D;
     for (int i = threadIdx.x; i < G * D; i += blockDim.x) sq[i] = qp[i];
@@ -326,11 +328,11 @@ cudaError_t append_dt(const kvd_cache &c, const void *k_new, const void *v_new, 
     return cudaGetLastError();
 }
 
-template <int G>
+template <int G, int DC = 0>
 cudaError_t score_g(const kvd_cache &c, const float *q, int H, int NB, uint32_t *keys,
                     int key_stride, cudaStream_t st) {
     const size_t smem = static_cast<size_t>(G) * c.head_dim * sizeof(float);
-    auto kern = gd_score_kernel<G>;
+    auto kern = gd_score_kernel<G, DC>;
     static LaunchCache lc;
     cudaError_t e = prepare_launch(kern, kScoreWarps * 32, smem, lc, nullptr);
     if (e != cudaSuccess) return e;
@@ -359,7 +361,15 @@ cudaError_t launch_select_gd(const kvd_cache &c, const float *q, int n_heads, in
     const bool rank = k_sel > 0 && k_sel < rb - se;
     if (rank) {  // the keys of every candidate (only candidates are ranked)
         cudaError_t e;
-        switch (G) {
+        const int D = c.head_dim;
+        // common head dims (64, 96, 256) of GQA groups of 4 and 8, with folded loops
+        if (G == 4 && D == 64) e = score_g<4, 64>(c, q, n_heads, NB, keys, key_stride, st);
+        else if (G == 8 && D == 64) e = score_g<8, 64>(c, q, n_heads, NB, keys, key_stride, st);
+        else if (G == 4 && D == 96) e = score_g<4, 96>(c, q, n_heads, NB, keys, key_stride, st);
+        else if (G == 8 && D == 96) e = score_g<8, 96>(c, q, n_heads, NB, keys, key_stride, st);
+        else if (G == 4 && D == 256) e = score_g<4, 256>(c, q, n_heads, NB, keys, key_stride, st);
+        else if (G == 8 && D == 256) e = score_g<8, 256>(c, q, n_heads, NB, keys, key_stride, st);
+        else switch (G) {
             case 1: e = score_g<1>(c, q, n_heads, NB, keys, key_stride, st); break;
             case 2: e = score_g<2>(c, q, n_heads, NB, keys, key_stride, st); break;
             case 4: e = score_g<4>(c, q, n_heads, NB, keys, key_stride, st); break;
