@@ -99,6 +99,30 @@ def check_selection(sel_idx, sel_cnt, oc, q_np, k_sel, sink, recent, G):
     return swaps
 
 
+def oracle_attend_list(oc, qg, b, g, sel, scale):
+    """The oracle's attention of query heads qg ([G, D] f32) over KV head g of
+    sequence b, restricted to the blocks of the list sel (the GPU's own
+    selection), for the cache type of oc: [G, D] float64.  Used wherever the
+    GPU's selection may differ from the oracle's inside the tie window, so
+    that the attention is still compared element by element."""
+    sel = np.asarray(sel, np.int32)
+    out = np.zeros(qg.shape, np.float64)
+    for h in range(qg.shape[0]):
+        if oc.dtype == kvd.F16:
+            out[h] = oracle.attend_f16(qg[h], oc.K[b, g], oc.V[b, g], oc.len, 64,
+                                       scale, sel=sel)
+            continue
+        c, qs = oracle.quantize_row(qg[h])
+        if oc.dtype == kvd.INT8:
+            out[h] = oracle.attend_int8(c, qs, oc.K[b, g], oc.V[b, g], oc.ks[b, g],
+                                        oc.vs[b, g], oc.len, 64, scale, sel=sel)
+        else:
+            att = oracle.attend_q8_0 if oc.dtype == kvd.Q8_0 else oracle.attend_q4_0
+            out[h] = att(c, qs, oc.K[b, g], oc.V[b, g], oc.kd[b, g], oc.vd[b, g], oc.len,
+                         64, scale, sel=sel)[0]
+    return out
+
+
 def seeded(shape, seed, scale=1.0, dtype=torch.float16, device=None):
     g = torch.Generator(device=device or dev())
     g.manual_seed(seed)

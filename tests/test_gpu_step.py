@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import long_context_decode_kv_gb300 as kvd
-from gpu_util import assert_outputs, check_selection, dev, make_pair, scale_for, seeded
+from gpu_util import (assert_outputs, check_selection, dev, make_pair, oracle_attend_list,
+                      scale_for, seeded)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,26 +38,12 @@ def test_steps_match_oracle(dtype, sparse):
             check_selection(sel_idx, sel_cnt, oc, qn, k_sel, sink, recent, G)
             # attend the GPU's own selection in the oracle (a tie swap, if
             # any, must not count against the attention kernel)
-            import oracle
             ref = np.zeros((B, Hkv * G, 128))
+            idx, cnt = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
             for b in range(B):
                 for g in range(Hkv):
-                    sel = sel_idx[b, g, :sel_cnt[b, g]].cpu().numpy()
-                    for h in range(G):
-                        hq = g * G + h
-                        if dtype == kvd.F16:
-                            ref[b, hq] = oracle.attend_f16(qn[b, hq], oc.K[b, g], oc.V[b, g],
-                                                           oc.len, 64, scale_for(), sel=sel)
-                        elif dtype in (kvd.Q8_0, kvd.Q4_0):
-                            c, qs = oracle.quantize_row(qn[b, hq])
-                            att = oracle.attend_q8_0 if dtype == kvd.Q8_0 else oracle.attend_q4_0
-                            ref[b, hq] = att(c, qs, oc.K[b, g], oc.V[b, g], oc.kd[b, g],
-                                             oc.vd[b, g], oc.len, 64, scale_for(), sel=sel)[0]
-                        else:
-                            c, qs = oracle.quantize_row(qn[b, hq])
-                            ref[b, hq] = oracle.attend_int8(c, qs, oc.K[b, g], oc.V[b, g],
-                                                            oc.ks[b, g], oc.vs[b, g], oc.len, 64,
-                                                            scale_for(), sel=sel)
+                    ref[b, g * G:(g + 1) * G] = oracle_attend_list(
+                        oc, qn[b, g * G:(g + 1) * G], b, g, idx[b, g, :cnt[b, g]], scale_for())
         else:
             ref, _, _ = oc.decode(qn, scale_for(), dense=True)
         assert_outputs(out, ref, dtype, f"step {s}")
