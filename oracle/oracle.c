@@ -990,8 +990,11 @@ void orc_attend_tail(int D, int L, int blk, const double *q_exact, const double 
 /* attended and no selection is made.  sel_idx ([B, Hkv, NB]) and        */
 /* sel_cnt ([B, Hkv]) receive the selection when not NULL.  For the      */
 /* int8 cache each query head is quantized once (CPUATT Method).         */
-/* Problems (seq, KV head) are independent; n_threads > 1 spreads them   */
-/* over OpenMP threads.  Returns 0, or -1 on bad arguments.              */
+/* Problems (seq, KV head) are independent, and so are the query heads   */
+/* once their problem's selection is made; n_threads > 1 spreads the      */
+/* selections, then the (problem, query head) attentions, over OpenMP     */
+/* threads.  Each head's arithmetic is the same on any thread count.      */
+/* Returns 0, or -1 on bad arguments.                                     */
 /* ------------------------------------------------------------------ */
 int orc_decode(const orc_cache *c, int H, const float *q, double scale, int k_sel,
                int sink_tokens, int recent_tokens, int dense, int *sel_idx, int *sel_cnt,
@@ -1002,59 +1005,73 @@ int orc_decode(const orc_cache *c, int H, const float *q, double scale, int k_se
     const int NB = (L + c->blk - 1) / c->blk;
     const int nbmax = c->max_seq / c->blk;
     const int P = c->B * c->Hkv;
+    int *sel_all = (int *)malloc(sizeof(int) * (size_t)NB * (size_t)P);
+    int *n_all = (int *)malloc(sizeof(int) * (size_t)P);
 #ifdef _OPENMP
     if (n_threads < 1) n_threads = 1;
+#endif
+    /* the selection of every problem (its group's shared block set) */
+#ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
 #endif
     for (int p = 0; p < P; ++p) {
         int b = p / c->Hkv, g = p % c->Hkv;
         const float *qg = q + ((size_t)b * H + (size_t)g * G) * D;
-        int *sel = (int *)malloc(sizeof(int) * (size_t)NB);
-        int n_sel = -1;
+        int *sel = sel_all + (size_t)p * NB;
+        n_all[p] = -1;
         if (!dense) {
             double *ub = (double *)malloc(sizeof(double) * (size_t)NB);
             orc_block_scores(G, D, NB, qg, c->kmin + bound_index(c, b, g, 0),
                              c->kmax + bound_index(c, b, g, 0), NULL, ub, NULL);
-            n_sel = orc_select(L, c->blk, ub, k_sel, sink_tokens, recent_tokens, sel, NULL);
+            n_all[p] = orc_select(L, c->blk, ub, k_sel, sink_tokens, recent_tokens, sel, NULL);
             free(ub);
-            if (sel_idx) memcpy(sel_idx + (size_t)p * nbmax, sel, sizeof(int) * (size_t)n_sel);
-            if (sel_cnt) sel_cnt[p] = n_sel;
+            if (sel_idx) memcpy(sel_idx + (size_t)p * nbmax, sel, sizeof(int) * (size_t)n_all[p]);
+            if (sel_cnt) sel_cnt[p] = n_all[p];
         }
-        size_t r0 = row_index(c, b, g, 0);
-        for (int hh = 0; hh < G; ++hh) {
-            const float *qh = qg + (size_t)hh * D;
-            double *o = out + ((size_t)b * H + (size_t)g * G + hh) * D;
-            if (c->dtype == ORC_F16) {
-                orc_attend_f16(D, L, c->blk, qh, scale, (const uint16_t *)c->K + r0 * D,
-                               (const uint16_t *)c->V + r0 * D, sel, n_sel, o);
-            } else if (c->dtype == ORC_Q4_0) {
-                int8_t *qc = (int8_t *)malloc((size_t)D);
-                float qs;
-                orc_quantize_row(qh, D, qc, &qs);
-                orc_attend_q4_0(D, L, c->blk, qc, qs, scale, (const uint8_t *)c->K + r0 * (D / 2),
-                                (const uint8_t *)c->V + r0 * (D / 2), c->kd + r0 * (D / ORC_QGROUP),
-                                c->vd + r0 * (D / ORC_QGROUP), sel, n_sel, 0.0, o, NULL);
-                free(qc);
-            } else if (c->dtype == ORC_Q8_0) {
-                int8_t *qc = (int8_t *)malloc((size_t)D);
-                float qs;
-                orc_quantize_row(qh, D, qc, &qs);
-                orc_attend_q8_0(D, L, c->blk, qc, qs, scale, (const int8_t *)c->K + r0 * D,
-                                (const int8_t *)c->V + r0 * D, c->kd + r0 * (D / ORC_QGROUP),
-                                c->vd + r0 * (D / ORC_QGROUP), sel, n_sel, 0.0, o, NULL);
-                free(qc);
-            } else {
-                int8_t *qc = (int8_t *)malloc((size_t)D);
-                float qs;
-                orc_quantize_row(qh, D, qc, &qs);
-                orc_attend_int8(D, L, c->blk, qc, qs, scale, (const int8_t *)c->K + r0 * D,
-                                (const int8_t *)c->V + r0 * D, c->ks + r0, c->vs + r0,
-                                sel, n_sel, o);
-                free(qc);
-            }
-        }
-        free(sel);
     }
+    /* each query head over its problem's selection (or every token) */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+#endif
+    for (int u = 0; u < P * G; ++u) {
+        const int p = u / G, hh = u % G;
+        const int b = p / c->Hkv, g = p % c->Hkv;
+        const int *sel = sel_all + (size_t)p * NB;
+        const int n_sel = n_all[p];
+        const size_t r0 = row_index(c, b, g, 0);
+        const float *qh = q + ((size_t)b * H + (size_t)g * G + hh) * D;
+        double *o = out + ((size_t)b * H + (size_t)g * G + hh) * D;
+        if (c->dtype == ORC_F16) {
+            orc_attend_f16(D, L, c->blk, qh, scale, (const uint16_t *)c->K + r0 * D,
+                           (const uint16_t *)c->V + r0 * D, sel, n_sel, o);
+        } else if (c->dtype == ORC_Q4_0) {
+            int8_t *qc = (int8_t *)malloc((size_t)D);
+            float qs;
+            orc_quantize_row(qh, D, qc, &qs);
+            orc_attend_q4_0(D, L, c->blk, qc, qs, scale, (const uint8_t *)c->K + r0 * (D / 2),
+                            (const uint8_t *)c->V + r0 * (D / 2), c->kd + r0 * (D / ORC_QGROUP),
+                            c->vd + r0 * (D / ORC_QGROUP), sel, n_sel, 0.0, o, NULL);
+            free(qc);
+        } else if (c->dtype == ORC_Q8_0) {
+            int8_t *qc = (int8_t *)malloc((size_t)D);
+            float qs;
+            orc_quantize_row(qh, D, qc, &qs);
+            orc_attend_q8_0(D, L, c->blk, qc, qs, scale, (const int8_t *)c->K + r0 * D,
+                            (const int8_t *)c->V + r0 * D, c->kd + r0 * (D / ORC_QGROUP),
+                            c->vd + r0 * (D / ORC_QGROUP), sel, n_sel, 0.0, o, NULL);
+            free(qc);
+        } else {
+            int8_t *qc = (int8_t *)malloc((size_t)D);
+            float qs;
+            orc_quantize_row(qh, D, qc, &qs);
+            orc_attend_int8(D, L, c->blk, qc, qs, scale, (const int8_t *)c->K + r0 * D,
+                            (const int8_t *)c->V + r0 * D, c->ks + r0, c->vs + r0,
+                            sel, n_sel, o);
+            free(qc);
+        }
+    }
+    free(sel_all);
+    free(n_all);
     return 0;
 }
 

@@ -45,8 +45,11 @@ MUTANTS = {
                        "lg[i] = (double)dot * (double)q_scale * scale;"),
     "int8_no_vscale": ("double sv = (double)vs[tok[i]];", "double sv = 1.0;"),
     "int8_vscale_from_k": ("double sv = (double)vs[tok[i]];", "double sv = (double)ks[tok[i]];"),
-    "gqa_modulo_mapping": ("int b = p / c->Hkv, g = p % c->Hkv;\n        const float *qg = q + ((size_t)b * H + (size_t)g * G) * D;",
-                           "int b = p / c->Hkv, g = p % c->Hkv;\n        const float *qg = q + ((size_t)b * H + (size_t)g) * D;"),
+    "gqa_modulo_mapping": ("const float *qh = q + ((size_t)b * H + (size_t)g * G + hh) * D;",
+                           "const float *qh = q + ((size_t)b * H + (size_t)g + hh) * D;"),
+    "gqa_modulo_mapping_select": (
+        "int b = p / c->Hkv, g = p % c->Hkv;\n        const float *qg = q + ((size_t)b * H + (size_t)g * G) * D;",
+        "int b = p / c->Hkv, g = p % c->Hkv;\n        const float *qg = q + ((size_t)b * H + (size_t)g) * D;"),
     "partial_block_overrun": ("t < (long)(sel[i] + 1) * blk && t < L; ++t)",
                               "t < (long)(sel[i] + 1) * blk; ++t)"),
     "half_subnormal_exp": ("mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);"),

@@ -366,6 +366,24 @@ def test_gqa_head_mapping():
         assert np.allclose(out[0, h], h // G + 1, atol=1e-12)
 
 
+def test_decode_selection_is_the_groups_selection():
+    # the decode step's list for (sequence b, KV head g) is the selection by
+    # the bound of query heads g*G .. g*G+G-1 (the group's max), nothing else
+    B, Hkv, D, L, G = 2, 3, 32, 900, 4
+    k, v = _rand_kv(B, L, Hkv, D)
+    c = oracle.OracleCache(oracle.F16, B, Hkv, D, max_seq=960, blk=64)
+    c.append(k, v)
+    q = RNG.standard_normal((B, Hkv * G, D)).astype(np.float32)
+    _, sel_idx, sel_cnt = c.decode(q, scale=0.1, k_sel=3, sink_tokens=4, recent_tokens=64)
+    nb = (L + 63) // 64
+    for b in range(B):
+        for g in range(Hkv):
+            ub, _, _ = oracle.block_scores(q[b, g * G:(g + 1) * G], c.kmin[b, g, :nb],
+                                           c.kmax[b, g, :nb])
+            want, _ = oracle.select(L, 64, ub, 3, 4, 64)
+            assert np.array_equal(sel_idx[b, g, :sel_cnt[b, g]], want)
+
+
 def test_dominant_key_returns_its_value():
     D, L = 32, 200
     K = RNG.standard_normal((256, D)).astype(np.float16)
