@@ -267,12 +267,14 @@ def oracle_leg(w, q, k, v, steps, problem=(0, 0)):
 
 
 def oracle_leg_all_cores(w, q, k, v, steps):
-    """The same oracle step on all host cores: as many (KV head) problems of
-    sequence 0 as there are threads, one per OpenMP thread; the step time is
-    scaled by the number of such batches the workload's B*Hkv problems make."""
+    """The same oracle step on all host cores: every KV-head problem of
+    sequence 0 at once, their selections and then their (problem, query head)
+    attentions spread over the OpenMP threads (the arithmetic of each head is
+    the same on any thread count); the step time is scaled by the workload's
+    B sequences."""
     import oracle
-    threads = max(1, oracle.threads_available())
-    hk = min(w.Hkv, threads)
+    threads = max(1, len(os.sched_getaffinity(0)))
+    hk = w.Hkv
     G = w.G
     oc = oracle.OracleCache(w.dtype, 1, hk, w.D, w.L + 64, 64)
     oc.append(k[0:1, :, :hk].contiguous().cpu().numpy(), v[0:1, :, :hk].contiguous().cpu().numpy())
@@ -287,13 +289,14 @@ def oracle_leg_all_cores(w, q, k, v, steps):
                   recent_tokens=w.recent_tokens, n_threads=threads)
         times.append(time.perf_counter() - t0)
     n_prob = w.B * w.Hkv
-    batches = -(-n_prob // hk)
-    used = min(threads, hk)
+    batches = w.B
+    used = min(threads, hk * G)
     return statistics.median(times) * 1e6 * batches, {
-        "kind": "oracle", "cores": used,
-        "sample": (f"{hk} of {n_prob} (sequence, KV head) problems of {w.name} at once on "
-                   f"{used} threads, {steps} steps (append + select + attend, fp64), median "
-                   f"step time x {batches} batch(es)")}
+        "kind": "oracle", "cores": used, "threads_available": threads,
+        "sample": (f"the {hk} KV-head problems of sequence 0 of {w.name} ({hk * G} query "
+                   f"heads) at once on {used} threads, {steps} steps (append + select + "
+                   f"attend, fp64), median step time x {batches} sequence(s) = {n_prob} "
+                   f"problems")}
 
 
 def run_reference(args, w):
@@ -613,69 +616,26 @@ def run_gqa_sweep(args):
         torch.cuda.empty_cache()
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--context", type=int, default=None,
-                    help="run the workload's recipe at this context instead (a multiple "
-                         "of 64; a smaller case for profiling)")
-    ap.add_argument("--head-dim", type=int, default=None,
-                    help="run the workload's recipe with this head dim instead (a multiple "
-                         "of 16 up to 1024; 128 runs the tuned kernels, others the general "
-                         "ones)")
-    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v", "tail", "gqa",
-                                        "head_dim"],
-                    default=None,
-                    help="instead of the bench line: sparse vs dense decode steps over the "
-                         "context sweep (16K..1M, 25%% coverage) or the 128K x 8 coverage "
-                         "sweep, decode attention with sparse-V at several eps, or decode "
-                         "attention with the moment tail, or the GQA-shared selection "
-                         "against one per query head; one JSON line per point")
-    args = ap.parse_args()
-    if args.sweep == "sparse_v":
-        return run_sparse_v_sweep(args)
-    if args.sweep == "tail":
-        return run_tail_sweep(args)
-    if args.sweep == "gqa":
-        return run_gqa_sweep(args)
-    if args.sweep:
-        return run_sweep(args)
-    w = synth.WORKLOADS[args.workload]
-    if args.context is not None:
-        if args.context < 64 or args.context % 64:
-            ap.error("--context must be a positive multiple of 64")
-        w = w.with_(L=args.context)
-    if args.head_dim is not None:
-        if not (16 <= args.head_dim <= 1024 and args.head_dim % 16 == 0):
-            ap.error("--head-dim must be a multiple of 16 in [16, 1024]")
-        w = w.with_(D=args.head_dim)
-    if args.impl == "reference":
-        return run_reference(args, w)
+# The metric's other contexts, reported beside the 1M headline.
+CONTEXT_WORKLOADS = ("qwen3_4b_gqa_32k_f16", "ctx128k_b8_int8")
 
-    world, rank, local = dist_setup(args.gpus)
-    dev = torch.device("cuda", local)
+
+def measure(w, dev, steps, warmup, flush_l2, world, local, headline):
+    """The bench protocol on one workload: K timed decode steps (value), then
+    the decode kernel, the selection and the append alone, the dense step, and
+    (headline) the end-to-end step through host buffers.  Returns a dict."""
     stream = torch.cuda.current_stream(dev)
-    warmup = max(3, args.warmup)
-
     q, k, v, needles = synth.make_workload(w, device=dev)
     cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, head_dim=w.D, device=dev)
     kvd.kv_append(cache, k, v)
+    if not headline:
+        del k, v
+        k = v = None
     ws = kvd.make_workspace(cache, w.H)
     nbmax = cache.max_seq // 64
     sel_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev)
     sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev)
     out = torch.empty(w.B, w.H, w.D, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def flush_l2(i):
-        flush.fill_(i & 0xFF)
-        return drain.sum()
     toks = [synth.make_step_token(w, s, device=dev) for s in range(8)]
     L1 = w.L + 1
     max_sel = kvd.selected_count(L1, w.k_sel, w.sink_tokens, w.recent_tokens)
@@ -716,13 +676,12 @@ def main():
             i += 1
             if i % 64 == 0:
                 torch.cuda.synchronize()
-        torch.cuda.nvtx.range_push("kvd_timed")
-        step_ms, wall = timed(lambda i: step(i), args.steps, warmup)
+        torch.cuda.nvtx.range_push("kvd_timed" if headline else "kvd_context")
+        step_ms, wall = timed(lambda i: step(i), steps, warmup)
         torch.cuda.nvtx.range_pop()
     clocks = clk.summary()
     assert cache.device_status() == 0, "device-side fault reported"
-    us_step = statistics.mean(step_ms) * 1e3
-    us_step = max_over_ranks(us_step, world)
+    us_step = max_over_ranks(statistics.mean(step_ms) * 1e3, world)
 
     # ---- selection statistics of the timed configuration
     tokens = attended_tokens(sel_idx, sel_cnt, L1)
@@ -735,43 +694,129 @@ def main():
 
     def dec(i):
         kvd.decode_attn(cache, q, w.scale, sel_idx, sel_cnt, max_sel, out, ws)
-    dec_ms, _ = timed(dec, args.steps, 3)
+    dec_ms, _ = timed(dec, steps, 3)
     dec_us = statistics.mean(dec_ms) * 1e3
 
     def sel(i):
         kvd.select_blocks(cache, q, w.k_sel, w.sink_tokens, w.recent_tokens, sel_idx, sel_cnt,
                           ws)
-    sel_ms, _ = timed(sel, args.steps, 3)
+    sel_ms, _ = timed(sel, steps, 3)
 
     def app(i):
         cache.len = w.L
         kn, vn = toks[i % len(toks)]
         kvd.kv_append(cache, kn, vn)
-    app_ms, _ = timed(app, args.steps, 3)
+    app_ms, _ = timed(app, steps, 3)
 
     # ---- dense arm at the same context (append + dense attend)
-    dense_ms, _ = timed(lambda i: step(i, dense=True), max(5, args.steps // 5), 2)
+    dense_ms, _ = timed(lambda i: step(i, dense=True), max(5, steps // 5), 2)
 
-    # ---- e2e: host buffers through the C ABI, copies inside the timed region
-    qh = q.cpu().pin_memory()
-    kh = [(a.cpu().pin_memory(), b.cpu().pin_memory()) for a, b in toks]
-    oh = torch.empty(w.B, w.H, w.D).pin_memory()
+    e2e = None
+    if headline:
+        # ---- e2e: host buffers through the C ABI, copies inside the timed region
+        qh = q.cpu().pin_memory()
+        kh = [(a.cpu().pin_memory(), b.cpu().pin_memory()) for a, b in toks]
+        oh = torch.empty(w.B, w.H, w.D).pin_memory()
 
-    def host_step(i):
-        cache.len = w.L
-        a, b = kh[i % len(kh)]
-        kvd.decode_step_host(cache, qh, a, b, w.scale, w.k_sel, w.sink_tokens, w.recent_tokens,
-                             oh, ws)
-    e2e_ms, _ = timed(host_step, args.steps, 3)
-    e2e_us = max_over_ranks(statistics.mean(e2e_ms) * 1e3, world)
-    h2d = qh.numel() * 4 + 2 * kh[0][0].numel() * 2
-    d2h = oh.numel() * 4
+        def host_step(i):
+            cache.len = w.L
+            a, b = kh[i % len(kh)]
+            kvd.decode_step_host(cache, qh, a, b, w.scale, w.k_sel, w.sink_tokens,
+                                 w.recent_tokens, oh, ws)
+        e2e_ms, _ = timed(host_step, steps, 3)
+        e2e_us = max_over_ranks(statistics.mean(e2e_ms) * 1e3, world)
+        e2e = {"value": e2e_us, "unit": "us/step",
+               "h2d_bytes_per_step": qh.numel() * 4 + 2 * kh[0][0].numel() * 2,
+               "d2h_bytes_per_step": oh.numel() * 4,
+               "host_buffers": "pinned; the kernels read q, k, v and write out in place "
+                               "over the host link (no staging copies)"}
+    assert cache.device_status() == 0, "device-side fault reported"
 
     peak, peak_kind = peaks()
     dbytes = decode_kernel_bytes(w, tokens, n_sel_total)
     sbytes = step_bytes(w, tokens, n_sel_total, L1)
     achieved = dbytes / (dec_us * 1e-6) / 1e9
     eff_step = sbytes / (us_step * 1e-6) / 1e9
+    kernel = ("decode_kernel" if w.D == 128 else "gd_decode_kernel") + " (kvd_decode_attn)"
+    res = {
+        "step_us": us_step, "effective_kv_gbs": eff_step, "effective_kv_frac": eff_step / peak,
+        "step_bytes": sbytes,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "kernel": kernel,
+                     "bytes": dbytes, "us": dec_us,
+                     "traffic": measured_traffic(w.name, tokens) if w.D == 128 else None,
+                     "tokens_attended": tokens},
+        "breakdown_us": {"append": statistics.mean(app_ms) * 1e3,
+                         "select": statistics.mean(sel_ms) * 1e3, "decode": dec_us,
+                         "step": us_step, "dense_step": statistics.mean(dense_ms) * 1e3},
+        "selected_blocks_per_problem": n_sel_total / (w.B * w.Hkv),
+        "coverage": n_sel_total / (w.B * w.Hkv) / ((L1 + 63) // 64),
+        "needles_selected": needle_ok, "e2e": e2e, "clocks": clocks,
+        "wall_s_timed_region": wall, "launches_per_step": launches_per_step(w, L1),
+        "_inputs": (q, k, v),
+    }
+    del cache, ws
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-contexts", action="store_true",
+                    help="leave out the 32K and 128K x 8 sub-records of the default line")
+    ap.add_argument("--context", type=int, default=None,
+                    help="run the workload's recipe at this context instead (a multiple "
+                         "of 64; a smaller case for profiling)")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="run the workload's recipe with this head dim instead (a multiple "
+                         "of 16 up to 1024; 128 runs the tuned kernels, others the general "
+                         "ones)")
+    ap.add_argument("--sweep", choices=["context", "coverage", "sparse_v", "tail", "gqa",
+                                        "head_dim"],
+                    default=None,
+                    help="instead of the bench line: sparse vs dense decode steps over the "
+                         "context sweep (16K..1M, 25%% coverage) or the 128K x 8 coverage "
+                         "sweep, decode attention with sparse-V at several eps, or decode "
+                         "attention with the moment tail, or the GQA-shared selection "
+                         "against one per query head; one JSON line per point")
+    args = ap.parse_args()
+    if args.sweep == "sparse_v":
+        return run_sparse_v_sweep(args)
+    if args.sweep == "tail":
+        return run_tail_sweep(args)
+    if args.sweep == "gqa":
+        return run_gqa_sweep(args)
+    if args.sweep:
+        return run_sweep(args)
+    w = synth.WORKLOADS[args.workload]
+    if args.context is not None:
+        if args.context < 64 or args.context % 64:
+            ap.error("--context must be a positive multiple of 64")
+        w = w.with_(L=args.context)
+    if args.head_dim is not None:
+        if not (16 <= args.head_dim <= 1024 and args.head_dim % 16 == 0):
+            ap.error("--head-dim must be a multiple of 16 in [16, 1024]")
+        w = w.with_(D=args.head_dim)
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    world, rank, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    warmup = max(3, args.warmup)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        return drain.sum()
+
+    m = measure(w, dev, args.steps, warmup, flush_l2, world, local, headline=True)
+    q, k, v = m.pop("_inputs")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -784,39 +829,57 @@ def main():
             cpu["sample_1_thread"] = one["sample"]
         except Exception as e:  # the baseline must not hide the GPU number
             cpu = {"kind": "oracle", "value": None, "error": str(e)[:200]}
+    del q, k, v
+    torch.cuda.empty_cache()
+
+    # ---- the metric's other contexts (32K f16 GQA, 128K x 8 int8), measured
+    # in the same run with the same protocol; the headline stays the workload's
+    contexts = {}
+    if args.workload == DEFAULT_WORKLOAD and args.context is None and args.head_dim is None \
+            and not args.no_contexts:
+        for name in CONTEXT_WORKLOADS:
+            cm = measure(synth.WORKLOADS[name], dev, args.steps, warmup, flush_l2, world, local,
+                         headline=False)
+            cm.pop("_inputs")
+            contexts[name] = cm
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
     line = {
-        "metric": "us_per_decode_step", "value": us_step, "unit": "us/step",
-        "n_gpus": world, "steps": args.steps, "warmup": warmup, "ms_per_step": us_step / 1e3,
+        "metric": "us_per_decode_step", "value": m["step_us"], "unit": "us/step",
+        "n_gpus": world, "steps": args.steps, "warmup": warmup,
+        "ms_per_step": m["step_us"] / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype_name(w.dtype), "data": "synthetic",
         "config": config_of(w),
-        "effective_kv_gbs": eff_step,
-        "effective_kv_frac": eff_step / peak,
-        "step_bytes": sbytes,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": ("decode_kernel" if w.D == 128 else "gd_decode_kernel") + " (kvd_decode_attn)", "bytes": dbytes,
-                     "us": dec_us, "traffic": measured_traffic(w.name, tokens) if w.D == 128 else None,
-                     "tokens_attended": tokens},
-        "breakdown_us": {"append": statistics.mean(app_ms) * 1e3,
-                         "select": statistics.mean(sel_ms) * 1e3, "decode": dec_us,
-                         "step": us_step, "dense_step": statistics.mean(dense_ms) * 1e3},
-        "sparse_over_dense": statistics.mean(dense_ms) * 1e3 / us_step,
-        "selected_blocks_per_problem": n_sel_total / (w.B * w.Hkv),
-        "coverage": n_sel_total / (w.B * w.Hkv) / ((L1 + 63) // 64),
-        "needles_selected": needle_ok,
-        "e2e": {"value": e2e_us, "unit": "us/step", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "host_buffers": "pinned; the kernels read q, k, v and write out in place "
-                                "over the host link (no staging copies)"},
-        "gpu_launches": launches_per_step(w, L1) * args.steps,
-        "clocks": clocks,
-        "wall_s_timed_region": wall,
+        "effective_kv_gbs": m["effective_kv_gbs"],
+        "effective_kv_frac": m["effective_kv_frac"],
+        "step_bytes": m["step_bytes"],
+        "roofline": m["roofline"],
+        "breakdown_us": m["breakdown_us"],
+        "sparse_over_dense": m["breakdown_us"]["dense_step"] / m["step_us"],
+        "selected_blocks_per_problem": m["selected_blocks_per_problem"],
+        "coverage": m["coverage"],
+        "needles_selected": m["needles_selected"],
+        "e2e": m["e2e"],
+        "gpu_launches": m["launches_per_step"] * args.steps,
+        "clocks": m["clocks"],
+        "wall_s_timed_region": m["wall_s_timed_region"],
         "cpu_baseline": cpu,
     }
+    if contexts:
+        line["contexts"] = {
+            name: {"config": config_of(synth.WORKLOADS[name]), "step_us": cm["step_us"],
+                   "select_us": cm["breakdown_us"]["select"],
+                   "decode_us": cm["breakdown_us"]["decode"],
+                   "dense_step_us": cm["breakdown_us"]["dense_step"],
+                   "sparse_over_dense": cm["breakdown_us"]["dense_step"] / cm["step_us"],
+                   "effective_kv_gbs": cm["effective_kv_gbs"],
+                   "effective_kv_frac": cm["effective_kv_frac"],
+                   "roofline": cm["roofline"], "coverage": cm["coverage"],
+                   "needles_selected": cm["needles_selected"], "clocks": cm["clocks"]}
+            for name, cm in contexts.items()}
     print(json.dumps(line), flush=True)
 
 

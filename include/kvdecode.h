@@ -30,7 +30,11 @@
  *    the cache's optional `dev_status` word (0 = fine); the kernels never
  *    trap.  Read the word after the stream has finished.
  *  - No call is thread-safe on the same cache or workspace; calls on one
- *    stream are ordered by the stream.
+ *    stream are ordered by the stream.  The library's own host state (per
+ *    device: the SM count, the kernels' shared-memory attributes and
+ *    occupancy, the workspace-free decode's array address) is filled once
+ *    per device under a lock, so host threads driving different devices, or
+ *    different caches on one device, may call at the same time.
  */
 #ifndef KVDECODE_H
 #define KVDECODE_H
@@ -333,7 +337,8 @@ KVD_API kvd_status kvd_decode_attn_tail(const kvd_cache *cache, const float *q,
 /* ---------------------------------------------------------------------- */
 /* kvd_decode_attn without a workspace: the paper has no counterpart; this  */
 /* is a convenience of this library.  Same arguments, arithmetic and output */
-/* as kvd_decode_attn, minus workspace/workspace_bytes.                     */
+/* as kvd_decode_attn, minus workspace/workspace_bytes, for head_dim 128    */
+/* only (the tuned kernels; other head dims return UNSUPPORTED).            */
 /*   For callers that cannot allocate device memory when they decode: a    */
 /*   plugin that an engine hands only its input and output buffers, or     */
 /*   code whose device memory is owned by another allocator.  The split     */
@@ -343,13 +348,17 @@ KVD_API kvd_status kvd_decode_attn_tail(const kvd_cache *cache, const float *q,
 /*   allocates nothing (no cudaMalloc/cudaFree, no library allocator).      */
 /*   The first call on a device looks up the array's device address (once  */
 /*   per device, with that device current); make that first call before    */
-/*   any stream capture.  Each call zeroes the counters on `stream` before  */
+/*   any stream capture.  cudaDeviceReset drops that address: after a reset */
+/*   of a device, do not call this entry point on it again in the same      */
+/*   process.  Each call zeroes the counters on `stream` before             */
 /*   its kernel.  All calls on a device share the array: two calls that    */
 /*   may overlap on the GPU (different streams, no ordering) race and give  */
 /*   wrong outputs; order them on one stream or with events.                */
-/* Errors: as kvd_decode_attn; WORKSPACE when this call's partials and      */
-/* counters would pass KVD_STATIC_SCRATCH_BYTES (on a 152-SM GPU every      */
-/* accepted shape needs under 0.7 MiB, so WORKSPACE does not occur there).  */
+/* Errors: as kvd_decode_attn (the same cache and head checks);             */
+/* UNSUPPORTED for a head_dim other than 128; WORKSPACE when this call's     */
+/* partials and counters would pass KVD_STATIC_SCRATCH_BYTES (on a 152-SM   */
+/* GPU every accepted shape needs under 0.7 MiB, so WORKSPACE does not      */
+/* occur there).                                                            */
 /* ---------------------------------------------------------------------- */
 #define KVD_STATIC_SCRATCH_BYTES (1u << 20)
 KVD_API kvd_status kvd_decode_attn_static(const kvd_cache *cache, const float *q,

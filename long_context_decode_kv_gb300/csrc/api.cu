@@ -1,7 +1,10 @@
 // api.cu -- the extern "C" entry points of libkvdecode.so: argument checks on
 // the host, workspace layout, and kernel dispatch on the caller's stream.
+#include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 #include "internal.h"
@@ -10,33 +13,79 @@ namespace kvd {
 
 int max_select_blocks();
 
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];  // 0: not asked yet
+
+struct KernelKey {
+    const void *fn;
+    int dev;
+    size_t smem;  // 0 in the table of attribute values
+    bool operator==(const KernelKey &o) const {
+        return fn == o.fn && dev == o.dev && smem == o.smem;
+    }
+};
+struct KernelKeyHash {
+    size_t operator()(const KernelKey &k) const {
+        return std::hash<const void *>()(k.fn) ^ (static_cast<size_t>(k.dev) << 48) ^
+               (k.smem << 20);
+    }
+};
+
+}  // namespace
+
 int device_sm_count() {
-    static int cached_dev = -1, cached_sms = 0;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
         return 152;  // GB300
     }
-    if (dev != cached_dev) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            sms <= 0) {
-            cudaGetLastError();
-            return 152;
-        }
-        cached_dev = dev;
-        cached_sms = sms;
+    int sms = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (sms > 0) return sms;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();
+        return 152;
     }
-    return cached_sms;
+    g_sm_count[dev].store(sms, std::memory_order_relaxed);  // every writer stores the same value
+    return sms;
+}
+
+cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *occ) {
+    static std::mutex mu;
+    // per (kernel, device): the largest dynamic shared memory opened so far
+    // (the attribute is only raised, so a launch sized below it stays valid);
+    // per (kernel, device, size): the occupancy
+    static std::unordered_map<KernelKey, size_t, KernelKeyHash> opened;
+    static std::unordered_map<KernelKey, int, KernelKeyHash> occupancy;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t &top = opened[KernelKey{fn, dev, 0}];
+    if (smem > top) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        top = smem;
+    }
+    const KernelKey key{fn, dev, smem};
+    auto it = occupancy.find(key);
+    if (it == occupancy.end()) {
+        int o = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, fn, threads, smem);
+        if (e != cudaSuccess) return e;
+        it = occupancy.emplace(key, o > 0 ? o : 1).first;
+    }
+    if (occ) *occ = it->second;
+    return cudaSuccess;
 }
 
 namespace {
-
-constexpr size_t kAlign = 256;
-
-size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
-
-bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) % 4) == 0; }
+}  // namespace
 
 kvd_status check_cache(const kvd_cache *c) {
     if (!c) return KVD_ERR_INVALID;
@@ -58,14 +107,14 @@ kvd_status check_cache(const kvd_cache *c) {
     if (c->reserved != 0) return KVD_ERR_INVALID;
     const void *ptrs[3] = {c->k, c->v, c->kbounds};
     for (const void *p : ptrs)
-        if (!p || !aligned(p, 16)) return KVD_ERR_INVALID;
+        if (!p || !aligned16(p)) return KVD_ERR_INVALID;
     if (c->dtype != KVD_F16) {
-        if (!c->k_scale || !c->v_scale || !aligned(c->k_scale, 16) || !aligned(c->v_scale, 16))
+        if (!c->k_scale || !c->v_scale || !aligned16(c->k_scale) || !aligned16(c->v_scale))
             return KVD_ERR_INVALID;
     }
-    if (c->dev_status && !aligned(c->dev_status, 4)) return KVD_ERR_INVALID;
-    if (c->moments && !aligned(c->moments, 16)) return KVD_ERR_INVALID;
-    if (c->seq_lens && !aligned(c->seq_lens, 4)) return KVD_ERR_INVALID;
+    if (c->dev_status && !aligned4(c->dev_status)) return KVD_ERR_INVALID;
+    if (c->moments && !aligned16(c->moments)) return KVD_ERR_INVALID;
+    if (c->seq_lens && !aligned4(c->seq_lens)) return KVD_ERR_INVALID;
     if (static_cast<long long>(c->batch) * c->n_kv_heads * 16 > 65535) return KVD_ERR_UNSUPPORTED;
     return KVD_OK;
 }
@@ -76,6 +125,14 @@ kvd_status check_heads(const kvd_cache *c, int n_heads) {
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return KVD_ERR_UNSUPPORTED;
     return KVD_OK;
 }
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // A head dim the general kernels serve (the tuned ones take 128).
 bool general_d(const kvd_cache *c) { return c->head_dim != kHeadDim; }

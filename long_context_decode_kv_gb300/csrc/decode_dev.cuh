@@ -1533,14 +1533,10 @@ __global__ void __launch_bounds__(TileW<DT, WIDE>::kThreads, TileW<DT, WIDE>::kM
 template <int DT, int GC, bool DENSE, bool SV, bool TAIL, bool WIDE = false>
 cudaError_t launch_decode_t(const DecodeArgs &a, int P_sub, cudaStream_t st, bool pdl) {
     using SL = SmemLayout<DT, GC, TAIL, WIDE>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SL::kTotal);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    const cudaError_t e = prepare_kernel(
+        reinterpret_cast<const void *>(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE>),
+        TileW<DT, WIDE>::kThreads, SL::kTotal);
+    if (e != cudaSuccess) return e;
     return launch_ex(decode_kernel<DT, GC, DENSE, SV, TAIL, WIDE>, dim3(a.splits, P_sub),
                      dim3(TileW<DT, WIDE>::kThreads), SL::kTotal, st, pdl, a);
 }

@@ -18,7 +18,6 @@
 //
 // Layouts are those of the header with head_dim = D: rows of D channels, the
 // bounds [.., D, 2] f16.
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -30,34 +29,6 @@ constexpr int kRankThreads = 1024;
 constexpr int kScoreWarps = 8;
 constexpr int kScoreBlocksPerCta = 16;  // two per warp: many loads in flight
 
-// Per kernel instance, the device and dynamic shared memory it was last
-// opened to and its occupancy there: the host-side driver calls run when the
-// size or the device changes, not at every launch.
-struct LaunchCache {
-    int dev = -1;
-    size_t smem = 0;
-    int occ = 0;
-};
-
-template <typename Kern>
-cudaError_t prepare_launch(Kern kern, int threads, size_t smem, LaunchCache &lc, int *occ) {
-    static std::mutex mu;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    if (lc.dev != dev || lc.smem != smem) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&lc.occ, kern, threads, smem);
-        if (e != cudaSuccess) return e;
-        lc.dev = dev;
-        lc.smem = smem;
-    }
-    if (occ) *occ = lc.occ;
-    return cudaSuccess;
-}
 
 __device__ __forceinline__ float in_value(const __half *p, size_t i) { return __half2float(p[i]); }
 __device__ __forceinline__ float in_value(const float *p, size_t i) { return p[i]; }
@@ -333,8 +304,7 @@ cudaError_t score_g(const kvd_cache &c, const float *q, int H, int NB, uint32_t 
                     int key_stride, cudaStream_t st) {
     const size_t smem = static_cast<size_t>(G) * c.head_dim * sizeof(float);
     auto kern = gd_score_kernel<G, DC>;
-    static LaunchCache lc;
-    cudaError_t e = prepare_launch(kern, kScoreWarps * 32, smem, lc, nullptr);
+    cudaError_t e = prepare_kernel(reinterpret_cast<const void *>(kern), kScoreWarps * 32, smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((NB + kScoreBlocksPerCta - 1) / kScoreBlocksPerCta,
                     c.batch * c.n_kv_heads);

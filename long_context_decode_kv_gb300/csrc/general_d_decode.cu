@@ -23,7 +23,6 @@
 //      tokens i / (D/4) (mod 256 / (D/4)) of the block.
 // The subgroups' sums are added in a fixed order at the end, so the result
 // does not depend on timing.
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -35,34 +34,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kStages = 3;  // K/V tiles in flight: the one read and two ahead
 
-// Per kernel instance, the device and dynamic shared memory it was last
-// opened to and its occupancy there: the host-side driver calls run when the
-// size or the device changes, not at every launch.
-struct LaunchCache {
-    int dev = -1;
-    size_t smem = 0;
-    int occ = 0;
-};
-
-template <typename Kern>
-cudaError_t prepare_launch(Kern kern, int threads, size_t smem, LaunchCache &lc, int *occ) {
-    static std::mutex mu;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    if (lc.dev != dev || lc.smem != smem) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&lc.occ, kern, threads, smem);
-        if (e != cudaSuccess) return e;
-        lc.dev = dev;
-        lc.smem = smem;
-    }
-    if (occ) *occ = lc.occ;
-    return cudaSuccess;
-}
 
 __device__ __forceinline__ void half8(const uint4 &w, float (&x)[8]) {
     const __half2 *h = reinterpret_cast<const __half2 *>(&w);
@@ -484,9 +455,8 @@ cudaError_t decode_g(const kvd_cache &c, const float *q, int H, float scale_log2
                         static_cast<size_t>(kStages) * stage_bytes(c.head_dim, kElt, T, DT != KVD_F16);
     auto kern = gd_decode_kernel<DT, G, DC>;
     // one wave: the CTAs that fit on every SM at once, shared by the problems
-    static LaunchCache lc;
     int occ = 0;
-    cudaError_t e = prepare_launch(kern, kThreads, smem, lc, &occ);
+    cudaError_t e = prepare_kernel(reinterpret_cast<const void *>(kern), kThreads, smem, &occ);
     if (e != cudaSuccess) return e;
     const int P = c.batch * c.n_kv_heads;
     const int splits = gd_splits(P, max_blocks, device_sm_count(), occ);

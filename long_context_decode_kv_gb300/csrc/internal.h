@@ -38,7 +38,20 @@ struct DecodePlan {
 DecodePlan plan_decode(const Geom &g, int max_blocks, int sm_count, bool one_head = false,
                        bool allow_wide = false);
 size_t decode_partials_bytes(const Geom &g, const DecodePlan &p);
+// SM count of the current device (cached per device ordinal; safe to call
+// from several host threads).
 int device_sm_count();
+// Opens kernel fn to smem bytes of dynamic shared memory on the current device
+// and returns (in occ, when not null) how many of its CTAs of `threads`
+// threads fit on one SM.  The driver calls run once per (kernel, device, smem);
+// later calls read a table under a lock, so host threads driving different
+// devices may launch at the same time.
+cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *occ = nullptr);
+
+// Host argument rules shared by the entry points (api.cu): the cache
+// descriptor, and the query-head count against it.
+kvd_status check_cache(const kvd_cache *c);
+kvd_status check_heads(const kvd_cache *c, int n_heads);
 
 cudaError_t launch_append(const kvd_cache &c, const void *k_new, const void *v_new, int n_new,
                           cudaStream_t st, bool pdl, bool f32_in = false);

@@ -43,17 +43,10 @@ __global__ void __launch_bounds__(256) fill_kernel_varlen(SelArgs a) {
 template <int G, int MODE>
 cudaError_t launch_select_t(const SelArgs &a0, int P, cudaStream_t st, bool pdl) {
     constexpr int smem = select_smem_bytes<G>();
-    static int occupancy = 0;
-    if (occupancy == 0) {
-        cudaError_t e = cudaFuncSetAttribute(select_kernel<G, MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, select_kernel<G, MODE>,
-                                                          kScoreThreads, smem);
-        if (e != cudaSuccess) return e;
-        occupancy = occ > 0 ? occ : 1;
-    }
+    int occupancy = 1;
+    const cudaError_t e = prepare_kernel(reinterpret_cast<const void *>(select_kernel<G, MODE>),
+                                         kScoreThreads, smem, &occupancy);
+    if (e != cudaSuccess) return e;
     SelArgs a = a0;
     // CTAs per problem: as many as fit on the GPU at once, split evenly (a
     // small problem still gains from many CTAs streaming its bounds)

@@ -10,6 +10,8 @@
 // already carved up.  They pay with a fixed KVD_STATIC_SCRATCH_BYTES on every
 // GPU that loads the library, and with one rule: calls that share the array
 // must not run at the same time on the GPU.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,15 +25,20 @@ static_assert(KVD_STATIC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-b
 static __device__ __align__(256) unsigned char g_static_scratch[KVD_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};  // device address, per device ordinal
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};  // device address, per device ordinal (under the lock)
 
 // In host code g_static_scratch names a host-side stand-in; the array's device
 // address is asked of the runtime once per device, with that device current.
+// cudaDeviceReset on a device drops the module holding the array, so the
+// address kept here is then stale: a process that resets a device must not
+// call this entry point on it again.
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_scratch);
@@ -46,29 +53,14 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 bool aligned_to(const void *p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
-// The argument rules of kvd_decode_attn, minus the workspace.
+// The argument rules of kvd_decode_attn (the same cache and head checks),
+// minus the workspace; only the tuned head dim (128) is served here.
 kvd_status check_args(const kvd_cache *c, const float *q, int n_heads, const int32_t *sel_idx,
                       const int32_t *sel_cnt, int max_sel, const float *out) {
-    if (!c) return KVD_ERR_INVALID;
-    if (c->dtype != KVD_F16 && c->dtype != KVD_INT8 && c->dtype != KVD_Q8_0 &&
-        c->dtype != KVD_Q4_0)
-        return KVD_ERR_INVALID;
-    if (c->batch < 1 || c->n_kv_heads < 1) return KVD_ERR_INVALID;
-    if (c->head_dim != kHeadDim || c->block != kBlock) return KVD_ERR_UNSUPPORTED;
-    if (c->max_seq < kBlock || c->max_seq % kBlock != 0) return KVD_ERR_INVALID;
-    if (c->len < 0 || c->len > c->max_seq || c->reserved != 0) return KVD_ERR_INVALID;
-    const void *ptrs[3] = {c->k, c->v, c->kbounds};
-    for (const void *p : ptrs)
-        if (!p || !aligned_to(p, 16)) return KVD_ERR_INVALID;
-    if (c->dtype != KVD_F16 && (!c->k_scale || !c->v_scale || !aligned_to(c->k_scale, 16) ||
-                                 !aligned_to(c->v_scale, 16)))
-        return KVD_ERR_INVALID;
-    if (c->dev_status && !aligned_to(c->dev_status, 4)) return KVD_ERR_INVALID;
-    if (c->seq_lens && !aligned_to(c->seq_lens, 4)) return KVD_ERR_INVALID;
-    if (static_cast<long long>(c->batch) * c->n_kv_heads * 16 > 65535) return KVD_ERR_UNSUPPORTED;
-    if (n_heads < 1 || n_heads % c->n_kv_heads != 0) return KVD_ERR_INVALID;
-    const int G = n_heads / c->n_kv_heads;
-    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return KVD_ERR_UNSUPPORTED;
+    kvd_status s = check_cache(c);
+    if (s != KVD_OK) return s;
+    if ((s = check_heads(c, n_heads)) != KVD_OK) return s;
+    if (c->head_dim != kHeadDim) return KVD_ERR_UNSUPPORTED;
     if (c->len < 1 || max_sel < 0) return KVD_ERR_INVALID;
     if (!q || !aligned_to(q, 16) || !out || !aligned_to(out, 16)) return KVD_ERR_INVALID;
     if (!sel_idx || !aligned_to(sel_idx, 4) || !sel_cnt || !aligned_to(sel_cnt, 4))

@@ -74,3 +74,14 @@ def test_traffic_scaled_per_token(tmp_path, monkeypatch):
     assert bench.measured_traffic("ctx128k_b8_int8", 25) is None
     monkeypatch.setattr(bench, "source_digest", lambda: "new")
     assert bench.measured_traffic("ctx1m_int8", 25) is None
+
+
+def test_oracle_baseline_uses_every_core_it_can():
+    # the all-core oracle leg spreads sequence 0's (KV head, query head)
+    # attentions over the threads of this process's CPU affinity
+    w = synth.QWEN3_32K.with_(L=2048, k_sel=8)
+    q, k, v, _ = synth.make_workload(w, device="cpu")
+    value, base = bench.oracle_leg_all_cores(w, q, k, v, 1)
+    assert value > 0
+    assert base["threads_available"] == len(os.sched_getaffinity(0))
+    assert base["cores"] == min(len(os.sched_getaffinity(0)), w.Hkv * w.G)

@@ -103,3 +103,30 @@ def test_static_matches_workspace_decode_two_calls(dtype):
             assert torch.isfinite(out).all(), f"case {i}"
             e = _rel_l2(out, ref)
             assert e <= tol and e <= 1e-4, f"case {i}: rel L2 {e:.3e}"
+
+
+@pytest.mark.gpu
+def test_static_extreme_shapes_two_calls():
+    # the shapes that size the array: the most problems the decode accepts
+    # (batch * KV heads * 16 <= 65535, here 4095 problems of 16 query heads:
+    # the most arrival counters), and a grid just under one wave of two CTAs
+    # per SM with two splits each (the most split partials, ~0.65 MiB on 152 SMs)
+    scale = 128 ** -0.5
+    cases = [
+        (kvd.F16, _case(kvd.F16, 4095, 1, 16, 100, 1, 0, 0, 903)),
+        (kvd.INT8, _case(kvd.INT8, 1, 38, 16, 2048, 24, 4, 64, 904)),
+    ]
+    refs = []
+    for _, (cache, q, ws, sel_idx, sel_cnt, max_sel) in cases:
+        ref = torch.full_like(q, float("nan"))
+        kvd.decode_attn(cache, q, scale, sel_idx, sel_cnt, max_sel, ref, ws)
+        refs.append(ref)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for (dtype, (cache, q, _ws, sel_idx, sel_cnt, max_sel)), ref in zip(cases, refs):
+            out = torch.full_like(q, float("nan"))
+            kvd.decode_attn_static(cache, q, scale, sel_idx, sel_cnt, max_sel, out)
+            torch.cuda.synchronize()
+            assert torch.isfinite(out).all()
+            e = _rel_l2(out, ref)
+            assert e <= {kvd.F16: 2e-3, kvd.INT8: 8e-3}[dtype] and e <= 1e-4, e
