@@ -616,6 +616,77 @@ def run_gqa_sweep(args):
         torch.cuda.empty_cache()
 
 
+SELECT_MARKS = {0: "entry", 1: "first bounds in", 2: "warp 0 scored", 3: "all warps scored",
+                4: "ticket taken", 6: "keys in shared memory", 7: "first digit",
+                8: "above-bitmap + bin collected", 9: "threshold found", 5: "list written",
+                10: "exit"}
+DECODE_MARKS = {0: "entry", 1: "dependency wait over", 8: "first copy issued",
+                2: "first stage in", 3: "all stages consumed", 4: "partial written",
+                5: "arrival counted", 6: "splits merged"}
+
+
+def run_stage_marks(args, w):
+    """Per-stage timings of one decode step from the kernels' %globaltimer marks
+    (a library built with KVD_MARKS=1 only).  Each of K steps runs after the
+    L2 flush; the marks of every CTA are read back after each step.  Printed:
+    per kernel and mark, the median over steps of the min / median / max over
+    CTAs, in microseconds from the step's first mark."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    marks = torch.zeros(kvd.MARK_KINDS * kvd.MARK_CTAS * kvd.MARK_SLOTS, dtype=torch.int64,
+                        device=dev)
+    kvd.debug_stage_marks(marks)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    drain = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    q, k, v, _ = synth.make_workload(w, device=dev)
+    cache = kvd.KVCache(w.dtype, w.B, w.Hkv, w.L + 64, head_dim=w.D, device=dev)
+    kvd.kv_append(cache, k, v)
+    del k, v
+    ws = kvd.make_workspace(cache, w.H)
+    nbmax = cache.max_seq // 64
+    sel_idx = torch.zeros((w.B, w.Hkv, nbmax), dtype=torch.int32, device=dev)
+    sel_cnt = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device=dev)
+    out = torch.empty(w.B, w.H, w.D, device=dev)
+    toks = [synth.make_step_token(w, s, device=dev) for s in range(8)]
+    per = {0: {}, 1: {}}
+    steps = max(1, args.steps)
+    for i in range(max(3, args.warmup) + steps):
+        flush.fill_(i & 0xFF)
+        drain.sum()
+        marks.zero_()
+        cache.len = w.L
+        kn, vn = toks[i % len(toks)]
+        kvd.decode_step(cache, q, kn, vn, w.scale, w.k_sel, w.sink_tokens, w.recent_tokens,
+                        out, ws, sel_idx=sel_idx, sel_cnt=sel_cnt)
+        torch.cuda.synchronize()
+        if i < max(3, args.warmup):
+            continue
+        m = marks.view(kvd.MARK_KINDS, kvd.MARK_CTAS, kvd.MARK_SLOTS).cpu().numpy()
+        live = m[:, :, 0] > 0
+        t0 = min(int(m[kind, live[kind], 0].min()) for kind in (0, 1) if live[kind].any())
+        for kind in (0, 1):
+            for slot in range(kvd.MARK_SLOTS):
+                vals = m[kind, :, slot]
+                vals = vals[vals > 0]
+                if vals.size:
+                    d = (vals - t0) / 1e3
+                    per[kind].setdefault(slot, []).append(
+                        (float(d.min()), float(np.median(d)), float(d.max()), int(vals.size)))
+    assert cache.device_status() == 0, "device-side fault reported"
+    kvd.debug_stage_marks(None)
+    for kind, names in ((0, SELECT_MARKS), (1, DECODE_MARKS)):
+        rows = []
+        for slot, vals in sorted(per[kind].items(), key=lambda kv: statistics.median(
+                x[1] for x in kv[1])):
+            med = [statistics.median(x[j] for x in vals) for j in range(4)]
+            rows.append({"mark": names.get(slot, str(slot)), "slot": slot,
+                         "us_min": round(med[0], 2), "us_median": round(med[1], 2),
+                         "us_max": round(med[2], 2), "ctas": int(med[3])})
+        print(json.dumps({"stage_marks": "select" if kind == 0 else "decode",
+                          "workload": w.name, "context": w.L, "steps": steps, "rows": rows}),
+              flush=True)
+
+
 # The metric's other contexts, reported beside the 1M headline.
 CONTEXT_WORKLOADS = ("qwen3_4b_gqa_32k_f16", "ctx128k_b8_int8")
 
@@ -767,6 +838,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage-marks", action="store_true",
+                    help="print per-stage timings of the step from the kernels' timer marks "
+                         "(needs the library built with KVD_MARKS=1)")
     ap.add_argument("--no-contexts", action="store_true",
                     help="leave out the 32K and 128K x 8 sub-records of the default line")
     ap.add_argument("--context", type=int, default=None,
@@ -804,6 +878,8 @@ def main():
         w = w.with_(D=args.head_dim)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.stage_marks:
+        return run_stage_marks(args, w)
 
     world, rank, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)

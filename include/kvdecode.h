@@ -450,6 +450,20 @@ KVD_API kvd_status kvd_debug_scores(const kvd_cache *cache, const float *q, int3
 /* ---------------------------------------------------------------------- */
 KVD_API kvd_status kvd_debug_wait_timeout(int32_t *dev_status, int32_t limit_us, void *stream);
 
+/* ---------------------------------------------------------------------- */
+/* Profiling export (no counterpart on the pages): stage marks.  In a      */
+/* library built with KVD_MARKS (build.py: environment KVD_MARKS=1) the    */
+/* kernels write the GPU's global nanosecond timer at numbered points of   */
+/* their work into `marks`, a caller-owned device buffer of at least       */
+/* 3 * 4096 * 16 * 8 bytes (16-byte aligned): region k (0 selection,       */
+/* 1 decode, 2 other kernels) holds 16 slots per CTA for up to 4096 CTAs,  */
+/* numbered x-fastest.  Later launches write into it until it is replaced; */
+/* marks = NULL turns recording off.  Host only; nothing is launched.      */
+/* Errors: UNSUPPORTED in every build without marks (the default);         */
+/* INVALID when the buffer is too small or misaligned.                     */
+/* ---------------------------------------------------------------------- */
+KVD_API kvd_status kvd_debug_stage_marks(void *marks, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

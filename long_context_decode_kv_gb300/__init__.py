@@ -39,7 +39,7 @@ EXPORTS = ("kvd_kv_append", "kvd_select_blocks", "kvd_decode_attn", "kvd_decode_
            "kvd_selected_count", "kvd_status_string", "kvd_abi_version", "kvd_debug_qk_int8",
            "kvd_debug_scores", "kvd_decode_attn_static", "kvd_decode_attn_sv",
            "kvd_decode_attn_tail", "kvd_kv_append_f32", "kvd_select_blocks_per_head",
-           "kvd_decode_attn_per_head", "kvd_debug_wait_timeout")
+           "kvd_decode_attn_per_head", "kvd_debug_wait_timeout", "kvd_debug_stage_marks")
 
 
 class KvdError(RuntimeError):
@@ -96,6 +96,7 @@ def lib():
         L.kvd_debug_qk_int8.argtypes = [cp, p, i32, p, p, p, p]
         L.kvd_debug_scores.argtypes = [cp, p, i32, p, p]
         L.kvd_debug_wait_timeout.argtypes = [p, i32, p]
+        L.kvd_debug_stage_marks.argtypes = [p, sz]
         _lib = L
     return _lib
 
@@ -368,12 +369,26 @@ def debug_wait_timeout(status: torch.Tensor, limit_us: int, stream=None):
         _ptr(status), int(limit_us), _stream(status, stream)))
 
 
+MARK_SLOTS = 16
+MARK_CTAS = 4096
+MARK_KINDS = 3
+
+
+def debug_stage_marks(marks: Optional[torch.Tensor]):
+    """Give the library a device buffer for stage marks (int64, at least
+    MARK_KINDS * MARK_CTAS * MARK_SLOTS elements), or None to stop recording.
+    Raises KvdError (UNSUPPORTED) unless the library was built with marks."""
+    n = 0 if marks is None else marks.numel() * marks.element_size()
+    _check("kvd_debug_stage_marks", lib().kvd_debug_stage_marks(_ptr(marks), n))
+
+
 def debug_scores(cache: KVCache, q: torch.Tensor, ub: torch.Tensor, stream=None):
     _check("kvd_debug_scores", lib().kvd_debug_scores(
         cache.ref(), _ptr(q), int(q.shape[1]), _ptr(ub), _stream(q, stream)))
 
 
 __all__ = ["F16", "INT8", "Q8_0", "Q4_0", "BLOCK", "HEAD_DIM", "KVCache", "KvdError", "CacheStruct", "lib",
+           "debug_stage_marks", "MARK_SLOTS", "MARK_CTAS", "MARK_KINDS",
            "workspace_bytes", "make_workspace", "selected_count", "status_string", "kv_append",
            "kv_append_f32", "select_blocks", "decode_attn", "decode_attn_dense", "decode_attn_static",
            "decode_attn_sv", "decode_attn_tail", "select_blocks_per_head",

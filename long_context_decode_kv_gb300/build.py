@@ -3,6 +3,12 @@
 Each ``csrc/*.cu`` compiles to an object in parallel, then one ``nvcc -shared``
 links them with the static CUDA runtime.  No torch headers are involved: the
 library's ABI is plain C (``include/kvdecode.h``).
+
+With the environment variable KVD_MARKS=1 the library is built with stage
+marks (``-DKVD_MARKS``: the kernels record %globaltimer at numbered points,
+read back through kvd_debug_stage_marks; ``bench.py --stage-marks``).  That
+build keeps its objects apart and relinks the library whenever the mode
+changes; the default build has no marks code at all.
 """
 from __future__ import annotations
 
@@ -16,13 +22,15 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-OBJDIR = os.path.join(PKG, "_build")
+MARKS = os.environ.get("KVD_MARKS") == "1"
+OBJDIR = os.path.join(PKG, "_build_marks" if MARKS else "_build")
 LIB = os.path.join(PKG, "libkvdecode.so")
+MODE_FILE = os.path.join(PKG, "_build", "library_mode")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",
-              "-I", INCLUDE, "-I", CSRC]
+              "-I", INCLUDE, "-I", CSRC] + (["-DKVD_MARKS"] if MARKS else [])
 
 
 def nvcc() -> str:
@@ -47,8 +55,17 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _mode_changed():
+    mode = "marks" if MARKS else "plain"
+    try:
+        return open(MODE_FILE).read().strip() != mode
+    except OSError:
+        return True
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     os.makedirs(OBJDIR, exist_ok=True)
+    os.makedirs(os.path.dirname(MODE_FILE), exist_ok=True)
     hdrs = _deps()
     srcs = sources()
     objs = [os.path.join(OBJDIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
@@ -72,12 +89,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
-    if force or jobs or _stale(LIB, objs):
+    if force or jobs or _stale(LIB, objs) or _mode_changed():
         cmd = [nvcc(), *ARCH, "-shared", "-o", LIB + ".tmp", *objs]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.run(cmd, check=True)
         os.replace(LIB + ".tmp", LIB)
+        with open(MODE_FILE, "w") as f:
+            f.write("marks" if MARKS else "plain")
     return LIB
 
 

@@ -83,6 +83,20 @@ cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *occ) {
 }
 
 namespace {
+std::atomic<unsigned long long *> g_marks{nullptr};
+}  // namespace
+
+unsigned long long *mark_region(int kind) {
+#ifdef KVD_MARKS
+    unsigned long long *m = g_marks.load(std::memory_order_relaxed);
+    return m ? m + static_cast<size_t>(kind) * kMarkCtas * kMarkSlots : nullptr;
+#else
+    (void)kind;
+    return nullptr;
+#endif
+}
+
+namespace {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) % 4) == 0; }
 }  // namespace
@@ -652,6 +666,19 @@ kvd_status kvd_debug_qk_int8(const kvd_cache *cache, const float *q, int32_t n_h
     const Geom g = make_geom(cache, n_heads, cache->len);
     return cuda_status(launch_qk_debug(*cache, g, q, dots, q_codes, q_scales,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+kvd_status kvd_debug_stage_marks(void *marks, size_t bytes) {
+#ifdef KVD_MARKS
+    const size_t need = static_cast<size_t>(kMarkKinds) * kMarkCtas * kMarkSlots * 8;
+    if (marks && (bytes < need || !aligned16(marks))) return KVD_ERR_INVALID;
+    g_marks.store(static_cast<unsigned long long *>(marks), std::memory_order_relaxed);
+    return KVD_OK;
+#else
+    (void)marks;
+    (void)bytes;
+    return KVD_ERR_UNSUPPORTED;
+#endif
 }
 
 kvd_status kvd_debug_wait_timeout(int32_t *dev_status, int32_t limit_us, void *stream) {

@@ -34,6 +34,25 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Stage marks (builds with -DKVD_MARKS only; kvd_debug_stage_marks): the
+// calling thread writes the global timer to slot `slot` of this CTA's row of
+// `marks` (kMarkSlots words per CTA, CTAs numbered x-fastest; rows past
+// kMarkCtas are not recorded).  Without the flag the macro is empty.
+constexpr int kMarkSlots = 16;
+constexpr int kMarkCtas = 4096;
+#ifdef KVD_MARKS
+#define KVD_MARK(marks, slot)                                                              \
+    do {                                                                                   \
+        const unsigned kvd_cta_ = blockIdx.y * gridDim.x + blockIdx.x;                     \
+        if ((marks) != nullptr && kvd_cta_ < static_cast<unsigned>(kMarkCtas))             \
+            (marks)[static_cast<size_t>(kvd_cta_) * kMarkSlots + (slot)] = global_timer_ns(); \
+    } while (0)
+#else
+#define KVD_MARK(marks, slot) \
+    do {                      \
+    } while (0)
+#endif
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
                  : "memory");

@@ -134,6 +134,7 @@ struct DecodeArgs {
     int per_head;      // lists per query head ([B, H] rows; one head per CTA)
     const int32_t *seq_lens;  // per-sequence lengths (<= len), or null
     int seq_add;              // tokens appended by this step that seq_lens lacks
+    unsigned long long *marks;  // stage marks (KVD_MARKS builds), or null
 };
 
 template <int DT, int GC, bool TAIL = false, bool WIDE = false>
@@ -1084,12 +1085,14 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         *abort_flag = 0;
         *issued_s = 0;
         fence_barrier_init();
+        KVD_MARK(a.marks, 0);  // entry
     }
     __syncthreads();
     // Inside a decode step the query was written before the step's first
     // kernel, so it may be read while the selection is still finishing.
     if (a.early_q) load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
     pdl_wait();  // upstream kernels (append, select) are complete past here
+    if (tid == 0) KVD_MARK(a.marks, 1);  // dependency wait over
     pdl_launch_dependents();
     // the list row: the KV head's, or with per-head lists the CTA's one head's
     const int lrow = a.per_head ? prob : bg;
@@ -1140,6 +1143,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                         ok = mbar_wait(&empty[s], ((i / TL::kStages) - 1) & 1, abort_flag);
                     if (ok) {
                         if (blk >= 0 && blk < NB) {
+                            if (i == 0) KVD_MARK(a.marks, 8);  // first copy issued
                             stage_blk[s] = blk;
                             uint8_t *dst = smem + SL::kStagesOff + s * TL::kStageBytes;
                             const size_t r = row0 + static_cast<size_t>(blk) * kBlock;
@@ -1229,6 +1233,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     break;
                 }
                 const int blk = stage_blk[s];
+                if (i == group && tid == 0) KVD_MARK(a.marks, 2);  // first stage in
                 if (blk == kEndMark) break;
                 if (TAIL && blk <= kTailBase) {
                     at_tail = true;
@@ -1256,6 +1261,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     break;
                 }
                 const int blk = stage_blk[s];
+                if (i == group && tid == 0) KVD_MARK(a.marks, 2);  // first stage in
                 if (blk == kEndMark) break;
                 if (TAIL && blk <= kTailBase) {
                     at_tail = true;
@@ -1287,6 +1293,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                     break;
                 }
                 const int blk = stage_blk[s];
+                if (i == group && tid == 0) KVD_MARK(a.marks, 2);  // first stage in
                 if (blk == kEndMark) break;
                 if (TAIL && blk <= kTailBase) {
                     at_tail = true;
@@ -1317,6 +1324,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         }
     }
     __syncthreads();  // (A) every stage consumed: the ring becomes scratch
+    if (tid == 0) KVD_MARK(a.marks, 3);  // every stage consumed
     const bool aborted = *abort_flag != 0;
     if (!aborted && warp < TL::kConsumerWarps) {
         float *mg = reinterpret_cast<float *>(smem + SL::kStagesOff);
@@ -1397,9 +1405,12 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
 
     // ---- the last CTA of this problem to arrive merges all splits
     __syncthreads();  // every partial store of the CTA precedes the release
-    if (tid == 0)
+    if (tid == 0) {
+        KVD_MARK(a.marks, 4);  // partial written
         *last_flag = atomic_add_acq_rel_gpu(&a.counters[prob], 1u) ==
                      static_cast<unsigned>(a.splits - 1);
+        KVD_MARK(a.marks, 5);  // arrival counted
+    }
     __syncthreads();
     if (!*last_flag) return;
     // Thread (part, h, 4 channels) merges the splits of its part online:
@@ -1480,7 +1491,10 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
                                     4 * d4) = make_float4(A.x * inv, A.y * inv, A.z * inv,
                                                           A.w * inv);
     }
-    if (tid == 0) a.counters[prob] = 0u;  // leave the counter ready for the next call
+    if (tid == 0) {
+        a.counters[prob] = 0u;  // leave the counter ready for the next call
+        KVD_MARK(a.marks, 6);   // splits merged
+    }
 }
 
 DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan &p,
@@ -1514,6 +1528,7 @@ DecodeArgs make_decode_args(const kvd_cache &c, const Geom &g, const DecodePlan 
     a.subgroups = p.subgroups;
     a.plan_blocks = p.blocks;
     a.scale_log2 = scale * kLog2e;
+    a.marks = mark_region(kMarkDecode);
     return a;
 }
 

@@ -48,6 +48,12 @@ int device_sm_count();
 // devices may launch at the same time.
 cudaError_t prepare_kernel(const void *fn, int threads, size_t smem, int *occ = nullptr);
 
+// Stage marks of kernel kind `kind` (0 selection, 1 decode, 2 other):
+// kMarkCtas * kMarkSlots words, or null when marks are off (every build
+// without -DKVD_MARKS, or no buffer given to kvd_debug_stage_marks).
+enum MarkKind { kMarkSelect = 0, kMarkDecode = 1, kMarkOther = 2, kMarkKinds = 3 };
+unsigned long long *mark_region(int kind);
+
 // Host argument rules shared by the entry points (api.cu): the cache
 // descriptor, and the query-head count against it.
 kvd_status check_cache(const kvd_cache *c);

@@ -48,6 +48,7 @@ cudaError_t launch_select_t(const SelArgs &a0, int P, cudaStream_t st, bool pdl)
                                          kScoreThreads, smem, &occupancy);
     if (e != cudaSuccess) return e;
     SelArgs a = a0;
+    a.marks = mark_region(kMarkSelect);
     // CTAs per problem: as many as fit on the GPU at once, split evenly (a
     // small problem still gains from many CTAs streaming its bounds)
     const long cap = static_cast<long>(occupancy) * device_sm_count();

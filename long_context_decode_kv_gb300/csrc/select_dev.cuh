@@ -217,6 +217,7 @@ struct SelArgs {
     // its block is forced (never scored); app_cache.len is the length before
     kvd_cache app_cache;
     const __half *app_k, *app_v;
+    unsigned long long *marks;  // stage marks (KVD_MARKS builds), or null
 };
 
 __device__ __forceinline__ int warp_inclusive_scan(int x, int lane) {
@@ -406,6 +407,7 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, size_t row, int 
     if (IN_SMEM && tid == 0) atomicAdd(&hist[0], n - (n + 3) / 4 * 4);  // padding keys (kmin)
     if (tid == 0) rs.ccount = 0;
     const int d1 = radix_digit<kBins1>(hist, krem, rs);
+    if (tid == 0) KVD_MARK(a.marks, 7);  // first digit found
 
     // ---- one pass: keys in bins above d1 are in; keys in bin d1 are collected.
     // Thread t builds word t (keys 32t .. 32t+31) in registers, reading its
@@ -460,6 +462,7 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, size_t row, int 
         }
     }
     __syncthreads();
+    if (tid == 0) KVD_MARK(a.marks, 8);  // above-bitmap written, threshold bin collected
     const int m = rs.ccount;
     const bool compact = m <= kCandCap;
     if (m <= kRankMax) {
@@ -477,6 +480,7 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, size_t row, int 
             if (lane == 0 && beats < krem) atomicOr(&gtw[jc >> 5], 1u << (jc & 31));
         }
         __syncthreads();
+        if (tid == 0) KVD_MARK(a.marks, 9);  // threshold bin ranked
         select_write_list(a, row, n, gtw, eqw, 0, rs);
         return;
     }
@@ -528,6 +532,7 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, size_t row, int 
         }
     }
     __syncthreads();
+    if (tid == 0) KVD_MARK(a.marks, 9);  // threshold found by the later digits
 
     // ================================================= phase 4: the list
     select_write_list(a, row, n, gtw, eqw, need_eq, rs);
@@ -633,6 +638,7 @@ __device__ __forceinline__ void select_rank(const SelArgs &a, int p, size_t row,
 
     // ================================================= phase 3: T
     if (in_smem && !mbar_wait(&rs.kbar, 0, abort_flag)) s_abort = 1;
+    if (tid == 0) KVD_MARK(a.marks, 6);  // keys in shared memory
     // the row's padding keys (up to 3 past n) read as kmin: bin 0, taken back out
     if (in_smem && tid < a.ldn - n && !s_abort)
         reinterpret_cast<uint32_t *>(ring)[n + tid] = rs.kmin;
@@ -724,6 +730,7 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
         rs.kmin = 0xffffffffu;
         rs.kmax = 0u;
         fence_barrier_init();
+        KVD_MARK(a_in.marks, 0);  // entry
     }
     __syncthreads();
     // overlap: inside a decode step whose appended token lands in a forced
@@ -784,6 +791,7 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
                 }
                 break;
             }
+            if (si == 0 && tid == 0) KVD_MARK(a.marks, 1);  // first bounds in
             const uint8_t *st = ring + s * kScoreStageBytes;
             float sc[2];
             int jr[2];
@@ -824,6 +832,7 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
                 }
             }
         }
+        if (tid == 0) KVD_MARK(a.marks, 2);  // warp 0 scored its blocks
         if constexpr (MODE != kExport) {
             tmin = __reduce_min_sync(kFullMask, tmin);
             tmax = __reduce_max_sync(kFullMask, tmax);
@@ -864,12 +873,14 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
         // zero-based maxima), then the ticket; its release covers the keys
         __syncthreads();
         if (tid == 0) {
+            KVD_MARK(a.marks, 3);  // every warp scored
             if (n > kSmallRank) {  // the radix tail bins over the keys' range
                 unsigned *rg = a.range + 2 * static_cast<size_t>(p);
                 atomicMax(rg, rs.kmax);
                 atomicMax(rg + 1, ~rs.kmin);
             }
             rs.last = atomic_add_acq_rel_gpu(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
+            KVD_MARK(a.marks, 4);  // ticket taken
         }
         __syncthreads();
     }
@@ -883,8 +894,10 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
         } else {
             select_rank(a, p, row, n, X, kp, in_smem, ring, rs, s_abort);
         }
+        if (tid == 0) KVD_MARK(a.marks, 5);  // list written
     }
     if (appends) fused_append(a, b, g, lane);
+    if (tid == 0) KVD_MARK(a.marks, 10);  // exit
 }
 
 

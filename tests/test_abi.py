@@ -210,6 +210,8 @@ def test_wait_timeout_validation():
     assert L.kvd_debug_wait_timeout(FAKE + 2, 1000, None) == INVALID
     assert L.kvd_debug_wait_timeout(FAKE, 0, None) == INVALID
     assert L.kvd_debug_wait_timeout(FAKE, 1000001, None) == INVALID
+    # stage marks exist only in a library built with KVD_MARKS=1
+    assert L.kvd_debug_stage_marks(FAKE, 3 * 4096 * 16 * 8) == UNSUPPORTED
 
 
 def test_append_validation():
