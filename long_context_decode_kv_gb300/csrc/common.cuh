@@ -199,18 +199,6 @@ __device__ __forceinline__ uint32_t float_to_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Four signed bytes of `w` -> four exact floats.  Flipping the sign bit
-// turns int8 b into the unsigned byte b+128; placed as the low mantissa
-// byte of 2^23 it reads as the float 2^23 + b + 128, and subtracting
-// 2^23 + 128 leaves b exactly.
-__device__ __forceinline__ void s8x4_to_f32(uint32_t w, float (&f)[4]) {
-    const uint32_t u = w ^ 0x80808080u;
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.0f;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.0f;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.0f;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.0f;
-}
-
 // q8_0 quantization of one 128-wide row held 4 values per lane by a full
 // warp: the 8 lanes 8g..8g+7 hold group g (channels 32g..32g+31).  The
 // group's scale is d = fl16(absmax/127) (the IEEE f32 quotient rounded to

@@ -528,16 +528,14 @@ __device__ __forceinline__ void sparse_v_keep(const float (&x)[NT], float bm, in
     for (int i = 0; i < NT; ++i) keep[i] = !(c[i] < thr);
 }
 
-// Four signed bytes -> two exact float pairs (see s8x4_to_f32 in common.cuh).
+// Four signed bytes -> two exact float pairs, one integer-to-float
+// conversion per byte (fewer instructions than building each float from
+// the byte's bits: this loop is the consumers' largest cost).
 __device__ __forceinline__ void s8x4_to_f32x2(uint32_t w, float2 &f01, float2 &f23) {
-    const uint32_t u = w ^ 0x80808080u;
-    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
-    f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)),
-                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651))),
-                     bias);
-    f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)),
-                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653))),
-                     bias);
+    f01 = make_float2(static_cast<float>(static_cast<int8_t>(w & 0xffu)),
+                      static_cast<float>(static_cast<int8_t>((w >> 8) & 0xffu)));
+    f23 = make_float2(static_cast<float>(static_cast<int8_t>((w >> 16) & 0xffu)),
+                      static_cast<float>(static_cast<int8_t>(w >> 24)));
 }
 
 // One stage (64-token block) for one consumer warp (wg = its index in the
