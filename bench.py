@@ -619,7 +619,8 @@ def run_gqa_sweep(args):
 SELECT_MARKS = {0: "entry", 1: "first bounds in", 2: "warp 0 scored", 3: "all warps scored",
                 4: "ticket taken", 6: "keys in shared memory", 7: "first digit",
                 8: "above-bitmap + bin collected", 9: "threshold found", 5: "list written",
-                10: "exit"}
+                10: "exit", 11: "first-digit keys counted (thread 0)",
+                12: "list offsets scanned", 13: "list written (last warp)"}
 DECODE_MARKS = {0: "entry", 1: "dependency wait over", 8: "first copy issued",
                 2: "first stage in", 3: "all stages consumed", 4: "partial written",
                 5: "arrival counted", 6: "splits merged"}

@@ -47,9 +47,21 @@ constexpr int kMarkCtas = 4096;
         if ((marks) != nullptr && kvd_cta_ < static_cast<unsigned>(kMarkCtas))             \
             (marks)[static_cast<size_t>(kvd_cta_) * kMarkSlots + (slot)] = global_timer_ns(); \
     } while (0)
+// The latest of the callers' timer values (every caller writes; the
+// maximum stays): when the last of several warps reached the mark.
+#define KVD_MARK_LAST(marks, slot)                                                         \
+    do {                                                                                   \
+        const unsigned kvd_cta_ = blockIdx.y * gridDim.x + blockIdx.x;                     \
+        if ((marks) != nullptr && kvd_cta_ < static_cast<unsigned>(kMarkCtas))             \
+            atomicMax((marks) + static_cast<size_t>(kvd_cta_) * kMarkSlots + (slot),       \
+                      global_timer_ns());                                                  \
+    } while (0)
 #else
 #define KVD_MARK(marks, slot) \
     do {                      \
+    } while (0)
+#define KVD_MARK_LAST(marks, slot) \
+    do {                           \
     } while (0)
 #endif
 

@@ -230,7 +230,6 @@ __device__ __forceinline__ int warp_inclusive_scan(int x, int lane) {
 }
 
 struct RadixShared {
-    uint64_t kbar;  // bulk copy of the keys (last CTA)
     int wsum[kScoreWarps + 1];
     int digit, above, last;
     unsigned kmin, kmax;  // the CTA's, then the problem's, key range
@@ -357,6 +356,7 @@ __device__ __forceinline__ void select_write_list(const SelArgs &a, size_t row, 
     const unsigned incl = static_cast<unsigned>(warp_inclusive_scan(static_cast<int>(mine), lane));
     if (lane == 31) rs.wsum[warp] = static_cast<int>(incl);
     __syncthreads();
+    if (tid == 0) KVD_MARK(a.marks, 12);  // list offsets scanned
     unsigned before = incl - mine;
     for (int w = 0; w < warp; ++w) before += static_cast<unsigned>(rs.wsum[w]);
     int g_before = static_cast<int>(before & 0xffffu), e_before = static_cast<int>(before >> 16);
@@ -377,6 +377,7 @@ __device__ __forceinline__ void select_write_list(const SelArgs &a, size_t row, 
     for (int j = tid; j < a.se; j += kScoreThreads) dst[j] = j;
     for (int j = a.rb + tid; j < a.NB; j += kScoreThreads) dst[a.se + a.keff + (j - a.rb)] = j;
     if (tid == 0) a.sel_cnt[row] = a.se + a.keff + (a.NB - a.rb);
+    if (lane == 0) KVD_MARK_LAST(a.marks, 13);  // the last warp's list entries written
 }
 
 // Phases 3-4 of the last CTA of a problem, with the problem's key range
@@ -403,6 +404,7 @@ __device__ __forceinline__ void select_finish(const SelArgs &a, size_t row, int 
 
     // ---- digit 1: the bin v >> shift of T (krem: keys still to take from it)
     count_digits<true, IN_SMEM>(ksrc, n, kmin, 31, 0u, shift, kBins1 - 1, hist);
+    if (tid == 0) KVD_MARK(a.marks, 11);  // thread 0's keys counted
     int krem = a.keff;
     if (IN_SMEM && tid == 0) atomicAdd(&hist[0], n - (n + 3) / 4 * 4);  // padding keys (kmin)
     if (tid == 0) rs.ccount = 0;
@@ -605,21 +607,34 @@ __device__ __forceinline__ void select_small(const SelArgs &a, size_t row, int n
 // (when they fit), the key range, then the radix select and the list.
 __device__ __forceinline__ void select_rank(const SelArgs &a, int p, size_t row, int n, int X,
                                             const uint32_t *kp, bool in_smem, uint8_t *ring,
-                                            RadixShared &rs, int &s_abort) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    volatile int *abort_flag = &s_abort;
-    if (in_smem && warp == kScoreWarps) {
-        // the problem's keys (L2-resident) into the ring by bulk copies; they
-        // were written by ordinary stores, so order those before the async proxy
-        const uint32_t bytes = static_cast<uint32_t>(a.ldn) * 4u;
-        const uint32_t off = static_cast<uint32_t>(lane) * kScoreStageBytes;
-        asm volatile("fence.proxy.async;" ::: "memory");
-        if (lane == 0) mbar_arrive_expect_tx(&rs.kbar, bytes);
-        __syncwarp();
-        if (off < bytes)
-            tma_load_1d(ring + off, reinterpret_cast<const uint8_t *>(kp) + off,
-                        min(static_cast<uint32_t>(kScoreStageBytes), bytes - off), &rs.kbar,
-                        l2_policy_evict_first());
+                                            RadixShared &rs) {
+    const int tid = threadIdx.x;
+    // the problem's key range: loads issued ahead of the copy, used after it
+    unsigned *rg = a.range + 2 * static_cast<size_t>(p);
+    unsigned r_max = 0u, r_nmin = 0u;
+    if (X > 1 && tid == 0) {
+        r_max = __ldcg(rg);
+        r_nmin = __ldcg(rg + 1);
+    }
+    if (in_smem) {
+        // the problem's keys (L2-resident) into the ring, 16 bytes per thread
+        // and load, eight loads in flight per thread before any store
+        const int nq = a.ldn / 4;
+        const uint4 *src = reinterpret_cast<const uint4 *>(kp);
+        uint4 *dst = reinterpret_cast<uint4 *>(ring);
+        for (int i0 = tid; i0 < nq; i0 += 8 * kScoreThreads) {
+            uint4 w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kScoreThreads;
+                w[u] = i < nq ? __ldcg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kScoreThreads;
+                if (i < nq) dst[i] = w[u];
+            }
+        }
     }
     // tail scratch: the ring past the keys (the histogram part zeroed)
     uint8_t *scratch = ring + (in_smem ? kRingKeys * 4 : 0);
@@ -628,29 +643,19 @@ __device__ __forceinline__ void select_rank(const SelArgs &a, int p, size_t row,
         for (int i = tid; i < kBins1 / 4; i += kScoreThreads) h4[i] = make_int4(0, 0, 0, 0);
     }
     if (X > 1 && tid == 0) {
-        unsigned *rg = a.range + 2 * static_cast<size_t>(p);
-        rs.kmax = __ldcg(rg);
-        rs.kmin = ~__ldcg(rg + 1);
+        rs.kmax = r_max;
+        rs.kmin = ~r_nmin;
         __stcg(rg, 0u);  // leave the words ready for the next call
         __stcg(rg + 1, 0u);
         a.ticket[p] = 0u;
     }
 
     // ================================================= phase 3: T
-    if (in_smem && !mbar_wait(&rs.kbar, 0, abort_flag)) s_abort = 1;
+    __syncthreads();  // keys copied; the range in rs
     if (tid == 0) KVD_MARK(a.marks, 6);  // keys in shared memory
     // the row's padding keys (up to 3 past n) read as kmin: bin 0, taken back out
-    if (in_smem && tid < a.ldn - n && !s_abort)
-        reinterpret_cast<uint32_t *>(ring)[n + tid] = rs.kmin;
-    if (__syncthreads_or(s_abort)) {
-        if (tid == 0) {
-            report_status(a.dev_status, KVD_ERR_TIMEOUT);
-            a.sel_cnt[row] = 0;
-            volatile int never = 0;
-            if (in_smem) (void)mbar_wait(&rs.kbar, 0, &never);  // copies in flight
-        }
-        return;
-    }
+    if (in_smem && tid < a.ldn - n) reinterpret_cast<uint32_t *>(ring)[n + tid] = rs.kmin;
+    __syncthreads();
     // the rest reads the keys from shared memory, or from L2 for a problem too
     // large for the ring; each variant is compiled with its address space known
     if (in_smem)
@@ -724,7 +729,6 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kScoreWarps);
         }
-        mbar_init(&rs.kbar, 1);
         s_abort = 0;
         s_issued = 0;
         rs.kmin = 0xffffffffu;
@@ -892,7 +896,7 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
             if (X > 1 && tid == 0) a.ticket[p] = 0u;  // ready for the next call
             select_small(a, row, n, kp, rs.wsum);
         } else {
-            select_rank(a, p, row, n, X, kp, in_smem, ring, rs, s_abort);
+            select_rank(a, p, row, n, X, kp, in_smem, ring, rs);
         }
         if (tid == 0) KVD_MARK(a.marks, 5);  // list written
     }
