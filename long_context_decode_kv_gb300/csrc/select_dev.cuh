@@ -231,7 +231,7 @@ __device__ __forceinline__ int warp_inclusive_scan(int x, int lane) {
 
 struct RadixShared {
     int wsum[kScoreWarps + 1];
-    int digit, above, last;
+    int digit, above, last, first;
     unsigned kmin, kmax;  // the CTA's, then the problem's, key range
     int ccount;           // keys collected from the threshold bin
 };
@@ -861,11 +861,11 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
     if (a.overlap) pdl_wait();  // the upstream kernels are complete past here
     if constexpr (MODE == kExport) return;
     // The decode step's token for (b, g) is appended by warp 0 of the first
-    // tile, after the dependency wait (the previous step's kernels may still
-    // read the row it replaces) and off the way to the ranking: once the
-    // tile's ticket shows another CTA ranks, else after its own ranking.  The
-    // step's decode kernel waits for this whole grid, so it sees the token.
-    const bool appends = a.app_k && x_tile == 0 && warp == 0;
+    // CTA of the problem to take its ticket, after the dependency wait (the
+    // previous step's kernels may still read the row it replaces) and off the
+    // way to the ranking, which the last CTA does (a problem of one CTA
+    // appends after its ranking).  The step's decode kernel waits for this
+    // whole grid, so it sees the token.
 
     // ================================================= phase 2: ticket
     const int X = n_tiles;
@@ -883,13 +883,17 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
                 atomicMax(rg, rs.kmax);
                 atomicMax(rg + 1, ~rs.kmin);
             }
-            rs.last = atomic_add_acq_rel_gpu(a.ticket + p, 1u) == static_cast<unsigned>(X - 1);
+            const unsigned t = atomic_add_acq_rel_gpu(a.ticket + p, 1u);
+            rs.last = t == static_cast<unsigned>(X - 1);
+            rs.first = t == 0u;
             KVD_MARK(a.marks, 4);  // ticket taken
         }
         __syncthreads();
     }
-    // the last CTA of the problem (every key is in) ranks; the step's token is
-    // appended on one path out of every CTA
+    // the first CTA to arrive appends the step's token; the last (every key
+    // is in) ranks
+    const bool appends = a.app_k && warp == 0 && (X == 1 || rs.first);
+    if (appends && X > 1) fused_append(a, b, g, lane);
     if (X == 1 || rs.last) {
         if (n <= kSmallRank) {
             __syncthreads();  // (X == 1) this CTA's key stores, seen by all its threads
@@ -900,7 +904,7 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
         }
         if (tid == 0) KVD_MARK(a.marks, 5);  // list written
     }
-    if (appends) fused_append(a, b, g, lane);
+    if (appends && X == 1) fused_append(a, b, g, lane);
     if (tid == 0) KVD_MARK(a.marks, 10);  // exit
 }
 

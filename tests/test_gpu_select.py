@@ -219,3 +219,37 @@ def test_select_crowded_threshold_bin(cluster, nb):
         assert kth == 1.0
         n = int(sel_cnt[0, 0])
         assert sel_idx[0, 0, :n].cpu().numpy().tolist() == want.tolist()
+
+
+@pytest.mark.parametrize("nb", [100, 531])
+def test_select_bounds_of_both_signs(nb):
+    # Each block's bound is one chosen f16 value (q = e_0, channel 0's kmin =
+    # kmax = value): seeded normal values, so the keys of one problem span
+    # negative and positive bounds (a key range of more than 2^31) and some
+    # values repeat.  The bounds are exact, so the list must equal the
+    # oracle's: the few-candidate ranking (100 blocks) and the radix tail (531).
+    B, Hkv, G = 1, 1, 1
+    L = nb * 64 - 17
+    gc = kvd.KVCache(kvd.F16, B, Hkv, nb * 64, device=dev())
+    rng = np.random.default_rng(97 + nb)
+    vals = (rng.standard_normal(nb) * 4.0).astype(np.float16)
+    vals[rng.integers(0, nb, 8)] = vals[3]  # ties
+    kb = torch.zeros((B, Hkv, nb, 128, 2), dtype=torch.float16)
+    kb[0, 0, :, 0, 0] = torch.from_numpy(vals)
+    kb[0, 0, :, 0, 1] = torch.from_numpy(vals)
+    gc.t["kbounds"].copy_(kb.to(dev()))
+    gc.len = L
+    q = torch.zeros((B, Hkv * G, 128), dtype=torch.float32, device=dev())
+    q[..., 0] = 1.0
+    ws = kvd.make_workspace(gc, Hkv * G)
+    sel_idx = torch.full((B, Hkv, nb), -7, dtype=torch.int32, device=dev())
+    sel_cnt = torch.full((B, Hkv), -7, dtype=torch.int32, device=dev())
+    for k_sel in (1, nb // 3, nb - 20):
+        kvd.select_blocks(gc, q, k_sel, 4, 256, sel_idx, sel_cnt, ws)
+        torch.cuda.synchronize()
+        ub, _, _ = oracle.block_scores(q[0].cpu().numpy(), gc.kmin[0, 0].cpu().numpy(),
+                                       gc.kmax[0, 0].cpu().numpy())
+        assert (ub < 0).any() and (ub > 0).any()
+        want, _ = oracle.select(L, 64, ub, k_sel, 4, 256)
+        n = int(sel_cnt[0, 0])
+        assert sel_idx[0, 0, :n].cpu().numpy().tolist() == want.tolist(), k_sel
