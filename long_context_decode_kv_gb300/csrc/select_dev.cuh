@@ -26,8 +26,8 @@
 // the few keys inside it, digits of those keys' low bits, then the
 // ascending list written in index order.  No CTA waits for another.
 // A problem of at most kSmallRank candidates skips the copy and the radix
-// passes: its last CTA holds one key per thread and builds T bit by bit from
-// block-wide counts (select_small).
+// passes over the whole ring: its last CTA holds one key per thread and finds
+// T from 8-bit radix digits over the keys' range (select_small).
 //
 // Modes (template MODE): kExport writes the bounds for the tests; kSelect
 // selects; kVarlen finds each problem's geometry from its own sequence length
@@ -563,41 +563,110 @@ __device__ __noinline__ void select_finish_from_l2(const SelArgs &a, size_t row,
     select_finish<false>(a, row, n, keys, scratch, rs);
 }
 
-// Exclusive count, over the CTA's threads in order, of flag (all threads
-// call; wsum: kScoreWarps + 1 ints of shared memory).
-__device__ __forceinline__ int block_exclusive_count(bool flag, int *wsum) {
+// Exclusive sum, over the CTA's threads in order, of v; every thread calls
+// (wsum: kScoreWarps + 1 ints of shared memory).
+__device__ __forceinline__ int block_exclusive_sum(int v, int *wsum) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const unsigned m = __ballot_sync(kFullMask, flag);
-    if (lane == 0) wsum[warp] = __popc(m);
+    const int incl = warp_inclusive_scan(v, lane);
+    if (lane == 31) wsum[warp] = incl;
     __syncthreads();
-    int before = __popc(m & ((1u << lane) - 1u));
+    int before = incl - v;
     for (int w = 0; w < warp; ++w) before += wsum[w];
     __syncthreads();  // wsum free for the next call
     return before;
 }
 
 // The list of a problem of n <= kSmallRank candidates, by its last CTA once
-// every key of row kp is in: thread t holds key t.  The keff-th largest key T is
-// built bit by bit from block-wide counts (count(key >= T | bit) >= keff
-// keeps the bit); keys above T are in, and of the keys equal to T the
-// lowest indices fill the rest.  All threads call.
+// every key of row kp is in: thread t holds key t.  With v = key - kmin over
+// the keys' range, the keff-th largest v, T, comes from 8-bit radix digits,
+// top down: each pass counts the digit of every key that matches the digits
+// found so far into a 256-bin histogram in shared memory (keys visited 37
+// apart, so that neighbouring blocks' close keys do not pile onto one bin in
+// one instruction), and warp 0 finds the digit by a warp scan.  Keys above T
+// are in, and of the keys equal to T the lowest indices fill the rest; one
+// scan of packed counts places them.  Two CTA barriers a pass (the histograms
+// alternate between two buffers, the idle one cleared by warp 1), where
+// building T bit by bit took 32 block-wide counts.  scratch: 4.3 KiB of
+// shared memory.  All threads call.
 __device__ __forceinline__ void select_small(const SelArgs &a, size_t row, int n,
-                                             const uint32_t *kp, int *wsum) {
-    const int tid = threadIdx.x;
+                                             const uint32_t *kp, uint8_t *scratch,
+                                             RadixShared &rs) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int *hist = reinterpret_cast<int *>(scratch);                       // [2][256]
+    uint32_t *ks = reinterpret_cast<uint32_t *>(scratch + 2048);        // [kSmallRank]
+    uint32_t *wmm = ks + kSmallRank;                                    // [2][kScoreWarps + 1]
+    constexpr int kWarps = kScoreWarps + 1;
     const bool have = tid < n;
     const uint32_t key = have ? __ldcg(kp + tid) : 0u;
-    uint32_t T = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t c = T | (1u << bit);
-        if (__syncthreads_count(have && key >= c) >= a.keff) T = c;
+    if (have) ks[tid] = key;
+    for (int i = tid; i < 512; i += kScoreThreads) hist[i] = 0;
+    const uint32_t lo = __reduce_min_sync(kFullMask, have ? key : 0xffffffffu);
+    const uint32_t hi = __reduce_max_sync(kFullMask, have ? key : 0u);
+    if (lane == 0) {
+        wmm[warp] = lo;
+        wmm[kWarps + warp] = hi;
     }
-    const int n_gt = __syncthreads_count(have && key > T);
-    const bool eq = have && key == T;
-    const int eq_before = block_exclusive_count(eq, wsum);
-    const bool in = have && (key > T || (eq && eq_before < a.keff - n_gt));
-    const int pos = block_exclusive_count(in, wsum);
+    __syncthreads();
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int w = 0; w < kWarps; ++w) {
+        kmin = min(kmin, wmm[w]);
+        kmax = max(kmax, wmm[kWarps + w]);
+    }
+    const uint32_t range = kmax - kmin;
+    int hb = range ? 32 - __clz(static_cast<int>(range)) : 0;  // v < 2^hb
+    // the key this thread counts (37 is odd: a permutation of 0 .. 511)
+    const int jc = (tid * 37) & 511;
+    const bool counts = tid < 512 && jc < n;
+    const uint32_t vc = counts ? ks[jc] - kmin : 0u;
+    int krem = a.keff;  // keys still to take among those matching prefix
+    uint32_t prefix = 0u;
+    for (int pass = 0; hb > 0; ++pass) {
+        const int db = hb < 8 ? hb : 8, lo_b = hb - db;
+        int *h = hist + 256 * (pass & 1);
+        if (counts && (hb >= 32 || (vc >> hb) == prefix))
+            atomicAdd(&h[(vc >> lo_b) & ((1u << db) - 1u)], 1);
+        __syncthreads();  // (A) the pass's histogram is complete
+        if (warp == 0) {
+            // lane l takes bins 255 - 8l down to 248 - 8l: a scan counts from the top
+            int c8[8], sum = 0;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                c8[jj] = h[255 - 8 * lane - jj];
+                sum += c8[jj];
+            }
+            const int incl = warp_inclusive_scan(sum, lane);
+            const int above = incl - sum;
+            if (above < krem && krem <= incl) {
+                int acc = above;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    if (krem > acc && krem <= acc + c8[jj]) {
+                        rs.digit = 255 - 8 * lane - jj;
+                        rs.above = acc;
+                    }
+                    acc += c8[jj];
+                }
+            }
+        } else if (warp == 1) {
+            // the other buffer (read by warp 0 in the previous pass) for the next
+            int *hn = hist + 256 * ((pass + 1) & 1);
+            for (int i = lane; i < 256; i += 32) hn[i] = 0;
+        }
+        __syncthreads();  // (B) the digit is known; the next buffer is clear
+        prefix = (prefix << db) | static_cast<uint32_t>(rs.digit);
+        krem -= rs.above;
+        hb = lo_b;
+    }
+    // prefix = T - kmin; krem of the keys equal to T are taken, lowest index first.
+    // One scan of (keys above T) | (keys equal to T) << 16 places every key:
+    // position = above-T keys before it + min(equal keys before it, krem).
+    const uint32_t v = key - kmin;
+    const bool gt = have && v > prefix, eq = have && v == prefix;
+    const int packed = (gt ? 1 : 0) | (eq ? 1 << 16 : 0);
+    const int before = block_exclusive_sum(packed, rs.wsum);
+    const int g_before = before & 0xffff, e_before = before >> 16;
     int32_t *dst = a.sel_idx + row * a.nbmax;
-    if (in) dst[a.se + pos] = a.se + tid;
+    if (gt || (eq && e_before < krem)) dst[a.se + g_before + min(e_before, krem)] = a.se + tid;
     for (int j = tid; j < a.se; j += kScoreThreads) dst[j] = j;
     for (int j = a.rb + tid; j < a.NB; j += kScoreThreads) dst[a.se + a.keff + (j - a.rb)] = j;
     if (tid == 0) a.sel_cnt[row] = a.se + a.keff + (a.NB - a.rb);
@@ -898,7 +967,7 @@ __device__ void select_body(const SelArgs &a_in, int x_tile, int n_tiles, int p,
         if (n <= kSmallRank) {
             __syncthreads();  // (X == 1) this CTA's key stores, seen by all its threads
             if (X > 1 && tid == 0) a.ticket[p] = 0u;  // ready for the next call
-            select_small(a, row, n, kp, rs.wsum);
+            select_small(a, row, n, kp, ring, rs);
         } else {
             select_rank(a, p, row, n, X, kp, in_smem, ring, rs);
         }
