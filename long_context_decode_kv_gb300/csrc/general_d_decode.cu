@@ -513,7 +513,10 @@ cudaError_t launch_decode_gd(const kvd_cache &c, const float *q, int n_heads, fl
     const int P = c.batch * c.n_kv_heads, G = n_heads / c.n_kv_heads, D = c.head_dim;
     const float scale_log2 = scale * kLog2e;
     int splits = 1;
-    cudaError_t e = c.dtype == KVD_F16
+    cudaError_t e = gd_fast_supported(c, G)
+                        ? launch_decode_gd_fast(c, q, n_heads, scale_log2, sel_idx, sel_cnt,
+                                                max_blocks, partials, &splits, st)
+                    : c.dtype == KVD_F16
                         ? decode_dt<KVD_F16>(c, q, n_heads, scale_log2, sel_idx, sel_cnt,
                                              max_blocks, partials, &splits, st)
                         : decode_dt<KVD_INT8>(c, q, n_heads, scale_log2, sel_idx, sel_cnt,

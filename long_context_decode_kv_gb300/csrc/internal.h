@@ -129,6 +129,14 @@ cudaError_t launch_select_gd(const kvd_cache &c, const float *q, int n_heads, in
                              cudaStream_t st);
 int gd_splits(int problems, int max_blocks, int sm_count, int per_sm);
 size_t gd_partials_bytes(int problems, int G, int D, int splits);
+// Head dims 64 and 256 with G in {1, 2, 4, 8, 16}: the warp-specialised
+// kernel (general_d_fast.cu); it writes the split partials gd_merge_kernel
+// reads and sets *splits.
+bool gd_fast_supported(const kvd_cache &c, int G);
+cudaError_t launch_decode_gd_fast(const kvd_cache &c, const float *q, int n_heads,
+                                  float scale_log2, const int32_t *sel_idx,
+                                  const int32_t *sel_cnt, int max_blocks, float *partials,
+                                  int *splits, cudaStream_t st);
 cudaError_t launch_decode_gd(const kvd_cache &c, const float *q, int n_heads, float scale,
                              const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
                              float *out, float *partials, cudaStream_t st);
