@@ -285,7 +285,8 @@ kvd_status decode_impl(const kvd_cache *c, const float *q, int n_heads, float sc
     if (general_d(c)) {
         if (sv_eps > 0.0f) return KVD_ERR_UNSUPPORTED;
         return cuda_status(launch_decode_gd(*c, q, n_heads, scale, sel_idx, sel_cnt, max_blocks,
-                                            out, ws_at<float>(ws, w.partials), st));
+                                            out, ws_at<float>(ws, w.partials),
+                                            ws_at<uint32_t>(ws, w.counters), st));
     }
     // the wide tile for listed blocks only: over every block (a long stream) the
     // two-CTA tile keeps two producers per SM and streams faster

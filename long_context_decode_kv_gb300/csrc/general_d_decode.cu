@@ -509,14 +509,14 @@ size_t gd_partials_bytes(int problems, int G, int D, int splits) {
 
 cudaError_t launch_decode_gd(const kvd_cache &c, const float *q, int n_heads, float scale,
                              const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
-                             float *out, float *partials, cudaStream_t st) {
+                             float *out, float *partials, uint32_t *counters, cudaStream_t st) {
     const int P = c.batch * c.n_kv_heads, G = n_heads / c.n_kv_heads, D = c.head_dim;
     const float scale_log2 = scale * kLog2e;
+    if (gd_fast_supported(c, G))  // its splits merge inside the launch
+        return launch_decode_gd_fast(c, q, n_heads, scale_log2, sel_idx, sel_cnt, max_blocks,
+                                     out, partials, counters, st);
     int splits = 1;
-    cudaError_t e = gd_fast_supported(c, G)
-                        ? launch_decode_gd_fast(c, q, n_heads, scale_log2, sel_idx, sel_cnt,
-                                                max_blocks, partials, &splits, st)
-                    : c.dtype == KVD_F16
+    cudaError_t e = c.dtype == KVD_F16
                         ? decode_dt<KVD_F16>(c, q, n_heads, scale_log2, sel_idx, sel_cnt,
                                              max_blocks, partials, &splits, st)
                         : decode_dt<KVD_INT8>(c, q, n_heads, scale_log2, sel_idx, sel_cnt,

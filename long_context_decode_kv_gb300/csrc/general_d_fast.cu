@@ -25,8 +25,9 @@
 //      pairs (int8: p times the token's V scale);
 //   3. P.V: a lane owns 4 (D = 64) or 8 (D = 256) channels of every head and
 //      every other token (D = 64) or every token (D = 256).
-// At the end the warps' states merge in shared memory in warp order, and the
-// CTA's (m, l, acc) go to the split partials that gd_merge_kernel combines.
+// At the end the warps' states merge in shared memory in warp order, the
+// CTA's (m, l, acc) go to the split partials, and the last CTA of the problem
+// to arrive merges the splits in split order and writes the output.
 #include "common.cuh"
 #include "internal.h"
 
@@ -76,7 +77,7 @@ template <int DT, int D, int GC>
 __global__ void __launch_bounds__(kFastThreads, 1)
     gd_fast_kernel(kvd_cache c, const float *q, int H, int G, float scale_log2,
                    const int32_t *sel_idx, const int32_t *sel_cnt, int splits, int subgroups,
-                   float *part_acc, float *part_ml) {
+                   float *part_acc, float *part_ml, float *out, uint32_t *counters) {
     using TL = FastTile<DT, D>;
     using SL = FastLayout<DT, D, GC>;
     constexpr int S = TL::kStages, T = TL::kT;
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kFastThreads, 1)
         }
         return;
     }
-    // the CTA's state per head, the warps taken in order
+    // the CTA's state per head, the warps taken in order (one split: the output)
     const size_t slot = static_cast<size_t>(p) * splits + split;
     for (int i = tid; i < GC * D; i += kFastWarps * 32) {
         const int g = i / D, d = i % D;
@@ -467,18 +468,67 @@ __global__ void __launch_bounds__(kFastThreads, 1)
             L = fmaf(wgt, r[D + 1], L);
         }
         const int gg = sub * GC + g;  // the head within the KV head's group
+        if (splits == 1) {
+            out[(static_cast<size_t>(b) * H + kvh * G + gg) * D + d] = L > 0.0f ? A * (1.0f / L) : 0.0f;
+            continue;
+        }
         part_acc[(slot * G + gg) * D + d] = A;
         if (d == 0) {
             part_ml[(slot * G + gg) * 2] = M;
             part_ml[(slot * G + gg) * 2 + 1] = L;
         }
     }
+    if (splits == 1) return;
+    // ---- the last CTA of this problem to arrive merges every split, in
+    // split order: weights 2^(m_s - M), divided by the merged mass
+    int *last_s = reinterpret_cast<int *>(smem + SL::kFlagOff + 8);
+    asm volatile("bar.sync 1, %0;" ::"n"(kFastWarps * 32) : "memory");  // every partial store first
+    if (tid == 0)
+        *last_s = atomic_add_acq_rel_gpu(&counters[prob], 1u) == static_cast<unsigned>(splits - 1);
+    asm volatile("bar.sync 1, %0;" ::"n"(kFastWarps * 32) : "memory");
+    if (!*last_s) return;
+    // (m, l) of every split and head into shared memory (the ring is free),
+    // then thread (head, 4 channels) sums the splits' accumulators
+    const float ninf = -__int_as_float(0x7f800000);
+    const size_t s0 = static_cast<size_t>(p) * splits;
+    float2 *ml = reinterpret_cast<float2 *>(smem);  // [GC][splits]
+    for (int i = tid; i < GC * splits; i += kFastWarps * 32) {
+        const int g = i / splits, sp = i % splits;
+        const float *r = part_ml + ((s0 + sp) * G + sub * GC + g) * 2;
+        ml[i] = make_float2(__ldcg(r), __ldcg(r + 1));
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kFastWarps * 32) : "memory");
+    static_assert(GC * D / 4 <= kFastWarps * 32, "one thread per 4 channels of a head");
+    if (tid < GC * D / 4) {
+        const int g = tid / (D / 4), d4 = tid % (D / 4), gg = sub * GC + g;
+        float M = ninf;
+        for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, ml[g * splits + sp].x);
+        float L = 0.0f;
+        float4 A = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+        for (int sp = 0; sp < splits; ++sp) {
+            const float2 r = ml[g * splits + sp];
+            const float w = r.x == ninf ? 0.0f : exp2f(r.x - M);
+            L = fmaf(w, r.y, L);
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(
+                part_acc + ((s0 + sp) * G + gg) * D + 4 * d4));
+            A.x = fmaf(w, a.x, A.x);
+            A.y = fmaf(w, a.y, A.y);
+            A.z = fmaf(w, a.z, A.z);
+            A.w = fmaf(w, a.w, A.w);
+        }
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        *reinterpret_cast<float4 *>(out + (static_cast<size_t>(b) * H + kvh * G + gg) * D +
+                                    4 * d4) = make_float4(A.x * inv, A.y * inv, A.z * inv,
+                                                          A.w * inv);
+    }
+    if (tid == 0) counters[prob] = 0u;  // ready for the next call
 }
 
 template <int DT, int D, int GC>
 cudaError_t fast_t(const kvd_cache &c, const float *q, int H, int G, float scale_log2,
                    const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
-                   float *partials, int *splits_out, cudaStream_t st) {
+                   float *out, float *partials, uint32_t *counters, cudaStream_t st) {
     using SL = FastLayout<DT, D, GC>;
     static_assert(SL::kTotal <= 227 * 1024, "shared memory");
     auto kern = gd_fast_kernel<DT, D, GC>;
@@ -495,23 +545,23 @@ cudaError_t fast_t(const kvd_cache &c, const float *q, int H, int G, float scale
     float *part_acc = partials;
     float *part_ml = partials + static_cast<size_t>(P) * splits * G * D;
     kern<<<dim3(splits, P_sub), kFastThreads, SL::kTotal, st>>>(
-        c, q, H, G, scale_log2, sel_idx, sel_cnt, splits, subgroups, part_acc, part_ml);
-    *splits_out = splits;
+        c, q, H, G, scale_log2, sel_idx, sel_cnt, splits, subgroups, part_acc, part_ml, out,
+        counters);
     return cudaGetLastError();
 }
 
 template <int DT, int D>
 cudaError_t fast_d(const kvd_cache &c, const float *q, int H, int G, float scale_log2,
-                   const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
-                   float *partials, int *splits, cudaStream_t st) {
+                   const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks, float *out,
+                   float *partials, uint32_t *counters, cudaStream_t st) {
     if (G == 1)
-        return fast_t<DT, D, 1>(c, q, H, G, scale_log2, sel_idx, sel_cnt, max_blocks, partials,
-                                splits, st);
+        return fast_t<DT, D, 1>(c, q, H, G, scale_log2, sel_idx, sel_cnt, max_blocks, out,
+                                partials, counters, st);
     if (G == 2)
-        return fast_t<DT, D, 2>(c, q, H, G, scale_log2, sel_idx, sel_cnt, max_blocks, partials,
-                                splits, st);
-    return fast_t<DT, D, 4>(c, q, H, G, scale_log2, sel_idx, sel_cnt, max_blocks, partials,
-                            splits, st);
+        return fast_t<DT, D, 2>(c, q, H, G, scale_log2, sel_idx, sel_cnt, max_blocks, out,
+                                partials, counters, st);
+    return fast_t<DT, D, 4>(c, q, H, G, scale_log2, sel_idx, sel_cnt, max_blocks, out,
+                            partials, counters, st);
 }
 
 }  // namespace
@@ -521,22 +571,26 @@ bool gd_fast_supported(const kvd_cache &c, int G) {
            (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
 }
 
-// The split partials of the fast kernel (the layout gd_merge_kernel reads);
-// *splits gets the split count.  Only for gd_fast_supported shapes.
+// The decode with the splits merged by the last CTA of each problem (the
+// output written directly); only for gd_fast_supported shapes.  counters:
+// one per (sequence, KV head, subgroup), zero between calls.
 cudaError_t launch_decode_gd_fast(const kvd_cache &c, const float *q, int n_heads,
                                   float scale_log2, const int32_t *sel_idx,
-                                  const int32_t *sel_cnt, int max_blocks, float *partials,
-                                  int *splits, cudaStream_t st) {
+                                  const int32_t *sel_cnt, int max_blocks, float *out,
+                                  float *partials, uint32_t *counters, cudaStream_t st) {
     const int G = n_heads / c.n_kv_heads;
     if (c.dtype == KVD_F16)
-        return c.head_dim == 64 ? fast_d<KVD_F16, 64>(c, q, n_heads, G, scale_log2, sel_idx,
-                                                       sel_cnt, max_blocks, partials, splits, st)
-                                : fast_d<KVD_F16, 256>(c, q, n_heads, G, scale_log2, sel_idx,
-                                                        sel_cnt, max_blocks, partials, splits, st);
+        return c.head_dim == 64
+                   ? fast_d<KVD_F16, 64>(c, q, n_heads, G, scale_log2, sel_idx, sel_cnt,
+                                         max_blocks, out, partials, counters, st)
+                   : fast_d<KVD_F16, 256>(c, q, n_heads, G, scale_log2, sel_idx, sel_cnt,
+                                          max_blocks, out, partials, counters, st);
     return c.head_dim == 64 ? fast_d<KVD_INT8, 64>(c, q, n_heads, G, scale_log2, sel_idx,
-                                                    sel_cnt, max_blocks, partials, splits, st)
+                                                    sel_cnt, max_blocks, out, partials,
+                                                    counters, st)
                             : fast_d<KVD_INT8, 256>(c, q, n_heads, G, scale_log2, sel_idx,
-                                                     sel_cnt, max_blocks, partials, splits, st);
+                                                     sel_cnt, max_blocks, out, partials,
+                                                     counters, st);
 }
 
 }  // namespace kvd

@@ -130,16 +130,16 @@ cudaError_t launch_select_gd(const kvd_cache &c, const float *q, int n_heads, in
 int gd_splits(int problems, int max_blocks, int sm_count, int per_sm);
 size_t gd_partials_bytes(int problems, int G, int D, int splits);
 // Head dims 64 and 256 with G in {1, 2, 4, 8, 16}: the warp-specialised
-// kernel (general_d_fast.cu); it writes the split partials gd_merge_kernel
-// reads and sets *splits.
+// kernel (general_d_fast.cu), its splits merged by the last CTA of each
+// problem into out (counters: B * H words, zero between calls).
 bool gd_fast_supported(const kvd_cache &c, int G);
 cudaError_t launch_decode_gd_fast(const kvd_cache &c, const float *q, int n_heads,
                                   float scale_log2, const int32_t *sel_idx,
-                                  const int32_t *sel_cnt, int max_blocks, float *partials,
-                                  int *splits, cudaStream_t st);
+                                  const int32_t *sel_cnt, int max_blocks, float *out,
+                                  float *partials, uint32_t *counters, cudaStream_t st);
 cudaError_t launch_decode_gd(const kvd_cache &c, const float *q, int n_heads, float scale,
                              const int32_t *sel_idx, const int32_t *sel_cnt, int max_blocks,
-                             float *out, float *partials, cudaStream_t st);
+                             float *out, float *partials, uint32_t *counters, cudaStream_t st);
 // A kernel whose one mbarrier wait runs out after limit_ns (selftest.cu).
 cudaError_t launch_wait_probe(int32_t *status, uint64_t limit_ns, cudaStream_t st);
 
