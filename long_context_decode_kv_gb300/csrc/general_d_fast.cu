@@ -1,5 +1,5 @@
-// general_d_fast.cu -- split-KV decode attention for head dims 64 and 256
-// (f16 and int8 caches), the warp-specialised counterpart of the tuned
+// general_d_fast.cu -- split-KV decode attention for head dims 64, 256 and
+// 512 (f16 and int8 caches), the warp-specialised counterpart of the tuned
 // head-dim-128 kernel.
 //
 // "Sparse Attention -- Quest-style block-selector for long-context decode
@@ -12,9 +12,10 @@
 //
 // CTA of split s of (sequence, KV head, subgroup of GC <= 4 query heads): one
 // producer warp copies tiles (T tokens of a listed block: its K rows, V rows
-// and on the int8 cache the two scale runs; at most 16 KiB) with 1-D bulk
-// copies into a ring of shared-memory stages, each completing on its own
-// mbarrier.  Each of the 8 consumer warps takes every 8th tile whole and
+// and on the int8 cache the two scale runs; about 8 KiB) with 1-D bulk
+// copies into a ring of shared-memory stages (16 or 24: a multiple of the
+// consumer warps, so that each stage serves one warp), each completing on its
+// own mbarrier.  Each of the 8 consumer warps takes every 8th tile whole and
 // keeps its own online softmax over the tiles it saw -- no CTA barrier inside
 // the tile loop:
 //   1. q.k: a token's row is read by D/16 lanes (16 channels each, the query
@@ -23,8 +24,8 @@
 //   2. softmax: the tile's max and mass per head over the lanes that hold
 //      that head; the weights go to the warp's shared-memory rows as (p, p)
 //      pairs (int8: p times the token's V scale);
-//   3. P.V: a lane owns 4 (D = 64) or 8 (D = 256) channels of every head and
-//      every other token (D = 64) or every token (D = 256).
+//   3. P.V: a lane owns 4 (D = 64) or D/32 (D >= 256) channels of every head
+//      and every other token (D = 64) or every token (D >= 256).
 // At the end the warps' states merge in shared memory in warp order, the
 // CTA's (m, l, acc) go to the split partials, and the last CTA of the problem
 // to arrive merges the splits in split order and writes the output.
@@ -34,7 +35,7 @@
 namespace kvd {
 namespace {
 
-constexpr int kFastWarps = 8;  // consumer warps; warp 8 produces
+constexpr int kFastWarps = 12;  // consumer warps; warp 12 produces
 constexpr int kFastThreads = 32 * (kFastWarps + 1);
 constexpr unsigned kAll = 0xffffffffu;
 
@@ -43,10 +44,19 @@ struct FastTile {
     static constexpr int kElt = DT == KVD_F16 ? 2 : 1;
     static constexpr int kRow = D * kElt;  // bytes of a token's row
     // tokens per tile: K + V of a tile within 16 KiB
-    static constexpr int kT = 2 * 64 * kRow <= 16384 ? 64 : 2 * 32 * kRow <= 16384 ? 32 : 16;
+    static constexpr int kT = 2 * 64 * kRow <= 16384   ? 64
+                              : 2 * 32 * kRow <= 16384 ? 32
+                              : 2 * 16 * kRow <= 16384 ? 16
+                                                       : 8;
     static constexpr int kScaleBytes = DT == KVD_F16 ? 0 : 2 * kT * 4;
     static constexpr int kStageBytes = 2 * kT * kRow + kScaleBytes;
-    static constexpr int kStages = 196608 / kStageBytes < 16 ? 196608 / kStageBytes : 16;
+    // a multiple of the consumer warps: tile u goes to warp u % 8 and stage
+    // u % kStages, so every tile of a stage goes to one warp, which waits on
+    // the stage's phases in order (warps sharing a stage could see a later
+    // phase's parity as an earlier one's and read it before it lands)
+    static constexpr int kStages =
+        (204800 / kStageBytes < 24 ? 204800 / kStageBytes : 24) / kFastWarps * kFastWarps;
+    static_assert(kStages >= kFastWarps, "a stage per consumer warp at least");
     static constexpr int kLPT = D / 16;      // q.k: lanes per token (16 channels each)
     static constexpr int kTPP = 32 / kLPT;   // tokens per q.k pass
     static constexpr int kPasses = kT / kTPP;
@@ -374,35 +384,31 @@ __global__ void __launch_bounds__(kFastThreads, 1)
             for (int t = vs; t < nt; t += TL::kTPV) {
                 float2 vv[TL::kCPL / 2];
                 if constexpr (DT == KVD_F16) {
-                    if constexpr (TL::kCPL == 8) {
-                        const uint4 w = *reinterpret_cast<const uint4 *>(vrow + t * TL::kRow);
-                        const __half2 *h2 = reinterpret_cast<const __half2 *>(&w);
+                    if constexpr (TL::kCPL >= 8) {  // 16-byte pieces of 8 channels
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) vv[i] = __half22float2(h2[i]);
+                        for (int j = 0; j < TL::kCPL / 8; ++j) {
+                            const uint4 w =
+                                reinterpret_cast<const uint4 *>(vrow + t * TL::kRow)[j];
+                            const __half2 *h2 = reinterpret_cast<const __half2 *>(&w);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) vv[4 * j + i] = __half22float2(h2[i]);
+                        }
                     } else {
                         const uint2 w = *reinterpret_cast<const uint2 *>(vrow + t * TL::kRow);
                         vv[0] = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
                         vv[1] = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
                     }
-                } else {
-                    if constexpr (TL::kCPL == 8) {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(vrow + t * TL::kRow);
-                        const uint32_t ww[2] = {w.x, w.y};
+                } else {  // 4-byte words of 4 codes
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {
-                            vv[2 * i] = make_float2(
-                                static_cast<float>(static_cast<int8_t>(ww[i] & 0xffu)),
-                                static_cast<float>(static_cast<int8_t>((ww[i] >> 8) & 0xffu)));
-                            vv[2 * i + 1] = make_float2(
-                                static_cast<float>(static_cast<int8_t>((ww[i] >> 16) & 0xffu)),
-                                static_cast<float>(static_cast<int8_t>(ww[i] >> 24)));
-                        }
-                    } else {
-                        const uint32_t w = *reinterpret_cast<const uint32_t *>(vrow + t * TL::kRow);
-                        vv[0] = make_float2(static_cast<float>(static_cast<int8_t>(w & 0xffu)),
-                                            static_cast<float>(static_cast<int8_t>((w >> 8) & 0xffu)));
-                        vv[1] = make_float2(static_cast<float>(static_cast<int8_t>((w >> 16) & 0xffu)),
-                                            static_cast<float>(static_cast<int8_t>(w >> 24)));
+                    for (int j = 0; j < TL::kCPL / 4; ++j) {
+                        const uint32_t w =
+                            reinterpret_cast<const uint32_t *>(vrow + t * TL::kRow)[j];
+                        vv[2 * j] = make_float2(
+                            static_cast<float>(static_cast<int8_t>(w & 0xffu)),
+                            static_cast<float>(static_cast<int8_t>((w >> 8) & 0xffu)));
+                        vv[2 * j + 1] = make_float2(
+                            static_cast<float>(static_cast<int8_t>((w >> 16) & 0xffu)),
+                            static_cast<float>(static_cast<int8_t>(w >> 24)));
                     }
                 }
 #pragma unroll
@@ -488,7 +494,7 @@ __global__ void __launch_bounds__(kFastThreads, 1)
     asm volatile("bar.sync 1, %0;" ::"n"(kFastWarps * 32) : "memory");
     if (!*last_s) return;
     // (m, l) of every split and head into shared memory (the ring is free),
-    // then thread (head, 4 channels) sums the splits' accumulators
+    // then a thread per (head, 4 channels) sums the splits' accumulators
     const float ninf = -__int_as_float(0x7f800000);
     const size_t s0 = static_cast<size_t>(p) * splits;
     float2 *ml = reinterpret_cast<float2 *>(smem);  // [GC][splits]
@@ -498,9 +504,8 @@ __global__ void __launch_bounds__(kFastThreads, 1)
         ml[i] = make_float2(__ldcg(r), __ldcg(r + 1));
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kFastWarps * 32) : "memory");
-    static_assert(GC * D / 4 <= kFastWarps * 32, "one thread per 4 channels of a head");
-    if (tid < GC * D / 4) {
-        const int g = tid / (D / 4), d4 = tid % (D / 4), gg = sub * GC + g;
+    for (int i = tid; i < GC * D / 4; i += kFastWarps * 32) {
+        const int g = i / (D / 4), d4 = i % (D / 4), gg = sub * GC + g;
         float M = ninf;
         for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, ml[g * splits + sp].x);
         float L = 0.0f;
@@ -567,7 +572,7 @@ cudaError_t fast_d(const kvd_cache &c, const float *q, int H, int G, float scale
 }  // namespace
 
 bool gd_fast_supported(const kvd_cache &c, int G) {
-    return (c.head_dim == 64 || c.head_dim == 256) &&
+    return (c.head_dim == 64 || c.head_dim == 256 || c.head_dim == 512) &&
            (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
 }
 
@@ -579,6 +584,13 @@ cudaError_t launch_decode_gd_fast(const kvd_cache &c, const float *q, int n_head
                                   const int32_t *sel_cnt, int max_blocks, float *out,
                                   float *partials, uint32_t *counters, cudaStream_t st) {
     const int G = n_heads / c.n_kv_heads;
+    if (c.head_dim == 512)
+        return c.dtype == KVD_F16 ? fast_d<KVD_F16, 512>(c, q, n_heads, G, scale_log2, sel_idx,
+                                                          sel_cnt, max_blocks, out, partials,
+                                                          counters, st)
+                                  : fast_d<KVD_INT8, 512>(c, q, n_heads, G, scale_log2, sel_idx,
+                                                           sel_cnt, max_blocks, out, partials,
+                                                           counters, st);
     if (c.dtype == KVD_F16)
         return c.head_dim == 64
                    ? fast_d<KVD_F16, 64>(c, q, n_heads, G, scale_log2, sel_idx, sel_cnt,

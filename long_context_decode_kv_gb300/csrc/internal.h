@@ -129,7 +129,7 @@ cudaError_t launch_select_gd(const kvd_cache &c, const float *q, int n_heads, in
                              cudaStream_t st);
 int gd_splits(int problems, int max_blocks, int sm_count, int per_sm);
 size_t gd_partials_bytes(int problems, int G, int D, int splits);
-// Head dims 64 and 256 with G in {1, 2, 4, 8, 16}: the warp-specialised
+// Head dims 64, 256 and 512 with G in {1, 2, 4, 8, 16}: the warp-specialised
 // kernel (general_d_fast.cu), its splits merged by the last CTA of each
 // problem into out (counters: B * H words, zero between calls).
 bool gd_fast_supported(const kvd_cache &c, int G);

@@ -3,8 +3,8 @@
 "cpu-attn", Requirements and limits: a head dim that is a multiple of 16, at
 most 1024.  The general kernels serve every such D but 128; the cases span
 the smallest (16), dims that are not powers of two (80, 96, 144), and the
-largest (1024), with group sizes 1 to 16; D = 64 and 256 (the warp-specialised
-decode kernel) with every group size it takes.
+largest (1024), with group sizes 1 to 16; D = 64, 256 and 512 (the
+warp-specialised decode kernel) with every group size it takes.
 
   * append: rows, scales and bounds bit-exact, across chunked appends that
     straddle blocks, from f16 and from f32 input;
@@ -25,8 +25,9 @@ from gpu_util import assert_outputs, check_selection, dev, make_pair, scale_for,
 pytestmark = pytest.mark.gpu
 DTYPES = [kvd.F16, kvd.INT8]
 CASES = [(16, 4), (64, 8), (80, 2), (96, 1), (144, 4), (256, 4), (1024, 16),
-         # D = 64 and 256 run the warp-specialised kernel: every head-group shape
-         (64, 1), (64, 2), (64, 16), (256, 1), (256, 2), (256, 8), (256, 16)]
+         # D = 64, 256 and 512 run the warp-specialised kernel: every head-group shape
+         (64, 1), (64, 2), (64, 16), (256, 1), (256, 2), (256, 8), (256, 16), (512, 4),
+         (512, 16)]
 
 
 def _oracle_head(dtype, oc, qh, b, g, L, D, sel):
