@@ -250,3 +250,32 @@ def test_host_step_equals_device_step(dtype, D, pinned):
         assert torch.equal(out_d.cpu(), out_h)
     assert a.len == b.len == L0 + 3
     assert a.device_status() == b.device_status() == 0
+
+
+@pytest.mark.parametrize("D", [256, 512])
+def test_repeated_steps_with_tiles_past_the_end(D):
+    # The fast kernel cuts a block into several tiles at these dims; the last
+    # block of a sequence ending one token into it leaves tiles past the end,
+    # whose stages complete at once.  Many steps over the same cache (the
+    # length reset each time, as the bench does) must never run into the
+    # kernel's bounded wait, and repeat bit for bit.
+    B, Hkv, G, L0 = 1, 8, 4, 64 * 200
+    k = seeded((B, L0, Hkv, D), 31 + D)
+    v = seeded((B, L0, Hkv, D), 32 + D)
+    gc = kvd.KVCache(kvd.F16, B, Hkv, L0 + 64, head_dim=D, device=dev())
+    kvd.kv_append(gc, k, v)
+    ws = kvd.make_workspace(gc, Hkv * G)
+    q = seeded((B, Hkv * G, D), 33 + D, scale=2.0, dtype=torch.float32)
+    kn = seeded((B, 1, Hkv, D), 34 + D)
+    vn = seeded((B, 1, Hkv, D), 35 + D)
+    out = torch.empty((B, Hkv * G, D), device=dev())
+    first = None
+    for step in range(300):
+        gc.len = L0
+        kvd.decode_step(gc, q, kn, vn, scale_for(D), 40, 4, 64, out, ws)
+        if step == 0:
+            torch.cuda.synchronize()
+            first = out.clone()
+    torch.cuda.synchronize()
+    assert gc.device_status() == 0
+    assert torch.equal(out, first)
