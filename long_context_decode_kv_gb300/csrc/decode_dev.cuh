@@ -36,6 +36,10 @@ namespace {
 
 constexpr int kWarpsPerGroup = 4;
 constexpr int kTokensPerWarp = kBlock / kWarpsPerGroup;    // 16
+// q4_0 PV weights: floats from one token's [4 groups][4 heads] pairs to the
+// next token's; 40 (not 32) puts tokens t and t + 1..3 on distinct banks, so
+// the pair stores of a QK pass take two wavefronts, not eight.
+constexpr int kQ4PwTok = 40;
 // Partial rows: m, l, two pad words, acc[128] (acc 16-byte aligned).
 constexpr int kPartStride = kHeadDim + 4;
 constexpr int kAccOff = 4;
@@ -161,8 +165,10 @@ struct SmemLayout {
     static constexpr int kCoefOff = kQOff + kQBytes;
     static constexpr int kQsumOff = kCoefOff + 16;  // q4_0: [GC][4] group sums of the codes
     static constexpr int kPwOff = kQsumOff + 64;
-    // [warp][16 tokens][4 heads] pairs (p, p)
-    static constexpr int kPwBytes = T::kConsumerWarps * kTokensPerWarp * 4 * 2 * 4;
+    // per warp: [16 tokens][4 heads] pairs (p, p); q4_0: [16 tokens][4 groups]
+    // [4 heads] pairs (w, w / 16), w = p times the group's value scale
+    static constexpr int kPwWarpFloats = kTokensPerWarp * (DT == KVD_Q4_0 ? kQ4PwTok : 4 * 2);
+    static constexpr int kPwBytes = T::kConsumerWarps * kPwWarpFloats * 4;
     static constexpr int kLOff = kPwOff + kPwBytes;  // split merge: L per head
     static constexpr int kFlagOff = kLOff + 16;
     // moment tail: the listed-block mask of each stage
@@ -383,12 +389,14 @@ __device__ __forceinline__ float qk_q4_row(const uint8_t *row, const QRegsQ4<GC>
     return reduce4_scatter<GC>(d, c);
 }
 
-// Two 4-bit codes per byte of w16 (channels 4l .. 4l+3 of the lane) -> the
-// exact floats code - 8, as pairs.
+// Two 4-bit codes per byte of w16 (channels 4l .. 4l+3 of the lane) -> exact
+// floats, as pairs: code - 8 for the low nibbles (channels 4l and 4l+2) and
+// 16 (code - 8) for the high ones (4l+1 and 4l+3), which are masked where
+// they stand instead of shifted down; their PV weights carry the 1/16.
 __device__ __forceinline__ void u4x4_to_f32x2(uint32_t w16, float2 &f01, float2 &f23) {
-    const uint32_t lo = w16 & 0x0f0fu;         // codes of channels 4l and 4l+2
-    const uint32_t hi = (w16 >> 4) & 0x0f0fu;  // codes of channels 4l+1 and 4l+3
-    const float2 bias = make_float2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
+    const uint32_t lo = w16 & 0x0f0fu;  // codes of channels 4l and 4l+2
+    const uint32_t hi = w16 & 0xf0f0u;  // 16 x the codes of channels 4l+1 and 4l+3
+    const float2 bias = make_float2(-8388616.0f, -8388736.0f);  // -(2^23 + 8), -(2^23 + 128)
     f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7650)),
                                  __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7650))),
                      bias);
@@ -690,7 +698,11 @@ __device__ __forceinline__ void consume_q8(const uint8_t *stage, int n_valid, co
 }
 
 // One stage for one consumer warp, q4_0 cache: consume_q8 with the 4-bit
-// rows unpacked in registers.
+// rows unpacked in registers, and the value scale of each (token, group)
+// folded into that group's PV weights: lane (t, c) writes, for its head, the
+// weights of GC of the four groups, and the lanes of group g (8g .. 8g+7)
+// read group g's.  pw: [16 tokens, kQ4PwTok floats apart][4 groups][4 heads]
+// pairs (w, w / 16).
 template <int GC, bool SV>
 __device__ __forceinline__ void consume_q4(const uint8_t *stage, int n_valid, const float *coef,
                                            const QRegsQ4<GC> &qr, float *pw, int wg, int lane,
@@ -731,17 +743,24 @@ __device__ __forceinline__ void consume_q4(const uint8_t *stage, int n_valid, co
         live = any_per_group<8, 4>(b0) | (any_per_group<8, 4>(b1) << 8);
     }
     constexpr int lph = 4 / GC;
-    if ((c % lph) == 0) {
-        const float w0 = tok0 < n_valid && keep[0] ? p0 : 0.0f;
-        const float w1 = tok1 < n_valid && keep[1] ? p1 : 0.0f;
-        *reinterpret_cast<float2 *>(pw + (t * 4 + hq) * 2) = make_float2(w0, w0);
-        *reinterpret_cast<float2 *>(pw + ((t + 8) * 4 + hq) * 2) = make_float2(w1, w1);
+    {
+        const int g0 = (c % lph) * GC;  // this lane's groups g0 .. g0 + GC - 1
+        const bool u0 = tok0 < n_valid && keep[0], u1 = tok1 < n_valid && keep[1];
+#pragma unroll
+        for (int j = 0; j < GC; ++j) {
+            const float a0 = u0 ? p0 * __half2float(vd[tok0 * (kHeadDim / 32) + g0 + j]) : 0.0f;
+            const float a1 = u1 ? p1 * __half2float(vd[tok1 * (kHeadDim / 32) + g0 + j]) : 0.0f;
+            *reinterpret_cast<float2 *>(pw + t * kQ4PwTok + (g0 + j) * 8 + 2 * hq) =
+                make_float2(a0, a0 * 0.0625f);
+            *reinterpret_cast<float2 *>(pw + (t + 8) * kQ4PwTok + (g0 + j) * 8 + 2 * hq) =
+                make_float2(a1, a1 * 0.0625f);
+        }
     }
     rescale<GC>(st, alpha, lph);
     __syncwarp();
     const int nt = min(kTokensPerWarp, n_valid - kTokensPerWarp * wg);
     const uint8_t *vrow = Vs + kTokensPerWarp * wg * TQ::kRowBytes + 2 * lane;
-    const __half *vdl = vd + kTokensPerWarp * wg * (kHeadDim / 32) + (lane >> 3);
+    const float *pwg = pw + (lane >> 3) * 8;  // the lane's group, token 0
     if ((SV && live != 0xffffu) || nt != kTokensPerWarp) {
         uint32_t m = live & ((1u << max(nt, 0)) - 1u);
         for (; m; m &= m - 1u) {
@@ -749,9 +768,7 @@ __device__ __forceinline__ void consume_q4(const uint8_t *stage, int n_valid, co
             float2 f01, f23;
             u4x4_to_f32x2(*reinterpret_cast<const uint16_t *>(vrow + t2 * TQ::kRowBytes), f01,
                           f23);
-            const float dv = __half2float(vdl[t2 * (kHeadDim / 32)]);
-            const float2 d2 = make_float2(dv, dv);
-            pv_token<GC>(st, pw + t2 * 8, __fmul2_rn(f01, d2), __fmul2_rn(f23, d2));
+            pv_token<GC>(st, pwg + t2 * kQ4PwTok, f01, f23);
         }
     } else {
 #pragma unroll
@@ -759,9 +776,7 @@ __device__ __forceinline__ void consume_q4(const uint8_t *stage, int n_valid, co
             float2 f01, f23;
             u4x4_to_f32x2(*reinterpret_cast<const uint16_t *>(vrow + t2 * TQ::kRowBytes), f01,
                           f23);
-            const float dv = __half2float(vdl[t2 * (kHeadDim / 32)]);
-            const float2 d2 = make_float2(dv, dv);
-            pv_token<GC>(st, pw + t2 * 8, __fmul2_rn(f01, d2), __fmul2_rn(f23, d2));
+            pv_token<GC>(st, pwg + t2 * kQ4PwTok, f01, f23);
         }
     }
 }
@@ -1213,7 +1228,7 @@ __device__ void decode_body(const DecodeArgs &a, int split, int prob, uint8_t *s
         if (!a.early_q) load_query<DT, GC>(a, b, h0, warp, lane, q_s, coef, nullptr, nullptr);
         // the query words and coefficients are visible to every consumer warp
         asm volatile("bar.sync 1, %0;" ::"r"(TL::kConsumerWarps * 32) : "memory");
-        float *pw = pw_all + warp * (kTokensPerWarp * 4 * 2);
+        float *pw = pw_all + warp * SL::kPwWarpFloats;
         const int group = warp / kWarpsPerGroup, wg = warp % kWarpsPerGroup;
         int i = group;         // stage sequence number of this group
         bool at_tail = false;  // stage i is the group's first moment-tail stage
