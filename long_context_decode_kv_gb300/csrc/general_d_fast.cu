@@ -12,12 +12,12 @@
 //
 // CTA of split s of (sequence, KV head, subgroup of GC <= 4 query heads): one
 // producer warp copies tiles (T tokens of a listed block: its K rows, V rows
-// and on the int8 cache the two scale runs; about 8 KiB) with 1-D bulk
-// copies into a ring of shared-memory stages (16 or 24: a multiple of the
-// consumer warps, so that each stage serves one warp), each completing on its
-// own mbarrier.  Each of the 8 consumer warps takes every 8th tile whole and
-// keeps its own online softmax over the tiles it saw -- no CTA barrier inside
-// the tile loop:
+// and on the int8 cache the two scale runs; 8-16 KiB) with 1-D bulk copies
+// into a ring of shared-memory stages (12 for the shipped shapes: a multiple
+// of the consumer warps, so that each stage serves one warp), each completing
+// on its own mbarrier.  Each of the 12 consumer warps takes every 12th tile
+// whole and keeps its own online softmax over the tiles it saw -- no CTA
+// barrier inside the tile loop:
 //   1. q.k: a token's row is read by D/16 lanes (16 channels each, the query
 //      chunk in registers), and a reduce-scatter over those lanes leaves
 //      every lane one head's score;
@@ -50,8 +50,8 @@ struct FastTile {
                                                        : 8;
     static constexpr int kScaleBytes = DT == KVD_F16 ? 0 : 2 * kT * 4;
     static constexpr int kStageBytes = 2 * kT * kRow + kScaleBytes;
-    // a multiple of the consumer warps: tile u goes to warp u % 8 and stage
-    // u % kStages, so every tile of a stage goes to one warp, which waits on
+    // a multiple of the consumer warps: tile u goes to warp u % kFastWarps and
+    // stage u % kStages, so every tile of a stage goes to one warp, which waits on
     // the stage's phases in order (warps sharing a stage could see a later
     // phase's parity as an earlier one's and read it before it lands)
     static constexpr int kStages =
