@@ -76,6 +76,32 @@ def test_traffic_scaled_per_token(tmp_path, monkeypatch):
     assert bench.measured_traffic("ctx1m_int8", 25) is None
 
 
+def test_committed_traffic_lines_are_well_formed():
+    # every data line: a known workload, its context, a 16-hex-digit source
+    # digest, and positive byte and token counts; each cited summary exists
+    path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+    seen = set()
+    for line in open(path):
+        if line.startswith("#"):
+            for word in line.split():
+                if word.startswith("profiles/") and word.endswith(".md"):
+                    assert os.path.exists(os.path.join(ROOT, word)), word
+            continue
+        parts = line.split()
+        if not parts:
+            continue
+        assert len(parts) == 5, line
+        name, ctx, digest, nbytes, tokens = parts
+        assert name in synth.WORKLOADS and name not in seen, name
+        seen.add(name)
+        assert int(ctx) > 0 and int(nbytes) > 0 and int(tokens) > 0
+        assert len(digest) == 16 and int(digest, 16) >= 0
+        # DRAM traffic at least the rows the tokens need: no impossible capture
+        w = synth.WORKLOADS[name]
+        assert int(nbytes) >= int(tokens) * bench.kv_bytes_per_token(w.dtype, w.D)
+    assert "ctx1m_int8" in seen
+
+
 def test_oracle_baseline_uses_every_core_it_can():
     # the all-core oracle leg spreads sequence 0's (KV head, query head)
     # attentions over the threads of this process's CPU affinity
