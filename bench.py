@@ -300,15 +300,16 @@ def oracle_leg_all_cores(w, q, k, v, steps):
 
 
 def run_reference(args, w):
-    # the oracle runs on rank 0's host cores only; other ranks exit without work
+    # the oracle, as cpu_baseline runs it (every host core it may use), on rank
+    # 0 only; other ranks exit without work
     if int(os.environ.get("RANK", "0")) != 0:
         return
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     q, k, v, _ = synth.make_workload(w, device="cuda")
     steps = max(1, args.steps)
     for _ in range(max(0, min(args.warmup, 1))):
-        oracle_leg(w, q, k, v, 1)
-    value, base = oracle_leg(w, q, k, v, steps)
+        oracle_leg_all_cores(w, q, k, v, 1)
+    value, base = oracle_leg_all_cores(w, q, k, v, steps)
     base["value"] = value
     base["unit"] = "us/step"
     line = {"impl": "reference", "metric": "us_per_decode_step", "value": value,
